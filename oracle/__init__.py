@@ -1,0 +1,207 @@
+"""The oracle: a plain fp64 CPU reference for decode attention over a paged KV cache.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg may import this package. It shares no
+code with the CUDA path (``kv_cache_decode_split_gb300``) and neither imports
+the other; both read the same seeded inputs from ``workloads``.
+
+The arithmetic lives in ``oracle.c`` (plain C loops in double precision, see
+its header for the passages each function follows). This module only loads
+the compiled library and marshals arrays. Inputs are passed exactly as stored
+(bf16 bit patterns or float32) and widened to double inside the C code.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+and ``tests/test_worked_numbers.py`` (brute force on tiny inputs, closed forms,
+the pages' printed numbers and the invariants the method states).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc (OpenMP over independent rows)."""
+    src = os.path.join(_HERE, "oracle.c")
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(src):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-o", tmp, src, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        i, l, d = ctypes.c_int, ctypes.c_long, ctypes.c_double
+        lib.oracle_kv_cache_bytes.restype = d
+        lib.oracle_kv_cache_bytes.argtypes = [d, d, d, d, d]
+        lib.oracle_mla_cache_bytes.restype = d
+        lib.oracle_mla_cache_bytes.argtypes = [d, d, d, d, d]
+        lib.oracle_attention_flops.restype = d
+        lib.oracle_attention_flops.argtypes = [d, d, d, d]
+        lib.oracle_gqa.restype = None
+        lib.oracle_gqa.argtypes = [P, P, P, i, P, P, i, i, i, i, i, i, d, l, l, P, P, i, P, P]
+        lib.oracle_mla.restype = None
+        lib.oracle_mla.argtypes = [P, P, i, P, P, P, P, i, i, i, i, i, i, i, d, P, i, P, P]
+        lib.oracle_indexer_scores.restype = None
+        lib.oracle_indexer_scores.argtypes = [P, P, P, P, P, i, i, i, i, P, i, l, P]
+        lib.oracle_topk.restype = i
+        lib.oracle_topk.argtypes = [P, l, i, P]
+        _lib = lib
+    return _lib
+
+
+def _arr(x):
+    """Contiguous numpy view of a CPU tensor/array, keeping bf16 as raw uint16 bits.
+
+    Returns (array, dtype_code) with dtype_code 0 = float32, 1 = bf16, -1 = other.
+    """
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.dtype == torch.bfloat16:
+                return np.ascontiguousarray(x.view(torch.int16).numpy().view(np.uint16)), 1
+            x = x.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        return x, 1
+    if x.dtype == np.float32:
+        return x, 0
+    return x, -1
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def kv_cache_bytes(tokens, layers, kv_heads, d_head, bytes_per_elem):
+    """KV cache size in bytes ("Attention Optimizations", KV cache size)."""
+    return _load().oracle_kv_cache_bytes(float(tokens), float(layers), float(kv_heads),
+                                         float(d_head), float(bytes_per_elem))
+
+
+def mla_cache_bytes(tokens, layers, d_latent, d_rope, bytes_per_elem):
+    """MLA latent cache size in bytes: one (latent + RoPE key) row per token per layer."""
+    return _load().oracle_mla_cache_bytes(float(tokens), float(layers), float(d_latent),
+                                          float(d_rope), float(bytes_per_elem))
+
+
+def attention_flops(S, layers, heads, head_dim):
+    """Attention FLOPs of one token seeing S tokens: 4*S*heads*head_dim per layer."""
+    return _load().oracle_attention_flops(float(S), float(layers), float(heads), float(head_dim))
+
+
+def _pairs_arg(pairs):
+    if pairs is None:
+        return None, 0
+    p = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    return p, p.shape[0]
+
+
+def gqa(q, k_pool, v_pool, block_table, seq_lens, scale, window=0, n_sink=0, sink_logit=None,
+        pairs=None):
+    """GQA / MHA / MQA decode with optional sliding window, sink tokens and learned sink.
+
+    Shapes: q [B,Hq,D]; k_pool, v_pool [num_pages,Hkv,P,D]; block_table [B,max_pages];
+    seq_lens [B]. Returns (out, lse) in float64: out [B,Hq,D] and lse [B,Hq], or
+    [n_pairs,D] and [n_pairs] when ``pairs`` lists (b, h) pairs.
+    """
+    qa, dt = _arr(q)
+    ka, dtk = _arr(k_pool)
+    va, dtv = _arr(v_pool)
+    assert dt in (0, 1) and dt == dtk == dtv
+    bt = np.ascontiguousarray(np.asarray(_arr(block_table)[0], dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(_arr(seq_lens)[0], dtype=np.int32))
+    B, Hq, D = qa.shape
+    _, Hkv, P, D2 = ka.shape
+    assert D2 == D and Hq % Hkv == 0
+    sink = None
+    if sink_logit is not None:
+        sink = np.ascontiguousarray(np.asarray(_arr(sink_logit)[0], dtype=np.float64))
+    pa, n_pairs = _pairs_arg(pairs)
+    n = n_pairs if pa is not None else B * Hq
+    out = np.zeros((n, D), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    _load().oracle_gqa(_ptr(qa), _ptr(ka), _ptr(va), dt, _ptr(bt), _ptr(sl), B, Hq, Hkv, D, P,
+                       bt.shape[1], float(scale), int(window), int(n_sink), _ptr(sink), _ptr(pa),
+                       n_pairs, _ptr(out), _ptr(lse))
+    if pa is None:
+        return out.reshape(B, Hq, D), lse.reshape(B, Hq)
+    return out, lse
+
+
+def mla(q, c_pool, block_table, seq_lens, scale, d_v=512, idx=None, idx_count=None, pairs=None):
+    """Absorbed-latent MLA decode, dense (idx None) or over selected token indices.
+
+    q [B,H,d_qk], c_pool [num_pages,P,d_qk] (both bf16 or both float32); idx [B,k] int32 logical token
+    indices with idx_count[b] valid entries. Returns (out [B,H,d_v], lse [B,H]) float64,
+    or per-pair arrays when ``pairs`` is given.
+    """
+    qa, dt = _arr(q)
+    ca, dtc = _arr(c_pool)
+    assert dt in (0, 1) and dt == dtc
+    bt = np.ascontiguousarray(np.asarray(_arr(block_table)[0], dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(_arr(seq_lens)[0], dtype=np.int32))
+    B, H, d_qk = qa.shape
+    P = ca.shape[1]
+    ia = ic = None
+    stride = 0
+    if idx is not None:
+        ia = np.ascontiguousarray(np.asarray(_arr(idx)[0], dtype=np.int32))
+        ic = np.ascontiguousarray(np.asarray(_arr(idx_count)[0], dtype=np.int32))
+        stride = ia.shape[1]
+    pa, n_pairs = _pairs_arg(pairs)
+    n = n_pairs if pa is not None else B * H
+    out = np.zeros((n, d_v), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    _load().oracle_mla(_ptr(qa), _ptr(ca), dt, _ptr(bt), _ptr(sl), _ptr(ia), _ptr(ic), stride, B, H,
+                       d_qk, d_v, P, bt.shape[1], float(scale), _ptr(pa), n_pairs, _ptr(out),
+                       _ptr(lse))
+    if pa is None:
+        return out.reshape(B, H, d_v), lse.reshape(B, H)
+    return out, lse
+
+
+def indexer_scores(q, k_pool, w, block_table, seq_lens, batches=None):
+    """fp64 indexer scores [n_b, max L] for the listed batch rows (NaN past L_b)."""
+    qa, dt = _arr(q)
+    ka, dtk = _arr(k_pool)
+    assert dt == 1 and dtk == 1
+    wa = np.ascontiguousarray(np.asarray(_arr(w)[0], dtype=np.float32))
+    bt = np.ascontiguousarray(np.asarray(_arr(block_table)[0], dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(_arr(seq_lens)[0], dtype=np.int32))
+    B, Hi, Di = qa.shape
+    P = ka.shape[1]
+    bl = np.arange(B, dtype=np.int32) if batches is None else np.asarray(batches, dtype=np.int32)
+    bl = np.ascontiguousarray(bl)
+    stride = int(sl[bl].max())
+    out = np.full((len(bl), stride), np.nan, dtype=np.float64)
+    _load().oracle_indexer_scores(_ptr(qa), _ptr(ka), _ptr(wa), _ptr(bt), _ptr(sl), Hi, Di, P,
+                                  bt.shape[1], _ptr(bl), len(bl), stride, _ptr(out))
+    return out
+
+
+def topk(scores, k):
+    """Indices (ascending) of the min(k, L) largest scores; ties go to the lower index.
+
+    ``scores`` is a 1-D array whose comparisons are taken in its own precision: pass
+    float32 values to decide in float32, float64 values to decide in float64.
+    """
+    s = np.ascontiguousarray(np.asarray(scores, dtype=np.float64).reshape(-1))
+    out = np.zeros((max(1, min(int(k), s.shape[0])),), dtype=np.int32)
+    cnt = _load().oracle_topk(_ptr(s), s.shape[0], int(k), _ptr(out))
+    return out[:cnt].copy()

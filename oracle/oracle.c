@@ -1,0 +1,248 @@
+/*
+ * oracle.c -- plain, slow fp64 CPU reference for single-token decode attention
+ * over a paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library. It shares no code,
+ * header or table with the CUDA path, and the CUDA path never calls it.
+ *
+ * Every result is the plain definition written out: scores, one softmax over
+ * the visible tokens, a weighted sum of values. No online softmax, no split,
+ * no tiling. Inputs are read as stored (bf16 or fp32) and widened exactly to
+ * double; all arithmetic is double; outputs are double.
+ *
+ * Sources (page title, section):
+ *  - "Overview of Attention Mechanism", GQA / Code (repeat_kv and
+ *    eager_attention_forward): scores q.k * scaling, softmax, times V; KV head
+ *    j serves query heads j*n_rep .. j*n_rep + n_rep-1.
+ *  - "All the attentions", section 4 (Sliding Window): key j is visible to
+ *    query i iff j <= i and j > i - W.
+ *  - "Long context, KV eviction and sparse attention", KV eviction:
+ *    StreamingLLM: the first n_sink tokens are kept alongside the window.
+ *  - "Attention Optimizations", Attention sinks; "Overview of Attention
+ *    Mechanism", StreamingLLM (softmax-off-by-one): a learned sink is one more
+ *    logit in the softmax denominator whose value vector is zero.
+ *  - "All the attentions", section 8 (PagedAttention): logical page n of
+ *    sequence b lives at physical page block_table[b][n]; output unchanged.
+ *  - "Attention Optimizations", DSA / Computation Path: MLA caches one
+ *    576-wide row per token (512 latent + 64 RoPE key); the first 512 entries
+ *    are the value part. Indexer score I_t = sum_h w_h * ReLU(q_h . k_t);
+ *    indices = the k largest scores.
+ *  - "Attention Optimizations", KV cache size: bytes = S * 2 * layers *
+ *    kv_heads * d_head * bytes_per_element.
+ *
+ * Conventions: seq_lens[b] counts cached tokens including the token being
+ * decoded, so the query sits at position i = L_b - 1 and every cached token
+ * t <= i. dtype 0 = float32, 1 = bfloat16 (stored as uint16).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static double widen(const void *base, int dtype, size_t i) {
+    if (dtype == 0) return (double)((const float *)base)[i];
+    uint32_t u = (uint32_t)((const uint16_t *)base)[i] << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Physical row of logical token t of sequence b; rows are page-major with
+ * `heads_per_page` head slots per page (the GQA pool stores [page][head][slot]). */
+static size_t pool_row(const int32_t *block_table, int max_pages, int page_size,
+                       int heads_per_page, int b, int head, long t) {
+    int page = block_table[(size_t)b * max_pages + t / page_size];
+    return ((size_t)page * heads_per_page + head) * page_size + (size_t)(t % page_size);
+}
+
+/* KV cache size: tokens * 2 (K and V) * layers * kv heads * head dim * bytes. */
+double oracle_kv_cache_bytes(double tokens, double layers, double kv_heads, double d_head,
+                             double bytes_per_elem) {
+    return tokens * 2.0 * layers * kv_heads * d_head * bytes_per_elem;
+}
+
+/* MLA cache size: one (latent + RoPE key) row per token per layer, no K/V pair. */
+double oracle_mla_cache_bytes(double tokens, double layers, double d_latent, double d_rope,
+                              double bytes_per_elem) {
+    return tokens * layers * (d_latent + d_rope) * bytes_per_elem;
+}
+
+/* Attention FLOPs for one token that sees S tokens: 4 * S * heads * head_dim per
+ * layer (half for q.k, half for p.v), times layers. */
+double oracle_attention_flops(double S, double layers, double heads, double head_dim) {
+    return 4.0 * S * heads * head_dim * layers;
+}
+
+/* Is token t visible to the query at position L-1?
+ * window <= 0 means no window (all t < L). */
+static int visible(long t, long L, long window, long n_sink) {
+    if (t < 0 || t >= L) return 0;
+    if (t < n_sink) return 1;
+    if (window <= 0) return 1;
+    long i = L - 1;
+    return t <= i && t > i - window;
+}
+
+/*
+ * Grouped-query attention for one decode token per sequence.
+ * q [B,Hq,D]; k_pool, v_pool [num_pages,Hkv,P,D]; out [B,Hq,D]; lse [B,Hq]
+ * (natural log of the softmax denominator, with the max folded back in).
+ * sink_logit: NULL or [Hq] (logit in the same units as scale*q.k).
+ * pairs: NULL (all (b,h)) or n_pairs (b,h) pairs; out/lse are then indexed by pair.
+ */
+void oracle_gqa(const void *q, const void *k_pool, const void *v_pool, int dtype,
+                const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv,
+                int D, int page_size, int max_pages, double scale, long window, long n_sink,
+                const double *sink_logit, const int32_t *pairs, int n_pairs, double *out,
+                double *lse) {
+    int n_rep = Hq / Hkv;
+    int n = pairs ? n_pairs : B * Hq;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int p = 0; p < n; p++) {
+        int b = pairs ? pairs[2 * p] : p / Hq;
+        int h = pairs ? pairs[2 * p + 1] : p % Hq;
+        int g = h / n_rep;
+        long L = seq_lens[b];
+        double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        double m = -INFINITY;
+        for (long t = 0; t < L; t++) {
+            if (!visible(t, L, window, n_sink)) continue;
+            size_t row = pool_row(block_table, max_pages, page_size, Hkv, b, g, t);
+            double dot = 0.0;
+            for (int d = 0; d < D; d++)
+                dot += widen(q, dtype, ((size_t)b * Hq + h) * D + d) *
+                       widen(k_pool, dtype, row * D + d);
+            s[t] = scale * dot;
+            if (s[t] > m) m = s[t];
+        }
+        double sig = sink_logit ? sink_logit[h] : -INFINITY;
+        if (sig > m) m = sig;
+        double denom = 0.0;
+        double *o = out + (size_t)p * D;
+        for (int d = 0; d < D; d++) o[d] = 0.0;
+        for (long t = 0; t < L; t++) {
+            if (!visible(t, L, window, n_sink)) continue;
+            size_t row = pool_row(block_table, max_pages, page_size, Hkv, b, g, t);
+            double e = exp(s[t] - m);
+            denom += e;
+            for (int d = 0; d < D; d++) o[d] += e * widen(v_pool, dtype, row * D + d);
+        }
+        if (sink_logit) denom += exp(sig - m); /* sink: denominator only, zero value */
+        for (int d = 0; d < D; d++) o[d] /= denom;
+        lse[p] = m + log(denom);
+        free(s);
+    }
+}
+
+/*
+ * Absorbed-latent MLA decode (one shared 576-wide row per token).
+ * q [B,H,d_qk]; c_pool [num_pages,P,d_qk] (dtype 0 float32 / 1 bf16);
+ * out [B,H,d_v]; lse [B,H].
+ * idx: NULL (dense: tokens 0..L_b-1) or [B, idx_stride] logical token indices
+ * with idx_count[b] valid entries (sparse, the DSA selection).
+ * Score s_t = scale * sum_{j<d_qk} q_j c_t[j]; value = c_t[0:d_v].
+ */
+void oracle_mla(const void *q, const void *c_pool, int dtype, const int32_t *block_table,
+                const int32_t *seq_lens, const int32_t *idx, const int32_t *idx_count,
+                int idx_stride, int B, int H, int d_qk, int d_v, int page_size, int max_pages,
+                double scale, const int32_t *pairs, int n_pairs, double *out, double *lse) {
+    int n = pairs ? n_pairs : B * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int p = 0; p < n; p++) {
+        int b = pairs ? pairs[2 * p] : p / H;
+        int h = pairs ? pairs[2 * p + 1] : p % H;
+        long L = seq_lens[b];
+        long cnt = idx ? idx_count[b] : L;
+        double *s = (double *)malloc(sizeof(double) * (size_t)(cnt > 0 ? cnt : 1));
+        double m = -INFINITY;
+        for (long j = 0; j < cnt; j++) {
+            long t = idx ? idx[(size_t)b * idx_stride + j] : j;
+            size_t row = pool_row(block_table, max_pages, page_size, 1, b, 0, t);
+            double dot = 0.0;
+            for (int d = 0; d < d_qk; d++)
+                dot += widen(q, dtype, ((size_t)b * H + h) * d_qk + d) *
+                       widen(c_pool, dtype, row * d_qk + d);
+            s[j] = scale * dot;
+            if (s[j] > m) m = s[j];
+        }
+        double denom = 0.0;
+        double *o = out + (size_t)p * d_v;
+        for (int d = 0; d < d_v; d++) o[d] = 0.0;
+        for (long j = 0; j < cnt; j++) {
+            long t = idx ? idx[(size_t)b * idx_stride + j] : j;
+            size_t row = pool_row(block_table, max_pages, page_size, 1, b, 0, t);
+            double e = exp(s[j] - m);
+            denom += e;
+            for (int d = 0; d < d_v; d++) o[d] += e * widen(c_pool, dtype, row * d_qk + d);
+        }
+        for (int d = 0; d < d_v; d++) o[d] /= denom;
+        lse[p] = m + log(denom);
+        free(s);
+    }
+}
+
+/*
+ * Lightning-indexer scores: I_t = sum_h w_h * max(0, sum_j q_h[j] k_t[j]).
+ * q [B,Hi,Di] bf16; k_pool [num_pages,P,Di] bf16; w [B,Hi] float32;
+ * scores [n_b, out_stride] for the listed batch rows (t < L_b written).
+ */
+void oracle_indexer_scores(const void *q, const void *k_pool, const float *w,
+                           const int32_t *block_table, const int32_t *seq_lens, int Hi, int Di,
+                           int page_size, int max_pages, const int32_t *b_list, int n_b,
+                           long out_stride, double *scores) {
+    for (int bi = 0; bi < n_b; bi++) {
+        int b = b_list[bi];
+        long L = seq_lens[b];
+#pragma omp parallel for schedule(static)
+        for (long t = 0; t < L; t++) {
+            size_t row = pool_row(block_table, max_pages, page_size, 1, b, 0, t);
+            double total = 0.0;
+            for (int h = 0; h < Hi; h++) {
+                double dot = 0.0;
+                for (int j = 0; j < Di; j++)
+                    dot += widen(q, 1, ((size_t)b * Hi + h) * Di + j) *
+                           widen(k_pool, 1, row * Di + j);
+                total += (double)w[(size_t)b * Hi + h] * (dot > 0.0 ? dot : 0.0);
+            }
+            scores[(size_t)bi * out_stride + t] = total;
+        }
+    }
+}
+
+typedef struct {
+    double score;
+    int32_t index;
+} scored_t;
+
+/* larger score first; equal scores: lower index first */
+static int by_score_then_index(const void *a, const void *b) {
+    const scored_t *x = (const scored_t *)a, *y = (const scored_t *)b;
+    if (x->score > y->score) return -1;
+    if (x->score < y->score) return 1;
+    return (x->index > y->index) - (x->index < y->index);
+}
+
+static int ascending_i32(const void *a, const void *b) {
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+/*
+ * Top-k selection: the indices of the min(k, L) largest scores, ties going to
+ * the lower index; written in ascending index order to idx_out[0..count-1].
+ * Returns count.
+ */
+int oracle_topk(const double *scores, long L, int k, int32_t *idx_out) {
+    scored_t *all = (scored_t *)malloc(sizeof(scored_t) * (size_t)(L > 0 ? L : 1));
+    for (long t = 0; t < L; t++) {
+        all[t].score = scores[t];
+        all[t].index = (int32_t)t;
+    }
+    qsort(all, (size_t)L, sizeof(scored_t), by_score_then_index);
+    int count = (long)k < L ? k : (int)L;
+    for (int j = 0; j < count; j++) idx_out[j] = all[j].index;
+    qsort(idx_out, (size_t)count, sizeof(int32_t), ascending_i32);
+    free(all);
+    return count;
+}
