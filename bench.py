@@ -1,0 +1,398 @@
+"""Benchmark: decode-attention KV-cache bandwidth (GB/s) and attention steps/s.
+
+One step = one decode-attention call over one batch of synthetic, seeded inputs whose
+KV cache is already resident in HBM. The headline workload is the Llama-3-8B-shaped GQA
+decode over a 64-token paged cache with a shuffled block table (B=32, Hq=32, Hkv=8,
+D=128, L ~ U[4096, 8192]); its KV bytes (~805 MB) exceed L2, so consecutive steps cannot
+be served from cache. The sliding-window, MLA and DSA workloads are measured too (one
+step each between L2 flushes, flush excluded) and reported under "workloads".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {kvdecode,reference}]
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead (a bounded sample
+of the same workload per step, same metric and unit).
+Under torchrun each rank runs the same workload on its own GPU (independent sequences:
+weak scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+NOMINAL_HBM_GBS = 8000.0
+HEADLINE = "llama3_8b_gqa_paged"
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+# ---------------------------------------------------------------------------------------
+# Workload runners (device side)
+# ---------------------------------------------------------------------------------------
+class GqaRunner:
+    """attn_decode_gqa_paged / attn_decode_swa_sink on a named workload."""
+    launches_per_step = 1
+    kernel = "gqa_decode_bf16_kernel"
+
+    def __init__(self, name, dev):
+        import kv_cache_decode_split_gb300 as kvd
+        self.kvd = kvd
+        self.name = name
+        self.x = x = W.build(name)
+        self.dev = dev
+        self.q = x.q.to(dev)
+        self.k = x.k_pool.to(dev)
+        self.v = x.v_pool.to(dev)
+        self.bt = x.block_table.to(dev)
+        self.sl = x.seq_lens.to(dev)
+        self.sink = x.sink_logit.to(dev) if x.sink_logit is not None else None
+        self.out = torch.empty_like(self.q)
+        self.ws = kvd.Workspace(dev)
+        self.swa = x.window > 0 or x.n_sink > 0 or x.sink_logit is not None
+        lens = x.seq_lens.tolist()
+        elt = x.q.element_size()
+        tok = 0
+        for L in lens:
+            if self.swa:
+                vis = set(range(min(x.n_sink, L))) | set(range(max(0, L - x.window), L))
+                tok += len(vis)
+            else:
+                tok += L
+        self.tokens = tok
+        self.bytes = tok * x.Hkv * x.D * 2 * elt      # K and V rows the method must read
+        self.flops = 4.0 * tok * x.Hkv * (x.Hq // x.Hkv) * x.D
+
+    def step(self, q=None, out=None):
+        x = self.x
+        q = self.q if q is None else q
+        out = self.out if out is None else out
+        if self.swa:
+            return self.kvd.attn_decode_swa_sink(q, self.k, self.v, self.bt, self.sl, x.window,
+                                                 x.n_sink, self.sink, scale=x.scale, out=out,
+                                                 workspace=self.ws)
+        return self.kvd.attn_decode_gqa_paged(q, self.k, self.v, self.bt, self.sl, scale=x.scale,
+                                              out=out, workspace=self.ws)
+
+    def config(self):
+        x = self.x
+        return {"workload": self.name, "B": x.B, "Hq": x.Hq, "Hkv": x.Hkv, "D": x.D,
+                "page_size": x.page_size, "window": x.window, "n_sink": x.n_sink,
+                "learned_sink": x.sink_logit is not None,
+                "seq_len_mean": float(x.seq_lens.float().mean()), "kv_bytes": self.bytes}
+
+    # --- end-to-end through the public API from pinned host buffers
+    def e2e_setup(self):
+        self.h_q = self.x.q.pin_memory()
+        self.h_bt = self.x.block_table.pin_memory()
+        self.h_sl = self.x.seq_lens.pin_memory()
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.d_q = torch.empty_like(self.q)
+        return (self.h_q.numel() * self.h_q.element_size() + self.h_bt.numel() * 4 +
+                self.h_sl.numel() * 4), self.h_out.numel() * self.h_out.element_size()
+
+    def e2e_step(self):
+        self.d_q.copy_(self.h_q, non_blocking=True)
+        self.bt.copy_(self.h_bt, non_blocking=True)
+        self.sl.copy_(self.h_sl, non_blocking=True)
+        self.step(q=self.d_q)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    # --- the oracle on host cores, over a bounded sample of the same workload
+    def oracle_sample(self, budget_s):
+        import numpy as np
+        import oracle
+        x = self.x
+        G = x.Hq // x.Hkv
+        rng = np.random.default_rng(0)
+        units = [(b, g) for b in range(x.B) for g in range(x.Hkv)]
+        rng.shuffle(units)
+        t0 = time.perf_counter()
+        done_bytes, n = 0, 0
+        lens = x.seq_lens.tolist()
+        for b, g in units:
+            pairs = [(b, g * G + j) for j in range(G)]
+            oracle.gqa(x.q, x.k_pool, x.v_pool, x.block_table, x.seq_lens, x.scale, x.window,
+                       x.n_sink, x.sink_logit, pairs=pairs)
+            L = lens[b]
+            if self.swa:
+                vis = len(set(range(min(x.n_sink, L))) | set(range(max(0, L - x.window), L)))
+            else:
+                vis = L
+            done_bytes += vis * x.D * 2 * x.q.element_size()
+            n += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        el = time.perf_counter() - t0
+        return done_bytes, el, f"{n} of {len(units)} (sequence, KV head) groups, all {G} query heads each"
+
+
+RUNNERS = {"gqa": GqaRunner, "swa": GqaRunner}
+
+
+def make_runner(name, dev):
+    return RUNNERS[W.WORKLOADS[name].kind](name, dev)
+
+
+# ---------------------------------------------------------------------------------------
+# Timing helpers
+# ---------------------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def flush_l2(buf):
+    buf.zero_()
+
+
+def time_steps(fn, steps, stream):
+    """Per-step CUDA-event durations (ms) on `stream`, back to back."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        fn()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return ev[0].elapsed_time(ev[-1]), per
+
+
+def time_flushed(fn, iters, stream, flush):
+    per = []
+    for _ in range(iters):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        per.append(a.elapsed_time(b))
+    return per
+
+
+# ---------------------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    name = args.workload
+    wl = W.WORKLOADS[name]
+    x_runner = GqaRunner.__new__(GqaRunner)
+    x_runner.x = x = W.build(name)
+    x_runner.swa = x.window > 0 or x.n_sink > 0 or x.sink_logit is not None
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    vals = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        nbytes, el, desc = x_runner.oracle_sample(per_step)
+        if i >= args.warmup:
+            vals.append(nbytes / el / 1e9)
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": "decode-attn KV GB/s", "value": v, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": {"workload": name, "desc": wl.description},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"per step: {desc}, about {per_step:.0f} s of CPU work"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="kvdecode", choices=["kvdecode", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--extra", default="all", help="comma list of extra workloads, 'all' or 'none'")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = measured_peaks()
+
+    r = make_runner(args.workload, dev)
+    for _ in range(args.warmup):
+        r.step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        total_ms, per = time_steps(r.step, args.steps, stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    value = world * r.bytes / (ms * 1e-3) / 1e9
+    clocks = clk.summary()
+
+    # end-to-end through the public API with pinned host buffers
+    h2d, d2h = r.e2e_setup()
+    for _ in range(3):
+        r.e2e_step()
+    torch.cuda.synchronize()
+    e2e_total, _ = time_steps(r.e2e_step, args.steps, stream)
+    e2e_ms = e2e_total / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    kern_ms = statistics.mean(per)
+    achieved = r.bytes / (kern_ms * 1e-3) / 1e9
+    line = {
+        "metric": "decode-attn KV GB/s", "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) rounded to bf16, shapes of the named workload",
+        "config": dict(r.config(), l2="KV bytes larger than L2; steps back to back",
+                       parallelism=f"replicas{world}" if world > 1 else "single"),
+        "steps_per_s": 1000.0 / ms,
+        "frac_of_nominal_8tbs": value / world / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "kernel": r.kernel, "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "peak_source": peak_src, "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None},
+        "e2e": {"value": world * r.bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": r.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+
+    # other workloads: one step between L2 flushes (flush excluded from the timing)
+    extras = [] if args.extra == "none" else (
+        [n for n in W.WORKLOADS if n not in (args.workload, "tiny_gqa_fp32")] if args.extra == "all"
+        else [n for n in args.extra.split(",") if n])
+    if extras and rank == 0:
+        flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        res = {}
+        del r
+        for name in extras:
+            try:
+                rr = make_runner(name, dev)
+            except KeyError:
+                res[name] = {"status": "not built"}
+                continue
+            try:
+                for _ in range(3):
+                    rr.step()
+                torch.cuda.synchronize()
+                per = time_flushed(rr.step, max(10, args.steps // 2), stream,
+                                   lambda: flush_l2(flush_buf))
+            except Exception as e:  # an entry point not built yet reports, not crashes
+                res[name] = {"status": f"error: {e}"}
+                del rr
+                continue
+            med = statistics.median(per)
+            gbs = rr.bytes / (med * 1e-3) / 1e9
+            res[name] = {"us_per_step": med * 1e3, "kv_GBps": gbs, "steps_per_s": 1000.0 / med,
+                         "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+                         "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+                         "tflops": rr.flops / (med * 1e-3) / 1e12, "kernel": rr.kernel,
+                         "l2": "flushed before each step", "config": rr.config()}
+            del rr
+            torch.cuda.empty_cache()
+        line["workloads"] = res
+
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        rr = GqaRunner.__new__(GqaRunner)
+        rr.x = W.build(args.workload)
+        rr.swa = False
+        nbytes, el, desc = rr.oracle_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": nbytes / el / 1e9, "unit": "GB/s",
+                                "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{desc}, {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

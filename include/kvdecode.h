@@ -1,0 +1,200 @@
+/*
+ * kvdecode.h -- C ABI of libkvdecode.so: single-token decode attention over a
+ * long, paged KV cache on one GB300 GPU (sm_103a).
+ *
+ * Operations (each names the passage that defines it):
+ *  - attn_decode_gqa_paged: grouped-query attention of one new token per
+ *    sequence over its paged cache. "Overview of Attention Mechanism", GQA /
+ *    Code (query head h reads KV head h / (Hq/Hkv), scores q.k * scaling,
+ *    softmax, weighted sum of V); "All the attentions", section 8
+ *    (PagedAttention: a block table maps each sequence's logical pages to
+ *    physical pages and the output does not change).
+ *  - attn_decode_swa_sink: the same over a sliding window plus attention
+ *    sinks. "All the attentions", section 4 (key j visible to query i iff
+ *    j <= i and j > i - W); "Long context, KV eviction and sparse attention",
+ *    KV eviction: StreamingLLM (the first tokens are always kept);
+ *    "Attention Optimizations", Attention sinks (a learned per-head sink
+ *    logit in the softmax denominator, with no value).
+ *  - attn_decode_mla: absorbed-latent MLA decode over one shared 576-wide
+ *    row per token (512 latent + 64 RoPE key; value = the first 512).
+ *    "Attention Optimizations", DSA / Computation Path and KV cache size;
+ *    "Overview of Attention Mechanism", MLA (absorption of W^UK and W^UV).
+ *  - dsa_indexer_topk: lightning-indexer scores of every cached token,
+ *    I_t = sum_h w_h * ReLU(q_h . k_t), then the indices of the k largest.
+ *    "Attention Optimizations", DSA / Computation Path; "All the
+ *    attentions", section 5 (DSA).
+ *  - dsa_topk: the selection step alone, over scores the caller provides.
+ *  - attn_decode_mla_sparse: MLA over only the selected tokens.
+ *    "Attention Optimizations", DSA / Computation Path (gather of the
+ *    selected cache rows, then attention).
+ *
+ * Common conventions
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *    never allocates, frees or retains memory. Tensors are dense, row-major,
+ *    16-byte aligned.
+ *  - seq_lens[b] (device, int32) counts cached tokens INCLUDING the token
+ *    being decoded: its K/V (or latent row) were appended before the call, so
+ *    the query sits at position L_b - 1. 1 <= L_b <= max_pages * page_size.
+ *  - block_table[b][n] (device, int32, [B, max_pages]) is the physical page of
+ *    logical page n of sequence b, 0 <= page < num_pages. Entries past the
+ *    last page of a sequence are not read.
+ *  - GQA pools are [num_pages, Hkv, page_size, D]; the MLA latent pool is
+ *    [num_pages, page_size, 576]; the indexer key pool [num_pages,
+ *    page_size, Di]. page_size is a power of two, 16 <= page_size <= 256.
+ *  - scale multiplies q.k before the softmax (1/sqrt(D) for GQA, 1/sqrt(192)
+ *    for DeepSeek-V3 MLA: the un-absorbed 128 + 64 query width).
+ *  - Every call is asynchronous on `stream`. Split-KV partial results live in
+ *    the caller's workspace `ws` of at least kvd_workspace_size(...) bytes,
+ *    zero-filled once before its first use; the kernels leave it ready for
+ *    the next call. Calls that share a workspace must be ordered on one
+ *    stream.
+ *  - Return value: KVD_OK, or a negative KVD_ERR_* code. Argument checks run
+ *    on the host before any launch; on failure nothing is launched and the
+ *    outputs are untouched. Faults the host cannot see (a block-table entry or
+ *    sequence length out of range, a bounded device wait that gave up) are
+ *    recorded in the workspace and read with kvd_check_device_error(); an
+ *    out-of-range page or length is clamped (never dereferenced).
+ */
+#ifndef KVDECODE_H
+#define KVDECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum kvd_status {
+    KVD_OK = 0,
+    KVD_ERR_INVALID_ARG = -1,         /* null pointer, bad size or alignment */
+    KVD_ERR_UNSUPPORTED = -2,         /* shape or dtype this build does not handle */
+    KVD_ERR_CUDA = -3,                /* a CUDA call or launch failed */
+    KVD_ERR_TIMEOUT = -4,             /* (device) a bounded wait gave up */
+    KVD_ERR_WORKSPACE_TOO_SMALL = -5, /* ws_bytes below kvd_workspace_size() */
+    KVD_ERR_DEVICE_OOB = -6           /* (device) page index or length out of range */
+};
+
+enum kvd_dtype { KVD_F32 = 0, KVD_BF16 = 1 };
+
+enum kvd_op {
+    KVD_OP_GQA = 0,
+    KVD_OP_SWA = 1,
+    KVD_OP_MLA = 2,
+    KVD_OP_DSA_TOPK = 3,
+    KVD_OP_MLA_SPARSE = 4
+};
+
+/*
+ * Dense GQA / MHA / MQA decode over a paged cache.
+ *  q       [B, Hq, D]                      dtype
+ *  k_pool  [num_pages, Hkv, page_size, D]  dtype
+ *  v_pool  [num_pages, Hkv, page_size, D]  dtype
+ *  out     [B, Hq, D]                      dtype (bf16 in -> bf16 out, f32 -> f32)
+ *  lse_out [B, Hq] float32, nullable: natural-log softmax normaliser
+ *          log(sum_t exp(scale q.k_t)).
+ * Supported: Hq % Hkv == 0, D in {64, 128}, dtype KVD_BF16 or KVD_F32,
+ * Hq/Hkv <= 128.
+ */
+int attn_decode_gqa_paged(const void *q, const void *k_pool, const void *v_pool,
+                          const int32_t *block_table, const int32_t *seq_lens, void *out,
+                          float *lse_out, int B, int Hq, int Hkv, int D, int page_size,
+                          int max_pages, int num_pages, float scale, int dtype, void *ws,
+                          size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Sliding-window + sink decode. Visible tokens of sequence b:
+ *   { t < min(n_sink_tokens, L_b) }  U  { L_b - window <= t < L_b }
+ * (the window counts the decoded token itself; sink tokens that fall inside
+ * the window are counted once). sink_logit [Hq] float32, nullable: a learned
+ * per-query-head logit, in the units of scale*q.k, added once to the softmax
+ * denominator with a zero value vector (sink_logit = 0 is softmax-off-by-one;
+ * -inf is no sink). Other arguments as attn_decode_gqa_paged; window >= 1,
+ * n_sink_tokens >= 0.
+ */
+int attn_decode_swa_sink(const void *q, const void *k_pool, const void *v_pool,
+                         const int32_t *block_table, const int32_t *seq_lens, void *out,
+                         float *lse_out, int B, int Hq, int Hkv, int D, int page_size,
+                         int max_pages, int num_pages, float scale, int dtype, int window,
+                         int n_sink_tokens, const float *sink_logit, void *ws, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/*
+ * Absorbed MLA decode over all cached tokens.
+ *  q       [B, H, d_qk] bf16: per head [W_UK^T q_nope (512) ; rotated q_pe (64)]
+ *  c_pool  [num_pages, page_size, d_qk] bf16: rows [c_KV (512) ; rotated k_pe (64)]
+ *  out     [B, H, d_v] bf16 = sum_t softmax_t(scale q.c_t) c_t[0:d_v]
+ *  lse_out [B, H] float32, nullable.
+ * Supported: H == 128, d_qk == 576, d_v == 512.
+ */
+int attn_decode_mla(const void *q, const void *c_pool, const int32_t *block_table,
+                    const int32_t *seq_lens, void *out, float *lse_out, int B, int H, int d_qk,
+                    int d_v, int page_size, int max_pages, int num_pages, float scale, void *ws,
+                    size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * DSA indexer + top-k.
+ *  q_idx      [B, Hi, Di] bf16 indexer queries
+ *  k_idx_pool [num_pages, page_size, Di] bf16 indexer key cache
+ *  w          [B, Hi] float32 per-head weights (any positive factor such as
+ *             Hi^-0.5 may be folded in; it does not change the selection)
+ *  topk_idx   [B, k] int32 out: logical token positions of the min(k, L_b)
+ *             largest scores, ascending; ties go to the lower position; slots
+ *             past the count hold -1
+ *  topk_count [B] int32 out: min(k, L_b)
+ *  scores_out [B, max_pages*page_size] float32, nullable: the fp32 scores
+ *             (entries past L_b are not written)
+ * Supported: Hi == 64, Di == 128, 1 <= k <= 4096.
+ */
+int dsa_indexer_topk(const void *q_idx, const void *k_idx_pool, const float *w,
+                     const int32_t *block_table, const int32_t *seq_lens, int32_t *topk_idx,
+                     int32_t *topk_count, float *scores_out, int B, int Hi, int Di, int page_size,
+                     int max_pages, int num_pages, int k, void *ws, size_t ws_bytes,
+                     cudaStream_t stream);
+
+/*
+ * Top-k selection alone over caller-provided scores.
+ *  scores [B, score_stride] float32 (row b holds lens[b] scores; NaN not allowed)
+ *  lens   [B] int32 device, 1 <= lens[b] <= score_stride
+ *  outputs and tie rule as dsa_indexer_topk. Supported: 1 <= k <= 4096.
+ */
+int dsa_topk(const float *scores, const int32_t *lens, int32_t *topk_idx, int32_t *topk_count,
+             int B, int score_stride, int k, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * MLA over the selected tokens only.
+ *  topk_idx [B, k] int32 logical positions (< L_b); topk_count [B] int32
+ *  (1 <= count <= k); other arguments as attn_decode_mla. Order of the
+ *  indices does not matter; each listed position is attended once.
+ */
+int attn_decode_mla_sparse(const void *q, const void *c_pool, const int32_t *block_table,
+                           const int32_t *seq_lens, const int32_t *topk_idx,
+                           const int32_t *topk_count, void *out, float *lse_out, int B, int H,
+                           int d_qk, int d_v, int k, int page_size, int max_pages, int num_pages,
+                           float scale, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Workspace bytes for one call of `op` (enum kvd_op). Arguments that do not
+ * apply to the op are ignored: H is Hq for GQA/SWA and the head count for
+ * MLA; D is the head dim (GQA/SWA) or d_v (MLA); max_len = max_pages *
+ * page_size; window/n_sink for SWA; k for the DSA ops. Returns 0 for an
+ * unknown op or an unsupported shape.
+ */
+size_t kvd_workspace_size(int op, int B, int H, int Hkv, int D, int max_len, int window,
+                          int n_sink, int k);
+
+/*
+ * Synchronise `stream`, return (and clear) the first device-side error that
+ * kernels using workspace `ws` recorded: KVD_OK, KVD_ERR_TIMEOUT or
+ * KVD_ERR_DEVICE_OOB; KVD_ERR_CUDA if the synchronisation itself failed.
+ */
+int kvd_check_device_error(void *ws, cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *kvd_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVDECODE_H */

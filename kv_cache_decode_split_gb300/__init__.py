@@ -1,0 +1,240 @@
+"""kv_cache_decode_split_gb300 -- single-token decode attention over a long, paged KV cache
+on one GB300 GPU.
+
+A thin Python binding over the C ABI of ``libkvdecode.so`` (``include/kvdecode.h``): each
+function has the name of its C entry point, takes torch CUDA tensors, and only marshals
+pointers, sizes and the current stream. Every step of the computation runs in the
+library's CUDA kernels; PyTorch provides device memory and streams.
+
+Operations:
+  attn_decode_gqa_paged   GQA / MHA / MQA over a paged cache
+  attn_decode_swa_sink    sliding window + sink tokens / learned sink logit
+  attn_decode_mla         absorbed-latent MLA (576-wide rows, value = first 512)
+  dsa_indexer_topk        indexer scores + top-k selection
+  dsa_topk                top-k selection over given scores
+  attn_decode_mla_sparse  MLA over the selected tokens
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+from ._lib import KvdError, OP
+
+lib = _lib.load()
+
+__all__ = [
+    "attn_decode_gqa_paged", "attn_decode_swa_sink", "attn_decode_mla", "dsa_indexer_topk",
+    "dsa_topk", "attn_decode_mla_sparse", "kvd_workspace_size", "kvd_check_device_error",
+    "Workspace", "KvdError",
+]
+
+_DT = {torch.float32: 0, torch.bfloat16: 1}
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status, where):
+    if status != 0:
+        raise KvdError(status, where)
+
+
+def _need(t, name, dtype=None, dim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dims")
+
+
+def kvd_workspace_size(op, B, H, Hkv=1, D=0, max_len=1, window=0, n_sink=0, k=0):
+    return int(lib.kvd_workspace_size(OP[op] if isinstance(op, str) else int(op), int(B), int(H),
+                                      int(Hkv), int(D), int(max_len), int(window), int(n_sink),
+                                      int(k)))
+
+
+def kvd_check_device_error(ws, stream=None):
+    """Synchronise and return the device error recorded in a workspace (0 if none)."""
+    buf = ws.buffer if isinstance(ws, Workspace) else ws
+    return int(lib.kvd_check_device_error(_p(buf), _stream(stream)))
+
+
+class Workspace:
+    """A zero-filled device buffer reused across calls (grown on demand).
+
+    The kernels leave it ready for the next call, so it is zeroed only when it is
+    (re)allocated. Calls sharing one workspace must be ordered on one stream.
+    """
+
+    def __init__(self, device=None):
+        self.device = torch.device(device) if device is not None else torch.device("cuda")
+        self.buffer = torch.zeros(0, dtype=torch.uint8, device=self.device)
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buffer.numel() < nbytes:
+            self.buffer = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=self.device)
+        return self.buffer
+
+
+_default_ws = {}
+
+
+def _ws(workspace, nbytes, device):
+    if workspace is None:
+        key = torch.device(device).index
+        workspace = _default_ws.setdefault(key, Workspace(device))
+    if isinstance(workspace, Workspace):
+        buf = workspace.get(nbytes)
+    else:
+        buf = workspace
+    if buf.numel() < nbytes:
+        raise KvdError(-5, "workspace")
+    return buf
+
+
+def _gqa_args(q, k_pool, v_pool, block_table, seq_lens):
+    _need(q, "q", dim=3)
+    _need(k_pool, "k_pool", q.dtype, 4)
+    _need(v_pool, "v_pool", q.dtype, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    if q.dtype not in _DT:
+        raise TypeError("q must be float32 or bfloat16")
+    B, Hq, D = q.shape
+    num_pages, Hkv, P, D2 = k_pool.shape
+    if D2 != D or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("k_pool / v_pool must be [num_pages, Hkv, page_size, D]")
+    if block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_table / seq_lens batch mismatch")
+    return B, Hq, Hkv, D, P, block_table.shape[1], num_pages
+
+
+def attn_decode_gqa_paged(q, k_pool, v_pool, block_table, seq_lens, scale=None, out=None,
+                          lse_out=None, workspace=None, stream=None):
+    """Decode attention of q [B,Hq,D] over a paged K/V pool [num_pages,Hkv,P,D]."""
+    B, Hq, Hkv, D, P, max_pages, num_pages = _gqa_args(q, k_pool, v_pool, block_table, seq_lens)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    nbytes = kvd_workspace_size("gqa", B, Hq, Hkv, D, max_pages * P)
+    ws = _ws(workspace, nbytes, q.device)
+    st = lib.attn_decode_gqa_paged(_p(q), _p(k_pool), _p(v_pool), _p(block_table), _p(seq_lens),
+                                   _p(out), _p(lse_out), B, Hq, Hkv, D, P, max_pages, num_pages,
+                                   scale, _DT[q.dtype], _p(ws), ws.numel(), _stream(stream))
+    _check(st, "attn_decode_gqa_paged")
+    return out
+
+
+def attn_decode_swa_sink(q, k_pool, v_pool, block_table, seq_lens, window, n_sink_tokens=0,
+                         sink_logit=None, scale=None, out=None, lse_out=None, workspace=None,
+                         stream=None):
+    """Sliding-window (+ sink tokens, + learned sink logit [Hq]) decode attention."""
+    B, Hq, Hkv, D, P, max_pages, num_pages = _gqa_args(q, k_pool, v_pool, block_table, seq_lens)
+    if sink_logit is not None:
+        _need(sink_logit, "sink_logit", torch.float32, 1)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    nbytes = kvd_workspace_size("swa", B, Hq, Hkv, D, max_pages * P, window, n_sink_tokens)
+    ws = _ws(workspace, nbytes, q.device)
+    st = lib.attn_decode_swa_sink(_p(q), _p(k_pool), _p(v_pool), _p(block_table), _p(seq_lens),
+                                  _p(out), _p(lse_out), B, Hq, Hkv, D, P, max_pages, num_pages,
+                                  scale, _DT[q.dtype], int(window), int(n_sink_tokens),
+                                  _p(sink_logit), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "attn_decode_swa_sink")
+    return out
+
+
+def _mla_args(q, c_pool, block_table, seq_lens):
+    _need(q, "q", torch.bfloat16, 3)
+    _need(c_pool, "c_pool", torch.bfloat16, 3)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, H, d_qk = q.shape
+    num_pages, P, d2 = c_pool.shape
+    if d2 != d_qk:
+        raise ValueError("c_pool must be [num_pages, page_size, d_qk]")
+    return B, H, d_qk, P, block_table.shape[1], num_pages
+
+
+def attn_decode_mla(q, c_pool, block_table, seq_lens, scale=1.0 / math.sqrt(192), d_v=512,
+                    out=None, lse_out=None, workspace=None, stream=None):
+    """Absorbed-latent MLA decode: q [B,H,576] over latent rows [num_pages,P,576]."""
+    B, H, d_qk, P, max_pages, num_pages = _mla_args(q, c_pool, block_table, seq_lens)
+    out = torch.empty(B, H, d_v, dtype=torch.bfloat16, device=q.device) if out is None else out
+    nbytes = kvd_workspace_size("mla", B, H, 1, d_v, max_pages * P)
+    ws = _ws(workspace, nbytes, q.device)
+    st = lib.attn_decode_mla(_p(q), _p(c_pool), _p(block_table), _p(seq_lens), _p(out),
+                             _p(lse_out), B, H, d_qk, d_v, P, max_pages, num_pages, float(scale),
+                             _p(ws), ws.numel(), _stream(stream))
+    _check(st, "attn_decode_mla")
+    return out
+
+
+def dsa_indexer_topk(q_idx, k_idx_pool, w, block_table, seq_lens, k=2048, topk_idx=None,
+                     topk_count=None, scores_out=None, workspace=None, stream=None):
+    """Indexer scores of every cached token and the indices of the k largest (ascending)."""
+    _need(q_idx, "q_idx", torch.bfloat16, 3)
+    _need(k_idx_pool, "k_idx_pool", torch.bfloat16, 3)
+    _need(w, "w", torch.float32, 2)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, Hi, Di = q_idx.shape
+    num_pages, P, _ = k_idx_pool.shape
+    max_pages = block_table.shape[1]
+    dev = q_idx.device
+    topk_idx = torch.empty(B, k, dtype=torch.int32, device=dev) if topk_idx is None else topk_idx
+    topk_count = torch.empty(B, dtype=torch.int32, device=dev) if topk_count is None else topk_count
+    nbytes = kvd_workspace_size("dsa_topk", B, Hi, 1, Di, max_pages * P, k=k)
+    ws = _ws(workspace, nbytes, dev)
+    st = lib.dsa_indexer_topk(_p(q_idx), _p(k_idx_pool), _p(w), _p(block_table), _p(seq_lens),
+                              _p(topk_idx), _p(topk_count), _p(scores_out), B, Hi, Di, P,
+                              max_pages, num_pages, int(k), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dsa_indexer_topk")
+    return topk_idx, topk_count
+
+
+def dsa_topk(scores, lens, k=2048, topk_idx=None, topk_count=None, workspace=None, stream=None):
+    """Top-k selection over scores [B, stride] float32 with lens [B] valid entries per row."""
+    _need(scores, "scores", torch.float32, 2)
+    _need(lens, "lens", torch.int32, 1)
+    B, stride = scores.shape
+    dev = scores.device
+    topk_idx = torch.empty(B, k, dtype=torch.int32, device=dev) if topk_idx is None else topk_idx
+    topk_count = torch.empty(B, dtype=torch.int32, device=dev) if topk_count is None else topk_count
+    nbytes = kvd_workspace_size("dsa_topk", B, 1, 1, 0, stride, k=k)
+    ws = _ws(workspace, nbytes, dev)
+    st = lib.dsa_topk(_p(scores), _p(lens), _p(topk_idx), _p(topk_count), B, stride, int(k),
+                      _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dsa_topk")
+    return topk_idx, topk_count
+
+
+def attn_decode_mla_sparse(q, c_pool, block_table, seq_lens, topk_idx, topk_count,
+                           scale=1.0 / math.sqrt(192), d_v=512, out=None, lse_out=None,
+                           workspace=None, stream=None):
+    """MLA over the selected tokens: topk_idx [B,k] logical positions, topk_count [B]."""
+    B, H, d_qk, P, max_pages, num_pages = _mla_args(q, c_pool, block_table, seq_lens)
+    _need(topk_idx, "topk_idx", torch.int32, 2)
+    _need(topk_count, "topk_count", torch.int32, 1)
+    k = topk_idx.shape[1]
+    out = torch.empty(B, H, d_v, dtype=torch.bfloat16, device=q.device) if out is None else out
+    nbytes = kvd_workspace_size("mla_sparse", B, H, 1, d_v, max_pages * P, k=k)
+    ws = _ws(workspace, nbytes, q.device)
+    st = lib.attn_decode_mla_sparse(_p(q), _p(c_pool), _p(block_table), _p(seq_lens),
+                                    _p(topk_idx), _p(topk_count), _p(out), _p(lse_out), B, H,
+                                    d_qk, d_v, k, P, max_pages, num_pages, float(scale), _p(ws),
+                                    ws.numel(), _stream(stream))
+    _check(st, "attn_decode_mla_sparse")
+    return out

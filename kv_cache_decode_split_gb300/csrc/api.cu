@@ -1,0 +1,255 @@
+// api.cu -- the C ABI of libkvdecode.so: argument validation, split planning,
+// workspace layout, tensor-map encoding and kernel launches. See include/kvdecode.h.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <algorithm>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "kvd_host.h"
+
+namespace kvd {
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+inline int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+}  // namespace
+
+int num_sms() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+    }
+    return n;
+}
+
+int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return KVD_ERR_CUDA;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KVD_OK : KVD_ERR_CUDA;
+}
+
+// Split plan: chunk length chosen so that the grid is a few waves of the resident CTAs.
+int gqa_plan(int B, int Hq, int Hkv, int D, int max_len, int window, int n_sink, int dtype,
+             GqaPlan* plan) {
+    const int G = Hq / Hkv;
+    plan->NHG = cdiv(G, 16);
+    plan->units = B * Hkv * plan->NHG;
+    const long long vis = window > 0 ? std::min<long long>(max_len, (long long)window + n_sink)
+                                     : max_len;
+    const int per_sm = (dtype == KVD_F32) ? 4 : (D == 128 ? 2 : 3);
+    const long long target = 4LL * num_sms() * per_sm;
+    long long chunk = (static_cast<long long>(plan->units) * vis) / std::max(1LL, target);
+    chunk = std::max(128LL, std::min(4096LL, (chunk / 64) * 64));
+    auto chunks_for = [&](long long C) -> int {
+        if (window <= 0) return cdiv(max_len, C);
+        const int a = (n_sink > 0 ? cdiv(std::min(n_sink, max_len), C) : 0) +
+                      cdiv(std::min(window, max_len) + 63, C);
+        const int m = cdiv(std::min<long long>(max_len, (long long)window + n_sink), C);
+        return std::max(a, m);
+    };
+    while (chunks_for(chunk) > kGqaMaxChunks) chunk += 64;
+    plan->chunk = static_cast<int>(chunk);
+    plan->max_chunks = std::max(1, chunks_for(chunk));
+    size_t off = kWsHeaderBytes;
+    plan->off_counters = off;
+    off = round256(off + sizeof(int) * plan->units);
+    plan->off_lse = off;
+    off = round256(off + sizeof(float) * (size_t)plan->units * plan->max_chunks * 16);
+    plan->off_o = off;
+    off = round256(off + sizeof(float) * (size_t)plan->units * plan->max_chunks * 16 * D);
+    plan->total = off;
+    return KVD_OK;
+}
+
+}  // namespace kvd
+
+using namespace kvd;
+
+namespace {
+
+int gqa_common(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+               const int32_t* seq_lens, void* out, float* lse_out, int B, int Hq, int Hkv, int D,
+               int page_size, int max_pages, int num_pages, float scale, int dtype, int window,
+               int n_sink, const float* sink_logit, void* ws, size_t ws_bytes,
+               cudaStream_t stream) {
+    if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out || !ws)
+        return KVD_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_pages < 1 || num_pages < 1)
+        return KVD_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || window < 0 || n_sink < 0) return KVD_ERR_INVALID_ARG;
+    if (!pow2(page_size) || page_size < 16 || page_size > 256) return KVD_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128) return KVD_ERR_UNSUPPORTED;
+    if (dtype != KVD_F32 && dtype != KVD_BF16) return KVD_ERR_UNSUPPORTED;
+    if (Hq / Hkv > 128) return KVD_ERR_UNSUPPORTED;
+    if ((long long)num_pages * Hkv * page_size >= (1LL << 31)) return KVD_ERR_UNSUPPORTED;
+    if ((long long)max_pages * page_size >= (1LL << 30)) return KVD_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
+        !aligned16(ws))
+        return KVD_ERR_INVALID_ARG;
+    const int max_len = max_pages * page_size;
+    GqaPlan plan;
+    gqa_plan(B, Hq, Hkv, D, max_len, window, n_sink, dtype, &plan);
+    if (ws_bytes < plan.total) return KVD_ERR_WORKSPACE_TOO_SMALL;
+
+    GqaParams p;
+    std::memset(&p, 0, sizeof p);
+    p.q = q;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.lse_out = lse_out;
+    p.sink_logit = sink_logit;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    p.err = reinterpret_cast<int*>(w);
+    p.counters = reinterpret_cast<int*>(w + plan.off_counters);
+    p.part_lse = reinterpret_cast<float*>(w + plan.off_lse);
+    p.part_o = reinterpret_cast<float*>(w + plan.off_o);
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.D = D;
+    p.G = Hq / Hkv;
+    p.NHG = plan.NHG;
+    p.page_size = page_size;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    p.max_len = max_len;
+    p.window = window;
+    p.n_sink = n_sink;
+    p.chunk = plan.chunk;
+    p.max_chunks = plan.max_chunks;
+    p.dtype = dtype;
+    p.scale_log2 = scale * 1.4426950408889634f;
+
+    if (dtype == KVD_F32) return gqa_launch(plan, p, nullptr, nullptr, stream);
+    CUtensorMap tk, tv;
+    const uint64_t rows = (uint64_t)num_pages * Hkv * page_size;
+    const uint32_t box_rows = page_size < 64 ? page_size : 64;
+    if (make_tmap_bf16_2d(&tk, k_pool, rows, D, box_rows) != KVD_OK) return KVD_ERR_CUDA;
+    if (make_tmap_bf16_2d(&tv, v_pool, rows, D, box_rows) != KVD_OK) return KVD_ERR_CUDA;
+    return gqa_launch(plan, p, &tk, &tv, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_decode_gqa_paged(const void* q, const void* k_pool, const void* v_pool,
+                          const int32_t* block_table, const int32_t* seq_lens, void* out,
+                          float* lse_out, int B, int Hq, int Hkv, int D, int page_size,
+                          int max_pages, int num_pages, float scale, int dtype, void* ws,
+                          size_t ws_bytes, cudaStream_t stream) {
+    return gqa_common(q, k_pool, v_pool, block_table, seq_lens, out, lse_out, B, Hq, Hkv, D,
+                      page_size, max_pages, num_pages, scale, dtype, 0, 0, nullptr, ws, ws_bytes,
+                      stream);
+}
+
+int attn_decode_swa_sink(const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* block_table, const int32_t* seq_lens, void* out,
+                         float* lse_out, int B, int Hq, int Hkv, int D, int page_size,
+                         int max_pages, int num_pages, float scale, int dtype, int window,
+                         int n_sink_tokens, const float* sink_logit, void* ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+    if (window < 1) return KVD_ERR_INVALID_ARG;
+    return gqa_common(q, k_pool, v_pool, block_table, seq_lens, out, lse_out, B, Hq, Hkv, D,
+                      page_size, max_pages, num_pages, scale, dtype, window, n_sink_tokens,
+                      sink_logit, ws, ws_bytes, stream);
+}
+
+int attn_decode_mla(const void*, const void*, const int32_t*, const int32_t*, void*, float*, int,
+                    int, int, int, int, int, int, float, void*, size_t, cudaStream_t) {
+    return KVD_ERR_UNSUPPORTED;
+}
+
+int dsa_indexer_topk(const void*, const void*, const float*, const int32_t*, const int32_t*,
+                     int32_t*, int32_t*, float*, int, int, int, int, int, int, int, void*, size_t,
+                     cudaStream_t) {
+    return KVD_ERR_UNSUPPORTED;
+}
+
+int dsa_topk(const float*, const int32_t*, int32_t*, int32_t*, int, int, int, void*, size_t,
+             cudaStream_t) {
+    return KVD_ERR_UNSUPPORTED;
+}
+
+int attn_decode_mla_sparse(const void*, const void*, const int32_t*, const int32_t*,
+                           const int32_t*, const int32_t*, void*, float*, int, int, int, int, int,
+                           int, int, int, float, void*, size_t, cudaStream_t) {
+    return KVD_ERR_UNSUPPORTED;
+}
+
+size_t kvd_workspace_size(int op, int B, int H, int Hkv, int D, int max_len, int window,
+                          int n_sink, int k) {
+    (void)k;
+    if (B < 1 || H < 1 || max_len < 1) return 0;
+    if (op == KVD_OP_GQA || op == KVD_OP_SWA) {
+        if (Hkv < 1 || H % Hkv != 0 || (D != 64 && D != 128)) return 0;
+        GqaPlan plan;
+        gqa_plan(B, H, Hkv, D, max_len, op == KVD_OP_SWA ? std::max(window, 1) : 0,
+                 op == KVD_OP_SWA ? std::max(n_sink, 0) : 0, KVD_BF16, &plan);
+        GqaPlan plan32;
+        gqa_plan(B, H, Hkv, D, max_len, op == KVD_OP_SWA ? std::max(window, 1) : 0,
+                 op == KVD_OP_SWA ? std::max(n_sink, 0) : 0, KVD_F32, &plan32);
+        return std::max(plan.total, plan32.total);
+    }
+    return 0;
+}
+
+int kvd_check_device_error(void* ws, cudaStream_t stream) {
+    if (!ws) return KVD_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return KVD_ERR_CUDA;
+    int flag = 0;
+    if (cudaMemcpy(&flag, ws, sizeof flag, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KVD_ERR_CUDA;
+    if (flag != 0) {
+        if (cudaMemset(ws, 0, sizeof flag) != cudaSuccess) return KVD_ERR_CUDA;
+    }
+    return flag;
+}
+
+const char* kvd_status_string(int status) {
+    switch (status) {
+        case KVD_OK: return "ok";
+        case KVD_ERR_INVALID_ARG: return "invalid argument";
+        case KVD_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case KVD_ERR_CUDA: return "CUDA error";
+        case KVD_ERR_TIMEOUT: return "device wait timed out";
+        case KVD_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case KVD_ERR_DEVICE_OOB: return "page index or sequence length out of range";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

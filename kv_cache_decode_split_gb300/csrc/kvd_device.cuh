@@ -1,0 +1,211 @@
+// kvd_device.cuh -- device-side building blocks shared by the decode kernels:
+// bounded mbarrier waits, TMA tile loads, ldmatrix / mma.sync / movmatrix
+// wrappers, the workspace error flag and the split-KV range arithmetic.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kvd_host.h"
+
+namespace kvd {
+
+__device__ __forceinline__ void record_error(int* flag, int code) {
+    if (flag) atomicCAS(flag, 0, code);
+}
+
+// A wait gives up after this many SM clock cycles (about 1-3 s at GB300 clocks),
+// records KVD_ERR_TIMEOUT and lets the kernel unwind instead of hanging the GPU.
+constexpr long long kWaitCycles = 4000000000LL;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until the phase with the given parity has completed. Returns false (and
+// records KVD_ERR_TIMEOUT) if that does not happen within kWaitCycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const long long start = clock64();
+    while (!mbar_try_wait(a, parity)) {
+        if (clock64() - start > kWaitCycles) {
+            record_error(err, KVD_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------------------
+// TMA (bulk tensor copies, global -> shared, completion counted on an mbarrier)
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Byte offset of the 16-byte chunk holding (row, col) of a tile that TMA wrote with
+// 128-byte swizzling: rows of 64 bf16 (128 B), chunk index XOR (row % 8), one box of
+// `rows` rows per 64 columns.
+__device__ __forceinline__ uint32_t swz128(int row, int col, int rows) {
+    return static_cast<uint32_t>((col >> 6) * rows * 128 + row * 128 +
+                                 ((((col & 63) >> 3) ^ (row & 7)) << 4));
+}
+
+// ---------------------------------------------------------------------------------------
+// Warp-level tensor-core helpers (ldmatrix, mma.sync m16n8k16 bf16, movmatrix)
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// c[16x8] += a[16x16] * b[16x8], bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 2^x on the SFU (ex2.approx); exp2(-inf) = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---------------------------------------------------------------------------------------
+// Visible ranges and split-KV chunks.
+// The visible set of a decode query at position L-1 is {t < min(n_sink, L)} U
+// {L - window <= t < L} (window <= 0: all t < L). It is at most two ranges. Each range
+// is cut into chunks of `chunk` tokens aligned to 64-token tile boundaries, so that
+// interior chunks cover whole tiles.
+// ---------------------------------------------------------------------------------------
+struct Ranges {
+    int lo0, hi0, lo1, hi1;
+};
+
+__device__ __forceinline__ Ranges visible_ranges(int L, int window, int n_sink) {
+    const int w0 = window > 0 ? max(0, L - window) : 0;
+    const int s = min(n_sink, L);
+    if (s >= w0) return Ranges{0, L, 0, 0};
+    return Ranges{0, s, w0, L};
+}
+
+__device__ __forceinline__ int range_chunks(int lo, int hi, int chunk) {
+    if (hi <= lo) return 0;
+    const int a = lo & ~63;
+    return (hi - a + chunk - 1) / chunk;
+}
+
+__device__ __forceinline__ int total_chunks(const Ranges& r, int chunk) {
+    return range_chunks(r.lo0, r.hi0, chunk) + range_chunks(r.lo1, r.hi1, chunk);
+}
+
+__device__ __forceinline__ bool chunk_bounds(const Ranges& r, int chunk, int c, int& lo,
+                                             int& hi) {
+    const int n0 = range_chunks(r.lo0, r.hi0, chunk);
+    int rlo = r.lo0, rhi = r.hi0;
+    if (c >= n0) {
+        c -= n0;
+        if (c >= range_chunks(r.lo1, r.hi1, chunk)) return false;
+        rlo = r.lo1;
+        rhi = r.hi1;
+    }
+    const int a = rlo & ~63;
+    lo = max(rlo, a + c * chunk);
+    hi = min(rhi, a + (c + 1) * chunk);
+    return lo < hi;
+}
+
+// Sequence length, clamped to [1, max_len]; an out-of-range value is recorded.
+__device__ __forceinline__ int load_len(const int32_t* seq_lens, int b, int max_len, int* err) {
+    int L = seq_lens[b];
+    if (L < 1 || L > max_len) {
+        record_error(err, KVD_ERR_DEVICE_OOB);
+        L = min(max(L, 1), max_len);
+    }
+    return L;
+}
+
+// Physical page of logical page n of sequence b, clamped to a valid page.
+__device__ __forceinline__ int load_page(const int32_t* block_table, int max_pages,
+                                         int num_pages, int b, int n, int* err) {
+    int pg = block_table[static_cast<size_t>(b) * max_pages + n];
+    if (pg < 0 || pg >= num_pages) {
+        record_error(err, KVD_ERR_DEVICE_OOB);
+        pg = 0;
+    }
+    return pg;
+}
+
+}  // namespace kvd

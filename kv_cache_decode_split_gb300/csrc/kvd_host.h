@@ -1,0 +1,62 @@
+// kvd_host.h -- internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kvdecode.h"
+
+namespace kvd {
+
+// The first 256 bytes of every workspace hold the device error flag (int32 at offset 0).
+constexpr size_t kWsHeaderBytes = 256;
+
+constexpr int kGqaMaxChunks = 256;  // split-KV chunks per (sequence, KV head, head block)
+
+// Kernel arguments of the GQA / SWA decode (one struct for both dtypes).
+struct GqaParams {
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    void* out;
+    float* lse_out;
+    const float* sink_logit;
+    float* part_o;    // [units, max_chunks, 16, D]
+    float* part_lse;  // [units, max_chunks, 16]   (log2 domain)
+    int* counters;    // [units]
+    int* err;         // workspace error flag
+    int B, Hq, Hkv, D, G, NHG;
+    int page_size, max_pages, num_pages, max_len;
+    int window, n_sink;  // window <= 0: dense
+    int chunk, max_chunks;
+    int dtype;
+    float scale_log2;  // scale * log2(e)
+};
+
+// Host-side split plan and workspace layout of one GQA / SWA call.
+struct GqaPlan {
+    int chunk;       // tokens per split (multiple of 64)
+    int max_chunks;  // grid.x
+    int NHG;         // head blocks of <= 16 query heads per KV head
+    int units;       // B * Hkv * NHG
+    size_t off_counters, off_lse, off_o, total;
+};
+
+int gqa_plan(int B, int Hq, int Hkv, int D, int max_len, int window, int n_sink, int dtype,
+             GqaPlan* plan);
+int gqa_launch(const GqaPlan& plan, const GqaParams& p, const CUtensorMap* tk,
+               const CUtensorMap* tv, cudaStream_t stream);
+int gqa_stage_bytes(int D);
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with a {64, box_rows} box and
+// 128-byte swizzle (cols a multiple of 64). Returns KVD_OK or KVD_ERR_CUDA.
+int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows);
+
+int num_sms();
+
+}  // namespace kvd

@@ -1,0 +1,84 @@
+"""The C ABI without a GPU: the library builds, loads, exports every entry point the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "kvdecode.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import importlib.util
+    import sys
+    sys.path.insert(0, ROOT)
+    import __graft_entry__ as g
+    path = g._builder().build()
+    spec = importlib.util.spec_from_file_location(
+        "kvdecode_lib", os.path.join(ROOT, "kv_cache_decode_split_gb300", "_lib.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.load(path)
+
+
+def test_header_declares_the_entry_points():
+    names = _header_functions()
+    for n in ("attn_decode_gqa_paged", "attn_decode_swa_sink", "attn_decode_mla",
+              "dsa_indexer_topk", "attn_decode_mla_sparse", "dsa_topk", "kvd_workspace_size",
+              "kvd_check_device_error", "kvd_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _header_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert lib.kvd_status_string(0) == b"ok"
+    assert lib.kvd_status_string(-5) == b"workspace too small"
+
+
+def _gqa(lib, **kw):
+    a = dict(q=16, k=16, v=16, bt=16, sl=16, out=16, lse=None, B=2, Hq=8, Hkv=2, D=64, P=64,
+             max_pages=4, num_pages=8, scale=0.125, dtype=1, ws=256, ws_bytes=1 << 30)
+    a.update(kw)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.attn_decode_gqa_paged(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["bt"]), vp(a["sl"]),
+                                     vp(a["out"]), vp(a["lse"]), a["B"], a["Hq"], a["Hkv"], a["D"],
+                                     a["P"], a["max_pages"], a["num_pages"], a["scale"], a["dtype"],
+                                     vp(a["ws"]), a["ws_bytes"], None)
+
+
+def test_gqa_argument_checks(lib):
+    assert _gqa(lib, q=None) == -1
+    assert _gqa(lib, Hq=6, Hkv=4) == -1
+    assert _gqa(lib, B=0) == -1
+    assert _gqa(lib, D=96) == -2
+    assert _gqa(lib, P=48) == -2
+    assert _gqa(lib, dtype=7) == -2
+    assert _gqa(lib, q=24) == -1                 # not 16-byte aligned
+    assert _gqa(lib, scale=float("nan")) == -1
+    assert _gqa(lib, ws_bytes=16) == -5
+
+
+def test_swa_requires_positive_window(lib):
+    vp = ctypes.c_void_p
+    st = lib.attn_decode_swa_sink(vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), None, 2, 8, 2, 64,
+                                  64, 4, 8, 0.125, 1, 0, 4, None, vp(256), 1 << 30, None)
+    assert st == -1
+
+
+def test_workspace_size_queries(lib):
+    assert lib.kvd_workspace_size(0, 32, 32, 8, 128, 8192, 0, 0, 0) > 0
+    assert lib.kvd_workspace_size(1, 8, 64, 8, 64, 32768, 4096, 4, 0) > 0
+    assert lib.kvd_workspace_size(0, 2, 6, 4, 64, 256, 0, 0, 0) == 0   # Hq % Hkv != 0
+    assert lib.kvd_workspace_size(99, 2, 8, 2, 64, 256, 0, 0, 0) == 0

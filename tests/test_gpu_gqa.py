@@ -1,0 +1,146 @@
+"""GPU parity of attn_decode_gqa_paged / attn_decode_swa_sink against the fp64 oracle.
+
+Small cases compare every output; the full-size Llama-3-8B-shaped and sliding-window
+workloads compare a seeded sample of (sequence, head) outputs, in the same launch
+configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.parity import assert_attn_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvd():
+    import kv_cache_decode_split_gb300 as m
+    return m
+
+
+_WS = {}
+
+
+def _run(kvd, x, lse=True):
+    dev = "cuda"
+    ws = _WS.setdefault("ws", kvd.Workspace(dev))
+    q, kp, vp = x.q.to(dev), x.k_pool.to(dev), x.v_pool.to(dev)
+    bt, sl = x.block_table.to(dev), x.seq_lens.to(dev)
+    lse_out = torch.empty(x.B, x.Hq, dtype=torch.float32, device=dev) if lse else None
+    if x.window > 0 or x.n_sink > 0 or x.sink_logit is not None:
+        sink = x.sink_logit.to(dev) if x.sink_logit is not None else None
+        out = kvd.attn_decode_swa_sink(q, kp, vp, bt, sl, max(x.window, 1) if x.window > 0 else 1 << 30,
+                                       x.n_sink, sink, scale=x.scale, lse_out=lse_out,
+                                       workspace=ws)
+    else:
+        out = kvd.attn_decode_gqa_paged(q, kp, vp, bt, sl, scale=x.scale, lse_out=lse_out,
+                                        workspace=ws)
+    torch.cuda.synchronize()
+    assert kvd.kvd_check_device_error(ws) == 0
+    return out, lse_out
+
+
+def _compare(kvd, x, tol=None, pairs=None):
+    out, lse = _run(kvd, x)
+    ref, ref_lse = oracle.gqa(x.q, x.k_pool, x.v_pool, x.block_table, x.seq_lens, x.scale,
+                              x.window, x.n_sink, x.sink_logit, pairs=pairs)
+    if pairs is not None:
+        pi = np.asarray(pairs)
+        out = out[pi[:, 0], pi[:, 1]]
+        lse = lse[pi[:, 0], pi[:, 1]]
+    kw = {} if tol is None else dict(max_abs=tol, mean_abs=tol, rel_l2=tol)
+    assert_attn_close(out, ref, what="out", **kw)
+    assert np.max(np.abs(to_np(lse) - ref_lse)) < 2e-3
+
+
+def test_tiny_fp32_workload(kvd):
+    x = W.build("tiny_gqa_fp32")
+    _compare(kvd, x, tol=1e-4)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (32, 8), (4, 4), (16, 1), (32, 1), (12, 4)])
+def test_bf16_paged_ragged(kvd, D, hq, hkv):
+    lens = [1, 63, 64, 65, 200, 1000, 1500, 2047]
+    x = W.make_gqa(len(lens), hq, hkv, D, lens, page_size=64, shuffle=True, extra_pages=5,
+                   seed=100 + D + hq)
+    _compare(kvd, x)
+
+
+@pytest.mark.parametrize("P", [16, 32, 128, 256])
+def test_page_sizes(kvd, P):
+    lens = [5, 130, 777]
+    x = W.make_gqa(3, 8, 2, 128, lens, page_size=P, shuffle=True, seed=200 + P)
+    _compare(kvd, x)
+
+
+def test_fp32_paged_shuffled(kvd):
+    x = W.make_gqa(3, 8, 2, 128, [3, 300, 700], page_size=32, shuffle=True, seed=7,
+                   dtype=torch.float32)
+    _compare(kvd, x, tol=1e-4)
+
+
+@pytest.mark.parametrize("window,n_sink,learned", [(1, 0, False), (64, 4, False), (100, 4, True),
+                                                   (300, 0, True), (5000, 4, False),
+                                                   (700, 70, False), (129, 200, True)])
+def test_swa_sink(kvd, window, n_sink, learned):
+    lens = [1, 3, 64, 190, 1000, 3000]
+    x = W.make_gqa(len(lens), 16, 2, 64, lens, page_size=64, shuffle=True, seed=300 + window,
+                   window=window, n_sink=n_sink, learned_sink=learned)
+    _compare(kvd, x)
+
+
+def test_learned_sink_values(kvd):
+    # softmax-off-by-one (sink logit 0) and a strongly dominant sink
+    x = W.make_gqa(2, 8, 2, 64, [50, 300], page_size=64, seed=9, window=128)
+    x.sink_logit = torch.zeros(8)
+    _compare(kvd, x)
+    x.sink_logit = torch.full((8,), 30.0)
+    _compare(kvd, x)
+
+
+def test_window_at_least_length_equals_dense(kvd):
+    x = W.make_gqa(4, 32, 8, 128, [100, 1000, 4000, 8000], page_size=64, shuffle=True, seed=11)
+    dense, _ = _run(kvd, x)
+    x.window = 8192
+    win, _ = _run(kvd, x)
+    assert torch.equal(dense, win) or torch.allclose(dense.float(), win.float(), atol=1e-2)
+
+
+def _sample_pairs(B, H, n, seed):
+    rng = np.random.default_rng(seed)
+    b = rng.integers(0, B, n)
+    h = rng.integers(0, H, n)
+    return np.stack([b, h], axis=1).astype(np.int32)
+
+
+def test_llama3_8b_full_size_sampled(kvd):
+    x = W.build("llama3_8b_gqa_paged")
+    _compare(kvd, x, pairs=_sample_pairs(x.B, x.Hq, 96, 1))
+
+
+@pytest.mark.parametrize("name", ["swa_sink_tokens", "swa_learned_sink"])
+def test_swa_full_size_sampled(kvd, name):
+    x = W.build(name)
+    _compare(kvd, x, pairs=_sample_pairs(x.B, x.Hq, 96, 2))
+
+
+def test_repeat_calls_reuse_workspace(kvd):
+    x = W.make_gqa(4, 32, 8, 128, [100, 1000, 4000, 8000], page_size=64, shuffle=True, seed=12)
+    a, _ = _run(kvd, x)
+    b, _ = _run(kvd, x)
+    assert torch.equal(a, b)
+
+
+def test_out_of_range_page_is_recorded_not_faulted(kvd):
+    x = W.make_gqa(2, 8, 2, 64, [100, 100], page_size=64, seed=13)
+    x.block_table[1, 0] = 10_000      # past num_pages: clamped on device, flagged
+    dev = "cuda"
+    ws = kvd.Workspace(dev)
+    kvd.attn_decode_gqa_paged(x.q.to(dev), x.k_pool.to(dev), x.v_pool.to(dev),
+                              x.block_table.to(dev), x.seq_lens.to(dev), workspace=ws)
+    assert kvd.kvd_check_device_error(ws) == -6
+    assert kvd.kvd_check_device_error(ws) == 0   # cleared
