@@ -30,8 +30,8 @@
  *
  * Common conventions
  *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
- *    never allocates, frees or retains memory. Tensors are dense, row-major,
- *    16-byte aligned.
+ *    never allocates or frees memory and keeps no pointer past a call. Tensors
+ *    are dense, row-major, 16-byte aligned.
  *  - seq_lens[b] (device, int32) counts cached tokens INCLUDING the token
  *    being decoded: its K/V (or latent row) were appended before the call, so
  *    the query sits at position L_b - 1. 1 <= L_b <= max_pages * page_size.
@@ -102,6 +102,33 @@ int attn_decode_gqa_paged(const void *q, const void *k_pool, const void *v_pool,
                           float *lse_out, int B, int Hq, int Hkv, int D, int page_size,
                           int max_pages, int num_pages, float scale, int dtype, void *ws,
                           size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * attn_decode_gqa_paged without a workspace argument. The pages have no counterpart to
+ * this entry point: it exists for callers that cannot allocate device memory (a plugin
+ * whose host engine owns all device memory and hands out only input and output buffers,
+ * or a decode loop that must not pay the device-wide synchronisation of cudaMalloc /
+ * cudaFree). It allocates nothing and calls no allocating routine.
+ *  - Scratch: a library-owned device array of 32 MiB (every GPU that loads the library
+ *    holds it until the process exits). Shapes whose split plan needs more scratch than
+ *    that return KVD_ERR_WORKSPACE_TOO_SMALL; the Llama-3-8B-shaped decode (B=32,
+ *    Hq=32, Hkv=8, D=128, up to 8192 tokens) needs about 11-21 MiB.
+ *  - The first call on each device looks up the array's device address (a
+ *    cudaGetSymbolAddress on the current device); make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array and clears its counters and error flag (an
+ *    asynchronous memset on `stream`) before launching. Calls that overlap on the GPU
+ *    (different streams without ordering, or concurrent host threads) race on it.
+ *  - Device-side faults are still contained (out-of-range pages and lengths are
+ *    clamped, waits are bounded), but their error flag is cleared by the next call and
+ *    cannot be read with kvd_check_device_error.
+ * Arguments, layouts and supported shapes as attn_decode_gqa_paged.
+ */
+int attn_decode_gqa_paged_static_ws(const void *q, const void *k_pool, const void *v_pool,
+                                    const int32_t *block_table, const int32_t *seq_lens,
+                                    void *out, float *lse_out, int B, int Hq, int Hkv, int D,
+                                    int page_size, int max_pages, int num_pages, float scale,
+                                    int dtype, cudaStream_t stream);
 
 /*
  * Sliding-window + sink decode. Visible tokens of sequence b:

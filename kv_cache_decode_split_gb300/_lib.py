@@ -13,6 +13,7 @@ LIB_PATH = os.path.join(_HERE, "libkvdecode.so")
 
 EXPORTS = (
     "attn_decode_gqa_paged",
+    "attn_decode_gqa_paged_static_ws",
     "attn_decode_swa_sink",
     "attn_decode_mla",
     "dsa_indexer_topk",
@@ -44,13 +45,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     gqa = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I]
     lib.attn_decode_gqa_paged.argtypes = gqa + [P, Z, P]
+    lib.attn_decode_gqa_paged_static_ws.argtypes = gqa + [P]
     lib.attn_decode_swa_sink.argtypes = gqa + [I, I, P, P, Z, P]
     lib.attn_decode_mla.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, Z, P]
     lib.dsa_indexer_topk.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P]
     lib.dsa_topk.argtypes = [P, P, P, P, I, I, I, P, Z, P]
     lib.attn_decode_mla_sparse.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P,
                                            Z, P]
-    for name in ("attn_decode_gqa_paged", "attn_decode_swa_sink", "attn_decode_mla",
+    for name in ("attn_decode_gqa_paged", "attn_decode_gqa_paged_static_ws", "attn_decode_swa_sink", "attn_decode_mla",
                  "dsa_indexer_topk", "dsa_topk", "attn_decode_mla_sparse",
                  "kvd_check_device_error"):
         getattr(lib, name).restype = I

@@ -95,9 +95,9 @@ int gqa_plan(int B, int Hq, int Hkv, int D, int max_len, int window, int n_sink,
 
 using namespace kvd;
 
-namespace {
+namespace kvd {
 
-int gqa_common(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
                const int32_t* seq_lens, void* out, float* lse_out, int B, int Hq, int Hkv, int D,
                int page_size, int max_pages, int num_pages, float scale, int dtype, int window,
                int n_sink, const float* sink_logit, void* ws, size_t ws_bytes,
@@ -162,7 +162,7 @@ int gqa_common(const void* q, const void* k_pool, const void* v_pool, const int3
     return gqa_launch(plan, p, &tk, &tv, stream);
 }
 
-}  // namespace
+}  // namespace kvd
 
 extern "C" {
 
@@ -171,7 +171,7 @@ int attn_decode_gqa_paged(const void* q, const void* k_pool, const void* v_pool,
                           float* lse_out, int B, int Hq, int Hkv, int D, int page_size,
                           int max_pages, int num_pages, float scale, int dtype, void* ws,
                           size_t ws_bytes, cudaStream_t stream) {
-    return gqa_common(q, k_pool, v_pool, block_table, seq_lens, out, lse_out, B, Hq, Hkv, D,
+    return gqa_run(q, k_pool, v_pool, block_table, seq_lens, out, lse_out, B, Hq, Hkv, D,
                       page_size, max_pages, num_pages, scale, dtype, 0, 0, nullptr, ws, ws_bytes,
                       stream);
 }
@@ -183,7 +183,7 @@ int attn_decode_swa_sink(const void* q, const void* k_pool, const void* v_pool,
                          int n_sink_tokens, const float* sink_logit, void* ws, size_t ws_bytes,
                          cudaStream_t stream) {
     if (window < 1) return KVD_ERR_INVALID_ARG;
-    return gqa_common(q, k_pool, v_pool, block_table, seq_lens, out, lse_out, B, Hq, Hkv, D,
+    return gqa_run(q, k_pool, v_pool, block_table, seq_lens, out, lse_out, B, Hq, Hkv, D,
                       page_size, max_pages, num_pages, scale, dtype, window, n_sink_tokens,
                       sink_logit, ws, ws_bytes, stream);
 }

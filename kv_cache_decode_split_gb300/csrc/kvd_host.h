@@ -52,6 +52,12 @@ int gqa_launch(const GqaPlan& plan, const GqaParams& p, const CUtensorMap* tk,
                const CUtensorMap* tv, cudaStream_t stream);
 int gqa_stage_bytes(int D);
 
+// Validate, plan and launch one GQA / SWA decode (window <= 0: dense) using workspace ws.
+int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+            const int32_t* seq_lens, void* out, float* lse_out, int B, int Hq, int Hkv, int D,
+            int page_size, int max_pages, int num_pages, float scale, int dtype, int window,
+            int n_sink, const float* sink_logit, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix with a {64, box_rows} box and
 // 128-byte swizzle (cols a multiple of 64). Returns KVD_OK or KVD_ERR_CUDA.
 int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
