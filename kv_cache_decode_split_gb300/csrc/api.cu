@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstring>
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -58,18 +59,27 @@ int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_
     return r == CUDA_SUCCESS ? KVD_OK : KVD_ERR_CUDA;
 }
 
-// Split plan: chunk length chosen so that the grid is a few waves of the resident CTAs.
-int gqa_plan(int B, int Hq, int Hkv, int D, int max_len, int window, int n_sink, int dtype,
-             GqaPlan* plan) {
+// Split plan. The bf16 kernel is persistent (one CTA per SM pulling work items from a
+// queue), so the chunk length trades load balance (more, shorter items) against the
+// per-item merge cost: aim for about six items per SM, at least four 64-token tiles each.
+int gqa_plan(int B, int Hq, int Hkv, int D, int page_size, int max_len, int window, int n_sink,
+             int dtype, GqaPlan* plan) {
     const int G = Hq / Hkv;
     plan->NHG = cdiv(G, 16);
     plan->units = B * Hkv * plan->NHG;
     const long long vis = window > 0 ? std::min<long long>(max_len, (long long)window + n_sink)
                                      : max_len;
-    const int per_sm = (dtype == KVD_F32) ? 4 : (D == 128 ? 2 : 3);
-    const long long target = 4LL * num_sms() * per_sm;
+    const long long target = (dtype == KVD_F32) ? 8LL * num_sms() : 6LL * num_sms();
     long long chunk = (static_cast<long long>(plan->units) * vis) / std::max(1LL, target);
-    chunk = std::max(128LL, std::min(4096LL, (chunk / 64) * 64));
+    chunk = std::max(256LL, std::min(8192LL, (chunk / 64) * 64));
+    if (dtype == KVD_F32) chunk = std::max(128LL, std::min(chunk, 1024LL));
+    if (const char* env = std::getenv("KVD_GQA_CHUNK")) {  // tuning override (tokens)
+        const long long c = std::atoll(env);
+        if (c >= 64) chunk = (c / 64) * 64;
+    }
+    // a chunk's page pieces must fit one item descriptor
+    const long long box_rows = std::min(page_size, 64);
+    chunk = std::min(chunk, kGqaMaxBoxesPerItem * box_rows);
     auto chunks_for = [&](long long C) -> int {
         if (window <= 0) return cdiv(max_len, C);
         const int a = (n_sink > 0 ? cdiv(std::min(n_sink, max_len), C) : 0) +
@@ -78,11 +88,12 @@ int gqa_plan(int B, int Hq, int Hkv, int D, int max_len, int window, int n_sink,
         return std::max(a, m);
     };
     while (chunks_for(chunk) > kGqaMaxChunks) chunk += 64;
+    if (chunk > kGqaMaxBoxesPerItem * box_rows) return KVD_ERR_UNSUPPORTED;  // too long
     plan->chunk = static_cast<int>(chunk);
     plan->max_chunks = std::max(1, chunks_for(chunk));
     size_t off = kWsHeaderBytes;
     plan->off_counters = off;
-    off = round256(off + sizeof(int) * plan->units);
+    off = round256(off + sizeof(int) * (plan->units + 2));
     plan->off_lse = off;
     off = round256(off + sizeof(float) * (size_t)plan->units * plan->max_chunks * 16);
     plan->off_o = off;
@@ -118,7 +129,8 @@ int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t
         return KVD_ERR_INVALID_ARG;
     const int max_len = max_pages * page_size;
     GqaPlan plan;
-    gqa_plan(B, Hq, Hkv, D, max_len, window, n_sink, dtype, &plan);
+    if (gqa_plan(B, Hq, Hkv, D, page_size, max_len, window, n_sink, dtype, &plan) != KVD_OK)
+        return KVD_ERR_UNSUPPORTED;
     if (ws_bytes < plan.total) return KVD_ERR_WORKSPACE_TOO_SMALL;
 
     GqaParams p;
@@ -142,6 +154,7 @@ int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t
     p.D = D;
     p.G = Hq / Hkv;
     p.NHG = plan.NHG;
+    p.units = plan.units;
     p.page_size = page_size;
     p.max_pages = max_pages;
     p.num_pages = num_pages;
@@ -217,12 +230,15 @@ size_t kvd_workspace_size(int op, int B, int H, int Hkv, int D, int max_len, int
     if (op == KVD_OP_GQA || op == KVD_OP_SWA) {
         if (Hkv < 1 || H % Hkv != 0 || (D != 64 && D != 128)) return 0;
         GqaPlan plan;
-        gqa_plan(B, H, Hkv, D, max_len, op == KVD_OP_SWA ? std::max(window, 1) : 0,
-                 op == KVD_OP_SWA ? std::max(n_sink, 0) : 0, KVD_BF16, &plan);
-        GqaPlan plan32;
-        gqa_plan(B, H, Hkv, D, max_len, op == KVD_OP_SWA ? std::max(window, 1) : 0,
-                 op == KVD_OP_SWA ? std::max(n_sink, 0) : 0, KVD_F32, &plan32);
-        return std::max(plan.total, plan32.total);
+        // the plan's chunk length is smallest (most partials) for 16-token pages
+        size_t need = 0;
+        for (int dt = 0; dt < 2; ++dt) {
+            GqaPlan plan;
+            if (gqa_plan(B, H, Hkv, D, 16, max_len, op == KVD_OP_SWA ? std::max(window, 1) : 0,
+                         op == KVD_OP_SWA ? std::max(n_sink, 0) : 0, dt, &plan) == KVD_OK)
+                need = std::max(need, plan.total);
+        }
+        return need;
     }
     return 0;
 }

@@ -58,13 +58,15 @@ extern "C" int attn_decode_gqa_paged_static_ws(const void* q, const void* k_pool
                             nullptr, 0, stream);
     if ((long long)max_pages * page_size >= (1LL << 30)) return KVD_ERR_UNSUPPORTED;
     kvd::GqaPlan plan;
-    kvd::gqa_plan(B, Hq, Hkv, D, max_pages * page_size, 0, 0, dtype, &plan);
+    if (kvd::gqa_plan(B, Hq, Hkv, D, page_size, max_pages * page_size, 0, 0, dtype, &plan) !=
+        KVD_OK)
+        return KVD_ERR_UNSUPPORTED;
     if (plan.total > kStaticWsBytes) return KVD_ERR_WORKSPACE_TOO_SMALL;
     void* ws = nullptr;
     const int st = static_ws_addr(&ws);
     if (st != KVD_OK) return st;
     // Every call shares the array and finds the previous call's contents in it: the error
-    // flag and the per-(sequence, KV head) completion counters must start at zero.
+    // flag and the work-queue counters must start at zero.
     if (cudaMemsetAsync(ws, 0, plan.off_lse, stream) != cudaSuccess) return KVD_ERR_CUDA;
     return kvd::gqa_run(q, k_pool, v_pool, block_table, seq_lens, out, lse_out, B, Hq, Hkv, D,
                         page_size, max_pages, num_pages, scale, dtype, 0, 0, nullptr, ws,

@@ -14,6 +14,7 @@ namespace kvd {
 constexpr size_t kWsHeaderBytes = 256;
 
 constexpr int kGqaMaxChunks = 256;  // split-KV chunks per (sequence, KV head, head block)
+constexpr int kGqaMaxBoxesPerItem = 64;  // TMA boxes (page pieces of <= 64 tokens) per chunk
 
 // Kernel arguments of the GQA / SWA decode (one struct for both dtypes).
 struct GqaParams {
@@ -27,9 +28,9 @@ struct GqaParams {
     const float* sink_logit;
     float* part_o;    // [units, max_chunks, 16, D]
     float* part_lse;  // [units, max_chunks, 16]   (log2 domain)
-    int* counters;    // [units]
+    int* counters;    // [units] completion counters, then the work queue head and exit count
     int* err;         // workspace error flag
-    int B, Hq, Hkv, D, G, NHG;
+    int B, Hq, Hkv, D, G, NHG, units;
     int page_size, max_pages, num_pages, max_len;
     int window, n_sink;  // window <= 0: dense
     int chunk, max_chunks;
@@ -40,17 +41,16 @@ struct GqaParams {
 // Host-side split plan and workspace layout of one GQA / SWA call.
 struct GqaPlan {
     int chunk;       // tokens per split (multiple of 64)
-    int max_chunks;  // grid.x
+    int max_chunks;  // chunk slots per unit (work items = units * max_chunks)
     int NHG;         // head blocks of <= 16 query heads per KV head
     int units;       // B * Hkv * NHG
     size_t off_counters, off_lse, off_o, total;
 };
 
-int gqa_plan(int B, int Hq, int Hkv, int D, int max_len, int window, int n_sink, int dtype,
-             GqaPlan* plan);
+int gqa_plan(int B, int Hq, int Hkv, int D, int page_size, int max_len, int window, int n_sink,
+             int dtype, GqaPlan* plan);
 int gqa_launch(const GqaPlan& plan, const GqaParams& p, const CUtensorMap* tk,
                const CUtensorMap* tv, cudaStream_t stream);
-int gqa_stage_bytes(int D);
 
 // Validate, plan and launch one GQA / SWA decode (window <= 0: dense) using workspace ws.
 int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
