@@ -102,6 +102,23 @@ int gqa_plan(int B, int Hq, int Hkv, int D, int page_size, int max_len, int wind
     return KVD_OK;
 }
 
+TopkLayout topk_layout(int B, int max_len, int k, bool with_scores) {
+    TopkLayout l;
+    size_t off = kWsHeaderBytes;
+    l.off_hist = off;
+    off = round256(off + sizeof(uint32_t) * (size_t)B * 2048);
+    l.off_counts = off;
+    off = round256(off + sizeof(int) * (size_t)B * 2);
+    l.off_sel = off;
+    off = round256(off + sizeof(int) * (size_t)B * k);
+    l.off_cand = off;
+    off = round256(off + sizeof(int) * (size_t)B * max_len);
+    l.off_scores = off;
+    if (with_scores) off = round256(off + sizeof(float) * (size_t)B * max_len);
+    l.total = off;
+    return l;
+}
+
 }  // namespace kvd
 
 using namespace kvd;
@@ -206,15 +223,93 @@ int attn_decode_mla(const void*, const void*, const int32_t*, const int32_t*, vo
     return KVD_ERR_UNSUPPORTED;
 }
 
-int dsa_indexer_topk(const void*, const void*, const float*, const int32_t*, const int32_t*,
-                     int32_t*, int32_t*, float*, int, int, int, int, int, int, int, void*, size_t,
-                     cudaStream_t) {
-    return KVD_ERR_UNSUPPORTED;
+int dsa_indexer_topk(const void* q_idx, const void* k_idx_pool, const float* w,
+                     const int32_t* block_table, const int32_t* seq_lens, int32_t* topk_idx,
+                     int32_t* topk_count, float* scores_out, int B, int Hi, int Di, int page_size,
+                     int max_pages, int num_pages, int k, void* ws, size_t ws_bytes,
+                     cudaStream_t stream) {
+    if (!q_idx || !k_idx_pool || !w || !block_table || !seq_lens || !topk_idx || !topk_count ||
+        !ws)
+        return KVD_ERR_INVALID_ARG;
+    if (B < 1 || max_pages < 1 || num_pages < 1 || k < 1) return KVD_ERR_INVALID_ARG;
+    if (Hi != 64 || Di != 128 || k > kTopkMaxK) return KVD_ERR_UNSUPPORTED;
+    if (!pow2(page_size) || page_size < 16 || page_size > 256) return KVD_ERR_UNSUPPORTED;
+    if ((long long)num_pages * page_size >= (1LL << 31) || (long long)B * 64 >= (1LL << 31))
+        return KVD_ERR_UNSUPPORTED;
+    if ((long long)max_pages * page_size >= (1LL << 30)) return KVD_ERR_UNSUPPORTED;
+    if (!aligned16(q_idx) || !aligned16(k_idx_pool) || !aligned16(ws) ||
+        (reinterpret_cast<uintptr_t>(w) & 3) || (reinterpret_cast<uintptr_t>(scores_out) & 3))
+        return KVD_ERR_INVALID_ARG;
+    const int max_len = max_pages * page_size;
+    const TopkLayout lay = topk_layout(B, max_len, k, scores_out == nullptr);
+    if (ws_bytes < lay.total) return KVD_ERR_WORKSPACE_TOO_SMALL;
+    uint8_t* wb = static_cast<uint8_t*>(ws);
+    IdxParams ip;
+    std::memset(&ip, 0, sizeof ip);
+    ip.q = q_idx;
+    ip.w = w;
+    ip.block_table = block_table;
+    ip.seq_lens = seq_lens;
+    ip.scores = scores_out ? scores_out : reinterpret_cast<float*>(wb + lay.off_scores);
+    ip.score_stride = max_len;
+    ip.hist = reinterpret_cast<uint32_t*>(wb + lay.off_hist);
+    ip.err = reinterpret_cast<int*>(wb);
+    ip.B = B;
+    ip.page_size = page_size;
+    ip.max_pages = max_pages;
+    ip.num_pages = num_pages;
+    ip.max_len = max_len;
+    ip.tiles_per_b = (max_len + 127) / 128;
+    CUtensorMap tk, tq;
+    if (make_tmap_bf16_2d(&tk, k_idx_pool, (uint64_t)num_pages * page_size, 128,
+                          page_size < 128 ? page_size : 128) != KVD_OK)
+        return KVD_ERR_CUDA;
+    if (make_tmap_bf16_2d(&tq, q_idx, (uint64_t)B * 64, 128, 64) != KVD_OK) return KVD_ERR_CUDA;
+    int st = dsa_indexer_launch(ip, tk, tq, stream);
+    if (st != KVD_OK) return st;
+    TopkParams tp;
+    std::memset(&tp, 0, sizeof tp);
+    tp.scores = ip.scores;
+    tp.score_stride = max_len;
+    tp.lens = seq_lens;
+    tp.hist = ip.hist;
+    tp.counts = reinterpret_cast<int*>(wb + lay.off_counts);
+    tp.sel = reinterpret_cast<int*>(wb + lay.off_sel);
+    tp.cand = reinterpret_cast<int*>(wb + lay.off_cand);
+    tp.topk_idx = topk_idx;
+    tp.topk_count = topk_count;
+    tp.err = ip.err;
+    tp.B = B;
+    tp.k = k;
+    tp.max_len = max_len;
+    return topk_launch(tp, false, stream);
 }
 
-int dsa_topk(const float*, const int32_t*, int32_t*, int32_t*, int, int, int, void*, size_t,
-             cudaStream_t) {
-    return KVD_ERR_UNSUPPORTED;
+int dsa_topk(const float* scores, const int32_t* lens, int32_t* topk_idx, int32_t* topk_count,
+             int B, int score_stride, int k, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!scores || !lens || !topk_idx || !topk_count || !ws) return KVD_ERR_INVALID_ARG;
+    if (B < 1 || score_stride < 1 || k < 1) return KVD_ERR_INVALID_ARG;
+    if (k > kTopkMaxK) return KVD_ERR_UNSUPPORTED;
+    if (!aligned16(ws) || (reinterpret_cast<uintptr_t>(scores) & 3)) return KVD_ERR_INVALID_ARG;
+    const TopkLayout lay = topk_layout(B, score_stride, k, false);
+    if (ws_bytes < lay.total) return KVD_ERR_WORKSPACE_TOO_SMALL;
+    uint8_t* wb = static_cast<uint8_t*>(ws);
+    TopkParams tp;
+    std::memset(&tp, 0, sizeof tp);
+    tp.scores = scores;
+    tp.score_stride = score_stride;
+    tp.lens = lens;
+    tp.hist = reinterpret_cast<uint32_t*>(wb + lay.off_hist);
+    tp.counts = reinterpret_cast<int*>(wb + lay.off_counts);
+    tp.sel = reinterpret_cast<int*>(wb + lay.off_sel);
+    tp.cand = reinterpret_cast<int*>(wb + lay.off_cand);
+    tp.topk_idx = topk_idx;
+    tp.topk_count = topk_count;
+    tp.err = reinterpret_cast<int*>(wb);
+    tp.B = B;
+    tp.k = k;
+    tp.max_len = score_stride;
+    return topk_launch(tp, true, stream);
 }
 
 int attn_decode_mla_sparse(const void*, const void*, const int32_t*, const int32_t*,
@@ -225,11 +320,13 @@ int attn_decode_mla_sparse(const void*, const void*, const int32_t*, const int32
 
 size_t kvd_workspace_size(int op, int B, int H, int Hkv, int D, int max_len, int window,
                           int n_sink, int k) {
-    (void)k;
     if (B < 1 || H < 1 || max_len < 1) return 0;
+    if (op == KVD_OP_DSA_TOPK) {
+        if (k < 1 || k > kTopkMaxK) return 0;
+        return topk_layout(B, max_len, k, true).total;
+    }
     if (op == KVD_OP_GQA || op == KVD_OP_SWA) {
         if (Hkv < 1 || H % Hkv != 0 || (D != 64 && D != 128)) return 0;
-        GqaPlan plan;
         // the plan's chunk length is smallest (most partials) for 16-token pages
         size_t need = 0;
         for (int dt = 0; dt < 2; ++dt) {

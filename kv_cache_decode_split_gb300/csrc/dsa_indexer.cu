@@ -1,0 +1,462 @@
+// dsa_indexer.cu -- the DSA lightning indexer and the top-k selection over its scores.
+//
+// What is computed ("Attention Optimizations", DSA / Computation Path; "All the
+// attentions", section 5): for every cached token t of sequence b,
+//   I_t = sum_h w_h * ReLU(q_h . k_t)        (64 heads x 128 dims, one 128-wide key per token)
+// then the indices of the k largest I_t (ties to the lower position), in ascending order.
+//
+// Indexer (GB300): a persistent kernel, one CTA per SM, each CTA owning a contiguous range
+// of 128-token tiles. One thread streams key tiles with TMA (128-byte swizzle) through a
+// shared-memory ring; one thread issues tcgen05.mma with the tokens as M and the heads as
+// N: D[128 tok x 64 heads] (TMEM, fp32) = K[128 x 128] * Q^T, double-buffered in tensor
+// memory; four epilogue warps read one token row each (tcgen05.ld), apply ReLU and the head
+// weights, write the fp32 score and count its top 11 key bits into a shared-memory
+// histogram, the first pass of the radix selection.
+//
+// Selection: a filter kernel finds, from that histogram, the bucket holding the k-th
+// largest score; tokens above it are selected and tokens inside it become candidates. A
+// finalize kernel (one CTA per sequence) narrows the candidates with further radix passes
+// over a 64-bit key (score key, then position reversed, so the order is total and ties go
+// to the lower position), then sorts the k chosen positions ascending.
+
+#include <algorithm>
+
+#include "kvd_device.cuh"
+#include "kvd_host.h"
+
+namespace kvd {
+
+namespace {
+
+constexpr int kItile = 128;             // tokens per indexer tile (MMA M)
+constexpr int kHi = 64;                 // indexer heads (MMA N)
+constexpr int kDi = 128;                // indexer head dim (MMA K)
+constexpr int kIdxTileBytes = kItile * kDi * 2;   // 32 KB: two 64-dim boxes of 16 KB
+constexpr int kIdxQBytes = kHi * kDi * 2;         // 16 KB: two 64-dim boxes of 8 KB
+constexpr int kIdxStages = 5;
+constexpr int kIdxThreads = 6 * 32;     // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kHistBins = 2048;         // top 11 key bits
+
+struct IdxSmem {
+    uint8_t stage[kIdxStages][kIdxTileBytes];   // 1024-aligned (offset 0)
+    uint8_t qbuf[2][kIdxQBytes];
+    uint32_t hist[kHistBins];
+    float wv[2][kHi];
+    uint64_t full[kIdxStages], empty[kIdxStages];
+    uint64_t qfull[2], qempty[2], tfull[2], tempty[2], done;
+    uint32_t tmem_base;
+};
+constexpr int kIdxSmem = static_cast<int>(sizeof(IdxSmem)) + 1024;
+
+// The tiles a CTA owns: a contiguous slice of the flattened (sequence, tile) list.
+struct TileRange {
+    int begin, end;
+};
+__device__ __forceinline__ TileRange my_tiles(int total) {
+    const long long G = gridDim.x, i = blockIdx.x;
+    return TileRange{static_cast<int>(i * total / G), static_cast<int>((i + 1) * total / G)};
+}
+
+__global__ void __launch_bounds__(kIdxThreads, 1)
+    dsa_indexer_kernel(const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmQ, const IdxParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    IdxSmem& sm = *reinterpret_cast<IdxSmem*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int total = p.B * p.tiles_per_b;
+    const TileRange tr = my_tiles(total);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kIdxStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.qfull[i], 1);
+            mbar_init(&sm.qempty[i], 1);
+            mbar_init(&sm.tfull[i], 1);
+            mbar_init(&sm.tempty[i], 4);
+        }
+        mbar_init(&sm.done, 1);
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sm.hist[i] = 0;
+    if (warp == 1) tmem_alloc(&sm.tmem_base, 128);  // two 64-column fp32 accumulators
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tensormap(&tmK);
+            prefetch_tensormap(&tmQ);
+            const int bp = min(p.page_size, kItile);
+            int cur_b = -1, L = 0;
+            uint32_t g = 0, nq = 0;
+            bool ok = true;
+            for (int f = tr.begin; f < tr.end && ok; ++f) {
+                const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
+                if (b != cur_b) {
+                    L = load_len(p.seq_lens, b, p.max_len, p.err);
+                }
+                if (j * kItile >= L) continue;
+                if (b != cur_b) {
+                    const int qs = nq & 1;
+                    if (!(ok = mbar_wait(&sm.qempty[qs], ((nq >> 1) & 1) ^ 1, p.err))) break;
+                    mbar_arrive_expect_tx(&sm.qfull[qs], kIdxQBytes);
+                    tma_load_2d(sm.qbuf[qs], &tmQ, &sm.qfull[qs], 0, b * kHi);
+                    tma_load_2d(sm.qbuf[qs] + kIdxQBytes / 2, &tmQ, &sm.qfull[qs], 64, b * kHi);
+                    ++nq;
+                    cur_b = b;
+                }
+                const int s = g % kIdxStages;
+                if (!(ok = mbar_wait(&sm.empty[s], ((g / kIdxStages) & 1) ^ 1, p.err))) break;
+                mbar_arrive_expect_tx(&sm.full[s], kIdxTileBytes);
+                for (int sub = 0; sub < kItile / bp; ++sub) {
+                    const int t = j * kItile + sub * bp;
+                    const int tc = t < L ? t : L - 1;  // rows past the end: a valid page
+                    const int pg = load_page(p.block_table, p.max_pages, p.num_pages, b,
+                                             tc / p.page_size, p.err);
+                    const int y = pg * p.page_size + (t % p.page_size);
+                    for (int half = 0; half < 2; ++half)
+                        tma_load_2d(sm.stage[s] + half * (kIdxTileBytes / 2) + sub * bp * 128,
+                                    &tmK, &sm.full[s], half * 64, y);
+                }
+                ++g;
+            }
+            // copies still in flight complete before the CTA may exit
+            const uint32_t first = g > kIdxStages ? g - kIdxStages : 0;
+            for (uint32_t i = first; i < g; ++i)
+                mbar_wait(&sm.full[i % kIdxStages], (i / kIdxStages) & 1, p.err);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kItile, kHi);
+            int cur_b = -1, L = 0;
+            uint32_t g = 0, nq = 0, nt = 0;
+            int qs = 0;
+            bool ok = true;
+            for (int f = tr.begin; f < tr.end && ok; ++f) {
+                const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
+                if (b != cur_b) L = load_len(p.seq_lens, b, p.max_len, nullptr);
+                if (j * kItile >= L) continue;
+                if (b != cur_b) {
+                    if (cur_b >= 0) tc_commit(&sm.qempty[qs]);  // previous q free after its MMAs
+                    qs = nq & 1;
+                    if (!(ok = mbar_wait(&sm.qfull[qs], (nq >> 1) & 1, p.err))) break;
+                    ++nq;
+                    cur_b = b;
+                }
+                const int s = g % kIdxStages;
+                if (!(ok = mbar_wait(&sm.full[s], (g / kIdxStages) & 1, p.err))) break;
+                const int acc = nt & 1;
+                if (!(ok = mbar_wait(&sm.tempty[acc], ((nt >> 1) & 1) ^ 1, p.err))) break;
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sm.stage[s]);
+                const uint32_t b0 = smem_u32(sm.qbuf[qs]);
+#pragma unroll
+                for (int k = 0; k < kDi / 16; ++k) {
+                    const uint32_t koff = (k & 3) * 32;  // 16 bf16 = 32 bytes per k-step
+                    const uint64_t ad =
+                        sw128_kmajor_desc(a0 + (k >> 2) * (kIdxTileBytes / 2) + koff);
+                    const uint64_t bd = sw128_kmajor_desc(b0 + (k >> 2) * (kIdxQBytes / 2) + koff);
+                    tc_mma_bf16(tmem + acc * kHi, ad, bd, idesc, k > 0 ? 1u : 0u);
+                }
+                tc_commit(&sm.empty[s]);     // the smem stage is free once these MMAs are done
+                tc_commit(&sm.tfull[acc]);   // the accumulator is ready
+                ++g;
+                ++nt;
+            }
+            tc_commit(&sm.done);  // every MMA of this CTA has completed
+            mbar_wait(&sm.done, 0, p.err);
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+        const int row = quad * 32 + lane;
+        const int etid = threadIdx.x - 64;  // 0..127
+        int cur_b = -1, L = 0;
+        uint32_t nt = 0, nb = 0;
+        auto flush_hist = [&](int b) {
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+            for (int i = etid; i < kHistBins; i += 128) {
+                const uint32_t c = sm.hist[i];
+                if (c) {
+                    atomicAdd(p.hist + static_cast<size_t>(b) * kHistBins + i, c);
+                    sm.hist[i] = 0;
+                }
+            }
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+        };
+        for (int f = tr.begin; f < tr.end; ++f) {
+            const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
+            if (b != cur_b) L = load_len(p.seq_lens, b, p.max_len, nullptr);
+            if (j * kItile >= L) continue;
+            if (b != cur_b) {
+                if (cur_b >= 0) flush_hist(cur_b);
+                if (etid < kHi) sm.wv[nb & 1][etid] = p.w[static_cast<size_t>(b) * kHi + etid];
+                asm volatile("bar.sync 2, 128;" ::: "memory");
+                ++nb;
+                cur_b = b;
+            }
+            const float* wv = sm.wv[(nb - 1) & 1];
+            const int acc = nt & 1;
+            if (!mbar_wait(&sm.tfull[acc], (nt >> 1) & 1, p.err)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * kHi;
+            float score = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + half * 32, r);
+                tmem_ld_wait(r);
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    score = fmaf(wv[half * 32 + c], fmaxf(__uint_as_float(r[c]), 0.f), score);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+            const int t = j * kItile + row;
+            if (t < L) {
+                p.scores[static_cast<size_t>(b) * p.score_stride + t] = score;
+                atomicAdd(&sm.hist[float_key(score) >> 21], 1u);
+            }
+            ++nt;
+        }
+        if (cur_b >= 0) flush_hist(cur_b);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 128);
+}
+
+// ---------------------------------------------------------------------------------------
+// Selection kernels
+// ---------------------------------------------------------------------------------------
+
+// Histogram of the top 11 key bits of caller-provided scores (dsa_topk only).
+__global__ void __launch_bounds__(256) topk_hist_kernel(const TopkParams p) {
+    __shared__ uint32_t h[kHistBins];
+    const int b = blockIdx.y;
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = 0;
+    __syncthreads();
+    const int L = load_len(p.lens, b, p.max_len, p.err);
+    const float* sc = p.scores + static_cast<size_t>(b) * p.score_stride;
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < L; t += gridDim.x * blockDim.x)
+        atomicAdd(&h[float_key(sc[t]) >> 21], 1u);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
+        if (h[i]) atomicAdd(p.hist + static_cast<size_t>(b) * kHistBins + i, h[i]);
+}
+
+// Find the bucket holding the k-th largest key, scanning buckets from the top. Returns the
+// bucket and the number of keys in higher buckets. All threads of the block take part.
+template <int NT>
+__device__ void find_bucket(const uint32_t* bins, int nbins, int k, int& bucket, int& above,
+                            int* s_tmp) {
+    // thread i owns a contiguous group of bins counted from the top
+    const int per = (nbins + NT - 1) / NT;
+    const int tid = threadIdx.x;
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+        const int r = tid * per + i;  // rank from the top
+        if (r < nbins) local += bins[nbins - 1 - r];
+    }
+    s_tmp[tid] = local;
+    __syncthreads();
+    // inclusive scan over threads (Hillis-Steele)
+    for (int off = 1; off < NT; off <<= 1) {
+        const int v = tid >= off ? s_tmp[tid - off] : 0;
+        __syncthreads();
+        s_tmp[tid] += v;
+        __syncthreads();
+    }
+    const int incl = s_tmp[tid];
+    const int excl = incl - local;
+    if (excl < k && incl >= k) {
+        int cum = excl;
+        for (int i = 0; i < per; ++i) {
+            const int r = tid * per + i;
+            if (r >= nbins) break;
+            const int c = bins[nbins - 1 - r];
+            if (cum + c >= k) {
+                s_tmp[NT] = nbins - 1 - r;
+                s_tmp[NT + 1] = cum;
+                break;
+            }
+            cum += c;
+        }
+    }
+    __syncthreads();
+    bucket = s_tmp[NT];
+    above = s_tmp[NT + 1];
+    __syncthreads();
+}
+
+// Tokens whose bucket is above the k-th's are selected; tokens inside it are candidates.
+__global__ void __launch_bounds__(256) topk_filter_kernel(const TopkParams p) {
+    __shared__ uint32_t h[kHistBins];
+    __shared__ int tmp[256 + 2];
+    const int b = blockIdx.y;
+    const int L = load_len(p.lens, b, p.max_len, nullptr);
+    if (L <= p.k) return;  // everything is selected; the finalize kernel writes it
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
+        h[i] = p.hist[static_cast<size_t>(b) * kHistBins + i];
+    __syncthreads();
+    int b1, above;
+    find_bucket<256>(h, kHistBins, p.k, b1, above, tmp);
+    const float* sc = p.scores + static_cast<size_t>(b) * p.score_stride;
+    int* sel = p.sel + static_cast<size_t>(b) * p.k;
+    int* cand = p.cand + static_cast<size_t>(b) * p.max_len;
+    const int lane = threadIdx.x % 32;
+    const int stride = gridDim.x * blockDim.x;
+    for (int base = blockIdx.x * blockDim.x; base < L; base += stride) {
+        const int t = base + threadIdx.x;
+        int bk = -1;
+        if (t < L) bk = static_cast<int>(float_key(sc[t]) >> 21);
+        // warp-aggregated appends
+        const unsigned m_sel = __ballot_sync(0xffffffffu, bk > b1);
+        const unsigned m_cand = __ballot_sync(0xffffffffu, bk == b1);
+        int sel_base = 0, cand_base = 0;
+        if (lane == 0) {
+            if (m_sel) sel_base = atomicAdd(p.counts + 2 * b, __popc(m_sel));
+            if (m_cand) cand_base = atomicAdd(p.counts + 2 * b + 1, __popc(m_cand));
+        }
+        sel_base = __shfl_sync(0xffffffffu, sel_base, 0);
+        cand_base = __shfl_sync(0xffffffffu, cand_base, 0);
+        const unsigned lower = (1u << lane) - 1u;
+        if (bk > b1) sel[sel_base + __popc(m_sel & lower)] = t;
+        if (bk == b1) cand[cand_base + __popc(m_cand & lower)] = t;
+    }
+}
+
+constexpr int kFinThreads = 1024;
+
+__device__ __forceinline__ uint64_t composite_key(float score, int t) {
+    return (static_cast<uint64_t>(float_key(score)) << 32) |
+           static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(t));
+}
+
+// One CTA per sequence: exact threshold among the candidates, then the sorted output.
+__global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkParams p) {
+    __shared__ uint32_t h[kHistBins];
+    __shared__ int tmp[kFinThreads + 2];
+    __shared__ int out_s[kTopkMaxK];
+    __shared__ int n_out;
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int L = load_len(p.lens, b, p.max_len, nullptr);
+    int32_t* idx_out = p.topk_idx + static_cast<size_t>(b) * p.k;
+    const int count = min(p.k, L);
+    if (tid == 0) p.topk_count[b] = count;
+    if (L <= p.k) {
+        for (int i = tid; i < p.k; i += kFinThreads) idx_out[i] = i < L ? i : -1;
+    } else {
+        const float* sc = p.scores + static_cast<size_t>(b) * p.score_stride;
+        const int* cand = p.cand + static_cast<size_t>(b) * p.max_len;
+        const int* sel = p.sel + static_cast<size_t>(b) * p.k;
+        for (int i = tid; i < kHistBins; i += kFinThreads)
+            h[i] = p.hist[static_cast<size_t>(b) * kHistBins + i];
+        __syncthreads();
+        int b1, above;
+        find_bucket<kFinThreads>(h, kHistBins, p.k, b1, above, tmp);
+        const int nc = p.counts[2 * b + 1];
+        int need = p.k - above;  // to take from the candidates (>= 1)
+        // radix passes over the 64-bit composite key below its top 11 bits
+        uint64_t prefix = static_cast<uint64_t>(b1);
+        int done_bits = 11;
+        while (done_bits < 64) {
+            const int wdt = min(11, 64 - done_bits);
+            const int shift = 64 - done_bits - wdt;
+            const int nb = 1 << wdt;
+            for (int i = tid; i < nb; i += kFinThreads) h[i] = 0;
+            __syncthreads();
+            for (int i = tid; i < nc; i += kFinThreads) {
+                const int t = cand[i];
+                const uint64_t ck = composite_key(sc[t], t);
+                if ((ck >> (64 - done_bits)) == prefix)
+                    atomicAdd(&h[static_cast<int>((ck >> shift) & (nb - 1))], 1u);
+            }
+            __syncthreads();
+            int bb, ab;
+            find_bucket<kFinThreads>(h, nb, need, bb, ab, tmp);
+            prefix = (prefix << wdt) | static_cast<uint64_t>(bb);
+            need -= ab;
+            done_bits += wdt;
+        }
+        const uint64_t T = prefix;  // the (k - above)-th largest candidate key
+        // gather: the selected tokens, then the candidates at or above the threshold
+        if (tid == 0) n_out = 0;
+        __syncthreads();
+        const int n_sel = p.counts[2 * b];
+        for (int i = tid; i < n_sel; i += kFinThreads) out_s[atomicAdd(&n_out, 1)] = sel[i];
+        for (int i = tid; i < nc; i += kFinThreads) {
+            const int t = cand[i];
+            if (composite_key(sc[t], t) >= T) out_s[atomicAdd(&n_out, 1)] = t;
+        }
+        __syncthreads();
+        const int n = n_out;  // == k
+        int P2 = 1;
+        while (P2 < n) P2 <<= 1;
+        for (int i = n + tid; i < P2; i += kFinThreads) out_s[i] = 0x7FFFFFFF;
+        __syncthreads();
+        // bitonic sort ascending
+        for (int size = 2; size <= P2; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = tid; i < P2; i += kFinThreads) {
+                    const int jx = i ^ stride;
+                    if (jx > i) {
+                        const bool up = (i & size) == 0;
+                        const int a = out_s[i], c = out_s[jx];
+                        if ((a > c) == up) {
+                            out_s[i] = c;
+                            out_s[jx] = a;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        for (int i = tid; i < p.k; i += kFinThreads) idx_out[i] = i < n ? out_s[i] : -1;
+    }
+    // leave the histogram and counters zeroed for the next call
+    __syncthreads();
+    for (int i = tid; i < kHistBins; i += kFinThreads)
+        p.hist[static_cast<size_t>(b) * kHistBins + i] = 0;
+    if (tid < 2) p.counts[2 * b + tid] = 0;
+}
+
+}  // namespace
+
+int idx_smem_bytes() { return kIdxSmem; }
+
+int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensorMap& tq,
+                       cudaStream_t stream) {
+    static int configured = 0;
+    if (!configured) {
+        if (cudaFuncSetAttribute(dsa_indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kIdxSmem) != cudaSuccess)
+            return KVD_ERR_CUDA;
+        configured = 1;
+    }
+    const int total = p.B * p.tiles_per_b;
+    const int grid = total < num_sms() ? total : num_sms();
+    dsa_indexer_kernel<<<grid, kIdxThreads, kIdxSmem, stream>>>(tk, tq, p);
+    return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
+}
+
+int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream) {
+    const int blocks_per_b = std::max(1, std::min(64, (p.max_len + 4095) / 4096));
+    if (need_hist) topk_hist_kernel<<<dim3(blocks_per_b, p.B), 256, 0, stream>>>(p);
+    topk_filter_kernel<<<dim3(blocks_per_b, p.B), 256, 0, stream>>>(p);
+    topk_finalize_kernel<<<p.B, kFinThreads, 0, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
+}
+
+}  // namespace kvd

@@ -60,6 +60,47 @@ int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t
 
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix with a {64, box_rows} box and
 // 128-byte swizzle (cols a multiple of 64). Returns KVD_OK or KVD_ERR_CUDA.
+// ---------------------------------------------------------------------------------------
+// DSA indexer + top-k
+// ---------------------------------------------------------------------------------------
+constexpr int kTopkMaxK = 4096;
+
+struct IdxParams {
+    const void* q;             // [B, 64, 128] bf16 (read through a tensor map)
+    const float* w;            // [B, 64]
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    float* scores;             // [B, score_stride]
+    long long score_stride;
+    uint32_t* hist;            // [B, 2048] top-11-bit key histogram
+    int* err;
+    int B, page_size, max_pages, num_pages, max_len, tiles_per_b;
+};
+
+struct TopkParams {
+    const float* scores;       // [B, score_stride]
+    long long score_stride;
+    const int32_t* lens;       // [B]
+    uint32_t* hist;            // [B, 2048]
+    int* counts;               // [B, 2]: selected, candidates
+    int* sel;                  // [B, k]
+    int* cand;                 // [B, max_len]
+    int32_t* topk_idx;         // [B, k]
+    int32_t* topk_count;       // [B]
+    int* err;
+    int B, k, max_len;
+};
+
+// Workspace layout of the DSA selection (offsets from the workspace base).
+struct TopkLayout {
+    size_t off_hist, off_counts, off_sel, off_cand, off_scores, total;
+};
+TopkLayout topk_layout(int B, int max_len, int k, bool with_scores);
+
+int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensorMap& tq,
+                       cudaStream_t stream);
+int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream);
+
 int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                       uint32_t box_rows);
 

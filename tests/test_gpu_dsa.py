@@ -1,0 +1,127 @@
+"""GPU parity of the DSA indexer and top-k selection against the fp64 oracle.
+
+* Indexer scores (fp32 on the GPU) are compared with the oracle's fp64 scores.
+* The selection step alone (dsa_topk) is bit-exact against the oracle's top-k on the same
+  seeded float32 score arrays, including arrays full of exact ties (lower position wins).
+* The full path (dsa_indexer_topk) is compared with the oracle's selection taken on its
+  own scores rounded to float32: any index in the symmetric difference must score within
+  1e-5 relative of the oracle's k-th score (a near-tie), and the sets have equal size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvd():
+    import kv_cache_decode_split_gb300 as m
+    return m
+
+
+def _check_selection(idx, cnt, ref_scores, L, k):
+    """GPU selection (ascending, -1 padded) vs the oracle's on fp32-rounded fp64 scores."""
+    idx = idx.cpu().numpy()
+    n = min(k, L)
+    assert int(cnt) == n
+    sel = idx[:n]
+    assert np.all(np.diff(sel) > 0), "not strictly ascending"
+    assert np.all(idx[n:] == -1)
+    assert sel.min() >= 0 and sel.max() < L
+    s32 = ref_scores[:L].astype(np.float32).astype(np.float64)
+    ref = oracle.topk(s32, k)
+    diff = np.setxor1d(sel, ref)
+    if diff.size:
+        kth = np.sort(s32)[::-1][n - 1]
+        tol = 1e-5 * abs(kth)
+        assert np.all(np.abs(ref_scores[diff] - kth) <= tol), (diff, ref_scores[diff], kth)
+
+
+def _run_indexer(kvd, x, k):
+    dev = "cuda"
+    scores = torch.full((x.B, x.max_pages * x.page_size), float("nan"), device=dev)
+    idx, cnt = kvd.dsa_indexer_topk(x.q.to(dev), x.k_pool.to(dev), x.w.to(dev),
+                                    x.block_table.to(dev), x.seq_lens.to(dev), k=k,
+                                    scores_out=scores)
+    torch.cuda.synchronize()
+    return idx, cnt, scores
+
+
+@pytest.mark.parametrize("P", [64, 16, 128])
+@pytest.mark.parametrize("k", [1, 16, 300])
+def test_indexer_scores_and_topk_small(kvd, P, k):
+    lens = [1, 100, 129, 1000, 2500]
+    x = W.make_indexer(len(lens), lens, k=k, page_size=P, shuffle=True, extra_pages=3,
+                       seed=500 + P + k)
+    idx, cnt, scores = _run_indexer(kvd, x, k)
+    ref = oracle.indexer_scores(x.q, x.k_pool, x.w, x.block_table, x.seq_lens)
+    sc = scores.cpu().double().numpy()
+    for b, L in enumerate(lens):
+        err = np.abs(sc[b, :L] - ref[b, :L])
+        assert err.max() <= 1e-4 * np.abs(ref[b, :L]).max() + 1e-3, err.max()
+        _check_selection(idx[b], cnt[b], ref[b], L, k)
+
+
+def test_indexer_without_scores_out(kvd):
+    x = W.make_indexer(2, [700, 3000], k=256, page_size=64, shuffle=True, seed=77)
+    dev = "cuda"
+    idx, cnt = kvd.dsa_indexer_topk(x.q.to(dev), x.k_pool.to(dev), x.w.to(dev),
+                                    x.block_table.to(dev), x.seq_lens.to(dev), k=256)
+    ref = oracle.indexer_scores(x.q, x.k_pool, x.w, x.block_table, x.seq_lens)
+    for b, L in enumerate([700, 3000]):
+        _check_selection(idx[b], cnt[b], ref[b], L, 256)
+
+
+@pytest.mark.parametrize("case", ["normal", "ties", "all_equal", "few_values", "k_ge_L"])
+def test_topk_alone_bit_exact(kvd, case):
+    B, stride = 3, 20000
+    lens = torch.tensor([20000, 7777, 3], dtype=torch.int32)
+    if case == "normal":
+        s = W.normal((B, stride), 900, 1.0, torch.float32)
+    elif case == "ties":
+        s = torch.randint(-50, 50, (B, stride), generator=torch.Generator().manual_seed(901)).float()
+    elif case == "all_equal":
+        s = torch.full((B, stride), 2.5)
+    elif case == "few_values":
+        s = torch.randint(0, 3, (B, stride), generator=torch.Generator().manual_seed(902)).float()
+    else:
+        s = W.normal((B, stride), 903, 1.0, torch.float32)
+    k = 50000 if case == "k_ge_L" else 2048
+    k = min(k, 4096)
+    if case == "k_ge_L":
+        lens = torch.tensor([4000, 10, 1], dtype=torch.int32)
+    idx, cnt = kvd.dsa_topk(s.cuda(), lens.cuda(), k=k)
+    torch.cuda.synchronize()
+    for b in range(B):
+        L = int(lens[b])
+        ref = oracle.topk(s[b, :L].numpy().astype(np.float64), k)
+        n = min(k, L)
+        assert int(cnt[b]) == n
+        got = idx[b].cpu().numpy()
+        assert np.array_equal(got[:n], ref), (case, b)
+        assert np.all(got[n:] == -1)
+
+
+def test_topk_repeat_calls(kvd):
+    s = W.normal((2, 50000), 904, 1.0, torch.float32).cuda()
+    lens = torch.tensor([50000, 40000], dtype=torch.int32).cuda()
+    a, _ = kvd.dsa_topk(s, lens, k=2048)
+    b, _ = kvd.dsa_topk(s, lens, k=2048)
+    assert torch.equal(a, b)
+
+
+def test_dsa_full_size_indexer_sampled(kvd):
+    idx_in, _ = W.build("dsa_sparse_mla")
+    x = idx_in
+    idx, cnt, scores = _run_indexer(kvd, x, x.k)
+    ref = oracle.indexer_scores(x.q, x.k_pool, x.w, x.block_table, x.seq_lens, batches=[0, 3])
+    sc = scores.cpu().double().numpy()
+    for r, b in enumerate([0, 3]):
+        L = int(x.seq_lens[b])
+        err = np.abs(sc[b, :L] - ref[r, :L])
+        assert err.max() <= 1e-4 * np.abs(ref[r, :L]).max() + 1e-3, err.max()
+        _check_selection(idx[b], cnt[b], ref[r], L, x.k)
