@@ -119,6 +119,76 @@ TopkLayout topk_layout(int B, int max_len, int k, bool with_scores) {
     return l;
 }
 
+// MLA split plan: dense units are (sequence, token chunk), about three per SM pair;
+// sparse units are (sequence, chunk of the index list), about one per SM pair.
+MlaPlan mla_plan(int B, int max_items, bool sparse) {
+    MlaPlan pl;
+    const long long clusters = std::max(1, num_sms() / 2);
+    const long long target = sparse ? clusters : 3 * clusters;
+    long long chunk = ((long long)B * max_items + target - 1) / target;
+    chunk = ((chunk + 63) / 64) * 64;
+    chunk = std::max<long long>(sparse ? 64 : 256, chunk);
+    chunk = std::min<long long>(chunk, ((max_items + 63) / 64) * 64);
+    pl.chunk = static_cast<int>(std::max(64LL, chunk));
+    pl.n_splits = cdiv(max_items, pl.chunk);
+    const size_t units = (size_t)B * pl.n_splits;
+    size_t off = kWsHeaderBytes;
+    pl.off_lse = off;
+    off = round256(off + sizeof(float) * units * 128);
+    pl.off_o = off;
+    off = round256(off + sizeof(float) * units * 128 * 512);
+    pl.total = off;
+    return pl;
+}
+
+int mla_run(const void* q, const void* c_pool, const int32_t* block_table,
+            const int32_t* seq_lens, const int32_t* idx, const int32_t* idx_count, int k,
+            void* out, float* lse_out, int B, int H, int d_qk, int d_v, int page_size,
+            int max_pages, int num_pages, float scale, void* ws, size_t ws_bytes,
+            cudaStream_t stream) {
+    if (!q || !c_pool || !block_table || !seq_lens || !out || !ws) return KVD_ERR_INVALID_ARG;
+    if (B < 1 || max_pages < 1 || num_pages < 1 || !std::isfinite(scale))
+        return KVD_ERR_INVALID_ARG;
+    if (H != 128 || d_qk != 576 || d_v != 512) return KVD_ERR_UNSUPPORTED;
+    if (!pow2(page_size) || page_size < 16 || page_size > 256) return KVD_ERR_UNSUPPORTED;
+    if ((long long)num_pages * page_size >= (1LL << 31) || (long long)B * 128 >= (1LL << 31))
+        return KVD_ERR_UNSUPPORTED;
+    if ((long long)max_pages * page_size >= (1LL << 30)) return KVD_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(c_pool) || !aligned16(out) || !aligned16(ws))
+        return KVD_ERR_INVALID_ARG;
+    const bool sparse = idx != nullptr;
+    const int max_len = max_pages * page_size;
+    const MlaPlan pl = mla_plan(B, sparse ? k : max_len, sparse);
+    if (ws_bytes < pl.total) return KVD_ERR_WORKSPACE_TOO_SMALL;
+    uint8_t* wb = static_cast<uint8_t*>(ws);
+    MlaParams p;
+    std::memset(&p, 0, sizeof p);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.idx = idx;
+    p.idx_count = idx_count;
+    p.c_pool = c_pool;
+    p.part_o = reinterpret_cast<float*>(wb + pl.off_o);
+    p.part_lse = reinterpret_cast<float*>(wb + pl.off_lse);
+    p.err = reinterpret_cast<int*>(wb);
+    p.B = B;
+    p.page_size = page_size;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    p.max_len = max_len;
+    p.chunk = pl.chunk;
+    p.n_splits = pl.n_splits;
+    p.idx_stride = k;
+    p.sparse = sparse ? 1 : 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    CUtensorMap tc, tq;
+    if (make_tmap_bf16_2d(&tc, c_pool, (uint64_t)num_pages * page_size, 576,
+                          page_size < 64 ? page_size : 64) != KVD_OK)
+        return KVD_ERR_CUDA;
+    if (make_tmap_bf16_2d(&tq, q, (uint64_t)B * 128, 576, 128) != KVD_OK) return KVD_ERR_CUDA;
+    return mla_launch(p, tc, tq, out, lse_out, stream);
+}
+
 }  // namespace kvd
 
 using namespace kvd;
@@ -218,9 +288,12 @@ int attn_decode_swa_sink(const void* q, const void* k_pool, const void* v_pool,
                       sink_logit, ws, ws_bytes, stream);
 }
 
-int attn_decode_mla(const void*, const void*, const int32_t*, const int32_t*, void*, float*, int,
-                    int, int, int, int, int, int, float, void*, size_t, cudaStream_t) {
-    return KVD_ERR_UNSUPPORTED;
+int attn_decode_mla(const void* q, const void* c_pool, const int32_t* block_table,
+                    const int32_t* seq_lens, void* out, float* lse_out, int B, int H, int d_qk,
+                    int d_v, int page_size, int max_pages, int num_pages, float scale, void* ws,
+                    size_t ws_bytes, cudaStream_t stream) {
+    return mla_run(q, c_pool, block_table, seq_lens, nullptr, nullptr, 0, out, lse_out, B, H,
+                   d_qk, d_v, page_size, max_pages, num_pages, scale, ws, ws_bytes, stream);
 }
 
 int dsa_indexer_topk(const void* q_idx, const void* k_idx_pool, const float* w,
@@ -312,10 +385,15 @@ int dsa_topk(const float* scores, const int32_t* lens, int32_t* topk_idx, int32_
     return topk_launch(tp, true, stream);
 }
 
-int attn_decode_mla_sparse(const void*, const void*, const int32_t*, const int32_t*,
-                           const int32_t*, const int32_t*, void*, float*, int, int, int, int, int,
-                           int, int, int, float, void*, size_t, cudaStream_t) {
-    return KVD_ERR_UNSUPPORTED;
+int attn_decode_mla_sparse(const void* q, const void* c_pool, const int32_t* block_table,
+                           const int32_t* seq_lens, const int32_t* topk_idx,
+                           const int32_t* topk_count, void* out, float* lse_out, int B, int H,
+                           int d_qk, int d_v, int k, int page_size, int max_pages, int num_pages,
+                           float scale, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!topk_idx || !topk_count) return KVD_ERR_INVALID_ARG;
+    if (k < 1) return KVD_ERR_INVALID_ARG;
+    return mla_run(q, c_pool, block_table, seq_lens, topk_idx, topk_count, k, out, lse_out, B, H,
+                   d_qk, d_v, page_size, max_pages, num_pages, scale, ws, ws_bytes, stream);
 }
 
 size_t kvd_workspace_size(int op, int B, int H, int Hkv, int D, int max_len, int window,
@@ -325,6 +403,8 @@ size_t kvd_workspace_size(int op, int B, int H, int Hkv, int D, int max_len, int
         if (k < 1 || k > kTopkMaxK) return 0;
         return topk_layout(B, max_len, k, true).total;
     }
+    if (op == KVD_OP_MLA) return mla_plan(B, max_len, false).total;
+    if (op == KVD_OP_MLA_SPARSE) return k >= 1 ? mla_plan(B, k, true).total : 0;
     if (op == KVD_OP_GQA || op == KVD_OP_SWA) {
         if (Hkv < 1 || H % Hkv != 0 || (D != 64 && D != 128)) return 0;
         // the plan's chunk length is smallest (most partials) for 16-token pages

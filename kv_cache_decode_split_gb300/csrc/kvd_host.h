@@ -101,6 +101,36 @@ int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensor
                        cudaStream_t stream);
 int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream);
 
+// ---------------------------------------------------------------------------------------
+// MLA (absorbed latent), dense or over selected tokens
+// ---------------------------------------------------------------------------------------
+struct MlaParams {
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const int32_t* idx;        // sparse: [B, idx_stride] logical positions
+    const int32_t* idx_count;  // sparse: [B]
+    const void* c_pool;        // [num_pages, P, 576] bf16 (gathered rows, sparse)
+    float* part_o;             // [B * n_splits, 128, 512]
+    float* part_lse;           // [B * n_splits, 128] (log2 domain)
+    int* err;
+    int B, page_size, max_pages, num_pages, max_len;
+    int chunk, n_splits, idx_stride, sparse;
+    float scale_log2;
+};
+
+struct MlaPlan {
+    int chunk, n_splits;
+    size_t off_lse, off_o, total;
+};
+MlaPlan mla_plan(int B, int max_items, bool sparse);
+int mla_run(const void* q, const void* c_pool, const int32_t* block_table,
+            const int32_t* seq_lens, const int32_t* idx, const int32_t* idx_count, int k,
+            void* out, float* lse_out, int B, int H, int d_qk, int d_v, int page_size,
+            int max_pages, int num_pages, float scale, void* ws, size_t ws_bytes,
+            cudaStream_t stream);
+int mla_launch(const MlaParams& p, const CUtensorMap& tc, const CUtensorMap& tq, void* out,
+               float* lse_out, cudaStream_t stream);
+
 int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                       uint32_t box_rows);
 
