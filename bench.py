@@ -146,7 +146,152 @@ class GqaRunner:
         return done_bytes, el, f"{n} of {len(units)} (sequence, KV head) groups, all {G} query heads each"
 
 
-RUNNERS = {"gqa": GqaRunner, "swa": GqaRunner}
+class MlaRunner:
+    """attn_decode_mla on the DeepSeek-V3-shaped workload (128 heads, 576-wide rows)."""
+    launches_per_step = 2          # split kernel (2-CTA clusters) + combine kernel
+    kernel = "mla_decode_kernel"
+
+    def __init__(self, name, dev, sharp=False):
+        import kv_cache_decode_split_gb300 as kvd
+        self.kvd = kvd
+        self.name = name
+        self.x = x = W.build(name, sharp=sharp)
+        self.dev = dev
+        self.q = x.q.to(dev)
+        self.c = x.c_pool.to(dev)
+        self.bt = x.block_table.to(dev)
+        self.sl = x.seq_lens.to(dev)
+        self.out = torch.empty(x.B, x.H, 512, dtype=torch.bfloat16, device=dev)
+        self.ws = kvd.Workspace(dev)
+        tok = int(x.seq_lens.sum())
+        self.bytes = tok * x.d_qk * 2
+        self.flops = 2.0 * tok * x.H * (x.d_qk + 512)
+
+    def step(self, q=None):
+        x = self.x
+        return self.kvd.attn_decode_mla(self.q if q is None else q, self.c, self.bt, self.sl,
+                                        scale=x.scale, out=self.out, workspace=self.ws)
+
+    def config(self):
+        x = self.x
+        return {"workload": self.name, "B": x.B, "H": x.H, "d_qk": x.d_qk, "d_v": 512,
+                "page_size": x.page_size, "seq_len_mean": float(x.seq_lens.float().mean()),
+                "kv_bytes": self.bytes, "flops": self.flops}
+
+    def e2e_setup(self):
+        self.h_q = self.x.q.pin_memory()
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.d_q = torch.empty_like(self.q)
+        return self.h_q.numel() * 2, self.h_out.numel() * 2
+
+    def e2e_step(self):
+        self.d_q.copy_(self.h_q, non_blocking=True)
+        self.step(q=self.d_q)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def oracle_sample(self, budget_s):
+        import oracle
+        x = self.x
+        t0 = time.perf_counter()
+        done, n = 0, 0
+        for b in range(x.B):
+            for h0 in range(0, x.H, 16):
+                pairs = [(b, h) for h in range(h0, h0 + 16)]
+                oracle.mla(x.q, x.c_pool, x.block_table, x.seq_lens, x.scale, pairs=pairs)
+                done += int(x.seq_lens[b]) * x.d_qk * 2 * 16 / x.H
+                n += 16
+                if time.perf_counter() - t0 > budget_s:
+                    break
+            if time.perf_counter() - t0 > budget_s:
+                break
+        el = time.perf_counter() - t0
+        return done, el, f"{n} of {x.B * x.H} (sequence, head) outputs, bytes counted pro rata"
+
+
+class DsaRunner:
+    """dsa_indexer_topk then attn_decode_mla_sparse (indexer, top-2048, sparse MLA)."""
+    launches_per_step = 5          # indexer, filter, finalize, sparse MLA, combine
+    kernel = "dsa_indexer_kernel"
+
+    def __init__(self, name, dev, sharp=False):
+        import kv_cache_decode_split_gb300 as kvd
+        self.kvd = kvd
+        self.name = name
+        self.xi, self.xm = xi, xm = W.build(name, sharp=sharp)
+        self.dev = dev
+        self.qi = xi.q.to(dev)
+        self.ki = xi.k_pool.to(dev)
+        self.w = xi.w.to(dev)
+        self.q = xm.q.to(dev)
+        self.c = xm.c_pool.to(dev)
+        self.bt = xm.block_table.to(dev)
+        self.sl = xm.seq_lens.to(dev)
+        self.k = xi.k
+        self.idx = torch.empty(xi.B, xi.k, dtype=torch.int32, device=dev)
+        self.cnt = torch.empty(xi.B, dtype=torch.int32, device=dev)
+        self.out = torch.empty(xm.B, xm.H, 512, dtype=torch.bfloat16, device=dev)
+        self.ws1 = kvd.Workspace(dev)
+        self.ws2 = kvd.Workspace(dev)
+        lens = [int(v) for v in xm.seq_lens]
+        sel = sum(min(self.k, L) for L in lens)
+        self.bytes = sum(lens) * xi.Di * 2 + sel * xm.d_qk * 2
+        self.flops = 2.0 * sum(lens) * xi.Hi * xi.Di + 2.0 * sel * xm.H * (xm.d_qk + 512)
+
+    def step(self, qi=None, q=None):
+        xm = self.xm
+        self.kvd.dsa_indexer_topk(self.qi if qi is None else qi, self.ki, self.w, self.bt,
+                                  self.sl, k=self.k, topk_idx=self.idx, topk_count=self.cnt,
+                                  workspace=self.ws1)
+        return self.kvd.attn_decode_mla_sparse(self.q if q is None else q, self.c, self.bt,
+                                               self.sl, self.idx, self.cnt, scale=xm.scale,
+                                               out=self.out, workspace=self.ws2)
+
+    def config(self):
+        xi, xm = self.xi, self.xm
+        return {"workload": self.name, "B": xm.B, "H": xm.H, "Hi": xi.Hi, "Di": xi.Di,
+                "k": self.k, "seq_len": int(xm.seq_lens[0]), "page_size": xm.page_size,
+                "kv_bytes": self.bytes, "flops": self.flops}
+
+    def e2e_setup(self):
+        self.h_qi = self.xi.q.pin_memory()
+        self.h_q = self.xm.q.pin_memory()
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.d_qi = torch.empty_like(self.qi)
+        self.d_q = torch.empty_like(self.q)
+        return (self.h_qi.numel() + self.h_q.numel()) * 2, self.h_out.numel() * 2
+
+    def e2e_step(self):
+        self.d_qi.copy_(self.h_qi, non_blocking=True)
+        self.d_q.copy_(self.h_q, non_blocking=True)
+        self.step(qi=self.d_qi, q=self.d_q)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def oracle_sample(self, budget_s):
+        import numpy as np
+        import oracle
+        xi, xm = self.xi, self.xm
+        t0 = time.perf_counter()
+        done, n = 0, 0
+        for b in range(xm.B):
+            sc = oracle.indexer_scores(xi.q, xi.k_pool, xi.w, xi.block_table, xi.seq_lens,
+                                       batches=[b])[0]
+            L = int(xm.seq_lens[b])
+            idx = oracle.topk(sc[:L].astype(np.float32), self.k)
+            full = np.full((xm.B, self.k), -1, np.int32)
+            full[b, :len(idx)] = idx
+            cnt = np.zeros(xm.B, np.int32)
+            cnt[b] = len(idx)
+            oracle.mla(xm.q, xm.c_pool, xm.block_table, xm.seq_lens, xm.scale, idx=full,
+                       idx_count=cnt, pairs=[(b, h) for h in range(xm.H)])
+            done += L * xi.Di * 2 + len(idx) * xm.d_qk * 2
+            n += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        el = time.perf_counter() - t0
+        return done, el, f"{n} of {xm.B} sequences (indexer, top-k and sparse MLA, all heads)"
+
+
+RUNNERS = {"gqa": GqaRunner, "swa": GqaRunner, "mla": MlaRunner, "dsa": DsaRunner}
 
 
 def make_runner(name, dev):
@@ -243,14 +388,27 @@ def time_flushed(fn, iters, stream, flush):
 
 
 # ---------------------------------------------------------------------------------------
+def oracle_runner(name):
+    """A runner holding only the CPU inputs of a workload, for timing the oracle."""
+    cls = RUNNERS[W.WORKLOADS[name].kind]
+    r = cls.__new__(cls)
+    r.name = name
+    if cls is DsaRunner:
+        r.xi, r.xm = W.build(name)
+        r.k = r.xi.k
+    else:
+        r.x = x = W.build(name)
+        if cls is GqaRunner:
+            r.swa = x.window > 0 or x.n_sink > 0 or x.sink_logit is not None
+    return r
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
     name = args.workload
     wl = W.WORKLOADS[name]
-    x_runner = GqaRunner.__new__(GqaRunner)
-    x_runner.x = x = W.build(name)
-    x_runner.swa = x.window > 0 or x.n_sink > 0 or x.sink_logit is not None
+    x_runner = oracle_runner(name)
     per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
     vals = []
     desc = ""
@@ -383,9 +541,7 @@ def main():
         line["workloads"] = res
 
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        rr = GqaRunner.__new__(GqaRunner)
-        rr.x = W.build(args.workload)
-        rr.swa = False
+        rr = oracle_runner(args.workload)
         nbytes, el, desc = rr.oracle_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": nbytes / el / 1e9, "unit": "GB/s",
                                 "cores": os.cpu_count(), "kind": "oracle",
