@@ -113,6 +113,8 @@ TopkLayout topk_layout(int B, int max_len, int k, bool with_scores) {
     off = round256(off + sizeof(int) * (size_t)B * k);
     l.off_cand = off;
     off = round256(off + sizeof(int) * (size_t)B * max_len);
+    l.off_bitmap = off;
+    off = round256(off + sizeof(uint32_t) * (size_t)B * ((max_len + 31) / 32));
     l.off_scores = off;
     if (with_scores) off = round256(off + sizeof(float) * (size_t)B * max_len);
     l.total = off;
@@ -349,6 +351,7 @@ int dsa_indexer_topk(const void* q_idx, const void* k_idx_pool, const float* w,
     tp.counts = reinterpret_cast<int*>(wb + lay.off_counts);
     tp.sel = reinterpret_cast<int*>(wb + lay.off_sel);
     tp.cand = reinterpret_cast<int*>(wb + lay.off_cand);
+    tp.bitmap = reinterpret_cast<uint32_t*>(wb + lay.off_bitmap);
     tp.topk_idx = topk_idx;
     tp.topk_count = topk_count;
     tp.err = ip.err;
@@ -376,6 +379,7 @@ int dsa_topk(const float* scores, const int32_t* lens, int32_t* topk_idx, int32_
     tp.counts = reinterpret_cast<int*>(wb + lay.off_counts);
     tp.sel = reinterpret_cast<int*>(wb + lay.off_sel);
     tp.cand = reinterpret_cast<int*>(wb + lay.off_cand);
+    tp.bitmap = reinterpret_cast<uint32_t*>(wb + lay.off_bitmap);
     tp.topk_idx = topk_idx;
     tp.topk_count = topk_count;
     tp.err = reinterpret_cast<int*>(wb);

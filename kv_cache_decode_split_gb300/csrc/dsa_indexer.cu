@@ -255,29 +255,46 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const TopkParams p) {
         if (h[i]) atomicAdd(p.hist + static_cast<size_t>(b) * kHistBins + i, h[i]);
 }
 
+// Block-wide inclusive scan of one int per thread (warp shuffles, then the warp totals).
+template <int NT>
+__device__ __forceinline__ int block_incl_scan(int v, int* s_warp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += n;
+    }
+    if (lane == 31) s_warp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < NT / 32 ? s_warp[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, t, off);
+            if (lane >= off) t += n;
+        }
+        if (lane < NT / 32) s_warp[lane] = t;
+    }
+    __syncthreads();
+    const int r = v + (warp > 0 ? s_warp[warp - 1] : 0);
+    __syncthreads();
+    return r;
+}
+
 // Find the bucket holding the k-th largest key, scanning buckets from the top. Returns the
-// bucket and the number of keys in higher buckets. All threads of the block take part.
+// bucket, the number of keys in higher buckets and the bucket's own count. All threads of
+// the block take part; s_tmp holds at least NT/32 + 3 ints.
 template <int NT>
 __device__ void find_bucket(const uint32_t* bins, int nbins, int k, int& bucket, int& above,
-                            int* s_tmp) {
-    // thread i owns a contiguous group of bins counted from the top
-    const int per = (nbins + NT - 1) / NT;
+                            int& in_bucket, int* s_tmp) {
+    const int per = (nbins + NT - 1) / NT;  // each thread owns `per` bins counted from the top
     const int tid = threadIdx.x;
     int local = 0;
     for (int i = 0; i < per; ++i) {
-        const int r = tid * per + i;  // rank from the top
+        const int r = tid * per + i;
         if (r < nbins) local += bins[nbins - 1 - r];
     }
-    s_tmp[tid] = local;
-    __syncthreads();
-    // inclusive scan over threads (Hillis-Steele)
-    for (int off = 1; off < NT; off <<= 1) {
-        const int v = tid >= off ? s_tmp[tid - off] : 0;
-        __syncthreads();
-        s_tmp[tid] += v;
-        __syncthreads();
-    }
-    const int incl = s_tmp[tid];
+    const int incl = block_incl_scan<NT>(local, s_tmp);
     const int excl = incl - local;
     if (excl < k && incl >= k) {
         int cum = excl;
@@ -286,31 +303,33 @@ __device__ void find_bucket(const uint32_t* bins, int nbins, int k, int& bucket,
             if (r >= nbins) break;
             const int c = bins[nbins - 1 - r];
             if (cum + c >= k) {
-                s_tmp[NT] = nbins - 1 - r;
-                s_tmp[NT + 1] = cum;
+                s_tmp[NT / 32] = nbins - 1 - r;
+                s_tmp[NT / 32 + 1] = cum;
+                s_tmp[NT / 32 + 2] = c;
                 break;
             }
             cum += c;
         }
     }
     __syncthreads();
-    bucket = s_tmp[NT];
-    above = s_tmp[NT + 1];
+    bucket = s_tmp[NT / 32];
+    above = s_tmp[NT / 32 + 1];
+    in_bucket = s_tmp[NT / 32 + 2];
     __syncthreads();
 }
 
 // Tokens whose bucket is above the k-th's are selected; tokens inside it are candidates.
 __global__ void __launch_bounds__(256) topk_filter_kernel(const TopkParams p) {
     __shared__ uint32_t h[kHistBins];
-    __shared__ int tmp[256 + 2];
+    __shared__ int tmp[256 / 32 + 3];
     const int b = blockIdx.y;
     const int L = load_len(p.lens, b, p.max_len, nullptr);
     if (L <= p.k) return;  // everything is selected; the finalize kernel writes it
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
         h[i] = p.hist[static_cast<size_t>(b) * kHistBins + i];
     __syncthreads();
-    int b1, above;
-    find_bucket<256>(h, kHistBins, p.k, b1, above, tmp);
+    int b1, above, in_b1;
+    find_bucket<256>(h, kHistBins, p.k, b1, above, in_b1, tmp);
     const float* sc = p.scores + static_cast<size_t>(b) * p.score_stride;
     int* sel = p.sel + static_cast<size_t>(b) * p.k;
     int* cand = p.cand + static_cast<size_t>(b) * p.max_len;
@@ -343,12 +362,11 @@ __device__ __forceinline__ uint64_t composite_key(float score, int t) {
            static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(t));
 }
 
-// One CTA per sequence: exact threshold among the candidates, then the sorted output.
+// One CTA per sequence: exact threshold among the candidates, then the output in
+// ascending position order from a bitmap of the chosen positions and a prefix scan.
 __global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkParams p) {
     __shared__ uint32_t h[kHistBins];
-    __shared__ int tmp[kFinThreads + 2];
-    __shared__ int out_s[kTopkMaxK];
-    __shared__ int n_out;
+    __shared__ int tmp[kFinThreads / 32 + 3];
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
     const int L = load_len(p.lens, b, p.max_len, nullptr);
@@ -361,17 +379,20 @@ __global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkPa
         const float* sc = p.scores + static_cast<size_t>(b) * p.score_stride;
         const int* cand = p.cand + static_cast<size_t>(b) * p.max_len;
         const int* sel = p.sel + static_cast<size_t>(b) * p.k;
+        const int n_words = (L + 31) / 32;
+        uint32_t* bits = p.bitmap + static_cast<size_t>(b) * ((p.max_len + 31) / 32);
         for (int i = tid; i < kHistBins; i += kFinThreads)
             h[i] = p.hist[static_cast<size_t>(b) * kHistBins + i];
         __syncthreads();
-        int b1, above;
-        find_bucket<kFinThreads>(h, kHistBins, p.k, b1, above, tmp);
+        int b1, above, in_b;
+        find_bucket<kFinThreads>(h, kHistBins, p.k, b1, above, in_b, tmp);
         const int nc = p.counts[2 * b + 1];
         int need = p.k - above;  // to take from the candidates (>= 1)
-        // radix passes over the 64-bit composite key below its top 11 bits
+        // radix passes over the 64-bit composite key below its top 11 bits, until the
+        // bucket that holds the threshold holds exactly the keys still needed
         uint64_t prefix = static_cast<uint64_t>(b1);
         int done_bits = 11;
-        while (done_bits < 64) {
+        while (done_bits < 64 && in_b != need) {
             const int wdt = min(11, 64 - done_bits);
             const int shift = 64 - done_bits - wdt;
             const int nb = 1 << wdt;
@@ -385,45 +406,41 @@ __global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkPa
             }
             __syncthreads();
             int bb, ab;
-            find_bucket<kFinThreads>(h, nb, need, bb, ab, tmp);
+            find_bucket<kFinThreads>(h, nb, need, bb, ab, in_b, tmp);
             prefix = (prefix << wdt) | static_cast<uint64_t>(bb);
             need -= ab;
             done_bits += wdt;
         }
-        const uint64_t T = prefix;  // the (k - above)-th largest candidate key
-        // gather: the selected tokens, then the candidates at or above the threshold
-        if (tid == 0) n_out = 0;
-        __syncthreads();
-        const int n_sel = p.counts[2 * b];
-        for (int i = tid; i < n_sel; i += kFinThreads) out_s[atomicAdd(&n_out, 1)] = sel[i];
+        // every key at or above T is chosen (T: the threshold prefix, low bits zero)
+        const uint64_t T = done_bits < 64 ? prefix << (64 - done_bits) : prefix;
+        for (int i = tid; i < above; i += kFinThreads) {
+            const int t = sel[i];
+            atomicOr(bits + (t >> 5), 1u << (t & 31));
+        }
         for (int i = tid; i < nc; i += kFinThreads) {
             const int t = cand[i];
-            if (composite_key(sc[t], t) >= T) out_s[atomicAdd(&n_out, 1)] = t;
+            if (composite_key(sc[t], t) >= T) atomicOr(bits + (t >> 5), 1u << (t & 31));
         }
+        __threadfence();  // the bit updates land in L2 before the words are read back
         __syncthreads();
-        const int n = n_out;  // == k
-        int P2 = 1;
-        while (P2 < n) P2 <<= 1;
-        for (int i = n + tid; i < P2; i += kFinThreads) out_s[i] = 0x7FFFFFFF;
-        __syncthreads();
-        // bitonic sort ascending
-        for (int size = 2; size <= P2; size <<= 1) {
-            for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                for (int i = tid; i < P2; i += kFinThreads) {
-                    const int jx = i ^ stride;
-                    if (jx > i) {
-                        const bool up = (i & size) == 0;
-                        const int a = out_s[i], c = out_s[jx];
-                        if ((a > c) == up) {
-                            out_s[i] = c;
-                            out_s[jx] = a;
-                        }
-                    }
-                }
-                __syncthreads();
+        // positions in ascending order: popcount prefix scan over the bitmap words
+        const int per = (n_words + kFinThreads - 1) / kFinThreads;
+        const int w0 = tid * per;
+        int local = 0;
+        for (int i = 0; i < per; ++i)
+            if (w0 + i < n_words) local += __popc(__ldcg(bits + w0 + i));
+        int pos = block_incl_scan<kFinThreads>(local, tmp) - local;
+        for (int i = 0; i < per; ++i) {
+            if (w0 + i >= n_words) break;
+            uint32_t w = __ldcg(bits + w0 + i);
+            bits[w0 + i] = 0;  // leave the bitmap clear for the next call
+            while (w) {
+                const int bit = __ffs(w) - 1;
+                if (pos < p.k) idx_out[pos] = (w0 + i) * 32 + bit;
+                ++pos;
+                w &= w - 1;
             }
         }
-        for (int i = tid; i < p.k; i += kFinThreads) idx_out[i] = i < n ? out_s[i] : -1;
     }
     // leave the histogram and counters zeroed for the next call
     __syncthreads();

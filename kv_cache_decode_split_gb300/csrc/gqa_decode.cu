@@ -99,12 +99,10 @@ __device__ void merge_chunk(const GqaParams& p, MergeSmem<D, HP>& ms, const Item
 // Combine the chunk partials of one (sequence, KV head, head block) with log-sum-exp
 // weights, the learned sink added once to the denominator:
 //   o = sum_c 2^{lse_c - M} o_c / (sum_c 2^{lse_c - M} + 2^{sigma - M}).
-// One CTA per unit, one warp per query head, lanes over the head dimension.
+// One CTA per unit; each thread owns four dims of one query head and streams every chunk.
 template <int D>
-__global__ void __launch_bounds__(128) gqa_combine_kernel(const GqaParams p) {
-    constexpr int J = D / 32;
+__global__ void __launch_bounds__(256) gqa_combine_kernel(const GqaParams p) {
     const int unit = blockIdx.x;
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (unit == 0 && threadIdx.x == 0) p.counters[p.units] = 0;  // work queue, next call
     const Item it = decode_item(p, unit * p.max_chunks);
     const int L = load_len(p.seq_lens, it.b, p.max_len, nullptr);
@@ -112,35 +110,38 @@ __global__ void __launch_bounds__(128) gqa_combine_kernel(const GqaParams p) {
     const int G_cta = min(kMaxHP, p.G - it.hg * kMaxHP);
     const float* uo = p.part_o + static_cast<size_t>(unit) * p.max_chunks * kMaxHP * D;
     const float* ul = p.part_lse + static_cast<size_t>(unit) * p.max_chunks * kMaxHP;
-    for (int h = warp; h < G_cta; h += 4) {
+    for (int idx = threadIdx.x; idx < G_cta * (D / 4); idx += blockDim.x) {
+        const int h = idx / (D / 4), d = (idx % (D / 4)) * 4;
         const int hq = it.kvh * p.G + it.hg * kMaxHP + h;
         float M = neg_inf();
-        for (int c = lane; c < n_chunks; c += 32) M = fmaxf(M, ul[c * kMaxHP + h]);
-        for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, ul[c * kMaxHP + h]);
         const float sig = p.sink_logit ? p.sink_logit[hq] * kLog2e : neg_inf();
         M = fmaxf(M, sig);
         float den = p.sink_logit ? fast_exp2(sig - M) : 0.f;
-        float acc[J];
-#pragma unroll
-        for (int j = 0; j < J; ++j) acc[j] = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
         for (int c = 0; c < n_chunks; ++c) {
             const float w = fast_exp2(ul[c * kMaxHP + h] - M);
             den += w;
-            const float* oc = uo + (static_cast<size_t>(c) * kMaxHP + h) * D;
-#pragma unroll
-            for (int j = 0; j < J; ++j) acc[j] += w * oc[lane + 32 * j];
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                uo + (static_cast<size_t>(c) * kMaxHP + h) * D + d));
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
         }
         const float inv = 1.f / den;
-        const size_t o_base = (static_cast<size_t>(it.b) * p.Hq + hq) * D;
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const float v = acc[j] * inv;
-            if (p.dtype == KVD_BF16)
-                reinterpret_cast<__nv_bfloat16*>(p.out)[o_base + lane + 32 * j] = __float2bfloat16_rn(v);
-            else
-                reinterpret_cast<float*>(p.out)[o_base + lane + 32 * j] = v;
+        const size_t o = (static_cast<size_t>(it.b) * p.Hq + hq) * D + d;
+        if (p.dtype == KVD_BF16) {
+            __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+            __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o) =
+                make_uint2(*reinterpret_cast<uint32_t*>(&lo2), *reinterpret_cast<uint32_t*>(&hi2));
+        } else {
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         }
-        if (lane == 0 && p.lse_out)
+        if (d == 0 && p.lse_out)
             p.lse_out[static_cast<size_t>(it.b) * p.Hq + hq] = (M + log2f(den)) * kLn2;
     }
 }
@@ -625,7 +626,7 @@ int launch_bf16(const GqaPlan& plan, const GqaParams& p, const CUtensorMap& tk,
     const int ctas = num_sms();
     const int grid = items < ctas ? items : ctas;
     kern<<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(tk, tv, p);
-    gqa_combine_kernel<D><<<plan.units, 128, 0, stream>>>(p);
+    gqa_combine_kernel<D><<<plan.units, 256, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
 
@@ -639,7 +640,7 @@ int launch_f32(const GqaPlan& plan, const GqaParams& p, cudaStream_t stream) {
         configured = 1;
     }
     kern<<<plan.units * plan.max_chunks, kConsumers * 32, bytes, stream>>>(p);
-    gqa_combine_kernel<D><<<plan.units, 128, 0, stream>>>(p);
+    gqa_combine_kernel<D><<<plan.units, 256, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
 

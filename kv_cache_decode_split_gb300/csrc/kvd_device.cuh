@@ -371,6 +371,17 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                  : "memory");
 }
 
+// Asynchronous 16-byte store into another CTA's shared memory that counts its bytes on
+// that CTA's mbarrier (transaction count): no fence on the sending side.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c,
+                                            float d, uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(remote_addr),
+        "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+        : "memory");
+}
+
 // Arrive on an mbarrier of another CTA of the cluster, ordering this thread's earlier
 // shared-memory writes (local or remote) before it.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {

@@ -85,6 +85,7 @@ struct TopkParams {
     int* counts;               // [B, 2]: selected, candidates
     int* sel;                  // [B, k]
     int* cand;                 // [B, max_len]
+    uint32_t* bitmap;          // [B, ceil(max_len / 32)] chosen positions (kept zero)
     int32_t* topk_idx;         // [B, k]
     int32_t* topk_count;       // [B]
     int* err;
@@ -93,7 +94,7 @@ struct TopkParams {
 
 // Workspace layout of the DSA selection (offsets from the workspace base).
 struct TopkLayout {
-    size_t off_hist, off_counts, off_sel, off_cand, off_scores, total;
+    size_t off_hist, off_counts, off_sel, off_cand, off_bitmap, off_scores, total;
 };
 TopkLayout topk_layout(int B, int max_len, int k, bool with_scores);
 

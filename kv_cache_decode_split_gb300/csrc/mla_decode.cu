@@ -92,8 +92,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(&sm.pfull[i], 4);
             mbar_init(&sm.pvdone[i], 1);
         }
-        mbar_init(&sm.xfull, kH);
-        mbar_init(&sm.peer_free, kH);
+        mbar_init(&sm.xfull, 1);      // armed with the exchanged byte count each tile
+        mbar_init(&sm.peer_free, 4);  // one arrive per softmax warp of the partner
         mbar_init(&sm.ofinal, 1);
         fence_mbar_init();
     }
@@ -256,13 +256,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.sempty[buf]);
-            // exchange partial scores with the partner CTA
+            // exchange partial scores with the partner CTA: asynchronous remote stores whose
+            // bytes complete the partner's barrier, so the sender needs no fence
+            if (h == 0) mbar_arrive_expect_tx(&sm.xfull, kH * kTok * 4);
             if (!(ok = mbar_wait_cluster(&sm.peer_free, (i & 1) ^ 1, p.err))) break;
 #pragma unroll
             for (int c4 = 0; c4 < kTok / 4; ++c4)
-                st_cluster_v4(peer_x + ((c4 ^ (h & 15)) << 4), s[4 * c4], s[4 * c4 + 1],
-                              s[4 * c4 + 2], s[4 * c4 + 3]);
-            mbar_arrive_remote(peer_xfull);
+                st_async_v4(peer_x + ((c4 ^ (h & 15)) << 4), s[4 * c4], s[4 * c4 + 1],
+                            s[4 * c4 + 2], s[4 * c4 + 3], peer_xfull);
             if (!(ok = mbar_wait_cluster(&sm.xfull, i & 1, p.err))) break;
 #pragma unroll
             for (int c4 = 0; c4 < kTok / 4; ++c4) {
@@ -272,7 +273,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 s[4 * c4 + 2] += v.z;
                 s[4 * c4 + 3] += v.w;
             }
-            mbar_arrive_remote(peer_free);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(peer_free);  // this warp's rows were read
             // online softmax in log2 units, lazily rescaled
             const int T0 = lo + i * kTok;
             float mt = neg_inf();
@@ -359,34 +361,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // Merge the splits of each (sequence, head): o = sum_s 2^{lse_s - M} o_s / sum_s 2^{lse_s - M}.
-__global__ void __launch_bounds__(128) mla_combine_kernel(const MlaParams p, __nv_bfloat16* out,
+// Two heads per block; each thread owns four value dims and streams every split.
+__global__ void __launch_bounds__(256) mla_combine_kernel(const MlaParams p, __nv_bfloat16* out,
                                                           float* lse_out) {
-    const int b = blockIdx.x / (kH / 4);
-    const int h = (blockIdx.x % (kH / 4)) * 4 + threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
+    const int b = blockIdx.x / (kH / 2);
+    const int h = (blockIdx.x % (kH / 2)) * 2 + threadIdx.x / 128;
+    const int d = (threadIdx.x % 128) * 4;
     const int L = load_len(p.seq_lens, b, p.max_len, nullptr);
     const int n_items = p.sparse ? min(max(p.idx_count[b], 0), p.idx_stride) : L;
     const int ns = min(p.n_splits, (n_items + p.chunk - 1) / p.chunk);
     const size_t u0 = static_cast<size_t>(b) * p.n_splits;
+    const float* lse = p.part_lse + u0 * kH + h;
     float M = neg_inf();
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, p.part_lse[(u0 + s) * kH + h]);
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, lse[s * kH]);
     float den = 0.f;
-    float acc[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
     for (int s = 0; s < ns; ++s) {
-        const float lse = p.part_lse[(u0 + s) * kH + h];
-        const float w = (M == neg_inf()) ? 0.f : fast_exp2(lse - M);
+        const float w = (M == neg_inf()) ? 0.f : fast_exp2(lse[s * kH] - M);
         den += w;
-        const float* po = p.part_o + ((u0 + s) * kH + h) * kDv;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] += w * po[lane + 32 * j];
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((u0 + s) * kH + h) * kDv + d));
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    __nv_bfloat16* o = out + (static_cast<size_t>(b) * kH + h) * kDv;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) o[lane + 32 * j] = __float2bfloat16_rn(acc[j] * inv);
-    if (lane == 0 && lse_out)
+    __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&lo2), *reinterpret_cast<uint32_t*>(&hi2));
+    *reinterpret_cast<uint2*>(out + (static_cast<size_t>(b) * kH + h) * kDv + d) = pk;
+    if (d == 0 && lse_out)
         lse_out[static_cast<size_t>(b) * kH + h] = den > 0.f ? (M + log2f(den)) * kLn2 : neg_inf();
 }
 
@@ -410,7 +415,7 @@ int mla_launch(const MlaParams& p, const CUtensorMap& tc, const CUtensorMap& tq,
         mla_decode_kernel<true><<<grid, kThreads, kMlaSmem, stream>>>(tc, tq, p);
     else
         mla_decode_kernel<false><<<grid, kThreads, kMlaSmem, stream>>>(tc, tq, p);
-    mla_combine_kernel<<<p.B * (kH / 4), 128, 0, stream>>>(p, static_cast<__nv_bfloat16*>(out),
+    mla_combine_kernel<<<p.B * (kH / 2), 256, 0, stream>>>(p, static_cast<__nv_bfloat16*>(out),
                                                             lse_out);
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
