@@ -165,6 +165,7 @@ int mla_run(const void* q, const void* c_pool, const int32_t* block_table,
     uint8_t* wb = static_cast<uint8_t*>(ws);
     MlaParams p;
     std::memset(&p, 0, sizeof p);
+    p.q = q;
     p.block_table = block_table;
     p.seq_lens = seq_lens;
     p.idx = idx;

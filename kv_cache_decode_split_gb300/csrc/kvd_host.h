@@ -106,6 +106,7 @@ int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream);
 // MLA (absorbed latent), dense or over selected tokens
 // ---------------------------------------------------------------------------------------
 struct MlaParams {
+    const void* q;             // [B, 128, 576] bf16 absorbed queries
     const int32_t* block_table;
     const int32_t* seq_lens;
     const int32_t* idx;        // sparse: [B, idx_stride] logical positions

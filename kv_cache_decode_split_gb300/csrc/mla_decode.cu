@@ -35,24 +35,24 @@ constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kTok = 64;              // tokens per tile
 constexpr int kNBox = 5;              // 64-dim boxes held per CTA (rank 0 uses 4)
-constexpr int kStages = 2;
+constexpr int kStages = 4;
 constexpr int kTileBox = kTok * 128;  // 8 KB: 64 tokens x 64 dims
 constexpr int kStageBytes = kNBox * kTileBox;
-constexpr int kQBox = kH * 128;       // 16 KB: 128 heads x 64 dims
-constexpr int kPBytes = kH * 128;     // 16 KB: 128 heads x 64 tokens
 constexpr int kThreads = 6 * 32;      // warps 0-3 softmax, 4 loads, 5 MMA
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct MlaSmem {
-    uint8_t q[kNBox][kQBox];               // offset 0, 1024-aligned
-    uint8_t stage[kStages][kStageBytes];
-    uint8_t p[2][kPBytes];
-    float x[kH][kTok];                     // the partner's partial scores (float4-swizzled)
-    uint64_t full[kStages], empty[kStages], qfull, sfull[2], sempty[2], xfull, peer_free,
-        pfull[2], pvdone[2], ofinal;
+    uint8_t stage[kStages][kStageBytes];   // offset 0, 1024-aligned
+    float x[2][kH][kTok];                  // the partner's partial scores (float4-swizzled)
+    uint64_t full[kStages], empty[kStages], qready, sfull, sempty, xfull[2], peer_free[2], pfull,
+        pvdone, ofinal;
     uint32_t tmem_base;
 };
+
+// Tensor-memory columns (all 512): this CTA's query slice (bf16 pairs, up to 320 dims), one
+// score tile, one P tile (bf16 pairs) and the 256-wide output accumulator.
+constexpr uint32_t kColQ = 0, kColS = 160, kColP = 224, kColO = 256;
 constexpr int kMlaSmem = static_cast<int>(sizeof(MlaSmem)) + 1024;
 static_assert(kMlaSmem <= 227 * 1024, "MLA shared memory");
 
@@ -85,15 +85,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(&sm.full[s], kSparse ? 32 : 1);
             mbar_init(&sm.empty[s], 1);
         }
-        mbar_init(&sm.qfull, 1);
+        mbar_init(&sm.qready, 4);
+        mbar_init(&sm.sfull, 1);
+        mbar_init(&sm.sempty, 4);
+        mbar_init(&sm.pfull, 4);
+        mbar_init(&sm.pvdone, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.sfull[i], 1);
-            mbar_init(&sm.sempty[i], 4);
-            mbar_init(&sm.pfull[i], 4);
-            mbar_init(&sm.pvdone[i], 1);
+            mbar_init(&sm.xfull[i], 1);      // armed with the exchanged byte count each tile
+            mbar_init(&sm.peer_free[i], 4);  // one arrive per softmax warp of the partner
         }
-        mbar_init(&sm.xfull, 1);      // armed with the exchanged byte count each tile
-        mbar_init(&sm.peer_free, 4);  // one arrive per softmax warp of the partner
         mbar_init(&sm.ofinal, 1);
         fence_mbar_init();
     }
@@ -106,12 +106,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (warp == 4) {
         // ------------------------------------------------------------------ loads
-        if (lane == 0) {
-            prefetch_tensormap(&tmQ);
-            mbar_arrive_expect_tx(&sm.qfull, nbox * kQBox);
-            for (int i = 0; i < nbox; ++i)
-                tma_load_2d(sm.q[i], &tmQ, &sm.qfull, dim0 + 64 * i, b * kH);
-        }
         if (!kSparse) {
             if (lane == 0) {
                 prefetch_tensormap(&tmC);
@@ -187,34 +181,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kH, kTok, 0, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kH, 256, 0, 1);
             const int nk = nbox * 4;  // 16-dim k-steps of the score product
-            bool ok = mbar_wait(&sm.qfull, 0, p.err);
+            bool ok = mbar_wait(&sm.qready, 0, p.err);
             auto qk = [&](int i) {
-                const int s = i % kStages, buf = i & 1;
+                const int s = i % kStages;
                 ok = ok && mbar_wait(&sm.full[s], (i / kStages) & 1, p.err);
-                ok = ok && mbar_wait(&sm.sempty[buf], ((i >> 1) & 1) ^ 1, p.err);
+                ok = ok && mbar_wait(&sm.sempty, (i & 1) ^ 1, p.err);
                 if (!ok) return;
                 tc_fence_after();
-                const uint32_t qa = smem_u32(sm.q[0]), ca = smem_u32(sm.stage[s]);
+                const uint32_t ca = smem_u32(sm.stage[s]);
                 for (int ks = 0; ks < nk; ++ks) {
-                    const uint64_t ad = sw128_kmajor_desc(qa + (ks >> 2) * kQBox + (ks & 3) * 32);
                     const uint64_t bd =
                         sw128_kmajor_desc(ca + (ks >> 2) * kTileBox + (ks & 3) * 32);
-                    tc_mma_bf16(tmem + buf * kTok, ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
+                    tc_mma_bf16_ts(tmem + kColS, tmem + kColQ + ks * 8, bd, idesc_qk,
+                                   ks > 0 ? 1u : 0u);
                 }
-                tc_commit(&sm.sfull[buf]);
+                tc_commit(&sm.sfull);
             };
             auto pv = [&](int i) {
-                const int s = i % kStages, pb = i & 1;
-                ok = ok && mbar_wait(&sm.pfull[pb], (i >> 1) & 1, p.err);
+                const int s = i % kStages;
+                ok = ok && mbar_wait(&sm.pfull, i & 1, p.err);
                 if (!ok) return;
                 tc_fence_after();
-                const uint32_t pa = smem_u32(sm.p[pb]), va = smem_u32(sm.stage[s]);
+                const uint32_t va = smem_u32(sm.stage[s]);
                 for (int ks = 0; ks < kTok / 16; ++ks) {
-                    const uint64_t ad = sw128_kmajor_desc(pa + ks * 32);
                     const uint64_t bd = sw128_mnmajor_desc(va + ks * 16 * 128, kTileBox);
-                    tc_mma_bf16(tmem + 256, ad, bd, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+                    tc_mma_bf16_ts(tmem + kColO, tmem + kColP + ks * 8, bd, idesc_pv,
+                                   (i > 0 || ks > 0) ? 1u : 0u);
                 }
-                tc_commit(&sm.pvdone[pb]);
+                tc_commit(&sm.pvdone);
                 tc_commit(&sm.empty[s]);
             };
             qk(0);
@@ -230,51 +224,79 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------------ softmax
         const int h = threadIdx.x;  // head = TMEM lane
         const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const uint32_t my_x = smem_u32(&sm.x[h][0]);
-        const uint32_t peer_x = map_peer(my_x, peer);
-        const uint32_t peer_xfull = map_peer(smem_u32(&sm.xfull), peer);
-        const uint32_t peer_free = map_peer(smem_u32(&sm.peer_free), peer);
+        {
+            // this CTA's query slice into TMEM (the A operand of the score product)
+            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                reinterpret_cast<const __nv_bfloat16*>(p.q) + (static_cast<size_t>(b) * kH + h) * kDqk +
+                dim0);
+            for (int c = 0; c < nbox * 32; c += 32) {
+                uint32_t r[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = __ldg(qrow + c + j);
+                tmem_st_32x32b_x32(trow + kColQ + c, r);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.qready);
+        }
+        // Tile j's partial score row is read (freeing the score tile for the next product)
+        // and sent to the partner one tile ahead of combining tile j - 1, so the exchange
+        // latency overlaps the previous tile's softmax.
+        const uint32_t peer_x0 = map_peer(smem_u32(&sm.x[0][h][0]), peer);
+        const uint32_t peer_x1 = map_peer(smem_u32(&sm.x[1][h][0]), peer);
+        const uint32_t peer_xfull0 = map_peer(smem_u32(&sm.xfull[0]), peer);
+        const uint32_t peer_xfull1 = map_peer(smem_u32(&sm.xfull[1]), peer);
+        const uint32_t peer_free0 = map_peer(smem_u32(&sm.peer_free[0]), peer);
+        const uint32_t peer_free1 = map_peer(smem_u32(&sm.peer_free[1]), peer);
         const float sl2 = p.scale_log2;
         float m_ref = neg_inf(), l = 0.f;
         bool ok = true;
-        for (int i = 0; i < n_tiles && ok; ++i) {
-            const int buf = i & 1;
-            if (!(ok = mbar_wait(&sm.sfull[buf], (i >> 1) & 1, p.err))) break;
+        auto send = [&](int j, float (&s)[kTok]) -> bool {
+            const int xb = j & 1;
+            if (!mbar_wait(&sm.sfull, j & 1, p.err)) return false;
             tc_fence_after();
-            float s[kTok];
             {
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(trow + buf * kTok, r);
+                tmem_ld_32x32b_x32(trow + kColS, r);
                 tmem_ld_wait(r);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(r[j]);
-                tmem_ld_32x32b_x32(trow + buf * kTok + 32, r);
+                for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(r[c]);
+                tmem_ld_32x32b_x32(trow + kColS + 32, r);
                 tmem_ld_wait(r);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(r[j]);
+                for (int c = 0; c < 32; ++c) s[32 + c] = __uint_as_float(r[c]);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.sempty[buf]);
-            // exchange partial scores with the partner CTA: asynchronous remote stores whose
-            // bytes complete the partner's barrier, so the sender needs no fence
-            if (h == 0) mbar_arrive_expect_tx(&sm.xfull, kH * kTok * 4);
-            if (!(ok = mbar_wait_cluster(&sm.peer_free, (i & 1) ^ 1, p.err))) break;
+            if (lane == 0) mbar_arrive(&sm.sempty);  // the score tile may be overwritten
+            if (h == 0) mbar_arrive_expect_tx(&sm.xfull[xb], kH * kTok * 4);
+            if (!mbar_wait_cluster(&sm.peer_free[xb], ((j >> 1) & 1) ^ 1, p.err)) return false;
+            const uint32_t px = xb ? peer_x1 : peer_x0;
+            const uint32_t pf = xb ? peer_xfull1 : peer_xfull0;
 #pragma unroll
             for (int c4 = 0; c4 < kTok / 4; ++c4)
-                st_async_v4(peer_x + ((c4 ^ (h & 15)) << 4), s[4 * c4], s[4 * c4 + 1],
-                            s[4 * c4 + 2], s[4 * c4 + 3], peer_xfull);
-            if (!(ok = mbar_wait_cluster(&sm.xfull, i & 1, p.err))) break;
+                st_async_v4(px + ((c4 ^ (h & 15)) << 4), s[4 * c4], s[4 * c4 + 1], s[4 * c4 + 2],
+                            s[4 * c4 + 3], pf);
+            return true;
+        };
+        float s[kTok];
+        ok = send(0, s);
+        for (int i = 0; i < n_tiles && ok; ++i) {
+            float sn[kTok];
+            if (i + 1 < n_tiles && !(ok = send(i + 1, sn))) break;
+            const int xb = i & 1;
+            if (!(ok = mbar_wait_cluster(&sm.xfull[xb], (i >> 1) & 1, p.err))) break;
 #pragma unroll
             for (int c4 = 0; c4 < kTok / 4; ++c4) {
-                const float4 v = *reinterpret_cast<const float4*>(&sm.x[h][(c4 ^ (h & 15)) * 4]);
+                const float4 v = *reinterpret_cast<const float4*>(&sm.x[xb][h][(c4 ^ (h & 15)) * 4]);
                 s[4 * c4] += v.x;
                 s[4 * c4 + 1] += v.y;
                 s[4 * c4 + 2] += v.z;
                 s[4 * c4 + 3] += v.w;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(peer_free);  // this warp's rows were read
+            if (lane == 0) mbar_arrive_remote(xb ? peer_free1 : peer_free0);  // slot read
             // online softmax in log2 units, lazily rescaled
             const int T0 = lo + i * kTok;
             float mt = neg_inf();
@@ -307,31 +329,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 pk[j] = *reinterpret_cast<const uint32_t*>(&v);
             }
             l += psum;
-            const int pb = i & 1;
-            if (i >= 2 && !(ok = mbar_wait(&sm.pvdone[pb], ((i >> 1) & 1) ^ 1, p.err))) break;
+            // the P tile (and O) are free once tile i - 1's value product has completed
+            if (i >= 1 && !(ok = mbar_wait(&sm.pvdone, (i - 1) & 1, p.err))) break;
+            tc_fence_after();
             if (__any_sync(0xffffffffu, resc)) {
-                // O += ... of the previous tile must land before it is rescaled
-                if (!(ok = mbar_wait(&sm.pvdone[(i - 1) & 1], ((i - 1) >> 1) & 1, p.err))) break;
-                tc_fence_after();
                 for (int c = 0; c < 8; ++c) {
                     uint32_t r[32];
-                    tmem_ld_32x32b_x32(trow + 256 + c * 32, r);
+                    tmem_ld_32x32b_x32(trow + kColO + c * 32, r);
                     tmem_ld_wait(r);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-                    tmem_st_32x32b_x32(trow + 256 + c * 32, r);
+                    tmem_st_32x32b_x32(trow + kColO + c * 32, r);
                 }
-                tmem_st_wait();
             }
-            uint8_t* prow = sm.p[pb] + h * 128;
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc)
-                *reinterpret_cast<uint4*>(prow + ((cc ^ (h & 7)) << 4)) =
-                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-            fence_proxy_async_smem();
+            tmem_st_32x32b_x32(trow + kColP, pk);  // P row: 64 bf16
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.pfull[pb]);
+            if (lane == 0) mbar_arrive(&sm.pfull);
+#pragma unroll
+            for (int j = 0; j < kTok; ++j) s[j] = sn[j];
         }
         // the split's partial: O / l for this CTA's 256 value dims, and log2-sum-exp
         if (ok && mbar_wait(&sm.ofinal, 0, p.err)) {
@@ -340,7 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float* po = p.part_o + (static_cast<size_t>(unit) * kH + h) * kDv + rank * 256;
             for (int c = 0; c < 8; ++c) {
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(trow + 256 + c * 32, r);
+                tmem_ld_32x32b_x32(trow + kColO + c * 32, r);
                 tmem_ld_wait(r);
 #pragma unroll
                 for (int j = 0; j < 32; j += 4)
