@@ -69,18 +69,25 @@ class GqaRunner:
         self.out = torch.empty_like(self.q)
         self.ws = kvd.Workspace(dev)
         self.swa = x.window > 0 or x.n_sink > 0 or x.sink_logit is not None
-        lens = x.seq_lens.tolist()
-        elt = x.q.element_size()
+        self._config, self.bytes, self.flops = self.describe(name, x)
+
+    @staticmethod
+    def describe(name, x):
+        """(config, algorithmic KV bytes, FLOPs) of one step, from the CPU inputs."""
+        swa = x.window > 0 or x.n_sink > 0 or x.sink_logit is not None
         tok = 0
-        for L in lens:
-            if self.swa:
-                vis = set(range(min(x.n_sink, L))) | set(range(max(0, L - x.window), L))
-                tok += len(vis)
+        for L in x.seq_lens.tolist():
+            if swa:
+                tok += len(set(range(min(x.n_sink, L))) | set(range(max(0, L - x.window), L)))
             else:
                 tok += L
-        self.tokens = tok
-        self.bytes = tok * x.Hkv * x.D * 2 * elt      # K and V rows the method must read
-        self.flops = 4.0 * tok * x.Hkv * (x.Hq // x.Hkv) * x.D
+        nbytes = tok * x.Hkv * x.D * 2 * x.q.element_size()   # K and V rows the method reads
+        flops = 4.0 * tok * x.Hkv * (x.Hq // x.Hkv) * x.D
+        cfg = {"workload": name, "B": x.B, "Hq": x.Hq, "Hkv": x.Hkv, "D": x.D,
+               "page_size": x.page_size, "window": x.window, "n_sink": x.n_sink,
+               "learned_sink": x.sink_logit is not None,
+               "seq_len_mean": float(x.seq_lens.float().mean()), "kv_bytes": nbytes}
+        return cfg, nbytes, flops
 
     def step(self, q=None, out=None):
         x = self.x
@@ -94,11 +101,7 @@ class GqaRunner:
                                               out=out, workspace=self.ws)
 
     def config(self):
-        x = self.x
-        return {"workload": self.name, "B": x.B, "Hq": x.Hq, "Hkv": x.Hkv, "D": x.D,
-                "page_size": x.page_size, "window": x.window, "n_sink": x.n_sink,
-                "learned_sink": x.sink_logit is not None,
-                "seq_len_mean": float(x.seq_lens.float().mean()), "kv_bytes": self.bytes}
+        return self._config
 
     # --- end-to-end through the public API from pinned host buffers
     def e2e_setup(self):
@@ -163,9 +166,17 @@ class MlaRunner:
         self.sl = x.seq_lens.to(dev)
         self.out = torch.empty(x.B, x.H, 512, dtype=torch.bfloat16, device=dev)
         self.ws = kvd.Workspace(dev)
+        self._config, self.bytes, self.flops = self.describe(name, x)
+
+    @staticmethod
+    def describe(name, x):
         tok = int(x.seq_lens.sum())
-        self.bytes = tok * x.d_qk * 2
-        self.flops = 2.0 * tok * x.H * (x.d_qk + 512)
+        nbytes = tok * x.d_qk * 2
+        flops = 2.0 * tok * x.H * (x.d_qk + 512)
+        cfg = {"workload": name, "B": x.B, "H": x.H, "d_qk": x.d_qk, "d_v": 512,
+               "page_size": x.page_size, "seq_len_mean": float(x.seq_lens.float().mean()),
+               "kv_bytes": nbytes, "flops": flops}
+        return cfg, nbytes, flops
 
     def step(self, q=None):
         x = self.x
@@ -173,10 +184,7 @@ class MlaRunner:
                                         scale=x.scale, out=self.out, workspace=self.ws)
 
     def config(self):
-        x = self.x
-        return {"workload": self.name, "B": x.B, "H": x.H, "d_qk": x.d_qk, "d_v": 512,
-                "page_size": x.page_size, "seq_len_mean": float(x.seq_lens.float().mean()),
-                "kv_bytes": self.bytes, "flops": self.flops}
+        return self._config
 
     def e2e_setup(self):
         self.h_q = self.x.q.pin_memory()
@@ -232,10 +240,18 @@ class DsaRunner:
         self.out = torch.empty(xm.B, xm.H, 512, dtype=torch.bfloat16, device=dev)
         self.ws1 = kvd.Workspace(dev)
         self.ws2 = kvd.Workspace(dev)
+        self._config, self.bytes, self.flops = self.describe(name, (xi, xm))
+
+    @staticmethod
+    def describe(name, x):
+        xi, xm = x
         lens = [int(v) for v in xm.seq_lens]
-        sel = sum(min(self.k, L) for L in lens)
-        self.bytes = sum(lens) * xi.Di * 2 + sel * xm.d_qk * 2
-        self.flops = 2.0 * sum(lens) * xi.Hi * xi.Di + 2.0 * sel * xm.H * (xm.d_qk + 512)
+        sel = sum(min(xi.k, L) for L in lens)
+        nbytes = sum(lens) * xi.Di * 2 + sel * xm.d_qk * 2
+        flops = 2.0 * sum(lens) * xi.Hi * xi.Di + 2.0 * sel * xm.H * (xm.d_qk + 512)
+        cfg = {"workload": name, "B": xm.B, "H": xm.H, "Hi": xi.Hi, "Di": xi.Di, "k": xi.k,
+               "seq_len": lens[0], "page_size": xm.page_size, "kv_bytes": nbytes, "flops": flops}
+        return cfg, nbytes, flops
 
     def step(self, qi=None, q=None):
         xm = self.xm
@@ -247,10 +263,7 @@ class DsaRunner:
                                                out=self.out, workspace=self.ws2)
 
     def config(self):
-        xi, xm = self.xi, self.xm
-        return {"workload": self.name, "B": xm.B, "H": xm.H, "Hi": xi.Hi, "Di": xi.Di,
-                "k": self.k, "seq_len": int(xm.seq_lens[0]), "page_size": xm.page_size,
-                "kv_bytes": self.bytes, "flops": self.flops}
+        return self._config
 
     def e2e_setup(self):
         self.h_qi = self.xi.q.pin_memory()
@@ -355,6 +368,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def shard_range(n, rank, world):
+    """Contiguous share [lo, hi) of n independent units (sequences) for one rank."""
+    per, extra = divmod(n, world)
+    lo = rank * per + min(rank, extra)
+    return lo, lo + per + (1 if rank < extra else 0)
+
+
+def aggregate(local_ms, bytes_per_rank, world, dist=None):
+    """Whole-job throughput: every rank's bytes over the slowest rank's time (max over
+    ranks). Returns (max_ms, GB/s)."""
+    t = torch.tensor([float(local_ms)], dtype=torch.float64)
+    if dist is not None and world > 1:
+        if t.device.type == "cpu" and dist.get_backend() == "nccl":
+            t = t.cuda()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    return ms, world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def flush_l2(buf):
     """Evict the workload from L2 by READING a buffer larger than L2 (a write-based flush
     would leave dirty lines whose write-back the next timed step would pay for)."""
@@ -410,17 +442,24 @@ def run_reference(args, rank, world):
     wl = W.WORKLOADS[name]
     x_runner = oracle_runner(name)
     per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
-    vals = []
+    vals, secs = [], []
     desc = ""
     for i in range(args.warmup + args.steps):
         nbytes, el, desc = x_runner.oracle_sample(per_step)
         if i >= args.warmup:
             vals.append(nbytes / el / 1e9)
+            secs.append(el)
     v = statistics.median(vals)
+    cls = RUNNERS[wl.kind]
+    xin = (x_runner.xi, x_runner.xm) if cls is DsaRunner else x_runner.x
+    cfg, _, _ = cls.describe(name, xin)
+    cfg = dict(cfg, l2="KV bytes larger than L2; steps back to back", parallelism="single")
     line = {"impl": "reference", "metric": "decode-attn KV GB/s", "value": v, "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic", "config": {"workload": name, "desc": wl.description},
+            "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic: seeded N(0,1) rounded to bf16, shapes of the named workload",
+            "config": cfg,
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"per step: {desc}, about {per_step:.0f} s of CPU work"},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -466,9 +505,7 @@ def main():
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, _ = aggregate(total_ms, r.bytes, world, dist if world > 1 else None)
     ms = total_ms / args.steps
     value = world * r.bytes / (ms * 1e-3) / 1e9
     clocks = clk.summary()
@@ -480,10 +517,7 @@ def main():
     torch.cuda.synchronize()
     e2e_total, _ = time_steps(r.e2e_step, args.steps, stream)
     e2e_ms = e2e_total / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms, _ = aggregate(e2e_ms, r.bytes, world, dist if world > 1 else None)
 
     kern_ms = statistics.mean(per)
     achieved = r.bytes / (kern_ms * 1e-3) / 1e9
