@@ -59,7 +59,8 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False) -> st
             if verbose and log:
                 print(f"== {os.path.basename(src)}\n{log}", file=sys.stderr)
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH
+    # -z defs: an unresolved symbol fails the build here, not the first import on the GPU machine
+    cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-Xlinker", "-z", "-Xlinker", "defs"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

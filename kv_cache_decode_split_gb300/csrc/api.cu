@@ -59,6 +59,31 @@ int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_
     return r == CUDA_SUCCESS ? KVD_OK : KVD_ERR_CUDA;
 }
 
+// 3-D view of a row-major [rows, cols] bf16 matrix as (64-element column piece, row,
+// column block); the block's stride (128 bytes) is smaller than the row pitch, so a box
+// {64, box_rows, nblocks} lands in shared memory as [block][row][64] with 128-byte swizzle.
+int make_tmap_bf16_blocked(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows, uint32_t nblocks) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode || cols % 64 != 0) return KVD_ERR_CUDA;
+    cuuint64_t dims[3] = {64, rows, cols / 64};
+    cuuint64_t strides[2] = {cols * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, nblocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KVD_OK : KVD_ERR_CUDA;
+}
+
 // Split plan. The bf16 kernel is persistent (one CTA per SM pulling work items from a
 // queue), so the chunk length trades load balance (more, shorter items) against the
 // per-item merge cost: aim for about six items per SM, at least four 64-token tiles each.
@@ -184,12 +209,15 @@ int mla_run(const void* q, const void* c_pool, const int32_t* block_table,
     p.idx_stride = k;
     p.sparse = sparse ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
-    CUtensorMap tc, tq;
-    if (make_tmap_bf16_2d(&tc, c_pool, (uint64_t)num_pages * page_size, 576,
-                          page_size < 64 ? page_size : 64) != KVD_OK)
+    // 3-D maps (rank 0: 4 blocks of 64 dims, rank 1: 5) for 64-token tiles within a page,
+    // and a 2-D map for pages shorter than a tile
+    CUtensorMap tc0, tc1, tc2;
+    const uint64_t rows = (uint64_t)num_pages * page_size;
+    if (make_tmap_bf16_blocked(&tc0, c_pool, rows, 576, 64, 4) != KVD_OK) return KVD_ERR_CUDA;
+    if (make_tmap_bf16_blocked(&tc1, c_pool, rows, 576, 64, 5) != KVD_OK) return KVD_ERR_CUDA;
+    if (make_tmap_bf16_2d(&tc2, c_pool, rows, 576, page_size < 64 ? page_size : 64) != KVD_OK)
         return KVD_ERR_CUDA;
-    if (make_tmap_bf16_2d(&tq, q, (uint64_t)B * 128, 576, 128) != KVD_OK) return KVD_ERR_CUDA;
-    return mla_launch(p, tc, tq, out, lse_out, stream);
+    return mla_launch(p, tc0, tc1, tc2, out, lse_out, stream);
 }
 
 }  // namespace kvd
@@ -260,8 +288,10 @@ int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t
     CUtensorMap tk, tv;
     const uint64_t rows = (uint64_t)num_pages * Hkv * page_size;
     const uint32_t box_rows = page_size < 64 ? page_size : 64;
-    if (make_tmap_bf16_2d(&tk, k_pool, rows, D, box_rows) != KVD_OK) return KVD_ERR_CUDA;
-    if (make_tmap_bf16_2d(&tv, v_pool, rows, D, box_rows) != KVD_OK) return KVD_ERR_CUDA;
+    if (make_tmap_bf16_blocked(&tk, k_pool, rows, D, box_rows, D / 64) != KVD_OK)
+        return KVD_ERR_CUDA;
+    if (make_tmap_bf16_blocked(&tv, v_pool, rows, D, box_rows, D / 64) != KVD_OK)
+        return KVD_ERR_CUDA;
     return gqa_launch(plan, p, &tk, &tv, stream);
 }
 
@@ -336,12 +366,16 @@ int dsa_indexer_topk(const void* q_idx, const void* k_idx_pool, const float* w,
     ip.num_pages = num_pages;
     ip.max_len = max_len;
     ip.tiles_per_b = (max_len + 127) / 128;
-    CUtensorMap tk, tq;
+    CUtensorMap tk, tk128, tq;
     if (make_tmap_bf16_2d(&tk, k_idx_pool, (uint64_t)num_pages * page_size, 128,
                           page_size < 128 ? page_size : 128) != KVD_OK)
         return KVD_ERR_CUDA;
+    // one instruction per 128-token tile when its rows are contiguous in the pool
+    if (make_tmap_bf16_blocked(&tk128, k_idx_pool, (uint64_t)num_pages * page_size, 128, 128,
+                               2) != KVD_OK)
+        return KVD_ERR_CUDA;
     if (make_tmap_bf16_2d(&tq, q_idx, (uint64_t)B * 64, 128, 64) != KVD_OK) return KVD_ERR_CUDA;
-    int st = dsa_indexer_launch(ip, tk, tq, stream);
+    int st = dsa_indexer_launch(ip, tk, tk128, tq, stream);
     if (st != KVD_OK) return st;
     TopkParams tp;
     std::memset(&tp, 0, sizeof tp);

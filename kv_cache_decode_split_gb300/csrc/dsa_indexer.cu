@@ -59,6 +59,7 @@ __device__ __forceinline__ TileRange my_tiles(int total) {
 
 __global__ void __launch_bounds__(kIdxThreads, 1)
     dsa_indexer_kernel(const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmK128,
                        const __grid_constant__ CUtensorMap tmQ, const IdxParams p) {
     extern __shared__ uint8_t smem_raw[];
     IdxSmem& sm = *reinterpret_cast<IdxSmem*>(
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tensormap(&tmK);
+            prefetch_tensormap(&tmK128);
             prefetch_tensormap(&tmQ);
             const int bp = min(p.page_size, kItile);
             int cur_b = -1, L = 0;
@@ -115,15 +117,25 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                 const int s = g % kIdxStages;
                 if (!(ok = mbar_wait(&sm.empty[s], ((g / kIdxStages) & 1) ^ 1, p.err))) break;
                 mbar_arrive_expect_tx(&sm.full[s], kIdxTileBytes);
+                // physical rows of the tile's page pieces; one 32 KB instruction when they
+                // are contiguous (adjacent pages, or pages of >= 128 tokens)
+                int ys[kItile / 16];
+                bool contiguous = true;
                 for (int sub = 0; sub < kItile / bp; ++sub) {
                     const int t = j * kItile + sub * bp;
                     const int tc = t < L ? t : L - 1;  // rows past the end: a valid page
                     const int pg = load_page(p.block_table, p.max_pages, p.num_pages, b,
                                              tc / p.page_size, p.err);
-                    const int y = pg * p.page_size + (t % p.page_size);
-                    for (int half = 0; half < 2; ++half)
-                        tma_load_2d(sm.stage[s] + half * (kIdxTileBytes / 2) + sub * bp * 128,
-                                    &tmK, &sm.full[s], half * 64, y);
+                    ys[sub] = pg * p.page_size + (t % p.page_size);
+                    if (sub > 0 && ys[sub] != ys[0] + sub * bp) contiguous = false;
+                }
+                if (contiguous && ys[0] + kItile <= p.num_pages * p.page_size) {
+                    tma_load_3d(sm.stage[s], &tmK128, &sm.full[s], 0, ys[0], 0);
+                } else {
+                    for (int sub = 0; sub < kItile / bp; ++sub)
+                        for (int half = 0; half < 2; ++half)
+                            tma_load_2d(sm.stage[s] + half * (kIdxTileBytes / 2) + sub * bp * 128,
+                                        &tmK, &sm.full[s], half * 64, ys[sub]);
                 }
                 ++g;
             }
@@ -453,8 +465,8 @@ __global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkPa
 
 int idx_smem_bytes() { return kIdxSmem; }
 
-int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensorMap& tq,
-                       cudaStream_t stream) {
+int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensorMap& tk128,
+                       const CUtensorMap& tq, cudaStream_t stream) {
     static int configured = 0;
     if (!configured) {
         if (cudaFuncSetAttribute(dsa_indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -464,7 +476,7 @@ int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensor
     }
     const int total = p.B * p.tiles_per_b;
     const int grid = total < num_sms() ? total : num_sms();
-    dsa_indexer_kernel<<<grid, kIdxThreads, kIdxSmem, stream>>>(tk, tq, p);
+    dsa_indexer_kernel<<<grid, kIdxThreads, kIdxSmem, stream>>>(tk, tk128, tq, p);
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
 

@@ -343,15 +343,14 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT>::kThreads, 1)
                         bulk_load(stageQ(s), qsrc, qbytes, &full[s]);
                     }
                     for (int sub = 0; sub < subs; ++sub) {
+                        // one instruction per piece for K and for V, all D/64 column blocks:
+                        // shared layout [piece][block][row][64]
                         const int j = tile * subs + sub;
                         const int t = t0 + j * bp;
                         const int y = (dd.pages[j] * p.Hkv + it.kvh) * p.page_size + (t % p.page_size);
-#pragma unroll
-                        for (int box = 0; box < D / 64; ++box) {
-                            const uint32_t off = box * kTile * 128 + sub * bp * 128;
-                            tma_load_2d(stageK(s) + off, &tmK, &full[s], box * 64, y);
-                            tma_load_2d(stageV(s) + off, &tmV, &full[s], box * 64, y);
-                        }
+                        const uint32_t off = sub * (D / 64) * bp * 128;
+                        tma_load_3d(stageK(s) + off, &tmK, &full[s], 0, y, 0);
+                        tma_load_3d(stageV(s) + off, &tmV, &full[s], 0, y, 0);
                     }
                     ++g;
                 }
@@ -368,6 +367,13 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT>::kThreads, 1)
         float m_run[NT][2], l_run[NT][2];
         const int r0 = warp * 16;
         const float sl2 = p.scale_log2;
+        // tile layout [piece][block][row][64] with pieces of bp rows (the page, at most 64)
+        const int lbp = 31 - __clz(min(p.page_size, kTile));
+        auto addr = [&](int row, int col) -> uint32_t {
+            return static_cast<uint32_t>(((row >> lbp) * (D / 64) + (col >> 6)) << (lbp + 7)) +
+                   (static_cast<uint32_t>(row & ((1 << lbp) - 1)) << 7) +
+                   ((((col & 63) >> 3) ^ (row & 7)) << 4);
+        };
         uint32_t g = 0;
         while (true) {
             const int s = g % S;
@@ -414,7 +420,7 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT>::kThreads, 1)
                     const int row = r0 + idx / (D / 8);
                     const int tok = T + row;
                     if (tok < lo || tok >= hi)
-                        *reinterpret_cast<uint4*>(vt + swz128(row, (idx % (D / 8)) * 8, kTile)) =
+                        *reinterpret_cast<uint4*>(vt + addr(row, (idx % (D / 8)) * 8)) =
                             make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();  // order these stores before later TMA writes
@@ -431,7 +437,7 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT>::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < KT; ++kk) {
                 uint32_t a[4];
-                ldsm_x4(kbase + swz128(r0 + (lane % 16), kk * 16 + (lane / 16) * 8, kTile), a);
+                ldsm_x4(kbase + addr(r0 + (lane % 16), kk * 16 + (lane / 16) * 8), a);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     if (kk & 1)
@@ -487,8 +493,8 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT>::kThreads, 1)
 #pragma unroll
             for (int mtl = 0; mtl < KT; ++mtl) {
                 uint32_t a[4];
-                ldsm_x4_t(vbase + swz128(r0 + (lane % 8) + (lane / 16) * 8,
-                                         mtl * 16 + ((lane / 8) % 2) * 8, kTile),
+                ldsm_x4_t(vbase + addr(r0 + (lane % 8) + (lane / 16) * 8,
+                                       mtl * 16 + ((lane / 8) % 2) * 8),
                           a);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)

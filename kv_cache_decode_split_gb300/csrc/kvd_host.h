@@ -98,8 +98,8 @@ struct TopkLayout {
 };
 TopkLayout topk_layout(int B, int max_len, int k, bool with_scores);
 
-int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensorMap& tq,
-                       cudaStream_t stream);
+int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensorMap& tk128,
+                       const CUtensorMap& tq, cudaStream_t stream);
 int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------------------
@@ -130,11 +130,16 @@ int mla_run(const void* q, const void* c_pool, const int32_t* block_table,
             void* out, float* lse_out, int B, int H, int d_qk, int d_v, int page_size,
             int max_pages, int num_pages, float scale, void* ws, size_t ws_bytes,
             cudaStream_t stream);
-int mla_launch(const MlaParams& p, const CUtensorMap& tc, const CUtensorMap& tq, void* out,
-               float* lse_out, cudaStream_t stream);
+int mla_launch(const MlaParams& p, const CUtensorMap& tc0, const CUtensorMap& tc1,
+               const CUtensorMap& tc2, void* out, float* lse_out, cudaStream_t stream);
 
 int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                       uint32_t box_rows);
+
+// 3-D bf16 tensor map over a row-major [rows, cols] matrix: box {64, box_rows, nblocks}
+// fills shared memory as [block][row][64] with 128-byte swizzle (cols a multiple of 64).
+int make_tmap_bf16_blocked(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows, uint32_t nblocks);
 
 int num_sms();
 

@@ -60,8 +60,9 @@ __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000);
 
 template <bool kSparse>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tmC,
-                      const __grid_constant__ CUtensorMap tmQ, const MlaParams p) {
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tmC0,
+                      const __grid_constant__ CUtensorMap tmC1,
+                      const __grid_constant__ CUtensorMap tmC2, const MlaParams p) {
     extern __shared__ uint8_t smem_raw[];
     MlaSmem& sm = *reinterpret_cast<MlaSmem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -79,6 +80,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int n_tiles = (hi - lo + kTok - 1) / kTok;
     const int nbox = rank == 0 ? 4 : 5;   // 64-dim boxes this CTA loads
     const int dim0 = rank == 0 ? 0 : 256;
+    const CUtensorMap& tmC = rank == 0 ? tmC0 : tmC1;  // 3-D maps with 4 / 5 blocks per box
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -109,6 +111,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!kSparse) {
             if (lane == 0) {
                 prefetch_tensormap(&tmC);
+                prefetch_tensormap(&tmC2);
                 const int bp = min(p.page_size, kTok);
                 for (int i = 0; i < n_tiles; ++i) {
                     const int s = i % kStages;
@@ -121,9 +124,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const int pg = load_page(p.block_table, p.max_pages, p.num_pages, b,
                                                  tc / p.page_size, p.err);
                         const int y = pg * p.page_size + (t % p.page_size);
-                        for (int bx = 0; bx < nbox; ++bx)
-                            tma_load_2d(sm.stage[s] + bx * kTileBox + sub * bp * 128, &tmC,
-                                        &sm.full[s], dim0 + 64 * bx, y);
+                        if (bp == kTok) {
+                            // all of this CTA's 64-dim blocks in one instruction
+                            tma_load_3d(sm.stage[s], &tmC, &sm.full[s], 0, y, dim0 / 64);
+                        } else {
+                            for (int bx = 0; bx < nbox; ++bx)
+                                tma_load_2d(sm.stage[s] + bx * kTileBox + sub * bp * 128, &tmC2,
+                                            &sm.full[s], dim0 + 64 * bx, y);
+                        }
                     }
                 }
                 const int first = n_tiles > kStages ? n_tiles - kStages : 0;
@@ -414,8 +422,8 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const MlaParams p, __n
 
 }  // namespace
 
-int mla_launch(const MlaParams& p, const CUtensorMap& tc, const CUtensorMap& tq, void* out,
-               float* lse_out, cudaStream_t stream) {
+int mla_launch(const MlaParams& p, const CUtensorMap& tc0, const CUtensorMap& tc1,
+               const CUtensorMap& tc2, void* out, float* lse_out, cudaStream_t stream) {
     static int configured[2] = {0, 0};
     const int which = p.sparse ? 1 : 0;
     if (!configured[which]) {
@@ -429,9 +437,9 @@ int mla_launch(const MlaParams& p, const CUtensorMap& tc, const CUtensorMap& tq,
     }
     const int grid = 2 * p.B * p.n_splits;
     if (p.sparse)
-        mla_decode_kernel<true><<<grid, kThreads, kMlaSmem, stream>>>(tc, tq, p);
+        mla_decode_kernel<true><<<grid, kThreads, kMlaSmem, stream>>>(tc0, tc1, tc2, p);
     else
-        mla_decode_kernel<false><<<grid, kThreads, kMlaSmem, stream>>>(tc, tq, p);
+        mla_decode_kernel<false><<<grid, kThreads, kMlaSmem, stream>>>(tc0, tc1, tc2, p);
     mla_combine_kernel<<<p.B * (kH / 2), 256, 0, stream>>>(p, static_cast<__nv_bfloat16*>(out),
                                                             lse_out);
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
