@@ -51,7 +51,7 @@ def measured_peaks():
 # ---------------------------------------------------------------------------------------
 class GqaRunner:
     """attn_decode_gqa_paged / attn_decode_swa_sink on a named workload."""
-    launches_per_step = 2          # split-KV kernel + log-sum-exp combine kernel
+    launches_per_step = 1          # split-KV kernel; its last CTA per group combines
     kernel = "gqa_decode_bf16_kernel"
 
     def __init__(self, name, dev):

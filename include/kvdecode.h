@@ -46,8 +46,16 @@
  *  - Every call is asynchronous on `stream`. Split-KV partial results live in
  *    the caller's workspace `ws` of at least kvd_workspace_size(...) bytes,
  *    zero-filled once before its first use; the kernels leave it ready for
- *    the next call. Calls that share a workspace must be ordered on one
- *    stream.
+ *    the next call of the same operation family. Calls that share a workspace
+ *    must be ordered on one stream.
+ *  - A workspace serves one operation family at a time: (1) GQA / SWA decode,
+ *    (2) MLA decode (dense or sparse), (3) DSA indexer / top-k. A family
+ *    keeps zero only the parts it relies on (completion counters, top-k
+ *    histograms and counters, the selection bitmap), and another family's
+ *    kernels leave other data there. Zero-fill the buffer again before
+ *    handing it to another family. A top-k that finds non-zero state stays in
+ *    bounds and records KVD_ERR_DEVICE_STATE; a GQA / SWA call may then
+ *    return wrong outputs.
  *  - Return value: KVD_OK, or a negative KVD_ERR_* code. Argument checks run
  *    on the host before any launch; on failure nothing is launched and the
  *    outputs are untouched. Faults the host cannot see (a block-table entry or
@@ -73,7 +81,8 @@ enum kvd_status {
     KVD_ERR_CUDA = -3,                /* a CUDA call or launch failed */
     KVD_ERR_TIMEOUT = -4,             /* (device) a bounded wait gave up */
     KVD_ERR_WORKSPACE_TOO_SMALL = -5, /* ws_bytes below kvd_workspace_size() */
-    KVD_ERR_DEVICE_OOB = -6           /* (device) page index or length out of range */
+    KVD_ERR_DEVICE_OOB = -6,          /* (device) page index or length out of range */
+    KVD_ERR_DEVICE_STATE = -7         /* (device) workspace was not in its zeroed state */
 };
 
 enum kvd_dtype { KVD_F32 = 0, KVD_BF16 = 1 };
@@ -213,8 +222,9 @@ size_t kvd_workspace_size(int op, int B, int H, int Hkv, int D, int max_len, int
 
 /*
  * Synchronise `stream`, return (and clear) the first device-side error that
- * kernels using workspace `ws` recorded: KVD_OK, KVD_ERR_TIMEOUT or
- * KVD_ERR_DEVICE_OOB; KVD_ERR_CUDA if the synchronisation itself failed.
+ * kernels using workspace `ws` recorded: KVD_OK, KVD_ERR_TIMEOUT,
+ * KVD_ERR_DEVICE_OOB or KVD_ERR_DEVICE_STATE; KVD_ERR_CUDA if the
+ * synchronisation itself failed.
  */
 int kvd_check_device_error(void *ws, cudaStream_t stream);
 

@@ -75,29 +75,37 @@ def kvd_check_device_error(ws, stream=None):
 class Workspace:
     """A zero-filled device buffer reused across calls (grown on demand).
 
-    The kernels leave it ready for the next call, so it is zeroed only when it is
-    (re)allocated. Calls sharing one workspace must be ordered on one stream.
+    The kernels of one operation family (GQA / SWA; MLA; DSA indexer / top-k) leave the
+    parts they rely on zeroed for the family's next call, so the buffer is zeroed only
+    when it is (re)allocated or handed to another family. Calls sharing one workspace
+    must be ordered on one stream.
     """
 
     def __init__(self, device=None):
         self.device = torch.device(device) if device is not None else torch.device("cuda")
         self.buffer = torch.zeros(0, dtype=torch.uint8, device=self.device)
+        self.family = None
 
-    def get(self, nbytes: int) -> torch.Tensor:
+    def get(self, nbytes: int, family=None) -> torch.Tensor:
         if self.buffer.numel() < nbytes:
             self.buffer = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=self.device)
+        elif family is not None and self.family is not None and family != self.family:
+            self.buffer.zero_()  # another family's kernels may have left non-zero state
+        if family is not None:
+            self.family = family
         return self.buffer
 
 
 _default_ws = {}
 
 
-def _ws(workspace, nbytes, device):
+def _ws(workspace, nbytes, device, family):
+    """Workspace buffer for one call of an operation family ("gqa", "mla" or "dsa")."""
     if workspace is None:
-        key = torch.device(device).index
+        key = (torch.device(device).index, family)
         workspace = _default_ws.setdefault(key, Workspace(device))
     if isinstance(workspace, Workspace):
-        buf = workspace.get(nbytes)
+        buf = workspace.get(nbytes, family)
     else:
         buf = workspace
     if buf.numel() < nbytes:
@@ -129,7 +137,7 @@ def attn_decode_gqa_paged(q, k_pool, v_pool, block_table, seq_lens, scale=None, 
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     out = torch.empty_like(q) if out is None else out
     nbytes = kvd_workspace_size("gqa", B, Hq, Hkv, D, max_pages * P)
-    ws = _ws(workspace, nbytes, q.device)
+    ws = _ws(workspace, nbytes, q.device, "gqa")
     st = lib.attn_decode_gqa_paged(_p(q), _p(k_pool), _p(v_pool), _p(block_table), _p(seq_lens),
                                    _p(out), _p(lse_out), B, Hq, Hkv, D, P, max_pages, num_pages,
                                    scale, _DT[q.dtype], _p(ws), ws.numel(), _stream(stream))
@@ -147,7 +155,7 @@ def attn_decode_swa_sink(q, k_pool, v_pool, block_table, seq_lens, window, n_sin
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     out = torch.empty_like(q) if out is None else out
     nbytes = kvd_workspace_size("swa", B, Hq, Hkv, D, max_pages * P, window, n_sink_tokens)
-    ws = _ws(workspace, nbytes, q.device)
+    ws = _ws(workspace, nbytes, q.device, "gqa")
     st = lib.attn_decode_swa_sink(_p(q), _p(k_pool), _p(v_pool), _p(block_table), _p(seq_lens),
                                   _p(out), _p(lse_out), B, Hq, Hkv, D, P, max_pages, num_pages,
                                   scale, _DT[q.dtype], int(window), int(n_sink_tokens),
@@ -174,7 +182,7 @@ def attn_decode_mla(q, c_pool, block_table, seq_lens, scale=1.0 / math.sqrt(192)
     B, H, d_qk, P, max_pages, num_pages = _mla_args(q, c_pool, block_table, seq_lens)
     out = torch.empty(B, H, d_v, dtype=torch.bfloat16, device=q.device) if out is None else out
     nbytes = kvd_workspace_size("mla", B, H, 1, d_v, max_pages * P)
-    ws = _ws(workspace, nbytes, q.device)
+    ws = _ws(workspace, nbytes, q.device, "mla")
     st = lib.attn_decode_mla(_p(q), _p(c_pool), _p(block_table), _p(seq_lens), _p(out),
                              _p(lse_out), B, H, d_qk, d_v, P, max_pages, num_pages, float(scale),
                              _p(ws), ws.numel(), _stream(stream))
@@ -197,7 +205,7 @@ def dsa_indexer_topk(q_idx, k_idx_pool, w, block_table, seq_lens, k=2048, topk_i
     topk_idx = torch.empty(B, k, dtype=torch.int32, device=dev) if topk_idx is None else topk_idx
     topk_count = torch.empty(B, dtype=torch.int32, device=dev) if topk_count is None else topk_count
     nbytes = kvd_workspace_size("dsa_topk", B, Hi, 1, Di, max_pages * P, k=k)
-    ws = _ws(workspace, nbytes, dev)
+    ws = _ws(workspace, nbytes, dev, "dsa")
     st = lib.dsa_indexer_topk(_p(q_idx), _p(k_idx_pool), _p(w), _p(block_table), _p(seq_lens),
                               _p(topk_idx), _p(topk_count), _p(scores_out), B, Hi, Di, P,
                               max_pages, num_pages, int(k), _p(ws), ws.numel(), _stream(stream))
@@ -214,7 +222,7 @@ def dsa_topk(scores, lens, k=2048, topk_idx=None, topk_count=None, workspace=Non
     topk_idx = torch.empty(B, k, dtype=torch.int32, device=dev) if topk_idx is None else topk_idx
     topk_count = torch.empty(B, dtype=torch.int32, device=dev) if topk_count is None else topk_count
     nbytes = kvd_workspace_size("dsa_topk", B, 1, 1, 0, stride, k=k)
-    ws = _ws(workspace, nbytes, dev)
+    ws = _ws(workspace, nbytes, dev, "dsa")
     st = lib.dsa_topk(_p(scores), _p(lens), _p(topk_idx), _p(topk_count), B, stride, int(k),
                       _p(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_topk")
@@ -231,7 +239,7 @@ def attn_decode_mla_sparse(q, c_pool, block_table, seq_lens, topk_idx, topk_coun
     k = topk_idx.shape[1]
     out = torch.empty(B, H, d_v, dtype=torch.bfloat16, device=q.device) if out is None else out
     nbytes = kvd_workspace_size("mla_sparse", B, H, 1, d_v, max_pages * P, k=k)
-    ws = _ws(workspace, nbytes, q.device)
+    ws = _ws(workspace, nbytes, q.device, "mla")
     st = lib.attn_decode_mla_sparse(_p(q), _p(c_pool), _p(block_table), _p(seq_lens),
                                     _p(topk_idx), _p(topk_count), _p(out), _p(lse_out), B, H,
                                     d_qk, d_v, k, P, max_pages, num_pages, float(scale), _p(ws),

@@ -26,7 +26,7 @@ EXPORTS = (
 
 STATUS = {
     0: "KVD_OK", -1: "KVD_ERR_INVALID_ARG", -2: "KVD_ERR_UNSUPPORTED", -3: "KVD_ERR_CUDA",
-    -4: "KVD_ERR_TIMEOUT", -5: "KVD_ERR_WORKSPACE_TOO_SMALL", -6: "KVD_ERR_DEVICE_OOB",
+    -4: "KVD_ERR_TIMEOUT", -5: "KVD_ERR_WORKSPACE_TOO_SMALL", -6: "KVD_ERR_DEVICE_OOB", -7: "KVD_ERR_DEVICE_STATE",
 }
 OP = {"gqa": 0, "swa": 1, "mla": 2, "dsa_topk": 3, "mla_sparse": 4}
 

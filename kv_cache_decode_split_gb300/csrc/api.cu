@@ -84,27 +84,40 @@ int make_tmap_bf16_blocked(CUtensorMap* map, const void* base, uint64_t rows, ui
     return r == CUDA_SUCCESS ? KVD_OK : KVD_ERR_CUDA;
 }
 
-// Split plan. The bf16 kernel is persistent (one CTA per SM pulling work items from a
-// queue), so the chunk length trades load balance (more, shorter items) against the
-// per-item merge cost: aim for about six items per SM, at least four 64-token tiles each.
+// Split plan. Every (sequence, group of KV heads, head block, chunk) is one CTA, two
+// CTAs per SM for bf16. A CTA pays a fixed start-up (barrier set-up, block-table read,
+// first TMA round trip) and a merge, and a second wave of CTAs pays them again, so:
+//  * few groups (at most half the CTA slots): cut the visible range into as many chunks
+//    as fit the slots in one wave;
+//  * many groups: four chunks of the longest visible range, so that ragged lengths still
+//    spread over the SMs.
+// Measured on the Llama-3-8B-shaped and sliding-window workloads (chunk sweeps).
 int gqa_plan(int B, int Hq, int Hkv, int D, int page_size, int max_len, int window, int n_sink,
              int dtype, GqaPlan* plan) {
     const int G = Hq / Hkv;
     plan->NHG = cdiv(G, 16);
     plan->units = B * Hkv * plan->NHG;
+    // two KV heads per tile when a 64-dim page fits one TMA box twice (16 KB per copy)
+    plan->hpt = (dtype == KVD_BF16 && D == 64 && Hkv % 2 == 0 && G <= 8 && page_size <= 64)
+                    ? 2
+                    : 1;
+    const long long groups = static_cast<long long>(B) * (Hkv / plan->hpt) * plan->NHG;
     const long long vis = window > 0 ? std::min<long long>(max_len, (long long)window + n_sink)
                                      : max_len;
-    const long long target = (dtype == KVD_F32) ? 8LL * num_sms() : 6LL * num_sms();
-    long long chunk = (static_cast<long long>(plan->units) * vis) / std::max(1LL, target);
-    chunk = std::max(256LL, std::min(8192LL, (chunk / 64) * 64));
-    if (dtype == KVD_F32) chunk = std::max(128LL, std::min(chunk, 1024LL));
+    long long chunk;
+    if (dtype == KVD_F32) {
+        chunk = (groups * vis) / std::max(1LL, 16LL * num_sms());
+        chunk = std::max(128LL, std::min(1024LL, (chunk / 64) * 64));
+    } else {
+        const long long slots = 2LL * num_sms();
+        const long long per_group = 2 * groups <= slots ? slots / groups : 4;
+        chunk = std::max(256LL, (vis + per_group - 1) / per_group);
+        chunk = (chunk + 63) / 64 * 64;
+    }
     if (const char* env = std::getenv("KVD_GQA_CHUNK")) {  // tuning override (tokens)
         const long long c = std::atoll(env);
         if (c >= 64) chunk = (c / 64) * 64;
     }
-    // a chunk's page pieces must fit one item descriptor
-    const long long box_rows = std::min(page_size, 64);
-    chunk = std::min(chunk, kGqaMaxBoxesPerItem * box_rows);
     auto chunks_for = [&](long long C) -> int {
         if (window <= 0) return cdiv(max_len, C);
         const int a = (n_sink > 0 ? cdiv(std::min(n_sink, max_len), C) : 0) +
@@ -113,12 +126,11 @@ int gqa_plan(int B, int Hq, int Hkv, int D, int page_size, int max_len, int wind
         return std::max(a, m);
     };
     while (chunks_for(chunk) > kGqaMaxChunks) chunk += 64;
-    if (chunk > kGqaMaxBoxesPerItem * box_rows) return KVD_ERR_UNSUPPORTED;  // too long
     plan->chunk = static_cast<int>(chunk);
     plan->max_chunks = std::max(1, chunks_for(chunk));
     size_t off = kWsHeaderBytes;
     plan->off_counters = off;
-    off = round256(off + sizeof(int) * (plan->units + 2));
+    off = round256(off + sizeof(int) * plan->units);
     plan->off_lse = off;
     off = round256(off + sizeof(float) * (size_t)plan->units * plan->max_chunks * 16);
     plan->off_o = off;
@@ -287,7 +299,7 @@ int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t
     if (dtype == KVD_F32) return gqa_launch(plan, p, nullptr, nullptr, stream);
     CUtensorMap tk, tv;
     const uint64_t rows = (uint64_t)num_pages * Hkv * page_size;
-    const uint32_t box_rows = page_size < 64 ? page_size : 64;
+    const uint32_t box_rows = (page_size < 64 ? page_size : 64) * plan.hpt;
     if (make_tmap_bf16_blocked(&tk, k_pool, rows, D, box_rows, D / 64) != KVD_OK)
         return KVD_ERR_CUDA;
     if (make_tmap_bf16_blocked(&tv, v_pool, rows, D, box_rows, D / 64) != KVD_OK)
@@ -480,6 +492,7 @@ const char* kvd_status_string(int status) {
         case KVD_ERR_TIMEOUT: return "device wait timed out";
         case KVD_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
         case KVD_ERR_DEVICE_OOB: return "page index or sequence length out of range";
+        case KVD_ERR_DEVICE_STATE: return "workspace not in its zeroed state";
         default: return "unknown status";
     }
 }

@@ -362,8 +362,19 @@ __global__ void __launch_bounds__(256) topk_filter_kernel(const TopkParams p) {
         sel_base = __shfl_sync(0xffffffffu, sel_base, 0);
         cand_base = __shfl_sync(0xffffffffu, cand_base, 0);
         const unsigned lower = (1u << lane) - 1u;
-        if (bk > b1) sel[sel_base + __popc(m_sel & lower)] = t;
-        if (bk == b1) cand[cand_base + __popc(m_cand & lower)] = t;
+        // a zeroed workspace keeps both lists inside their buffers (fewer than k tokens lie
+        // above the k-th's bucket); counters left non-zero by other kernels must not write
+        // outside them
+        if (bk > b1) {
+            const int si = sel_base + __popc(m_sel & lower);
+            if (si >= 0 && si < p.k) sel[si] = t;
+            else record_error(p.err, KVD_ERR_DEVICE_STATE);
+        }
+        if (bk == b1) {
+            const int ci = cand_base + __popc(m_cand & lower);
+            if (ci >= 0 && ci < p.max_len) cand[ci] = t;
+            else record_error(p.err, KVD_ERR_DEVICE_STATE);
+        }
     }
 }
 
@@ -398,7 +409,12 @@ __global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkPa
         __syncthreads();
         int b1, above, in_b;
         find_bucket<kFinThreads>(h, kHistBins, p.k, b1, above, in_b, tmp);
-        const int nc = p.counts[2 * b + 1];
+        int nc = p.counts[2 * b + 1];
+        if (nc < 0 || nc > L || above < 0 || above >= p.k) {  // not a zeroed workspace
+            if (tid == 0) record_error(p.err, KVD_ERR_DEVICE_STATE);
+            nc = min(max(nc, 0), L);
+            above = min(max(above, 0), p.k - 1);
+        }
         int need = p.k - above;  // to take from the candidates (>= 1)
         // radix passes over the 64-bit composite key below its top 11 bits, until the
         // bucket that holds the threshold holds exactly the keys still needed
@@ -412,6 +428,7 @@ __global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkPa
             __syncthreads();
             for (int i = tid; i < nc; i += kFinThreads) {
                 const int t = cand[i];
+                if (t < 0 || t >= L) continue;  // only after a non-zeroed workspace
                 const uint64_t ck = composite_key(sc[t], t);
                 if ((ck >> (64 - done_bits)) == prefix)
                     atomicAdd(&h[static_cast<int>((ck >> shift) & (nb - 1))], 1u);
@@ -427,11 +444,12 @@ __global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkPa
         const uint64_t T = done_bits < 64 ? prefix << (64 - done_bits) : prefix;
         for (int i = tid; i < above; i += kFinThreads) {
             const int t = sel[i];
-            atomicOr(bits + (t >> 5), 1u << (t & 31));
+            if (t >= 0 && t < L) atomicOr(bits + (t >> 5), 1u << (t & 31));
         }
         for (int i = tid; i < nc; i += kFinThreads) {
             const int t = cand[i];
-            if (composite_key(sc[t], t) >= T) atomicOr(bits + (t >> 5), 1u << (t & 31));
+            if (t >= 0 && t < L && composite_key(sc[t], t) >= T)
+                atomicOr(bits + (t >> 5), 1u << (t & 31));
         }
         __threadfence();  // the bit updates land in L2 before the words are read back
         __syncthreads();

@@ -14,7 +14,6 @@ namespace kvd {
 constexpr size_t kWsHeaderBytes = 256;
 
 constexpr int kGqaMaxChunks = 256;  // split-KV chunks per (sequence, KV head, head block)
-constexpr int kGqaMaxBoxesPerItem = 64;  // TMA boxes (page pieces of <= 64 tokens) per chunk
 
 // Kernel arguments of the GQA / SWA decode (one struct for both dtypes).
 struct GqaParams {
@@ -28,7 +27,7 @@ struct GqaParams {
     const float* sink_logit;
     float* part_o;    // [units, max_chunks, 16, D]
     float* part_lse;  // [units, max_chunks, 16]   (log2 domain)
-    int* counters;    // [units] completion counters, then the work queue head and exit count
+    int* counters;    // [units] completion counters (zero between calls)
     int* err;         // workspace error flag
     int B, Hq, Hkv, D, G, NHG, units;
     int page_size, max_pages, num_pages, max_len;
@@ -41,7 +40,8 @@ struct GqaParams {
 // Host-side split plan and workspace layout of one GQA / SWA call.
 struct GqaPlan {
     int chunk;       // tokens per split (multiple of 64)
-    int max_chunks;  // chunk slots per unit (work items = units * max_chunks)
+    int max_chunks;  // chunk slots per unit (grid.x)
+    int hpt;         // KV heads per K/V tile (2: D = 64 pages of <= 64 tokens, G <= 8)
     int NHG;         // head blocks of <= 16 query heads per KV head
     int units;       // B * Hkv * NHG
     size_t off_counters, off_lse, off_o, total;

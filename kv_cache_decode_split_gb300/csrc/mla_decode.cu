@@ -219,12 +219,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_commit(&sm.pvdone);
                 tc_commit(&sm.empty[s]);
             };
+            // The softmax warps read score tile j + 1 (and send it to the partner) before
+            // they finish tile j, so the score product runs two tiles ahead of the value
+            // product: tile j + 2's scores are issued as soon as tile j + 1's have been read,
+            // and overlap the exchange and softmax of tile j.
             qk(0);
-            for (int i = 1; i < n_tiles; ++i) {
-                qk(i);
-                pv(i - 1);
+            if (n_tiles > 1) qk(1);
+            for (int j = 0; j < n_tiles; ++j) {
+                if (j + 2 < n_tiles) qk(j + 2);
+                pv(j);
             }
-            pv(n_tiles - 1);
             tc_commit(&sm.ofinal);
             mbar_wait(&sm.ofinal, 0, p.err);  // every MMA of this CTA has completed
         }
@@ -234,14 +238,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         {
             // this CTA's query slice into TMEM (the A operand of the score product)
-            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+            const uint4* qrow = reinterpret_cast<const uint4*>(
                 reinterpret_cast<const __nv_bfloat16*>(p.q) + (static_cast<size_t>(b) * kH + h) * kDqk +
                 dim0);
-            for (int c = 0; c < nbox * 32; c += 32) {
-                uint32_t r[32];
+            // 64 dims (32 columns) per box; the loads of up to three boxes are in flight at once
+            for (int c0 = 0; c0 < nbox; c0 += 3) {
+                uint4 v[3][8];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = __ldg(qrow + c + j);
-                tmem_st_32x32b_x32(trow + kColQ + c, r);
+                for (int bx = 0; bx < 3; ++bx)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (c0 + bx < nbox) v[bx][j] = __ldg(qrow + (c0 + bx) * 8 + j);
+#pragma unroll
+                for (int bx = 0; bx < 3; ++bx) {
+                    if (c0 + bx >= nbox) break;
+                    uint32_t r[32];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        r[4 * j] = v[bx][j].x;
+                        r[4 * j + 1] = v[bx][j].y;
+                        r[4 * j + 2] = v[bx][j].z;
+                        r[4 * j + 3] = v[bx][j].w;
+                    }
+                    tmem_st_32x32b_x32(trow + kColQ + (c0 + bx) * 32, r);
+                }
             }
             tmem_st_wait();
             tc_fence_before();

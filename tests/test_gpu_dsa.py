@@ -125,3 +125,40 @@ def test_dsa_full_size_indexer_sampled(kvd):
         err = np.abs(sc[b, :L] - ref[r, :L])
         assert err.max() <= 1e-4 * np.abs(ref[r, :L]).max() + 1e-3, err.max()
         _check_selection(idx[b], cnt[b], ref[r], L, x.k)
+
+
+def test_workspace_shared_with_mla(kvd):
+    # one Workspace object handed first to the MLA decode (which leaves its partials in the
+    # buffer) and then to the selection: the binding zero-fills it on the change of family
+    ws = kvd.Workspace("cuda")
+    xm = W.make_mla(2, 128, [300, 2000], page_size=64, seed=905)
+    kvd.attn_decode_mla(xm.q.cuda(), xm.c_pool.cuda(), xm.block_table.cuda(),
+                        xm.seq_lens.cuda(), scale=xm.scale, workspace=ws)
+    s = W.normal((2, 20000), 906, 1.0, torch.float32)
+    lens = torch.tensor([20000, 9000], dtype=torch.int32)
+    idx, cnt = kvd.dsa_topk(s.cuda(), lens.cuda(), k=2048, workspace=ws)
+    assert kvd.kvd_check_device_error(ws) == 0
+    for b in range(2):
+        L = int(lens[b])
+        ref = oracle.topk(s[b, :L].numpy().astype(np.float64), 2048)
+        assert np.array_equal(idx[b].cpu().numpy(), ref)
+
+
+def test_topk_non_zeroed_workspace_is_reported(kvd):
+    # a raw workspace whose counters and histograms hold another kernel's data: the
+    # selection stays inside its buffers, records KVD_ERR_DEVICE_STATE and leaves its
+    # state zeroed, so that the next call is exact again
+    B, k = 2, 256
+    s = W.normal((B, 3000), 907, 1.0, torch.float32)
+    lens = torch.tensor([3000, 2000], dtype=torch.int32)
+    nbytes = kvd.kvd_workspace_size("dsa_topk", B, 1, max_len=3000, k=k)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")
+    ws[:256] = 0  # the error flag starts clear
+    kvd.dsa_topk(s.cuda(), lens.cuda(), k=k, workspace=ws)
+    assert kvd.kvd_check_device_error(ws) == -7
+    idx, cnt = kvd.dsa_topk(s.cuda(), lens.cuda(), k=k, workspace=ws)
+    assert kvd.kvd_check_device_error(ws) == 0
+    for b in range(B):
+        L = int(lens[b])
+        ref = oracle.topk(s[b, :L].numpy().astype(np.float64), k)
+        assert np.array_equal(idx[b].cpu().numpy(), ref)

@@ -70,10 +70,23 @@ def test_bf16_paged_ragged(kvd, D, hq, hkv):
     _compare(kvd, x)
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("P", [16, 32, 128, 256])
-def test_page_sizes(kvd, P):
+def test_page_sizes(kvd, P, D):
+    # D = 64 with an even KV-head count and pages of <= 64 tokens moves two KV heads per
+    # tile; larger pages split into 64-token pieces
     lens = [5, 130, 777]
-    x = W.make_gqa(3, 8, 2, 128, lens, page_size=P, shuffle=True, seed=200 + P)
+    x = W.make_gqa(3, 8, 2, D, lens, page_size=P, shuffle=True, seed=200 + P + D)
+    _compare(kvd, x)
+
+
+@pytest.mark.parametrize("chunk", [64, 192])
+@pytest.mark.parametrize("D", [64, 128])
+def test_many_chunks(kvd, monkeypatch, chunk, D):
+    # short chunks: up to 126 chunk partials per head block in the final combine
+    monkeypatch.setenv("KVD_GQA_CHUNK", str(chunk))
+    lens = [1, 100, 4000, 8000]
+    x = W.make_gqa(len(lens), 16, 4, D, lens, page_size=64, shuffle=True, seed=400 + chunk + D)
     _compare(kvd, x)
 
 
