@@ -401,6 +401,30 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
                  : "memory");
 }
 
+// Bulk copy of `bytes` from this CTA's shared memory to another CTA's (cluster address),
+// completing on the destination's mbarrier; tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void* src,
+                                                  uint32_t bytes, uint32_t dst_bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(dst_cluster),
+        "r"(smem_u32(src)), "r"(bytes), "r"(dst_bar_cluster)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until the issuing thread's bulk copies have finished reading their sources.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Remote arrive without release ordering: for "slot consumed" signals whose reads have
+// already returned (their values are in registers), so nothing needs to be made visible.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+                 : "memory");
+}
+
 // Wait with acquire at cluster scope (for barriers that remote CTAs arrive on).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;

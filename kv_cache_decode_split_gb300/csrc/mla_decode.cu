@@ -16,10 +16,14 @@
 //     distributed shared memory. Float addition is commutative, so both CTAs hold the
 //     bit-identical full tile and run the same online softmax.
 //   * Each CTA accumulates its half of the value dims, O_r += P V_r (tcgen05, M = 128,
-//     N = 256, K = 64 tokens; P in shared memory, V read MN-major from the same tile).
-// The running max is only raised (and O rescaled in TMEM) when it grows by more than 2^8,
-// so the common tile touches O only through the MMA. Splits are merged by log-sum-exp in
-// a small combine kernel.
+//     N = 256, K = 64 tokens; P in tensor memory, V read MN-major from the same tile).
+// The exchange (32 KB per tile each way) is the slowest step, so two groups of four softmax
+// warps take alternate tiles: while one group's partial scores drain to the partner, the
+// other group runs its softmax. The running max passes from group to group through shared
+// memory; it is only raised (and O rescaled in TMEM) when it grows by more than 2^8, so the
+// common tile touches O only through the MMA. Score and value products are issued by two
+// threads, so that a score product never waits behind a value product that waits for a
+// softmax. Splits are merged by log-sum-exp in a small combine kernel.
 
 #include <algorithm>
 
@@ -35,18 +39,31 @@ constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kTok = 64;              // tokens per tile
 constexpr int kNBox = 5;              // 64-dim boxes held per CTA (rank 0 uses 4)
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kTileBox = kTok * 128;  // 8 KB: 64 tokens x 64 dims
 constexpr int kStageBytes = kNBox * kTileBox;
-constexpr int kThreads = 6 * 32;      // warps 0-3 softmax, 4 loads, 5 MMA
+// warps 0-7: softmax (group = warp / 4 takes tiles of that parity, TMEM lane quarter =
+// warp % 4); warp 8: loads; warp 9: score products (and TMEM allocation); warp 10: value
+// products; warp 11: score exchange
+constexpr int kThreads = 12 * 32;
+constexpr int kWarpLoad = 8, kWarpQK = 9, kWarpPV = 10, kWarpX = 11;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct MlaSmem {
     uint8_t stage[kStages][kStageBytes];   // offset 0, 1024-aligned
-    float x[2][kH][kTok];                  // the partner's partial scores (float4-swizzled)
-    uint64_t full[kStages], empty[kStages], qready, sfull, sempty, xfull[2], peer_free[2], pfull,
-        pvdone, ofinal;
+    float x[2][kH][kTok];                  // the partner's partial scores, one slot per group
+                                           // (16-byte chunks XOR-ed with row % 16)
+    float y[kH][kTok];                     // this CTA's partial scores on their way out
+    float mref[2][kH];                     // running max after each group's latest tile
+    // Barriers waited by one group only exist once per group (tile parity), so that each
+    // waiter goes through its barrier's phases in order.
+    uint64_t full[kStages], empty[kStages], qready, sfull[2], sempty, pfull, pvdone[2], ofinal;
+    uint64_t xfull[2];       // the partner's partial of a tile has arrived in x[parity]
+    uint64_t xused[2];       // x[parity] has been read (four warps of that group)
+    uint64_t peer_free[2];   // the partner has read our previous partial in its x[parity]
+    uint64_t yfull, yfree[2];  // y written (four warps) / y read by the copy of a tile
+    uint64_t hand[2];        // group published its running max
     uint32_t tmem_base;
 };
 
@@ -57,6 +74,32 @@ constexpr int kMlaSmem = static_cast<int>(sizeof(MlaSmem)) + 1024;
 static_assert(kMlaSmem <= 227 * 1024, "MLA shared memory");
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
+
+// Score product of one tile: S (TMEM) = q_r (TMEM, NK 16-dim k-steps) x this CTA's
+// 64-dim boxes of the tile (shared memory, K-major). Fully unrolled with the descriptors
+// advanced by constants, so that one thread keeps the tensor pipe fed.
+template <int NK>
+__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t tile_addr) {
+    constexpr uint32_t idesc = idesc_bf16_f32(kH, kTok, 0, 0);
+    const uint64_t bd = sw128_kmajor_desc(tile_addr);
+#pragma unroll
+    for (int ks = 0; ks < NK; ++ks)
+        tc_mma_bf16_ts(tmem + kColS, tmem + kColQ + ks * 8,
+                       bd + static_cast<uint64_t>(((ks >> 2) * kTileBox + (ks & 3) * 32) >> 4),
+                       idesc, ks > 0 ? 1u : 0u);
+}
+
+// Value product of one tile: O_r (TMEM, 256 columns) += P (TMEM) x V_r, V_r being this
+// CTA's first four boxes of the tile read MN-major (16 tokens x 256 dims per k-step).
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t tile_addr, bool accumulate) {
+    constexpr uint32_t idesc = idesc_bf16_f32(kH, 256, 0, 1);
+    const uint64_t bd = sw128_mnmajor_desc(tile_addr, kTileBox);
+#pragma unroll
+    for (int ks = 0; ks < kTok / 16; ++ks)
+        tc_mma_bf16_ts(tmem + kColO, tmem + kColP + ks * 8,
+                       bd + static_cast<uint64_t>((ks * 16 * 128) >> 4), idesc,
+                       (accumulate || ks > 0) ? 1u : 0u);
+}
 
 template <bool kSparse>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -81,32 +124,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int nbox = rank == 0 ? 4 : 5;   // 64-dim boxes this CTA loads
     const int dim0 = rank == 0 ? 0 : 256;
     const CUtensorMap& tmC = rank == 0 ? tmC0 : tmC1;  // 3-D maps with 4 / 5 blocks per box
+    constexpr uint32_t kXBytes = kH * kTok * 4;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.full[s], kSparse ? 32 : 1);
             mbar_init(&sm.empty[s], 1);
         }
-        mbar_init(&sm.qready, 4);
-        mbar_init(&sm.sfull, 1);
-        mbar_init(&sm.sempty, 4);
+        mbar_init(&sm.qready, 8);
+        mbar_init(&sm.sempty, 4);  // the four warps of the group that owns the tile
         mbar_init(&sm.pfull, 4);
-        mbar_init(&sm.pvdone, 1);
+        mbar_init(&sm.yfull, 4);
         for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.sfull[i], 1);
+            mbar_init(&sm.pvdone[i], 1);
             mbar_init(&sm.xfull[i], 1);      // armed with the exchanged byte count each tile
-            mbar_init(&sm.peer_free[i], 4);  // one arrive per softmax warp of the partner
+            mbar_init(&sm.xused[i], 4);
+            mbar_init(&sm.peer_free[i], 1);  // remote arrive by the partner's exchange thread
+            mbar_init(&sm.yfree[i], 1);
+            mbar_init(&sm.hand[i], 4);
         }
         mbar_init(&sm.ofinal, 1);
         fence_mbar_init();
+        // the partner's partial scores of tiles 0 and 1 (later tiles: armed by the group
+        // once the slot's previous phase has completed)
+        for (int i = 0; i < 2 && i < n_tiles; ++i) mbar_arrive_expect_tx(&sm.xfull[i], kXBytes);
     }
-    if (warp == 5) tmem_alloc(&sm.tmem_base, 512);
+    if (warp == kWarpQK) tmem_alloc(&sm.tmem_base, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     cluster_sync();  // the partner's barriers exist before anyone signals them
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == 4) {
+    if (warp == kWarpLoad) {
         // ------------------------------------------------------------------ loads
         if (!kSparse) {
             if (lane == 0) {
@@ -183,190 +234,209 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 cp_async_wait<0>();
             }
         }
-    } else if (warp == 5) {
-        // ------------------------------------------------------------------ MMA issuer
+    } else if (warp == kWarpQK) {
+        // ------------------------------------------------------------------ score products
+        // Tile j's product starts as soon as its data is in and tile j - 1's scores have been
+        // read, independently of the value products.
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kH, kTok, 0, 0);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kH, 256, 0, 1);
-            const int nk = nbox * 4;  // 16-dim k-steps of the score product
             bool ok = mbar_wait(&sm.qready, 0, p.err);
-            auto qk = [&](int i) {
-                const int s = i % kStages;
-                ok = ok && mbar_wait(&sm.full[s], (i / kStages) & 1, p.err);
-                ok = ok && mbar_wait(&sm.sempty, (i & 1) ^ 1, p.err);
-                if (!ok) return;
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int s = j % kStages;
+                ok = mbar_wait(&sm.full[s], (j / kStages) & 1, p.err) &&
+                     mbar_wait(&sm.sempty, (j & 1) ^ 1, p.err);
+                if (!ok) break;
                 tc_fence_after();
-                const uint32_t ca = smem_u32(sm.stage[s]);
-                for (int ks = 0; ks < nk; ++ks) {
-                    const uint64_t bd =
-                        sw128_kmajor_desc(ca + (ks >> 2) * kTileBox + (ks & 3) * 32);
-                    tc_mma_bf16_ts(tmem + kColS, tmem + kColQ + ks * 8, bd, idesc_qk,
-                                   ks > 0 ? 1u : 0u);
-                }
-                tc_commit(&sm.sfull);
-            };
-            auto pv = [&](int i) {
-                const int s = i % kStages;
-                ok = ok && mbar_wait(&sm.pfull, i & 1, p.err);
-                if (!ok) return;
+                if (nbox == 4)
+                    issue_qk<16>(tmem, smem_u32(sm.stage[s]));
+                else
+                    issue_qk<20>(tmem, smem_u32(sm.stage[s]));
+                tc_commit(&sm.sfull[j & 1]);
+            }
+        }
+    } else if (warp == kWarpPV) {
+        // ------------------------------------------------------------------ value products
+        if (lane == 0) {
+            bool ok = true;
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int s = j % kStages;
+                if (!(ok = mbar_wait(&sm.pfull, j & 1, p.err))) break;
                 tc_fence_after();
-                const uint32_t va = smem_u32(sm.stage[s]);
-                for (int ks = 0; ks < kTok / 16; ++ks) {
-                    const uint64_t bd = sw128_mnmajor_desc(va + ks * 16 * 128, kTileBox);
-                    tc_mma_bf16_ts(tmem + kColO, tmem + kColP + ks * 8, bd, idesc_pv,
-                                   (i > 0 || ks > 0) ? 1u : 0u);
-                }
-                tc_commit(&sm.pvdone);
-                tc_commit(&sm.empty[s]);
-            };
-            // The softmax warps read score tile j + 1 (and send it to the partner) before
-            // they finish tile j, so the score product runs two tiles ahead of the value
-            // product: tile j + 2's scores are issued as soon as tile j + 1's have been read,
-            // and overlap the exchange and softmax of tile j.
-            qk(0);
-            if (n_tiles > 1) qk(1);
-            for (int j = 0; j < n_tiles; ++j) {
-                if (j + 2 < n_tiles) qk(j + 2);
-                pv(j);
+                issue_pv(tmem, smem_u32(sm.stage[s]), j > 0);
+                tc_commit(&sm.pvdone[j & 1]);
+                tc_commit(&sm.empty[s]);  // the tile's score product completed before its P
             }
             tc_commit(&sm.ofinal);
-            mbar_wait(&sm.ofinal, 0, p.err);  // every MMA of this CTA has completed
+            mbar_wait(&sm.ofinal, 0, p.err);  // every value product of this CTA has completed
+        }
+    } else if (warp == kWarpX) {
+        // ------------------------------------------------------------------ score exchange
+        // One bulk copy per tile moves this CTA's partial scores (staged in y by the tile's
+        // group) into the partner's slot for that tile's parity. The copies drain over
+        // distributed shared memory at its own rate, off the softmax warps' instruction path.
+        if (lane == 0) {
+            uint32_t peer_x[2], peer_xfull[2], peer_free[2];
+            for (int i = 0; i < 2; ++i) {
+                peer_x[i] = map_peer(smem_u32(&sm.x[i][0][0]), peer);
+                peer_xfull[i] = map_peer(smem_u32(&sm.xfull[i]), peer);
+                peer_free[i] = map_peer(smem_u32(&sm.peer_free[i]), peer);
+            }
+            for (int j = 0; j < n_tiles; ++j) {
+                const int xb = j & 1;
+                // our x[xb] has been read for tile j - 2: the partner may send tile j into it
+                if (j >= 2) {
+                    if (!mbar_wait(&sm.xused[xb], ((j - 2) >> 1) & 1, p.err)) break;
+                    mbar_arrive_remote_relaxed(peer_free[xb]);
+                }
+                if (!mbar_wait(&sm.yfull, j & 1, p.err)) break;
+                if (!mbar_wait_cluster(&sm.peer_free[xb], ((j >> 1) & 1) ^ 1, p.err)) break;
+                bulk_copy_to_peer(peer_x[xb], &sm.y[0][0], kXBytes, peer_xfull[xb]);
+                bulk_wait_read_all();
+                mbar_arrive(&sm.yfree[xb]);
+            }
         }
     } else {
         // ------------------------------------------------------------------ softmax
-        const int h = threadIdx.x;  // head = TMEM lane
-        const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const int grp = warp >> 2;                 // takes tiles j with j % 2 == grp
+        const int h = (warp & 3) * 32 + lane;      // head = TMEM lane
+        const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         {
-            // this CTA's query slice into TMEM (the A operand of the score product)
+            // this CTA's query slice into TMEM (the A operand of the score product): group 0
+            // boxes 0-2, group 1 the rest
             const uint4* qrow = reinterpret_cast<const uint4*>(
                 reinterpret_cast<const __nv_bfloat16*>(p.q) + (static_cast<size_t>(b) * kH + h) * kDqk +
                 dim0);
-            // 64 dims (32 columns) per box; the loads of up to three boxes are in flight at once
-            for (int c0 = 0; c0 < nbox; c0 += 3) {
-                uint4 v[3][8];
+            const int bx0 = grp == 0 ? 0 : 3, bx1 = grp == 0 ? 3 : nbox;
+            uint4 v[3][8];
 #pragma unroll
-                for (int bx = 0; bx < 3; ++bx)
+            for (int k = 0; k < 3; ++k)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (c0 + bx < nbox) v[bx][j] = __ldg(qrow + (c0 + bx) * 8 + j);
+                for (int j = 0; j < 8; ++j)
+                    if (bx0 + k < bx1) v[k][j] = __ldg(qrow + (bx0 + k) * 8 + j);
 #pragma unroll
-                for (int bx = 0; bx < 3; ++bx) {
-                    if (c0 + bx >= nbox) break;
-                    uint32_t r[32];
+            for (int k = 0; k < 3; ++k) {
+                if (bx0 + k >= bx1) break;
+                uint32_t r[32];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        r[4 * j] = v[bx][j].x;
-                        r[4 * j + 1] = v[bx][j].y;
-                        r[4 * j + 2] = v[bx][j].z;
-                        r[4 * j + 3] = v[bx][j].w;
-                    }
-                    tmem_st_32x32b_x32(trow + kColQ + (c0 + bx) * 32, r);
+                for (int j = 0; j < 8; ++j) {
+                    r[4 * j] = v[k][j].x;
+                    r[4 * j + 1] = v[k][j].y;
+                    r[4 * j + 2] = v[k][j].z;
+                    r[4 * j + 3] = v[k][j].w;
                 }
+                tmem_st_32x32b_x32(trow + kColQ + (bx0 + k) * 32, r);
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.qready);
         }
-        // Tile j's partial score row is read (freeing the score tile for the next product)
-        // and sent to the partner one tile ahead of combining tile j - 1, so the exchange
-        // latency overlaps the previous tile's softmax.
-        const uint32_t peer_x0 = map_peer(smem_u32(&sm.x[0][h][0]), peer);
-        const uint32_t peer_x1 = map_peer(smem_u32(&sm.x[1][h][0]), peer);
-        const uint32_t peer_xfull0 = map_peer(smem_u32(&sm.xfull[0]), peer);
-        const uint32_t peer_xfull1 = map_peer(smem_u32(&sm.xfull[1]), peer);
-        const uint32_t peer_free0 = map_peer(smem_u32(&sm.peer_free[0]), peer);
-        const uint32_t peer_free1 = map_peer(smem_u32(&sm.peer_free[1]), peer);
         const float sl2 = p.scale_log2;
-        float m_ref = neg_inf(), l = 0.f;
+        float l = 0.f, m_l = neg_inf();  // this group's sum of P, relative to 2^m_l
+        float m_last = neg_inf();        // running max after this group's latest tile
         bool ok = true;
-        auto send = [&](int j, float (&s)[kTok]) -> bool {
-            const int xb = j & 1;
-            if (!mbar_wait(&sm.sfull, j & 1, p.err)) return false;
+        for (int j = grp; j < n_tiles && ok; j += 2) {
+            const int it = j >> 1;  // this group's iteration
+            // 1. this CTA's partial scores; reading them frees S for tile j + 1's product
+            if (!(ok = mbar_wait(&sm.sfull[grp], it & 1, p.err))) break;
             tc_fence_after();
+            float s[kTok];
             {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(trow + kColS, r);
-                tmem_ld_wait(r);
+                uint32_t r0[32], r1[32];
+                tmem_ld_32x32b_x32(trow + kColS, r0);
+                tmem_ld_32x32b_x32(trow + kColS + 32, r1);
+                tmem_ld_wait(r0);
+                tmem_ld_wait(r1);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(r[c]);
-                tmem_ld_32x32b_x32(trow + kColS + 32, r);
-                tmem_ld_wait(r);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) s[32 + c] = __uint_as_float(r[c]);
+                for (int c = 0; c < 32; ++c) {
+                    s[c] = __uint_as_float(r0[c]);
+                    s[32 + c] = __uint_as_float(r1[c]);
+                }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.sempty);  // the score tile may be overwritten
-            if (h == 0) mbar_arrive_expect_tx(&sm.xfull[xb], kH * kTok * 4);
-            if (!mbar_wait_cluster(&sm.peer_free[xb], ((j >> 1) & 1) ^ 1, p.err)) return false;
-            const uint32_t px = xb ? peer_x1 : peer_x0;
-            const uint32_t pf = xb ? peer_xfull1 : peer_xfull0;
+            if (lane == 0) mbar_arrive(&sm.sempty);
+            // 2. stage them for the exchange thread once tile j - 1's copy has read y
+            if (j >= 1 && !(ok = mbar_wait(&sm.yfree[grp ^ 1], ((j - 1) >> 1) & 1, p.err))) break;
 #pragma unroll
             for (int c4 = 0; c4 < kTok / 4; ++c4)
-                st_async_v4(px + ((c4 ^ (h & 15)) << 4), s[4 * c4], s[4 * c4 + 1], s[4 * c4 + 2],
-                            s[4 * c4 + 3], pf);
-            return true;
-        };
-        float s[kTok];
-        ok = send(0, s);
-        for (int i = 0; i < n_tiles && ok; ++i) {
-            float sn[kTok];
-            if (i + 1 < n_tiles && !(ok = send(i + 1, sn))) break;
-            const int xb = i & 1;
-            if (!(ok = mbar_wait_cluster(&sm.xfull[xb], (i >> 1) & 1, p.err))) break;
+                *reinterpret_cast<float4*>(&sm.y[h][(c4 ^ (h & 15)) * 4]) =
+                    make_float4(s[4 * c4], s[4 * c4 + 1], s[4 * c4 + 2], s[4 * c4 + 3]);
+            fence_proxy_async_smem();  // generic stores before the bulk copy reads them
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.yfull);
+            // 3. the partner's partial
+            if (!(ok = mbar_wait_cluster(&sm.xfull[grp], it & 1, p.err))) break;
 #pragma unroll
             for (int c4 = 0; c4 < kTok / 4; ++c4) {
-                const float4 v = *reinterpret_cast<const float4*>(&sm.x[xb][h][(c4 ^ (h & 15)) * 4]);
+                const float4 v = *reinterpret_cast<const float4*>(&sm.x[grp][h][(c4 ^ (h & 15)) * 4]);
                 s[4 * c4] += v.x;
                 s[4 * c4 + 1] += v.y;
                 s[4 * c4 + 2] += v.z;
                 s[4 * c4 + 3] += v.w;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(xb ? peer_free1 : peer_free0);  // slot read
-            // online softmax in log2 units, lazily rescaled
-            const int T0 = lo + i * kTok;
+            if (lane == 0) mbar_arrive(&sm.xused[grp]);
+            // the slot's phase is complete: arm it for this group's next tile
+            if (warp == 4 * grp && lane == 0 && j + 2 < n_tiles)
+                mbar_arrive_expect_tx(&sm.xfull[grp], kXBytes);
+            // 4. tile max, then the running max handed over from tile j - 1
+            const int T0 = lo + j * kTok;
             float mt = neg_inf();
 #pragma unroll
-            for (int j = 0; j < kTok; ++j) {
-                s[j] = (T0 + j < hi) ? s[j] * sl2 : neg_inf();
-                mt = fmaxf(mt, s[j]);
+            for (int c = 0; c < kTok; ++c) {
+                s[c] = (T0 + c < hi) ? s[c] * sl2 : neg_inf();
+                mt = fmaxf(mt, s[c]);
             }
+            float m_prev = neg_inf();
+            if (j >= 1) {
+                if (!(ok = mbar_wait(&sm.hand[grp ^ 1], ((j - 1) >> 1) & 1, p.err))) break;
+                m_prev = sm.mref[grp ^ 1][h];
+            }
+            // raise the reference only on the first tile or when the max grows by > 2^8
+            float m_new = m_prev;
             bool resc = false;
-            float alpha = 1.f;
-            if (mt > m_ref) {
-                if (m_ref == neg_inf()) {
-                    m_ref = mt;
-                } else if (mt > m_ref + kRescaleThreshold) {
-                    alpha = fast_exp2(m_ref - mt);
-                    m_ref = mt;
-                    l *= alpha;
+            if (mt > m_prev) {
+                if (m_prev == neg_inf()) {
+                    m_new = mt;
+                } else if (mt > m_prev + kRescaleThreshold) {
+                    m_new = mt;
                     resc = true;
                 }
             }
-            const float mu = m_ref == neg_inf() ? 0.f : m_ref;
+            sm.mref[grp][h] = m_new;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.hand[grp]);
+            m_last = m_new;
+            // 5. P relative to 2^m_new, and this group's running sum moved to that reference
+            if (m_new != m_l) {
+                if (l > 0.f) l *= fast_exp2(m_l - m_new);
+                m_l = m_new;
+            }
+            const float mu = m_new == neg_inf() ? 0.f : m_new;
             uint32_t pk[kTok / 2];
             float psum = 0.f;
 #pragma unroll
-            for (int j = 0; j < kTok / 2; ++j) {
+            for (int c = 0; c < kTok / 2; ++c) {
                 const __nv_bfloat162 v =
-                    __floats2bfloat162_rn(fast_exp2(s[2 * j] - mu), fast_exp2(s[2 * j + 1] - mu));
+                    __floats2bfloat162_rn(fast_exp2(s[2 * c] - mu), fast_exp2(s[2 * c + 1] - mu));
                 const float2 f = __bfloat1622float2(v);
                 psum += f.x + f.y;
-                pk[j] = *reinterpret_cast<const uint32_t*>(&v);
+                pk[c] = *reinterpret_cast<const uint32_t*>(&v);
             }
             l += psum;
-            // the P tile (and O) are free once tile i - 1's value product has completed
-            if (i >= 1 && !(ok = mbar_wait(&sm.pvdone, (i - 1) & 1, p.err))) break;
+            // 6. P (and O) are free once tile j - 1's value product has completed
+            if (j >= 1 && !(ok = mbar_wait(&sm.pvdone[grp ^ 1], ((j - 1) >> 1) & 1, p.err))) break;
             tc_fence_after();
             if (__any_sync(0xffffffffu, resc)) {
+                // rare: O was accumulated relative to 2^m_prev
+                const float alpha = resc ? fast_exp2(m_prev - m_new) : 1.f;
+#pragma unroll 1
                 for (int c = 0; c < 8; ++c) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(trow + kColO + c * 32, r);
                     tmem_ld_wait(r);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+                    for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
                     tmem_st_32x32b_x32(trow + kColO + c * 32, r);
                 }
             }
@@ -375,34 +445,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.pfull);
-#pragma unroll
-            for (int j = 0; j < kTok; ++j) s[j] = sn[j];
         }
-        // the split's partial: O / l for this CTA's 256 value dims, and log2-sum-exp
+        // the split's partial: O / l for this CTA's 256 value dims, and log2-sum-exp. The
+        // final reference is the running max after the last tile.
+        const int jl = n_tiles - 1;
+        if (ok && (jl & 1) != grp) {
+            ok = mbar_wait(&sm.hand[grp ^ 1], (jl >> 1) & 1, p.err);
+            if (ok) m_last = sm.mref[grp ^ 1][h];
+        }
+        // both groups' sums relative to 2^m_last, added through shared memory (the exchange
+        // slots are no longer written by the partner once its last partial has arrived)
+        float* lsum = &sm.x[0][0][0];
+        lsum[grp * kH + h] = (l > 0.f) ? l * fast_exp2(m_l - m_last) : 0.f;
+        asm volatile("bar.sync 1, %0;" ::"r"(8 * 32) : "memory");
+        const float l_tot = lsum[h] + lsum[kH + h];
         if (ok && mbar_wait(&sm.ofinal, 0, p.err)) {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
             float* po = p.part_o + (static_cast<size_t>(unit) * kH + h) * kDv + rank * 256;
-            for (int c = 0; c < 8; ++c) {
+            // group g writes value dims 128 g .. 128 g + 127 of this CTA's half
+            for (int c = 4 * grp; c < 4 * grp + 4; ++c) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(trow + kColO + c * 32, r);
                 tmem_ld_wait(r);
 #pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    __stcg(reinterpret_cast<float4*>(po + c * 32 + j),
-                           make_float4(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv,
-                                       __uint_as_float(r[j + 2]) * inv,
-                                       __uint_as_float(r[j + 3]) * inv));
+                for (int k = 0; k < 32; k += 4)
+                    __stcg(reinterpret_cast<float4*>(po + c * 32 + k),
+                           make_float4(__uint_as_float(r[k]) * inv, __uint_as_float(r[k + 1]) * inv,
+                                       __uint_as_float(r[k + 2]) * inv,
+                                       __uint_as_float(r[k + 3]) * inv));
             }
-            if (rank == 0)
-                p.part_lse[static_cast<size_t>(unit) * kH + h] = l > 0.f ? m_ref + log2f(l) : neg_inf();
+            if (rank == 0 && grp == 0)
+                p.part_lse[static_cast<size_t>(unit) * kH + h] =
+                    l_tot > 0.f ? m_last + log2f(l_tot) : neg_inf();
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     cluster_sync();  // the partner is done with this CTA's shared memory
-    if (warp == 5) tmem_dealloc(tmem, 512);
+    if (warp == kWarpQK) tmem_dealloc(tmem, 512);
 }
 
 // Merge the splits of each (sequence, head): o = sum_s 2^{lse_s - M} o_s / sum_s 2^{lse_s - M}.
