@@ -161,21 +161,16 @@ TopkLayout topk_layout(int B, int max_len, int k, bool with_scores) {
 // MLA split plan: dense units are (sequence, token chunk), about three per SM pair;
 // sparse units are (sequence, chunk of the index list), about one per SM pair.
 MlaPlan mla_plan(int B, int max_items, bool sparse) {
+    (void)sparse;
     MlaPlan pl;
-    const long long clusters = std::max(1, num_sms() / 2);
-    const long long target = sparse ? clusters : 3 * clusters;
-    long long chunk = ((long long)B * max_items + target - 1) / target;
-    chunk = ((chunk + 63) / 64) * 64;
-    chunk = std::max<long long>(sparse ? 64 : 256, chunk);
-    chunk = std::min<long long>(chunk, ((max_items + 63) / 64) * 64);
-    pl.chunk = static_cast<int>(std::max(64LL, chunk));
-    pl.n_splits = cdiv(max_items, pl.chunk);
-    const size_t units = (size_t)B * pl.n_splits;
+    const long long max_tiles = (long long)B * ((max_items + 63) / 64);
+    pl.n_clusters = static_cast<int>(std::max(1LL, std::min<long long>(num_sms() / 2, max_tiles)));
+    const size_t slots = (size_t)pl.n_clusters + B - 1;
     size_t off = kWsHeaderBytes;
     pl.off_lse = off;
-    off = round256(off + sizeof(float) * units * 128);
+    off = round256(off + sizeof(float) * slots * 128);
     pl.off_o = off;
-    off = round256(off + sizeof(float) * units * 128 * 512);
+    off = round256(off + sizeof(float) * slots * 128 * 512);
     pl.total = off;
     return pl;
 }
@@ -216,8 +211,7 @@ int mla_run(const void* q, const void* c_pool, const int32_t* block_table,
     p.max_pages = max_pages;
     p.num_pages = num_pages;
     p.max_len = max_len;
-    p.chunk = pl.chunk;
-    p.n_splits = pl.n_splits;
+    p.n_clusters = pl.n_clusters;
     p.idx_stride = k;
     p.sparse = sparse ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;

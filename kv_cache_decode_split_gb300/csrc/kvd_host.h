@@ -112,16 +112,18 @@ struct MlaParams {
     const int32_t* idx;        // sparse: [B, idx_stride] logical positions
     const int32_t* idx_count;  // sparse: [B]
     const void* c_pool;        // [num_pages, P, 576] bf16 (gathered rows, sparse)
-    float* part_o;             // [B * n_splits, 128, 512]
-    float* part_lse;           // [B * n_splits, 128] (log2 domain)
+    float* part_o;             // [n_clusters + B - 1, 128, 512] one slot per piece
+    float* part_lse;           // [n_clusters + B - 1, 128] (log2 domain)
     int* err;
     int B, page_size, max_pages, num_pages, max_len;
-    int chunk, n_splits, idx_stride, sparse;
+    int n_clusters, idx_stride, sparse;
     float scale_log2;
 };
 
+// Persistent plan: n_clusters two-CTA clusters share all tiles in equal contiguous ranges;
+// the pieces a range cuts out of the sequences get slots cluster + sequence.
 struct MlaPlan {
-    int chunk, n_splits;
+    int n_clusters;
     size_t off_lse, off_o, total;
 };
 MlaPlan mla_plan(int B, int max_items, bool sparse);
