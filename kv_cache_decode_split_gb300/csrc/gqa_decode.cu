@@ -49,87 +49,117 @@ struct MergeSmem {
     float o[kConsumers][HP][D];
 };
 
-// Scratch of the final combine.
-template <int HP>
+// Scratch of the final combine: one row per (KV head of the group, query head).
+template <int ROWS>
 struct CombineSmem {
-    float wgt[HP][kGqaMaxChunks];
-    float inv_denom[HP];
-    float lse_nat[HP];
+    float wgt[ROWS][kGqaMaxChunks];
+    float inv_denom[ROWS];
+    float lse_nat[ROWS];
 };
 
 __device__ __forceinline__ size_t unit_of(const GqaParams& p, int b, int kvh, int hg) {
     return (static_cast<size_t>(b) * p.Hkv + kvh) * p.NHG + hg;
 }
 
-// Merge the four warps' partials of one KV head into chunk c's (o, log2-sum-exp) partial.
+// Merge the four warps' partials of NKV KV heads into chunk c's (o, log2-sum-exp)
+// partials: one thread per head turns the warps' (m, l) into weights 2^{m_w - M} / L
+// (stored over m), then every thread sums float4 slices of the weighted warp outputs.
 template <int D, int HP>
-__device__ void merge_chunk(const GqaParams& p, const MergeSmem<D, HP>& ms, size_t unit, int c,
-                            int G_cta) {
-    float* part_o = p.part_o + (unit * p.max_chunks + c) * kMaxHP * D;
-    float* part_lse = p.part_lse + (unit * p.max_chunks + c) * kMaxHP;
-    for (int idx = threadIdx.x; idx < G_cta * D; idx += blockDim.x) {
-        const int h = idx / D, d = idx % D;
+__device__ void merge_chunks(const GqaParams& p, MergeSmem<D, HP>* ms, int b, int kv0, int nkv,
+                             int hg, int c, int G_cta) {
+    const int rows = nkv * G_cta;
+    for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+        MergeSmem<D, HP>& m = ms[r / G_cta];
+        const int h = r % G_cta;
         float M = neg_inf();
 #pragma unroll
-        for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, ms.m[w][h]);
-        float lsum = 0.f, osum = 0.f;
+        for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, m.m[w][h]);
+        float f[kConsumers], L = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumers; ++w) {
-            const float f = fast_exp2(ms.m[w][h] - M);
-            lsum += ms.l[w][h] * f;
-            osum += ms.o[w][h][d] * f;
+            f[w] = fast_exp2(m.m[w][h] - M);
+            L += m.l[w][h] * f[w];
         }
-        __stcg(part_o + h * D + d, osum / lsum);
-        if (d == 0) __stcg(part_lse + h, M + log2f(lsum));
+        const float inv = 1.f / L;
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) m.m[w][h] = f[w] * inv;
+        const size_t unit = unit_of(p, b, kv0 + r / G_cta, hg);
+        __stcg(p.part_lse + (unit * p.max_chunks + c) * kMaxHP + h, M + log2f(L));
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < rows * (D / 4); idx += blockDim.x) {
+        const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
+        const MergeSmem<D, HP>& m = ms[r / G_cta];
+        const int h = r % G_cta;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) {
+            const float f = m.m[w][h];
+            const float4 v = *reinterpret_cast<const float4*>(&m.o[w][h][d]);
+            o.x += f * v.x;
+            o.y += f * v.y;
+            o.z += f * v.z;
+            o.w += f * v.w;
+        }
+        const size_t unit = unit_of(p, b, kv0 + r / G_cta, hg);
+        __stcg(reinterpret_cast<float4*>(p.part_o + ((unit * p.max_chunks + c) * kMaxHP + h) * D + d),
+               o);
     }
 }
 
-// Combine every chunk partial of one (sequence, KV head, head block) and write its output
-// rows, the learned sink added once to the denominator:
+// Combine every chunk partial of NKV KV heads of one (sequence, head block) and write the
+// output rows, the learned sink added once to each denominator:
 //   o = sum_c 2^{lse_c - M} o_c / (sum_c 2^{lse_c - M} + 2^{sigma - M}).
-template <int D, int HP>
-__device__ void combine_unit(const GqaParams& p, CombineSmem<HP>& cs, int b, int kvh, int hg,
-                             int n_chunks, int G_cta) {
-    const size_t unit = unit_of(p, b, kvh, hg);
-    const float* uo = p.part_o + unit * p.max_chunks * kMaxHP * D;
-    const float* ul = p.part_lse + unit * p.max_chunks * kMaxHP;
+// All chunk log-sum-exps are fetched in one parallel pass, then one warp per row turns them
+// into weights, then every thread sums float4 slices of the chunk outputs.
+template <int D, int ROWS>
+__device__ void combine_units(const GqaParams& p, CombineSmem<ROWS>& cs, int b, int kv0, int nkv,
+                              int hg, int n_chunks, int G_cta) {
+    const int rows = nkv * G_cta;
+    for (int idx = threadIdx.x; idx < rows * n_chunks; idx += blockDim.x) {
+        const int r = idx / n_chunks, cc = idx % n_chunks;
+        const size_t unit = unit_of(p, b, kv0 + r / G_cta, hg);
+        cs.wgt[r][cc] = __ldcg(p.part_lse + (unit * p.max_chunks + cc) * kMaxHP + r % G_cta);
+    }
+    __syncthreads();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
-    for (int h = warp; h < G_cta; h += nwarps) {
-        const int hq = kvh * p.G + hg * kMaxHP + h;
+    for (int r = warp; r < rows; r += nwarps) {
+        const int hq = (kv0 + r / G_cta) * p.G + hg * kMaxHP + r % G_cta;
         float M = neg_inf();
-        for (int cc = lane; cc < n_chunks; cc += 32) M = fmaxf(M, __ldcg(ul + cc * kMaxHP + h));
+        for (int cc = lane; cc < n_chunks; cc += 32) M = fmaxf(M, cs.wgt[r][cc]);
         for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         const float sig = p.sink_logit ? p.sink_logit[hq] * kLog2e : neg_inf();
         M = fmaxf(M, sig);
         float den = 0.f;
         for (int cc = lane; cc < n_chunks; cc += 32) {
-            const float wv = fast_exp2(__ldcg(ul + cc * kMaxHP + h) - M);
-            cs.wgt[h][cc] = wv;
+            const float wv = fast_exp2(cs.wgt[r][cc] - M);
+            cs.wgt[r][cc] = wv;
             den += wv;
         }
         for (int off = 16; off; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
         if (p.sink_logit) den += fast_exp2(sig - M);
         if (lane == 0) {
-            cs.inv_denom[h] = 1.f / den;
-            cs.lse_nat[h] = (M + log2f(den)) * kLn2;
+            cs.inv_denom[r] = 1.f / den;
+            cs.lse_nat[r] = (M + log2f(den)) * kLn2;
         }
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < G_cta * (D / 4); idx += blockDim.x) {
-        const int h = idx / (D / 4), d = (idx % (D / 4)) * 4;
+    for (int idx = threadIdx.x; idx < rows * (D / 4); idx += blockDim.x) {
+        const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
+        const size_t unit = unit_of(p, b, kv0 + r / G_cta, hg);
+        const float* uo = p.part_o + (unit * p.max_chunks * kMaxHP + r % G_cta) * D + d;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+#pragma unroll 8
         for (int cc = 0; cc < n_chunks; ++cc) {
-            const float w = cs.wgt[h][cc];
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                uo + (static_cast<size_t>(cc) * kMaxHP + h) * D + d));
+            const float w = cs.wgt[r][cc];
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(uo + static_cast<size_t>(cc) * kMaxHP * D));
             acc.x += w * v.x;
             acc.y += w * v.y;
             acc.z += w * v.z;
             acc.w += w * v.w;
         }
-        const float inv = cs.inv_denom[h];
-        const int hq = kvh * p.G + hg * kMaxHP + h;
+        const float inv = cs.inv_denom[r];
+        const int hq = (kv0 + r / G_cta) * p.G + hg * kMaxHP + r % G_cta;
         const size_t o = (static_cast<size_t>(b) * p.Hq + hq) * D + d;
         if (p.dtype == KVD_BF16) {
             __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
@@ -140,15 +170,14 @@ __device__ void combine_unit(const GqaParams& p, CombineSmem<HP>& cs, int b, int
             *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) =
                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         }
-        if (d == 0 && p.lse_out) p.lse_out[static_cast<size_t>(b) * p.Hq + hq] = cs.lse_nat[h];
+        if (d == 0 && p.lse_out) p.lse_out[static_cast<size_t>(b) * p.Hq + hq] = cs.lse_nat[r];
     }
-    __syncthreads();
 }
 
 // After this CTA's chunk partials are written: count the chunk in, and if it was the last
 // one of group `grp`, combine the NKV KV heads kv0 .. kv0+NKV-1 of that group.
-template <int D, int HP>
-__device__ void finish_group(const GqaParams& p, CombineSmem<HP>& cs, int b, int kv0, int nkv,
+template <int D, int ROWS>
+__device__ void finish_group(const GqaParams& p, CombineSmem<ROWS>& cs, int b, int kv0, int nkv,
                              int hg, int grp, int n_chunks, int G_cta) {
     __shared__ int s_last;
     __threadfence();  // partials visible device-wide before the count
@@ -161,7 +190,7 @@ __device__ void finish_group(const GqaParams& p, CombineSmem<HP>& cs, int b, int
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    for (int hh = 0; hh < nkv; ++hh) combine_unit<D, HP>(p, cs, b, kv0 + hh, hg, n_chunks, G_cta);
+    combine_units<D, ROWS>(p, cs, b, kv0, nkv, hg, n_chunks, G_cta);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -173,7 +202,7 @@ struct GqaBf16Cfg {
     static constexpr int kTileBytes = HPT * kTile * D * 2;  // one K (or V) tile
     static constexpr int kRingBytes = 2 * kStages * kTileBytes;
     static constexpr int kMergeBytes = HPT * static_cast<int>(sizeof(MergeSmem<D, NT * 8>));
-    static constexpr int kCombBytes = static_cast<int>(sizeof(CombineSmem<NT * 8>));
+    static constexpr int kCombBytes = static_cast<int>(sizeof(CombineSmem<HPT * NT * 8>));
     static constexpr int kOverlay =
         kRingBytes > kMergeBytes + kCombBytes ? kRingBytes : kMergeBytes + kCombBytes;
     static constexpr int kSmem = 1024 + kOverlay + 2 * kStages * 8;
@@ -186,7 +215,7 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
                            const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
     using Cfg = GqaBf16Cfg<D, NT, HPT>;
     using MS = MergeSmem<D, NT * 8>;
-    using CS = CombineSmem<NT * 8>;
+    using CS = CombineSmem<HPT * NT * 8>;
     constexpr int S = Cfg::kStages;
     constexpr int KT = D / 16;  // k-steps of QK, m-tiles of PV
     constexpr int NB = D / 64;  // 64-dim column blocks
@@ -430,10 +459,9 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
             }
     }
     __syncthreads();
-    for (int hh = 0; hh < HPT; ++hh)
-        merge_chunk<D, NT * 8>(p, ms[hh], unit_of(p, b, kvg * HPT + hh, hg), c, G_cta);
+    merge_chunks<D, NT * 8>(p, ms, b, kvg * HPT, HPT, hg, c, G_cta);
     const int grp = (b * n_kvg + kvg) * p.NHG + hg;
-    finish_group<D, NT * 8>(p, cs, b, kvg * HPT, HPT, hg, grp, n_chunks, G_cta);
+    finish_group<D, HPT * NT * 8>(p, cs, b, kvg * HPT, HPT, hg, grp, n_chunks, G_cta);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -511,7 +539,7 @@ __global__ void __launch_bounds__(kConsumers * 32) gqa_decode_f32_kernel(const G
     }
     __syncthreads();
     const size_t unit = unit_of(p, b, kvh, hg);
-    merge_chunk<D, kMaxHP>(p, ms, unit, c, G_cta);
+    merge_chunks<D, kMaxHP>(p, &ms, b, kvh, 1, hg, c, G_cta);
     finish_group<D, kMaxHP>(p, cs, b, kvh, 1, hg, static_cast<int>(unit), n_chunks, G_cta);
 }
 
