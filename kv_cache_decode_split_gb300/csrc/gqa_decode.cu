@@ -115,15 +115,51 @@ __device__ void merge_chunks(const GqaParams& p, MergeSmem<D, HP>* ms, int b, in
 template <int D, int ROWS>
 __device__ void combine_units(const GqaParams& p, CombineSmem<ROWS>& cs, int b, int kv0, int nkv,
                               int hg, int n_chunks, int G_cta) {
+    constexpr int kBuf = 16;  // chunks of one output slice held in registers at once
     const int rows = nkv * G_cta;
+    const int n_out = rows * (D / 4);
+    const bool in_regs = n_chunks <= kBuf;
+    auto slice = [&](int idx) -> const float* {
+        const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
+        const size_t unit = unit_of(p, b, kv0 + r / G_cta, hg);
+        return p.part_o + (unit * p.max_chunks * kMaxHP + r % G_cta) * D + d;
+    };
+    auto fetch = [&](int idx, float4 (&v)[kBuf]) {
+        const float* uo = slice(idx);
+#pragma unroll
+        for (int cc = 0; cc < kBuf; ++cc)
+            if (cc < n_chunks)
+                v[cc] = __ldcg(reinterpret_cast<const float4*>(uo + static_cast<size_t>(cc) * kMaxHP * D));
+    };
+    // the chunk log-sum-exps, with the first output slice's partials in flight alongside
     for (int idx = threadIdx.x; idx < rows * n_chunks; idx += blockDim.x) {
         const int r = idx / n_chunks, cc = idx % n_chunks;
         const size_t unit = unit_of(p, b, kv0 + r / G_cta, hg);
         cs.wgt[r][cc] = __ldcg(p.part_lse + (unit * p.max_chunks + cc) * kMaxHP + r % G_cta);
     }
+    float4 v[kBuf];
+    if (in_regs && static_cast<int>(threadIdx.x) < n_out) fetch(threadIdx.x, v);
     __syncthreads();
+    // weights: one thread per row when there are few chunks (short serial loops over
+    // shared memory, all rows at once), one warp per row otherwise
+    if (n_chunks <= 32) {
+        for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+            const int hq = (kv0 + r / G_cta) * p.G + hg * kMaxHP + r % G_cta;
+            float M = p.sink_logit ? p.sink_logit[hq] * kLog2e : neg_inf();
+            const float sig = M;
+            for (int cc = 0; cc < n_chunks; ++cc) M = fmaxf(M, cs.wgt[r][cc]);
+            float den = p.sink_logit ? fast_exp2(sig - M) : 0.f;
+            for (int cc = 0; cc < n_chunks; ++cc) {
+                const float wv = fast_exp2(cs.wgt[r][cc] - M);
+                cs.wgt[r][cc] = wv;
+                den += wv;
+            }
+            cs.inv_denom[r] = 1.f / den;
+            cs.lse_nat[r] = (M + log2f(den)) * kLn2;
+        }
+    }
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = blockDim.x / 32;
-    for (int r = warp; r < rows; r += nwarps) {
+    for (int r = warp; r < rows && n_chunks > 32; r += nwarps) {
         const int hq = (kv0 + r / G_cta) * p.G + hg * kMaxHP + r % G_cta;
         float M = neg_inf();
         for (int cc = lane; cc < n_chunks; cc += 32) M = fmaxf(M, cs.wgt[r][cc]);
@@ -144,19 +180,32 @@ __device__ void combine_units(const GqaParams& p, CombineSmem<ROWS>& cs, int b, 
         }
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < rows * (D / 4); idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < n_out; idx += blockDim.x) {
         const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
-        const size_t unit = unit_of(p, b, kv0 + r / G_cta, hg);
-        const float* uo = p.part_o + (unit * p.max_chunks * kMaxHP + r % G_cta) * D + d;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (in_regs) {
+            if (idx != static_cast<int>(threadIdx.x)) fetch(idx, v);
+#pragma unroll
+            for (int cc = 0; cc < kBuf; ++cc) {
+                if (cc < n_chunks) {
+                    const float w = cs.wgt[r][cc];
+                    acc.x += w * v[cc].x;
+                    acc.y += w * v[cc].y;
+                    acc.z += w * v[cc].z;
+                    acc.w += w * v[cc].w;
+                }
+            }
+        } else {
+            const float* uo = slice(idx);
 #pragma unroll 8
-        for (int cc = 0; cc < n_chunks; ++cc) {
-            const float w = cs.wgt[r][cc];
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(uo + static_cast<size_t>(cc) * kMaxHP * D));
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
+            for (int cc = 0; cc < n_chunks; ++cc) {
+                const float w = cs.wgt[r][cc];
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(uo + static_cast<size_t>(cc) * kMaxHP * D));
+                acc.x += w * x.x;
+                acc.y += w * x.y;
+                acc.z += w * x.z;
+                acc.w += w * x.w;
+            }
         }
         const float inv = cs.inv_denom[r];
         const int hq = (kv0 + r / G_cta) * p.G + hg * kMaxHP + r % G_cta;
