@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
 // Histogram of the top 11 key bits of caller-provided scores (dsa_topk only).
 __global__ void __launch_bounds__(256) topk_hist_kernel(const TopkParams p) {
-    __shared__ uint32_t h[kHistBins];
+    __shared__ __align__(16) uint32_t h[kHistBins];
     const int b = blockIdx.y;
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = 0;
     __syncthreads();
@@ -330,50 +330,90 @@ __device__ void find_bucket(const uint32_t* bins, int nbins, int k, int& bucket,
     __syncthreads();
 }
 
+// The 2048-bin histogram of one sequence into shared memory, all loads in flight at once.
+template <int NT>
+__device__ __forceinline__ void load_hist(uint32_t* h, const uint32_t* src) {
+    constexpr int kVec = kHistBins / 4;  // uint4 loads
+    constexpr int kPer = (kVec + NT - 1) / NT;
+    uint4 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int i = threadIdx.x + k * NT;
+        if (i < kVec) v[k] = __ldcg(reinterpret_cast<const uint4*>(src) + i);
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int i = threadIdx.x + k * NT;
+        if (i < kVec) reinterpret_cast<uint4*>(h)[i] = v[k];
+    }
+}
+
 // Tokens whose bucket is above the k-th's are selected; tokens inside it are candidates.
-__global__ void __launch_bounds__(256) topk_filter_kernel(const TopkParams p) {
-    __shared__ uint32_t h[kHistBins];
-    __shared__ int tmp[256 / 32 + 3];
+// Each block classifies its share of the scores in registers, counts both lists with one
+// block scan and reserves its space with one atomic per list, so the two per-sequence
+// counters see a few dozen atomics instead of one per warp and 32 scores.
+constexpr int kFiltThreads = 256;
+constexpr int kFiltPerThread = 16;
+__global__ void __launch_bounds__(kFiltThreads) topk_filter_kernel(const TopkParams p) {
+    __shared__ __align__(16) uint32_t h[kHistBins];
+    __shared__ int tmp[kFiltThreads / 32 + 3];
+    __shared__ int s_base[2];
     const int b = blockIdx.y;
     const int L = load_len(p.lens, b, p.max_len, nullptr);
     if (L <= p.k) return;  // everything is selected; the finalize kernel writes it
-    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
-        h[i] = p.hist[static_cast<size_t>(b) * kHistBins + i];
+    load_hist<kFiltThreads>(h, p.hist + static_cast<size_t>(b) * kHistBins);
     __syncthreads();
     int b1, above, in_b1;
-    find_bucket<256>(h, kHistBins, p.k, b1, above, in_b1, tmp);
+    find_bucket<kFiltThreads>(h, kHistBins, p.k, b1, above, in_b1, tmp);
     const float* sc = p.scores + static_cast<size_t>(b) * p.score_stride;
     int* sel = p.sel + static_cast<size_t>(b) * p.k;
     int* cand = p.cand + static_cast<size_t>(b) * p.max_len;
-    const int lane = threadIdx.x % 32;
-    const int stride = gridDim.x * blockDim.x;
-    for (int base = blockIdx.x * blockDim.x; base < L; base += stride) {
-        const int t = base + threadIdx.x;
-        int bk = -1;
-        if (t < L) bk = static_cast<int>(float_key(sc[t]) >> 21);
-        // warp-aggregated appends
-        const unsigned m_sel = __ballot_sync(0xffffffffu, bk > b1);
-        const unsigned m_cand = __ballot_sync(0xffffffffu, bk == b1);
-        int sel_base = 0, cand_base = 0;
-        if (lane == 0) {
-            if (m_sel) sel_base = atomicAdd(p.counts + 2 * b, __popc(m_sel));
-            if (m_cand) cand_base = atomicAdd(p.counts + 2 * b + 1, __popc(m_cand));
+    constexpr int kSpan = kFiltThreads * kFiltPerThread;
+    for (int base = blockIdx.x * kSpan; base < L; base += gridDim.x * kSpan) {
+        // 2 bits per element: 1 = selected, 2 = candidate
+        uint32_t cls = 0;
+        int n_sel = 0, n_cand = 0;
+#pragma unroll
+        for (int k = 0; k < kFiltPerThread; ++k) {
+            const int t = base + k * kFiltThreads + threadIdx.x;
+            if (t < L) {
+                const int bk = static_cast<int>(float_key(sc[t]) >> 21);
+                if (bk > b1) {
+                    cls |= 1u << (2 * k);
+                    ++n_sel;
+                } else if (bk == b1) {
+                    cls |= 2u << (2 * k);
+                    ++n_cand;
+                }
+            }
         }
-        sel_base = __shfl_sync(0xffffffffu, sel_base, 0);
-        cand_base = __shfl_sync(0xffffffffu, cand_base, 0);
-        const unsigned lower = (1u << lane) - 1u;
-        // a zeroed workspace keeps both lists inside their buffers (fewer than k tokens lie
-        // above the k-th's bucket); counters left non-zero by other kernels must not write
-        // outside them
-        if (bk > b1) {
-            const int si = sel_base + __popc(m_sel & lower);
-            if (si >= 0 && si < p.k) sel[si] = t;
-            else record_error(p.err, KVD_ERR_DEVICE_STATE);
+        // both counts in one scan (each at most 4096 per block)
+        const int packed = n_sel | (n_cand << 16);
+        const int incl = block_incl_scan<kFiltThreads>(packed, tmp);
+        const int excl = incl - packed;
+        if (threadIdx.x == kFiltThreads - 1) {
+            s_base[0] = (incl & 0xFFFF) ? atomicAdd(p.counts + 2 * b, incl & 0xFFFF) : 0;
+            s_base[1] = (incl >> 16) ? atomicAdd(p.counts + 2 * b + 1, incl >> 16) : 0;
         }
-        if (bk == b1) {
-            const int ci = cand_base + __popc(m_cand & lower);
-            if (ci >= 0 && ci < p.max_len) cand[ci] = t;
-            else record_error(p.err, KVD_ERR_DEVICE_STATE);
+        __syncthreads();
+        int si = s_base[0] + (excl & 0xFFFF), ci = s_base[1] + (excl >> 16);
+        __syncthreads();  // s_base read before the next span overwrites it
+#pragma unroll
+        for (int k = 0; k < kFiltPerThread; ++k) {
+            const int t = base + k * kFiltThreads + threadIdx.x;
+            const uint32_t c = (cls >> (2 * k)) & 3u;
+            // a zeroed workspace keeps both lists inside their buffers (fewer than k tokens
+            // lie above the k-th's bucket); counters left non-zero by other kernels must not
+            // write outside them
+            if (c == 1u) {
+                if (si >= 0 && si < p.k) sel[si] = t;
+                else record_error(p.err, KVD_ERR_DEVICE_STATE);
+                ++si;
+            } else if (c == 2u) {
+                if (ci >= 0 && ci < p.max_len) cand[ci] = t;
+                else record_error(p.err, KVD_ERR_DEVICE_STATE);
+                ++ci;
+            }
         }
     }
 }
@@ -385,11 +425,21 @@ __device__ __forceinline__ uint64_t composite_key(float score, int t) {
            static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(t));
 }
 
+// Shared-memory copies of the finalize step when they fit: the candidates' composite keys
+// (read once from global memory, then reused by every radix pass) and the bitmap of chosen
+// positions (no global atomics, fence or read-back).
+constexpr int kFinCandSmem = 4096;
+constexpr int kFinWordsSmem = 8192;
+constexpr int kFinDynSmem = kFinCandSmem * 8 + kFinWordsSmem * 4;
+
 // One CTA per sequence: exact threshold among the candidates, then the output in
 // ascending position order from a bitmap of the chosen positions and a prefix scan.
 __global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkParams p) {
-    __shared__ uint32_t h[kHistBins];
+    __shared__ __align__(16) uint32_t h[kHistBins];
     __shared__ int tmp[kFinThreads / 32 + 3];
+    extern __shared__ uint64_t fin_dyn[];
+    uint64_t* keys = fin_dyn;
+    uint32_t* sbits = reinterpret_cast<uint32_t*>(fin_dyn + kFinCandSmem);
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
     const int L = load_len(p.lens, b, p.max_len, nullptr);
@@ -403,9 +453,13 @@ __global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkPa
         const int* cand = p.cand + static_cast<size_t>(b) * p.max_len;
         const int* sel = p.sel + static_cast<size_t>(b) * p.k;
         const int n_words = (L + 31) / 32;
-        uint32_t* bits = p.bitmap + static_cast<size_t>(b) * ((p.max_len + 31) / 32);
-        for (int i = tid; i < kHistBins; i += kFinThreads)
-            h[i] = p.hist[static_cast<size_t>(b) * kHistBins + i];
+        const bool bits_in_smem = n_words <= kFinWordsSmem;
+        uint32_t* bits = bits_in_smem
+                             ? sbits
+                             : p.bitmap + static_cast<size_t>(b) * ((p.max_len + 31) / 32);
+        load_hist<kFinThreads>(h, p.hist + static_cast<size_t>(b) * kHistBins);
+        if (bits_in_smem)
+            for (int i = tid; i < n_words; i += kFinThreads) sbits[i] = 0;
         __syncthreads();
         int b1, above, in_b;
         find_bucket<kFinThreads>(h, kHistBins, p.k, b1, above, in_b, tmp);
@@ -414,6 +468,21 @@ __global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkPa
             if (tid == 0) record_error(p.err, KVD_ERR_DEVICE_STATE);
             nc = min(max(nc, 0), L);
             above = min(max(above, 0), p.k - 1);
+        }
+        // the candidates' keys (a position outside [0, L) only follows a non-zeroed
+        // workspace; its key is 0 and it is never chosen below)
+        const bool keys_in_smem = nc <= kFinCandSmem;
+        auto cand_key = [&](int i) -> uint64_t {
+            if (keys_in_smem) return keys[i];
+            const int t = cand[i];
+            return (t >= 0 && t < L) ? composite_key(sc[t], t) : 0ull;
+        };
+        if (keys_in_smem) {
+            for (int i = tid; i < nc; i += kFinThreads) {
+                const int t = cand[i];
+                keys[i] = (t >= 0 && t < L) ? composite_key(sc[t], t) : 0ull;
+            }
+            __syncthreads();
         }
         int need = p.k - above;  // to take from the candidates (>= 1)
         // radix passes over the 64-bit composite key below its top 11 bits, until the
@@ -427,10 +496,8 @@ __global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkPa
             for (int i = tid; i < nb; i += kFinThreads) h[i] = 0;
             __syncthreads();
             for (int i = tid; i < nc; i += kFinThreads) {
-                const int t = cand[i];
-                if (t < 0 || t >= L) continue;  // only after a non-zeroed workspace
-                const uint64_t ck = composite_key(sc[t], t);
-                if ((ck >> (64 - done_bits)) == prefix)
+                const uint64_t ck = cand_key(i);
+                if (ck != 0ull && (ck >> (64 - done_bits)) == prefix)
                     atomicAdd(&h[static_cast<int>((ck >> shift) & (nb - 1))], 1u);
             }
             __syncthreads();
@@ -447,23 +514,26 @@ __global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkPa
             if (t >= 0 && t < L) atomicOr(bits + (t >> 5), 1u << (t & 31));
         }
         for (int i = tid; i < nc; i += kFinThreads) {
-            const int t = cand[i];
-            if (t >= 0 && t < L && composite_key(sc[t], t) >= T)
+            const uint64_t ck = cand_key(i);
+            if (ck != 0ull && ck >= T) {
+                const int t = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(ck));
                 atomicOr(bits + (t >> 5), 1u << (t & 31));
+            }
         }
-        __threadfence();  // the bit updates land in L2 before the words are read back
+        if (!bits_in_smem) __threadfence();  // global bit updates land in L2 first
         __syncthreads();
         // positions in ascending order: popcount prefix scan over the bitmap words
         const int per = (n_words + kFinThreads - 1) / kFinThreads;
         const int w0 = tid * per;
         int local = 0;
         for (int i = 0; i < per; ++i)
-            if (w0 + i < n_words) local += __popc(__ldcg(bits + w0 + i));
+            if (w0 + i < n_words)
+                local += __popc(bits_in_smem ? sbits[w0 + i] : __ldcg(bits + w0 + i));
         int pos = block_incl_scan<kFinThreads>(local, tmp) - local;
         for (int i = 0; i < per; ++i) {
             if (w0 + i >= n_words) break;
-            uint32_t w = __ldcg(bits + w0 + i);
-            bits[w0 + i] = 0;  // leave the bitmap clear for the next call
+            uint32_t w = bits_in_smem ? sbits[w0 + i] : __ldcg(bits + w0 + i);
+            if (!bits_in_smem) bits[w0 + i] = 0;  // leave the global bitmap clear
             while (w) {
                 const int bit = __ffs(w) - 1;
                 if (pos < p.k) idx_out[pos] = (w0 + i) * 32 + bit;
@@ -501,8 +571,18 @@ int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensor
 int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream) {
     const int blocks_per_b = std::max(1, std::min(64, (p.max_len + 4095) / 4096));
     if (need_hist) topk_hist_kernel<<<dim3(blocks_per_b, p.B), 256, 0, stream>>>(p);
-    topk_filter_kernel<<<dim3(blocks_per_b, p.B), 256, 0, stream>>>(p);
-    topk_finalize_kernel<<<p.B, kFinThreads, 0, stream>>>(p);
+    const int filt_per_b =
+        std::max(1, std::min(64, (p.max_len + kFiltThreads * kFiltPerThread - 1) /
+                                     (kFiltThreads * kFiltPerThread)));
+    topk_filter_kernel<<<dim3(filt_per_b, p.B), kFiltThreads, 0, stream>>>(p);
+    static int fin_configured = 0;
+    if (!fin_configured) {
+        if (cudaFuncSetAttribute(topk_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kFinDynSmem) != cudaSuccess)
+            return KVD_ERR_CUDA;
+        fin_configured = 1;
+    }
+    topk_finalize_kernel<<<p.B, kFinThreads, kFinDynSmem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
 

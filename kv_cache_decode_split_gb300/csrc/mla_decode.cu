@@ -633,26 +633,48 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const MlaParams p, __n
         }
         T += n;
     }
-    // clusters whose ranges [T c / C, T (c + 1) / C) hold b's first and last tile: the one
-    // holding tile t is floor((t C + C - 1) / T)
-    const long long C = p.n_clusters;
-    int c0 = 0, c1 = -1;
-    if (nb > 0) {
-        c0 = static_cast<int>((Sb * C + C - 1) / T);
-        c1 = static_cast<int>(((Sb + nb - 1) * C + C - 1) / T);
+    // Clusters whose ranges [T c / C, T (c + 1) / C) meet b's tiles: the one holding tile t
+    // is floor((t C + C - 1) / T). With at least as many tiles as clusters every range is
+    // non-empty, so the clusters holding b's first and last tiles bound a contiguous run;
+    // otherwise b has fewer than C tiles and each one names its cluster. Block-wide, once.
+    constexpr int kMaxRun = 256;
+    __shared__ int s_slot[kMaxRun];
+    __shared__ int s_n;
+    if (threadIdx.x == 0) {
+        const long long C = p.n_clusters;
+        int n = 0;
+        if (nb > 0 && T >= C) {
+            const int c0 = static_cast<int>((Sb * C + C - 1) / T);
+            const int c1 = static_cast<int>(((Sb + nb - 1) * C + C - 1) / T);
+            for (int c = c0; c <= c1 && n < kMaxRun; ++c) s_slot[n++] = c + b;
+        } else {
+            int last = -1;
+            for (int t = 0; t < nb && n < kMaxRun; ++t) {
+                const int c = static_cast<int>(((Sb + t) * C + C - 1) / T);
+                if (c != last) s_slot[n++] = c + b;
+                last = c;
+            }
+        }
+        s_n = n;
     }
-    // clusters with an empty range (more clusters than tiles) wrote no slot
-    auto nonempty = [&](int c) { return T * (c + 1) / C > T * c / C; };
-    const float* lse = p.part_lse + (static_cast<size_t>(c0) + b) * kH + h;
+    __shared__ float s_lse[2][kMaxRun];
+    __syncthreads();
+    const int n_slots = s_n;
+    // both heads' log-sum-exps of every slot, fetched in parallel
+    for (int i = threadIdx.x; i < 2 * n_slots; i += blockDim.x)
+        s_lse[i / n_slots][i % n_slots] =
+            __ldcg(p.part_lse + static_cast<size_t>(s_slot[i % n_slots]) * kH +
+                   (blockIdx.x % (kH / 2)) * 2 + i / n_slots);
+    __syncthreads();
+    const float* lse = s_lse[threadIdx.x / 128];
     float M = neg_inf();
-    for (int c = c0; c <= c1; ++c)
-        if (nonempty(c)) M = fmaxf(M, lse[(c - c0) * kH]);
+    for (int i = 0; i < n_slots; ++i) M = fmaxf(M, lse[i]);
     float den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = c0; c <= c1; ++c) {
-        if (!nonempty(c)) continue;
-        const size_t slot = static_cast<size_t>(c) + b;
-        const float w = (M == neg_inf()) ? 0.f : fast_exp2(lse[(c - c0) * kH] - M);
+#pragma unroll 8
+    for (int i = 0; i < n_slots; ++i) {
+        const size_t slot = s_slot[i];
+        const float w = (M == neg_inf()) ? 0.f : fast_exp2(lse[i] - M);
         den += w;
         const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + (slot * kH + h) * kDv + d));
         acc.x += w * v.x;
