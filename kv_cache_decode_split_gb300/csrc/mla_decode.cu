@@ -47,8 +47,11 @@ constexpr int kStageBytes = kNBox * kTileBox;
 // warps 0-7: softmax (group = warp / 4 takes tiles of that parity, TMEM lane quarter =
 // warp % 4); warp 8: loads; warp 9: score products (and TMEM allocation); warp 10: value
 // products; warp 11: score exchange
-constexpr int kThreads = 12 * 32;
-constexpr int kWarpLoad = 8, kWarpQK = 9, kWarpPV = 10, kWarpX = 11;
+constexpr int kGroups = 3;  // softmax warp groups, taking tiles j with j % kGroups == group
+constexpr int kSoftWarps = 4 * kGroups;
+constexpr int kThreads = (kSoftWarps + 4) * 32;
+constexpr int kWarpLoad = kSoftWarps, kWarpQK = kSoftWarps + 1, kWarpPV = kSoftWarps + 2,
+              kWarpX = kSoftWarps + 3;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -59,18 +62,19 @@ struct MlaSmem {
     float x[2][kH][kTok / 2];              // the partner's halves, one slot per half (16-byte
                                            // chunks XOR-ed with row % 8)
     float y[2][kH][kTok / 2];              // this CTA's halves on their way out
-    float mref[2][kH];                     // running max after each group's latest tile
+    float mref[kGroups][kH];               // running max after each group's latest tile; at
+                                           // the end of a piece: each group's row sum
     // Barriers waited by one group only exist once per group (tile parity), so that each
     // waiter goes through its barrier's phases in order.
-    uint64_t full[kStages], empty[kStages], qready, sfull[2], sempty, pfull, pvdone[2], ofinal;
-    uint64_t xfull[2][2];    // [half][tile parity]: the partner's half has arrived
-    uint64_t xused[2];       // x[half] has been read (four warps of the tile's group)
-    uint64_t peer_free[2];   // the partner has read our previous half in its x[half]
+    uint64_t full[kStages], empty[kStages], qready, sfull[kGroups], sempty, pfull,
+        pvdone[kGroups], ofinal;
+    uint64_t xfull[2][kGroups];  // [half][tile group]: the partner's half has arrived
+    uint64_t peer_free[2];   // the partner has read our previous half in its x[half] (remote
+                             // arrives by the four warps of the partner's group)
     uint64_t yfull[2];       // y[half] written (four warps of the tile's group)
-    uint64_t yfree[2][2];    // [half][tile parity]: the copy of y[half] has read it
-    uint64_t hand[2];        // group published its running max
+    uint64_t yfree[2][kGroups];  // [half][tile group]: the copy of y[half] has read it
+    uint64_t hand[kGroups];  // group published its running max
     uint64_t ofree;          // O of the current piece has been read (eight softmax warps)
-    float lsum[2][kH];       // both groups' row sums at the end of a piece
     uint32_t tmem_base;
 };
 
@@ -176,27 +180,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(&sm.full[s], kSparse ? 32 : 1);
             mbar_init(&sm.empty[s], 1);
         }
-        mbar_init(&sm.qready, 8);
+        mbar_init(&sm.qready, kSoftWarps);
         mbar_init(&sm.sempty, 4);  // the four warps of the group that owns the tile
         mbar_init(&sm.pfull, 4);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.sfull[i], 1);
-            mbar_init(&sm.pvdone[i], 1);
-            mbar_init(&sm.xfull[0][i], 1);   // armed with the exchanged byte count each tile
-            mbar_init(&sm.xfull[1][i], 1);
-            mbar_init(&sm.xused[i], 4);
-            mbar_init(&sm.peer_free[i], 1);  // remote arrive by the partner's exchange thread
+            mbar_init(&sm.peer_free[i], 4);
             mbar_init(&sm.yfull[i], 4);
-            mbar_init(&sm.yfree[0][i], 1);
-            mbar_init(&sm.yfree[1][i], 1);
-            mbar_init(&sm.hand[i], 4);
+        }
+        for (int g = 0; g < kGroups; ++g) {
+            mbar_init(&sm.sfull[g], 1);
+            mbar_init(&sm.pvdone[g], 1);
+            mbar_init(&sm.xfull[0][g], 1);   // armed with the exchanged byte count each tile
+            mbar_init(&sm.xfull[1][g], 1);
+            mbar_init(&sm.yfree[0][g], 1);
+            mbar_init(&sm.yfree[1][g], 1);
+            mbar_init(&sm.hand[g], 4);
         }
         mbar_init(&sm.ofinal, 1);
-        mbar_init(&sm.ofree, 8);
+        mbar_init(&sm.ofree, kSoftWarps);
         fence_mbar_init();
-        // the partner's partial scores of tiles 0 and 1 (later tiles: armed by the group
-        // once the slot's previous phase has completed)
-        for (int i = 0; i < 2 && i < n_tiles; ++i)
+        // the partner's partial scores of the first tile of each group (later tiles: armed
+        // by the group once the slot's previous phase has completed)
+        for (int i = 0; i < kGroups && i < n_tiles; ++i)
             for (int hf = 0; hf < 2; ++hf) mbar_arrive_expect_tx(&sm.xfull[hf][i], kXBytes / 2);
     }
     if (warp == kWarpQK) tmem_alloc(&sm.tmem_base, 512);
@@ -332,7 +337,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         issue_qk<16>(tmem, smem_u32(sm.stage[s]));
                     else
                         issue_qk<20>(tmem, smem_u32(sm.stage[s]));
-                    tc_commit(&sm.sfull[g & 1]);
+                    tc_commit(&sm.sfull[g % kGroups]);
                 }
             });
         }
@@ -351,7 +356,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (!(ok = mbar_wait(&sm.pfull, g & 1, p.err))) return;
                     tc_fence_after();
                     issue_pv(tmem, smem_u32(sm.stage[s]), i > 0);
-                    tc_commit(&sm.pvdone[g & 1]);
+                    tc_commit(&sm.pvdone[g % kGroups]);
                     tc_commit(&sm.empty[s]);  // the tile's score product completed before its P
                 }
                 tc_commit(&sm.ofinal);  // every product of the piece (and before) completed
@@ -364,42 +369,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // distributed shared memory at its own rate, off the softmax warps' instruction path;
         // each half of y is released as soon as its own copy has read it.
         if (lane == 0) {
-            uint32_t peer_x[2], peer_free[2], peer_xfull[2][2];
+            uint32_t peer_x[2], peer_xfull[2][kGroups];
             for (int hf = 0; hf < 2; ++hf) {
                 peer_x[hf] = map_peer(smem_u32(&sm.x[hf][0][0]), peer);
-                peer_free[hf] = map_peer(smem_u32(&sm.peer_free[hf]), peer);
-                for (int i = 0; i < 2; ++i)
-                    peer_xfull[hf][i] = map_peer(smem_u32(&sm.xfull[hf][i]), peer);
+                for (int g = 0; g < kGroups; ++g)
+                    peer_xfull[hf][g] = map_peer(smem_u32(&sm.xfull[hf][g]), peer);
             }
             bool ok = true;
             for (int j = 0; j < n_tiles && ok; ++j) {
                 for (int hf = 0; hf < 2; ++hf) {
-                    // our x[hf] has been read for tile j - 1: the partner may send into it
-                    if (j >= 1) {
-                        if (!(ok = mbar_wait(&sm.xused[hf], (j - 1) & 1, p.err))) break;
-                        mbar_arrive_remote_relaxed(peer_free[hf]);
-                    }
                     if (!(ok = mbar_wait(&sm.yfull[hf], j & 1, p.err))) break;
                     if (!(ok = mbar_wait_cluster(&sm.peer_free[hf], (j & 1) ^ 1, p.err))) break;
                     bulk_copy_to_peer(peer_x[hf], &sm.y[hf][0][0], kXBytes / 2,
-                                      peer_xfull[hf][j & 1]);
+                                      peer_xfull[hf][j % kGroups]);
                     // the previous copy (the other half) has been read: release it
                     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
                     if (hf == 1)
-                        mbar_arrive(&sm.yfree[0][j & 1]);
+                        mbar_arrive(&sm.yfree[0][j % kGroups]);
                     else if (j >= 1)
-                        mbar_arrive(&sm.yfree[1][(j - 1) & 1]);
+                        mbar_arrive(&sm.yfree[1][(j - 1) % kGroups]);
                 }
             }
             bulk_wait_read_all();
-            if (ok) mbar_arrive(&sm.yfree[1][(n_tiles - 1) & 1]);
+            if (ok) mbar_arrive(&sm.yfree[1][(n_tiles - 1) % kGroups]);
         }
     } else {
         // ------------------------------------------------------------------ softmax
-        const int grp = warp >> 2;                 // takes tiles g with g % 2 == grp
+        const int grp = warp >> 2;                 // takes tiles j with j % kGroups == grp
         const int h = (warp & 3) * 32 + lane;      // head = TMEM lane
         const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const float sl2 = p.scale_log2;
+        const uint32_t peer_free_hf[2] = {map_peer(smem_u32(&sm.peer_free[0]), peer),
+                                          map_peer(smem_u32(&sm.peer_free[1]), peer)};
         int g0 = 0;  // first tile of the current piece within this CTA's range
         bool ok = true;
         // Every piece ends in two named barriers of all eight warps, reached even after a
@@ -413,7 +414,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint4* qrow = reinterpret_cast<const uint4*>(
                     reinterpret_cast<const __nv_bfloat16*>(p.q) +
                     (static_cast<size_t>(b) * kH + h) * kDqk + dim0);
-                const int bx0 = grp == 0 ? 0 : 3, bx1 = grp == 0 ? 3 : nbox;
+                constexpr int kQBoxes = (kNBox + kGroups - 1) / kGroups;
+                const int bx0 = grp * kQBoxes, bx1 = min(nbox, bx0 + kQBoxes);
                 // one 64-dim box (32 columns) at a time: few registers, outside the tile loop
 #pragma unroll 1
                 for (int bx = bx0; bx < bx1; ++bx) {
@@ -439,8 +441,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float m_last = neg_inf();        // running max after this group's latest tile
             for (int i = 0; i < nt && ok; ++i) {
                 const int j = g0 + i;  // tile index within the range (barrier phases)
-                if ((j & 1) != grp) continue;
-                const int it = j >> 1;  // this group's iteration
+                if (j % kGroups != grp) continue;
+                const int it = j / kGroups;  // this group's iteration
+                const int pg = (j + kGroups - 1) % kGroups;  // group of tile j - 1
+                const int pit = ((j - 1) / kGroups) & 1;     // its barrier parity
                 // 1. this CTA's partial scores; reading them frees S for the next product
                 if (!(ok = mbar_wait(&sm.sfull[grp], it & 1, p.err))) break;
                 tc_fence_after();
@@ -465,7 +469,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     if (j >= 1 &&
-                        !(ok = mbar_wait(&sm.yfree[hf][grp ^ 1], ((j - 1) >> 1) & 1, p.err)))
+                        !(ok = mbar_wait(&sm.yfree[hf][pg], pit, p.err)))
                         break;
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
@@ -491,9 +495,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         s[32 * hf + 4 * c + 3] += v.w;
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&sm.xused[hf]);
+                    // x[hf] has been read: the partner may send its next half into it (the
+                    // values are in registers, so a relaxed arrive suffices)
+                    if (lane == 0) mbar_arrive_remote_relaxed(peer_free_hf[hf]);
                     // the slot's phase is complete: arm it for this group's next tile
-                    if (warp == 4 * grp && lane == 0 && j + 2 < n_tiles)
+                    if (warp == 4 * grp && lane == 0 && j + kGroups < n_tiles)
                         mbar_arrive_expect_tx(&sm.xfull[hf][grp], kXBytes / 2);
                 }
                 if (!ok) break;
@@ -508,8 +514,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 float m_prev = neg_inf();
                 if (j >= 1) {
-                    if (!(ok = mbar_wait(&sm.hand[grp ^ 1], ((j - 1) >> 1) & 1, p.err))) break;
-                    if (i > 0) m_prev = sm.mref[grp ^ 1][h];
+                    if (!(ok = mbar_wait(&sm.hand[pg], pit, p.err))) break;
+                    if (i > 0) m_prev = sm.mref[pg][h];
                 }
                 // raise the reference only on the first tile or when the max grows by > 2^8
                 float m_new = m_prev;
@@ -545,7 +551,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 l += psum;
                 // 6. P (and O) are free once tile j - 1's value product has completed
                 if (j >= 1 &&
-                    !(ok = mbar_wait(&sm.pvdone[grp ^ 1], ((j - 1) >> 1) & 1, p.err)))
+                    !(ok = mbar_wait(&sm.pvdone[pg], pit, p.err)))
                     break;
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, resc)) {
@@ -571,21 +577,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // The piece's partial: O / l for this CTA's 256 value dims, and log2-sum-exp.
             // The final reference is the running max after the piece's last tile.
             const int jl = g0 + nt - 1;
-            if (ok && (jl & 1) != grp) {
-                ok = mbar_wait(&sm.hand[grp ^ 1], (jl >> 1) & 1, p.err);
-                if (ok) m_last = sm.mref[grp ^ 1][h];
+            const int lg = jl % kGroups;  // group of the piece's last tile
+            if (ok && lg != grp) {
+                ok = mbar_wait(&sm.hand[lg], (jl / kGroups) & 1, p.err);
+                if (ok) m_last = sm.mref[lg][h];
             }
-            sm.lsum[grp][h] = (l > 0.f) ? l * fast_exp2(m_l - m_last) : 0.f;
-            asm volatile("bar.sync 1, %0;" ::"r"(8 * 32) : "memory");
-            const float l_tot = sm.lsum[0][h] + sm.lsum[1][h];
-            asm volatile("bar.sync 1, %0;" ::"r"(8 * 32) : "memory");  // lsum read
+            // every group's sum relative to 2^m_last, added through shared memory (over the
+            // running-max array, once every group has read the final max)
+            asm volatile("bar.sync 1, %0;" ::"r"(kSoftWarps * 32) : "memory");
+            sm.mref[grp][h] = (l > 0.f) ? l * fast_exp2(m_l - m_last) : 0.f;
+            asm volatile("bar.sync 1, %0;" ::"r"(kSoftWarps * 32) : "memory");
+            float l_tot = 0.f;
+#pragma unroll
+            for (int g = 0; g < kGroups; ++g) l_tot += sm.mref[g][h];
+            asm volatile("bar.sync 1, %0;" ::"r"(kSoftWarps * 32) : "memory");  // sums read
             if (ok && (ok = mbar_wait(&sm.ofinal, k & 1, p.err))) {
                 tc_fence_after();
                 const size_t slot = static_cast<size_t>(cl) + b;
                 const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
                 float* po = p.part_o + (slot * kH + h) * kDv + rank * 256;
-                // group g writes value dims 128 g .. 128 g + 127 of this CTA's half
-                for (int c = 4 * grp; c < 4 * grp + 4; ++c) {
+                // the groups split this CTA's 256 value dims in 32-column slices
+                constexpr int kOSlices = (8 + kGroups - 1) / kGroups;
+                for (int c = grp * kOSlices; c < min(8, (grp + 1) * kOSlices); ++c) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(trow + kColO + c * 32, r);
                     tmem_ld_wait(r);
