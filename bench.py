@@ -245,7 +245,7 @@ class MlaRunner:
 
 class DsaRunner:
     """dsa_indexer_topk then attn_decode_mla_sparse (indexer, top-2048, sparse MLA)."""
-    launches_per_step = 5          # indexer, filter, finalize, sparse MLA, combine
+    launches_per_step = 4          # indexer, selection, sparse MLA, combine
     kernel = "dsa_indexer_kernel"
 
     def __init__(self, name, dev, sharp=False):

@@ -145,11 +145,11 @@ TopkLayout topk_layout(int B, int max_len, int k, bool with_scores) {
     l.off_hist = off;
     off = round256(off + sizeof(uint32_t) * (size_t)B * 2048);
     l.off_counts = off;
-    off = round256(off + sizeof(int) * (size_t)B * 2);
+    off = round256(off + sizeof(int) * (size_t)B * 4);
     l.off_sel = off;
     off = round256(off + sizeof(int) * (size_t)B * k);
     l.off_cand = off;
-    off = round256(off + sizeof(int) * (size_t)B * max_len);
+    off = round256(off + sizeof(uint64_t) * (size_t)B * max_len);
     l.off_bitmap = off;
     off = round256(off + sizeof(uint32_t) * (size_t)B * ((max_len + 31) / 32));
     l.off_scores = off;
@@ -164,7 +164,13 @@ MlaPlan mla_plan(int B, int max_items, bool sparse) {
     (void)sparse;
     MlaPlan pl;
     const long long max_tiles = (long long)B * ((max_items + 63) / 64);
-    pl.n_clusters = static_cast<int>(std::max(1LL, std::min<long long>(num_sms() / 2, max_tiles)));
+    long long min_tiles = 1;  // tiles a cluster takes at least
+    if (const char* env = std::getenv("KVD_MLA_MIN_TILES")) {  // tuning override
+        const long long t = std::atoll(env);
+        if (t >= 1) min_tiles = t;
+    }
+    pl.n_clusters = static_cast<int>(std::max(
+        1LL, std::min<long long>(num_sms() / 2, (max_tiles + min_tiles - 1) / min_tiles)));
     const size_t slots = (size_t)pl.n_clusters + B - 1;
     size_t off = kWsHeaderBytes;
     pl.off_lse = off;
@@ -365,6 +371,7 @@ int dsa_indexer_topk(const void* q_idx, const void* k_idx_pool, const float* w,
     ip.scores = scores_out ? scores_out : reinterpret_cast<float*>(wb + lay.off_scores);
     ip.score_stride = max_len;
     ip.hist = reinterpret_cast<uint32_t*>(wb + lay.off_hist);
+    ip.counts = reinterpret_cast<int*>(wb + lay.off_counts);
     ip.err = reinterpret_cast<int*>(wb);
     ip.B = B;
     ip.page_size = page_size;
@@ -391,7 +398,7 @@ int dsa_indexer_topk(const void* q_idx, const void* k_idx_pool, const float* w,
     tp.hist = ip.hist;
     tp.counts = reinterpret_cast<int*>(wb + lay.off_counts);
     tp.sel = reinterpret_cast<int*>(wb + lay.off_sel);
-    tp.cand = reinterpret_cast<int*>(wb + lay.off_cand);
+    tp.cand = reinterpret_cast<uint64_t*>(wb + lay.off_cand);
     tp.bitmap = reinterpret_cast<uint32_t*>(wb + lay.off_bitmap);
     tp.topk_idx = topk_idx;
     tp.topk_count = topk_count;
@@ -419,7 +426,7 @@ int dsa_topk(const float* scores, const int32_t* lens, int32_t* topk_idx, int32_
     tp.hist = reinterpret_cast<uint32_t*>(wb + lay.off_hist);
     tp.counts = reinterpret_cast<int*>(wb + lay.off_counts);
     tp.sel = reinterpret_cast<int*>(wb + lay.off_sel);
-    tp.cand = reinterpret_cast<int*>(wb + lay.off_cand);
+    tp.cand = reinterpret_cast<uint64_t*>(wb + lay.off_cand);
     tp.bitmap = reinterpret_cast<uint32_t*>(wb + lay.off_bitmap);
     tp.topk_idx = topk_idx;
     tp.topk_count = topk_count;

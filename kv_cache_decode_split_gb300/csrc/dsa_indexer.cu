@@ -6,18 +6,18 @@
 // then the indices of the k largest I_t (ties to the lower position), in ascending order.
 //
 // Indexer (GB300): a persistent kernel, one CTA per SM, each CTA owning a contiguous range
-// of 128-token tiles. One thread streams key tiles with TMA (128-byte swizzle) through a
-// shared-memory ring; one thread issues tcgen05.mma with the tokens as M and the heads as
+// of 128-token tiles. One warp resolves the tiles' page rows ahead of time and one of its
+// threads streams key tiles with TMA (128-byte swizzle) through a shared-memory ring; one thread issues tcgen05.mma with the tokens as M and the heads as
 // N: D[128 tok x 64 heads] (TMEM, fp32) = K[128 x 128] * Q^T, double-buffered in tensor
 // memory; four epilogue warps read one token row each (tcgen05.ld), apply ReLU and the head
 // weights, write the fp32 score and count its top 11 key bits into a shared-memory
 // histogram, the first pass of the radix selection.
 //
-// Selection: a filter kernel finds, from that histogram, the bucket holding the k-th
-// largest score; tokens above it are selected and tokens inside it become candidates. A
-// finalize kernel (one CTA per sequence) narrows the candidates with further radix passes
-// over a 64-bit key (score key, then position reversed, so the order is total and ties go
-// to the lower position), then sorts the k chosen positions ascending.
+// Selection: one kernel. Its blocks split each sequence's scores, find from that histogram
+// the bucket holding the k-th largest score, and sort tokens into selected (above it) and
+// candidates (inside it). The last block of a sequence to finish narrows the candidates with
+// further radix passes over a 64-bit key (score key, then position reversed, so the order is
+// total and ties go to the lower position) and writes the k chosen positions ascending.
 
 #include <algorithm>
 
@@ -83,6 +83,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sm.hist[i] = 0;
+    // the selection's counters start from zero whatever an earlier call left in them
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < 4 * p.B; i += blockDim.x) p.counts[i] = 0;
     if (warp == 1) tmem_alloc(&sm.tmem_base, 128);  // two 64-column fp32 accumulators
     tc_fence_before();
     __syncthreads();
@@ -91,55 +94,94 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
+        // The warp resolves the physical rows of the range's page pieces 32 at a time (lane
+        // k: piece 32 m + k), the next batch in flight while the current one is used; lane 0
+        // issues the copies.
         if (lane == 0) {
             prefetch_tensormap(&tmK);
             prefetch_tensormap(&tmK128);
             prefetch_tensormap(&tmQ);
-            const int bp = min(p.page_size, kItile);
-            int cur_b = -1, L = 0;
-            uint32_t g = 0, nq = 0;
-            bool ok = true;
-            for (int f = tr.begin; f < tr.end && ok; ++f) {
-                const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
-                if (b != cur_b) {
-                    L = load_len(p.seq_lens, b, p.max_len, p.err);
+        }
+        const int bp = min(p.page_size, kItile);
+        const int per_tile = kItile / bp;
+        const int n_pieces = (tr.end - tr.begin) * per_tile;
+        // first physical row of piece q, or -1 for a tile past its sequence's end
+        auto piece_row = [&](int q) -> int {
+            if (q >= n_pieces) return -1;
+            const int f = tr.begin + q / per_tile, sub = q % per_tile;
+            const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
+            const int L = load_len(p.seq_lens, b, p.max_len, p.err);
+            if (j * kItile >= L) return -1;
+            const int t = j * kItile + sub * bp;
+            const int tc = t < L ? t : L - 1;  // rows past the end: a valid page
+            const int pg = load_page(p.block_table, p.max_pages, p.num_pages, b,
+                                     tc / p.page_size, p.err);
+            return pg * p.page_size + (t % p.page_size);
+        };
+        int cur = piece_row(lane), nxt = piece_row(32 + lane);
+        int cur_b = -1;
+        uint32_t g = 0, nq = 0;
+        bool ok = true;
+        for (int f = tr.begin; f < tr.end && ok; ++f) {
+            const int fi = f - tr.begin;
+            int ys[kItile / 16];
+#pragma unroll
+            for (int sub = 0; sub < kItile / 16; ++sub) {
+                if (sub >= per_tile) break;
+                const int q = fi * per_tile + sub;
+                if (q > 0 && (q & 31) == 0) {
+                    cur = nxt;
+                    nxt = piece_row(q + 32 + lane);
                 }
-                if (j * kItile >= L) continue;
+                ys[sub] = __shfl_sync(0xffffffffu, cur, q & 31);
+            }
+            if (ys[0] < 0) continue;  // the tile lies past its sequence's end
+            const int b = f / p.tiles_per_b;
+            if (lane == 0) {
                 if (b != cur_b) {
                     const int qs = nq & 1;
-                    if (!(ok = mbar_wait(&sm.qempty[qs], ((nq >> 1) & 1) ^ 1, p.err))) break;
-                    mbar_arrive_expect_tx(&sm.qfull[qs], kIdxQBytes);
-                    tma_load_2d(sm.qbuf[qs], &tmQ, &sm.qfull[qs], 0, b * kHi);
-                    tma_load_2d(sm.qbuf[qs] + kIdxQBytes / 2, &tmQ, &sm.qfull[qs], 64, b * kHi);
-                    ++nq;
-                    cur_b = b;
+                    ok = mbar_wait(&sm.qempty[qs], ((nq >> 1) & 1) ^ 1, p.err);
+                    if (ok) {
+                        mbar_arrive_expect_tx(&sm.qfull[qs], kIdxQBytes);
+                        tma_load_2d(sm.qbuf[qs], &tmQ, &sm.qfull[qs], 0, b * kHi);
+                        tma_load_2d(sm.qbuf[qs] + kIdxQBytes / 2, &tmQ, &sm.qfull[qs], 64,
+                                    b * kHi);
+                    }
                 }
                 const int s = g % kIdxStages;
-                if (!(ok = mbar_wait(&sm.empty[s], ((g / kIdxStages) & 1) ^ 1, p.err))) break;
-                mbar_arrive_expect_tx(&sm.full[s], kIdxTileBytes);
-                // physical rows of the tile's page pieces; one 32 KB instruction when they
-                // are contiguous (adjacent pages, or pages of >= 128 tokens)
-                int ys[kItile / 16];
-                bool contiguous = true;
-                for (int sub = 0; sub < kItile / bp; ++sub) {
-                    const int t = j * kItile + sub * bp;
-                    const int tc = t < L ? t : L - 1;  // rows past the end: a valid page
-                    const int pg = load_page(p.block_table, p.max_pages, p.num_pages, b,
-                                             tc / p.page_size, p.err);
-                    ys[sub] = pg * p.page_size + (t % p.page_size);
-                    if (sub > 0 && ys[sub] != ys[0] + sub * bp) contiguous = false;
+                if (ok) ok = mbar_wait(&sm.empty[s], ((g / kIdxStages) & 1) ^ 1, p.err);
+                if (ok) {
+                    mbar_arrive_expect_tx(&sm.full[s], kIdxTileBytes);
+                    // one 32 KB instruction when the pieces are contiguous (adjacent pages,
+                    // or pages of >= 128 tokens)
+                    bool contiguous = true;
+#pragma unroll
+                    for (int sub = 1; sub < kItile / 16; ++sub)
+                        if (sub < per_tile && ys[sub] != ys[0] + sub * bp) contiguous = false;
+                    if (contiguous && ys[0] + kItile <= p.num_pages * p.page_size) {
+                        tma_load_3d(sm.stage[s], &tmK128, &sm.full[s], 0, ys[0], 0);
+                    } else {
+#pragma unroll
+                        for (int sub = 0; sub < kItile / 16; ++sub) {
+                            if (sub >= per_tile) break;
+                            for (int half = 0; half < 2; ++half)
+                                tma_load_2d(sm.stage[s] + half * (kIdxTileBytes / 2) +
+                                                sub * bp * 128,
+                                            &tmK, &sm.full[s], half * 64, ys[sub]);
+                        }
+                    }
                 }
-                if (contiguous && ys[0] + kItile <= p.num_pages * p.page_size) {
-                    tma_load_3d(sm.stage[s], &tmK128, &sm.full[s], 0, ys[0], 0);
-                } else {
-                    for (int sub = 0; sub < kItile / bp; ++sub)
-                        for (int half = 0; half < 2; ++half)
-                            tma_load_2d(sm.stage[s] + half * (kIdxTileBytes / 2) + sub * bp * 128,
-                                        &tmK, &sm.full[s], half * 64, ys[sub]);
-                }
-                ++g;
             }
-            // copies still in flight complete before the CTA may exit
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (b != cur_b) {
+                ++nq;
+                cur_b = b;
+            }
+            ++g;
+        }
+        // copies still in flight complete before the CTA may exit
+        if (lane == 0) {
             const uint32_t first = g > kIdxStages ? g - kIdxStages : 0;
             for (uint32_t i = first; i < g; ++i)
                 mbar_wait(&sm.full[i % kIdxStages], (i / kIdxStages) & 1, p.err);
@@ -256,6 +298,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 __global__ void __launch_bounds__(256) topk_hist_kernel(const TopkParams p) {
     __shared__ __align__(16) uint32_t h[kHistBins];
     const int b = blockIdx.y;
+    // the selection's counters start from zero whatever an earlier call left in them
+    if (blockIdx.x == 0 && threadIdx.x < 4) p.counts[4 * b + threadIdx.x] = 0;
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = 0;
     __syncthreads();
     const int L = load_len(p.lens, b, p.max_len, p.err);
@@ -294,11 +338,11 @@ __device__ __forceinline__ int block_incl_scan(int v, int* s_warp) {
 }
 
 // Find the bucket holding the k-th largest key, scanning buckets from the top. Returns the
-// bucket, the number of keys in higher buckets and the bucket's own count. All threads of
-// the block take part; s_tmp holds at least NT/32 + 3 ints.
+// bucket, the number of keys in higher buckets, the bucket's own count and (if asked) the
+// total over all buckets. All threads of the block take part; s_tmp holds NT/32 + 4 ints.
 template <int NT>
 __device__ void find_bucket(const uint32_t* bins, int nbins, int k, int& bucket, int& above,
-                            int& in_bucket, int* s_tmp) {
+                            int& in_bucket, int* s_tmp, int* total = nullptr) {
     const int per = (nbins + NT - 1) / NT;  // each thread owns `per` bins counted from the top
     const int tid = threadIdx.x;
     int local = 0;
@@ -308,6 +352,7 @@ __device__ void find_bucket(const uint32_t* bins, int nbins, int k, int& bucket,
     }
     const int incl = block_incl_scan<NT>(local, s_tmp);
     const int excl = incl - local;
+    if (tid == NT - 1) s_tmp[NT / 32 + 3] = incl;
     if (excl < k && incl >= k) {
         int cum = excl;
         for (int i = 0; i < per; ++i) {
@@ -327,6 +372,7 @@ __device__ void find_bucket(const uint32_t* bins, int nbins, int k, int& bucket,
     bucket = s_tmp[NT / 32];
     above = s_tmp[NT / 32 + 1];
     in_bucket = s_tmp[NT / 32 + 2];
+    if (total) *total = s_tmp[NT / 32 + 3];
     __syncthreads();
 }
 
@@ -348,59 +394,120 @@ __device__ __forceinline__ void load_hist(uint32_t* h, const uint32_t* src) {
     }
 }
 
-// Tokens whose bucket is above the k-th's are selected; tokens inside it are candidates.
-// Each block classifies its share of the scores in registers, counts both lists with one
-// block scan and reserves its space with one atomic per list, so the two per-sequence
-// counters see a few dozen atomics instead of one per warp and 32 scores.
-constexpr int kFiltThreads = 256;
-constexpr int kFiltPerThread = 16;
-__global__ void __launch_bounds__(kFiltThreads) topk_filter_kernel(const TopkParams p) {
+constexpr int kSelThreads = 256;
+constexpr int kSelPerThread = 16;
+constexpr int kRankMax = 256;  // a threshold bucket this small is finished by ranking its keys
+constexpr int kRadixBits = 8;  // digit of the passes after the histogram's top 11 bits
+
+__device__ __forceinline__ uint64_t composite_key(float score, int t) {
+    return (static_cast<uint64_t>(float_key(score)) << 32) |
+           static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(t));
+}
+
+// Shared-memory copies for the final step when they fit: the candidates' keys (reused by
+// every radix pass) and the bitmap of chosen positions (no global atomics, fence or
+// read-back); larger cases use the global copies.
+constexpr int kFinCandSmem = 4096;
+constexpr int kFinWordsSmem = 8192;
+constexpr int kSelDynSmem = kFinCandSmem * 8 + kFinWordsSmem * 4 + kTopkMaxK * 4;
+
+// Reserve consecutive slots of a shared counter for the lanes of a warp whose `pred` holds
+// (one atomic per warp); returns the lane's slot, or -1. Every lane of the warp calls it.
+__device__ __forceinline__ int warp_append(bool pred, int* counter) {
+    const unsigned mask = __ballot_sync(0xffffffffu, pred);
+    if (mask == 0u) return -1;
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(mask) - 1;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(counter, __popc(mask));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    return pred ? base + __popc(mask & ((1u << lane) - 1u)) : -1;
+}
+
+// The top-k selection of each sequence, given its scores and the histogram of their top 11
+// key bits. All blocks of a sequence split its scores: tokens whose bucket is above the
+// k-th's are selected (positions), tokens inside it are candidates (64-bit keys: score key,
+// then reversed position, so that ties go to the lower position). Each block classifies its
+// scores in registers, counts both lists with one block scan and reserves its space with
+// one atomic per list. The block that finishes last (a counter per sequence) narrows the
+// candidates with radix passes until the bucket holding the threshold either holds exactly
+// the keys still needed or at most kRankMax keys (then ranked against each other), marks all
+// chosen positions in a bitmap, and writes each one at its rank in ascending order (chosen
+// positions before its bitmap word, from per-word prefix counts, plus those below it in the
+// word), then leaves histogram and counters zeroed for the next call.
+__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const TopkParams p) {
     __shared__ __align__(16) uint32_t h[kHistBins];
-    __shared__ int tmp[kFiltThreads / 32 + 3];
+    __shared__ int tmp[kSelThreads / 32 + 4];
+    __shared__ int s_nlist, s_nchosen;
     __shared__ int s_base[2];
+    __shared__ int s_last;
+    extern __shared__ uint64_t sel_dyn[];
     const int b = blockIdx.y;
+    const int tid = threadIdx.x;
     const int L = load_len(p.lens, b, p.max_len, nullptr);
-    if (L <= p.k) return;  // everything is selected; the finalize kernel writes it
-    load_hist<kFiltThreads>(h, p.hist + static_cast<size_t>(b) * kHistBins);
-    __syncthreads();
-    int b1, above, in_b1;
-    find_bucket<kFiltThreads>(h, kHistBins, p.k, b1, above, in_b1, tmp);
+    int* cnt = p.counts + 4 * b;
+    uint32_t* hist = p.hist + static_cast<size_t>(b) * kHistBins;
+    int32_t* idx_out = p.topk_idx + static_cast<size_t>(b) * p.k;
+    if (L <= p.k) {
+        // every token is selected: block 0 writes the identity and clears the histogram
+        if (blockIdx.x == 0) {
+            for (int i = tid; i < p.k; i += kSelThreads) idx_out[i] = i < L ? i : -1;
+            for (int i = tid; i < kHistBins; i += kSelThreads) hist[i] = 0;
+            if (tid == 0) p.topk_count[b] = L;
+        }
+        return;
+    }
     const float* sc = p.scores + static_cast<size_t>(b) * p.score_stride;
     int* sel = p.sel + static_cast<size_t>(b) * p.k;
-    int* cand = p.cand + static_cast<size_t>(b) * p.max_len;
-    constexpr int kSpan = kFiltThreads * kFiltPerThread;
+    uint64_t* cand = p.cand + static_cast<size_t>(b) * p.max_len;
+    constexpr int kSpan = kSelThreads * kSelPerThread;
+    // all of this thread's scores of a span in flight at once (the first span's while the
+    // histogram is read)
+    float v[kSelPerThread];
+    auto load_span = [&](int base) {
+#pragma unroll
+        for (int k = 0; k < kSelPerThread; ++k) {
+            const int t = base + k * kSelThreads + tid;
+            v[k] = t < L ? __ldcg(sc + t) : 0.f;
+        }
+    };
+    load_span(blockIdx.x * kSpan);
+    load_hist<kSelThreads>(h, hist);
+    __syncthreads();
+    int b1, above, in_b1, total;
+    find_bucket<kSelThreads>(h, kHistBins, p.k, b1, above, in_b1, tmp, &total);
+    // a histogram left by anything but this call's scores does not count L tokens
+    if (tid == 0 && total != L) record_error(p.err, KVD_ERR_DEVICE_STATE);
     for (int base = blockIdx.x * kSpan; base < L; base += gridDim.x * kSpan) {
-        // 2 bits per element: 1 = selected, 2 = candidate
-        uint32_t cls = 0;
+        if (base != blockIdx.x * kSpan) load_span(base);
+        uint32_t cls = 0;  // 2 bits per element: 1 = selected, 2 = candidate
         int n_sel = 0, n_cand = 0;
 #pragma unroll
-        for (int k = 0; k < kFiltPerThread; ++k) {
-            const int t = base + k * kFiltThreads + threadIdx.x;
-            if (t < L) {
-                const int bk = static_cast<int>(float_key(sc[t]) >> 21);
-                if (bk > b1) {
-                    cls |= 1u << (2 * k);
-                    ++n_sel;
-                } else if (bk == b1) {
-                    cls |= 2u << (2 * k);
-                    ++n_cand;
-                }
+        for (int k = 0; k < kSelPerThread; ++k) {
+            const int t = base + k * kSelThreads + tid;
+            const int bk = static_cast<int>(float_key(v[k]) >> 21);
+            if (t < L && bk > b1) {
+                cls |= 1u << (2 * k);
+                ++n_sel;
+            } else if (t < L && bk == b1) {
+                cls |= 2u << (2 * k);
+                ++n_cand;
             }
         }
         // both counts in one scan (each at most 4096 per block)
         const int packed = n_sel | (n_cand << 16);
-        const int incl = block_incl_scan<kFiltThreads>(packed, tmp);
+        const int incl = block_incl_scan<kSelThreads>(packed, tmp);
         const int excl = incl - packed;
-        if (threadIdx.x == kFiltThreads - 1) {
-            s_base[0] = (incl & 0xFFFF) ? atomicAdd(p.counts + 2 * b, incl & 0xFFFF) : 0;
-            s_base[1] = (incl >> 16) ? atomicAdd(p.counts + 2 * b + 1, incl >> 16) : 0;
+        if (tid == kSelThreads - 1) {
+            s_base[0] = (incl & 0xFFFF) ? atomicAdd(cnt, incl & 0xFFFF) : 0;
+            s_base[1] = (incl >> 16) ? atomicAdd(cnt + 1, incl >> 16) : 0;
         }
         __syncthreads();
         int si = s_base[0] + (excl & 0xFFFF), ci = s_base[1] + (excl >> 16);
         __syncthreads();  // s_base read before the next span overwrites it
 #pragma unroll
-        for (int k = 0; k < kFiltPerThread; ++k) {
-            const int t = base + k * kFiltThreads + threadIdx.x;
+        for (int k = 0; k < kSelPerThread; ++k) {
+            const int t = base + k * kSelThreads + tid;
             const uint32_t c = (cls >> (2 * k)) & 3u;
             // a zeroed workspace keeps both lists inside their buffers (fewer than k tokens
             // lie above the k-th's bucket); counters left non-zero by other kernels must not
@@ -410,143 +517,226 @@ __global__ void __launch_bounds__(kFiltThreads) topk_filter_kernel(const TopkPar
                 else record_error(p.err, KVD_ERR_DEVICE_STATE);
                 ++si;
             } else if (c == 2u) {
-                if (ci >= 0 && ci < p.max_len) cand[ci] = t;
+                if (ci >= 0 && ci < p.max_len) cand[ci] = composite_key(v[k], t);
                 else record_error(p.err, KVD_ERR_DEVICE_STATE);
                 ++ci;
             }
         }
     }
-}
-
-constexpr int kFinThreads = 1024;
-
-__device__ __forceinline__ uint64_t composite_key(float score, int t) {
-    return (static_cast<uint64_t>(float_key(score)) << 32) |
-           static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(t));
-}
-
-// Shared-memory copies of the finalize step when they fit: the candidates' composite keys
-// (read once from global memory, then reused by every radix pass) and the bitmap of chosen
-// positions (no global atomics, fence or read-back).
-constexpr int kFinCandSmem = 4096;
-constexpr int kFinWordsSmem = 8192;
-constexpr int kFinDynSmem = kFinCandSmem * 8 + kFinWordsSmem * 4;
-
-// One CTA per sequence: exact threshold among the candidates, then the output in
-// ascending position order from a bitmap of the chosen positions and a prefix scan.
-__global__ void __launch_bounds__(kFinThreads) topk_finalize_kernel(const TopkParams p) {
-    __shared__ __align__(16) uint32_t h[kHistBins];
-    __shared__ int tmp[kFinThreads / 32 + 3];
-    extern __shared__ uint64_t fin_dyn[];
-    uint64_t* keys = fin_dyn;
-    uint32_t* sbits = reinterpret_cast<uint32_t*>(fin_dyn + kFinCandSmem);
-    const int b = blockIdx.x;
-    const int tid = threadIdx.x;
-    const int L = load_len(p.lens, b, p.max_len, nullptr);
-    int32_t* idx_out = p.topk_idx + static_cast<size_t>(b) * p.k;
-    const int count = min(p.k, L);
-    if (tid == 0) p.topk_count[b] = count;
-    if (L <= p.k) {
-        for (int i = tid; i < p.k; i += kFinThreads) idx_out[i] = i < L ? i : -1;
-    } else {
-        const float* sc = p.scores + static_cast<size_t>(b) * p.score_stride;
-        const int* cand = p.cand + static_cast<size_t>(b) * p.max_len;
-        const int* sel = p.sel + static_cast<size_t>(b) * p.k;
-        const int n_words = (L + 31) / 32;
-        const bool bits_in_smem = n_words <= kFinWordsSmem;
-        uint32_t* bits = bits_in_smem
-                             ? sbits
-                             : p.bitmap + static_cast<size_t>(b) * ((p.max_len + 31) / 32);
-        load_hist<kFinThreads>(h, p.hist + static_cast<size_t>(b) * kHistBins);
-        if (bits_in_smem)
-            for (int i = tid; i < n_words; i += kFinThreads) sbits[i] = 0;
-        __syncthreads();
-        int b1, above, in_b;
-        find_bucket<kFinThreads>(h, kHistBins, p.k, b1, above, in_b, tmp);
-        int nc = p.counts[2 * b + 1];
-        if (nc < 0 || nc > L || above < 0 || above >= p.k) {  // not a zeroed workspace
-            if (tid == 0) record_error(p.err, KVD_ERR_DEVICE_STATE);
-            nc = min(max(nc, 0), L);
-            above = min(max(above, 0), p.k - 1);
-        }
-        // the candidates' keys (a position outside [0, L) only follows a non-zeroed
-        // workspace; its key is 0 and it is never chosen below)
-        const bool keys_in_smem = nc <= kFinCandSmem;
-        auto cand_key = [&](int i) -> uint64_t {
-            if (keys_in_smem) return keys[i];
-            const int t = cand[i];
-            return (t >= 0 && t < L) ? composite_key(sc[t], t) : 0ull;
-        };
-        if (keys_in_smem) {
-            for (int i = tid; i < nc; i += kFinThreads) {
-                const int t = cand[i];
-                keys[i] = (t >= 0 && t < L) ? composite_key(sc[t], t) : 0ull;
-            }
-            __syncthreads();
-        }
-        int need = p.k - above;  // to take from the candidates (>= 1)
-        // radix passes over the 64-bit composite key below its top 11 bits, until the
-        // bucket that holds the threshold holds exactly the keys still needed
-        uint64_t prefix = static_cast<uint64_t>(b1);
-        int done_bits = 11;
-        while (done_bits < 64 && in_b != need) {
-            const int wdt = min(11, 64 - done_bits);
-            const int shift = 64 - done_bits - wdt;
-            const int nb = 1 << wdt;
-            for (int i = tid; i < nb; i += kFinThreads) h[i] = 0;
-            __syncthreads();
-            for (int i = tid; i < nc; i += kFinThreads) {
-                const uint64_t ck = cand_key(i);
-                if (ck != 0ull && (ck >> (64 - done_bits)) == prefix)
-                    atomicAdd(&h[static_cast<int>((ck >> shift) & (nb - 1))], 1u);
-            }
-            __syncthreads();
-            int bb, ab;
-            find_bucket<kFinThreads>(h, nb, need, bb, ab, in_b, tmp);
-            prefix = (prefix << wdt) | static_cast<uint64_t>(bb);
-            need -= ab;
-            done_bits += wdt;
-        }
-        // every key at or above T is chosen (T: the threshold prefix, low bits zero)
-        const uint64_t T = done_bits < 64 ? prefix << (64 - done_bits) : prefix;
-        for (int i = tid; i < above; i += kFinThreads) {
-            const int t = sel[i];
-            if (t >= 0 && t < L) atomicOr(bits + (t >> 5), 1u << (t & 31));
-        }
-        for (int i = tid; i < nc; i += kFinThreads) {
-            const uint64_t ck = cand_key(i);
-            if (ck != 0ull && ck >= T) {
-                const int t = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(ck));
-                atomicOr(bits + (t >> 5), 1u << (t & 31));
-            }
-        }
-        if (!bits_in_smem) __threadfence();  // global bit updates land in L2 first
-        __syncthreads();
-        // positions in ascending order: popcount prefix scan over the bitmap words
-        const int per = (n_words + kFinThreads - 1) / kFinThreads;
-        const int w0 = tid * per;
-        int local = 0;
-        for (int i = 0; i < per; ++i)
-            if (w0 + i < n_words)
-                local += __popc(bits_in_smem ? sbits[w0 + i] : __ldcg(bits + w0 + i));
-        int pos = block_incl_scan<kFinThreads>(local, tmp) - local;
-        for (int i = 0; i < per; ++i) {
-            if (w0 + i >= n_words) break;
-            uint32_t w = bits_in_smem ? sbits[w0 + i] : __ldcg(bits + w0 + i);
-            if (!bits_in_smem) bits[w0 + i] = 0;  // leave the global bitmap clear
-            while (w) {
-                const int bit = __ffs(w) - 1;
-                if (pos < p.k) idx_out[pos] = (w0 + i) * 32 + bit;
-                ++pos;
-                w &= w - 1;
-            }
+    // the last block of the sequence finishes it
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(cnt + 2, 1) == static_cast<int>(gridDim.x) - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    uint64_t* keys = sel_dyn;
+    uint32_t* sbits = reinterpret_cast<uint32_t*>(sel_dyn + kFinCandSmem);
+    int* chosen = reinterpret_cast<int*>(sbits + kFinWordsSmem);  // chosen candidates' positions
+    const int n_words = (L + 31) / 32;
+    const bool bits_in_smem = n_words <= kFinWordsSmem;
+    uint32_t* bits =
+        bits_in_smem ? sbits : p.bitmap + static_cast<size_t>(b) * ((p.max_len + 31) / 32);
+    // the candidate keys (as many as shared memory holds) and the selected positions, all in
+    // flight together with the candidate count
+    constexpr int kKeyPer = kFinCandSmem / kSelThreads;
+    constexpr int kPosPer = kTopkMaxK / kSelThreads;
+    static_assert(kKeyPer * kSelThreads == kFinCandSmem && kPosPer * kSelThreads == kTopkMaxK, "");
+    const int n_pre = min(kFinCandSmem, p.max_len);
+    const int above_c = min(max(above, 0), p.k - 1);
+    uint64_t kv[kKeyPer];
+    int tv[kPosPer];
+#pragma unroll
+    for (int r = 0; r < kKeyPer; ++r) {
+        const int i = r * kSelThreads + tid;
+        kv[r] = i < n_pre ? __ldcg(cand + i) : 0ull;
+    }
+#pragma unroll
+    for (int r = 0; r < kPosPer; ++r) {
+        const int i = r * kSelThreads + tid;
+        tv[r] = i < above_c ? __ldcg(sel + i) : -1;
+    }
+    int nc = __ldcg(cnt + 1);
+    if (nc < 0 || nc > L || above != above_c) {  // not a zeroed workspace
+        if (tid == 0) record_error(p.err, KVD_ERR_DEVICE_STATE);
+        nc = min(max(nc, 0), L);
+        above = above_c;
+    }
+    const bool keys_in_smem = nc <= kFinCandSmem;
+    if (keys_in_smem) {
+#pragma unroll
+        for (int r = 0; r < kKeyPer; ++r) {
+            const int i = r * kSelThreads + tid;
+            if (i < nc) keys[i] = kv[r];
         }
     }
-    // leave the histogram and counters zeroed for the next call
+    if (bits_in_smem)
+        for (int i = tid; i < n_words; i += kSelThreads) sbits[i] = 0;
     __syncthreads();
-    for (int i = tid; i < kHistBins; i += kFinThreads)
-        p.hist[static_cast<size_t>(b) * kHistBins + i] = 0;
-    if (tid < 2) p.counts[2 * b + tid] = 0;
+    auto cand_key = [&](int i) -> uint64_t { return keys_in_smem ? keys[i] : __ldcg(cand + i); };
+    auto key_pos = [](uint64_t ck) { return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(ck)); };
+    const int need0 = p.k - above;  // to take from the candidates (>= 1)
+#pragma unroll
+    for (int r = 0; r < kPosPer; ++r)
+        if (tv[r] >= 0 && tv[r] < L) atomicOr(bits + (tv[r] >> 5), 1u << (tv[r] & 31));
+    // radix passes (8-bit digits, a bin per thread) over the 64-bit key below its top 11
+    // bits, until the bucket that holds the threshold either holds exactly the keys still
+    // needed or is small enough to rank
+    int need = need0;
+    uint64_t prefix = static_cast<uint64_t>(b1);
+    int done_bits = 11;
+    int in_b = in_b1;
+    while (done_bits < 64 && in_b != need && in_b > kRankMax) {
+        const int wdt = min(kRadixBits, 64 - done_bits);
+        const int shift = 64 - done_bits - wdt;
+        const int nb = 1 << wdt;
+        for (int i = tid; i < nb; i += kSelThreads) h[i] = 0;
+        __syncthreads();
+        for (int i = tid; i < nc; i += kSelThreads) {
+            const uint64_t ck = cand_key(i);
+            if ((ck >> (64 - done_bits)) == prefix)
+                atomicAdd(&h[static_cast<int>((ck >> shift) & (nb - 1))], 1u);
+        }
+        __syncthreads();
+        int bb, ab;
+        find_bucket<kSelThreads>(h, nb, need, bb, ab, in_b, tmp);
+        prefix = (prefix << wdt) | static_cast<uint64_t>(bb);
+        need -= ab;
+        done_bits += wdt;
+    }
+    // keys above the bucket are chosen; the bucket's keys all are when it holds exactly the
+    // ones needed, else they go to a short list and are chosen by rank (keys are distinct:
+    // the position is part of the key). Chosen positions are marked in the bitmap and listed.
+    const bool rank_bucket = in_b != need;
+    uint64_t* lst = reinterpret_cast<uint64_t*>(h);  // kRankMax keys
+    if (tid == 0) {
+        s_nlist = 0;
+        s_nchosen = 0;
+    }
+    __syncthreads();
+    auto choose = [&](bool pick, int t) {  // all lanes of the warp take part
+        const bool ok = pick && t >= 0 && t < L;
+        const int slot = warp_append(ok, &s_nchosen);
+        if (ok) {
+            atomicOr(bits + (t >> 5), 1u << (t & 31));
+            if (slot < kTopkMaxK) chosen[slot] = t;
+        }
+    };
+    for (int i0 = 0; i0 < nc; i0 += kSelThreads) {
+        const int i = i0 + tid;
+        const uint64_t ck = i < nc ? cand_key(i) : 0ull;
+        const uint64_t top = done_bits < 64 ? ck >> (64 - done_bits) : ck;
+        const bool above_b = i < nc && (top > prefix || (top == prefix && !rank_bucket));
+        choose(above_b, key_pos(ck));
+        const int slot = warp_append(i < nc && top == prefix && rank_bucket, &s_nlist);
+        if (slot >= 0 && slot < kRankMax) lst[slot] = ck;
+    }
+    __syncthreads();
+    if (rank_bucket) {
+        const int nl = min(s_nlist, kRankMax);
+        if (tid == 0 && s_nlist != in_b) record_error(p.err, KVD_ERR_DEVICE_STATE);
+        static_assert(kRankMax <= kSelThreads, "one list key per thread");
+        const uint64_t ck = tid < nl ? lst[tid] : 0ull;
+        int rank = 0;
+        if (tid < nl)
+            for (int jj = 0; jj < nl; ++jj) rank += lst[jj] > ck ? 1 : 0;
+        choose(tid < nl && rank < need, key_pos(ck));
+    }
+    if (!bits_in_smem) __threadfence();  // global bit updates land in L2 first
+    __syncthreads();
+    if (tid == 0 && above + s_nchosen != p.k) record_error(p.err, KVD_ERR_DEVICE_STATE);
+    if (bits_in_smem) {
+        // every chosen position goes straight to its rank: the chosen positions before its
+        // bitmap word (a prefix count per word, in the key buffer that is no longer read)
+        // plus those below it in its own word
+        int* wpre = reinterpret_cast<int*>(keys);
+        static_assert(kFinCandSmem * 2 >= kFinWordsSmem, "");
+        const int per = ((n_words + kSelThreads - 1) / kSelThreads + 3) & ~3;
+        const int w0 = min(n_words, tid * per), w1 = min(n_words, w0 + per);
+        int c = 0;
+        for (int wi = w0; wi < w1; wi += 4) {
+            if (wi + 4 <= w1) {
+                const uint4 x = *reinterpret_cast<const uint4*>(sbits + wi);
+                c += __popc(x.x) + __popc(x.y) + __popc(x.z) + __popc(x.w);
+            } else {
+                for (int r = wi; r < w1; ++r) c += __popc(sbits[r]);
+            }
+        }
+        int run = block_incl_scan<kSelThreads>(c, tmp) - c;
+        for (int wi = w0; wi < w1; wi += 4) {
+            if (wi + 4 <= w1) {
+                const uint4 x = *reinterpret_cast<const uint4*>(sbits + wi);
+                int4 o;
+                o.x = run;
+                o.y = o.x + __popc(x.x);
+                o.z = o.y + __popc(x.y);
+                o.w = o.z + __popc(x.z);
+                run = o.w + __popc(x.w);
+                *reinterpret_cast<int4*>(wpre + wi) = o;
+            } else {
+                for (int r = wi; r < w1; ++r) {
+                    wpre[r] = run;
+                    run += __popc(sbits[r]);
+                }
+            }
+        }
+        __syncthreads();
+        auto place = [&](int t) {
+            const int wi = t >> 5;
+            const int rk = wpre[wi] + __popc(sbits[wi] & ((1u << (t & 31)) - 1u));
+            if (rk >= 0 && rk < p.k) idx_out[rk] = t;
+        };
+#pragma unroll
+        for (int r = 0; r < kPosPer; ++r)
+            if (tv[r] >= 0 && tv[r] < L) place(tv[r]);
+        const int n_ch = min(s_nchosen, kTopkMaxK);
+        for (int i = tid; i < n_ch; i += kSelThreads) place(chosen[i]);
+    } else {
+        // a bitmap in global memory: each warp owns a contiguous run of words, each lane 16
+        // consecutive words a round; warp totals first, then one warp scan a round, after
+        // which every lane writes its own positions and clears its words
+        constexpr int kWarps = kSelThreads / 32;
+        constexpr int kLaneWords = 16;
+        const int warp = tid / 32, lane = tid % 32;
+        const int wrun = ((n_words + kWarps - 1) / kWarps + kLaneWords - 1) & ~(kLaneWords - 1);
+        const int wbeg = min(n_words, warp * wrun), wend = min(n_words, wbeg + wrun);
+        int cnt_w = 0;
+        for (int i = wbeg + kLaneWords * lane; i < wend; i += 32 * kLaneWords)
+            for (int r = 0; r < kLaneWords && i + r < wend; ++r) cnt_w += __popc(__ldcg(bits + i + r));
+        for (int off = 16; off; off >>= 1) cnt_w += __shfl_xor_sync(0xffffffffu, cnt_w, off);
+        if (lane == 0) tmp[warp] = cnt_w;
+        __syncthreads();
+        int pos = 0;
+        for (int w2 = 0; w2 < warp; ++w2) pos += tmp[w2];
+        __syncthreads();
+        for (int i0 = wbeg; i0 < wend; i0 += 32 * kLaneWords) {
+            const int i = i0 + kLaneWords * lane;
+            int c = 0;
+            for (int r = 0; r < kLaneWords && i + r < wend; ++r) c += __popc(__ldcg(bits + i + r));
+            int incl = c;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += n;
+            }
+            int q = pos + incl - c;
+            for (int r = 0; r < kLaneWords && i + r < wend; ++r) {
+                uint32_t m = __ldcg(bits + i + r);
+                bits[i + r] = 0;  // leave the bitmap clear
+                while (m) {
+                    const int bit = __ffs(m) - 1;
+                    if (q < p.k) idx_out[q] = (i + r) * 32 + bit;
+                    ++q;
+                    m &= m - 1;
+                }
+            }
+            pos += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    if (tid == 0) p.topk_count[b] = p.k;
+    // leave the histogram and counters zeroed for the next call
+    for (int i = tid; i < kHistBins; i += kSelThreads) hist[i] = 0;
+    if (tid < 3) cnt[tid] = 0;
 }
 
 }  // namespace
@@ -571,18 +761,17 @@ int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensor
 int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream) {
     const int blocks_per_b = std::max(1, std::min(64, (p.max_len + 4095) / 4096));
     if (need_hist) topk_hist_kernel<<<dim3(blocks_per_b, p.B), 256, 0, stream>>>(p);
-    const int filt_per_b =
-        std::max(1, std::min(64, (p.max_len + kFiltThreads * kFiltPerThread - 1) /
-                                     (kFiltThreads * kFiltPerThread)));
-    topk_filter_kernel<<<dim3(filt_per_b, p.B), kFiltThreads, 0, stream>>>(p);
-    static int fin_configured = 0;
-    if (!fin_configured) {
-        if (cudaFuncSetAttribute(topk_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kFinDynSmem) != cudaSuccess)
+    static int configured = 0;
+    if (!configured) {
+        if (cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSelDynSmem) != cudaSuccess)
             return KVD_ERR_CUDA;
-        fin_configured = 1;
+        configured = 1;
     }
-    topk_finalize_kernel<<<p.B, kFinThreads, kFinDynSmem, stream>>>(p);
+    const int sel_per_b =
+        std::max(1, std::min(64, (p.max_len + kSelThreads * kSelPerThread - 1) /
+                                     (kSelThreads * kSelPerThread)));
+    topk_select_kernel<<<dim3(sel_per_b, p.B), kSelThreads, kSelDynSmem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
 

@@ -73,6 +73,7 @@ struct IdxParams {
     float* scores;             // [B, score_stride]
     long long score_stride;
     uint32_t* hist;            // [B, 2048] top-11-bit key histogram
+    int* counts;               // [B, 4] selection counters, zeroed here for the selection
     int* err;
     int B, page_size, max_pages, num_pages, max_len, tiles_per_b;
 };
@@ -82,9 +83,9 @@ struct TopkParams {
     long long score_stride;
     const int32_t* lens;       // [B]
     uint32_t* hist;            // [B, 2048]
-    int* counts;               // [B, 2]: selected, candidates
-    int* sel;                  // [B, k]
-    int* cand;                 // [B, max_len]
+    int* counts;               // [B, 4]: selected, candidates, blocks done, (pad)
+    int* sel;                  // [B, k] selected positions
+    uint64_t* cand;            // [B, max_len] candidates' (score key, reversed position) keys
     uint32_t* bitmap;          // [B, ceil(max_len / 32)] chosen positions (kept zero)
     int32_t* topk_idx;         // [B, k]
     int32_t* topk_count;       // [B]

@@ -88,6 +88,31 @@ static_assert(kMlaSmem <= 227 * 1024, "MLA shared memory");
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
 
+// Transpose an 8 x 8 array of 16-byte chunks held by each group of eight lanes: lane i of the
+// group holds chunk j of row i in ch[j] on entry and chunk i of row j on exit (three
+// butterfly stages of shuffles). All lanes of the warp take part.
+__device__ __forceinline__ void transpose8_chunks(float4 (&ch)[8], int lane) {
+#pragma unroll
+    for (int m = 4; m >= 1; m >>= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j & m) continue;
+            const int hi = j | m;
+            float4 send = upper ? ch[j] : ch[hi];
+            float4 recv;
+            recv.x = __shfl_xor_sync(0xffffffffu, send.x, m);
+            recv.y = __shfl_xor_sync(0xffffffffu, send.y, m);
+            recv.z = __shfl_xor_sync(0xffffffffu, send.z, m);
+            recv.w = __shfl_xor_sync(0xffffffffu, send.w, m);
+            if (upper)
+                ch[j] = recv;
+            else
+                ch[hi] = recv;
+        }
+    }
+}
+
 // Score product of one tile: S (TMEM) = q_r (TMEM, NK 16-dim k-steps) x this CTA's
 // 64-dim boxes of the tile (shared memory, K-major). Fully unrolled with the descriptors
 // advanced by constants, so that one thread keeps the tensor pipe fed.
@@ -265,35 +290,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             } else {
                 // gather the selected rows: each lane copies rows lane and lane + 32 of the
-                // tile; a tile's arrival is signalled once the next tile's copies are issued
+                // tile (one row per lane and instruction issues faster than one row per
+                // instruction); a tile's arrival is signalled once the next tile's copies are
+                // issued. Row sources are resolved a tile ahead (token indices two tiles
+                // ahead), so that neither dependent load waits in front of the copies.
                 const int L = load_len(p.seq_lens, b, p.max_len, nullptr);
                 const __nv_bfloat16* cpool = reinterpret_cast<const __nv_bfloat16*>(p.c_pool);
                 const int32_t* idx = p.idx + static_cast<size_t>(b) * p.idx_stride;
+                auto has_row = [&](int i, int rr) {
+                    return i < nt && lo + i * kTok + lane + 32 * rr < hi;
+                };
+                auto tok_of = [&](int i, int rr) -> int {
+                    return has_row(i, rr) ? idx[lo + i * kTok + lane + 32 * rr] : -1;
+                };
+                auto page_of = [&](int t) -> int {
+                    return (t >= 0 && t < L) ? load_page(p.block_table, p.max_pages, p.num_pages,
+                                                         b, t / p.page_size, p.err)
+                                             : 0;
+                };
+                // the row's first element of this CTA's dims, or null for a zero row
+                auto src_of = [&](bool has, int t, int pg) -> const __nv_bfloat16* {
+                    if (!has) return nullptr;
+                    if (t < 0 || t >= L) {
+                        record_error(p.err, KVD_ERR_DEVICE_OOB);
+                        return nullptr;
+                    }
+                    return cpool +
+                           (static_cast<size_t>(pg) * p.page_size + t % p.page_size) * kDqk + dim0;
+                };
+                const __nv_bfloat16* src_cur[2];
+                int t_nxt[2];
+                {
+                    const int t0a = tok_of(0, 0), t0b = tok_of(0, 1);
+                    t_nxt[0] = tok_of(1, 0);
+                    t_nxt[1] = tok_of(1, 1);
+                    const int pa = page_of(t0a), pb = page_of(t0b);
+                    src_cur[0] = src_of(has_row(0, 0), t0a, pa);
+                    src_cur[1] = src_of(has_row(0, 1), t0b, pb);
+                }
                 for (int i = 0; i < nt && ok; ++i, ++g) {
                     const int s = g % kStages;
                     if (lane == 0) ok = mbar_wait(&sm.empty[s], ((g / kStages) & 1) ^ 1, p.err);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
+                    const int t_nn0 = tok_of(i + 2, 0), t_nn1 = tok_of(i + 2, 1);
+                    const int pg_n0 = page_of(t_nxt[0]), pg_n1 = page_of(t_nxt[1]);
                     const uint32_t base = smem_u32(sm.stage[s]);
+#pragma unroll
                     for (int rr = 0; rr < 2; ++rr) {
                         const int r = lane + 32 * rr;
-                        const int j = lo + i * kTok + r;
-                        const int t = j < hi ? idx[j] : -1;
-                        const bool valid = t >= 0 && t < L;
-                        if (j < hi && !valid) record_error(p.err, KVD_ERR_DEVICE_OOB);
-                        const __nv_bfloat16* src = cpool;
-                        if (valid) {
-                            const int pg = load_page(p.block_table, p.max_pages, p.num_pages, b,
-                                                     t / p.page_size, p.err);
-                            src = cpool +
-                                  (static_cast<size_t>(pg) * p.page_size + t % p.page_size) * kDqk +
-                                  dim0;
-                        }
+                        const __nv_bfloat16* src = src_cur[rr];
                         for (int c = 0; c < nbox * 8; ++c) {
                             const int bx = c >> 3, cc = c & 7;
                             const uint32_t dst =
                                 base + bx * kTileBox + r * 128 + ((cc ^ (r & 7)) << 4);
-                            cp_async_16(dst, valid ? src + c * 8 : cpool, valid ? 16u : 0u);
+                            cp_async_16(dst, src ? src + c * 8 : cpool, src ? 16u : 0u);
                         }
                     }
                     cp_async_commit();
@@ -302,6 +353,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         fence_proxy_async_smem();
                         mbar_arrive(&sm.full[(g - 1) % kStages]);
                     }
+                    src_cur[0] = src_of(has_row(i + 1, 0), t_nxt[0], pg_n0);
+                    src_cur[1] = src_of(has_row(i + 1, 1), t_nxt[1], pg_n1);
+                    t_nxt[0] = t_nn0;
+                    t_nxt[1] = t_nn1;
                 }
             }
         });
@@ -416,6 +471,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     (static_cast<size_t>(b) * kH + h) * kDqk + dim0);
                 constexpr int kQBoxes = (kNBox + kGroups - 1) / kGroups;
                 const int bx0 = grp * kQBoxes, bx1 = min(nbox, bx0 + kQBoxes);
+                // the group's rows of this piece's and the next sequence's queries head for L2
+                // first, so that only the first box waits on memory
+#pragma unroll
+                for (int bi = 0; bi < kQBoxes; ++bi) {
+                    if (bx0 + bi >= bx1) continue;
+                    prefetch_l2(qrow + (bx0 + bi) * 8);
+                    if (b + 1 < p.B)
+                        prefetch_l2(qrow + static_cast<size_t>(kH) * kDqk / 8 + (bx0 + bi) * 8);
+                }
                 // one 64-dim box (32 columns) at a time: few registers, outside the tile loop
 #pragma unroll 1
                 for (int bx = bx0; bx < bx1; ++bx) {
@@ -595,20 +659,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const size_t slot = static_cast<size_t>(cl) + b;
                 const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-                float* po = p.part_o + (slot * kH + h) * kDv + rank * 256;
+                // rows of the eight heads of this lane's group of eight lanes; after the
+                // transpose below, lane i of the group holds 16-byte chunk i of each of them
+                float* po = p.part_o +
+                            (slot * kH + (h & ~7)) * kDv + rank * 256 + (lane & 7) * 4;
                 // the groups split this CTA's 256 value dims in 32-column slices
                 constexpr int kOSlices = (8 + kGroups - 1) / kGroups;
                 for (int c = grp * kOSlices; c < min(8, (grp + 1) * kOSlices); ++c) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(trow + kColO + c * 32, r);
                     tmem_ld_wait(r);
+                    float4 ch[8];
 #pragma unroll
-                    for (int kk = 0; kk < 32; kk += 4)
-                        __stcg(reinterpret_cast<float4*>(po + c * 32 + kk),
-                               make_float4(__uint_as_float(r[kk]) * inv,
-                                           __uint_as_float(r[kk + 1]) * inv,
-                                           __uint_as_float(r[kk + 2]) * inv,
-                                           __uint_as_float(r[kk + 3]) * inv));
+                    for (int jj = 0; jj < 8; ++jj)
+                        ch[jj] = make_float4(__uint_as_float(r[4 * jj]) * inv,
+                                             __uint_as_float(r[4 * jj + 1]) * inv,
+                                             __uint_as_float(r[4 * jj + 2]) * inv,
+                                             __uint_as_float(r[4 * jj + 3]) * inv);
+                    transpose8_chunks(ch, lane);
+                    // each store writes four whole 128-byte rows (one per group of lanes)
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj)
+                        __stcg(reinterpret_cast<float4*>(po + jj * kDv + c * 32), ch[jj]);
                 }
                 if (rank == 0 && grp == 0)
                     p.part_lse[slot * kH + h] = l_tot > 0.f ? m_last + log2f(l_tot) : neg_inf();

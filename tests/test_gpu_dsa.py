@@ -106,6 +106,27 @@ def test_topk_alone_bit_exact(kvd, case):
         assert np.all(got[n:] == -1)
 
 
+@pytest.mark.parametrize("case", ["normal", "ties"])
+def test_topk_long_sequences(kvd, case):
+    # past 262,144 tokens the chosen-position bitmap lives in the workspace, not in shared
+    # memory; a second call checks that the first left it clear
+    B, stride = 2, 300000
+    lens = torch.tensor([300000, 270001], dtype=torch.int32)
+    if case == "normal":
+        s = W.normal((B, stride), 905, 1.0, torch.float32)
+    else:
+        s = torch.randint(-30, 30, (B, stride), generator=torch.Generator().manual_seed(906)).float()
+    ws = kvd.Workspace(torch.device("cuda"))
+    for _ in range(2):
+        idx, cnt = kvd.dsa_topk(s.cuda(), lens.cuda(), k=2048, workspace=ws)
+        torch.cuda.synchronize()
+        for b in range(B):
+            L = int(lens[b])
+            ref = oracle.topk(s[b, :L].numpy().astype(np.float64), 2048)
+            assert int(cnt[b]) == 2048
+            assert np.array_equal(idx[b].cpu().numpy(), ref), (case, b)
+
+
 def test_topk_repeat_calls(kvd):
     s = W.normal((2, 50000), 904, 1.0, torch.float32).cuda()
     lens = torch.tensor([50000, 40000], dtype=torch.int32).cuda()
