@@ -55,6 +55,13 @@ constexpr int kWarpLoad = kSoftWarps, kWarpQK = kSoftWarps + 1, kWarpPV = kSoftW
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Part of a cluster's tile range inside one sequence: tokens [lo, hi) of sequence b, which
+// holds `items` tokens (or selected tokens).
+struct Piece {
+    int b, items, lo, hi;
+};
+constexpr int kMaxPieces = 32;
+
 struct MlaSmem {
     uint8_t stage[kStages][kStageBytes];   // offset 0, 1024-aligned
     // Partial scores cross in two halves of 32 columns (16 KB each), so that the next
@@ -76,6 +83,11 @@ struct MlaSmem {
     uint64_t hand[kGroups];  // group published its running max
     uint64_t ofree;          // O of the current piece has been read (eight softmax warps)
     uint32_t tmem_base;
+    // the cluster's schedule, built once: tile range and its pieces (n_pieces < 0: more
+    // pieces than the table holds, walked from the sequence lengths instead)
+    long long t0, t1;
+    int n_pieces;
+    Piece piece[kMaxPieces];
 };
 
 // Tensor-memory columns (all 512): this CTA's query slice (bf16 pairs, up to 320 dims), one
@@ -146,21 +158,65 @@ __device__ __forceinline__ int seq_items(const MlaParams& p, int b, int* err) {
     return load_len(p.seq_lens, b, p.max_len, err);
 }
 
-// Total tiles of all sequences, and cluster c's range [t0, t1) of the tile list.
+// Cluster c's range [t0, t1) of the list of all sequences' tiles and the pieces it meets,
+// into shared memory. One warp: the lanes load 32 sequences' lengths at a time and a warp
+// scan turns their tile counts into tile offsets, so that the walk costs one memory round
+// trip per 32 sequences.
 template <bool kSparse>
-__device__ __forceinline__ void cluster_range(const MlaParams& p, int c, int n_clusters,
-                                              long long& t0, long long& t1, int* err) {
+__device__ void build_schedule(const MlaParams& p, int c, int n_clusters, MlaSmem& sm,
+                               int lane, int* err) {
     long long T = 0;
-    for (int b = 0; b < p.B; ++b) T += (seq_items<kSparse>(p, b, err) + kTok - 1) / kTok;
-    t0 = T * c / n_clusters;
-    t1 = T * (c + 1) / n_clusters;
+    for (int base = 0; base < p.B; base += 32) {
+        const int bb = base + lane;
+        int n = bb < p.B ? (seq_items<kSparse>(p, bb, err) + kTok - 1) / kTok : 0;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+        T += n;
+    }
+    const long long t0 = T * c / n_clusters, t1 = T * (c + 1) / n_clusters;
+    long long run = 0;
+    int np = 0;
+    for (int base = 0; base < p.B && run < t1; base += 32) {
+        const int bb = base + lane;
+        const int items = bb < p.B ? seq_items<kSparse>(p, bb, nullptr) : 0;
+        const int n = (items + kTok - 1) / kTok;
+        int incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        const long long sb = run + incl - n;  // the lane's sequence's first tile
+        const long long lo_t = max(t0, sb) - sb, hi_t = min(t1, sb + n) - sb;
+        const bool has = bb < p.B && hi_t > lo_t;
+        const unsigned m = __ballot_sync(0xffffffffu, has);
+        const int slot = np + __popc(m & ((1u << lane) - 1u));
+        if (has && slot < kMaxPieces)
+            sm.piece[slot] = Piece{bb, items, static_cast<int>(lo_t) * kTok,
+                                   min(static_cast<int>(hi_t) * kTok, items)};
+        np += __popc(m);
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+        sm.t0 = t0;
+        sm.t1 = t1;
+        sm.n_pieces = np <= kMaxPieces ? np : -1;
+    }
 }
 
 // Calls f(b, items, lo, hi, k) for the k-th piece of the range: tokens [lo, hi) of
 // sequence b (multiples of 64 except at the end of the sequence).
 template <bool kSparse, typename F>
-__device__ __forceinline__ void for_each_piece(const MlaParams& p, long long t0, long long t1,
-                                               F&& f) {
+__device__ __forceinline__ void for_each_piece(const MlaParams& p, const MlaSmem& sm, F&& f) {
+    const int np = sm.n_pieces;
+    if (np >= 0) {
+        for (int k = 0; k < np; ++k) {
+            const Piece pc = sm.piece[k];
+            f(pc.b, pc.items, pc.lo, pc.hi, k);
+        }
+        return;
+    }
+    const long long t0 = sm.t0, t1 = sm.t1;
     long long base = 0;
     int k = 0;
     for (int b = 0; b < p.B && base < t1; ++b) {
@@ -191,8 +247,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0) record_error(p.err, KVD_ERR_CUDA);
         return;
     }
-    long long t0, t1;
-    cluster_range<kSparse>(p, cl, n_cl, t0, t1, (rank == 0 && threadIdx.x == 0) ? p.err : nullptr);
+    if (warp == 0)
+        build_schedule<kSparse>(p, cl, n_cl, sm, lane, rank == 0 ? p.err : nullptr);
+    __syncthreads();
+    const long long t0 = sm.t0, t1 = sm.t1;
     if (t0 >= t1) return;  // both CTAs of the pair take this exit together
     const int n_tiles = static_cast<int>(t1 - t0);
     const int nbox = rank == 0 ? 4 : 5;   // 64-dim boxes this CTA loads
@@ -244,7 +302,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         int g = 0;  // tile index within this CTA's range
         bool ok = true;
-        for_each_piece<kSparse>(p, t0, t1, [&](int b, int items, int lo, int hi, int) {
+        for_each_piece<kSparse>(p, sm, [&](int b, int items, int lo, int hi, int) {
             if (!ok) return;
             const int nt = (hi - lo + kTok - 1) / kTok;
             if (!kSparse) {
@@ -379,7 +437,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int g = 0;
             bool ok = true;
-            for_each_piece<kSparse>(p, t0, t1, [&](int, int, int lo, int hi, int k) {
+            for_each_piece<kSparse>(p, sm, [&](int, int, int lo, int hi, int k) {
                 if (!ok || !(ok = mbar_wait(&sm.qready, k & 1, p.err))) return;
                 const int nt = (hi - lo + kTok - 1) / kTok;
                 for (int i = 0; i < nt; ++i, ++g) {
@@ -401,7 +459,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int g = 0;
             bool ok = true;
-            for_each_piece<kSparse>(p, t0, t1, [&](int, int, int lo, int hi, int k) {
+            for_each_piece<kSparse>(p, sm, [&](int, int, int lo, int hi, int k) {
                 if (!ok) return;
                 const int nt = (hi - lo + kTok - 1) / kTok;
                 for (int i = 0; i < nt; ++i, ++g) {
@@ -460,7 +518,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool ok = true;
         // Every piece ends in two named barriers of all eight warps, reached even after a
         // failed wait, so that no warp is left waiting there.
-        for_each_piece<kSparse>(p, t0, t1, [&](int b, int, int lo, int hi, int k) {
+        for_each_piece<kSparse>(p, sm, [&](int b, int, int lo, int hi, int k) {
             const int nt = (hi - lo + kTok - 1) / kTok;
             if (ok) {
                 // this piece's query slice into TMEM (the A operand of the score product):
@@ -701,23 +759,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // Merge the pieces of each (sequence, head): o = sum_i 2^{lse_i - M} o_i / sum_i 2^{lse_i - M}.
 // Two heads per block; each thread owns four value dims and streams every piece. Sequence
 // b's pieces come from the clusters whose tile ranges meet b's tiles (slot = cluster + b).
-__global__ void __launch_bounds__(256) mla_combine_kernel(const MlaParams p, __nv_bfloat16* out,
-                                                          float* lse_out) {
+__global__ void __launch_bounds__(256, 4) mla_combine_kernel(const MlaParams p,
+                                                             __nv_bfloat16* out,
+                                                             float* lse_out) {
     const int b = blockIdx.x / (kH / 2);
     const int h = (blockIdx.x % (kH / 2)) * 2 + threadIdx.x / 128;
     const int d = (threadIdx.x % 128) * 4;
-    long long T = 0, Sb = 0;
-    int nb = 0;
-    for (int bb = 0; bb < p.B; ++bb) {
-        const int items = p.sparse ? min(max(p.idx_count[bb], 0), p.idx_stride)
-                                   : load_len(p.seq_lens, bb, p.max_len, nullptr);
-        const int n = (items + kTok - 1) / kTok;
-        if (bb == b) {
-            Sb = T;
-            nb = n;
-        }
-        T += n;
-    }
+    // Tile counts of all sequences, their total T and sequence b's first tile Sb and count nb:
+    // the first warp loads 32 sequences' lengths at a time and scans them.
     // Clusters whose ranges [T c / C, T (c + 1) / C) meet b's tiles: the one holding tile t
     // is floor((t C + C - 1) / T). With at least as many tiles as clusters every range is
     // non-empty, so the clusters holding b's first and last tiles bound a contiguous run;
@@ -725,48 +774,86 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const MlaParams p, __n
     constexpr int kMaxRun = 256;
     __shared__ int s_slot[kMaxRun];
     __shared__ int s_n;
-    if (threadIdx.x == 0) {
-        const long long C = p.n_clusters;
-        int n = 0;
-        if (nb > 0 && T >= C) {
-            const int c0 = static_cast<int>((Sb * C + C - 1) / T);
-            const int c1 = static_cast<int>(((Sb + nb - 1) * C + C - 1) / T);
-            for (int c = c0; c <= c1 && n < kMaxRun; ++c) s_slot[n++] = c + b;
-        } else {
-            int last = -1;
-            for (int t = 0; t < nb && n < kMaxRun; ++t) {
-                const int c = static_cast<int>(((Sb + t) * C + C - 1) / T);
-                if (c != last) s_slot[n++] = c + b;
-                last = c;
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        long long T = 0, Sb = 0;
+        int nb = 0;
+        for (int base = 0; base < p.B; base += 32) {
+            const int bb = base + lane;
+            int items = 0;
+            if (bb < p.B)
+                items = p.sparse ? min(max(p.idx_count[bb], 0), p.idx_stride)
+                                 : load_len(p.seq_lens, bb, p.max_len, nullptr);
+            const int n = (items + kTok - 1) / kTok;
+            int incl = n;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
             }
+            if (bb == b) {
+                Sb = T + incl - n;
+                nb = n;
+            }
+            T += __shfl_sync(0xffffffffu, incl, 31);
         }
-        s_n = n;
+        Sb = __shfl_sync(0xffffffffu, Sb, b & 31);
+        nb = __shfl_sync(0xffffffffu, nb, b & 31);
+        if (lane == 0) {
+            const long long C = p.n_clusters;
+            int n = 0;
+            if (nb > 0 && T >= C) {
+                const int c0 = static_cast<int>((Sb * C + C - 1) / T);
+                const int c1 = static_cast<int>(((Sb + nb - 1) * C + C - 1) / T);
+                for (int c = c0; c <= c1 && n < kMaxRun; ++c) s_slot[n++] = c + b;
+            } else {
+                int last = -1;
+                for (int t = 0; t < nb && n < kMaxRun; ++t) {
+                    const int c = static_cast<int>(((Sb + t) * C + C - 1) / T);
+                    if (c != last) s_slot[n++] = c + b;
+                    last = c;
+                }
+            }
+            s_n = n;
+        }
     }
     __shared__ float s_lse[2][kMaxRun];
     __syncthreads();
     const int n_slots = s_n;
-    // both heads' log-sum-exps of every slot, fetched in parallel
+    // both heads' log-sum-exps of every slot, fetched in parallel with the first kBuf
+    // partials of this thread's dims
     for (int i = threadIdx.x; i < 2 * n_slots; i += blockDim.x)
         s_lse[i / n_slots][i % n_slots] =
             __ldcg(p.part_lse + static_cast<size_t>(s_slot[i % n_slots]) * kH +
                    (blockIdx.x % (kH / 2)) * 2 + i / n_slots);
+    auto part = [&](int i) {
+        return __ldcg(reinterpret_cast<const float4*>(
+            p.part_o + (static_cast<size_t>(s_slot[i]) * kH + h) * kDv + d));
+    };
+    constexpr int kBuf = 8;
+    float4 vb[kBuf];
+#pragma unroll
+    for (int i = 0; i < kBuf; ++i)
+        if (i < n_slots) vb[i] = part(i);
     __syncthreads();
     const float* lse = s_lse[threadIdx.x / 128];
     float M = neg_inf();
     for (int i = 0; i < n_slots; ++i) M = fmaxf(M, lse[i]);
     float den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int i = 0; i < n_slots; ++i) {
-        const size_t slot = s_slot[i];
+    auto add = [&](int i, const float4& v) {
         const float w = (M == neg_inf()) ? 0.f : fast_exp2(lse[i] - M);
         den += w;
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + (slot * kH + h) * kDv + d));
         acc.x += w * v.x;
         acc.y += w * v.y;
         acc.z += w * v.z;
         acc.w += w * v.w;
-    }
+    };
+#pragma unroll
+    for (int i = 0; i < kBuf; ++i)
+        if (i < n_slots) add(i, vb[i]);
+#pragma unroll 8
+    for (int i = kBuf; i < n_slots; ++i) add(i, part(i));
     const float inv = den > 0.f ? 1.f / den : 0.f;
     __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
     __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
