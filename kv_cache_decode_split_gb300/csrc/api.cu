@@ -26,6 +26,14 @@ std::once_flag g_encode_once;
 
 }  // namespace
 
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* env = std::getenv("KVD_PDL");
+        return !(env && env[0] == '0');
+    }();
+    return on;
+}
+
 int num_sms() {
     static int n = 0;
     if (n == 0) {

@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     dsa_indexer_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmK128,
                        const __grid_constant__ CUtensorMap tmQ, const IdxParams p) {
+    griddep_wait();
     extern __shared__ uint8_t smem_raw[];
     IdxSmem& sm = *reinterpret_cast<IdxSmem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -296,6 +297,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
 // Histogram of the top 11 key bits of caller-provided scores (dsa_topk only).
 __global__ void __launch_bounds__(256) topk_hist_kernel(const TopkParams p) {
+    griddep_wait();
     __shared__ __align__(16) uint32_t h[kHistBins];
     const int b = blockIdx.y;
     // the selection's counters start from zero whatever an earlier call left in them
@@ -436,6 +438,7 @@ __device__ __forceinline__ int warp_append(bool pred, int* counter) {
 // positions before its bitmap word, from per-word prefix counts, plus those below it in the
 // word), then leaves histogram and counters zeroed for the next call.
 __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const TopkParams p) {
+    griddep_wait();
     __shared__ __align__(16) uint32_t h[kHistBins];
     __shared__ int tmp[kSelThreads / 32 + 4];
     __shared__ int s_nlist, s_nchosen;
@@ -754,13 +757,17 @@ int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensor
     }
     const int total = p.B * p.tiles_per_b;
     const int grid = total < num_sms() ? total : num_sms();
-    dsa_indexer_kernel<<<grid, kIdxThreads, kIdxSmem, stream>>>(tk, tk128, tq, p);
+    if (launch_kernel(dsa_indexer_kernel, dim3(grid), dim3(kIdxThreads), kIdxSmem, stream, tk,
+                      tk128, tq, p) != cudaSuccess)
+        return KVD_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
 
 int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream) {
     const int blocks_per_b = std::max(1, std::min(64, (p.max_len + 4095) / 4096));
-    if (need_hist) topk_hist_kernel<<<dim3(blocks_per_b, p.B), 256, 0, stream>>>(p);
+    if (need_hist && launch_kernel(topk_hist_kernel, dim3(blocks_per_b, p.B), dim3(256), 0,
+                                   stream, p) != cudaSuccess)
+        return KVD_ERR_CUDA;
     static int configured = 0;
     if (!configured) {
         if (cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -771,7 +778,9 @@ int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream) {
     const int sel_per_b =
         std::max(1, std::min(64, (p.max_len + kSelThreads * kSelPerThread - 1) /
                                      (kSelThreads * kSelPerThread)));
-    topk_select_kernel<<<dim3(sel_per_b, p.B), kSelThreads, kSelDynSmem, stream>>>(p);
+    if (launch_kernel(topk_select_kernel, dim3(sel_per_b, p.B), dim3(kSelThreads), kSelDynSmem,
+                      stream, p) != cudaSuccess)
+        return KVD_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
 

@@ -262,6 +262,7 @@ template <int D, int NT, int HPT>
 __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
     gqa_decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
+    griddep_wait();
     using Cfg = GqaBf16Cfg<D, NT, HPT>;
     using MS = MergeSmem<D, NT * 8>;
     using CS = CombineSmem<HPT * NT * 8>;
@@ -518,6 +519,7 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
 // ---------------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(kConsumers * 32) gqa_decode_f32_kernel(const GqaParams p) {
+    griddep_wait();
     constexpr int J = D / 32;  // dims per lane
     extern __shared__ uint8_t smem_raw[];
     MergeSmem<D, kMaxHP>& ms = *reinterpret_cast<MergeSmem<D, kMaxHP>*>(smem_raw);
@@ -611,7 +613,9 @@ int launch_bf16(const GqaPlan& plan, const GqaParams& p, const CUtensorMap& tk,
         configured = 1;
     }
     const dim3 grid(plan.max_chunks, (p.Hkv / HPT) * p.NHG, p.B);
-    kern<<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(tk, tv, p);
+    if (launch_kernel(kern, grid, dim3(Cfg::kThreads), Cfg::kSmem, stream, tk, tv, p) !=
+        cudaSuccess)
+        return KVD_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
 
@@ -626,7 +630,8 @@ int launch_f32(const GqaPlan& plan, const GqaParams& p, cudaStream_t stream) {
         configured = 1;
     }
     const dim3 grid(plan.max_chunks, p.Hkv * p.NHG, p.B);
-    kern<<<grid, kConsumers * 32, bytes, stream>>>(p);
+    if (launch_kernel(kern, grid, dim3(kConsumers * 32), bytes, stream, p) != cudaSuccess)
+        return KVD_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
 

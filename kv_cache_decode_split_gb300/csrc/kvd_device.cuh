@@ -109,6 +109,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// Wait until the grids this one depends on (programmatic launch) have completed and their
+// memory is visible; returns at once for a plain launch. First statement of every kernel.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Hint: bring the global line holding `ptr` into L2 (no data returned).
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));

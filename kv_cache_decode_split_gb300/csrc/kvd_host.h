@@ -146,4 +146,27 @@ int make_tmap_bf16_blocked(CUtensorMap* map, const void* base, uint64_t rows, ui
 
 int num_sms();
 
+// Programmatic dependent launch is on unless KVD_PDL=0 (read once).
+bool pdl_enabled();
+
+// Launch with programmatic stream serialization: the kernel may be scheduled while its
+// predecessor on the stream finishes (launch and set-up overlap that tail). Every kernel of
+// the library waits for the predecessor (griddepcontrol.wait) before it touches memory, so
+// the order of memory effects is that of a plain launch.
+template <typename... P, typename... A>
+inline cudaError_t launch_kernel(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, A&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+}
+
 }  // namespace kvd

@@ -237,6 +237,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmC0,
                       const __grid_constant__ CUtensorMap tmC1,
                       const __grid_constant__ CUtensorMap tmC2, const MlaParams p) {
+    griddep_wait();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     MlaSmem& sm = *reinterpret_cast<MlaSmem*>(smem_raw);
     const uint32_t rank = cluster_rank();
@@ -762,6 +763,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256, 4) mla_combine_kernel(const MlaParams p,
                                                              __nv_bfloat16* out,
                                                              float* lse_out) {
+    griddep_wait();
     const int b = blockIdx.x / (kH / 2);
     const int h = (blockIdx.x % (kH / 2)) * 2 + threadIdx.x / 128;
     const int d = (threadIdx.x % 128) * 4;
@@ -879,12 +881,15 @@ int mla_launch(const MlaParams& p, const CUtensorMap& tc0, const CUtensorMap& tc
         configured[which] = 1;
     }
     const int grid = 2 * p.n_clusters;
-    if (p.sparse)
-        mla_decode_kernel<true><<<grid, kThreads, kMlaSmem, stream>>>(tc0, tc1, tc2, p);
-    else
-        mla_decode_kernel<false><<<grid, kThreads, kMlaSmem, stream>>>(tc0, tc1, tc2, p);
-    mla_combine_kernel<<<p.B * (kH / 2), 256, 0, stream>>>(p, static_cast<__nv_bfloat16*>(out),
-                                                            lse_out);
+    const cudaError_t e1 =
+        p.sparse ? launch_kernel(mla_decode_kernel<true>, dim3(grid), dim3(kThreads), kMlaSmem,
+                                 stream, tc0, tc1, tc2, p)
+                 : launch_kernel(mla_decode_kernel<false>, dim3(grid), dim3(kThreads), kMlaSmem,
+                                 stream, tc0, tc1, tc2, p);
+    if (e1 != cudaSuccess) return KVD_ERR_CUDA;
+    if (launch_kernel(mla_combine_kernel, dim3(p.B * (kH / 2)), dim3(256), 0, stream, p,
+                      static_cast<__nv_bfloat16*>(out), lse_out) != cudaSuccess)
+        return KVD_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
 
