@@ -61,7 +61,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     dsa_indexer_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmK128,
                        const __grid_constant__ CUtensorMap tmQ, const IdxParams p) {
-    griddep_wait();
     extern __shared__ uint8_t smem_raw[];
     IdxSmem& sm = *reinterpret_cast<IdxSmem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -84,14 +83,17 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sm.hist[i] = 0;
-    // the selection's counters start from zero whatever an earlier call left in them
-    if (blockIdx.x == 0)
-        for (int i = threadIdx.x; i < 4 * p.B; i += blockDim.x) p.counts[i] = 0;
     if (warp == 1) tmem_alloc(&sm.tmem_base, 128);  // two 64-column fp32 accumulators
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    // the set-up above touches no global memory: it runs while the previous kernel on the
+    // stream may still be finishing (programmatic launch)
+    griddep_wait();
+    // the selection's counters start from zero whatever an earlier call left in them
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < 4 * p.B; i += blockDim.x) p.counts[i] = 0;
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer

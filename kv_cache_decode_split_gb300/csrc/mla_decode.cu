@@ -237,7 +237,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmC0,
                       const __grid_constant__ CUtensorMap tmC1,
                       const __grid_constant__ CUtensorMap tmC2, const MlaParams p) {
-    griddep_wait();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     MlaSmem& sm = *reinterpret_cast<MlaSmem*>(smem_raw);
     const uint32_t rank = cluster_rank();
@@ -245,20 +244,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int cl = blockIdx.x >> 1, n_cl = gridDim.x >> 1;
     if (smem_u32(smem_raw) & 1023u) {  // the layout needs a 1024-byte aligned window
+        griddep_wait();
         if (threadIdx.x == 0) record_error(p.err, KVD_ERR_CUDA);
         return;
     }
-    if (warp == 0)
-        build_schedule<kSparse>(p, cl, n_cl, sm, lane, rank == 0 ? p.err : nullptr);
-    __syncthreads();
-    const long long t0 = sm.t0, t1 = sm.t1;
-    if (t0 >= t1) return;  // both CTAs of the pair take this exit together
-    const int n_tiles = static_cast<int>(t1 - t0);
     const int nbox = rank == 0 ? 4 : 5;   // 64-dim boxes this CTA loads
     const int dim0 = rank == 0 ? 0 : 256;
     const CUtensorMap& tmC = rank == 0 ? tmC0 : tmC1;  // 3-D maps with 4 / 5 blocks per box
     constexpr uint32_t kXBytes = kH * kTok * 4;
 
+    // Set-up that touches no global memory runs while the previous kernel on the stream
+    // may still be finishing (programmatic launch).
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.full[s], kSparse ? 32 : 1);
@@ -283,10 +279,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(&sm.ofinal, 1);
         mbar_init(&sm.ofree, kSoftWarps);
         fence_mbar_init();
-        // the partner's partial scores of the first tile of each group (later tiles: armed
-        // by the group once the slot's previous phase has completed)
-        for (int i = 0; i < kGroups && i < n_tiles; ++i)
-            for (int hf = 0; hf < 2; ++hf) mbar_arrive_expect_tx(&sm.xfull[hf][i], kXBytes / 2);
     }
     if (warp == kWarpQK) tmem_alloc(&sm.tmem_base, 512);
     tc_fence_before();
@@ -294,6 +286,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     cluster_sync();  // the partner's barriers exist before anyone signals them
     const uint32_t tmem = sm.tmem_base;
+
+    griddep_wait();  // lengths, selected indices and the workspace are read from here on
+    if (warp == 0)
+        build_schedule<kSparse>(p, cl, n_cl, sm, lane, rank == 0 ? p.err : nullptr);
+    __syncthreads();
+    const long long t0 = sm.t0, t1 = sm.t1;
+    if (t0 >= t1) {  // both CTAs of the pair take this exit together, with no remote access
+        if (warp == kWarpQK) tmem_dealloc(tmem, 512);
+        return;
+    }
+    const int n_tiles = static_cast<int>(t1 - t0);
+    // the partner's partial scores of the first tile of each group (later tiles: armed by
+    // the group once the slot's previous phase has completed). A copy that lands before
+    // its arming leaves the transaction count below zero until then.
+    if (threadIdx.x == 0)
+        for (int i = 0; i < kGroups && i < n_tiles; ++i)
+            for (int hf = 0; hf < 2; ++hf) mbar_arrive_expect_tx(&sm.xfull[hf][i], kXBytes / 2);
 
     if (warp == kWarpLoad) {
         // ------------------------------------------------------------------ loads
