@@ -421,15 +421,18 @@ def flush_l2(buf):
 
 
 def time_steps(fn, steps, stream):
-    """Per-step CUDA-event durations (ms) on `stream`, back to back."""
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-    ev[0].record(stream)
-    for i in range(steps):
+    """Total CUDA-event duration (ms) of `steps` back-to-back steps on `stream`, and the mean
+    per step. Only the two bracketing events are recorded: an event between steps would sit
+    between two kernels and keep the second from launching while the first finishes."""
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
         fn()
-        ev[i + 1].record(stream)
+    b.record(stream)
     torch.cuda.synchronize()
-    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
-    return ev[0].elapsed_time(ev[-1]), per
+    total = a.elapsed_time(b)
+    return total, [total / steps] * steps
 
 
 def time_flushed(fn, iters, stream, flush):
