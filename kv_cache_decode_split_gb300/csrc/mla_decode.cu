@@ -62,6 +62,17 @@ struct Piece {
 };
 constexpr int kMaxPieces = 32;
 
+// A range that moves on to the next sequence pays for an output write and a query load,
+// worth about kPieceGap tiles of streaming. Ranges are cut in a virtual tile list with
+// kPieceGap empty positions before every sequence but the first, so that such a range holds
+// fewer tiles; only when ranges span at least 2 kPieceGap positions, so that every range
+// still holds tiles.
+constexpr int kPieceGap = 6;
+__device__ __forceinline__ long long piece_gap(long long T, int B, int n_clusters) {
+    const long long V = T + static_cast<long long>(kPieceGap) * (B - 1);
+    return V >= 2LL * kPieceGap * n_clusters ? kPieceGap : 0;
+}
+
 struct MlaSmem {
     uint8_t stage[kStages][kStageBytes];   // offset 0, 1024-aligned
     // Partial scores cross in two halves of 32 columns (16 KB each), so that the next
@@ -85,7 +96,8 @@ struct MlaSmem {
     uint32_t tmem_base;
     // the cluster's schedule, built once: tile range and its pieces (n_pieces < 0: more
     // pieces than the table holds, walked from the sequence lengths instead)
-    long long t0, t1;
+    long long t0, t1, gap;   // virtual tile range and the gap before each later sequence
+    int n_tiles;             // tiles of the range
     int n_pieces;
     Piece piece[kMaxPieces];
 };
@@ -173,10 +185,12 @@ __device__ void build_schedule(const MlaParams& p, int c, int n_clusters, MlaSme
         for (int off = 16; off; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
         T += n;
     }
-    const long long t0 = T * c / n_clusters, t1 = T * (c + 1) / n_clusters;
-    long long run = 0;
-    int np = 0;
-    for (int base = 0; base < p.B && run < t1; base += 32) {
+    const long long X = piece_gap(T, p.B, n_clusters);
+    const long long V = T + X * (p.B - 1);
+    const long long t0 = V * c / n_clusters, t1 = V * (c + 1) / n_clusters;
+    long long run = 0;  // tiles of the sequences before this batch
+    int np = 0, n_real = 0;
+    for (int base = 0; base < p.B && run + X * base < t1; base += 32) {
         const int bb = base + lane;
         const int items = bb < p.B ? seq_items<kSparse>(p, bb, nullptr) : 0;
         const int n = (items + kTok - 1) / kTok;
@@ -186,7 +200,7 @@ __device__ void build_schedule(const MlaParams& p, int c, int n_clusters, MlaSme
             const int v = __shfl_up_sync(0xffffffffu, incl, off);
             if (lane >= off) incl += v;
         }
-        const long long sb = run + incl - n;  // the lane's sequence's first tile
+        const long long sb = run + incl - n + X * bb;  // the lane's sequence's first position
         const long long lo_t = max(t0, sb) - sb, hi_t = min(t1, sb + n) - sb;
         const bool has = bb < p.B && hi_t > lo_t;
         const unsigned m = __ballot_sync(0xffffffffu, has);
@@ -194,12 +208,18 @@ __device__ void build_schedule(const MlaParams& p, int c, int n_clusters, MlaSme
         if (has && slot < kMaxPieces)
             sm.piece[slot] = Piece{bb, items, static_cast<int>(lo_t) * kTok,
                                    min(static_cast<int>(hi_t) * kTok, items)};
+        int nr = has ? static_cast<int>(hi_t - lo_t) : 0;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) nr += __shfl_xor_sync(0xffffffffu, nr, off);
+        n_real += nr;
         np += __popc(m);
         run += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) {
         sm.t0 = t0;
         sm.t1 = t1;
+        sm.gap = X;
+        sm.n_tiles = n_real;
         sm.n_pieces = np <= kMaxPieces ? np : -1;
     }
 }
@@ -216,8 +236,8 @@ __device__ __forceinline__ void for_each_piece(const MlaParams& p, const MlaSmem
         }
         return;
     }
-    const long long t0 = sm.t0, t1 = sm.t1;
-    long long base = 0;
+    const long long t0 = sm.t0, t1 = sm.t1, X = sm.gap;
+    long long base = 0;  // virtual position of sequence b's first tile
     int k = 0;
     for (int b = 0; b < p.B && base < t1; ++b) {
         const int items = seq_items<kSparse>(p, b, nullptr);
@@ -228,7 +248,7 @@ __device__ __forceinline__ void for_each_piece(const MlaParams& p, const MlaSmem
               min(static_cast<int>(hi_t) * kTok, items), k);
             ++k;
         }
-        base += n;
+        base += n + X;
     }
 }
 
@@ -291,12 +311,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0)
         build_schedule<kSparse>(p, cl, n_cl, sm, lane, rank == 0 ? p.err : nullptr);
     __syncthreads();
-    const long long t0 = sm.t0, t1 = sm.t1;
-    if (t0 >= t1) {  // both CTAs of the pair take this exit together, with no remote access
+    const int n_tiles = sm.n_tiles;
+    if (n_tiles == 0) {  // both CTAs of the pair take this exit together, with no remote access
         if (warp == kWarpQK) tmem_dealloc(tmem, 512);
         return;
     }
-    const int n_tiles = static_cast<int>(t1 - t0);
     // the partner's partial scores of the first tile of each group (later tiles: armed by
     // the group once the slot's previous phase has completed). A copy that lands before
     // its arming leaves the transaction count below zero until then.
@@ -312,6 +331,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         int g = 0;  // tile index within this CTA's range
         bool ok = true;
+        // No tile is of use before the first piece's queries are in tensor memory: their
+        // loads go out first instead of queueing behind every SM's first tiles. (Page ids
+        // and row sources of the first tiles are resolved meanwhile.)
+        auto wait_queries = [&]() {
+            if (lane == 0) ok = mbar_wait(&sm.qready, 0, p.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+        };
         for_each_piece<kSparse>(p, sm, [&](int b, int items, int lo, int hi, int) {
             if (!ok) return;
             const int nt = (hi - lo + kTok - 1) / kTok;
@@ -331,7 +357,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 int cur = piece_page(lane), nxt = piece_page(32 + lane);
                 for (int i = 0; i < nt && ok; ++i, ++g) {
                     const int s = g % kStages;
-                    if (lane == 0) ok = mbar_wait(&sm.empty[s], ((g / kStages) & 1) ^ 1, p.err);
+                    if (g == 0) wait_queries();
+                    if (lane == 0 && ok)
+                        ok = mbar_wait(&sm.empty[s], ((g / kStages) & 1) ^ 1, p.err);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
                     if (lane == 0) mbar_arrive_expect_tx(&sm.full[s], nbox * kTileBox);
@@ -398,7 +426,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 for (int i = 0; i < nt && ok; ++i, ++g) {
                     const int s = g % kStages;
-                    if (lane == 0) ok = mbar_wait(&sm.empty[s], ((g / kStages) & 1) ^ 1, p.err);
+                    if (g == 0) wait_queries();
+                    if (lane == 0 && ok)
+                        ok = mbar_wait(&sm.empty[s], ((g / kStages) & 1) ^ 1, p.err);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
                     const int t_nn0 = tok_of(i + 2, 0), t_nn1 = tok_of(i + 2, 1);
@@ -526,54 +556,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                           map_peer(smem_u32(&sm.peer_free[1]), peer)};
         int g0 = 0;  // first tile of the current piece within this CTA's range
         bool ok = true;
+        constexpr int kQBoxes = (kNBox + kGroups - 1) / kGroups;
+        const int bx0 = grp * kQBoxes, bx1 = min(nbox, bx0 + kQBoxes);
+        auto q_rows = [&](int b) {  // this lane's head row of sequence b's queries, our dims
+            return reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                                                  (static_cast<size_t>(b) * kH + h) * kDqk +
+                                                  dim0);
+        };
+        auto prefetch_q = [&](int b) {
+#pragma unroll
+            for (int bi = 0; bi < kQBoxes; ++bi)
+                if (bx0 + bi < bx1) prefetch_l2(q_rows(b) + (bx0 + bi) * 8);
+        };
+        // Sequence b's query slice into TMEM (the A operand of the score product), the group's
+        // 64-dim boxes one at a time (few registers), then the group's share of qready.
+        auto load_q = [&](int b) {
+            const uint4* qrow = q_rows(b);
+#pragma unroll 1
+            for (int bx = bx0; bx < bx1; ++bx) {
+                uint4 v[8];
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) v[jj] = __ldg(qrow + bx * 8 + jj);
+                uint32_t r[32];
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    r[4 * jj] = v[jj].x;
+                    r[4 * jj + 1] = v[jj].y;
+                    r[4 * jj + 2] = v[jj].z;
+                    r[4 * jj + 3] = v[jj].w;
+                }
+                tmem_st_32x32b_x32(trow + kColQ + bx * 32, r);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.qready);
+        };
+        // With the piece table, the next piece's queries are loaded as soon as the current
+        // piece's score products have all completed (before its output is written), so that
+        // the next products overlap that write; otherwise each piece loads its own.
+        const int n_pieces = sm.n_pieces;
         // Every piece ends in two named barriers of all eight warps, reached even after a
         // failed wait, so that no warp is left waiting there.
         for_each_piece<kSparse>(p, sm, [&](int b, int, int lo, int hi, int k) {
             const int nt = (hi - lo + kTok - 1) / kTok;
-            if (ok) {
-                // this piece's query slice into TMEM (the A operand of the score product):
-                // group 0 boxes 0-2, group 1 the rest. The previous piece's products have
-                // all completed (its O has been read).
-                const uint4* qrow = reinterpret_cast<const uint4*>(
-                    reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                    (static_cast<size_t>(b) * kH + h) * kDqk + dim0);
-                constexpr int kQBoxes = (kNBox + kGroups - 1) / kGroups;
-                const int bx0 = grp * kQBoxes, bx1 = min(nbox, bx0 + kQBoxes);
-                // the group's rows of this piece's and the next sequence's queries head for L2
-                // first, so that only the first box waits on memory
-#pragma unroll
-                for (int bi = 0; bi < kQBoxes; ++bi) {
-                    if (bx0 + bi >= bx1) continue;
-                    prefetch_l2(qrow + (bx0 + bi) * 8);
-                    if (b + 1 < p.B)
-                        prefetch_l2(qrow + static_cast<size_t>(kH) * kDqk / 8 + (bx0 + bi) * 8);
-                }
-                // one 64-dim box (32 columns) at a time: few registers, outside the tile loop
-#pragma unroll 1
-                for (int bx = bx0; bx < bx1; ++bx) {
-                    uint4 v[8];
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) v[jj] = __ldg(qrow + bx * 8 + jj);
-                    uint32_t r[32];
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        r[4 * jj] = v[jj].x;
-                        r[4 * jj + 1] = v[jj].y;
-                        r[4 * jj + 2] = v[jj].z;
-                        r[4 * jj + 3] = v[jj].w;
-                    }
-                    tmem_st_32x32b_x32(trow + kColQ + bx * 32, r);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.qready);
+            const int next_b = (n_pieces >= 0 && k + 1 < n_pieces) ? sm.piece[k + 1].b : -1;
+            if (ok && (k == 0 || n_pieces < 0)) {
+                prefetch_q(b);
+                load_q(b);
             }
+            bool next_prefetched = false;
             float l = 0.f, m_l = neg_inf();  // this group's sum of P, relative to 2^m_l
             float m_last = neg_inf();        // running max after this group's latest tile
             for (int i = 0; i < nt && ok; ++i) {
                 const int j = g0 + i;  // tile index within the range (barrier phases)
                 if (j % kGroups != grp) continue;
+                if (next_b >= 0 && !next_prefetched && i + 2 * kGroups >= nt) {
+                    prefetch_q(next_b);  // a few tiles before it is needed
+                    next_prefetched = true;
+                }
                 const int it = j / kGroups;  // this group's iteration
                 const int pg = (j + kGroups - 1) % kGroups;  // group of tile j - 1
                 const int pit = ((j - 1) / kGroups) & 1;     // its barrier parity
@@ -714,6 +755,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(&sm.hand[lg], (jl / kGroups) & 1, p.err);
                 if (ok) m_last = sm.mref[lg][h];
             }
+            // every score product of the piece has completed (the last tile's scores have
+            // been read): the query slice may now take the next piece's queries
+            if (ok && next_b >= 0) {
+                if (!next_prefetched) prefetch_q(next_b);
+                load_q(next_b);
+            }
             // every group's sum relative to 2^m_last, added through shared memory (over the
             // running-max array, once every group has read the final max)
             asm volatile("bar.sync 1, %0;" ::"r"(kSoftWarps * 32) : "memory");
@@ -778,10 +825,12 @@ __global__ void __launch_bounds__(256, 4) mla_combine_kernel(const MlaParams p,
     const int d = (threadIdx.x % 128) * 4;
     // Tile counts of all sequences, their total T and sequence b's first tile Sb and count nb:
     // the first warp loads 32 sequences' lengths at a time and scans them.
-    // Clusters whose ranges [T c / C, T (c + 1) / C) meet b's tiles: the one holding tile t
-    // is floor((t C + C - 1) / T). With at least as many tiles as clusters every range is
-    // non-empty, so the clusters holding b's first and last tiles bound a contiguous run;
-    // otherwise b has fewer than C tiles and each one names its cluster. Block-wide, once.
+    // Clusters whose ranges [V c / C, V (c + 1) / C) of the virtual tile list (V = T plus a
+    // gap of X positions before every later sequence) meet b's tiles: the one holding
+    // position v is floor((v C + C - 1) / V). When every range holds tiles (a gap, or at
+    // least as many tiles as clusters), the clusters holding b's first and last tiles bound
+    // a contiguous run; otherwise (no gap, fewer tiles than clusters) each tile names its
+    // cluster. Block-wide, once.
     constexpr int kMaxRun = 256;
     __shared__ int s_slot[kMaxRun];
     __shared__ int s_n;
@@ -812,10 +861,13 @@ __global__ void __launch_bounds__(256, 4) mla_combine_kernel(const MlaParams p,
         nb = __shfl_sync(0xffffffffu, nb, b & 31);
         if (lane == 0) {
             const long long C = p.n_clusters;
+            // the decode kernel's virtual tile list (a gap before every later sequence)
+            const long long X = piece_gap(T, p.B, p.n_clusters);
+            const long long V = T + X * (p.B - 1), Vb = Sb + X * b;
             int n = 0;
-            if (nb > 0 && T >= C) {
-                const int c0 = static_cast<int>((Sb * C + C - 1) / T);
-                const int c1 = static_cast<int>(((Sb + nb - 1) * C + C - 1) / T);
+            if (nb > 0 && (X > 0 || T >= C)) {
+                const int c0 = static_cast<int>((Vb * C + C - 1) / V);
+                const int c1 = static_cast<int>(((Vb + nb - 1) * C + C - 1) / V);
                 for (int c = c0; c <= c1 && n < kMaxRun; ++c) s_slot[n++] = c + b;
             } else {
                 int last = -1;

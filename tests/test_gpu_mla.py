@@ -119,6 +119,18 @@ def test_mla_full_size_sampled(kvd, sharp):
     assert np.max(np.abs(to_np(lse)[pr[:, 0], pr[:, 1]] - ref_lse)) < 2e-3 * max(1.0, np.abs(ref_lse).max())
 
 
+def test_mla_ragged_many_tiles_every_head(kvd):
+    # enough tiles that the ranges are cut with a gap before every later sequence, and
+    # lengths that put sequence boundaries, tiny sequences and partial tiles inside ranges;
+    # every (sequence, head) output is checked
+    lens = [60001, 1, 30000, 64, 65, 20000, 7, 5000]
+    x = W.make_mla(len(lens), 128, lens, page_size=64, shuffle=True, extra_pages=5, seed=640)
+    out, lse = _dense(kvd, x)
+    ref, ref_lse = oracle.mla(x.q, x.c_pool, x.block_table, x.seq_lens, x.scale)
+    assert_attn_close(out, ref, what="mla ragged many tiles")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) < 2e-3 * max(1.0, np.abs(ref_lse).max())
+
+
 def test_dsa_full_size_sparse_mla_sampled(kvd):
     idx_in, x = W.build("dsa_sparse_mla")
     rng = np.random.default_rng(11)
