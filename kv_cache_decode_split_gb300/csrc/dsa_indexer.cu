@@ -398,7 +398,7 @@ __device__ __forceinline__ void load_hist(uint32_t* h, const uint32_t* src) {
     }
 }
 
-constexpr int kSelThreads = 256;
+constexpr int kSelThreads = 512;
 constexpr int kSelPerThread = 16;
 constexpr int kRankMax = 256;  // a threshold bucket this small is finished by ranking its keys
 constexpr int kRadixBits = 8;  // digit of the passes after the histogram's top 11 bits

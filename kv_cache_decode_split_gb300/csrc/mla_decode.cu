@@ -331,9 +331,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         int g = 0;  // tile index within this CTA's range
         bool ok = true;
-        // No tile is of use before the first piece's queries are in tensor memory: their
-        // loads go out first instead of queueing behind every SM's first tiles. (Page ids
-        // and row sources of the first tiles are resolved meanwhile.)
+        // Dense: no tile is of use before the first piece's queries are in tensor memory, so
+        // their loads go out first instead of queueing behind every SM's first tiles (page
+        // ids of the first tiles are resolved meanwhile).
         auto wait_queries = [&]() {
             if (lane == 0) ok = mbar_wait(&sm.qready, 0, p.err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -426,9 +426,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 for (int i = 0; i < nt && ok; ++i, ++g) {
                     const int s = g % kStages;
-                    if (g == 0) wait_queries();
-                    if (lane == 0 && ok)
-                        ok = mbar_wait(&sm.empty[s], ((g / kStages) & 1) ^ 1, p.err);
+                    // (no wait for the queries here: the gather's latency dominates)
+                    if (lane == 0) ok = mbar_wait(&sm.empty[s], ((g / kStages) & 1) ^ 1, p.err);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
                     const int t_nn0 = tok_of(i + 2, 0), t_nn1 = tok_of(i + 2, 1);
