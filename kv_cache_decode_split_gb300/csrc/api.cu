@@ -237,7 +237,11 @@ int mla_run(const void* q, const void* c_pool, const int32_t* block_table,
     if (make_tmap_bf16_blocked(&tc1, c_pool, rows, 576, 64, 5) != KVD_OK) return KVD_ERR_CUDA;
     if (make_tmap_bf16_2d(&tc2, c_pool, rows, 576, page_size < 64 ? page_size : 64) != KVD_OK)
         return KVD_ERR_CUDA;
-    return mla_launch(p, tc0, tc1, tc2, out, lse_out, stream);
+    // the queries as [B * 128 rows, 576] (128-row boxes: one head block of one sequence)
+    CUtensorMap tq;
+    if (make_tmap_bf16_2d(&tq, q, static_cast<uint64_t>(B) * 128, 576, 128) != KVD_OK)
+        return KVD_ERR_CUDA;
+    return mla_launch(p, tc0, tc1, tc2, tq, out, lse_out, stream);
 }
 
 }  // namespace kvd

@@ -134,7 +134,8 @@ int mla_run(const void* q, const void* c_pool, const int32_t* block_table,
             int max_pages, int num_pages, float scale, void* ws, size_t ws_bytes,
             cudaStream_t stream);
 int mla_launch(const MlaParams& p, const CUtensorMap& tc0, const CUtensorMap& tc1,
-               const CUtensorMap& tc2, void* out, float* lse_out, cudaStream_t stream);
+               const CUtensorMap& tc2, const CUtensorMap& tq, void* out, float* lse_out,
+               cudaStream_t stream);
 
 int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                       uint32_t box_rows);

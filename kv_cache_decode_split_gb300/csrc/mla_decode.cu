@@ -93,6 +93,7 @@ struct MlaSmem {
     uint64_t yfree[2][kGroups];  // [half][tile group]: the copy of y[half] has read it
     uint64_t hand[kGroups];  // group published its running max
     uint64_t ofree;          // O of the current piece has been read (eight softmax warps)
+    uint64_t qfull;          // dense: the first piece's queries have landed in stages 2-3
     uint32_t tmem_base;
     // the cluster's schedule, built once: tile range and its pieces (n_pieces < 0: more
     // pieces than the table holds, walked from the sequence lengths instead)
@@ -256,7 +257,8 @@ template <bool kSparse>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmC0,
                       const __grid_constant__ CUtensorMap tmC1,
-                      const __grid_constant__ CUtensorMap tmC2, const MlaParams p) {
+                      const __grid_constant__ CUtensorMap tmC2,
+                      const __grid_constant__ CUtensorMap tmQ, const MlaParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     MlaSmem& sm = *reinterpret_cast<MlaSmem*>(smem_raw);
     const uint32_t rank = cluster_rank();
@@ -298,6 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mbar_init(&sm.ofinal, 1);
         mbar_init(&sm.ofree, kSoftWarps);
+        mbar_init(&sm.qfull, 1);
         fence_mbar_init();
     }
     if (warp == kWarpQK) tmem_alloc(&sm.tmem_base, 512);
@@ -316,6 +319,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (warp == kWarpQK) tmem_dealloc(tmem, 512);
         return;
     }
+    // Dense, with the piece table: the first piece's query slice comes by TMA into ring
+    // stages 2-3 (16 KB per 64-dim box), issued ahead of the first tiles, which take stages
+    // 0-1; the producer reuses stages 2-3 once the queries are in tensor memory.
+    const bool tma_q = !kSparse && sm.n_pieces > 0;
+    constexpr int kQBox = kH * 128;
     // the partner's partial scores of the first tile of each group (later tiles: armed by
     // the group once the slot's previous phase has completed). A copy that lands before
     // its arming leaves the transaction count below zero until then.
@@ -328,6 +336,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tensormap(&tmC);
             prefetch_tensormap(&tmC2);
+            if (tma_q) {
+                mbar_arrive_expect_tx(&sm.qfull, nbox * kQBox);
+                for (int bx = 0; bx < nbox; ++bx)
+                    tma_load_2d(sm.stage[2] + bx * kQBox, &tmQ, &sm.qfull, dim0 + 64 * bx,
+                                sm.piece[0].b * kH);
+            }
         }
         int g = 0;  // tile index within this CTA's range
         bool ok = true;
@@ -357,7 +371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 int cur = piece_page(lane), nxt = piece_page(32 + lane);
                 for (int i = 0; i < nt && ok; ++i, ++g) {
                     const int s = g % kStages;
-                    if (g == 0) wait_queries();
+                    if (g == (tma_q ? 2 : 0)) wait_queries();
                     if (lane == 0 && ok)
                         ok = mbar_wait(&sm.empty[s], ((g / kStages) & 1) ^ 1, p.err);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -591,6 +605,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.qready);
         };
+        // The first piece's queries from the TMA copy in stages 2-3 (128-byte swizzled rows).
+        auto load_q_staged = [&]() {
+            if (!(ok = mbar_wait(&sm.qfull, 0, p.err))) return;
+#pragma unroll 1
+            for (int bx = bx0; bx < bx1; ++bx) {
+                const uint8_t* row = sm.stage[2] + bx * kQBox + h * 128;
+                uint32_t r[32];
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(row + ((jj ^ (h & 7)) << 4));
+                    r[4 * jj] = v.x;
+                    r[4 * jj + 1] = v.y;
+                    r[4 * jj + 2] = v.z;
+                    r[4 * jj + 3] = v.w;
+                }
+                tmem_st_32x32b_x32(trow + kColQ + bx * 32, r);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.qready);
+        };
         // With the piece table, the next piece's queries are loaded as soon as the current
         // piece's score products have all completed (before its output is written), so that
         // the next products overlap that write; otherwise each piece loads its own.
@@ -600,7 +636,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for_each_piece<kSparse>(p, sm, [&](int b, int, int lo, int hi, int k) {
             const int nt = (hi - lo + kTok - 1) / kTok;
             const int next_b = (n_pieces >= 0 && k + 1 < n_pieces) ? sm.piece[k + 1].b : -1;
-            if (ok && (k == 0 || n_pieces < 0)) {
+            if (ok && k == 0 && tma_q) {
+                load_q_staged();
+            } else if (ok && (k == 0 || n_pieces < 0)) {
                 prefetch_q(b);
                 load_q(b);
             }
@@ -928,7 +966,8 @@ __global__ void __launch_bounds__(256, 4) mla_combine_kernel(const MlaParams p,
 }  // namespace
 
 int mla_launch(const MlaParams& p, const CUtensorMap& tc0, const CUtensorMap& tc1,
-               const CUtensorMap& tc2, void* out, float* lse_out, cudaStream_t stream) {
+               const CUtensorMap& tc2, const CUtensorMap& tq, void* out, float* lse_out,
+               cudaStream_t stream) {
     static int configured[2] = {0, 0};
     const int which = p.sparse ? 1 : 0;
     if (!configured[which]) {
@@ -943,9 +982,9 @@ int mla_launch(const MlaParams& p, const CUtensorMap& tc0, const CUtensorMap& tc
     const int grid = 2 * p.n_clusters;
     const cudaError_t e1 =
         p.sparse ? launch_kernel(mla_decode_kernel<true>, dim3(grid), dim3(kThreads), kMlaSmem,
-                                 stream, tc0, tc1, tc2, p)
+                                 stream, tc0, tc1, tc2, tq, p)
                  : launch_kernel(mla_decode_kernel<false>, dim3(grid), dim3(kThreads), kMlaSmem,
-                                 stream, tc0, tc1, tc2, p);
+                                 stream, tc0, tc1, tc2, tq, p);
     if (e1 != cudaSuccess) return KVD_ERR_CUDA;
     if (launch_kernel(mla_combine_kernel, dim3(p.B * (kH / 2)), dim3(256), 0, stream, p,
                       static_cast<__nv_bfloat16*>(out), lse_out) != cudaSuccess)
