@@ -308,22 +308,44 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
 
     if (warp == kConsumers) {
         // ------------------------------------------------------------------ producer
+        // The warp resolves the page ids of the CTA's page pieces 32 at a time (lane k: piece
+        // 32 m + k), the next batch in flight while the current one is used, so that filling
+        // the ring costs one lookup round trip rather than one per tile; lane 0 issues.
         if (lane == 0) {
             prefetch_tensormap(&tmK);
             prefetch_tensormap(&tmV);
-            for (int i = 0; i < n_tiles; ++i) {
-                const int s = i % S;
-                if (!mbar_wait(&empty[s], ((i / S) & 1) ^ 1, p.err)) break;
-                mbar_arrive_expect_tx(&full[s], 2 * Cfg::kTileBytes);
-                const int T = t0 + i * kTile;
-                for (int sub = 0; sub < kTile / bp; ++sub) {
-                    const int t = T + sub * bp;
-                    const int tc = t < L ? t : L - 1;  // pieces past the end: any valid page
-                    const int pg = load_page(p.block_table, p.max_pages, p.num_pages, b,
-                                             tc / p.page_size, p.err);
+        }
+        const int per_tile = kTile / bp;
+        const int n_pieces = n_tiles * per_tile;
+        auto piece_page = [&](int pc) -> int {
+            if (pc >= n_pieces) return 0;
+            const int t = t0 + pc * bp;
+            const int tc = t < L ? t : L - 1;  // pieces past the end: any valid page
+            return load_page(p.block_table, p.max_pages, p.num_pages, b, tc / p.page_size,
+                             p.err);
+        };
+        int cur = piece_page(lane), nxt = piece_page(32 + lane);
+        for (int i = 0; i < n_tiles; ++i) {
+            const int s = i % S;
+            bool ok = true;
+            if (lane == 0) {
+                ok = mbar_wait(&empty[s], ((i / S) & 1) ^ 1, p.err);
+                if (ok) mbar_arrive_expect_tx(&full[s], 2 * Cfg::kTileBytes);
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            for (int sub = 0; sub < per_tile; ++sub) {
+                const int pc = i * per_tile + sub;
+                if (pc > 0 && (pc & 31) == 0) {
+                    cur = nxt;
+                    nxt = piece_page(pc + 32 + lane);
+                }
+                const int pg = __shfl_sync(0xffffffffu, cur, pc & 31);
+                if (lane == 0) {
+                    const int t = t0 + pc * bp;
                     // rows of KV heads kvg*HPT .. +HPT-1 of this piece (HPT > 1 only when a
                     // piece is a whole page, so the heads' rows are adjacent), all blocks
-                    const int y = (pg * p.Hkv + kvg * HPT) * p.page_size + (t & (p.page_size - 1));
+                    const int y =
+                        (pg * p.Hkv + kvg * HPT) * p.page_size + (t & (p.page_size - 1));
                     const uint32_t off = static_cast<uint32_t>(sub * NB * HPT) << (lbp + 7);
                     tma_load_3d(sK + s * Cfg::kTileBytes + off, &tmK, &full[s], 0, y, 0);
                     tma_load_3d(sV + s * Cfg::kTileBytes + off, &tmV, &full[s], 0, y, 0);
