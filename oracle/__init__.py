@@ -58,6 +58,14 @@ def _load():
         lib.oracle_indexer_scores.argtypes = [P, P, P, P, P, i, i, i, i, P, i, l, P]
         lib.oracle_topk.restype = i
         lib.oracle_topk.argtypes = [P, l, i, P]
+        lib.oracle_e4m3_decode.restype = d
+        lib.oracle_e4m3_decode.argtypes = [i]
+        lib.oracle_e4m3_encode.restype = i
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_quantize_e4m3_rows.restype = None
+        lib.oracle_quantize_e4m3_rows.argtypes = [P, l, i, P, P]
+        lib.oracle_indexer_scores_fp8.restype = None
+        lib.oracle_indexer_scores_fp8.argtypes = [P, P, P, P, P, P, P, i, i, i, i, P, i, l, P]
         _lib = lib
     return _lib
 
@@ -192,6 +200,57 @@ def indexer_scores(q, k_pool, w, block_table, seq_lens, batches=None):
     out = np.full((len(bl), stride), np.nan, dtype=np.float64)
     _load().oracle_indexer_scores(_ptr(qa), _ptr(ka), _ptr(wa), _ptr(bt), _ptr(sl), Hi, Di, P,
                                   bt.shape[1], _ptr(bl), len(bl), stride, _ptr(out))
+    return out
+
+
+def e4m3_decode(codes):
+    """Exact value (float64) of each e4m3 code (uint8 array-like; NaN for S.1111.111)."""
+    c = np.asarray(codes, dtype=np.int64)
+    lib = _load()
+    return np.vectorize(lambda v: lib.oracle_e4m3_decode(int(v)), otypes=[np.float64])(c)
+
+
+def e4m3_encode(x):
+    """Nearest e4m3 code (uint8) to each float32 value, saturating at +-448."""
+    xs = np.asarray(x, dtype=np.float32)
+    lib = _load()
+    return np.vectorize(lambda v: lib.oracle_e4m3_encode(float(v)), otypes=[np.uint8])(xs)
+
+
+def quantize_e4m3_rows(x):
+    """bf16 x [..., C] -> (e4m3 codes uint8 [..., C], float32 scale per row [...])."""
+    xa, dt = _arr(x)
+    assert dt == 1
+    C = xa.shape[-1]
+    rows = int(np.prod(xa.shape[:-1]))
+    codes = np.zeros(xa.shape, dtype=np.uint8)
+    scales = np.zeros(xa.shape[:-1], dtype=np.float32)
+    _load().oracle_quantize_e4m3_rows(_ptr(xa), rows, C, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def indexer_scores_fp8(q8, q_scale, k8_pool, k_scale, w, block_table, seq_lens, batches=None):
+    """fp64 FP8-indexer scores [n_b, max L] for the listed batch rows (NaN past L_b).
+
+    q8 [B,Hi,Di] and k8_pool [num_pages,P,Di] hold e4m3 codes (uint8), q_scale [B,Hi] and
+    k_scale [num_pages,P] their float32 row scales.
+    """
+    qa = np.ascontiguousarray(np.asarray(q8, dtype=np.uint8))
+    ka = np.ascontiguousarray(np.asarray(k8_pool, dtype=np.uint8))
+    qs = np.ascontiguousarray(np.asarray(q_scale, dtype=np.float32))
+    ks = np.ascontiguousarray(np.asarray(k_scale, dtype=np.float32))
+    wa = np.ascontiguousarray(np.asarray(_arr(w)[0], dtype=np.float32))
+    bt = np.ascontiguousarray(np.asarray(_arr(block_table)[0], dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(_arr(seq_lens)[0], dtype=np.int32))
+    B, Hi, Di = qa.shape
+    P = ka.shape[1]
+    bl = np.arange(B, dtype=np.int32) if batches is None else np.asarray(batches, dtype=np.int32)
+    bl = np.ascontiguousarray(bl)
+    stride = int(sl[bl].max())
+    out = np.full((len(bl), stride), np.nan, dtype=np.float64)
+    _load().oracle_indexer_scores_fp8(_ptr(qa), _ptr(qs), _ptr(ka), _ptr(ks), _ptr(wa), _ptr(bt),
+                                      _ptr(sl), Hi, Di, P, bt.shape[1], _ptr(bl), len(bl), stride,
+                                      _ptr(out))
     return out
 
 

@@ -246,3 +246,92 @@ int oracle_topk(const double *scores, long L, int k, int32_t *idx_out) {
     free(all);
     return count;
 }
+
+/*
+ * FP8 lightning indexer ("Long context, KV eviction and sparse attention", section on
+ * exact selection with a fast scorer: the indexer scores every past token with few heads
+ * in FP8). The pages give neither the code format nor the scaling; the readings used:
+ *  - codes are e4m3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent field
+ *    0 holds subnormals (m/8 * 2^-6); S.1111.111 is NaN; no infinities; largest finite
+ *    value 448;
+ *  - one float32 scale per key row (token) and per query row (head): amax / 448, so that
+ *    the largest magnitude lands on the largest finite code (a row of zeros: scale 1);
+ *  - a value is encoded as the nearest code to x / scale (ties: the code with the even
+ *    last bit), magnitudes above 448 saturating to 448.
+ */
+double oracle_e4m3_decode(int code) {
+    int sign = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = (e == 0) ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Nearest e4m3 code to the float32 x, by comparison with every finite code. */
+int oracle_e4m3_encode(float xf) {
+    double x = (double)xf;
+    if (isnan(x)) return 0x7F;
+    int sign = x < 0 || (x == 0 && signbit(x));
+    double a = fabs(x);
+    if (a >= 448.0) return (sign << 7) | 0x7E;
+    int best = 0;
+    double best_d = a;  /* distance to code 0 (value 0) */
+    for (int c = 1; c <= 0x7E; c++) {
+        double d = fabs(oracle_e4m3_decode(c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (sign << 7) | best;
+}
+
+/* Row-wise quantization of bf16 x [rows, cols] to e4m3 codes and one float32 scale per row.
+ * The scale and the quotients are computed in float32, as the kernel does, so that both
+ * sides round the same values. */
+void oracle_quantize_e4m3_rows(const void *x, long rows, int cols, uint8_t *codes,
+                               float *scales) {
+    for (long r = 0; r < rows; r++) {
+        float amax = 0.0f;
+        for (int c = 0; c < cols; c++) {
+            float v = (float)widen(x, 1, (size_t)r * cols + c);
+            if (fabsf(v) > amax) amax = fabsf(v);
+        }
+        float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scales[r] = s;
+        for (int c = 0; c < cols; c++) {
+            float v = (float)widen(x, 1, (size_t)r * cols + c);
+            codes[(size_t)r * cols + c] = (uint8_t)oracle_e4m3_encode(v / s);
+        }
+    }
+}
+
+/*
+ * FP8 indexer scores: I_t = sum_h w_h * max(0, sum_j (sq_h q8_h[j]) (sk_t k8_t[j])) with
+ * every code decoded exactly. q8 [B,Hi,Di], q_scale [B,Hi]; k8_pool [num_pages,P,Di],
+ * k_scale [num_pages*P] (per physical row); w [B,Hi].
+ */
+void oracle_indexer_scores_fp8(const uint8_t *q8, const float *q_scale, const uint8_t *k8_pool,
+                               const float *k_scale, const float *w,
+                               const int32_t *block_table, const int32_t *seq_lens, int Hi,
+                               int Di, int page_size, int max_pages, const int32_t *b_list,
+                               int n_b, long out_stride, double *scores) {
+    for (int bi = 0; bi < n_b; bi++) {
+        int b = b_list[bi];
+        long L = seq_lens[b];
+#pragma omp parallel for schedule(static)
+        for (long t = 0; t < L; t++) {
+            size_t row = pool_row(block_table, max_pages, page_size, 1, b, 0, t);
+            double sk = (double)k_scale[row];
+            double total = 0.0;
+            for (int h = 0; h < Hi; h++) {
+                double sq = (double)q_scale[(size_t)b * Hi + h];
+                double dot = 0.0;
+                for (int j = 0; j < Di; j++)
+                    dot += (sq * oracle_e4m3_decode(q8[((size_t)b * Hi + h) * Di + j])) *
+                           (sk * oracle_e4m3_decode(k8_pool[row * Di + j]));
+                total += (double)w[(size_t)b * Hi + h] * (dot > 0.0 ? dot : 0.0);
+            }
+            scores[(size_t)bi * out_stride + t] = total;
+        }
+    }
+}

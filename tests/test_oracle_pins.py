@@ -351,3 +351,103 @@ def test_topk_single_head_positive_weight_is_topk_of_dot():
     dots = (x.k_pool.double().reshape(-1, 8)[:200] @ x.q[0, 0].double()).numpy()
     assert np.all(dots > 0)
     assert list(oracle.topk(s[0], 16)) == bf.topk_full_sort(list(dots), 16)
+
+
+# ----------------------------------------------------------------------------- FP8 indexer
+def test_e4m3_decode_format_points():
+    # format facts: a wrong exponent bias, subnormal rule, sign or NaN pattern fails one
+    cases = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+             0x3F: 1.875, 0x40: 2.0, 0x77: 240.0, 0x7E: 448.0, 0xFE: -448.0, 0xB8: -1.0}
+    got = oracle.e4m3_decode(list(cases))
+    assert list(got) == list(cases.values())
+    assert np.all(np.isnan(oracle.e4m3_decode([0x7F, 0xFF])))
+
+
+def test_e4m3_decode_matches_torch_float8():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().double().numpy()
+    got = oracle.e4m3_decode(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin])
+
+
+def test_e4m3_encode_matches_torch_rounding():
+    # nearest code, ties to the even code: a truncating or ties-away encoder fails the
+    # midpoints, a wrong binade boundary fails the random values
+    g = torch.Generator().manual_seed(970)
+    vals = np.array([oracle.e4m3_decode(c) for c in range(0x7F)])
+    mids = (vals[:-1] + vals[1:]) / 2
+    x = torch.cat([torch.randn(20000, generator=g) * s for s in (0.003, 1.0, 30.0, 150.0)] +
+                  [torch.tensor(mids, dtype=torch.float32), -torch.tensor(mids, dtype=torch.float32)])
+    x = x.clamp(-448.0, 448.0)
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle.e4m3_encode(x.numpy())
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_encode_saturates():
+    # magnitudes beyond the largest finite value clamp to it (no NaN, no wrap)
+    got = oracle.e4m3_encode([448.0, 449.0, 464.0, 1e6, -500.0, np.inf, -np.inf])
+    assert list(got) == [0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x7E, 0xFE]
+
+
+def test_quantize_rows_amax_lands_on_448_and_error_bound():
+    x = W.normal((64, 128), 971)
+    codes, s = oracle.quantize_e4m3_rows(x)
+    dec = oracle.e4m3_decode(codes)
+    # a scale off by a factor (or taken from the wrong row) moves the row maximum off 448
+    assert np.all(np.max(np.abs(dec), axis=1) == 448.0)
+    xf = x.float().numpy().astype(np.float64)
+    err = np.abs(dec * s[:, None] - xf)
+    # half a code step: 2^-4 relative for normals, 2^-10 of the scale below them
+    bound = np.maximum(np.abs(xf) * 2.0 ** -4, s[:, None] * 2.0 ** -10)
+    assert np.all(err <= bound * (1 + 1e-6))
+    z, sz = oracle.quantize_e4m3_rows(torch.zeros(2, 16, dtype=torch.bfloat16))
+    assert np.all(z == 0) and np.all(sz == 1.0)
+
+
+def _fp8_case(seed):
+    x = W.make_indexer(2, [37, 70], Hi=4, Di=32, page_size=16, shuffle=True, extra_pages=2,
+                       seed=seed)
+    rng = np.random.default_rng(seed)
+    cq = rng.integers(0, 256, size=tuple(x.q.shape)).astype(np.uint8)
+    ck = rng.integers(0, 256, size=tuple(x.k_pool.shape)).astype(np.uint8)
+    cq[(cq & 0x7F) == 0x7F] = 0x38  # no NaN codes
+    ck[(ck & 0x7F) == 0x7F] = 0x38
+    return x, cq, ck
+
+
+@pytest.mark.parametrize("seed", [972, 973])
+def test_indexer_fp8_unit_scales_equals_bf16_indexer(seed):
+    # every e4m3 value is a bf16 value: with unit scales the FP8 score is the (pinned) bf16
+    # indexer on the decoded codes; a mis-decoded code or a wrong row mapping fails
+    x, cq, ck = _fp8_case(seed)
+    qb = torch.from_numpy(oracle.e4m3_decode(cq)).to(torch.bfloat16)
+    kb = torch.from_numpy(oracle.e4m3_decode(ck)).to(torch.bfloat16)
+    ref = oracle.indexer_scores(qb, kb, x.w, x.block_table, x.seq_lens)
+    ones_q = np.ones(tuple(x.q.shape[:2]), np.float32)
+    ones_k = np.ones(tuple(x.k_pool.shape[:2]), np.float32)
+    got = oracle.indexer_scores_fp8(cq, ones_q, ck, ones_k, x.w, x.block_table, x.seq_lens)
+    fin = ~np.isnan(ref)
+    assert np.array_equal(fin, ~np.isnan(got))
+    _close(got[fin], ref[fin], 1e-12)
+
+
+def test_indexer_fp8_scales_factor_out():
+    # ReLU is positively homogeneous: a head's scale multiplies that head's weight and a
+    # token's scale multiplies its score; a scale on the wrong operand or row fails
+    x, cq, ck = _fp8_case(974)
+    rng = np.random.default_rng(975)
+    sq = rng.uniform(0.01, 2.0, size=tuple(x.q.shape[:2])).astype(np.float32)
+    sk = rng.uniform(0.01, 2.0, size=tuple(x.k_pool.shape[:2])).astype(np.float32)
+    got = oracle.indexer_scores_fp8(cq, sq, ck, sk, x.w, x.block_table, x.seq_lens)
+    w2 = (x.w.double() * torch.from_numpy(sq).double()).float()
+    base = oracle.indexer_scores_fp8(cq, np.ones_like(sq), ck, np.ones_like(sk), w2,
+                                     x.block_table, x.seq_lens)
+    bt = x.block_table.numpy()
+    for b, L in enumerate(x.seq_lens.tolist()):
+        rows = np.array([bt[b, t // 16] * 16 + t % 16 for t in range(L)])
+        ref = base[b, :L] * sk.reshape(-1)[rows].astype(np.float64)
+        # the weights product w*sq is rounded to float32 on this side only
+        _close(got[b, :L], ref, 1e-6)
