@@ -46,8 +46,10 @@
  *  - Every call is asynchronous on `stream`. Split-KV partial results live in
  *    the caller's workspace `ws` of at least kvd_workspace_size(...) bytes,
  *    zero-filled once before its first use; the kernels leave it ready for
- *    the next call of the same operation family. Calls that share a workspace
- *    must be ordered on one stream.
+ *    the next call of the same operation family with the same shape arguments
+ *    (the workspace's layout follows B, the head counts, the lengths and k).
+ *    Zero-fill it again before a call of the family with other shape
+ *    arguments. Calls that share a workspace must be ordered on one stream.
  *  - A workspace serves one operation family at a time: (1) GQA / SWA decode,
  *    (2) MLA decode (dense or sparse), (3) DSA indexer / top-k. A family
  *    keeps zero only the parts it relies on (completion counters, top-k
@@ -188,6 +190,50 @@ int dsa_indexer_topk(const void *q_idx, const void *k_idx_pool, const float *w,
                      int32_t *topk_count, float *scores_out, int B, int Hi, int Di, int page_size,
                      int max_pages, int num_pages, int k, void *ws, size_t ws_bytes,
                      cudaStream_t stream);
+
+/*
+ * FP8 lightning indexer + top-k. "Long context, KV eviction and sparse attention" (exact
+ * selection with a fast scorer): the indexer scores every past token with few heads in FP8.
+ * Codes are e4m3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no infinities; 448
+ * the largest finite value) with one float32 scale per row:
+ *  q8       [B, Hi, Di] e4m3 codes (uint8), device; q_scale [B, Hi] float32 (per head)
+ *  k8_pool  [num_pages, page_size, Di] e4m3 codes; k_scale [num_pages, page_size] float32
+ *           (per token, 16-byte aligned)
+ *  w        [B, Hi] float32
+ * Score of token t: I_t = k_scale(t) * sum_h w_h q_scale_h * ReLU(q8_h . k8_t), the codes
+ * decoded exactly and the dot products accumulated in fp32. Outputs, tie rule, workspace
+ * (kvd_workspace_size(KVD_OP_DSA_TOPK, ...)) and errors as dsa_indexer_topk.
+ * Supported: Hi == 64, Di == 128, 1 <= k <= 4096.
+ */
+int dsa_indexer_topk_fp8(const void *q8, const float *q_scale, const void *k8_pool,
+                         const float *k_scale, const float *w, const int32_t *block_table,
+                         const int32_t *seq_lens, int32_t *topk_idx, int32_t *topk_count,
+                         float *scores_out, int B, int Hi, int Di, int page_size, int max_pages,
+                         int num_pages, int k, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Row quantization to e4m3 (the FP8 indexer's query and key format): for each row of
+ * x [rows, cols] bf16 (device), scale = amax / 448 (1 for a row of zeros) and each code is
+ * the nearest e4m3 value to x / scale computed in float32 (ties to even, magnitudes above 448
+ * saturating). codes [rows, cols] uint8, scales [rows] float32, both device, caller-owned.
+ * Supported: 1 <= cols <= 65536. No workspace.
+ */
+int kvd_quantize_e4m3_rows(const void *x, void *codes, float *scales, int rows, int cols,
+                           cudaStream_t stream);
+
+/*
+ * FP8 indexer cache append ("Attention Optimizations", DSA / Computation Path: the new
+ * token's indexer key is written to the indexer cache before scoring): quantizes each
+ * sequence's new key k_new [B, Di] bf16 as kvd_quantize_e4m3_rows does and stores the codes
+ * and the scale at the cache row of position seq_lens[b] - 1 (page block_table[b][t / P],
+ * slot t % P) of k8_pool [num_pages, page_size, Di] / k_scale [num_pages, page_size].
+ * err: a device int that receives KVD_ERR_DEVICE_OOB when a length or page index is out of
+ * range (the write is then redirected to a clamped, valid row). Supported: Di <= 65536.
+ */
+int dsa_indexer_cache_append_fp8(const void *k_new, const int32_t *block_table,
+                                 const int32_t *seq_lens, void *k8_pool, float *k_scale, int B,
+                                 int Di, int page_size, int max_pages, int num_pages, int *err,
+                                 cudaStream_t stream);
 
 /*
  * Top-k selection alone over caller-provided scores.

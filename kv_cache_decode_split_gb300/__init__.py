@@ -28,6 +28,7 @@ lib = _lib.load()
 
 __all__ = [
     "attn_decode_gqa_paged", "attn_decode_swa_sink", "attn_decode_mla", "dsa_indexer_topk",
+    "dsa_indexer_topk_fp8", "quantize_e4m3_rows", "dsa_indexer_cache_append_fp8",
     "dsa_topk", "attn_decode_mla_sparse", "kvd_workspace_size", "kvd_check_device_error",
     "Workspace", "KvdError",
 ]
@@ -76,36 +77,42 @@ class Workspace:
     """A zero-filled device buffer reused across calls (grown on demand).
 
     The kernels of one operation family (GQA / SWA; MLA; DSA indexer / top-k) leave the
-    parts they rely on zeroed for the family's next call, so the buffer is zeroed only
-    when it is (re)allocated or handed to another family. Calls sharing one workspace
-    must be ordered on one stream.
+    parts they rely on zeroed for the family's next call with the same shape arguments (the
+    layout of the buffer follows them), so the buffer is zeroed only when it is
+    (re)allocated, handed to another family, or used with other shape arguments. Calls
+    sharing one workspace must be ordered on one stream.
     """
 
     def __init__(self, device=None):
         self.device = torch.device(device) if device is not None else torch.device("cuda")
         self.buffer = torch.zeros(0, dtype=torch.uint8, device=self.device)
         self.family = None
+        self.layout = None
 
-    def get(self, nbytes: int, family=None) -> torch.Tensor:
+    def get(self, nbytes: int, family=None, layout=None) -> torch.Tensor:
+        key = (family, layout)
         if self.buffer.numel() < nbytes:
             self.buffer = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=self.device)
-        elif family is not None and self.family is not None and family != self.family:
-            self.buffer.zero_()  # another family's kernels may have left non-zero state
+        elif family is not None and self.family is not None and key != (self.family, self.layout):
+            # another family's kernels, or the same family with another layout, may have
+            # left non-zero state where this call's kernels expect zeros
+            self.buffer.zero_()
         if family is not None:
-            self.family = family
+            self.family, self.layout = family, layout
         return self.buffer
 
 
 _default_ws = {}
 
 
-def _ws(workspace, nbytes, device, family):
-    """Workspace buffer for one call of an operation family ("gqa", "mla" or "dsa")."""
+def _ws(workspace, nbytes, device, family, layout=None):
+    """Workspace buffer for one call of an operation family ("gqa", "mla" or "dsa");
+    `layout` names the shape arguments the buffer's layout follows."""
     if workspace is None:
         key = (torch.device(device).index, family)
         workspace = _default_ws.setdefault(key, Workspace(device))
     if isinstance(workspace, Workspace):
-        buf = workspace.get(nbytes, family)
+        buf = workspace.get(nbytes, family, layout)
     else:
         buf = workspace
     if buf.numel() < nbytes:
@@ -137,7 +144,7 @@ def attn_decode_gqa_paged(q, k_pool, v_pool, block_table, seq_lens, scale=None, 
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     out = torch.empty_like(q) if out is None else out
     nbytes = kvd_workspace_size("gqa", B, Hq, Hkv, D, max_pages * P)
-    ws = _ws(workspace, nbytes, q.device, "gqa")
+    ws = _ws(workspace, nbytes, q.device, "gqa", layout=("gqa", B, Hq, Hkv, D, max_pages * P))
     st = lib.attn_decode_gqa_paged(_p(q), _p(k_pool), _p(v_pool), _p(block_table), _p(seq_lens),
                                    _p(out), _p(lse_out), B, Hq, Hkv, D, P, max_pages, num_pages,
                                    scale, _DT[q.dtype], _p(ws), ws.numel(), _stream(stream))
@@ -155,7 +162,8 @@ def attn_decode_swa_sink(q, k_pool, v_pool, block_table, seq_lens, window, n_sin
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     out = torch.empty_like(q) if out is None else out
     nbytes = kvd_workspace_size("swa", B, Hq, Hkv, D, max_pages * P, window, n_sink_tokens)
-    ws = _ws(workspace, nbytes, q.device, "gqa")
+    ws = _ws(workspace, nbytes, q.device, "gqa",
+             layout=("swa", B, Hq, Hkv, D, max_pages * P, window, n_sink_tokens))
     st = lib.attn_decode_swa_sink(_p(q), _p(k_pool), _p(v_pool), _p(block_table), _p(seq_lens),
                                   _p(out), _p(lse_out), B, Hq, Hkv, D, P, max_pages, num_pages,
                                   scale, _DT[q.dtype], int(window), int(n_sink_tokens),
@@ -182,7 +190,7 @@ def attn_decode_mla(q, c_pool, block_table, seq_lens, scale=1.0 / math.sqrt(192)
     B, H, d_qk, P, max_pages, num_pages = _mla_args(q, c_pool, block_table, seq_lens)
     out = torch.empty(B, H, d_v, dtype=torch.bfloat16, device=q.device) if out is None else out
     nbytes = kvd_workspace_size("mla", B, H, 1, d_v, max_pages * P)
-    ws = _ws(workspace, nbytes, q.device, "mla")
+    ws = _ws(workspace, nbytes, q.device, "mla", layout=("mla", B, H, max_pages * P))
     st = lib.attn_decode_mla(_p(q), _p(c_pool), _p(block_table), _p(seq_lens), _p(out),
                              _p(lse_out), B, H, d_qk, d_v, P, max_pages, num_pages, float(scale),
                              _p(ws), ws.numel(), _stream(stream))
@@ -205,12 +213,72 @@ def dsa_indexer_topk(q_idx, k_idx_pool, w, block_table, seq_lens, k=2048, topk_i
     topk_idx = torch.empty(B, k, dtype=torch.int32, device=dev) if topk_idx is None else topk_idx
     topk_count = torch.empty(B, dtype=torch.int32, device=dev) if topk_count is None else topk_count
     nbytes = kvd_workspace_size("dsa_topk", B, Hi, 1, Di, max_pages * P, k=k)
-    ws = _ws(workspace, nbytes, dev, "dsa")
+    ws = _ws(workspace, nbytes, dev, "dsa", layout=(B, max_pages * P, int(k)))
     st = lib.dsa_indexer_topk(_p(q_idx), _p(k_idx_pool), _p(w), _p(block_table), _p(seq_lens),
                               _p(topk_idx), _p(topk_count), _p(scores_out), B, Hi, Di, P,
                               max_pages, num_pages, int(k), _p(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_indexer_topk")
     return topk_idx, topk_count
+
+
+def dsa_indexer_topk_fp8(q8, q_scale, k8_pool, k_scale, w, block_table, seq_lens, k=2048,
+                         topk_idx=None, topk_count=None, scores_out=None, workspace=None,
+                         stream=None):
+    """FP8 indexer: e4m3 codes (uint8) with float32 row scales; same outputs as the bf16 one."""
+    _need(q8, "q8", torch.uint8, 3)
+    _need(q_scale, "q_scale", torch.float32, 2)
+    _need(k8_pool, "k8_pool", torch.uint8, 3)
+    _need(k_scale, "k_scale", torch.float32, 2)
+    _need(w, "w", torch.float32, 2)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, Hi, Di = q8.shape
+    num_pages, P, _ = k8_pool.shape
+    max_pages = block_table.shape[1]
+    dev = q8.device
+    topk_idx = torch.empty(B, k, dtype=torch.int32, device=dev) if topk_idx is None else topk_idx
+    topk_count = torch.empty(B, dtype=torch.int32, device=dev) if topk_count is None else topk_count
+    nbytes = kvd_workspace_size("dsa_topk", B, Hi, 1, Di, max_pages * P, k=k)
+    ws = _ws(workspace, nbytes, dev, "dsa", layout=(B, max_pages * P, int(k)))
+    st = lib.dsa_indexer_topk_fp8(_p(q8), _p(q_scale), _p(k8_pool), _p(k_scale), _p(w),
+                                  _p(block_table), _p(seq_lens), _p(topk_idx), _p(topk_count),
+                                  _p(scores_out), B, Hi, Di, P, max_pages, num_pages, int(k),
+                                  _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dsa_indexer_topk_fp8")
+    return topk_idx, topk_count
+
+
+def quantize_e4m3_rows(x, codes=None, scales=None, stream=None):
+    """bf16 x [..., C] -> (e4m3 codes uint8 [..., C], float32 scale per row [...])."""
+    _need(x, "x", torch.bfloat16)
+    C = x.shape[-1]
+    rows = x.numel() // C
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if codes is None else codes
+    scales = (torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+              if scales is None else scales)
+    st = lib.kvd_quantize_e4m3_rows(_p(x), _p(codes), _p(scales), rows, C, _stream(stream))
+    _check(st, "kvd_quantize_e4m3_rows")
+    return codes, scales
+
+
+def dsa_indexer_cache_append_fp8(k_new, block_table, seq_lens, k8_pool, k_scale, err=None,
+                                 stream=None):
+    """Quantize each sequence's new indexer key k_new [B, Di] bf16 into its cache row at
+    position seq_lens[b] - 1. `err` (int32 [1] on the device) receives a device error code."""
+    _need(k_new, "k_new", torch.bfloat16, 2)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(k8_pool, "k8_pool", torch.uint8, 3)
+    _need(k_scale, "k_scale", torch.float32, 2)
+    B, Di = k_new.shape
+    num_pages, P, _ = k8_pool.shape
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=k_new.device)
+    st = lib.dsa_indexer_cache_append_fp8(_p(k_new), _p(block_table), _p(seq_lens), _p(k8_pool),
+                                          _p(k_scale), B, Di, P, block_table.shape[1], num_pages,
+                                          _p(err), _stream(stream))
+    _check(st, "dsa_indexer_cache_append_fp8")
+    return err
 
 
 def dsa_topk(scores, lens, k=2048, topk_idx=None, topk_count=None, workspace=None, stream=None):
@@ -222,7 +290,7 @@ def dsa_topk(scores, lens, k=2048, topk_idx=None, topk_count=None, workspace=Non
     topk_idx = torch.empty(B, k, dtype=torch.int32, device=dev) if topk_idx is None else topk_idx
     topk_count = torch.empty(B, dtype=torch.int32, device=dev) if topk_count is None else topk_count
     nbytes = kvd_workspace_size("dsa_topk", B, 1, 1, 0, stride, k=k)
-    ws = _ws(workspace, nbytes, dev, "dsa")
+    ws = _ws(workspace, nbytes, dev, "dsa", layout=(B, stride, int(k)))
     st = lib.dsa_topk(_p(scores), _p(lens), _p(topk_idx), _p(topk_count), B, stride, int(k),
                       _p(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_topk")
@@ -239,7 +307,7 @@ def attn_decode_mla_sparse(q, c_pool, block_table, seq_lens, topk_idx, topk_coun
     k = topk_idx.shape[1]
     out = torch.empty(B, H, d_v, dtype=torch.bfloat16, device=q.device) if out is None else out
     nbytes = kvd_workspace_size("mla_sparse", B, H, 1, d_v, max_pages * P, k=k)
-    ws = _ws(workspace, nbytes, q.device, "mla")
+    ws = _ws(workspace, nbytes, q.device, "mla", layout=("mla_sparse", B, H, int(k)))
     st = lib.attn_decode_mla_sparse(_p(q), _p(c_pool), _p(block_table), _p(seq_lens),
                                     _p(topk_idx), _p(topk_count), _p(out), _p(lse_out), B, H,
                                     d_qk, d_v, k, P, max_pages, num_pages, float(scale), _p(ws),

@@ -67,6 +67,29 @@ int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_
     return r == CUDA_SUCCESS ? KVD_OK : KVD_ERR_CUDA;
 }
 
+// Row-major [rows, cols] bytes (e4m3 codes): 128-byte boxes of box_rows rows, 128-byte swizzle.
+int make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return KVD_ERR_CUDA;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KVD_OK : KVD_ERR_CUDA;
+}
+
 // 3-D view of a row-major [rows, cols] bf16 matrix as (64-element column piece, row,
 // column block); the block's stride (128 bytes) is smaller than the row pitch, so a box
 // {64, box_rows, nblocks} lands in shared memory as [block][row][64] with 128-byte swizzle.
@@ -353,13 +376,18 @@ int attn_decode_mla(const void* q, const void* c_pool, const int32_t* block_tabl
                    d_qk, d_v, page_size, max_pages, num_pages, scale, ws, ws_bytes, stream);
 }
 
-int dsa_indexer_topk(const void* q_idx, const void* k_idx_pool, const float* w,
-                     const int32_t* block_table, const int32_t* seq_lens, int32_t* topk_idx,
-                     int32_t* topk_count, float* scores_out, int B, int Hi, int Di, int page_size,
-                     int max_pages, int num_pages, int k, void* ws, size_t ws_bytes,
-                     cudaStream_t stream) {
+// Both indexer precisions (fp8: e4m3 codes with row scales): validation, workspace layout,
+// tensor maps, the indexer launch, then the selection.
+static int indexer_topk(bool fp8, const void* q_idx, const float* q_scale, const void* k_idx_pool,
+                        const float* k_scale, const float* w, const int32_t* block_table,
+                        const int32_t* seq_lens, int32_t* topk_idx, int32_t* topk_count,
+                        float* scores_out, int B, int Hi, int Di, int page_size, int max_pages,
+                        int num_pages, int k, void* ws, size_t ws_bytes, cudaStream_t stream) {
     if (!q_idx || !k_idx_pool || !w || !block_table || !seq_lens || !topk_idx || !topk_count ||
         !ws)
+        return KVD_ERR_INVALID_ARG;
+    if (fp8 && (!q_scale || !k_scale || !aligned16(k_scale) ||
+                (reinterpret_cast<uintptr_t>(q_scale) & 3)))
         return KVD_ERR_INVALID_ARG;
     if (B < 1 || max_pages < 1 || num_pages < 1 || k < 1) return KVD_ERR_INVALID_ARG;
     if (Hi != 64 || Di != 128 || k > kTopkMaxK) return KVD_ERR_UNSUPPORTED;
@@ -378,6 +406,8 @@ int dsa_indexer_topk(const void* q_idx, const void* k_idx_pool, const float* w,
     std::memset(&ip, 0, sizeof ip);
     ip.q = q_idx;
     ip.w = w;
+    ip.q_scale = q_scale;
+    ip.k_scale = k_scale;
     ip.block_table = block_table;
     ip.seq_lens = seq_lens;
     ip.scores = scores_out ? scores_out : reinterpret_cast<float*>(wb + lay.off_scores);
@@ -392,15 +422,25 @@ int dsa_indexer_topk(const void* q_idx, const void* k_idx_pool, const float* w,
     ip.max_len = max_len;
     ip.tiles_per_b = (max_len + 127) / 128;
     CUtensorMap tk, tk128, tq;
-    if (make_tmap_bf16_2d(&tk, k_idx_pool, (uint64_t)num_pages * page_size, 128,
-                          page_size < 128 ? page_size : 128) != KVD_OK)
-        return KVD_ERR_CUDA;
-    // one instruction per 128-token tile when its rows are contiguous in the pool
-    if (make_tmap_bf16_blocked(&tk128, k_idx_pool, (uint64_t)num_pages * page_size, 128, 128,
-                               2) != KVD_OK)
-        return KVD_ERR_CUDA;
-    if (make_tmap_bf16_2d(&tq, q_idx, (uint64_t)B * 64, 128, 64) != KVD_OK) return KVD_ERR_CUDA;
-    int st = dsa_indexer_launch(ip, tk, tk128, tq, stream);
+    const uint64_t rows = (uint64_t)num_pages * page_size;
+    const uint32_t piece = page_size < 128 ? page_size : 128;
+    int st;
+    if (fp8) {
+        // one-byte codes: a 128-dim row is one 128-byte box
+        if (make_tmap_u8_2d(&tk, k_idx_pool, rows, 128, piece) != KVD_OK ||
+            make_tmap_u8_2d(&tk128, k_idx_pool, rows, 128, 128) != KVD_OK ||
+            make_tmap_u8_2d(&tq, q_idx, (uint64_t)B * 64, 128, 64) != KVD_OK)
+            return KVD_ERR_CUDA;
+        st = dsa_indexer_fp8_launch(ip, tk, tk128, tq, stream);
+    } else {
+        if (make_tmap_bf16_2d(&tk, k_idx_pool, rows, 128, piece) != KVD_OK) return KVD_ERR_CUDA;
+        // one instruction per 128-token tile when its rows are contiguous in the pool
+        if (make_tmap_bf16_blocked(&tk128, k_idx_pool, rows, 128, 128, 2) != KVD_OK)
+            return KVD_ERR_CUDA;
+        if (make_tmap_bf16_2d(&tq, q_idx, (uint64_t)B * 64, 128, 64) != KVD_OK)
+            return KVD_ERR_CUDA;
+        st = dsa_indexer_launch(ip, tk, tk128, tq, stream);
+    }
     if (st != KVD_OK) return st;
     TopkParams tp;
     std::memset(&tp, 0, sizeof tp);
@@ -419,6 +459,73 @@ int dsa_indexer_topk(const void* q_idx, const void* k_idx_pool, const float* w,
     tp.k = k;
     tp.max_len = max_len;
     return topk_launch(tp, false, stream);
+}
+
+int dsa_indexer_topk(const void* q_idx, const void* k_idx_pool, const float* w,
+                     const int32_t* block_table, const int32_t* seq_lens, int32_t* topk_idx,
+                     int32_t* topk_count, float* scores_out, int B, int Hi, int Di, int page_size,
+                     int max_pages, int num_pages, int k, void* ws, size_t ws_bytes,
+                     cudaStream_t stream) {
+    return indexer_topk(false, q_idx, nullptr, k_idx_pool, nullptr, w, block_table, seq_lens,
+                        topk_idx, topk_count, scores_out, B, Hi, Di, page_size, max_pages,
+                        num_pages, k, ws, ws_bytes, stream);
+}
+
+int dsa_indexer_topk_fp8(const void* q8, const float* q_scale, const void* k8_pool,
+                         const float* k_scale, const float* w, const int32_t* block_table,
+                         const int32_t* seq_lens, int32_t* topk_idx, int32_t* topk_count,
+                         float* scores_out, int B, int Hi, int Di, int page_size, int max_pages,
+                         int num_pages, int k, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    return indexer_topk(true, q8, q_scale, k8_pool, k_scale, w, block_table, seq_lens, topk_idx,
+                        topk_count, scores_out, B, Hi, Di, page_size, max_pages, num_pages, k, ws,
+                        ws_bytes, stream);
+}
+
+int kvd_quantize_e4m3_rows(const void* x, void* codes, float* scales, int rows, int cols,
+                           cudaStream_t stream) {
+    if (!x || !codes || !scales) return KVD_ERR_INVALID_ARG;
+    if (rows < 1 || cols < 1 || cols > 65536) return KVD_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) & 1) || (reinterpret_cast<uintptr_t>(scales) & 3))
+        return KVD_ERR_INVALID_ARG;
+    QuantParams qp;
+    std::memset(&qp, 0, sizeof qp);
+    qp.x = x;
+    qp.codes = codes;
+    qp.scales = scales;
+    qp.rows = rows;
+    qp.cols = cols;
+    return quantize_e4m3_launch(qp, stream);
+}
+
+int dsa_indexer_cache_append_fp8(const void* k_new, const int32_t* block_table,
+                                 const int32_t* seq_lens, void* k8_pool, float* k_scale, int B,
+                                 int Di, int page_size, int max_pages, int num_pages, int* err,
+                                 cudaStream_t stream) {
+    if (!k_new || !block_table || !seq_lens || !k8_pool || !k_scale || !err)
+        return KVD_ERR_INVALID_ARG;
+    if (B < 1 || Di < 1 || Di > 65536 || max_pages < 1 || num_pages < 1 || page_size < 1)
+        return KVD_ERR_INVALID_ARG;
+    if ((long long)num_pages * page_size >= (1LL << 31) ||
+        (long long)max_pages * page_size >= (1LL << 30))
+        return KVD_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(k_new) & 1) || (reinterpret_cast<uintptr_t>(k_scale) & 3) ||
+        (reinterpret_cast<uintptr_t>(err) & 3))
+        return KVD_ERR_INVALID_ARG;
+    QuantParams qp;
+    std::memset(&qp, 0, sizeof qp);
+    qp.x = k_new;
+    qp.codes = k8_pool;
+    qp.scales = k_scale;
+    qp.block_table = block_table;
+    qp.seq_lens = seq_lens;
+    qp.err = err;
+    qp.rows = B;
+    qp.cols = Di;
+    qp.page_size = page_size;
+    qp.max_pages = max_pages;
+    qp.num_pages = num_pages;
+    qp.max_len = max_pages * page_size;
+    return quantize_e4m3_launch(qp, stream);
 }
 
 int dsa_topk(const float* scores, const int32_t* lens, int32_t* topk_idx, int32_t* topk_count,

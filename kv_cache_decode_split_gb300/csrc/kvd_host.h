@@ -66,8 +66,10 @@ int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t
 constexpr int kTopkMaxK = 4096;
 
 struct IdxParams {
-    const void* q;             // [B, 64, 128] bf16 (read through a tensor map)
+    const void* q;             // [B, 64, 128] bf16 or e4m3 (read through a tensor map)
     const float* w;            // [B, 64]
+    const float* q_scale;      // FP8 indexer: [B, 64] per-head query scales
+    const float* k_scale;      // FP8 indexer: [num_pages * page_size] per-token key scales
     const int32_t* block_table;
     const int32_t* seq_lens;
     float* scores;             // [B, score_stride]
@@ -76,6 +78,18 @@ struct IdxParams {
     int* counts;               // [B, 4] selection counters, zeroed here for the selection
     int* err;
     int B, page_size, max_pages, num_pages, max_len, tiles_per_b;
+};
+
+// Row quantization to e4m3 (dsa_indexer_fp8.cu). With a block table, row r is sequence r's
+// newest token (position seq_lens[r] - 1) and lands on that token's row of the paged cache.
+struct QuantParams {
+    const void* x;             // [rows, cols] bf16
+    void* codes;               // e4m3 codes, [rows or cache rows, cols]
+    float* scales;             // one float32 scale per row
+    const int32_t* block_table;  // null: row r to row r
+    const int32_t* seq_lens;
+    int* err;
+    int rows, cols, page_size, max_pages, num_pages, max_len;
 };
 
 struct TopkParams {
@@ -101,6 +115,9 @@ TopkLayout topk_layout(int B, int max_len, int k, bool with_scores);
 
 int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensorMap& tk128,
                        const CUtensorMap& tq, cudaStream_t stream);
+int dsa_indexer_fp8_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensorMap& tk128,
+                           const CUtensorMap& tq, cudaStream_t stream);
+int quantize_e4m3_launch(const QuantParams& p, cudaStream_t stream);
 int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------------------
@@ -142,6 +159,8 @@ int make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_
 
 // 3-D bf16 tensor map over a row-major [rows, cols] matrix: box {64, box_rows, nblocks}
 // fills shared memory as [block][row][64] with 128-byte swizzle (cols a multiple of 64).
+int make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows);
 int make_tmap_bf16_blocked(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                            uint32_t box_rows, uint32_t nblocks);
 

@@ -183,3 +183,21 @@ def test_topk_non_zeroed_workspace_is_reported(kvd):
         L = int(lens[b])
         ref = oracle.topk(s[b, :L].numpy().astype(np.float64), k)
         assert np.array_equal(idx[b].cpu().numpy(), ref)
+
+
+def test_workspace_reused_across_shapes(kvd):
+    # one workspace, large from the start, serving selections of other batch sizes, lengths
+    # and k in turn: the layout moves with them, so stale lists from one call must not be
+    # read as the next call's zeroed histogram
+    ws = kvd.Workspace(torch.device("cuda"))
+    ws.get(64 << 20)
+    for B, L, k in [(2, 50000, 2048), (4, 20000, 300), (3, 7000, 2048), (4, 20000, 300)]:
+        s = W.normal((B, L), 999 + B + k, 1.0, torch.float32)
+        lens = torch.full((B,), L, dtype=torch.int32)
+        idx, cnt = kvd.dsa_topk(s.cuda(), lens.cuda(), k=k, workspace=ws)
+        torch.cuda.synchronize()
+        for b in range(B):
+            ref = oracle.topk(s[b].numpy().astype(np.float64), k)
+            assert int(cnt[b]) == min(k, L)
+            assert np.array_equal(idx[b].cpu().numpy()[:len(ref)], ref), (B, L, k, b)
+        assert kvd.kvd_check_device_error(ws) == 0

@@ -237,7 +237,56 @@ WORKLOADS = {
         "dsa_sparse_mla", 5, "dsa",
         dict(B=4, H=128, L=131072, Hi=64, Di=128, k=2048, page_size=64, factor=0.1),
         "DSA: indexer (64 heads x 128) over L=131072, top-2048, then 128-head sparse MLA, B=4"),
+    "dsa_fp8_sparse_mla": Workload(
+        "dsa_fp8_sparse_mla", 6, "dsa_fp8",
+        dict(B=4, H=128, L=131072, Hi=64, Di=128, k=2048, page_size=64, factor=0.1),
+        "DSA with the FP8 indexer: e4m3 keys and queries with float32 row scales (64 heads x "
+        "128) over L=131072, top-2048, then 128-head sparse MLA, B=4"),
 }
+
+
+@dataclass
+class IndexerFp8Inputs:
+    q8: torch.Tensor           # [B, Hi, Di] uint8 e4m3 codes
+    q_scale: torch.Tensor      # [B, Hi] float32
+    k8_pool: torch.Tensor      # [num_pages, P, Di] uint8 e4m3 codes
+    k_scale: torch.Tensor      # [num_pages, P] float32
+    w: torch.Tensor            # [B, Hi] float32
+    block_table: torch.Tensor  # [B, max_pages] int32
+    seq_lens: torch.Tensor     # [B] int32
+    page_size: int
+    k: int
+
+    @property
+    def B(self): return self.q8.shape[0]
+    @property
+    def max_pages(self): return self.block_table.shape[1]
+    @property
+    def num_pages(self): return self.k8_pool.shape[0]
+
+
+def e4m3_codes(shape, seed: int, factor: float = 1.0) -> torch.Tensor:
+    """uint8 e4m3 codes of seeded N(0,1) * factor draws (torch's float8 conversion)."""
+    return normal(shape, seed, factor, torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def uniform_f32(shape, lo: float, hi: float, seed: int) -> torch.Tensor:
+    """float32 draws uniform in [lo, hi)."""
+    return lo + (hi - lo) * torch.rand(*shape, generator=_gen(seed), dtype=torch.float32)
+
+
+def make_indexer_fp8(B, seq_lens, *, Hi=64, Di=128, k=2048, page_size=64, max_pages=None,
+                     shuffle=False, extra_pages=0, seed=0, block_table=None) -> IndexerFp8Inputs:
+    """FP8 indexer inputs: codes of N(0,1) draws, per-row scales uniform in [0.25, 1)."""
+    base = make_indexer(B, seq_lens, Hi=Hi, Di=Di, k=k, page_size=page_size,
+                        max_pages=max_pages, shuffle=shuffle, extra_pages=extra_pages, seed=seed,
+                        block_table=block_table)
+    num_pages = base.k_pool.shape[0]
+    return IndexerFp8Inputs(
+        e4m3_codes((B, Hi, Di), seed + 8), uniform_f32((B, Hi), 0.25, 1.0, seed + 10),
+        e4m3_codes((num_pages, page_size, Di), seed + 9),
+        uniform_f32((num_pages, page_size), 0.25, 1.0, seed + 11), base.w, base.block_table,
+        base.seq_lens, page_size, int(k))
 
 
 def build(name: str, *, sharp: bool = False):
@@ -266,5 +315,11 @@ def build(name: str, *, sharp: bool = False):
                        factor=factor)
         idx = make_indexer(p["B"], [p["L"]] * p["B"], Hi=p["Hi"], Di=p["Di"], k=p["k"],
                            page_size=p["page_size"], seed=base, block_table=mla.block_table)
+        return idx, mla
+    if w.kind == "dsa_fp8":
+        mla = make_mla(p["B"], p["H"], [p["L"]] * p["B"], page_size=p["page_size"], seed=base,
+                       factor=factor)
+        idx = make_indexer_fp8(p["B"], [p["L"]] * p["B"], Hi=p["Hi"], Di=p["Di"], k=p["k"],
+                               page_size=p["page_size"], seed=base, block_table=mla.block_table)
         return idx, mla
     raise KeyError(name)
