@@ -331,7 +331,92 @@ class DsaRunner:
         return done, el, f"{n} of {xm.B} sequences (indexer, top-k and sparse MLA, all heads)"
 
 
-RUNNERS = {"gqa": GqaRunner, "swa": GqaRunner, "mla": MlaRunner, "dsa": DsaRunner}
+class DsaFp8Runner(DsaRunner):
+    """dsa_indexer_topk_fp8 then attn_decode_mla_sparse (FP8 indexer, top-2048, sparse MLA)."""
+    kernel = "dsa_indexer_fp8_kernel"
+
+    def __init__(self, name, dev, sharp=False):
+        import kv_cache_decode_split_gb300 as kvd
+        self.kvd = kvd
+        self.name = name
+        self.xi, self.xm = xi, xm = W.build(name, sharp=sharp)
+        self.dev = dev
+        self.qi = xi.q8.to(dev)
+        self.qs = xi.q_scale.to(dev)
+        self.ki = xi.k8_pool.to(dev)
+        self.ks = xi.k_scale.to(dev)
+        self.w = xi.w.to(dev)
+        self.q = xm.q.to(dev)
+        self.c = xm.c_pool.to(dev)
+        self.bt = xm.block_table.to(dev)
+        self.sl = xm.seq_lens.to(dev)
+        self.k = xi.k
+        self.idx = torch.empty(xi.B, xi.k, dtype=torch.int32, device=dev)
+        self.cnt = torch.empty(xi.B, dtype=torch.int32, device=dev)
+        self.out = torch.empty(xm.B, xm.H, 512, dtype=torch.bfloat16, device=dev)
+        self.ws1 = kvd.Workspace(dev)
+        self.ws2 = kvd.Workspace(dev)
+        self._config, self.bytes, self.flops = self.describe(name, (xi, xm))
+
+    @staticmethod
+    def describe(name, x):
+        xi, xm = x
+        lens = [int(v) for v in xm.seq_lens]
+        Hi, Di = xi.q8.shape[1], xi.q8.shape[2]
+        sel = sum(min(xi.k, L) for L in lens)
+        # one-byte key codes and a float32 scale per token, then the selected latent rows
+        nbytes = sum(lens) * (Di + 4) + sel * xm.d_qk * 2
+        flops = 2.0 * sum(lens) * Hi * Di + 2.0 * sel * xm.H * (xm.d_qk + 512)
+        cfg = {"workload": name, "B": xm.B, "H": xm.H, "Hi": Hi, "Di": Di, "k": xi.k,
+               "seq_len": lens[0], "page_size": xm.page_size, "indexer": "e4m3 + f32 row scales",
+               "kv_bytes": nbytes, "flops": flops}
+        return cfg, nbytes, flops
+
+    def step(self, qi=None, q=None):
+        xm = self.xm
+        self.kvd.dsa_indexer_topk_fp8(self.qi if qi is None else qi, self.qs, self.ki, self.ks,
+                                      self.w, self.bt, self.sl, k=self.k, topk_idx=self.idx,
+                                      topk_count=self.cnt, workspace=self.ws1)
+        return self.kvd.attn_decode_mla_sparse(self.q if q is None else q, self.c, self.bt,
+                                               self.sl, self.idx, self.cnt, scale=xm.scale,
+                                               out=self.out, workspace=self.ws2)
+
+    def e2e_setup(self):
+        self.h_qi = self.xi.q8.pin_memory()
+        self.h_q = self.xm.q.pin_memory()
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.d_qi = torch.empty_like(self.qi)
+        self.d_q = torch.empty_like(self.q)
+        return self.h_qi.numel() + self.h_q.numel() * 2, self.h_out.numel() * 2
+
+    def oracle_sample(self, budget_s):
+        import numpy as np
+        import oracle
+        xi, xm = self.xi, self.xm
+        t0 = time.perf_counter()
+        done, n = 0, 0
+        for b in range(xm.B):
+            sc = oracle.indexer_scores_fp8(xi.q8.numpy(), xi.q_scale.numpy(), xi.k8_pool.numpy(),
+                                           xi.k_scale.numpy(), xi.w, xi.block_table,
+                                           xi.seq_lens, batches=[b])[0]
+            L = int(xm.seq_lens[b])
+            idx = oracle.topk(sc[:L].astype(np.float32), self.k)
+            full = np.full((xm.B, self.k), -1, np.int32)
+            full[b, :len(idx)] = idx
+            cnt = np.zeros(xm.B, np.int32)
+            cnt[b] = len(idx)
+            oracle.mla(xm.q, xm.c_pool, xm.block_table, xm.seq_lens, xm.scale, idx=full,
+                       idx_count=cnt, pairs=[(b, h) for h in range(xm.H)])
+            done += L * (xi.q8.shape[2] + 4) + len(idx) * xm.d_qk * 2
+            n += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        el = time.perf_counter() - t0
+        return done, el, f"{n} of {xm.B} sequences (FP8 indexer, top-k and sparse MLA, all heads)"
+
+
+RUNNERS = {"gqa": GqaRunner, "swa": GqaRunner, "mla": MlaRunner, "dsa": DsaRunner,
+           "dsa_fp8": DsaFp8Runner}
 
 
 def make_runner(name, dev):
@@ -455,7 +540,7 @@ def oracle_runner(name):
     cls = RUNNERS[W.WORKLOADS[name].kind]
     r = cls.__new__(cls)
     r.name = name
-    if cls is DsaRunner:
+    if cls in (DsaRunner, DsaFp8Runner):
         r.xi, r.xm = W.build(name)
         r.k = r.xi.k
     else:
