@@ -35,6 +35,7 @@ constexpr int kFStages = 8;
 constexpr int kFScaleSlots = 8;
 constexpr int kFThreads = 6 * 32;                 // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kFHistBins = 2048;                  // top 11 key bits
+constexpr int kFRowCap = 512;                     // page pieces resolved ahead (a chunk)
 
 struct IdxF8Smem {
     uint8_t stage[kFStages][kFTileBytes];         // 1024-aligned (offset 0)
@@ -45,6 +46,7 @@ struct IdxF8Smem {
     uint64_t full[kFStages], empty[kFStages], sfull[kFScaleSlots], sempty[kFScaleSlots];
     uint64_t qfull[2], qempty[2], tfull[2], tempty[2], done;
     uint32_t tmem_base;
+    int prow[kFRowCap];                           // first physical row of each piece
 };
 constexpr int kFSmem = static_cast<int>(sizeof(IdxF8Smem)) + 1024;
 
@@ -55,6 +57,19 @@ __device__ __forceinline__ F8Range f8_tiles(int total) {
     const long long G = gridDim.x, i = blockIdx.x;
     return F8Range{static_cast<int>(i * total / G), static_cast<int>((i + 1) * total / G)};
 }
+
+// (sequence, tile within it) of flat tile f, advanced without a division per tile
+struct TileCursor {
+    int b, j, per_b;
+    __device__ TileCursor(int f, int tiles_per_b)
+        : b(f / tiles_per_b), j(f % tiles_per_b), per_b(tiles_per_b) {}
+    __device__ void next() {
+        if (++j == per_b) {
+            j = 0;
+            ++b;
+        }
+    }
+};
 
 __global__ void __launch_bounds__(kFThreads, 1)
     dsa_indexer_fp8_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -100,92 +115,82 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
-        // The warp resolves the physical rows of the range's page pieces 32 at a time (lane
-        // k: piece 32 m + k), the next batch in flight while the current one is used; lane 0
-        // issues the key copies and the copies of the matching per-token scales.
+        // The warp resolves the physical rows of the range's page pieces a chunk at a time
+        // into shared memory; lane 0 then issues the key copies and the copies of the
+        // matching per-token scales.
         if (lane == 0) {
             prefetch_tensormap(&tmK);
             prefetch_tensormap(&tmK128);
             prefetch_tensormap(&tmQ);
         }
         const int bp = min(p.page_size, kFTile);
-        const int per_tile = kFTile / bp;
-        const int n_pieces = (tr.end - tr.begin) * per_tile;
-        // first physical row of piece q, or -1 for a tile past its sequence's end
-        auto piece_row = [&](int q) -> int {
-            if (q >= n_pieces) return -1;
-            const int f = tr.begin + q / per_tile, sub = q % per_tile;
-            const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
-            const int L = load_len(p.seq_lens, b, p.max_len, p.err);
-            if (j * kFTile >= L) return -1;
-            const int t = j * kFTile + sub * bp;
-            const int tc = t < L ? t : L - 1;  // rows past the end: a valid page
-            const int pg = load_page(p.block_table, p.max_pages, p.num_pages, b,
-                                     tc / p.page_size, p.err);
-            return pg * p.page_size + (t % p.page_size);
-        };
-        int cur = piece_row(lane), nxt = piece_row(32 + lane);
-        int cur_b = -1;
+        const int per_tile = kFTile / bp;  // 1, 2, 4 or 8 pieces a tile
+        const int chunk = kFRowCap / per_tile;
         uint32_t g = 0, nq = 0;
+        int cur_b = -1;
         bool ok = true;
-        for (int f = tr.begin; f < tr.end && ok; ++f) {
-            const int fi = f - tr.begin;
-            int ys[kFTile / 16];
-#pragma unroll
-            for (int sub = 0; sub < kFTile / 16; ++sub) {
-                if (sub >= per_tile) break;
-                const int q = fi * per_tile + sub;
-                if (q > 0 && (q & 31) == 0) {
-                    cur = nxt;
-                    nxt = piece_row(q + 32 + lane);
+        for (int c0 = tr.begin; c0 < tr.end && ok; c0 += chunk) {
+            const int c1 = min(tr.end, c0 + chunk);
+            // the warp resolves the chunk's piece rows (first physical row of each piece, or
+            // -1 for a tile past its sequence's end), lane k taking pieces k, k + 32, ...
+            for (int q = lane; q < (c1 - c0) * per_tile; q += 32) {
+                const int f = c0 + q / per_tile, sub = q % per_tile;
+                const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
+                const int L = load_len(p.seq_lens, b, p.max_len, p.err);
+                int row = -1;
+                if (j * kFTile < L) {
+                    const int t = j * kFTile + sub * bp;
+                    const int tc = t < L ? t : L - 1;  // rows past the end: a valid page
+                    const int pg = load_page(p.block_table, p.max_pages, p.num_pages, b,
+                                             tc / p.page_size, p.err);
+                    row = pg * p.page_size + (t % p.page_size);
                 }
-                ys[sub] = __shfl_sync(0xffffffffu, cur, q & 31);
+                sm.prow[q] = row;
             }
-            if (ys[0] < 0) continue;  // the tile lies past its sequence's end
-            const int b = f / p.tiles_per_b;
+            __syncwarp();
+            // lane 0 alone issues the chunk's copies: no warp-wide step per tile
             if (lane == 0) {
-                if (b != cur_b) {
-                    const int qs = nq & 1;
-                    ok = mbar_wait(&sm.qempty[qs], ((nq >> 1) & 1) ^ 1, p.err);
-                    if (ok) {
+                TileCursor tc(c0, p.tiles_per_b);
+                for (int f = c0; f < c1 && ok; ++f, tc.next()) {
+                    const int* ys = sm.prow + (f - c0) * per_tile;
+                    if (ys[0] < 0) continue;  // the tile lies past its sequence's end
+                    const int b = tc.b;
+                    if (b != cur_b) {
+                        const int qs = nq & 1;
+                        ok = mbar_wait(&sm.qempty[qs], ((nq >> 1) & 1) ^ 1, p.err);
+                        if (!ok) break;
                         mbar_arrive_expect_tx(&sm.qfull[qs], kFQBytes);
                         tma_load_2d(sm.qbuf[qs], &tmQ, &sm.qfull[qs], 0, b * kFHi);
+                        ++nq;
+                        cur_b = b;
                     }
-                }
-                const int s = g % kFStages, ss = g % kFScaleSlots;
-                if (ok) ok = mbar_wait(&sm.empty[s], ((g / kFStages) & 1) ^ 1, p.err);
-                if (ok) ok = mbar_wait(&sm.sempty[ss], ((g / kFScaleSlots) & 1) ^ 1, p.err);
-                if (ok) {
+                    const int s = g % kFStages, ss = g % kFScaleSlots;
+                    ok = mbar_wait(&sm.empty[s], ((g / kFStages) & 1) ^ 1, p.err) &&
+                         mbar_wait(&sm.sempty[ss], ((g / kFScaleSlots) & 1) ^ 1, p.err);
+                    if (!ok) break;
                     mbar_arrive_expect_tx(&sm.full[s], kFTileBytes);
                     mbar_arrive_expect_tx(&sm.sfull[ss], kFTile * 4);
-                    // one 16 KB instruction when the pieces are contiguous (adjacent pages,
-                    // or pages of >= 128 tokens)
+                    // one 16 KB instruction when the pieces are contiguous (adjacent pages, or
+                    // pages of >= 128 tokens)
                     bool contiguous = true;
-#pragma unroll
-                    for (int sub = 1; sub < kFTile / 16; ++sub)
-                        if (sub < per_tile && ys[sub] != ys[0] + sub * bp) contiguous = false;
+                    for (int sub = 1; sub < per_tile; ++sub)
+                        if (ys[sub] != ys[0] + sub * bp) contiguous = false;
                     if (contiguous && ys[0] + kFTile <= p.num_pages * p.page_size) {
                         tma_load_2d(sm.stage[s], &tmK128, &sm.full[s], 0, ys[0]);
                         bulk_load(sm.ks[ss], p.k_scale + ys[0], kFTile * 4, &sm.sfull[ss]);
                     } else {
-#pragma unroll
-                        for (int sub = 0; sub < kFTile / 16; ++sub) {
-                            if (sub >= per_tile) break;
+                        for (int sub = 0; sub < per_tile; ++sub) {
                             tma_load_2d(sm.stage[s] + sub * bp * kFDi, &tmK, &sm.full[s], 0,
                                         ys[sub]);
                             bulk_load(sm.ks[ss] + sub * bp, p.k_scale + ys[sub], bp * 4,
                                       &sm.sfull[ss]);
                         }
                     }
+                    ++g;
                 }
             }
+            // the rows of this chunk stay until lane 0 has issued them
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (b != cur_b) {
-                ++nq;
-                cur_b = b;
-            }
-            ++g;
         }
         // copies still in flight complete before the CTA may exit
         if (lane == 0) {
@@ -204,8 +209,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
             uint32_t g = 0, nq = 0, nt = 0;
             int qs = 0;
             bool ok = true;
-            for (int f = tr.begin; f < tr.end && ok; ++f) {
-                const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
+            TileCursor tc(tr.begin, p.tiles_per_b);
+            for (int f = tr.begin; f < tr.end && ok; ++f, tc.next()) {
+                const int b = tc.b, j = tc.j;
                 if (b != cur_b) L = load_len(p.seq_lens, b, p.max_len, nullptr);
                 if (j * kFTile >= L) continue;
                 if (b != cur_b) {
@@ -243,6 +249,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         const int etid = threadIdx.x - 64;  // 0..127
         int cur_b = -1, L = 0;
         uint32_t nt = 0, nb = 0;
+        float wr[kFHi];  // w_h * sq_h of the current sequence
         auto flush_hist = [&](int b) {
             asm volatile("bar.sync 2, 128;" ::: "memory");
             for (int i = etid; i < kFHistBins; i += 128) {
@@ -254,8 +261,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
             asm volatile("bar.sync 2, 128;" ::: "memory");
         };
-        for (int f = tr.begin; f < tr.end; ++f) {
-            const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
+        TileCursor tc(tr.begin, p.tiles_per_b);
+        for (int f = tr.begin; f < tr.end; ++f, tc.next()) {
+            const int b = tc.b, j = tc.j;
             if (b != cur_b) L = load_len(p.seq_lens, b, p.max_len, nullptr);
             if (j * kFTile >= L) continue;
             if (b != cur_b) {
@@ -265,27 +273,32 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     sm.wv[nb & 1][etid] = p.w[i] * p.q_scale[i];
                 }
                 asm volatile("bar.sync 2, 128;" ::: "memory");
+#pragma unroll
+                for (int h = 0; h < kFHi; ++h) wr[h] = sm.wv[nb & 1][h];
                 ++nb;
                 cur_b = b;
             }
-            const float* wv = sm.wv[(nb - 1) & 1];
             const int acc = nt & 1, ss = nt % kFScaleSlots;
             if (!mbar_wait(&sm.tfull[acc], (nt >> 1) & 1, p.err)) break;
             if (!mbar_wait(&sm.sfull[ss], (nt / kFScaleSlots) & 1, p.err)) break;
             const float sk = sm.ks[ss][row];
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * kFHi;
-            float score = 0.f;
+            // both 32-column halves of the row in flight at once; four independent sums
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(taddr, r0);
+            tmem_ld_32x32b_x32(taddr + 32, r1);
+            tmem_ld_wait(r0);
+            tmem_ld_wait(r1);
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + half * 32, r);
-                tmem_ld_wait(r);
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    score = fmaf(wv[half * 32 + c], fmaxf(__uint_as_float(r[c]), 0.f), score);
+            for (int c = 0; c < 32; c += 2) {
+                a0 = fmaf(wr[c], fmaxf(__uint_as_float(r0[c]), 0.f), a0);
+                a1 = fmaf(wr[c + 1], fmaxf(__uint_as_float(r0[c + 1]), 0.f), a1);
+                a2 = fmaf(wr[32 + c], fmaxf(__uint_as_float(r1[c]), 0.f), a2);
+                a3 = fmaf(wr[33 + c], fmaxf(__uint_as_float(r1[c + 1]), 0.f), a3);
             }
-            score *= sk;
+            const float score = ((a0 + a1) + (a2 + a3)) * sk;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
