@@ -66,6 +66,8 @@ def _load():
         lib.oracle_quantize_e4m3_rows.argtypes = [P, l, i, P, P]
         lib.oracle_indexer_scores_fp8.restype = None
         lib.oracle_indexer_scores_fp8.argtypes = [P, P, P, P, P, P, P, i, i, i, i, P, i, l, P]
+        lib.oracle_delta_step.restype = None
+        lib.oracle_delta_step.argtypes = [P, P, P, P, P, P, i, i, i, i, P, P]
         _lib = lib
     return _lib
 
@@ -252,6 +254,25 @@ def indexer_scores_fp8(q8, q_scale, k8_pool, k_scale, w, block_table, seq_lens, 
                                       _ptr(sl), Hi, Di, P, bt.shape[1], _ptr(bl), len(bl), stride,
                                       _ptr(out))
     return out
+
+
+def delta_step(S, q, k, v, a, beta):
+    """One gated delta-rule decode step per head -> (S_new, o), both float64.
+
+    S [n, dv, dk], q and k [n, dk], v [n, dv], beta [n] (float32). a is [n, dk] (one decay
+    per key channel, KDA) or [n] (one decay per head, Gated DeltaNet).
+    """
+    f32 = lambda x: np.ascontiguousarray(np.asarray(_arr(x)[0], dtype=np.float32))
+    Sa, qa, ka, va, aa, ba = f32(S), f32(q), f32(k), f32(v), f32(a), f32(beta)
+    n, dv, dk = Sa.shape
+    per_channel = 1 if aa.ndim == 2 else 0
+    assert qa.shape == (n, dk) and ka.shape == (n, dk) and va.shape == (n, dv)
+    assert ba.shape == (n,) and (aa.shape == (n, dk) if per_channel else aa.shape == (n,))
+    S_out = np.zeros((n, dv, dk), dtype=np.float64)
+    o = np.zeros((n, dv), dtype=np.float64)
+    _load().oracle_delta_step(_ptr(Sa), _ptr(qa), _ptr(ka), _ptr(va), _ptr(aa), _ptr(ba), n, dk,
+                              dv, per_channel, _ptr(S_out), _ptr(o))
+    return S_out, o
 
 
 def topk(scores, k):

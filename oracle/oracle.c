@@ -30,6 +30,9 @@
  *    indices = the k largest scores.
  *  - "Attention Optimizations", KV cache size: bytes = S * 2 * layers *
  *    kv_heads * d_head * bytes_per_element.
+ *  - "All the attentions", sections 6 (Gated DeltaNet) and 7 (KDA); "Attention
+ *    Optimizations", KDA: one decode step of the gated delta rule per head on
+ *    a dv x dk state: fade, correction write, read.
  *
  * Conventions: seq_lens[b] counts cached tokens including the token being
  * decoded, so the query sits at position i = L_b - 1 and every cached token
@@ -332,6 +335,43 @@ void oracle_indexer_scores_fp8(const uint8_t *q8, const float *q_scale, const ui
                 total += (double)w[(size_t)b * Hi + h] * (dot > 0.0 ? dot : 0.0);
             }
             scores[(size_t)bi * out_stride + t] = total;
+        }
+    }
+}
+
+/*
+ * One decode step of the gated delta rule, for n independent heads ("All the attentions",
+ * section 6 Gated DeltaNet and section 7 KDA). Per head, with state S (dv rows x dk
+ * columns, row-major), key k and query q (dk), value v (dv), write strength beta:
+ *   fade:        S[i][j] *= a[j]   (KDA: one decay per key channel j; Gated DeltaNet: one
+ *                                   value for the whole head, a_per_channel = 0)
+ *   correction:  e[i] = v[i] - sum_j S[i][j] k[j]      (what the faded memory gets wrong)
+ *   write:       S[i][j] += beta e[i] k[j]
+ *   read:        o[i] = sum_j S[i][j] q[j]             (with the updated S)
+ * S (float32 in) is widened to double; S_out and o are double. a holds n*dk values when
+ * a_per_channel, else n.
+ */
+void oracle_delta_step(const float *S, const float *q, const float *k, const float *v,
+                       const float *a, const float *beta, int n, int dk, int dv,
+                       int a_per_channel, double *S_out, double *o) {
+#pragma omp parallel for schedule(static)
+    for (int h = 0; h < n; h++) {
+        const float *Sh = S + (size_t)h * dv * dk;
+        double *Th = S_out + (size_t)h * dv * dk;
+        const float *qh = q + (size_t)h * dk, *kh = k + (size_t)h * dk;
+        for (int i = 0; i < dv; i++) {
+            for (int j = 0; j < dk; j++) {
+                double decay = a_per_channel ? (double)a[(size_t)h * dk + j] : (double)a[h];
+                Th[(size_t)i * dk + j] = decay * (double)Sh[(size_t)i * dk + j];
+            }
+            double pred = 0.0;
+            for (int j = 0; j < dk; j++) pred += Th[(size_t)i * dk + j] * (double)kh[j];
+            double e = (double)v[(size_t)h * dv + i] - pred;
+            for (int j = 0; j < dk; j++)
+                Th[(size_t)i * dk + j] += (double)beta[h] * e * (double)kh[j];
+            double out = 0.0;
+            for (int j = 0; j < dk; j++) out += Th[(size_t)i * dk + j] * (double)qh[j];
+            o[(size_t)h * dv + i] = out;
         }
     }
 }
