@@ -415,8 +415,77 @@ class DsaFp8Runner(DsaRunner):
         return done, el, f"{n} of {xm.B} sequences (FP8 indexer, top-k and sparse MLA, all heads)"
 
 
+class DeltaRunner:
+    """delta_decode_step: one gated delta-rule (KDA) token step over every head's state."""
+    launches_per_step = 1
+    kernel = "delta_step_kernel"
+    dtype = "f32"
+    data = "synthetic: seeded float32 draws (state, unit-norm keys and queries), Kimi Linear shapes"
+
+    def __init__(self, name, dev, sharp=False):
+        import kv_cache_decode_split_gb300 as kvd
+        self.kvd = kvd
+        self.name = name
+        self.x = x = W.build(name)
+        self.dev = dev
+        self.S = x.S.to(dev)
+        self.q, self.k, self.v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+        self.a, self.beta = x.a.to(dev), x.beta.to(dev)
+        self.o = torch.empty(x.v.shape, dtype=torch.float32, device=dev)
+        self._config, self.bytes, self.flops = self.describe(name, x)
+
+    @staticmethod
+    def describe(name, x):
+        n, dv, dk = x.S.shape
+        # the state read and written once; q, k, a, v, beta read and o written per head
+        nbytes = n * (2 * dv * dk + 2 * dk + x.a[0].numel() + 2 * dv + 1) * 4
+        flops = n * dv * dk * 7.0
+        p = W.WORKLOADS[name].params
+        cfg = {"workload": name, "B": p["B"], "H": p["H"], "dk": dk, "dv": dv,
+               "gate": "per key channel" if x.a.dim() == 2 else "per head",
+               "state_bytes": n * dv * dk * 4, "kv_bytes": nbytes, "flops": flops}
+        return cfg, nbytes, flops
+
+    def step(self, q=None):
+        return self.kvd.delta_decode_step(self.S, self.q if q is None else q, self.k, self.v,
+                                          self.a, self.beta, o=self.o)
+
+    def config(self):
+        return self._config
+
+    def e2e_setup(self):
+        # the per-token inputs come from the host every step; the states stay resident
+        self.h_in = [t.pin_memory() for t in (self.x.q, self.x.k, self.x.v, self.x.a,
+                                               self.x.beta)]
+        self.d_in = [torch.empty_like(t, device=self.dev) for t in self.h_in]
+        self.h_out = torch.empty(self.o.shape, dtype=torch.float32).pin_memory()
+        return sum(t.numel() * 4 for t in self.h_in), self.h_out.numel() * 4
+
+    def e2e_step(self):
+        for d, h in zip(self.d_in, self.h_in):
+            d.copy_(h, non_blocking=True)
+        q, k, v, a, beta = self.d_in
+        self.kvd.delta_decode_step(self.S, q, k, v, a, beta, o=self.o)
+        self.h_out.copy_(self.o, non_blocking=True)
+
+    def oracle_sample(self, budget_s):
+        import oracle
+        x = self.x
+        n, dv, dk = x.S.shape
+        t0 = time.perf_counter()
+        done, heads = 0, 0
+        per_head = (2 * dv * dk + 2 * dk + x.a[0].numel() + 2 * dv + 1) * 4
+        while heads < n and time.perf_counter() - t0 < budget_s:
+            sl = slice(heads, min(n, heads + 64))
+            oracle.delta_step(x.S[sl], x.q[sl], x.k[sl], x.v[sl], x.a[sl], x.beta[sl])
+            done += (sl.stop - sl.start) * per_head
+            heads = sl.stop
+        el = time.perf_counter() - t0
+        return done, el, f"{heads} of {n} heads (one token step each)"
+
+
 RUNNERS = {"gqa": GqaRunner, "swa": GqaRunner, "mla": MlaRunner, "dsa": DsaRunner,
-           "dsa_fp8": DsaFp8Runner}
+           "dsa_fp8": DsaFp8Runner, "delta": DeltaRunner}
 
 
 def make_runner(name, dev):
@@ -566,17 +635,19 @@ def run_reference(args, rank, world):
             secs.append(el)
     v = statistics.median(vals)
     cls = RUNNERS[wl.kind]
-    xin = (x_runner.xi, x_runner.xm) if cls is DsaRunner else x_runner.x
+    xin = (x_runner.xi, x_runner.xm) if cls in (DsaRunner, DsaFp8Runner) else x_runner.x
     cfg, _, _ = cls.describe(name, xin)
     cfg = dict(cfg, l2="KV bytes larger than L2; steps back to back", parallelism="single")
     line = {"impl": "reference", "metric": "decode-attn KV GB/s", "value": v, "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic: seeded N(0,1) rounded to bf16, shapes of the named workload",
+            "data": getattr(cls, "data", "synthetic: seeded N(0,1) rounded to bf16, shapes of "
+                                         "the named workload"),
             "config": cfg,
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"per step: {desc}, about {per_step:.0f} s of CPU work"},
+                             "sample": f"per step: {desc}, {statistics.median(secs):.2f} s of CPU work "
+                                       f"(budget {per_step:.0f} s)"},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -639,8 +710,9 @@ def main():
     line = {
         "metric": "decode-attn KV GB/s", "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic: seeded N(0,1) rounded to bf16, shapes of the named workload",
+        "scaling": "weak", "vs_baseline": None, "dtype": getattr(r, "dtype", "bf16"),
+        "data": getattr(r, "data", "synthetic: seeded N(0,1) rounded to bf16, shapes of the "
+                                   "named workload"),
         "config": dict(r.config(), l2="KV bytes larger than L2; steps back to back",
                        parallelism=f"replicas{world}" if world > 1 else "single"),
         "steps_per_s": 1000.0 / ms,

@@ -277,6 +277,27 @@ int kvd_check_device_error(void *ws, cudaStream_t stream);
 /* Static, human-readable name of a status code. */
 const char *kvd_status_string(int status);
 
+/*
+ * One decode step of the gated delta rule for n independent heads ("All the attentions",
+ * section 6 Gated DeltaNet and section 7 KDA; "Attention Optimizations", KDA). Per head h,
+ * with state S_h of dv rows and dk columns (row-major, float32, device, updated in place):
+ *   fade        S[i][j] *= a[j]                (a_per_channel != 0: a [n, dk], one decay per
+ *                                               key channel (KDA); else a [n], one per head)
+ *   correction  e[i] = v[i] - sum_j S[i][j] k[j]
+ *   write       S[i][j] += beta * e[i] * k[j]
+ *   read        o[i] = sum_j S[i][j] q[j]       (the updated state)
+ *  S     [n, dv, dk] float32, 16-byte aligned (8-byte when dk == 64)
+ *  q, k  [n, dk] float32, same alignment; v [n, dv] float32; beta [n] float32
+ *  o     [n, dv] float32 output, must not overlap S
+ * q and k are used as given (any normalisation belongs to the caller). Each row's dot
+ * products are accumulated in float32. All buffers are caller-owned device memory; no
+ * workspace. Supported: dk in {64, 128, 256}, 1 <= dv <= 65536. Errors: KVD_ERR_INVALID_ARG
+ * for null or misaligned pointers or n < 1; KVD_ERR_UNSUPPORTED for other dk or dv.
+ */
+int kvd_delta_decode_step(float *S, const float *q, const float *k, const float *v,
+                          const float *a, const float *beta, float *o, int n, int dk, int dv,
+                          int a_per_channel, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,6 +13,9 @@ Operations:
   dsa_indexer_topk        indexer scores + top-k selection
   dsa_topk                top-k selection over given scores
   attn_decode_mla_sparse  MLA over the selected tokens
+  dsa_indexer_topk_fp8    the indexer on e4m3 keys and queries with row scales
+  quantize_e4m3_rows      e4m3 row quantizer; dsa_indexer_cache_append_fp8 its cache append
+  delta_decode_step       one gated delta-rule (Gated DeltaNet / KDA) decode step
 """
 from __future__ import annotations
 
@@ -29,6 +32,7 @@ lib = _lib.load()
 __all__ = [
     "attn_decode_gqa_paged", "attn_decode_swa_sink", "attn_decode_mla", "dsa_indexer_topk",
     "dsa_indexer_topk_fp8", "quantize_e4m3_rows", "dsa_indexer_cache_append_fp8",
+    "delta_decode_step",
     "dsa_topk", "attn_decode_mla_sparse", "kvd_workspace_size", "kvd_check_device_error",
     "Workspace", "KvdError",
 ]
@@ -279,6 +283,38 @@ def dsa_indexer_cache_append_fp8(k_new, block_table, seq_lens, k8_pool, k_scale,
                                           _p(err), _stream(stream))
     _check(st, "dsa_indexer_cache_append_fp8")
     return err
+
+
+def delta_decode_step(S, q, k, v, a, beta, o=None, stream=None):
+    """One gated delta-rule decode step per head, in place on S.
+
+    S [..., dv, dk] float32 (updated), q and k [..., dk], v [..., dv], beta [...] float32;
+    a is [..., dk] (one decay per key channel, KDA) or [...] (one per head, Gated DeltaNet).
+    Returns o [..., dv] float32 = S_new q.
+    """
+    _need(S, "S", torch.float32)
+    dv, dk = S.shape[-2], S.shape[-1]
+    n = S.numel() // (dv * dk)
+    for t, name, width in ((q, "q", dk), (k, "k", dk), (v, "v", dv)):
+        _need(t, name, torch.float32)
+        if t.numel() != n * width:
+            raise ValueError(f"{name} must hold {n} x {width} values")
+    _need(a, "a", torch.float32)
+    _need(beta, "beta", torch.float32)
+    if beta.numel() != n:
+        raise ValueError(f"beta must hold {n} values")
+    if a.numel() == n * dk:
+        per_channel = 1
+    elif a.numel() == n:
+        per_channel = 0
+    else:
+        raise ValueError(f"a must hold {n} x {dk} (per channel) or {n} (per head) values")
+    o = torch.empty(S.shape[:-1], dtype=torch.float32, device=S.device) if o is None else o
+    _need(o, "o", torch.float32)
+    st = lib.kvd_delta_decode_step(_p(S), _p(q), _p(k), _p(v), _p(a), _p(beta), _p(o), n, dk,
+                                   dv, per_channel, _stream(stream))
+    _check(st, "kvd_delta_decode_step")
+    return o
 
 
 def dsa_topk(scores, lens, k=2048, topk_idx=None, topk_count=None, workspace=None, stream=None):

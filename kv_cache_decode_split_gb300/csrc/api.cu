@@ -497,6 +497,39 @@ int kvd_quantize_e4m3_rows(const void* x, void* codes, float* scales, int rows, 
     return quantize_e4m3_launch(qp, stream);
 }
 
+int kvd_delta_decode_step(float* S, const float* q, const float* k, const float* v,
+                          const float* a, const float* beta, float* o, int n, int dk, int dv,
+                          int a_per_channel, cudaStream_t stream) {
+    if (!S || !q || !k || !v || !a || !beta || !o || n < 1) return KVD_ERR_INVALID_ARG;
+    if (dk != 64 && dk != 128 && dk != 256) return KVD_ERR_UNSUPPORTED;
+    if (dv < 1 || dv > 65536) return KVD_ERR_UNSUPPORTED;
+    const uintptr_t vec = dk == 64 ? 7 : 15;  // the kernel's vector width in bytes, minus 1
+    if ((reinterpret_cast<uintptr_t>(S) & vec) || (reinterpret_cast<uintptr_t>(q) & vec) ||
+        (reinterpret_cast<uintptr_t>(k) & vec) ||
+        (a_per_channel && (reinterpret_cast<uintptr_t>(a) & vec)) ||
+        (reinterpret_cast<uintptr_t>(v) & 3) || (reinterpret_cast<uintptr_t>(a) & 3) ||
+        (reinterpret_cast<uintptr_t>(beta) & 3) || (reinterpret_cast<uintptr_t>(o) & 3))
+        return KVD_ERR_INVALID_ARG;
+    // o must not overlap the state it is read from
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(S), o0 = reinterpret_cast<uintptr_t>(o);
+    const uintptr_t s1 = s0 + (uintptr_t)n * dv * dk * 4, o1 = o0 + (uintptr_t)n * dv * 4;
+    if (o0 < s1 && s0 < o1) return KVD_ERR_INVALID_ARG;
+    DeltaParams dp;
+    std::memset(&dp, 0, sizeof dp);
+    dp.S = S;
+    dp.q = q;
+    dp.k = k;
+    dp.v = v;
+    dp.a = a;
+    dp.beta = beta;
+    dp.o = o;
+    dp.n = n;
+    dp.dk = dk;
+    dp.dv = dv;
+    dp.a_per_channel = a_per_channel ? 1 : 0;
+    return delta_step_launch(dp, stream);
+}
+
 int dsa_indexer_cache_append_fp8(const void* k_new, const int32_t* block_table,
                                  const int32_t* seq_lens, void* k8_pool, float* k_scale, int B,
                                  int Di, int page_size, int max_pages, int num_pages, int* err,

@@ -118,6 +118,19 @@ int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensor
 int dsa_indexer_fp8_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensorMap& tk128,
                            const CUtensorMap& tq, cudaStream_t stream);
 int quantize_e4m3_launch(const QuantParams& p, cudaStream_t stream);
+
+// Arguments of one gated delta-rule decode step over n independent heads.
+struct DeltaParams {
+    float* S;                  // [n, dv, dk] state, updated in place
+    const float* q;            // [n, dk]
+    const float* k;            // [n, dk]
+    const float* v;            // [n, dv]
+    const float* a;            // [n, dk] (per key channel) or [n] (per head)
+    const float* beta;         // [n]
+    float* o;                  // [n, dv]
+    int n, dk, dv, a_per_channel;
+};
+int delta_step_launch(const DeltaParams& p, cudaStream_t stream);
 int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------------------

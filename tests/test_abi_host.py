@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
     names = _header_functions()
     for n in ("attn_decode_gqa_paged", "attn_decode_swa_sink", "attn_decode_mla",
               "dsa_indexer_topk", "attn_decode_mla_sparse", "dsa_topk", "kvd_workspace_size",
-              "kvd_check_device_error", "kvd_status_string"):
+              "kvd_check_device_error", "kvd_status_string", "dsa_indexer_topk_fp8",
+              "kvd_quantize_e4m3_rows", "dsa_indexer_cache_append_fp8", "kvd_delta_decode_step"):
         assert n in names
 
 
@@ -82,3 +83,19 @@ def test_workspace_size_queries(lib):
     assert lib.kvd_workspace_size(1, 8, 64, 8, 64, 32768, 4096, 4, 0) > 0
     assert lib.kvd_workspace_size(0, 2, 6, 4, 64, 256, 0, 0, 0) == 0   # Hq % Hkv != 0
     assert lib.kvd_workspace_size(99, 2, 8, 2, 64, 256, 0, 0, 0) == 0
+
+
+def test_delta_step_argument_checks(lib):
+    # rejected on the host, before any launch (the pointers are never dereferenced)
+    vp = ctypes.c_void_p
+    def call(S=1 << 20, q=2 << 20, k=3 << 20, v=4 << 20, a=5 << 20, beta=6 << 20, o=7 << 20,
+             n=4, dk=128, dv=128, per_channel=1):
+        return lib.kvd_delta_decode_step(vp(S) if S else None, vp(q), vp(k), vp(v), vp(a),
+                                         vp(beta), vp(o), n, dk, dv, per_channel, None)
+    assert call(S=0) == -1                       # null state
+    assert call(n=0) == -1
+    assert call(dk=96) == -2 and call(dk=512) == -2
+    assert call(dv=0) == -2
+    assert call(S=(1 << 20) + 4) == -1           # state not 16-byte aligned
+    assert call(a=(5 << 20) + 4) == -1           # per-channel decays not 16-byte aligned
+    assert call(o=(1 << 20) + 64) == -1          # output inside the state

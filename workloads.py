@@ -201,7 +201,7 @@ def make_indexer(B, seq_lens, *, Hi=64, Di=128, k=2048, page_size=64, max_pages=
 class Workload:
     name: str
     wid: int
-    kind: str               # "gqa" | "swa" | "mla" | "dsa"
+    kind: str               # "gqa" | "swa" | "mla" | "dsa" | "dsa_fp8" | "delta"
     params: dict = field(default_factory=dict)
     description: str = ""
 
@@ -237,6 +237,11 @@ WORKLOADS = {
         "dsa_sparse_mla", 5, "dsa",
         dict(B=4, H=128, L=131072, Hi=64, Di=128, k=2048, page_size=64, factor=0.1),
         "DSA: indexer (64 heads x 128) over L=131072, top-2048, then 128-head sparse MLA, B=4"),
+    "kda_decode": Workload(
+        "kda_decode", 7, "delta",
+        dict(B=128, H=32, dk=128, dv=128, per_channel=True),
+        "KDA decode step, Kimi Linear shapes (32 heads, 128 x 128 float32 state per head), "
+        "per-channel decay, B=128 sequences (4096 states, 268 MB)"),
     "dsa_fp8_sparse_mla": Workload(
         "dsa_fp8_sparse_mla", 6, "dsa_fp8",
         dict(B=4, H=128, L=131072, Hi=64, Di=128, k=2048, page_size=64, factor=0.1),
@@ -289,6 +294,35 @@ def make_indexer_fp8(B, seq_lens, *, Hi=64, Di=128, k=2048, page_size=64, max_pa
         base.seq_lens, page_size, int(k))
 
 
+@dataclass
+class DeltaInputs:
+    S: torch.Tensor      # [n, dv, dk] float32 state
+    q: torch.Tensor      # [n, dk] float32, unit norm times dk^-1/2
+    k: torch.Tensor      # [n, dk] float32, unit norm
+    v: torch.Tensor      # [n, dv] float32
+    a: torch.Tensor      # [n, dk] (per key channel) or [n] (per head) float32 in [0.9, 1)
+    beta: torch.Tensor   # [n] float32 in [0, 1)
+
+    @property
+    def n(self):
+        return self.S.shape[0]
+
+
+def make_delta(n, dk=128, dv=128, *, per_channel=True, seed=0, state_factor=0.1):
+    """Gated delta-rule step inputs for n heads: state N(0,1)*state_factor, keys and queries
+    scaled to unit norm (queries then by dk^-1/2), values N(0,1), decays uniform in
+    [0.9, 1), write strengths uniform in [0, 1)."""
+    S = normal((n, dv, dk), seed + 1, state_factor, torch.float32)
+    k = normal((n, dk), seed + 2, 1.0, torch.float32)
+    k = k / k.norm(dim=1, keepdim=True)
+    q = normal((n, dk), seed + 3, 1.0, torch.float32)
+    q = q / q.norm(dim=1, keepdim=True) / math.sqrt(dk)
+    v = normal((n, dv), seed + 4, 1.0, torch.float32)
+    a = uniform_f32((n, dk) if per_channel else (n,), 0.9, 1.0, seed + 5)
+    beta = uniform_f32((n,), 0.0, 1.0, seed + 6)
+    return DeltaInputs(S.contiguous(), q.contiguous(), k.contiguous(), v, a, beta)
+
+
 def build(name: str, *, sharp: bool = False):
     """Materialise a named workload on the CPU (deterministic)."""
     w = WORKLOADS[name]
@@ -306,6 +340,9 @@ def build(name: str, *, sharp: bool = False):
         return make_gqa(p["B"], p["Hq"], p["Hkv"], p["D"], [p["L"]] * p["B"],
                         page_size=p["page_size"], seed=base, window=p["window"],
                         n_sink=p["n_sink"], learned_sink=p["learned_sink"])
+    if w.kind == "delta":
+        return make_delta(p["B"] * p["H"], p["dk"], p["dv"], per_channel=p["per_channel"],
+                          seed=base)
     factor = 1.0 if sharp else p["factor"]
     if w.kind == "mla":
         return make_mla(p["B"], p["H"], [p["L"]] * p["B"], page_size=p["page_size"], seed=base,
