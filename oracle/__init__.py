@@ -52,6 +52,8 @@ def _load():
         lib.oracle_attention_flops.argtypes = [d, d, d, d]
         lib.oracle_gqa.restype = None
         lib.oracle_gqa.argtypes = [P, P, P, i, P, P, i, i, i, i, i, i, d, l, l, P, P, i, P, P]
+        lib.oracle_gqa_ring.restype = None
+        lib.oracle_gqa_ring.argtypes = lib.oracle_gqa.argtypes
         lib.oracle_mla.restype = None
         lib.oracle_mla.argtypes = [P, P, i, P, P, P, P, i, i, i, i, i, i, i, d, P, i, P, P]
         lib.oracle_indexer_scores.restype = None
@@ -66,6 +68,8 @@ def _load():
         lib.oracle_quantize_e4m3_rows.argtypes = [P, l, i, P, P]
         lib.oracle_indexer_scores_fp8.restype = None
         lib.oracle_indexer_scores_fp8.argtypes = [P, P, P, P, P, P, P, i, i, i, i, P, i, l, P]
+        lib.oracle_cache_append.restype = None
+        lib.oracle_cache_append.argtypes = [P, P, P, P, i, i, l, i, i, i, i]
         lib.oracle_delta_step.restype = None
         lib.oracle_delta_step.argtypes = [P, P, P, P, P, P, i, i, i, i, P, P]
         _lib = lib
@@ -123,13 +127,16 @@ def _pairs_arg(pairs):
 
 
 def gqa(q, k_pool, v_pool, block_table, seq_lens, scale, window=0, n_sink=0, sink_logit=None,
-        pairs=None):
+        pairs=None, ring=False):
     """GQA / MHA / MQA decode with optional sliding window, sink tokens and learned sink.
 
     Shapes: q [B,Hq,D]; k_pool, v_pool [num_pages,Hkv,P,D]; block_table [B,max_pages];
     seq_lens [B]. Returns (out, lse) in float64: out [B,Hq,D] and lse [B,Hq], or
-    [n_pairs,D] and [n_pairs] when ``pairs`` lists (b, h) pairs.
+    [n_pairs,D] and [n_pairs] when ``pairs`` lists (b, h) pairs. ``ring``: the pools are
+    rolling caches of n_sink + window slots (seq_lens the true lengths), position t read
+    from the slot cache append writes it to.
     """
+    assert not ring or window > 0
     qa, dt = _arr(q)
     ka, dtk = _arr(k_pool)
     va, dtv = _arr(v_pool)
@@ -146,9 +153,10 @@ def gqa(q, k_pool, v_pool, block_table, seq_lens, scale, window=0, n_sink=0, sin
     n = n_pairs if pa is not None else B * Hq
     out = np.zeros((n, D), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
-    _load().oracle_gqa(_ptr(qa), _ptr(ka), _ptr(va), dt, _ptr(bt), _ptr(sl), B, Hq, Hkv, D, P,
-                       bt.shape[1], float(scale), int(window), int(n_sink), _ptr(sink), _ptr(pa),
-                       n_pairs, _ptr(out), _ptr(lse))
+    fn = _load().oracle_gqa_ring if ring else _load().oracle_gqa
+    fn(_ptr(qa), _ptr(ka), _ptr(va), dt, _ptr(bt), _ptr(sl), B, Hq, Hkv, D, P, bt.shape[1],
+       float(scale), int(window), int(n_sink), _ptr(sink), _ptr(pa), n_pairs, _ptr(out),
+       _ptr(lse))
     if pa is None:
         return out.reshape(B, Hq, D), lse.reshape(B, Hq)
     return out, lse
@@ -253,6 +261,26 @@ def indexer_scores_fp8(q8, q_scale, k8_pool, k_scale, w, block_table, seq_lens, 
     _load().oracle_indexer_scores_fp8(_ptr(qa), _ptr(qs), _ptr(ka), _ptr(ks), _ptr(wa), _ptr(bt),
                                       _ptr(sl), Hi, Di, P, bt.shape[1], _ptr(bl), len(bl), stride,
                                       _ptr(out))
+    return out
+
+
+def cache_append(pool, new, block_table, seq_lens, window=0, n_sink=0):
+    """A copy of `pool` [num_pages, H, P, D] (or [num_pages, P, D]) with each sequence's
+    newest token row new[b] ([B, H, D] or [B, D]) written to its paged (window == 0) or
+    rolling (window > 0, n_sink + window slots) cache slot. Tensors in, tensor out."""
+    import torch
+    out = torch.as_tensor(pool).detach().cpu().contiguous().clone()
+    src = torch.as_tensor(new).detach().cpu().contiguous().reshape(-1).view(torch.uint8).numpy()
+    dst = out.reshape(-1).view(torch.uint8).numpy()     # shares memory with out
+    H = out.shape[1] if out.dim() == 4 else 1
+    P = out.shape[-2]
+    row_bytes = out.shape[-1] * out.element_size()
+    bt = np.ascontiguousarray(np.asarray(_arr(block_table)[0], dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(_arr(seq_lens)[0], dtype=np.int32))
+    B = sl.shape[0]
+    assert src.size == B * H * row_bytes
+    _load().oracle_cache_append(_ptr(dst), _ptr(src), _ptr(bt), _ptr(sl), B, H, row_bytes, P,
+                                bt.shape[1], int(window), int(n_sink))
     return out
 
 

@@ -30,6 +30,10 @@
  *    indices = the k largest scores.
  *  - "Attention Optimizations", KV cache size: bytes = S * 2 * layers *
  *    kv_heads * d_head * bytes_per_element.
+ *  - "All the attentions", section 4: a sliding window's cache is a rolling
+ *    buffer of W entries, the newest replacing the oldest; "Attention
+ *    Optimizations", DSA / Computation Path: the new token's row goes into the
+ *    cache before attention (update_cache).
  *  - "All the attentions", sections 6 (Gated DeltaNet) and 7 (KDA); "Attention
  *    Optimizations", KDA: one decode step of the gated delta rule per head on
  *    a dv x dk state: fade, correction write, read.
@@ -94,11 +98,18 @@ static int visible(long t, long L, long window, long n_sink) {
  * sink_logit: NULL or [Hq] (logit in the same units as scale*q.k).
  * pairs: NULL (all (b,h)) or n_pairs (b,h) pairs; out/lse are then indexed by pair.
  */
-void oracle_gqa(const void *q, const void *k_pool, const void *v_pool, int dtype,
-                const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv,
-                int D, int page_size, int max_pages, double scale, long window, long n_sink,
-                const double *sink_logit, const int32_t *pairs, int n_pairs, double *out,
-                double *lse) {
+/* Cache slot of token t: t itself in a paged cache (ring_window == 0); in a rolling cache of
+ * ring_sink + ring_window slots the sinks keep theirs and later tokens cycle through the rest. */
+static long cache_slot(long t, long ring_window, long ring_sink) {
+    if (ring_window <= 0 || t < ring_sink) return t;
+    return ring_sink + (t - ring_sink) % ring_window;
+}
+
+static void gqa_impl(const void *q, const void *k_pool, const void *v_pool, int dtype,
+                     const int32_t *block_table, const int32_t *seq_lens, int B, int Hq,
+                     int Hkv, int D, int page_size, int max_pages, double scale, long window,
+                     long n_sink, const double *sink_logit, const int32_t *pairs, int n_pairs,
+                     double *out, double *lse, long ring_window, long ring_sink) {
     int n_rep = Hq / Hkv;
     int n = pairs ? n_pairs : B * Hq;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -111,7 +122,8 @@ void oracle_gqa(const void *q, const void *k_pool, const void *v_pool, int dtype
         double m = -INFINITY;
         for (long t = 0; t < L; t++) {
             if (!visible(t, L, window, n_sink)) continue;
-            size_t row = pool_row(block_table, max_pages, page_size, Hkv, b, g, t);
+            size_t row = pool_row(block_table, max_pages, page_size, Hkv, b, g,
+                                  cache_slot(t, ring_window, ring_sink));
             double dot = 0.0;
             for (int d = 0; d < D; d++)
                 dot += widen(q, dtype, ((size_t)b * Hq + h) * D + d) *
@@ -126,7 +138,8 @@ void oracle_gqa(const void *q, const void *k_pool, const void *v_pool, int dtype
         for (int d = 0; d < D; d++) o[d] = 0.0;
         for (long t = 0; t < L; t++) {
             if (!visible(t, L, window, n_sink)) continue;
-            size_t row = pool_row(block_table, max_pages, page_size, Hkv, b, g, t);
+            size_t row = pool_row(block_table, max_pages, page_size, Hkv, b, g,
+                                  cache_slot(t, ring_window, ring_sink));
             double e = exp(s[t] - m);
             denom += e;
             for (int d = 0; d < D; d++) o[d] += e * widen(v_pool, dtype, row * D + d);
@@ -136,6 +149,31 @@ void oracle_gqa(const void *q, const void *k_pool, const void *v_pool, int dtype
         lse[p] = m + log(denom);
         free(s);
     }
+}
+
+void oracle_gqa(const void *q, const void *k_pool, const void *v_pool, int dtype,
+                const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv,
+                int D, int page_size, int max_pages, double scale, long window, long n_sink,
+                const double *sink_logit, const int32_t *pairs, int n_pairs, double *out,
+                double *lse) {
+    gqa_impl(q, k_pool, v_pool, dtype, block_table, seq_lens, B, Hq, Hkv, D, page_size,
+             max_pages, scale, window, n_sink, sink_logit, pairs, n_pairs, out, lse, 0, 0);
+}
+
+/*
+ * Sliding window + sinks read from a rolling cache: the visible positions are those of
+ * oracle_gqa with the same window and n_sink (L = seq_lens[b], the true length), and the
+ * K/V of position t are read from cache slot n_sink + (t - n_sink) mod window (t itself for
+ * a sink), where cache append put them.
+ */
+void oracle_gqa_ring(const void *q, const void *k_ring, const void *v_ring, int dtype,
+                     const int32_t *block_table, const int32_t *seq_lens, int B, int Hq,
+                     int Hkv, int D, int page_size, int max_pages, double scale, long window,
+                     long n_sink, const double *sink_logit, const int32_t *pairs, int n_pairs,
+                     double *out, double *lse) {
+    gqa_impl(q, k_ring, v_ring, dtype, block_table, seq_lens, B, Hq, Hkv, D, page_size,
+             max_pages, scale, window, n_sink, sink_logit, pairs, n_pairs, out, lse, window,
+             n_sink);
 }
 
 /*
@@ -372,6 +410,32 @@ void oracle_delta_step(const float *S, const float *q, const float *k, const flo
             double out = 0.0;
             for (int j = 0; j < dk; j++) out += Th[(size_t)i * dk + j] * (double)qh[j];
             o[(size_t)h * dv + i] = out;
+        }
+    }
+}
+
+/*
+ * Cache append: the newest token of sequence b, position t = L_b - 1, is written to logical
+ * slot r of its cache and so to physical row (block_table[b][r / P], r % P). A paged cache
+ * keeps every token (r = t). A rolling cache (window > 0) has n_sink + window slots: the
+ * first n_sink tokens keep their own slots, and every later token takes the slot of the
+ * token window positions before it (r = n_sink + (t - n_sink) mod window), so the ring
+ * always holds the sinks and the newest window tokens. Rows are copied byte for byte.
+ * pool [num_pages, H, P, row_bytes] (updated), src [B, H, row_bytes].
+ */
+void oracle_cache_append(uint8_t *pool, const uint8_t *src, const int32_t *block_table,
+                         const int32_t *seq_lens, int B, int H, long row_bytes, int page_size,
+                         int max_pages, int window, int n_sink) {
+    for (int b = 0; b < B; b++) {
+        long t = (long)seq_lens[b] - 1;
+        long r = t;
+        if (window > 0 && t >= n_sink) r = n_sink + (t - n_sink) % window;
+        long page = block_table[(size_t)b * max_pages + r / page_size];
+        long slot = r % page_size;
+        for (int h = 0; h < H; h++) {
+            uint8_t *dst = pool + (((size_t)page * H + h) * page_size + slot) * row_bytes;
+            const uint8_t *from = src + ((size_t)b * H + h) * row_bytes;
+            for (long i = 0; i < row_bytes; i++) dst[i] = from[i];
         }
     }
 }

@@ -88,6 +88,7 @@ class GQAInputs:
     window: int = 0            # 0: no window (dense)
     n_sink: int = 0            # sink tokens always kept
     sink_logit: torch.Tensor | None = None  # [Hq] float32, learned sink logit
+    ring: bool = False         # pools are rolling caches of n_sink + window slots
 
     @property
     def B(self): return self.q.shape[0]
@@ -118,6 +119,24 @@ def make_gqa(B, Hq, Hkv, D, seq_lens, *, page_size=64, max_pages=None, dtype=tor
     return GQAInputs(q, k, v, bt, lens, page_size,
                      float(scale if scale is not None else 1.0 / math.sqrt(D)),
                      int(window), int(n_sink), sink)
+
+
+def make_ring(B, Hq, Hkv, D, seq_lens, window, *, n_sink=0, page_size=64, dtype=torch.bfloat16,
+              shuffle=True, extra_pages=0, seed=0, factor=1.0, learned_sink=False) -> GQAInputs:
+    """Sliding-window inputs on rolling caches: every sequence owns n_sink + window slots
+    (all its pages allocated up front), filled with normals; seq_lens are the true lengths
+    and may exceed the capacity."""
+    cap = n_sink + window
+    max_pages = -(-cap // page_size)
+    bt, num_pages = block_table_for([cap] * B, page_size, max_pages, shuffle, seed + 3,
+                                    extra_pages)
+    lens = torch.as_tensor(seq_lens, dtype=torch.int32).reshape(B)
+    q = normal((B, Hq, D), seed + 0, factor, dtype)
+    k = normal((num_pages, Hkv, page_size, D), seed + 1, factor, dtype)
+    v = normal((num_pages, Hkv, page_size, D), seed + 2, factor, dtype)
+    sink = normal((Hq,), seed + 4, 1.0, torch.float32) if learned_sink else None
+    return GQAInputs(q, k, v, bt, lens, page_size, 1.0 / math.sqrt(D), int(window), int(n_sink),
+                     sink, ring=True)
 
 
 @dataclass
@@ -228,6 +247,12 @@ WORKLOADS = {
              page_size=64),
         "sliding window W=4096 with a learned per-head sink logit ~ N(0,1), bf16, "
         "B=8 Hq=64 Hkv=8 D=64 L=32768"),
+    "swa_ring_sink_tokens": Workload(
+        "swa_ring_sink_tokens", 8, "swa",
+        dict(B=8, Hq=64, Hkv=8, D=64, L=32768, window=4096, n_sink=4, learned_sink=False,
+             page_size=64, ring=True),
+        "sliding window W=4096 plus the first 4 tokens on rolling caches of 4100 slots "
+        "(O(W) memory), bf16, B=8 Hq=64 Hkv=8 D=64, true length 32768"),
     "mla_dsv3": Workload(
         "mla_dsv3", 4, "mla",
         dict(B=16, H=128, L=16384, page_size=64, factor=0.1),
@@ -336,6 +361,10 @@ def build(name: str, *, sharp: bool = False):
         return make_gqa(p["B"], p["Hq"], p["Hkv"], p["D"], lens, page_size=p["page_size"],
                         max_pages=p["max_pages"], shuffle=p["shuffle"],
                         extra_pages=p["extra_pages"], seed=base)
+    if w.kind == "swa" and p.get("ring"):
+        return make_ring(p["B"], p["Hq"], p["Hkv"], p["D"], [p["L"]] * p["B"], p["window"],
+                         n_sink=p["n_sink"], page_size=p["page_size"], seed=base,
+                         learned_sink=p["learned_sink"])
     if w.kind == "swa":
         return make_gqa(p["B"], p["Hq"], p["Hkv"], p["D"], [p["L"]] * p["B"],
                         page_size=p["page_size"], seed=base, window=p["window"],
