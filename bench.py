@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129e6                   # GB300 L2
 HEADLINE = "llama3_8b_gqa_paged"
 
 
@@ -77,7 +78,8 @@ def measured_peaks():
 # Workload runners (device side)
 # ---------------------------------------------------------------------------------------
 class GqaRunner:
-    """attn_decode_gqa_paged / attn_decode_swa_sink on a named workload."""
+    """attn_decode_gqa_paged / attn_decode_swa_sink on a named workload; on rolling caches,
+    cache_append of the step's new token then attn_decode_swa_ring."""
     launches_per_step = 1          # split-KV kernel; its last CTA per group combines
     kernel = "gqa_decode_bf16_kernel"
 
@@ -96,6 +98,15 @@ class GqaRunner:
         self.out = torch.empty_like(self.q)
         self.ws = kvd.Workspace(dev)
         self.swa = x.window > 0 or x.n_sink > 0 or x.sink_logit is not None
+        self.ring = x.ring
+        if self.ring:
+            # the step's new token (K and V rows of every sequence), appended before attention
+            wid = W.WORKLOADS[name].wid
+            self.h_knew = W.normal((x.B, x.Hkv, x.D), 1000 * wid + 20, 1.0, x.q.dtype)
+            self.h_vnew = W.normal((x.B, x.Hkv, x.D), 1000 * wid + 21, 1.0, x.q.dtype)
+            self.knew, self.vnew = self.h_knew.to(dev), self.h_vnew.to(dev)
+            self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+            self.launches_per_step = 2
         self._config, self.bytes, self.flops = self.describe(name, x)
 
     @staticmethod
@@ -109,17 +120,28 @@ class GqaRunner:
             else:
                 tok += L
         nbytes = tok * x.Hkv * x.D * 2 * x.q.element_size()   # K and V rows the method reads
+        if x.ring:   # plus the new token's K and V rows, read once and written once
+            nbytes += 2 * 2 * x.B * x.Hkv * x.D * x.q.element_size()
         flops = 4.0 * tok * x.Hkv * (x.Hq // x.Hkv) * x.D
         cfg = {"workload": name, "B": x.B, "Hq": x.Hq, "Hkv": x.Hkv, "D": x.D,
                "page_size": x.page_size, "window": x.window, "n_sink": x.n_sink,
                "learned_sink": x.sink_logit is not None,
                "seq_len_mean": float(x.seq_lens.float().mean()), "kv_bytes": nbytes}
+        if x.ring:
+            cfg["cache"] = f"rolling, {x.n_sink + x.window} slots per sequence"
+            cfg["step"] = "cache_append of the new token, then attention"
         return cfg, nbytes, flops
 
     def step(self, q=None, out=None):
         x = self.x
         q = self.q if q is None else q
         out = self.out if out is None else out
+        if self.ring:
+            self.kvd.cache_append(self.knew, self.vnew, self.k, self.v, self.bt, self.sl,
+                                  window=x.window, n_sink=x.n_sink, err=self.err)
+            return self.kvd.attn_decode_swa_ring(q, self.k, self.v, self.bt, self.sl, x.window,
+                                                 x.n_sink, self.sink, scale=x.scale, out=out,
+                                                 workspace=self.ws)
         if self.swa:
             return self.kvd.attn_decode_swa_sink(q, self.k, self.v, self.bt, self.sl, x.window,
                                                  x.n_sink, self.sink, scale=x.scale, out=out,
@@ -137,10 +159,17 @@ class GqaRunner:
         self.h_sl = self.x.seq_lens.pin_memory()
         self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
         self.d_q = torch.empty_like(self.q)
-        return (self.h_q.numel() * self.h_q.element_size() + self.h_bt.numel() * 4 +
-                self.h_sl.numel() * 4), self.h_out.numel() * self.h_out.element_size()
+        h2d = (self.h_q.numel() * self.h_q.element_size() + self.h_bt.numel() * 4 +
+               self.h_sl.numel() * 4)
+        if self.ring:
+            self.h_knew, self.h_vnew = self.h_knew.pin_memory(), self.h_vnew.pin_memory()
+            h2d += 2 * self.h_knew.numel() * self.h_knew.element_size()
+        return h2d, self.h_out.numel() * self.h_out.element_size()
 
     def e2e_step(self):
+        if self.ring:
+            self.knew.copy_(self.h_knew, non_blocking=True)
+            self.vnew.copy_(self.h_vnew, non_blocking=True)
         self.d_q.copy_(self.h_q, non_blocking=True)
         self.bt.copy_(self.h_bt, non_blocking=True)
         self.sl.copy_(self.h_sl, non_blocking=True)
@@ -162,7 +191,7 @@ class GqaRunner:
         for b, g in units:
             pairs = [(b, g * G + j) for j in range(G)]
             oracle.gqa(x.q, x.k_pool, x.v_pool, x.block_table, x.seq_lens, x.scale, x.window,
-                       x.n_sink, x.sink_logit, pairs=pairs)
+                       x.n_sink, x.sink_logit, pairs=pairs, ring=x.ring)
             L = lens[b]
             if self.swa:
                 vis = len(set(range(min(x.n_sink, L))) | set(range(max(0, L - x.window), L)))
@@ -685,9 +714,17 @@ def main():
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
+    # a workload whose data fit in L2 is timed one step at a time between L2 flushes (flush
+    # excluded); larger ones back to back
+    small = r.bytes < L2_BYTES
+    flush_main = torch.zeros(128 << 20, dtype=torch.float32, device=dev) if small else None
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
-        total_ms, per = time_steps(r.step, args.steps, stream)
+        if small:
+            per = time_flushed(r.step, args.steps, stream, lambda: flush_l2(flush_main))
+            total_ms = sum(per)
+        else:
+            total_ms, per = time_steps(r.step, args.steps, stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -713,7 +750,9 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": getattr(r, "dtype", "bf16"),
         "data": getattr(r, "data", "synthetic: seeded N(0,1) rounded to bf16, shapes of the "
                                    "named workload"),
-        "config": dict(r.config(), l2="KV bytes larger than L2; steps back to back",
+        "config": dict(r.config(), l2=("flushed before each step (512 MB read), flush "
+                                       "excluded" if small else
+                                       "KV bytes larger than L2; steps back to back"),
                        parallelism=f"replicas{world}" if world > 1 else "single"),
         "steps_per_s": 1000.0 / ms,
         "frac_of_nominal_8tbs": value / world / NOMINAL_HBM_GBS,

@@ -27,6 +27,17 @@
  *  - attn_decode_mla_sparse: MLA over only the selected tokens.
  *    "Attention Optimizations", DSA / Computation Path (gather of the
  *    selected cache rows, then attention).
+ *  - dsa_indexer_topk_fp8, kvd_quantize_e4m3_rows, dsa_indexer_cache_append_fp8:
+ *    the indexer on e4m3 codes with row scales and the quantizer that fills its
+ *    cache. "Long context, KV eviction and sparse attention", exact selection
+ *    with a fast scorer (the indexer runs in FP8).
+ *  - kvd_cache_append, attn_decode_swa_ring: the new token's K/V (or latent
+ *    row) written into a paged or rolling cache, and sliding-window attention
+ *    read from the rolling cache. "Attention Optimizations", DSA / Computation
+ *    Path (update_cache before attention) and Sliding-window (a rolling buffer
+ *    of W entries); "All the attentions", section 4.
+ *  - kvd_delta_decode_step: one Gated DeltaNet / KDA decode step on each head's
+ *    fixed-size state. "All the attentions", sections 6 and 7.
  *
  * Common conventions
  *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
@@ -157,6 +168,49 @@ int attn_decode_swa_sink(const void *q, const void *k_pool, const void *v_pool,
                          int max_pages, int num_pages, float scale, int dtype, int window,
                          int n_sink_tokens, const float *sink_logit, void *ws, size_t ws_bytes,
                          cudaStream_t stream);
+
+/*
+ * Sliding-window + sink decode over a ROLLING cache ("All the attentions", section 4: the
+ * window's cache is a buffer of W entries, each new entry replacing the oldest; "Attention
+ * Optimizations", Sliding-window: Mistral's rolling buffer, O(W) cache). Sequence b's cache
+ * has n_sink_tokens + window slots (logical positions of its block table): the first
+ * n_sink_tokens hold the sink tokens, and token t >= n_sink_tokens lives in slot
+ * n_sink_tokens + (t - n_sink_tokens) mod window (as kvd_cache_append writes it). seq_lens
+ * holds the TRUE sequence lengths L_b (tokens decoded so far, >= 1, unbounded); the visible
+ * set is every filled slot, the first min(L_b, n_sink_tokens + window), which is exactly
+ * the set attn_decode_swa_sink sees on a full cache. sink_logit as attn_decode_swa_sink.
+ * Requires window >= 1, n_sink_tokens >= 0 and n_sink_tokens + window <= max_pages *
+ * page_size; other arguments, workspace (as KVD_OP_GQA with max_len = max_pages *
+ * page_size) and errors as attn_decode_gqa_paged.
+ */
+int attn_decode_swa_ring(const void *q, const void *k_ring, const void *v_ring,
+                         const int32_t *block_table, const int32_t *seq_lens, void *out,
+                         float *lse_out, int B, int Hq, int Hkv, int D, int page_size,
+                         int max_pages, int num_pages, float scale, int dtype, int window,
+                         int n_sink_tokens, const float *sink_logit, void *ws, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/*
+ * Cache append ("Attention Optimizations", DSA / Computation Path: the new token's cache
+ * row is written before attention runs): for each sequence b, the rows of its newest token,
+ * position t = seq_lens[b] - 1, are copied into the cache slot
+ *   r = t                                      (window == 0: paged cache), or
+ *   r = t if t < n_sink, else n_sink + (t - n_sink) mod window   (window > 0: rolling cache)
+ * at page block_table[b][r / page_size], offset r % page_size.
+ *  k_new, v_new  [B, H, D] (dtype KVD_F32 or KVD_BF16), device; v_new and v_pool both null
+ *                for a single pool (the MLA latent cache: H = 1, D = 576)
+ *  k_pool, v_pool [num_pages, H, page_size, D], device, updated in place
+ *  err           int32 on the device: set to KVD_ERR_DEVICE_OOB when a length or page id is
+ *                out of range (that sequence's rows are then not written); never cleared
+ * Bytes are copied unchanged. Requires D * element size a multiple of 16 (and at most
+ * 1 MiB), 16-byte aligned rows, and for a rolling cache n_sink + window <= max_pages *
+ * page_size; a paged cache needs 1 <= L_b <= max_pages * page_size. Host-side errors:
+ * KVD_ERR_INVALID_ARG, KVD_ERR_UNSUPPORTED. No workspace.
+ */
+int kvd_cache_append(const void *k_new, const void *v_new, void *k_pool, void *v_pool,
+                     const int32_t *block_table, const int32_t *seq_lens, int B, int H, int D,
+                     int page_size, int max_pages, int num_pages, int dtype, int window,
+                     int n_sink, int *err, cudaStream_t stream);
 
 /*
  * Absorbed MLA decode over all cached tokens.

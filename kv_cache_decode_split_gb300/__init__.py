@@ -16,6 +16,8 @@ Operations:
   dsa_indexer_topk_fp8    the indexer on e4m3 keys and queries with row scales
   quantize_e4m3_rows      e4m3 row quantizer; dsa_indexer_cache_append_fp8 its cache append
   delta_decode_step       one gated delta-rule (Gated DeltaNet / KDA) decode step
+  cache_append            the new token's K/V (or latent row) into a paged or rolling cache
+  attn_decode_swa_ring    sliding window + sinks over a rolling cache
 """
 from __future__ import annotations
 
@@ -32,7 +34,7 @@ lib = _lib.load()
 __all__ = [
     "attn_decode_gqa_paged", "attn_decode_swa_sink", "attn_decode_mla", "dsa_indexer_topk",
     "dsa_indexer_topk_fp8", "quantize_e4m3_rows", "dsa_indexer_cache_append_fp8",
-    "delta_decode_step",
+    "delta_decode_step", "attn_decode_swa_ring", "cache_append",
     "dsa_topk", "attn_decode_mla_sparse", "kvd_workspace_size", "kvd_check_device_error",
     "Workspace", "KvdError",
 ]
@@ -174,6 +176,69 @@ def attn_decode_swa_sink(q, k_pool, v_pool, block_table, seq_lens, window, n_sin
                                   _p(sink_logit), _p(ws), ws.numel(), _stream(stream))
     _check(st, "attn_decode_swa_sink")
     return out
+
+
+def attn_decode_swa_ring(q, k_ring, v_ring, block_table, seq_lens, window, n_sink_tokens=0,
+                         sink_logit=None, scale=None, out=None, lse_out=None, workspace=None,
+                         stream=None):
+    """Sliding-window (+ sinks) decode over a rolling cache of n_sink_tokens + window slots
+    per sequence (written by cache_append with the same window); seq_lens are the true
+    sequence lengths."""
+    B, Hq, Hkv, D, P, max_pages, num_pages = _gqa_args(q, k_ring, v_ring, block_table, seq_lens)
+    if sink_logit is not None:
+        _need(sink_logit, "sink_logit", torch.float32, 1)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    # the ring is read like a dense cache of max_pages * P slots
+    nbytes = kvd_workspace_size("gqa", B, Hq, Hkv, D, max_pages * P)
+    ws = _ws(workspace, nbytes, q.device, "gqa", layout=("gqa", B, Hq, Hkv, D, max_pages * P))
+    st = lib.attn_decode_swa_ring(_p(q), _p(k_ring), _p(v_ring), _p(block_table), _p(seq_lens),
+                                  _p(out), _p(lse_out), B, Hq, Hkv, D, P, max_pages, num_pages,
+                                  scale, _DT[q.dtype], int(window), int(n_sink_tokens),
+                                  _p(sink_logit), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "attn_decode_swa_ring")
+    return out
+
+
+def cache_append(k_new, v_new, k_pool, v_pool, block_table, seq_lens, window=0, n_sink=0,
+                 err=None, stream=None):
+    """Write each sequence's newest token (position seq_lens[b] - 1) into its cache slot.
+
+    k_new / v_new [B, H, D] into k_pool / v_pool [num_pages, H, page_size, D]; for the MLA
+    latent cache pass v_new = v_pool = None, k_new [B, 576] and k_pool [num_pages, P, 576].
+    window > 0: a rolling cache of n_sink + window slots. `err` (int32 [1], device) receives
+    a device error code and is returned.
+    """
+    _need(k_new, "k_new")
+    _need(k_pool, "k_pool", k_new.dtype)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    if k_new.dtype not in _DT:
+        raise TypeError("k_new must be float32 or bfloat16")
+    if (v_new is None) != (v_pool is None):
+        raise ValueError("v_new and v_pool go together")
+    if v_new is not None:
+        _need(v_new, "v_new", k_new.dtype)
+        _need(v_pool, "v_pool", k_new.dtype)
+        if v_new.shape != k_new.shape or v_pool.shape != k_pool.shape:
+            raise ValueError("v_new / v_pool must match k_new / k_pool")
+    B, D = k_new.shape[0], k_new.shape[-1]
+    if k_pool.dim() == 4:
+        num_pages, H, P, D2 = k_pool.shape
+    elif k_pool.dim() == 3:
+        (num_pages, P, D2), H = k_pool.shape, 1
+    else:
+        raise ValueError("k_pool must be [num_pages, H, P, D] or [num_pages, P, D]")
+    if D2 != D or k_new.numel() != B * H * D:
+        raise ValueError("k_new must be [B, H, D] matching the pool")
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=k_new.device)
+    st = lib.kvd_cache_append(_p(k_new), _p(v_new), _p(k_pool), _p(v_pool), _p(block_table),
+                              _p(seq_lens), B, H, D, P, block_table.shape[1], num_pages,
+                              _DT[k_new.dtype], int(window), int(n_sink), _p(err),
+                              _stream(stream))
+    _check(st, "kvd_cache_append")
+    return err
 
 
 def _mla_args(q, c_pool, block_table, seq_lens):

@@ -277,8 +277,10 @@ int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t
                const int32_t* seq_lens, void* out, float* lse_out, int B, int Hq, int Hkv, int D,
                int page_size, int max_pages, int num_pages, float scale, int dtype, int window,
                int n_sink, const float* sink_logit, void* ws, size_t ws_bytes,
-               cudaStream_t stream) {
+               cudaStream_t stream, int ring) {
     if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out || !ws)
+        return KVD_ERR_INVALID_ARG;
+    if (ring < 0 || (ring > 0 && (window != 0 || n_sink != 0 || ring > max_pages * page_size)))
         return KVD_ERR_INVALID_ARG;
     if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_pages < 1 || num_pages < 1)
         return KVD_ERR_INVALID_ARG;
@@ -326,6 +328,7 @@ int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t
     p.max_len = max_len;
     p.window = window;
     p.n_sink = n_sink;
+    p.ring = ring;
     p.chunk = plan.chunk;
     p.max_chunks = plan.max_chunks;
     p.dtype = dtype;
@@ -366,6 +369,59 @@ int attn_decode_swa_sink(const void* q, const void* k_pool, const void* v_pool,
     return gqa_run(q, k_pool, v_pool, block_table, seq_lens, out, lse_out, B, Hq, Hkv, D,
                       page_size, max_pages, num_pages, scale, dtype, window, n_sink_tokens,
                       sink_logit, ws, ws_bytes, stream);
+}
+
+int attn_decode_swa_ring(const void* q, const void* k_ring, const void* v_ring,
+                         const int32_t* block_table, const int32_t* seq_lens, void* out,
+                         float* lse_out, int B, int Hq, int Hkv, int D, int page_size,
+                         int max_pages, int num_pages, float scale, int dtype, int window,
+                         int n_sink_tokens, const float* sink_logit, void* ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+    if (window < 1 || n_sink_tokens < 0) return KVD_ERR_INVALID_ARG;
+    const long long cap = (long long)n_sink_tokens + window;
+    if (cap > (long long)max_pages * page_size) return KVD_ERR_INVALID_ARG;
+    return gqa_run(q, k_ring, v_ring, block_table, seq_lens, out, lse_out, B, Hq, Hkv, D,
+                   page_size, max_pages, num_pages, scale, dtype, 0, 0, sink_logit, ws, ws_bytes,
+                   stream, static_cast<int>(cap));
+}
+
+int kvd_cache_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                     const int32_t* block_table, const int32_t* seq_lens, int B, int H, int D,
+                     int page_size, int max_pages, int num_pages, int dtype, int window,
+                     int n_sink, int* err, cudaStream_t stream) {
+    if (!k_new || !k_pool || !block_table || !seq_lens || !err) return KVD_ERR_INVALID_ARG;
+    if (!v_new != !v_pool) return KVD_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || D < 1 || page_size < 1 || max_pages < 1 || num_pages < 1 ||
+        window < 0 || n_sink < 0)
+        return KVD_ERR_INVALID_ARG;
+    if (dtype != KVD_F32 && dtype != KVD_BF16) return KVD_ERR_UNSUPPORTED;
+    const long long row_bytes = (long long)D * (dtype == KVD_F32 ? 4 : 2);
+    if (row_bytes % 16 != 0 || row_bytes > (1 << 20)) return KVD_ERR_UNSUPPORTED;
+    if ((long long)max_pages * page_size >= (1LL << 30)) return KVD_ERR_UNSUPPORTED;
+    if (window > 0 && (long long)n_sink + window > (long long)max_pages * page_size)
+        return KVD_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(k_pool) || (v_new && !aligned16(v_new)) ||
+        (v_pool && !aligned16(v_pool)) || (reinterpret_cast<uintptr_t>(err) & 3))
+        return KVD_ERR_INVALID_ARG;
+    AppendParams ap;
+    std::memset(&ap, 0, sizeof ap);
+    ap.src[0] = k_new;
+    ap.pool[0] = k_pool;
+    ap.src[1] = v_new;
+    ap.pool[1] = v_pool;
+    ap.n_pools = v_new ? 2 : 1;
+    ap.block_table = block_table;
+    ap.seq_lens = seq_lens;
+    ap.err = err;
+    ap.B = B;
+    ap.H = H;
+    ap.row_bytes = static_cast<int>(row_bytes);
+    ap.page_size = page_size;
+    ap.max_pages = max_pages;
+    ap.num_pages = num_pages;
+    ap.window = window;
+    ap.n_sink = n_sink;
+    return append_launch(ap, stream);
 }
 
 int attn_decode_mla(const void* q, const void* c_pool, const int32_t* block_table,

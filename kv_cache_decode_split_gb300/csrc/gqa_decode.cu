@@ -6,7 +6,10 @@
 //   o_h = sum_{t in V} e^{s_t} v_{g(h),t} / (sum_{t in V} e^{s_t} + [sink] e^{sigma_h}),
 //   s_t = scale * q_h . k_{g(h),t},  g(h) = h / (Hq / Hkv),
 // with V the visible set of the query at position L-1 (all tokens, or the window of W
-// tokens ending at the query plus the first n_sink tokens).
+// tokens ending at the query plus the first n_sink tokens). On a rolling cache ("All the
+// attentions", section 4: the window's cache is a buffer of W entries, the newest replacing
+// the oldest; sinks in their own first slots) every filled slot is visible: the first
+// min(L, n_sink + W) slots, in whatever order the ring holds them.
 //
 // How (GB300), bf16: one CTA per (sequence, group of HPT KV heads, block of <= 16 query
 // heads per KV head, chunk of the visible range), two CTAs per SM. A producer warp streams
@@ -38,6 +41,18 @@ constexpr int kConsumers = 4;    // consumer warps, 16 tokens of each tile each
 constexpr int kMaxHP = 16;       // query heads per KV head handled by one CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+
+// Tokens the query sees through the cache: L (paged cache; checked against its capacity) or,
+// on a rolling cache of p.ring slots, the filled slots min(L, ring) (L itself unbounded).
+__device__ __forceinline__ int visible_len(const GqaParams& p, int b) {
+    if (p.ring <= 0) return load_len(p.seq_lens, b, p.max_len, p.err);
+    int L = p.seq_lens[b];
+    if (L < 1) {
+        record_error(p.err, KVD_ERR_DEVICE_OOB);
+        L = 1;
+    }
+    return min(L, p.ring);
+}
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
 
@@ -285,7 +300,7 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
     const int kvg = blockIdx.y % n_kvg;
     const int hg = blockIdx.y / n_kvg;
     const int b = blockIdx.z;
-    const int L = load_len(p.seq_lens, b, p.max_len, p.err);
+    const int L = visible_len(p, b);
     const Ranges R = visible_ranges(L, p.window, p.n_sink);
     int lo, hi;
     if (!chunk_bounds(R, p.chunk, c, lo, hi)) return;
@@ -551,7 +566,7 @@ __global__ void __launch_bounds__(kConsumers * 32) gqa_decode_f32_kernel(const G
     const int kvh = blockIdx.y % p.Hkv;
     const int hg = blockIdx.y / p.Hkv;
     const int b = blockIdx.z;
-    const int L = load_len(p.seq_lens, b, p.max_len, p.err);
+    const int L = visible_len(p, b);
     const Ranges R = visible_ranges(L, p.window, p.n_sink);
     int lo, hi;
     if (!chunk_bounds(R, p.chunk, c, lo, hi)) return;

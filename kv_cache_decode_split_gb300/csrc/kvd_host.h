@@ -32,6 +32,7 @@ struct GqaParams {
     int B, Hq, Hkv, D, G, NHG, units;
     int page_size, max_pages, num_pages, max_len;
     int window, n_sink;  // window <= 0: dense
+    int ring;            // > 0: a rolling cache of this many slots; visible = min(L, ring)
     int chunk, max_chunks;
     int dtype;
     float scale_log2;  // scale * log2(e)
@@ -56,7 +57,8 @@ int gqa_launch(const GqaPlan& plan, const GqaParams& p, const CUtensorMap* tk,
 int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
             const int32_t* seq_lens, void* out, float* lse_out, int B, int Hq, int Hkv, int D,
             int page_size, int max_pages, int num_pages, float scale, int dtype, int window,
-            int n_sink, const float* sink_logit, void* ws, size_t ws_bytes, cudaStream_t stream);
+            int n_sink, const float* sink_logit, void* ws, size_t ws_bytes, cudaStream_t stream,
+            int ring = 0);
 
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix with a {64, box_rows} box and
 // 128-byte swizzle (cols a multiple of 64). Returns KVD_OK or KVD_ERR_CUDA.
@@ -131,6 +133,19 @@ struct DeltaParams {
     int n, dk, dv, a_per_channel;
 };
 int delta_step_launch(const DeltaParams& p, cudaStream_t stream);
+
+// Arguments of the cache append: each sequence's newest token (position seq_lens[b] - 1)
+// copied into its cache slot, for n_pools pools (K and V, or one latent pool).
+struct AppendParams {
+    const void* src[2];        // [B, H, row_bytes] each
+    void* pool[2];             // [num_pages, H, page_size, row_bytes] each
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    int* err;
+    int n_pools, B, H, row_bytes, page_size, max_pages, num_pages;
+    int window, n_sink;        // window > 0: rolling cache of n_sink + window slots
+};
+int append_launch(const AppendParams& p, cudaStream_t stream);
 int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------------------
