@@ -68,6 +68,10 @@ def _load():
         lib.oracle_quantize_e4m3_rows.argtypes = [P, l, i, P, P]
         lib.oracle_indexer_scores_fp8.restype = None
         lib.oracle_indexer_scores_fp8.argtypes = [P, P, P, P, P, P, P, i, i, i, i, P, i, l, P]
+        lib.oracle_quest_minmax.restype = None
+        lib.oracle_quest_minmax.argtypes = [P, i, P, i, i, i, i, P, P]
+        lib.oracle_quest.restype = None
+        lib.oracle_quest.argtypes = [P, P, P, i, P, P, i, i, i, i, i, i, d, i, P, i, P, P, P, P]
         lib.oracle_cache_append.restype = None
         lib.oracle_cache_append.argtypes = [P, P, P, P, i, i, l, i, i, i, i]
         lib.oracle_delta_step.restype = None
@@ -262,6 +266,46 @@ def indexer_scores_fp8(q8, q_scale, k8_pool, k_scale, w, block_table, seq_lens, 
                                       _ptr(sl), Hi, Di, P, bt.shape[1], _ptr(bl), len(bl), stride,
                                       _ptr(out))
     return out
+
+
+def quest_minmax(k_pool, pages=None):
+    """Elementwise (min, max) over each page's keys: k_pool [num_pages, Hkv, P, D] ->
+    two float64 arrays [n, Hkv, D] for the listed physical pages (all by default)."""
+    ka, dt = _arr(k_pool)
+    num_pages, Hkv, P, D = ka.shape
+    pl = np.arange(num_pages, dtype=np.int32) if pages is None else \
+        np.ascontiguousarray(np.asarray(pages, dtype=np.int32))
+    kmin = np.zeros((len(pl), Hkv, D)); kmax = np.zeros((len(pl), Hkv, D))
+    _load().oracle_quest_minmax(_ptr(ka), dt, _ptr(pl), len(pl), Hkv, P, D, _ptr(kmin),
+                                _ptr(kmax))
+    return kmin, kmax
+
+
+def quest(q, k_pool, v_pool, block_table, seq_lens, scale, n_sel, pairs=None):
+    """Quest decode per query head: page bounds, the n_sel best full pages plus the tail,
+    attention over them. Returns (out, lse, sel, ub) in float64 / int32:
+    out [B,Hq,D], lse [B,Hq], sel [B,Hq,n_sel] (ascending logical pages, -1 padded),
+    ub [B,Hq,max_pages] (NaN past the full pages); flattened over ``pairs`` when given."""
+    qa, dt = _arr(q)
+    ka, dtk = _arr(k_pool)
+    va, dtv = _arr(v_pool)
+    assert dt in (0, 1) and dt == dtk == dtv
+    bt = np.ascontiguousarray(np.asarray(_arr(block_table)[0], dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(_arr(seq_lens)[0], dtype=np.int32))
+    B, Hq, D = qa.shape
+    _, Hkv, P, _ = ka.shape
+    pa, n_pairs = _pairs_arg(pairs)
+    n = n_pairs if pa is not None else B * Hq
+    mp = bt.shape[1]
+    out = np.zeros((n, D)); lse = np.zeros((n,))
+    sel = np.zeros((n, n_sel), dtype=np.int32); ub = np.zeros((n, mp))
+    _load().oracle_quest(_ptr(qa), _ptr(ka), _ptr(va), dt, _ptr(bt), _ptr(sl), B, Hq, Hkv, D, P,
+                         mp, float(scale), int(n_sel), _ptr(pa), n_pairs, _ptr(out), _ptr(lse),
+                         _ptr(sel), _ptr(ub))
+    if pa is None:
+        return (out.reshape(B, Hq, D), lse.reshape(B, Hq), sel.reshape(B, Hq, n_sel),
+                ub.reshape(B, Hq, mp))
+    return out, lse, sel, ub
 
 
 def cache_append(pool, new, block_table, seq_lens, window=0, n_sink=0):

@@ -34,6 +34,11 @@
  *    buffer of W entries, the newest replacing the oldest; "Attention
  *    Optimizations", DSA / Computation Path: the new token's row goes into the
  *    cache before attention (update_cache).
+ *  - "Long context, KV eviction and sparse attention", Sparse attention (Quest):
+ *    per page of keys the elementwise minimum and maximum; the upper bound of
+ *    a query's scores in a page is sum_d max(q_d kmin_d, q_d kmax_d); each
+ *    query head attends over the pages with the largest bounds plus the
+ *    trailing partial page.
  *  - "All the attentions", sections 6 (Gated DeltaNet) and 7 (KDA); "Attention
  *    Optimizations", KDA: one decode step of the gated delta rule per head on
  *    a dv x dk state: fade, correction write, read.
@@ -437,5 +442,117 @@ void oracle_cache_append(uint8_t *pool, const uint8_t *src, const int32_t *block
             const uint8_t *from = src + ((size_t)b * H + h) * row_bytes;
             for (long i = 0; i < row_bytes; i++) dst[i] = from[i];
         }
+    }
+}
+
+/*
+ * Quest page summaries: for each listed physical page and KV head, the elementwise minimum
+ * and maximum of the page's P keys. k_pool [num_pages, Hkv, P, D] (dtype 0/1);
+ * kmin, kmax [n_list, Hkv, D] double.
+ */
+void oracle_quest_minmax(const void *k_pool, int dtype, const int32_t *pages, int n_list,
+                         int Hkv, int P, int D, double *kmin, double *kmax) {
+    for (int i = 0; i < n_list; i++)
+        for (int g = 0; g < Hkv; g++)
+            for (int d = 0; d < D; d++) {
+                double lo = INFINITY, hi = -INFINITY;
+                for (int t = 0; t < P; t++) {
+                    double x = widen(k_pool, dtype, (((size_t)pages[i] * Hkv + g) * P + t) * D + d);
+                    if (x < lo) lo = x;
+                    if (x > hi) hi = x;
+                }
+                kmin[((size_t)i * Hkv + g) * D + d] = lo;
+                kmax[((size_t)i * Hkv + g) * D + d] = hi;
+            }
+}
+
+/*
+ * Quest decode step for query head h of sequence b (L = seq_lens[b], P tokens a page):
+ *   full pages n < L / P get the bound U_n = sum_d max(q_d kmin_{n,d}, q_d kmax_{n,d}) from
+ *   the keys of KV head h / (Hq / Hkv) (summaries computed here from the cache);
+ *   the n_sel pages with the largest U (ties: the lower page index) are chosen, all of them
+ *   when there are no more than n_sel; the tokens past the last full page are always kept;
+ *   attention (scores q.k * scale, one softmax, weighted sum of V) runs over the chosen
+ *   pages' tokens and the kept tail.
+ * Outputs: out [n, D] and lse [n] for the n listed (b, h) pairs (all when pairs is NULL),
+ * sel [n, n_sel] the chosen logical pages in ascending order (-1 padded), ub [n, max_pages]
+ * the bounds (NaN for pages that are not full).
+ */
+void oracle_quest(const void *q, const void *k_pool, const void *v_pool, int dtype,
+                  const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv,
+                  int D, int page_size, int max_pages, double scale, int n_sel,
+                  const int32_t *pairs, int n_pairs, double *out, double *lse, int32_t *sel,
+                  double *ub) {
+    int n_rep = Hq / Hkv;
+    int n = pairs ? n_pairs : B * Hq;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int p = 0; p < n; p++) {
+        int b = pairs ? pairs[2 * p] : p / Hq;
+        int h = pairs ? pairs[2 * p + 1] : p % Hq;
+        int g = h / n_rep;
+        long L = seq_lens[b];
+        long full = L / page_size;
+        double *U = ub + (size_t)p * max_pages;
+        for (long m = 0; m < max_pages; m++) U[m] = NAN;
+        for (long m = 0; m < full; m++) {
+            double u = 0.0;
+            for (int d = 0; d < D; d++) {
+                double lo = INFINITY, hi = -INFINITY;
+                for (int t = 0; t < page_size; t++) {
+                    size_t row = pool_row(block_table, max_pages, page_size, Hkv, b, g,
+                                          m * page_size + t);
+                    double x = widen(k_pool, dtype, row * D + d);
+                    if (x < lo) lo = x;
+                    if (x > hi) hi = x;
+                }
+                double qd = widen(q, dtype, ((size_t)b * Hq + h) * D + d);
+                double a = qd * lo, c = qd * hi;
+                u += a > c ? a : c;
+            }
+            U[m] = u;
+        }
+        /* choose: repeatedly the largest remaining bound, the lower index on ties */
+        char *taken = (char *)calloc((size_t)(full > 0 ? full : 1), 1);
+        long n_take = full < n_sel ? full : n_sel;
+        for (long r = 0; r < n_take; r++) {
+            long best = -1;
+            for (long m = 0; m < full; m++)
+                if (!taken[m] && (best < 0 || U[m] > U[best])) best = m;
+            taken[best] = 1;
+        }
+        int32_t *sp = sel + (size_t)p * n_sel;
+        long k = 0;
+        for (long m = 0; m < full; m++)
+            if (taken[m]) sp[k++] = (int32_t)m;
+        for (; k < n_sel; k++) sp[k] = -1;
+        /* attention over the chosen pages and the tail */
+        double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        double m_ = -INFINITY;
+        for (long t = 0; t < L; t++) {
+            long pg = t / page_size;
+            if (pg < full && !taken[pg]) continue;
+            size_t row = pool_row(block_table, max_pages, page_size, Hkv, b, g, t);
+            double dot = 0.0;
+            for (int d = 0; d < D; d++)
+                dot += widen(q, dtype, ((size_t)b * Hq + h) * D + d) *
+                       widen(k_pool, dtype, row * D + d);
+            s[t] = scale * dot;
+            if (s[t] > m_) m_ = s[t];
+        }
+        double denom = 0.0;
+        double *o = out + (size_t)p * D;
+        for (int d = 0; d < D; d++) o[d] = 0.0;
+        for (long t = 0; t < L; t++) {
+            long pg = t / page_size;
+            if (pg < full && !taken[pg]) continue;
+            size_t row = pool_row(block_table, max_pages, page_size, Hkv, b, g, t);
+            double e = exp(s[t] - m_);
+            denom += e;
+            for (int d = 0; d < D; d++) o[d] += e * widen(v_pool, dtype, row * D + d);
+        }
+        for (int d = 0; d < D; d++) o[d] /= denom;
+        lse[p] = m_ + log(denom);
+        free(s);
+        free(taken);
     }
 }
