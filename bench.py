@@ -513,8 +513,75 @@ class DeltaRunner:
         return done, el, f"{heads} of {n} heads (one token step each)"
 
 
+class QuestRunner(GqaRunner):
+    """quest_select_pages then attn_decode_quest (page summaries computed once, at set-up,
+    as pages fill in a real decode)."""
+    launches_per_step = 3          # bounds, choice, attention
+    kernel = "quest_attn_kernel"
+
+    def __init__(self, name, dev):
+        super().__init__(name, dev)
+        self.n_sel = W.WORKLOADS[name].params["n_sel"]
+        self.kmin, self.kmax, self.err = self.kvd.quest_page_minmax(self.k)
+        self.sel = torch.empty(self.x.B, self.x.Hq, self.n_sel, dtype=torch.int32, device=dev)
+        self.ub = torch.empty(self.x.B, self.x.Hq, self.x.max_pages, dtype=torch.float32,
+                              device=dev)
+        self._config, self.bytes, self.flops = self.describe(name, self.x)
+
+    @staticmethod
+    def describe(name, x):
+        n_sel = W.WORKLOADS[name].params["n_sel"]
+        P, esz = x.page_size, x.q.element_size()
+        summ, rows = 0, 0
+        for L in x.seq_lens.tolist():
+            full = L // P
+            summ += full * x.Hkv * 2 * x.D * esz                  # kmin and kmax rows read
+            rows += x.Hq * (min(full, n_sel) * P + L - full * P)  # K/V rows each head reads
+        nbytes = summ + rows * x.D * 2 * esz + x.q.numel() * esz
+        flops = 4.0 * rows * x.D
+        cfg = {"workload": name, "B": x.B, "Hq": x.Hq, "Hkv": x.Hkv, "D": x.D, "page_size": P,
+               "n_sel": n_sel, "budget_tokens": n_sel * P,
+               "seq_len_mean": float(x.seq_lens.float().mean()), "kv_bytes": nbytes,
+               "dense_kv_bytes": int(x.seq_lens.sum()) * x.Hkv * x.D * 2 * esz}
+        return cfg, nbytes, flops
+
+    def step(self, q=None, out=None):
+        x = self.x
+        q = self.q if q is None else q
+        out = self.out if out is None else out
+        self.kvd.quest_select_pages(q, self.kmin, self.kmax, self.bt, self.sl, self.n_sel,
+                                    x.page_size, sel=self.sel, ub_out=self.ub, err=self.err)
+        return self.kvd.attn_decode_quest(q, self.k, self.v, self.bt, self.sl, self.sel,
+                                          scale=x.scale, out=out, err=self.err)
+
+    def oracle_sample(self, budget_s):
+        import numpy as np
+        import oracle
+        x = self.x
+        rng = np.random.default_rng(0)
+        pairs_all = [(b, h) for b in range(x.B) for h in range(x.Hq)]
+        rng.shuffle(pairs_all)
+        t0 = time.perf_counter()
+        done, n = 0, 0
+        P = x.page_size
+        for i in range(0, len(pairs_all), 8):
+            pairs = pairs_all[i:i + 8]
+            oracle.quest(x.q, x.k_pool, x.v_pool, x.block_table, x.seq_lens, x.scale,
+                         self.n_sel, pairs=pairs)
+            for b, h in pairs:
+                L = int(x.seq_lens[b])
+                full = L // P
+                done += (full * 2 * x.D + (min(full, self.n_sel) * P + L - full * P) * x.D * 2) \
+                    * x.q.element_size()
+            n += len(pairs)
+            if time.perf_counter() - t0 > budget_s:
+                break
+        el = time.perf_counter() - t0
+        return done, el, f"{n} of {len(pairs_all)} (sequence, query head) pairs"
+
+
 RUNNERS = {"gqa": GqaRunner, "swa": GqaRunner, "mla": MlaRunner, "dsa": DsaRunner,
-           "dsa_fp8": DsaFp8Runner, "delta": DeltaRunner}
+           "dsa_fp8": DsaFp8Runner, "delta": DeltaRunner, "quest": QuestRunner}
 
 
 def make_runner(name, dev):
@@ -643,7 +710,9 @@ def oracle_runner(name):
         r.k = r.xi.k
     else:
         r.x = x = W.build(name)
-        if cls is GqaRunner:
+        if cls is QuestRunner:
+            r.n_sel = W.WORKLOADS[name].params["n_sel"]
+        if cls in (GqaRunner, QuestRunner):
             r.swa = x.window > 0 or x.n_sink > 0 or x.sink_logit is not None
     return r
 

@@ -36,6 +36,9 @@
  *    read from the rolling cache. "Attention Optimizations", DSA / Computation
  *    Path (update_cache before attention) and Sliding-window (a rolling buffer
  *    of W entries); "All the attentions", section 4.
+ *  - quest_page_minmax, quest_select_pages, attn_decode_quest: query-aware page
+ *    selection. "Long context, KV eviction and sparse attention", Sparse attention
+ *    (Quest: per-page key bounds, the best pages, attention over them).
  *  - kvd_delta_decode_step: one Gated DeltaNet / KDA decode step on each head's
  *    fixed-size state. "All the attentions", sections 6 and 7.
  *
@@ -211,6 +214,54 @@ int kvd_cache_append(const void *k_new, const void *v_new, void *k_pool, void *v
                      const int32_t *block_table, const int32_t *seq_lens, int B, int H, int D,
                      int page_size, int max_pages, int num_pages, int dtype, int window,
                      int n_sink, int *err, cudaStream_t stream);
+
+/*
+ * Quest page summaries ("Long context, KV eviction and sparse attention", Sparse attention:
+ * each page of keys is summarised by its elementwise minimum and maximum). For each listed
+ * physical page (pages [n_list] int32, device; null = every page 0..num_pages-1) and KV head:
+ *   kmin[page][g][d] = min_t k_pool[page][g][t][d],  kmax likewise (t < page_size)
+ *  k_pool [num_pages, Hkv, page_size, D], kmin / kmax [num_pages, Hkv, D], all of dtype
+ *  (KVD_BF16 or KVD_F32; the extremes of stored values are stored exactly), device.
+ * Compute a page's summary once it is full (only full pages are scored). err: int32 on the
+ * device, set to KVD_ERR_DEVICE_OOB for a listed page out of range (skipped). Supported:
+ * D in {64, 128}. No workspace.
+ */
+int quest_page_minmax(const void *k_pool, void *kmin, void *kmax, const int32_t *pages,
+                      int n_list, int num_pages, int Hkv, int page_size, int D, int dtype,
+                      int *err, cudaStream_t stream);
+
+/*
+ * Quest page choice for every query head (same passage): sequence b has full = L_b /
+ * page_size full pages (logical); query head h (KV head g = h / (Hq / Hkv)) bounds its
+ * scores on page n by U = sum_d max(q_d kmin_d, q_d kmax_d) (the summaries of the page's
+ * physical page, head g; products and sums in float32) and keeps the n_sel pages with the
+ * largest U, ties to the lower page (all full pages when there are no more than n_sel).
+ *  sel    [B, Hq, n_sel] int32 output: the chosen logical pages in ascending order, -1 padded
+ *  ub_out [B, Hq, max_pages] float32 output (required; the bounds are computed there, then
+ *         chosen from): U, NaN past the full pages
+ * Other arguments as attn_decode_gqa_paged. Supported: D in {64, 128}, Hq / Hkv <= 16,
+ * 1 <= n_sel <= 64, max_pages <= 12800. err as quest_page_minmax (KVD_ERR_DEVICE_OOB for a
+ * length or page id out of range, clamped). Two launches; no workspace.
+ */
+int quest_select_pages(const void *q, const void *kmin, const void *kmax,
+                       const int32_t *block_table, const int32_t *seq_lens, int32_t *sel,
+                       float *ub_out, int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                       int num_pages, int n_sel, int dtype, int *err, cudaStream_t stream);
+
+/*
+ * Attention of each query head over its chosen pages and the tokens past the last full page
+ * (same passage): scores scale * q.k, one softmax, weighted sum of V, over the tokens of the
+ * pages listed in sel (as quest_select_pages writes it; entries past min(full, n_sel) are
+ * not read) plus positions full * page_size .. L_b - 1. out [B, Hq, D] (dtype of q),
+ * lse_out [B, Hq] float32 natural log (nullable). Other arguments as
+ * attn_decode_gqa_paged; err as quest_select_pages (a listed page outside 0..full-1 is
+ * flagged and skipped). No workspace.
+ */
+int attn_decode_quest(const void *q, const void *k_pool, const void *v_pool,
+                      const int32_t *block_table, const int32_t *seq_lens, const int32_t *sel,
+                      void *out, float *lse_out, int B, int Hq, int Hkv, int D, int page_size,
+                      int max_pages, int num_pages, int n_sel, float scale, int dtype, int *err,
+                      cudaStream_t stream);
 
 /*
  * Absorbed MLA decode over all cached tokens.

@@ -18,6 +18,7 @@ Operations:
   delta_decode_step       one gated delta-rule (Gated DeltaNet / KDA) decode step
   cache_append            the new token's K/V (or latent row) into a paged or rolling cache
   attn_decode_swa_ring    sliding window + sinks over a rolling cache
+  quest_page_minmax, quest_select_pages, attn_decode_quest   Quest page selection
 """
 from __future__ import annotations
 
@@ -34,7 +35,8 @@ lib = _lib.load()
 __all__ = [
     "attn_decode_gqa_paged", "attn_decode_swa_sink", "attn_decode_mla", "dsa_indexer_topk",
     "dsa_indexer_topk_fp8", "quantize_e4m3_rows", "dsa_indexer_cache_append_fp8",
-    "delta_decode_step", "attn_decode_swa_ring", "cache_append",
+    "delta_decode_step", "attn_decode_swa_ring", "cache_append", "quest_page_minmax",
+    "quest_select_pages", "attn_decode_quest",
     "dsa_topk", "attn_decode_mla_sparse", "kvd_workspace_size", "kvd_check_device_error",
     "Workspace", "KvdError",
 ]
@@ -239,6 +241,73 @@ def cache_append(k_new, v_new, k_pool, v_pool, block_table, seq_lens, window=0, 
                               _stream(stream))
     _check(st, "kvd_cache_append")
     return err
+
+
+def _err(err, device):
+    return torch.zeros(1, dtype=torch.int32, device=device) if err is None else err
+
+
+def quest_page_minmax(k_pool, kmin=None, kmax=None, pages=None, err=None, stream=None):
+    """Per-page elementwise key minimum and maximum: k_pool [num_pages, Hkv, P, D] ->
+    (kmin, kmax) [num_pages, Hkv, D] in the pool's dtype, for the physical pages listed in
+    `pages` (int32, device; None = all). Returns (kmin, kmax, err)."""
+    _need(k_pool, "k_pool", dim=4)
+    if k_pool.dtype not in _DT:
+        raise TypeError("k_pool must be float32 or bfloat16")
+    num_pages, Hkv, P, D = k_pool.shape
+    shape = (num_pages, Hkv, D)
+    kmin = torch.empty(shape, dtype=k_pool.dtype, device=k_pool.device) if kmin is None else kmin
+    kmax = torch.empty(shape, dtype=k_pool.dtype, device=k_pool.device) if kmax is None else kmax
+    _need(kmin, "kmin", k_pool.dtype)
+    _need(kmax, "kmax", k_pool.dtype)
+    if pages is not None:
+        _need(pages, "pages", torch.int32, 1)
+    err = _err(err, k_pool.device)
+    st = lib.quest_page_minmax(_p(k_pool), _p(kmin), _p(kmax), _p(pages),
+                               0 if pages is None else pages.numel(), num_pages, Hkv, P, D,
+                               _DT[k_pool.dtype], _p(err), _stream(stream))
+    _check(st, "quest_page_minmax")
+    return kmin, kmax, err
+
+
+def quest_select_pages(q, kmin, kmax, block_table, seq_lens, n_sel, page_size, sel=None,
+                       ub_out=None, err=None, stream=None):
+    """Each query head's n_sel full pages with the largest score bound (ascending logical
+    page ids, -1 padded): sel [B, Hq, n_sel] int32."""
+    _need(q, "q", dim=3)
+    _need(kmin, "kmin", q.dtype, 3)
+    _need(kmax, "kmax", q.dtype, 3)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, Hq, D = q.shape
+    num_pages, Hkv, _ = kmin.shape
+    max_pages = block_table.shape[1]
+    sel = torch.empty(B, Hq, n_sel, dtype=torch.int32, device=q.device) if sel is None else sel
+    if ub_out is None:
+        ub_out = torch.empty(B, Hq, max_pages, dtype=torch.float32, device=q.device)
+    err = _err(err, q.device)
+    st = lib.quest_select_pages(_p(q), _p(kmin), _p(kmax), _p(block_table), _p(seq_lens),
+                                _p(sel), _p(ub_out), B, Hq, Hkv, D, int(page_size), max_pages,
+                                num_pages, int(n_sel), _DT[q.dtype], _p(err), _stream(stream))
+    _check(st, "quest_select_pages")
+    return sel
+
+
+def attn_decode_quest(q, k_pool, v_pool, block_table, seq_lens, sel, scale=None, out=None,
+                      lse_out=None, err=None, stream=None):
+    """Attention of each query head over its chosen pages (sel from quest_select_pages)
+    and the tokens past the last full page."""
+    B, Hq, Hkv, D, P, max_pages, num_pages = _gqa_args(q, k_pool, v_pool, block_table, seq_lens)
+    _need(sel, "sel", torch.int32, 3)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    err = _err(err, q.device)
+    st = lib.attn_decode_quest(_p(q), _p(k_pool), _p(v_pool), _p(block_table), _p(seq_lens),
+                               _p(sel), _p(out), _p(lse_out), B, Hq, Hkv, D, P, max_pages,
+                               num_pages, sel.shape[2], scale, _DT[q.dtype], _p(err),
+                               _stream(stream))
+    _check(st, "attn_decode_quest")
+    return out
 
 
 def _mla_args(q, c_pool, block_table, seq_lens):

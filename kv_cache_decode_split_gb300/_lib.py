@@ -23,6 +23,9 @@ EXPORTS = (
     "kvd_delta_decode_step",
     "attn_decode_swa_ring",
     "kvd_cache_append",
+    "quest_page_minmax",
+    "quest_select_pages",
+    "attn_decode_quest",
     "dsa_topk",
     "attn_decode_mla_sparse",
     "kvd_workspace_size",
@@ -62,13 +65,18 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kvd_delta_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P]
     lib.attn_decode_swa_ring.argtypes = gqa + [I, I, P, P, Z, P]
     lib.kvd_cache_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P]
+    lib.quest_page_minmax.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P]
+    lib.quest_select_pages.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P]
+    lib.attn_decode_quest.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P,
+                                      P]
     lib.dsa_topk.argtypes = [P, P, P, P, I, I, I, P, Z, P]
     lib.attn_decode_mla_sparse.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P,
                                            Z, P]
     for name in ("attn_decode_gqa_paged", "attn_decode_gqa_paged_static_ws", "attn_decode_swa_sink", "attn_decode_mla",
                  "dsa_indexer_topk", "dsa_indexer_topk_fp8", "kvd_quantize_e4m3_rows",
                  "dsa_indexer_cache_append_fp8", "kvd_delta_decode_step",
-                 "attn_decode_swa_ring", "kvd_cache_append", "dsa_topk",
+                 "attn_decode_swa_ring", "kvd_cache_append", "quest_page_minmax",
+                 "quest_select_pages", "attn_decode_quest", "dsa_topk",
                  "attn_decode_mla_sparse",
                  "kvd_check_device_error"):
         getattr(lib, name).restype = I

@@ -424,6 +424,106 @@ int kvd_cache_append(const void* k_new, const void* v_new, void* k_pool, void* v
     return append_launch(ap, stream);
 }
 
+// Checks shared by the three Quest entry points.
+static int quest_common(QuestParams& qp, int B, int Hq, int Hkv, int D, int page_size,
+                        int max_pages, int num_pages, int dtype, int* err) {
+    if (!err || (reinterpret_cast<uintptr_t>(err) & 3)) return KVD_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || page_size < 1 || max_pages < 1 ||
+        num_pages < 1)
+        return KVD_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return KVD_ERR_UNSUPPORTED;
+    if (dtype != KVD_F32 && dtype != KVD_BF16) return KVD_ERR_UNSUPPORTED;
+    if (Hq / Hkv > 16) return KVD_ERR_UNSUPPORTED;
+    if ((long long)num_pages * Hkv * page_size >= (1LL << 31) ||
+        (long long)max_pages * page_size >= (1LL << 30))
+        return KVD_ERR_UNSUPPORTED;
+    std::memset(&qp, 0, sizeof qp);
+    qp.B = B;
+    qp.Hq = Hq;
+    qp.Hkv = Hkv;
+    qp.D = D;
+    qp.page_size = page_size;
+    qp.max_pages = max_pages;
+    qp.num_pages = num_pages;
+    qp.max_len = max_pages * page_size;
+    qp.dtype = dtype;
+    qp.err = err;
+    return KVD_OK;
+}
+
+int quest_page_minmax(const void* k_pool, void* kmin, void* kmax, const int32_t* pages,
+                      int n_list, int num_pages, int Hkv, int page_size, int D, int dtype,
+                      int* err, cudaStream_t stream) {
+    if (!k_pool || !kmin || !kmax) return KVD_ERR_INVALID_ARG;
+    QuestParams qp;
+    const int st = quest_common(qp, 1, Hkv, Hkv, D, page_size, 1, num_pages, dtype, err);
+    if (st != KVD_OK) return st;
+    if (!pages) n_list = num_pages;
+    if (n_list < 1) return KVD_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(kmin) || !aligned16(kmax) ||
+        (pages && (reinterpret_cast<uintptr_t>(pages) & 3)))
+        return KVD_ERR_INVALID_ARG;
+    qp.k_pool = k_pool;
+    qp.kmin = kmin;
+    qp.kmax = kmax;
+    qp.pages = pages;
+    qp.n_list = n_list;
+    return quest_minmax_launch(qp, stream);
+}
+
+int quest_select_pages(const void* q, const void* kmin, const void* kmax,
+                       const int32_t* block_table, const int32_t* seq_lens, int32_t* sel,
+                       float* ub_out, int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                       int num_pages, int n_sel, int dtype, int* err, cudaStream_t stream) {
+    if (!q || !kmin || !kmax || !block_table || !seq_lens || !sel || !ub_out)
+        return KVD_ERR_INVALID_ARG;
+    QuestParams qp;
+    const int st = quest_common(qp, B, Hq, Hkv, D, page_size, max_pages, num_pages, dtype, err);
+    if (st != KVD_OK) return st;
+    if (n_sel < 1 || n_sel > 64) return KVD_ERR_UNSUPPORTED;
+    if (quest_select_smem(Hq, Hkv, max_pages) > 200 * 1024) return KVD_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(kmin) || !aligned16(kmax) ||
+        (reinterpret_cast<uintptr_t>(sel) & 3) || (reinterpret_cast<uintptr_t>(ub_out) & 3))
+        return KVD_ERR_INVALID_ARG;
+    qp.q = q;
+    qp.kmin = const_cast<void*>(kmin);
+    qp.kmax = const_cast<void*>(kmax);
+    qp.block_table = block_table;
+    qp.seq_lens = seq_lens;
+    qp.sel = sel;
+    qp.ub_out = ub_out;
+    qp.n_sel = n_sel;
+    return quest_select_launch(qp, stream);
+}
+
+int attn_decode_quest(const void* q, const void* k_pool, const void* v_pool,
+                      const int32_t* block_table, const int32_t* seq_lens, const int32_t* sel,
+                      void* out, float* lse_out, int B, int Hq, int Hkv, int D, int page_size,
+                      int max_pages, int num_pages, int n_sel, float scale, int dtype, int* err,
+                      cudaStream_t stream) {
+    if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !sel || !out)
+        return KVD_ERR_INVALID_ARG;
+    QuestParams qp;
+    const int st = quest_common(qp, B, Hq, Hkv, D, page_size, max_pages, num_pages, dtype, err);
+    if (st != KVD_OK) return st;
+    if (n_sel < 1 || n_sel > 64) return KVD_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return KVD_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(sel) & 3) || (reinterpret_cast<uintptr_t>(lse_out) & 3))
+        return KVD_ERR_INVALID_ARG;
+    qp.q = q;
+    qp.k_pool = k_pool;
+    qp.v_pool = v_pool;
+    qp.block_table = block_table;
+    qp.seq_lens = seq_lens;
+    qp.sel = const_cast<int32_t*>(sel);
+    qp.out = out;
+    qp.lse_out = lse_out;
+    qp.n_sel = n_sel;
+    qp.scale = scale;
+    return quest_attn_launch(qp, stream);
+}
+
 int attn_decode_mla(const void* q, const void* c_pool, const int32_t* block_table,
                     const int32_t* seq_lens, void* out, float* lse_out, int B, int H, int d_qk,
                     int d_v, int page_size, int max_pages, int num_pages, float scale, void* ws,

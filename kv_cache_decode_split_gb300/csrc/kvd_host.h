@@ -146,6 +146,29 @@ struct AppendParams {
     int window, n_sink;        // window > 0: rolling cache of n_sink + window slots
 };
 int append_launch(const AppendParams& p, cudaStream_t stream);
+
+// Arguments of the Quest kernels (page summaries, page selection, attention over the pages).
+struct QuestParams {
+    const void* q;             // [B, Hq, D]
+    const void* k_pool;        // [num_pages, Hkv, P, D]
+    const void* v_pool;
+    void* kmin;                // [num_pages, Hkv, D], the pool's dtype
+    void* kmax;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const int32_t* pages;      // summaries: the physical pages to (re)compute, null = all
+    int32_t* sel;              // [B, Hq, n_sel] chosen logical pages, ascending, -1 padded
+    float* ub_out;             // [B, Hq, max_pages] bounds (optional)
+    void* out;                 // [B, Hq, D]
+    float* lse_out;            // [B, Hq] (optional)
+    int* err;
+    int B, Hq, Hkv, D, page_size, max_pages, num_pages, max_len, n_sel, n_list, dtype;
+    float scale;
+};
+int quest_minmax_launch(const QuestParams& p, cudaStream_t stream);
+size_t quest_select_smem(int Hq, int Hkv, int max_pages);
+int quest_select_launch(const QuestParams& p, cudaStream_t stream);
+int quest_attn_launch(const QuestParams& p, cudaStream_t stream);
 int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------------------

@@ -1,0 +1,471 @@
+// quest.cu -- query-aware page selection (Quest) for GQA decode over a paged cache.
+//
+// What is computed ("Long context, KV eviction and sparse attention", Sparse attention):
+// every page of keys is summarised by its elementwise minimum and maximum; a query head's
+// score for any key of the page is at most U = sum_d max(q_d kmin_d, q_d kmax_d); each query
+// head keeps the n_sel full pages with the largest U (ties: the lower page) and the tokens
+// past the last full page, and attends over those only.
+//
+// GB300: four small kernels, all bound by memory traffic or latency.
+//  * quest_minmax_kernel: one warp per (page, KV head): the page's keys once, min and max in
+//    the cache's own dtype (exact). Run once per page, when it fills.
+//  * quest_bounds_kernel: one CTA per (sequence, KV head, 128 pages), a warp per 32 pages
+//    (their page ids in one load, eight pages' summaries in flight): a lane holds its D/32
+//    dims of kmin/kmax and of the group's queries, and warp sums give every query head of
+//    the group its bound, written to the caller's bound array.
+//  * quest_choose_kernel: one warp per (sequence, query head) picks the n_sel best bounds by
+//    repeated warp arg-max (value, then lower index) and writes them in ascending order.
+//  * quest_attn_kernel: one CTA per (sequence, query head) over its chosen pages and tail:
+//    warps take pages, eight rows in flight per warp, scores by warp sums, running max /
+//    running sum softmax, then the four warps merge in shared memory.
+// The selected rows are a few hundred per head, read with plain vector loads; there is no
+// shared contraction across heads (each head reads its own pages) for the tensor cores.
+
+#include <algorithm>
+#include <cuda_bf16.h>
+
+#include "kvd_device.cuh"
+#include "kvd_host.h"
+
+namespace kvd {
+
+namespace {
+
+constexpr float kQLog2e = 1.4426950408889634f;
+constexpr int kAttnWarps = 4;
+constexpr int kRowsInFlight = 16;
+
+// VEC consecutive elements of a row as float (bf16 or float32 storage).
+template <int VEC, bool BF16>
+__device__ __forceinline__ void load_vec(const void* base, size_t elem, float (&x)[VEC]) {
+    if constexpr (BF16) {
+        const __nv_bfloat16* p = static_cast<const __nv_bfloat16*>(base) + elem;
+        if constexpr (VEC == 2) {
+            const __nv_bfloat162 t = *reinterpret_cast<const __nv_bfloat162*>(p);
+            x[0] = __low2float(t), x[1] = __high2float(t);
+        } else {
+#pragma unroll
+            for (int i = 0; i < VEC; i += 4) {
+                const uint2 raw = *reinterpret_cast<const uint2*>(p + i);
+                const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+                const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+                x[i] = __low2float(a), x[i + 1] = __high2float(a);
+                x[i + 2] = __low2float(b), x[i + 3] = __high2float(b);
+            }
+        }
+    } else {
+        const float* p = static_cast<const float*>(base) + elem;
+        if constexpr (VEC == 2) {
+            const float2 t = *reinterpret_cast<const float2*>(p);
+            x[0] = t.x, x[1] = t.y;
+        } else {
+#pragma unroll
+            for (int i = 0; i < VEC; i += 4) {
+                const float4 t = *reinterpret_cast<const float4*>(p + i);
+                x[i] = t.x, x[i + 1] = t.y, x[i + 2] = t.z, x[i + 3] = t.w;
+            }
+        }
+    }
+}
+
+// A lane's VEC elements of a row kept as stored (bf16 pairs or floats) until used, so that
+// many rows can be in flight in few registers.
+template <int VEC, bool BF16>
+struct Raw {
+    static constexpr int kWords = BF16 ? VEC / 2 : VEC;
+    uint32_t w[kWords];
+    __device__ __forceinline__ void load(const void* base, size_t elem) {
+        if constexpr (BF16) {
+            const uint32_t* src =
+                reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(base) + elem);
+            if constexpr (kWords == 1) {
+                w[0] = *src;
+            } else {
+#pragma unroll
+                for (int i = 0; i < kWords; i += 2) {
+                    const uint2 t = *reinterpret_cast<const uint2*>(src + i);
+                    w[i] = t.x, w[i + 1] = t.y;
+                }
+            }
+        } else {
+            const uint32_t* src =
+                reinterpret_cast<const uint32_t*>(static_cast<const float*>(base) + elem);
+#pragma unroll
+            for (int i = 0; i < kWords; i += (kWords >= 4 ? 4 : 2)) {
+                if constexpr (kWords >= 4) {
+                    const uint4 t = *reinterpret_cast<const uint4*>(src + i);
+                    w[i] = t.x, w[i + 1] = t.y, w[i + 2] = t.z, w[i + 3] = t.w;
+                } else {
+                    const uint2 t = *reinterpret_cast<const uint2*>(src + i);
+                    w[i] = t.x, w[i + 1] = t.y;
+                }
+            }
+        }
+    }
+    __device__ __forceinline__ float at(int i) const {
+        if constexpr (BF16) {
+            const uint32_t x = w[i / 2];
+            return __uint_as_float((i & 1) ? (x & 0xffff0000u) : (x << 16));
+        } else {
+            return __uint_as_float(w[i]);
+        }
+    }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// ---------------------------------------------------------------------------- summaries
+template <int VEC, bool BF16>
+__global__ void __launch_bounds__(256) quest_minmax_kernel(const QuestParams p) {
+    griddep_wait();
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+    const int n_units = p.n_list * p.Hkv;
+    if (warp >= n_units) return;
+    const int i = warp / p.Hkv, g = warp % p.Hkv;
+    const int pg = p.pages ? p.pages[i] : i;
+    if (pg < 0 || pg >= p.num_pages) {
+        if (lane == 0) record_error(p.err, KVD_ERR_DEVICE_OOB);
+        return;
+    }
+    const int D = VEC * 32;
+    const size_t row0 = (static_cast<size_t>(pg) * p.Hkv + g) * p.page_size;
+    float lo[VEC], hi[VEC];
+    load_vec<VEC, BF16>(p.k_pool, row0 * D + lane * VEC, lo);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) hi[j] = lo[j];
+    for (int t = 1; t < p.page_size; ++t) {
+        float x[VEC];
+        load_vec<VEC, BF16>(p.k_pool, (row0 + t) * D + lane * VEC, x);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) lo[j] = fminf(lo[j], x[j]), hi[j] = fmaxf(hi[j], x[j]);
+    }
+    const size_t o = (static_cast<size_t>(pg) * p.Hkv + g) * D + lane * VEC;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+        // min and max of stored values are stored values: the conversion back is exact
+        if constexpr (BF16) {
+            static_cast<__nv_bfloat16*>(p.kmin)[o + j] = __float2bfloat16(lo[j]);
+            static_cast<__nv_bfloat16*>(p.kmax)[o + j] = __float2bfloat16(hi[j]);
+        } else {
+            static_cast<float*>(p.kmin)[o + j] = lo[j];
+            static_cast<float*>(p.kmax)[o + j] = hi[j];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------- bounds
+// One CTA of kBoundWarps warps per (sequence, KV head, 32 * kBoundWarps pages); a warp takes
+// 32 pages: their page ids in one load, then kPagesInFlight pages' summaries at once, and
+// for each page the bounds of the KG (>= G) query heads of the group by warp sums.
+constexpr int kBoundWarps = 4;
+constexpr int kPagesInFlight = 8;
+
+template <int VEC, bool BF16, int KG>
+__global__ void __launch_bounds__(kBoundWarps * 32) quest_bounds_kernel(const QuestParams p) {
+    constexpr int D = VEC * 32;
+    griddep_wait();
+    const int b = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
+    const int G = p.Hq / p.Hkv;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int L = load_len(p.seq_lens, b, p.max_len, p.err);
+    const int full = L / p.page_size;
+    const int m0 = (blockIdx.y * kBoundWarps + warp) * 32;
+    float* ub = p.ub_out + (static_cast<size_t>(b) * p.Hq + g * G) * p.max_pages;
+    // pages that are not full have no bound
+    for (int j = 0; j < G; ++j)
+        if (m0 + lane >= full && m0 + lane < p.max_pages)
+            ub[static_cast<size_t>(j) * p.max_pages + m0 + lane] = __int_as_float(0x7fc00000);
+    if (m0 >= full) return;
+    float q[KG][VEC];
+#pragma unroll
+    for (int j = 0; j < KG; ++j)
+        if (j < G)
+            load_vec<VEC, BF16>(p.q, (static_cast<size_t>(b) * p.Hq + g * G + j) * D + lane * VEC,
+                                q[j]);
+    const int my = m0 + lane;
+    const int pg_lane =
+        my < full ? load_page(p.block_table, p.max_pages, p.num_pages, b, my, p.err) : 0;
+    const int n_here = min(32, full - m0);
+    for (int c = 0; c < n_here; c += kPagesInFlight) {
+        Raw<VEC, BF16> lo[kPagesInFlight], hi[kPagesInFlight];
+#pragma unroll
+        for (int k = 0; k < kPagesInFlight; ++k) {
+            const int pg = __shfl_sync(0xffffffffu, pg_lane, (c + k) & 31);
+            if (c + k < n_here) {
+                const size_t o = (static_cast<size_t>(pg) * p.Hkv + g) * D + lane * VEC;
+                lo[k].load(p.kmin, o);
+                hi[k].load(p.kmax, o);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kPagesInFlight; ++k) {
+            if (c + k >= n_here) break;
+            float u[KG];
+#pragma unroll
+            for (int j = 0; j < KG; ++j) {
+                u[j] = 0.f;
+#pragma unroll
+                for (int i = 0; i < VEC; ++i)
+                    u[j] += fmaxf(q[j][i] * lo[k].at(i), q[j][i] * hi[k].at(i));
+            }
+#pragma unroll
+            for (int off = 16; off; off >>= 1)
+#pragma unroll
+                for (int j = 0; j < KG; ++j) u[j] += __shfl_xor_sync(0xffffffffu, u[j], off);
+            // lane j writes head j's bound
+#pragma unroll
+            for (int j = 0; j < KG; ++j)
+                if (lane == j && j < G) ub[static_cast<size_t>(j) * p.max_pages + m0 + c + k] = u[j];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------- choice
+// One warp per (sequence, query head): the bounds of its full pages into shared memory,
+// then n_sel rounds of warp arg-max (the larger bound, then the lower page), a chosen page's
+// bound set to -inf; the chosen pages are written in ascending order.
+constexpr int kChooseWarps = 4;
+
+__global__ void __launch_bounds__(kChooseWarps * 32) quest_choose_kernel(const QuestParams p) {
+    extern __shared__ float ubs[];  // [kChooseWarps][max_pages]
+    griddep_wait();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int bh = blockIdx.x * kChooseWarps + warp;
+    if (bh >= p.B * p.Hq) return;
+    const int b = bh / p.Hq;
+    const int L = load_len(p.seq_lens, b, p.max_len, p.err);
+    const int full = L / p.page_size;
+    float* u = ubs + static_cast<size_t>(warp) * p.max_pages;
+    const float* src = p.ub_out + static_cast<size_t>(bh) * p.max_pages;
+    for (int m = lane; m < full; m += 32) u[m] = src[m];
+    __syncwarp();
+    int32_t* out = p.sel + static_cast<size_t>(bh) * p.n_sel;
+    const int n_take = min(full, p.n_sel);
+    int mine0 = -1, mine1 = -1;  // this lane's picks: rounds lane and lane + 32
+    for (int r = 0; r < n_take; ++r) {
+        float best = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int m = lane; m < full; m += 32) {
+            const float v = u[m];
+            if (v > best || (v == best && m < bi)) best = v, bi = m;
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, best, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (ov > best || (ov == best && oi < bi)) best = ov, bi = oi;
+        }
+        if (bi >= full) bi = 0;  // every remaining bound is -inf or NaN
+        if (lane == (r & 31)) {
+            if (r < 32) mine0 = bi; else mine1 = bi;
+        }
+        if (lane == 0) u[bi] = -INFINITY;
+        __syncwarp();
+    }
+    // ascending order: each pick goes to its rank among the picks
+    int rank0 = 0, rank1 = 0;
+    for (int r = 0; r < n_take; ++r) {
+        const int other = __shfl_sync(0xffffffffu, r < 32 ? mine0 : mine1, r & 31);
+        rank0 += other < mine0;
+        rank1 += other < mine1;
+    }
+    if (lane < n_take) out[rank0] = mine0;
+    if (lane + 32 < n_take) out[rank1] = mine1;
+    for (int r = n_take + lane; r < p.n_sel; r += 32) out[r] = -1;
+}
+
+// ---------------------------------------------------------------------------- attention
+template <int VEC, bool BF16>
+__global__ void __launch_bounds__(kAttnWarps * 32) quest_attn_kernel(const QuestParams p) {
+    constexpr int D = VEC * 32;
+    __shared__ float m_s[kAttnWarps], l_s[kAttnWarps];
+    __shared__ float o_s[kAttnWarps][D];
+    griddep_wait();
+    const int b = blockIdx.x / p.Hq, h = blockIdx.x % p.Hq;
+    const int g = h / (p.Hq / p.Hkv);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int L = load_len(p.seq_lens, b, p.max_len, p.err);
+    const int full = L / p.page_size;
+    const int n_take = min(full, p.n_sel);
+    const int tail = L - full * p.page_size;
+    const int32_t* sel = p.sel + (static_cast<size_t>(b) * p.Hq + h) * p.n_sel;
+
+    float q[VEC];
+    load_vec<VEC, BF16>(p.q, (static_cast<size_t>(b) * p.Hq + h) * D + lane * VEC, q);
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) q[i] *= p.scale * kQLog2e;
+    float m = -INFINITY, l = 0.f, o[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) o[i] = 0.f;
+
+    // units of work: the chosen pages, then the tail as one more (partial) page; their
+    // physical pages are resolved up front, all lanes at once (at most 65 units)
+    __shared__ int unit_pg[65];
+    const int n_units = n_take + (tail > 0 ? 1 : 0);
+    for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
+        int lp = u < n_take ? sel[u] : full;
+        if (lp < 0 || lp >= full + (u < n_take ? 0 : 1)) {
+            record_error(p.err, KVD_ERR_DEVICE_OOB);
+            unit_pg[u] = -1;
+            continue;
+        }
+        unit_pg[u] = load_page(p.block_table, p.max_pages, p.num_pages, b, lp, p.err);
+    }
+    __syncthreads();
+    for (int u = warp; u < n_units; u += kAttnWarps) {
+        const int pg = unit_pg[u];
+        if (pg < 0) continue;
+        const int rows = u < n_take ? p.page_size : tail;
+        const size_t row0 = (static_cast<size_t>(pg) * p.Hkv + g) * p.page_size;
+        for (int t0 = 0; t0 < rows; t0 += kRowsInFlight) {
+            // the K and V rows of the batch all in flight together
+            Raw<VEC, BF16> k[kRowsInFlight], v[kRowsInFlight];
+            float s[kRowsInFlight];
+#pragma unroll
+            for (int r = 0; r < kRowsInFlight; ++r)
+                if (t0 + r < rows) {
+                    k[r].load(p.k_pool, (row0 + t0 + r) * D + lane * VEC);
+                    v[r].load(p.v_pool, (row0 + t0 + r) * D + lane * VEC);
+                }
+#pragma unroll
+            for (int r = 0; r < kRowsInFlight; ++r) {
+                float acc = 0.f;
+                if (t0 + r < rows)
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) acc = fmaf(q[i], k[r].at(i), acc);
+                s[r] = acc;
+            }
+#pragma unroll
+            for (int off = 16; off; off >>= 1)
+#pragma unroll
+                for (int r = 0; r < kRowsInFlight; ++r) s[r] += __shfl_xor_sync(0xffffffffu, s[r], off);
+            float mx = m;
+#pragma unroll
+            for (int r = 0; r < kRowsInFlight; ++r)
+                if (t0 + r < rows) mx = fmaxf(mx, s[r]);
+            const float corr = exp2f(m - mx);
+            l *= corr;
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) o[i] *= corr;
+            m = mx;
+#pragma unroll
+            for (int r = 0; r < kRowsInFlight; ++r) {
+                if (t0 + r >= rows) break;
+                const float e = exp2f(s[r] - m);
+                l += e;
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) o[i] = fmaf(e, v[r].at(i), o[i]);
+            }
+        }
+    }
+    // merge the warps
+    if (lane == 0) m_s[warp] = m, l_s[warp] = l;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) o_s[warp][lane * VEC + i] = o[i];
+    __syncthreads();
+    if (warp == 0) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, m_s[w]);
+        float Lsum = 0.f, acc[VEC];
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) {
+            const float f = m_s[w] == -INFINITY ? 0.f : exp2f(m_s[w] - M);
+            Lsum += f * l_s[w];
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) acc[i] += f * o_s[w][lane * VEC + i];
+        }
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        const size_t oo = (static_cast<size_t>(b) * p.Hq + h) * D + lane * VEC;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            if constexpr (BF16)
+                static_cast<__nv_bfloat16*>(p.out)[oo + i] = __float2bfloat16(acc[i] * inv);
+            else
+                static_cast<float*>(p.out)[oo + i] = acc[i] * inv;
+        }
+        if (p.lse_out && lane == 0)
+            p.lse_out[static_cast<size_t>(b) * p.Hq + h] = (M + log2f(Lsum)) / kQLog2e;
+    }
+}
+
+}  // namespace
+
+#define KVD_QUEST_DISPATCH(KERNEL, GRID, BLOCK, SMEM)                                          \
+    do {                                                                                       \
+        cudaError_t e_ = cudaErrorInvalidValue;                                                \
+        if (p.dtype == KVD_BF16 && p.D == 64)                                                  \
+            e_ = launch_kernel(KERNEL<2, true>, GRID, BLOCK, SMEM, stream, p);                 \
+        else if (p.dtype == KVD_BF16 && p.D == 128)                                            \
+            e_ = launch_kernel(KERNEL<4, true>, GRID, BLOCK, SMEM, stream, p);                 \
+        else if (p.dtype == KVD_F32 && p.D == 64)                                              \
+            e_ = launch_kernel(KERNEL<2, false>, GRID, BLOCK, SMEM, stream, p);                \
+        else if (p.dtype == KVD_F32 && p.D == 128)                                             \
+            e_ = launch_kernel(KERNEL<4, false>, GRID, BLOCK, SMEM, stream, p);                \
+        else                                                                                   \
+            return KVD_ERR_UNSUPPORTED;                                                        \
+        if (e_ != cudaSuccess) return KVD_ERR_CUDA;                                            \
+    } while (0)
+
+int quest_minmax_launch(const QuestParams& p, cudaStream_t stream) {
+    const long long warps = static_cast<long long>(p.n_list) * p.Hkv;
+    const dim3 grid(static_cast<unsigned>((warps + 7) / 8)), block(256);
+    KVD_QUEST_DISPATCH(quest_minmax_kernel, grid, block, 0);
+    return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
+}
+
+size_t quest_select_smem(int Hq, int Hkv, int max_pages) {
+    (void)Hq;
+    (void)Hkv;
+    return sizeof(float) * static_cast<size_t>(kChooseWarps) * max_pages;
+}
+
+template <int VEC, bool BF16>
+static cudaError_t bounds_launch(const QuestParams& p, dim3 grid, cudaStream_t stream) {
+    const int G = p.Hq / p.Hkv;
+    const dim3 block(kBoundWarps * 32);
+    if (G <= 1) return launch_kernel(quest_bounds_kernel<VEC, BF16, 1>, grid, block, 0, stream, p);
+    if (G <= 2) return launch_kernel(quest_bounds_kernel<VEC, BF16, 2>, grid, block, 0, stream, p);
+    if (G <= 4) return launch_kernel(quest_bounds_kernel<VEC, BF16, 4>, grid, block, 0, stream, p);
+    if (G <= 8) return launch_kernel(quest_bounds_kernel<VEC, BF16, 8>, grid, block, 0, stream, p);
+    return launch_kernel(quest_bounds_kernel<VEC, BF16, 16>, grid, block, 0, stream, p);
+}
+
+int quest_select_launch(const QuestParams& p, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>(p.B * p.Hkv),
+                    static_cast<unsigned>((p.max_pages + 32 * kBoundWarps - 1) / (32 * kBoundWarps)));
+    cudaError_t e = cudaErrorInvalidValue;
+    if (p.dtype == KVD_BF16 && p.D == 64) e = bounds_launch<2, true>(p, grid, stream);
+    else if (p.dtype == KVD_BF16 && p.D == 128) e = bounds_launch<4, true>(p, grid, stream);
+    else if (p.dtype == KVD_F32 && p.D == 64) e = bounds_launch<2, false>(p, grid, stream);
+    else if (p.dtype == KVD_F32 && p.D == 128) e = bounds_launch<4, false>(p, grid, stream);
+    else return KVD_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return KVD_ERR_CUDA;
+    const size_t smem = quest_select_smem(p.Hq, p.Hkv, p.max_pages);
+    static size_t configured = 0;
+    if (smem > 48 * 1024 && configured < smem) {
+        if (cudaFuncSetAttribute(quest_choose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return KVD_ERR_CUDA;
+        configured = smem;
+    }
+    const unsigned blocks = static_cast<unsigned>((p.B * p.Hq + kChooseWarps - 1) / kChooseWarps);
+    if (launch_kernel(quest_choose_kernel, dim3(blocks), dim3(kChooseWarps * 32), smem, stream, p) !=
+        cudaSuccess)
+        return KVD_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
+}
+
+int quest_attn_launch(const QuestParams& p, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>(p.B * p.Hq)), block(kAttnWarps * 32);
+    KVD_QUEST_DISPATCH(quest_attn_kernel, grid, block, 0);
+    return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
+}
+
+}  // namespace kvd

@@ -1,0 +1,138 @@
+"""GPU parity of Quest page selection (summaries, choice, attention over the chosen pages)
+against the oracle, through the C ABI.
+
+* Summaries: bit-exact (minimum and maximum of stored values).
+* Bounds: the GPU sums d products in float32, the oracle in fp64: |dU| <= 2^-20 * sum|terms|
+  (the float32 sum of D terms, each term exact or rounded once).
+* Choice: the GPU's pages must equal the oracle's, except across a near-tie of the n_sel-th
+  bound (within the bound's tolerance), where any page whose oracle bound reaches the
+  n_sel-th bound minus that tolerance is valid.
+* Attention: for every (sequence, head) whose choice equals the oracle's, the attention bar
+  of the other decode kernels (tests/parity.py).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.parity import assert_attn_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def kvd():
+    import kv_cache_decode_split_gb300 as m
+    return m
+
+
+def _gpu(kvd, x, n_sel):
+    q, kp, vp = x.q.to(DEV), x.k_pool.to(DEV), x.v_pool.to(DEV)
+    bt, sl = x.block_table.to(DEV), x.seq_lens.to(DEV)
+    kmin, kmax, err = kvd.quest_page_minmax(kp)
+    ub = torch.full((x.B, x.Hq, x.max_pages), 7.0, device=DEV)
+    sel = kvd.quest_select_pages(q, kmin, kmax, bt, sl, n_sel, x.page_size, ub_out=ub, err=err)
+    lse = torch.empty(x.B, x.Hq, device=DEV)
+    out = kvd.attn_decode_quest(q, kp, vp, bt, sl, sel, scale=x.scale, lse_out=lse, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return kmin.cpu(), kmax.cpu(), sel.cpu().numpy(), ub.cpu().double().numpy(), out, lse
+
+
+def _bound_tol(x):
+    # sum over d of |q_d| max(|kmin_d|, |kmax_d|) bounds the terms of every page's bound
+    q = x.q.double().abs().numpy()
+    kabs = x.k_pool.double().abs().amax(2).numpy()       # [pages, Hkv, D] >= |kmin|, |kmax|
+    G = x.Hq // x.Hkv
+    worst = np.einsum("bhd,phd->bhp", q, kabs[:, np.arange(x.Hq) // G]).max()
+    return 2.0 ** -20 * worst + 1e-30
+
+
+def _check(kvd, x, n_sel, min_compared=0.9):
+    kmin, kmax, sel, ub, out, lse = _gpu(kvd, x, n_sel)
+    rmin, rmax = oracle.quest_minmax(x.k_pool)
+    assert np.array_equal(kmin.double().numpy(), rmin) and np.array_equal(kmax.double().numpy(), rmax)
+    ref, ref_lse, ref_sel, ref_ub = oracle.quest(x.q, x.k_pool, x.v_pool, x.block_table,
+                                                 x.seq_lens, x.scale, n_sel)
+    tol = _bound_tol(x)
+    finite = ~np.isnan(ref_ub)
+    assert np.array_equal(np.isnan(ub), ~finite)
+    assert np.abs(ub[finite] - ref_ub[finite]).max(initial=0.0) <= tol
+    same = np.zeros((x.B, x.Hq), dtype=bool)
+    for b in range(x.B):
+        full = int(x.seq_lens[b]) // x.page_size
+        for h in range(x.Hq):
+            if np.array_equal(sel[b, h], ref_sel[b, h]):
+                same[b, h] = True
+                continue
+            u = ref_ub[b, h, :full]
+            kth = np.sort(u)[::-1][min(n_sel, full) - 1]
+            got = sel[b, h][sel[b, h] >= 0]
+            assert len(got) == min(n_sel, full) and len(set(got.tolist())) == len(got)
+            assert (u[got] >= kth - 2 * tol).all(), (b, h)
+    assert same.mean() >= min_compared, same.mean()
+    bi, hi = np.nonzero(same)
+    assert_attn_close(out.cpu()[bi, hi], ref[bi, hi], what="quest")
+    assert np.abs(lse.cpu().double().numpy()[bi, hi] - ref_lse[bi, hi]).max() < 2e-3
+
+
+@pytest.mark.parametrize("D,P,n_sel", [(128, 16, 16), (64, 16, 4), (128, 32, 1), (64, 8, 64)])
+def test_quest_bf16(kvd, D, P, n_sel):
+    lens = [1, 7, P, P + 1, 5 * P, 300, 1000, 2047]
+    x = W.make_gqa(len(lens), 16, 4, D, lens, page_size=P, shuffle=True, extra_pages=4,
+                   seed=9000 + D + P + n_sel)
+    _check(kvd, x, n_sel)
+
+
+def test_quest_fp32(kvd):
+    lens = [5, 64, 333]
+    x = W.make_gqa(3, 8, 2, 64, lens, page_size=16, shuffle=True, seed=9100,
+                   dtype=torch.float32)
+    _check(kvd, x, 6)
+
+
+def test_quest_every_page_is_dense(kvd):
+    lens = [100, 64, 1000]
+    x = W.make_gqa(3, 32, 8, 128, lens, page_size=16, shuffle=True, seed=9200)
+    _, _, _, _, out, _ = _gpu(kvd, x, 64)
+    ref, _ = oracle.gqa(x.q, x.k_pool, x.v_pool, x.block_table, x.seq_lens, x.scale)
+    assert_attn_close(out, ref, what="all pages (at most 64 full pages)")
+
+
+def test_quest_full_size_sampled(kvd):
+    x = W.build("quest_llama3")
+    n_sel = W.WORKLOADS["quest_llama3"].params["n_sel"]
+    kmin, kmax, sel, ub, out, _ = _gpu(kvd, x, n_sel)
+    pairs = [(b, h) for b in (0, 13, 31) for h in (0, 5, 31)]
+    ref, _, ref_sel, _ = oracle.quest(x.q, x.k_pool, x.v_pool, x.block_table, x.seq_lens,
+                                      x.scale, n_sel, pairs=pairs)
+    for i, (b, h) in enumerate(pairs):
+        if np.array_equal(sel[b, h], ref_sel[i]):
+            assert_attn_close(out[b, h][None].cpu(), ref[i][None], what=f"({b},{h})")
+
+
+def test_quest_summaries_of_listed_pages_only(kvd):
+    x = W.make_gqa(2, 8, 2, 64, [64, 64], page_size=16, seed=9300)
+    kp = x.k_pool.to(DEV)
+    kmin = torch.full((x.num_pages, 2, 64), 5.0, dtype=torch.bfloat16, device=DEV)
+    kmax = kmin.clone()
+    pages = torch.tensor([1, 6], dtype=torch.int32, device=DEV)
+    _, _, err = kvd.quest_page_minmax(kp, kmin, kmax, pages=pages)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rmin, rmax = oracle.quest_minmax(x.k_pool, [1, 6])
+    got = kmin.cpu().double().numpy()
+    assert np.array_equal(got[[1, 6]], rmin)
+    assert (got[[0, 2, 3, 4, 5, 7]] == 5.0).all()
+
+
+def test_quest_bad_selection_entry_is_flagged(kvd):
+    x = W.make_gqa(1, 4, 1, 64, [64], page_size=16, seed=9400)
+    sel = torch.tensor([[[0, 9], [1, 2], [0, 3], [2, 3]]], dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kvd.attn_decode_quest(x.q.to(DEV), x.k_pool.to(DEV), x.v_pool.to(DEV),
+                          x.block_table.to(DEV), x.seq_lens.to(DEV), sel, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == -6

@@ -220,7 +220,7 @@ def make_indexer(B, seq_lens, *, Hi=64, Di=128, k=2048, page_size=64, max_pages=
 class Workload:
     name: str
     wid: int
-    kind: str               # "gqa" | "swa" | "mla" | "dsa" | "dsa_fp8" | "delta"
+    kind: str               # "gqa" | "swa" | "mla" | "dsa" | "dsa_fp8" | "delta" | "quest"
     params: dict = field(default_factory=dict)
     description: str = ""
 
@@ -253,6 +253,13 @@ WORKLOADS = {
              page_size=64, ring=True),
         "sliding window W=4096 plus the first 4 tokens on rolling caches of 4100 slots "
         "(O(W) memory), bf16, B=8 Hq=64 Hkv=8 D=64, true length 32768"),
+    "quest_llama3": Workload(
+        "quest_llama3", 9, "quest",
+        dict(B=32, Hq=32, Hkv=8, D=128, L_lo=4096, L_hi=8192, page_size=16, max_pages=512,
+             shuffle=True, extra_pages=64, n_sel=16),
+        "Quest page selection on the Llama-3-8B-shaped GQA cache with 16-token pages "
+        "(L ~ U[4096, 8192]): per-head bounds from page min/max keys, the best 16 pages "
+        "(256 tokens) plus the partial tail, attention over them"),
     "mla_dsv3": Workload(
         "mla_dsv3", 4, "mla",
         dict(B=16, H=128, L=16384, page_size=64, factor=0.1),
@@ -356,7 +363,7 @@ def build(name: str, *, sharp: bool = False):
     if w.kind == "gqa" and p.get("dtype") == "fp32":
         return make_gqa(p["B"], p["Hq"], p["Hkv"], p["D"], [p["L"]] * p["B"],
                         page_size=p["page_size"], dtype=torch.float32, seed=base)
-    if w.kind == "gqa":
+    if w.kind in ("gqa", "quest"):
         lens = uniform_int(p["L_lo"], p["L_hi"], p["B"], base + 9)
         return make_gqa(p["B"], p["Hq"], p["Hkv"], p["D"], lens, page_size=p["page_size"],
                         max_pages=p["max_pages"], shuffle=p["shuffle"],
