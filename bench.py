@@ -522,7 +522,7 @@ class DeltaRunner:
 class QuestRunner(GqaRunner):
     """quest_select_pages then attn_decode_quest (page summaries computed once, at set-up,
     as pages fill in a real decode)."""
-    launches_per_step = 3          # bounds, choice, attention
+    launches_per_step = 2          # bounds; choice + attention
     kernel = "quest_attn_kernel"
 
     def __init__(self, name, dev):
@@ -555,10 +555,11 @@ class QuestRunner(GqaRunner):
         x = self.x
         q = self.q if q is None else q
         out = self.out if out is None else out
-        self.kvd.quest_select_pages(q, self.kmin, self.kmax, self.bt, self.sl, self.n_sel,
-                                    x.page_size, sel=self.sel, ub_out=self.ub, err=self.err)
-        return self.kvd.attn_decode_quest(q, self.k, self.v, self.bt, self.sl, self.sel,
-                                          scale=x.scale, out=out, err=self.err)
+        self.kvd.quest_page_bounds(q, self.kmin, self.kmax, self.bt, self.sl, x.page_size,
+                                   ub=self.ub, err=self.err)
+        return self.kvd.attn_decode_quest_from_bounds(q, self.k, self.v, self.bt, self.sl,
+                                                      self.ub, self.n_sel, scale=x.scale,
+                                                      sel_out=self.sel, out=out, err=self.err)[0]
 
     def oracle_sample(self, budget_s):
         import numpy as np

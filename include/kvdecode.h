@@ -36,7 +36,8 @@
  *    read from the rolling cache. "Attention Optimizations", DSA / Computation
  *    Path (update_cache before attention) and Sliding-window (a rolling buffer
  *    of W entries); "All the attentions", section 4.
- *  - quest_page_minmax, quest_select_pages, attn_decode_quest: query-aware page
+ *  - quest_page_minmax, quest_select_pages, attn_decode_quest (and the split
+ *    quest_page_bounds + attn_decode_quest_from_bounds): query-aware page
  *    selection. "Long context, KV eviction and sparse attention", Sparse attention
  *    (Quest: per-page key bounds, the best pages, attention over them).
  *  - kvd_delta_decode_step: one Gated DeltaNet / KDA decode step on each head's
@@ -262,6 +263,30 @@ int attn_decode_quest(const void *q, const void *k_pool, const void *v_pool,
                       void *out, float *lse_out, int B, int Hq, int Hkv, int D, int page_size,
                       int max_pages, int num_pages, int n_sel, float scale, int dtype, int *err,
                       cudaStream_t stream);
+
+/*
+ * The bound step of quest_select_pages alone: ub [B, Hq, max_pages] float32 (device,
+ * caller-owned) receives each query head's page bounds U (NaN past the full pages).
+ * Arguments, support and errors as quest_select_pages. One launch.
+ */
+int quest_page_bounds(const void *q, const void *kmin, const void *kmax,
+                      const int32_t *block_table, const int32_t *seq_lens, float *ub, int B,
+                      int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                      int dtype, int *err, cudaStream_t stream);
+
+/*
+ * Choice and attention in one launch: each query head takes the n_sel largest of its bounds
+ * ub (as quest_page_bounds writes them; ties to the lower page), writes them to sel_out
+ * [B, Hq, n_sel] (ascending, -1 padded, exactly as quest_select_pages would), and attends
+ * over those pages and the tail as attn_decode_quest does. Supported: as attn_decode_quest,
+ * max_pages <= 51200. One launch.
+ */
+int attn_decode_quest_from_bounds(const void *q, const void *k_pool, const void *v_pool,
+                                  const int32_t *block_table, const int32_t *seq_lens,
+                                  const float *ub, int32_t *sel_out, void *out, float *lse_out,
+                                  int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                                  int num_pages, int n_sel, float scale, int dtype, int *err,
+                                  cudaStream_t stream);
 
 /*
  * Absorbed MLA decode over all cached tokens.

@@ -36,7 +36,8 @@ __all__ = [
     "attn_decode_gqa_paged", "attn_decode_swa_sink", "attn_decode_mla", "dsa_indexer_topk",
     "dsa_indexer_topk_fp8", "quantize_e4m3_rows", "dsa_indexer_cache_append_fp8",
     "delta_decode_step", "attn_decode_swa_ring", "cache_append", "quest_page_minmax",
-    "quest_select_pages", "attn_decode_quest",
+    "quest_select_pages", "attn_decode_quest", "quest_page_bounds",
+    "attn_decode_quest_from_bounds",
     "dsa_topk", "attn_decode_mla_sparse", "kvd_workspace_size", "kvd_check_device_error",
     "Workspace", "KvdError",
 ]
@@ -308,6 +309,47 @@ def attn_decode_quest(q, k_pool, v_pool, block_table, seq_lens, sel, scale=None,
                                _stream(stream))
     _check(st, "attn_decode_quest")
     return out
+
+
+def quest_page_bounds(q, kmin, kmax, block_table, seq_lens, page_size, ub=None, err=None,
+                      stream=None):
+    """Each query head's page bounds: ub [B, Hq, max_pages] float32 (NaN past full pages)."""
+    _need(q, "q", dim=3)
+    _need(kmin, "kmin", q.dtype, 3)
+    _need(kmax, "kmax", q.dtype, 3)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, Hq, D = q.shape
+    num_pages, Hkv, _ = kmin.shape
+    max_pages = block_table.shape[1]
+    ub = torch.empty(B, Hq, max_pages, dtype=torch.float32, device=q.device) if ub is None else ub
+    err = _err(err, q.device)
+    st = lib.quest_page_bounds(_p(q), _p(kmin), _p(kmax), _p(block_table), _p(seq_lens), _p(ub),
+                               B, Hq, Hkv, D, int(page_size), max_pages, num_pages, _DT[q.dtype],
+                               _p(err), _stream(stream))
+    _check(st, "quest_page_bounds")
+    return ub
+
+
+def attn_decode_quest_from_bounds(q, k_pool, v_pool, block_table, seq_lens, ub, n_sel,
+                                  scale=None, sel_out=None, out=None, lse_out=None, err=None,
+                                  stream=None):
+    """Choice of each head's n_sel best pages from ub and attention over them, one launch.
+    Returns (out, sel_out)."""
+    B, Hq, Hkv, D, P, max_pages, num_pages = _gqa_args(q, k_pool, v_pool, block_table, seq_lens)
+    _need(ub, "ub", torch.float32, 3)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    sel_out = (torch.empty(B, Hq, n_sel, dtype=torch.int32, device=q.device)
+               if sel_out is None else sel_out)
+    err = _err(err, q.device)
+    st = lib.attn_decode_quest_from_bounds(_p(q), _p(k_pool), _p(v_pool), _p(block_table),
+                                           _p(seq_lens), _p(ub), _p(sel_out), _p(out),
+                                           _p(lse_out), B, Hq, Hkv, D, P, max_pages, num_pages,
+                                           int(n_sel), scale, _DT[q.dtype], _p(err),
+                                           _stream(stream))
+    _check(st, "attn_decode_quest_from_bounds")
+    return out, sel_out
 
 
 def _mla_args(q, c_pool, block_table, seq_lens):

@@ -26,6 +26,8 @@ EXPORTS = (
     "quest_page_minmax",
     "quest_select_pages",
     "attn_decode_quest",
+    "quest_page_bounds",
+    "attn_decode_quest_from_bounds",
     "dsa_topk",
     "attn_decode_mla_sparse",
     "kvd_workspace_size",
@@ -69,6 +71,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.quest_select_pages.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P]
     lib.attn_decode_quest.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P,
                                       P]
+    lib.quest_page_bounds.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, P]
+    lib.attn_decode_quest_from_bounds.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I,
+                                                  I, I, F, I, P, P]
     lib.dsa_topk.argtypes = [P, P, P, P, I, I, I, P, Z, P]
     lib.attn_decode_mla_sparse.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P,
                                            Z, P]
@@ -76,7 +81,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                  "dsa_indexer_topk", "dsa_indexer_topk_fp8", "kvd_quantize_e4m3_rows",
                  "dsa_indexer_cache_append_fp8", "kvd_delta_decode_step",
                  "attn_decode_swa_ring", "kvd_cache_append", "quest_page_minmax",
-                 "quest_select_pages", "attn_decode_quest", "dsa_topk",
+                 "quest_select_pages", "attn_decode_quest", "quest_page_bounds",
+                 "attn_decode_quest_from_bounds", "dsa_topk",
                  "attn_decode_mla_sparse",
                  "kvd_check_device_error"):
         getattr(lib, name).restype = I

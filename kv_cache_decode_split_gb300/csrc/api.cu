@@ -521,7 +521,59 @@ int attn_decode_quest(const void* q, const void* k_pool, const void* v_pool,
     qp.lse_out = lse_out;
     qp.n_sel = n_sel;
     qp.scale = scale;
-    return quest_attn_launch(qp, stream);
+    return quest_attn_launch(qp, false, stream);
+}
+
+int quest_page_bounds(const void* q, const void* kmin, const void* kmax,
+                      const int32_t* block_table, const int32_t* seq_lens, float* ub, int B,
+                      int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                      int dtype, int* err, cudaStream_t stream) {
+    if (!q || !kmin || !kmax || !block_table || !seq_lens || !ub) return KVD_ERR_INVALID_ARG;
+    QuestParams qp;
+    const int st = quest_common(qp, B, Hq, Hkv, D, page_size, max_pages, num_pages, dtype, err);
+    if (st != KVD_OK) return st;
+    if (!aligned16(q) || !aligned16(kmin) || !aligned16(kmax) ||
+        (reinterpret_cast<uintptr_t>(ub) & 3))
+        return KVD_ERR_INVALID_ARG;
+    qp.q = q;
+    qp.kmin = const_cast<void*>(kmin);
+    qp.kmax = const_cast<void*>(kmax);
+    qp.block_table = block_table;
+    qp.seq_lens = seq_lens;
+    qp.ub_out = ub;
+    return quest_bounds_launch(qp, stream);
+}
+
+int attn_decode_quest_from_bounds(const void* q, const void* k_pool, const void* v_pool,
+                                  const int32_t* block_table, const int32_t* seq_lens,
+                                  const float* ub, int32_t* sel_out, void* out, float* lse_out,
+                                  int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                                  int num_pages, int n_sel, float scale, int dtype, int* err,
+                                  cudaStream_t stream) {
+    if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !ub || !sel_out || !out)
+        return KVD_ERR_INVALID_ARG;
+    QuestParams qp;
+    const int st = quest_common(qp, B, Hq, Hkv, D, page_size, max_pages, num_pages, dtype, err);
+    if (st != KVD_OK) return st;
+    if (n_sel < 1 || n_sel > 64) return KVD_ERR_UNSUPPORTED;
+    if ((size_t)max_pages * 4 > 200 * 1024) return KVD_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return KVD_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(ub) & 3) || (reinterpret_cast<uintptr_t>(sel_out) & 3) ||
+        (reinterpret_cast<uintptr_t>(lse_out) & 3))
+        return KVD_ERR_INVALID_ARG;
+    qp.q = q;
+    qp.k_pool = k_pool;
+    qp.v_pool = v_pool;
+    qp.block_table = block_table;
+    qp.seq_lens = seq_lens;
+    qp.ub_out = const_cast<float*>(ub);
+    qp.sel = sel_out;
+    qp.out = out;
+    qp.lse_out = lse_out;
+    qp.n_sel = n_sel;
+    qp.scale = scale;
+    return quest_attn_launch(qp, true, stream);
 }
 
 int attn_decode_mla(const void* q, const void* c_pool, const int32_t* block_table,

@@ -167,8 +167,9 @@ struct QuestParams {
 };
 int quest_minmax_launch(const QuestParams& p, cudaStream_t stream);
 size_t quest_select_smem(int Hq, int Hkv, int max_pages);
-int quest_select_launch(const QuestParams& p, cudaStream_t stream);
-int quest_attn_launch(const QuestParams& p, cudaStream_t stream);
+int quest_bounds_launch(const QuestParams& p, cudaStream_t stream);
+int quest_select_launch(const QuestParams& p, cudaStream_t stream);   // bounds, then choice
+int quest_attn_launch(const QuestParams& p, bool choose, cudaStream_t stream);
 int topk_launch(const TopkParams& p, bool need_hist, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------------------

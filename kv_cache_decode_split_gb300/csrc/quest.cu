@@ -162,7 +162,6 @@ __global__ void __launch_bounds__(256) quest_minmax_kernel(const QuestParams p) 
 // 32 pages: their page ids in one load, then kPagesInFlight pages' summaries at once, and
 // for each page the bounds of the KG (>= G) query heads of the group by warp sums.
 constexpr int kBoundWarps = 4;
-constexpr int kPagesInFlight = 8;
 
 template <int VEC, bool BF16, int KG>
 __global__ void __launch_bounds__(kBoundWarps * 32) quest_bounds_kernel(const QuestParams p) {
@@ -190,10 +189,14 @@ __global__ void __launch_bounds__(kBoundWarps * 32) quest_bounds_kernel(const Qu
     const int pg_lane =
         my < full ? load_page(p.block_table, p.max_pages, p.num_pages, b, my, p.err) : 0;
     const int n_here = min(32, full - m0);
-    for (int c = 0; c < n_here; c += kPagesInFlight) {
-        Raw<VEC, BF16> lo[kPagesInFlight], hi[kPagesInFlight];
+    // 32 / KG pages at a time: their 32 (page, head) partial sums are reduced across the
+    // warp together by a transposing butterfly (31 shuffles for all 32 sums; lane i ends
+    // with sum i), instead of five shuffle levels per sum
+    constexpr int NP = 32 / KG;
+    for (int c = 0; c < n_here; c += NP) {
+        Raw<VEC, BF16> lo[NP], hi[NP];
 #pragma unroll
-        for (int k = 0; k < kPagesInFlight; ++k) {
+        for (int k = 0; k < NP; ++k) {
             const int pg = __shfl_sync(0xffffffffu, pg_lane, (c + k) & 31);
             if (c + k < n_here) {
                 const size_t o = (static_cast<size_t>(pg) * p.Hkv + g) * D + lane * VEC;
@@ -201,26 +204,31 @@ __global__ void __launch_bounds__(kBoundWarps * 32) quest_bounds_kernel(const Qu
                 hi[k].load(p.kmax, o);
             }
         }
+        float v[32];  // v[k * KG + j]: page c + k, head j
 #pragma unroll
-        for (int k = 0; k < kPagesInFlight; ++k) {
-            if (c + k >= n_here) break;
-            float u[KG];
+        for (int k = 0; k < NP; ++k)
 #pragma unroll
             for (int j = 0; j < KG; ++j) {
-                u[j] = 0.f;
+                float a = 0.f;
+                if (c + k < n_here)
 #pragma unroll
-                for (int i = 0; i < VEC; ++i)
-                    u[j] += fmaxf(q[j][i] * lo[k].at(i), q[j][i] * hi[k].at(i));
+                    for (int i = 0; i < VEC; ++i)
+                        a += fmaxf(q[j][i] * lo[k].at(i), q[j][i] * hi[k].at(i));
+                v[k * KG + j] = a;
             }
 #pragma unroll
-            for (int off = 16; off; off >>= 1)
+        for (int sft = 16; sft >= 1; sft >>= 1) {
+            const bool upper = (lane & sft) != 0;
 #pragma unroll
-                for (int j = 0; j < KG; ++j) u[j] += __shfl_xor_sync(0xffffffffu, u[j], off);
-            // lane j writes head j's bound
-#pragma unroll
-            for (int j = 0; j < KG; ++j)
-                if (lane == j && j < G) ub[static_cast<size_t>(j) * p.max_pages + m0 + c + k] = u[j];
+            for (int i = 0; i < sft; ++i) {
+                const float send = upper ? v[i] : v[i + sft];
+                const float keep = upper ? v[i + sft] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, sft);
+            }
         }
+        // lane i holds the sum of page c + i / KG, head i % KG
+        const int k = lane / KG, j = lane % KG;
+        if (c + k < n_here && j < G) ub[static_cast<size_t>(j) * p.max_pages + m0 + c + k] = v[0];
     }
 }
 
@@ -230,21 +238,11 @@ __global__ void __launch_bounds__(kBoundWarps * 32) quest_bounds_kernel(const Qu
 // bound set to -inf; the chosen pages are written in ascending order.
 constexpr int kChooseWarps = 4;
 
-__global__ void __launch_bounds__(kChooseWarps * 32) quest_choose_kernel(const QuestParams p) {
-    extern __shared__ float ubs[];  // [kChooseWarps][max_pages]
-    griddep_wait();
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int bh = blockIdx.x * kChooseWarps + warp;
-    if (bh >= p.B * p.Hq) return;
-    const int b = bh / p.Hq;
-    const int L = load_len(p.seq_lens, b, p.max_len, p.err);
-    const int full = L / p.page_size;
-    float* u = ubs + static_cast<size_t>(warp) * p.max_pages;
-    const float* src = p.ub_out + static_cast<size_t>(bh) * p.max_pages;
-    for (int m = lane; m < full; m += 32) u[m] = src[m];
-    __syncwarp();
-    int32_t* out = p.sel + static_cast<size_t>(bh) * p.n_sel;
-    const int n_take = min(full, p.n_sel);
+// One warp: the n_sel best of the bounds u[0..full) (shared memory, consumed), written to
+// out[0..n_sel) in ascending order, -1 padded.
+__device__ __forceinline__ void choose_pages(float* u, int full, int n_sel, int32_t* out) {
+    const int lane = threadIdx.x % 32;
+    const int n_take = min(full, n_sel);
     int mine0 = -1, mine1 = -1;  // this lane's picks: rounds lane and lane + 32
     for (int r = 0; r < n_take; ++r) {
         float best = -INFINITY;
@@ -275,15 +273,35 @@ __global__ void __launch_bounds__(kChooseWarps * 32) quest_choose_kernel(const Q
     }
     if (lane < n_take) out[rank0] = mine0;
     if (lane + 32 < n_take) out[rank1] = mine1;
-    for (int r = n_take + lane; r < p.n_sel; r += 32) out[r] = -1;
+    for (int r = n_take + lane; r < n_sel; r += 32) out[r] = -1;
+}
+
+__global__ void __launch_bounds__(kChooseWarps * 32) quest_choose_kernel(const QuestParams p) {
+    extern __shared__ float ubs[];  // [kChooseWarps][max_pages]
+    griddep_wait();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int bh = blockIdx.x * kChooseWarps + warp;
+    if (bh >= p.B * p.Hq) return;
+    const int b = bh / p.Hq;
+    const int L = load_len(p.seq_lens, b, p.max_len, p.err);
+    const int full = L / p.page_size;
+    float* u = ubs + static_cast<size_t>(warp) * p.max_pages;
+    const float* src = p.ub_out + static_cast<size_t>(bh) * p.max_pages;
+    for (int m = lane; m < full; m += 32) u[m] = src[m];
+    __syncwarp();
+    choose_pages(u, full, p.n_sel, p.sel + static_cast<size_t>(bh) * p.n_sel);
 }
 
 // ---------------------------------------------------------------------------- attention
-template <int VEC, bool BF16>
+// CHOOSE: warp 0 first picks the head's pages from its bounds (p.ub_out), writes them to
+// p.sel for the caller, and the CTA attends over them (no separate choice launch).
+template <int VEC, bool BF16, bool CHOOSE>
 __global__ void __launch_bounds__(kAttnWarps * 32) quest_attn_kernel(const QuestParams p) {
     constexpr int D = VEC * 32;
     __shared__ float m_s[kAttnWarps], l_s[kAttnWarps];
     __shared__ float o_s[kAttnWarps][D];
+    __shared__ int32_t sel_s[64];
+    extern __shared__ float ubrow[];  // CHOOSE: the head's bounds [max_pages]
     griddep_wait();
     const int b = blockIdx.x / p.Hq, h = blockIdx.x % p.Hq;
     const int g = h / (p.Hq / p.Hkv);
@@ -293,6 +311,19 @@ __global__ void __launch_bounds__(kAttnWarps * 32) quest_attn_kernel(const Quest
     const int n_take = min(full, p.n_sel);
     const int tail = L - full * p.page_size;
     const int32_t* sel = p.sel + (static_cast<size_t>(b) * p.Hq + h) * p.n_sel;
+    if constexpr (CHOOSE) {
+        if (warp == 0) {
+            const float* src = p.ub_out + (static_cast<size_t>(b) * p.Hq + h) * p.max_pages;
+            for (int m = lane; m < full; m += 32) ubrow[m] = src[m];
+            __syncwarp();
+            choose_pages(ubrow, full, p.n_sel, sel_s);
+            __syncwarp();
+            int32_t* dst = p.sel + (static_cast<size_t>(b) * p.Hq + h) * p.n_sel;
+            for (int r = lane; r < p.n_sel; r += 32) dst[r] = sel_s[r];
+        }
+        __syncthreads();
+        sel = sel_s;
+    }
 
     float q[VEC];
     load_vec<VEC, BF16>(p.q, (static_cast<size_t>(b) * p.Hq + h) * D + lane * VEC, q);
@@ -437,7 +468,7 @@ static cudaError_t bounds_launch(const QuestParams& p, dim3 grid, cudaStream_t s
     return launch_kernel(quest_bounds_kernel<VEC, BF16, 16>, grid, block, 0, stream, p);
 }
 
-int quest_select_launch(const QuestParams& p, cudaStream_t stream) {
+int quest_bounds_launch(const QuestParams& p, cudaStream_t stream) {
     const dim3 grid(static_cast<unsigned>(p.B * p.Hkv),
                     static_cast<unsigned>((p.max_pages + 32 * kBoundWarps - 1) / (32 * kBoundWarps)));
     cudaError_t e = cudaErrorInvalidValue;
@@ -447,6 +478,12 @@ int quest_select_launch(const QuestParams& p, cudaStream_t stream) {
     else if (p.dtype == KVD_F32 && p.D == 128) e = bounds_launch<4, false>(p, grid, stream);
     else return KVD_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return KVD_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
+}
+
+int quest_select_launch(const QuestParams& p, cudaStream_t stream) {
+    const int st = quest_bounds_launch(p, stream);
+    if (st != KVD_OK) return st;
     const size_t smem = quest_select_smem(p.Hq, p.Hkv, p.max_pages);
     static size_t configured = 0;
     if (smem > 48 * 1024 && configured < smem) {
@@ -462,10 +499,39 @@ int quest_select_launch(const QuestParams& p, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
 
-int quest_attn_launch(const QuestParams& p, cudaStream_t stream) {
+template <bool CHOOSE>
+static int attn_launch(const QuestParams& p, cudaStream_t stream) {
     const dim3 grid(static_cast<unsigned>(p.B * p.Hq)), block(kAttnWarps * 32);
-    KVD_QUEST_DISPATCH(quest_attn_kernel, grid, block, 0);
+    const size_t smem = CHOOSE ? sizeof(float) * static_cast<size_t>(p.max_pages) : 0;
+    if (smem > 48 * 1024) {
+        static size_t configured = 0;
+        if (configured < smem) {
+            cudaError_t e = cudaSuccess;
+            if (p.dtype == KVD_BF16 && p.D == 64) e = cudaFuncSetAttribute(quest_attn_kernel<2, true, CHOOSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (p.dtype == KVD_BF16 && p.D == 128) e = cudaFuncSetAttribute(quest_attn_kernel<4, true, CHOOSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (p.dtype == KVD_F32 && p.D == 64) e = cudaFuncSetAttribute(quest_attn_kernel<2, false, CHOOSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (p.dtype == KVD_F32 && p.D == 128) e = cudaFuncSetAttribute(quest_attn_kernel<4, false, CHOOSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (e != cudaSuccess) return KVD_ERR_CUDA;
+            configured = smem;
+        }
+    }
+    cudaError_t e;
+    if (p.dtype == KVD_BF16 && p.D == 64)
+        e = launch_kernel(quest_attn_kernel<2, true, CHOOSE>, grid, block, smem, stream, p);
+    else if (p.dtype == KVD_BF16 && p.D == 128)
+        e = launch_kernel(quest_attn_kernel<4, true, CHOOSE>, grid, block, smem, stream, p);
+    else if (p.dtype == KVD_F32 && p.D == 64)
+        e = launch_kernel(quest_attn_kernel<2, false, CHOOSE>, grid, block, smem, stream, p);
+    else if (p.dtype == KVD_F32 && p.D == 128)
+        e = launch_kernel(quest_attn_kernel<4, false, CHOOSE>, grid, block, smem, stream, p);
+    else
+        return KVD_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return KVD_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
+}
+
+int quest_attn_launch(const QuestParams& p, bool choose, cudaStream_t stream) {
+    return choose ? attn_launch<true>(p, stream) : attn_launch<false>(p, stream);
 }
 
 }  // namespace kvd

@@ -36,8 +36,17 @@ def _gpu(kvd, x, n_sel):
     sel = kvd.quest_select_pages(q, kmin, kmax, bt, sl, n_sel, x.page_size, ub_out=ub, err=err)
     lse = torch.empty(x.B, x.Hq, device=DEV)
     out = kvd.attn_decode_quest(q, kp, vp, bt, sl, sel, scale=x.scale, lse_out=lse, err=err)
+    # the split path: bounds alone, then choice and attention in one launch -- same pages,
+    # same outputs
+    ub2 = kvd.quest_page_bounds(q, kmin, kmax, bt, sl, x.page_size, err=err)
+    lse2 = torch.empty(x.B, x.Hq, device=DEV)
+    out2, sel2 = kvd.attn_decode_quest_from_bounds(q, kp, vp, bt, sl, ub2, n_sel, scale=x.scale,
+                                                   lse_out=lse2, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+    assert torch.equal(sel2, sel) and torch.equal(out2, out) and torch.equal(lse2, lse)
+    assert torch.equal(torch.isnan(ub2), torch.isnan(ub)) and \
+        torch.equal(torch.nan_to_num(ub2), torch.nan_to_num(ub))
     return kmin.cpu(), kmax.cpu(), sel.cpu().numpy(), ub.cpu().double().numpy(), out, lse
 
 
