@@ -373,7 +373,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) quest_attn_kernel(const Quest
 #pragma unroll
             for (int off = 16; off; off >>= 1)
 #pragma unroll
-                for (int r = 0; r < kRowsInFlight; ++r) s[r] += __shfl_xor_sync(0xffffffffu, s[r], off);
+                for (int r = 0; r < kRowsInFlight; ++r)
+                    s[r] += __shfl_xor_sync(0xffffffffu, s[r], off);
             float mx = m;
 #pragma unroll
             for (int r = 0; r < kRowsInFlight; ++r)
@@ -469,8 +470,9 @@ static cudaError_t bounds_launch(const QuestParams& p, dim3 grid, cudaStream_t s
 }
 
 int quest_bounds_launch(const QuestParams& p, cudaStream_t stream) {
+    const int per_cta = 32 * kBoundWarps;
     const dim3 grid(static_cast<unsigned>(p.B * p.Hkv),
-                    static_cast<unsigned>((p.max_pages + 32 * kBoundWarps - 1) / (32 * kBoundWarps)));
+                    static_cast<unsigned>((p.max_pages + per_cta - 1) / per_cta));
     cudaError_t e = cudaErrorInvalidValue;
     if (p.dtype == KVD_BF16 && p.D == 64) e = bounds_launch<2, true>(p, grid, stream);
     else if (p.dtype == KVD_BF16 && p.D == 128) e = bounds_launch<4, true>(p, grid, stream);
@@ -493,8 +495,8 @@ int quest_select_launch(const QuestParams& p, cudaStream_t stream) {
         configured = smem;
     }
     const unsigned blocks = static_cast<unsigned>((p.B * p.Hq + kChooseWarps - 1) / kChooseWarps);
-    if (launch_kernel(quest_choose_kernel, dim3(blocks), dim3(kChooseWarps * 32), smem, stream, p) !=
-        cudaSuccess)
+    if (launch_kernel(quest_choose_kernel, dim3(blocks), dim3(kChooseWarps * 32), smem, stream,
+                      p) != cudaSuccess)
         return KVD_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
@@ -506,11 +508,17 @@ static int attn_launch(const QuestParams& p, cudaStream_t stream) {
     if (smem > 48 * 1024) {
         static size_t configured = 0;
         if (configured < smem) {
+            const int bytes = static_cast<int>(smem);
+            constexpr auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
             cudaError_t e = cudaSuccess;
-            if (p.dtype == KVD_BF16 && p.D == 64) e = cudaFuncSetAttribute(quest_attn_kernel<2, true, CHOOSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-            if (p.dtype == KVD_BF16 && p.D == 128) e = cudaFuncSetAttribute(quest_attn_kernel<4, true, CHOOSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-            if (p.dtype == KVD_F32 && p.D == 64) e = cudaFuncSetAttribute(quest_attn_kernel<2, false, CHOOSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-            if (p.dtype == KVD_F32 && p.D == 128) e = cudaFuncSetAttribute(quest_attn_kernel<4, false, CHOOSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (p.dtype == KVD_BF16 && p.D == 64)
+                e = cudaFuncSetAttribute(quest_attn_kernel<2, true, CHOOSE>, attr, bytes);
+            if (p.dtype == KVD_BF16 && p.D == 128)
+                e = cudaFuncSetAttribute(quest_attn_kernel<4, true, CHOOSE>, attr, bytes);
+            if (p.dtype == KVD_F32 && p.D == 64)
+                e = cudaFuncSetAttribute(quest_attn_kernel<2, false, CHOOSE>, attr, bytes);
+            if (p.dtype == KVD_F32 && p.D == 128)
+                e = cudaFuncSetAttribute(quest_attn_kernel<4, false, CHOOSE>, attr, bytes);
             if (e != cudaSuccess) return KVD_ERR_CUDA;
             configured = smem;
         }
