@@ -95,6 +95,15 @@ def test_quest_bf16(kvd, D, P, n_sel):
     _check(kvd, x, n_sel)
 
 
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (16, 2), (32, 2), (12, 4)])
+def test_quest_group_sizes(kvd, hq, hkv):
+    # every bound-kernel width (group sizes 1, 2, 8, 16 and a padded 3)
+    lens = [40, 500, 1111]
+    x = W.make_gqa(3, hq, hkv, 128, lens, page_size=16, shuffle=True, extra_pages=2,
+                   seed=9050 + hq + hkv)
+    _check(kvd, x, 8)
+
+
 def test_quest_fp32(kvd):
     lens = [5, 64, 333]
     x = W.make_gqa(3, 8, 2, 64, lens, page_size=16, shuffle=True, seed=9100,
