@@ -241,7 +241,7 @@ int quest_page_minmax(const void *k_pool, void *kmin, void *kmax, const int32_t 
  *  ub_out [B, Hq, max_pages] float32 output (required; the bounds are computed there, then
  *         chosen from): U, NaN past the full pages
  * Other arguments as attn_decode_gqa_paged. Supported: D in {64, 128}, Hq / Hkv <= 16,
- * 1 <= n_sel <= 64, max_pages <= 12800. err as quest_page_minmax (KVD_ERR_DEVICE_OOB for a
+ * 1 <= n_sel <= 64, max_pages <= 6400. err as quest_page_minmax (KVD_ERR_DEVICE_OOB for a
  * length or page id out of range, clamped). Two launches; no workspace.
  */
 int quest_select_pages(const void *q, const void *kmin, const void *kmax,
@@ -279,7 +279,7 @@ int quest_page_bounds(const void *q, const void *kmin, const void *kmax,
  * ub (as quest_page_bounds writes them; ties to the lower page), writes them to sel_out
  * [B, Hq, n_sel] (ascending, -1 padded, exactly as quest_select_pages would), and attends
  * over those pages and the tail as attn_decode_quest does. Supported: as attn_decode_quest,
- * max_pages <= 51200. One launch.
+ * max_pages <= 25600. One launch.
  */
 int attn_decode_quest_from_bounds(const void *q, const void *k_pool, const void *v_pool,
                                   const int32_t *block_table, const int32_t *seq_lens,

@@ -556,7 +556,7 @@ int attn_decode_quest_from_bounds(const void* q, const void* k_pool, const void*
     const int st = quest_common(qp, B, Hq, Hkv, D, page_size, max_pages, num_pages, dtype, err);
     if (st != KVD_OK) return st;
     if (n_sel < 1 || n_sel > 64) return KVD_ERR_UNSUPPORTED;
-    if ((size_t)max_pages * 4 > 200 * 1024) return KVD_ERR_UNSUPPORTED;
+    if ((size_t)max_pages * 8 > 200 * 1024) return KVD_ERR_UNSUPPORTED;
     if (!std::isfinite(scale)) return KVD_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(ub) & 3) || (reinterpret_cast<uintptr_t>(sel_out) & 3) ||

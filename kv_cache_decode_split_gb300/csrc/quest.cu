@@ -13,8 +13,9 @@
 //    (their page ids in one load, eight pages' summaries in flight): a lane holds its D/32
 //    dims of kmin/kmax and of the group's queries, and warp sums give every query head of
 //    the group its bound, written to the caller's bound array.
-//  * quest_choose_kernel: one warp per (sequence, query head) picks the n_sel best bounds by
-//    repeated warp arg-max (value, then lower index) and writes them in ascending order.
+//  * quest_choose_kernel: one warp per (sequence, query head) picks the n_sel best bounds
+//    (value, then lower index): each lane sorts its own pages once, then every round takes
+//    the best of the lanes' heads by two warp max-reductions; written in ascending order.
 //  * quest_attn_kernel: one CTA per (sequence, query head) over its chosen pages and tail:
 //    warps take pages, eight rows in flight per warp, scores by warp sums, running max /
 //    running sum softmax, then the four warps merge in shared memory.
@@ -111,12 +112,6 @@ struct Raw {
         }
     }
 };
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    return v;
-}
 
 // ---------------------------------------------------------------------------- summaries
 template <int VEC, bool BF16>
@@ -233,36 +228,53 @@ __global__ void __launch_bounds__(kBoundWarps * 32) quest_bounds_kernel(const Qu
 }
 
 // ---------------------------------------------------------------------------- choice
-// One warp per (sequence, query head): the bounds of its full pages into shared memory,
-// then n_sel rounds of warp arg-max (the larger bound, then the lower page), a chosen page's
-// bound set to -inf; the chosen pages are written in ascending order.
+// One warp per (sequence, query head): the sort keys of its full pages' bounds into shared
+// memory, then choose_pages.
 constexpr int kChooseWarps = 4;
 
-// One warp: the n_sel best of the bounds u[0..full) (shared memory, consumed), written to
-// out[0..n_sel) in ascending order, -1 padded.
-__device__ __forceinline__ void choose_pages(float* u, int full, int n_sel, int32_t* out) {
+// Sort key of a bound: larger bound first, then the lower page (a NaN bound ranks below
+// every number); 0 marks "no candidate".
+__device__ __forceinline__ uint64_t bound_key(float v, int m) {
+    uint32_t o = 0u;
+    if (v == v) {
+        const uint32_t b = __float_as_uint(v);
+        o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    }
+    return (static_cast<uint64_t>(o) << 32) | (0xffffffffu - static_cast<uint32_t>(m));
+}
+
+// One warp: the n_sel best of the pages 0..full-1, whose keys are in key[] (shared memory,
+// consumed), written to out[0..n_sel) in ascending page order, -1 padded. Each lane sorts
+// its own pages (m = lane mod 32) once; a round is then two warp max-reductions over the
+// lanes' current heads and one step of the winning lane's list.
+__device__ __forceinline__ void choose_pages(uint64_t* key, int full, int n_sel, int32_t* out) {
     const int lane = threadIdx.x % 32;
     const int n_take = min(full, n_sel);
+    const int n_l = lane < full ? (full - lane + 31) / 32 : 0;
+    for (int i = 1; i < n_l; ++i) {  // insertion sort, descending
+        const uint64_t x = key[lane + 32 * i];
+        int j = i - 1;
+        while (j >= 0 && key[lane + 32 * j] < x) {
+            key[lane + 32 * (j + 1)] = key[lane + 32 * j];
+            --j;
+        }
+        key[lane + 32 * (j + 1)] = x;
+    }
+    int ptr = 0;
+    uint64_t cand = n_l > 0 ? key[lane] : 0ull;
     int mine0 = -1, mine1 = -1;  // this lane's picks: rounds lane and lane + 32
     for (int r = 0; r < n_take; ++r) {
-        float best = -INFINITY;
-        int bi = 0x7fffffff;
-        for (int m = lane; m < full; m += 32) {
-            const float v = u[m];
-            if (v > best || (v == best && m < bi)) best = v, bi = m;
-        }
-#pragma unroll
-        for (int off = 16; off; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, best, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (ov > best || (ov == best && oi < bi)) best = ov, bi = oi;
-        }
-        if (bi >= full) bi = 0;  // every remaining bound is -inf or NaN
+        const uint32_t hi = static_cast<uint32_t>(cand >> 32), lo = static_cast<uint32_t>(cand);
+        const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
+        const uint32_t mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? lo : 0u);
+        const int page = static_cast<int>(0xffffffffu - mlo);
         if (lane == (r & 31)) {
-            if (r < 32) mine0 = bi; else mine1 = bi;
+            if (r < 32) mine0 = page; else mine1 = page;
         }
-        if (lane == 0) u[bi] = -INFINITY;
-        __syncwarp();
+        if (cand != 0ull && hi == mhi && lo == mlo) {
+            ++ptr;
+            cand = ptr < n_l ? key[lane + 32 * ptr] : 0ull;
+        }
     }
     // ascending order: each pick goes to its rank among the picks
     int rank0 = 0, rank1 = 0;
@@ -277,7 +289,7 @@ __device__ __forceinline__ void choose_pages(float* u, int full, int n_sel, int3
 }
 
 __global__ void __launch_bounds__(kChooseWarps * 32) quest_choose_kernel(const QuestParams p) {
-    extern __shared__ float ubs[];  // [kChooseWarps][max_pages]
+    extern __shared__ uint64_t ubs[];  // [kChooseWarps][max_pages] sort keys
     griddep_wait();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bh = blockIdx.x * kChooseWarps + warp;
@@ -285,9 +297,9 @@ __global__ void __launch_bounds__(kChooseWarps * 32) quest_choose_kernel(const Q
     const int b = bh / p.Hq;
     const int L = load_len(p.seq_lens, b, p.max_len, p.err);
     const int full = L / p.page_size;
-    float* u = ubs + static_cast<size_t>(warp) * p.max_pages;
+    uint64_t* u = ubs + static_cast<size_t>(warp) * p.max_pages;
     const float* src = p.ub_out + static_cast<size_t>(bh) * p.max_pages;
-    for (int m = lane; m < full; m += 32) u[m] = src[m];
+    for (int m = lane; m < full; m += 32) u[m] = bound_key(src[m], m);
     __syncwarp();
     choose_pages(u, full, p.n_sel, p.sel + static_cast<size_t>(bh) * p.n_sel);
 }
@@ -301,7 +313,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) quest_attn_kernel(const Quest
     __shared__ float m_s[kAttnWarps], l_s[kAttnWarps];
     __shared__ float o_s[kAttnWarps][D];
     __shared__ int32_t sel_s[64];
-    extern __shared__ float ubrow[];  // CHOOSE: the head's bounds [max_pages]
+    extern __shared__ uint64_t ubrow[];  // CHOOSE: the head's bound keys [max_pages]
     griddep_wait();
     const int b = blockIdx.x / p.Hq, h = blockIdx.x % p.Hq;
     const int g = h / (p.Hq / p.Hkv);
@@ -314,7 +326,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) quest_attn_kernel(const Quest
     if constexpr (CHOOSE) {
         if (warp == 0) {
             const float* src = p.ub_out + (static_cast<size_t>(b) * p.Hq + h) * p.max_pages;
-            for (int m = lane; m < full; m += 32) ubrow[m] = src[m];
+            for (int m = lane; m < full; m += 32) ubrow[m] = bound_key(src[m], m);
             __syncwarp();
             choose_pages(ubrow, full, p.n_sel, sel_s);
             __syncwarp();
@@ -455,7 +467,7 @@ int quest_minmax_launch(const QuestParams& p, cudaStream_t stream) {
 size_t quest_select_smem(int Hq, int Hkv, int max_pages) {
     (void)Hq;
     (void)Hkv;
-    return sizeof(float) * static_cast<size_t>(kChooseWarps) * max_pages;
+    return sizeof(uint64_t) * static_cast<size_t>(kChooseWarps) * max_pages;
 }
 
 template <int VEC, bool BF16>
@@ -504,23 +516,25 @@ int quest_select_launch(const QuestParams& p, cudaStream_t stream) {
 template <bool CHOOSE>
 static int attn_launch(const QuestParams& p, cudaStream_t stream) {
     const dim3 grid(static_cast<unsigned>(p.B * p.Hq)), block(kAttnWarps * 32);
-    const size_t smem = CHOOSE ? sizeof(float) * static_cast<size_t>(p.max_pages) : 0;
-    if (smem > 48 * 1024) {
-        static size_t configured = 0;
-        if (configured < smem) {
-            const int bytes = static_cast<int>(smem);
-            constexpr auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-            cudaError_t e = cudaSuccess;
-            if (p.dtype == KVD_BF16 && p.D == 64)
-                e = cudaFuncSetAttribute(quest_attn_kernel<2, true, CHOOSE>, attr, bytes);
-            if (p.dtype == KVD_BF16 && p.D == 128)
-                e = cudaFuncSetAttribute(quest_attn_kernel<4, true, CHOOSE>, attr, bytes);
-            if (p.dtype == KVD_F32 && p.D == 64)
-                e = cudaFuncSetAttribute(quest_attn_kernel<2, false, CHOOSE>, attr, bytes);
-            if (p.dtype == KVD_F32 && p.D == 128)
-                e = cudaFuncSetAttribute(quest_attn_kernel<4, false, CHOOSE>, attr, bytes);
-            if (e != cudaSuccess) return KVD_ERR_CUDA;
-            configured = smem;
+    const size_t smem = CHOOSE ? sizeof(uint64_t) * static_cast<size_t>(p.max_pages) : 0;
+    if constexpr (CHOOSE) {
+        if (smem > 48 * 1024) {
+            static size_t configured = 0;
+            if (configured < smem) {
+                const int bytes = static_cast<int>(smem);
+                constexpr auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+                cudaError_t e = cudaSuccess;
+                if (p.dtype == KVD_BF16 && p.D == 64)
+                    e = cudaFuncSetAttribute(quest_attn_kernel<2, true, CHOOSE>, attr, bytes);
+                if (p.dtype == KVD_BF16 && p.D == 128)
+                    e = cudaFuncSetAttribute(quest_attn_kernel<4, true, CHOOSE>, attr, bytes);
+                if (p.dtype == KVD_F32 && p.D == 64)
+                    e = cudaFuncSetAttribute(quest_attn_kernel<2, false, CHOOSE>, attr, bytes);
+                if (p.dtype == KVD_F32 && p.D == 128)
+                    e = cudaFuncSetAttribute(quest_attn_kernel<4, false, CHOOSE>, attr, bytes);
+                if (e != cudaSuccess) return KVD_ERR_CUDA;
+                configured = smem;
+            }
         }
     }
     cudaError_t e;
