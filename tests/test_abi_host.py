@@ -99,3 +99,45 @@ def test_delta_step_argument_checks(lib):
     assert call(S=(1 << 20) + 4) == -1           # state not 16-byte aligned
     assert call(a=(5 << 20) + 4) == -1           # per-channel decays not 16-byte aligned
     assert call(o=(1 << 20) + 64) == -1          # output inside the state
+
+
+def test_append_ring_and_quest_argument_checks(lib):
+    # every call below breaks exactly one host-side rule, so none reaches a launch
+    vp = ctypes.c_void_p
+    A = 1 << 20   # a 16-byte aligned stand-in address, never dereferenced
+
+    def append(k_new=A, v_new=A, err=A, D=64, dtype=1, P=64, max_pages=4, window=0, n_sink=0):
+        return lib.kvd_cache_append(vp(k_new) if k_new else None, vp(v_new) if v_new else None,
+                                    vp(A), vp(A) if v_new else None, vp(A), vp(A), 2, 8, D, P,
+                                    max_pages, 16, dtype, window, n_sink,
+                                    vp(err) if err else None, None)
+    assert append(k_new=0) == -1
+    assert append(err=0) == -1
+    assert append(D=6) == -2                       # 12-byte rows
+    assert append(dtype=5) == -2
+    assert append(window=250, n_sink=7) == -1      # ring larger than the table's 256 slots
+    assert append(k_new=A + 8) == -1               # not 16-byte aligned
+
+    def ring(window=64, n_sink=4, max_pages=4):
+        return lib.attn_decode_swa_ring(vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), None, 2, 8, 2,
+                                        64, 16, max_pages, 16, 0.125, 1, window, n_sink, None,
+                                        vp(A), 1 << 30, None)
+    assert ring(window=0) == -1
+    assert ring(n_sink=-1) == -1
+    assert ring(window=64, n_sink=4, max_pages=4) == -1   # 68 slots > 4 pages of 16
+
+    def select(n_sel=16, Hq=8, Hkv=2, ub=A, D=128):
+        return lib.quest_select_pages(vp(A), vp(A), vp(A), vp(A), vp(A), vp(A),
+                                      vp(ub) if ub else None, 2, Hq, Hkv, D, 16, 64, 128, n_sel,
+                                      1, vp(A), None)
+    assert select(n_sel=0) == -2 and select(n_sel=65) == -2
+    assert select(Hq=64, Hkv=2) == -2              # group of 32 query heads
+    assert select(ub=0) == -1
+    assert select(D=96) == -2
+
+    def fused(max_pages=64, n_sel=16):
+        return lib.attn_decode_quest_from_bounds(vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), vp(A),
+                                                 vp(A), None, 2, 8, 2, 128, 16, max_pages, 128,
+                                                 n_sel, 0.125, 1, vp(A), None)
+    assert fused(max_pages=30000) == -2            # bound keys beyond shared memory
+    assert fused(n_sel=100) == -2
