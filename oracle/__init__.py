@@ -10,9 +10,12 @@ its header for the passages each function follows). This module only loads
 the compiled library and marshals arrays. Inputs are passed exactly as stored
 (bf16 bit patterns or float32) and widened to double inside the C code.
 
-Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
-and ``tests/test_worked_numbers.py`` (brute force on tiny inputs, closed forms,
-the pages' printed numbers and the invariants the method states).
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``,
+``tests/test_worked_numbers.py``, ``tests/test_oracle_ring.py`` (cache append and
+rolling caches), ``tests/test_oracle_quest.py`` (Quest) and
+``tests/test_oracle_delta.py`` (the gated delta rule): brute force on tiny inputs,
+closed forms, the pages' printed numbers, independent formulations (the chunk-wise
+delta rule, the box maximum) and the invariants the method states.
 """
 from __future__ import annotations
 
