@@ -1,6 +1,7 @@
 /*
  * oracle.c -- plain, slow fp64 CPU reference for single-token decode attention
- * over a paged KV cache.
+ * over a paged KV cache (and the cache append, the rolling sliding-window cache,
+ * Quest page selection, the FP8 indexer and the gated delta-rule decode step).
  *
  * TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the
  * benchmark's CPU-baseline leg may load this library. It shares no code,
@@ -9,7 +10,9 @@
  * Every result is the plain definition written out: scores, one softmax over
  * the visible tokens, a weighted sum of values. No online softmax, no split,
  * no tiling. Inputs are read as stored (bf16 or fp32) and widened exactly to
- * double; all arithmetic is double; outputs are double.
+ * double; all arithmetic is double (except where a function says it follows the
+ * kernel's float32 to decide an integer, as the e4m3 quantizer does); outputs are
+ * double.
  *
  * Sources (page title, section):
  *  - "Overview of Attention Mechanism", GQA / Code (repeat_kv and
