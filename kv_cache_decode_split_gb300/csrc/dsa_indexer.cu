@@ -36,6 +36,7 @@ constexpr int kIdxQBytes = kHi * kDi * 2;         // 16 KB: two 64-dim boxes of 
 constexpr int kIdxStages = 5;
 constexpr int kIdxThreads = 6 * 32;     // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kHistBins = 2048;         // top 11 key bits
+constexpr int kIdxRowCap = 512;         // page pieces resolved ahead (a chunk)
 
 struct IdxSmem {
     uint8_t stage[kIdxStages][kIdxTileBytes];   // 1024-aligned (offset 0)
@@ -45,12 +46,26 @@ struct IdxSmem {
     uint64_t full[kIdxStages], empty[kIdxStages];
     uint64_t qfull[2], qempty[2], tfull[2], tempty[2], done;
     uint32_t tmem_base;
+    int prow[kIdxRowCap];                       // first physical row of each piece
 };
 constexpr int kIdxSmem = static_cast<int>(sizeof(IdxSmem)) + 1024;
 
 // The tiles a CTA owns: a contiguous slice of the flattened (sequence, tile) list.
 struct TileRange {
     int begin, end;
+};
+
+// (sequence, tile within it) of flat tile f, advanced without a division per tile
+struct IdxCursor {
+    int b, j, per_b;
+    __device__ IdxCursor(int f, int tiles_per_b)
+        : b(f / tiles_per_b), j(f % tiles_per_b), per_b(tiles_per_b) {}
+    __device__ void next() {
+        if (++j == per_b) {
+            j = 0;
+            ++b;
+        }
+    }
 };
 __device__ __forceinline__ TileRange my_tiles(int total) {
     const long long G = gridDim.x, i = blockIdx.x;
@@ -97,91 +112,79 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
-        // The warp resolves the physical rows of the range's page pieces 32 at a time (lane
-        // k: piece 32 m + k), the next batch in flight while the current one is used; lane 0
-        // issues the copies.
+        // The warp resolves the physical rows of the range's page pieces a chunk at a time
+        // into shared memory; lane 0 then issues the copies.
         if (lane == 0) {
             prefetch_tensormap(&tmK);
             prefetch_tensormap(&tmK128);
             prefetch_tensormap(&tmQ);
         }
         const int bp = min(p.page_size, kItile);
-        const int per_tile = kItile / bp;
-        const int n_pieces = (tr.end - tr.begin) * per_tile;
-        // first physical row of piece q, or -1 for a tile past its sequence's end
-        auto piece_row = [&](int q) -> int {
-            if (q >= n_pieces) return -1;
-            const int f = tr.begin + q / per_tile, sub = q % per_tile;
-            const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
-            const int L = load_len(p.seq_lens, b, p.max_len, p.err);
-            if (j * kItile >= L) return -1;
-            const int t = j * kItile + sub * bp;
-            const int tc = t < L ? t : L - 1;  // rows past the end: a valid page
-            const int pg = load_page(p.block_table, p.max_pages, p.num_pages, b,
-                                     tc / p.page_size, p.err);
-            return pg * p.page_size + (t % p.page_size);
-        };
-        int cur = piece_row(lane), nxt = piece_row(32 + lane);
-        int cur_b = -1;
+        const int per_tile = kItile / bp;  // 1, 2, 4 or 8 pieces a tile
+        const int chunk = kIdxRowCap / per_tile;
         uint32_t g = 0, nq = 0;
+        int cur_b = -1;
         bool ok = true;
-        for (int f = tr.begin; f < tr.end && ok; ++f) {
-            const int fi = f - tr.begin;
-            int ys[kItile / 16];
-#pragma unroll
-            for (int sub = 0; sub < kItile / 16; ++sub) {
-                if (sub >= per_tile) break;
-                const int q = fi * per_tile + sub;
-                if (q > 0 && (q & 31) == 0) {
-                    cur = nxt;
-                    nxt = piece_row(q + 32 + lane);
+        for (int c0 = tr.begin; c0 < tr.end && ok; c0 += chunk) {
+            const int c1 = min(tr.end, c0 + chunk);
+            // the warp resolves the chunk's piece rows (first physical row of each piece, or
+            // -1 for a tile past its sequence's end), lane k taking pieces k, k + 32, ...
+            for (int q = lane; q < (c1 - c0) * per_tile; q += 32) {
+                const int f = c0 + q / per_tile, sub = q % per_tile;
+                const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
+                const int L = load_len(p.seq_lens, b, p.max_len, p.err);
+                int row = -1;
+                if (j * kItile < L) {
+                    const int t = j * kItile + sub * bp;
+                    const int tc = t < L ? t : L - 1;  // rows past the end: a valid page
+                    const int pg = load_page(p.block_table, p.max_pages, p.num_pages, b,
+                                             tc / p.page_size, p.err);
+                    row = pg * p.page_size + (t % p.page_size);
                 }
-                ys[sub] = __shfl_sync(0xffffffffu, cur, q & 31);
+                sm.prow[q] = row;
             }
-            if (ys[0] < 0) continue;  // the tile lies past its sequence's end
-            const int b = f / p.tiles_per_b;
+            __syncwarp();
+            // lane 0 alone issues the chunk's copies: no warp-wide step per tile
             if (lane == 0) {
-                if (b != cur_b) {
-                    const int qs = nq & 1;
-                    ok = mbar_wait(&sm.qempty[qs], ((nq >> 1) & 1) ^ 1, p.err);
-                    if (ok) {
+                IdxCursor tc(c0, p.tiles_per_b);
+                for (int f = c0; f < c1 && ok; ++f, tc.next()) {
+                    const int* ys = sm.prow + (f - c0) * per_tile;
+                    if (ys[0] < 0) continue;  // the tile lies past its sequence's end
+                    const int b = tc.b;
+                    if (b != cur_b) {
+                        const int qs = nq & 1;
+                        ok = mbar_wait(&sm.qempty[qs], ((nq >> 1) & 1) ^ 1, p.err);
+                        if (!ok) break;
                         mbar_arrive_expect_tx(&sm.qfull[qs], kIdxQBytes);
                         tma_load_2d(sm.qbuf[qs], &tmQ, &sm.qfull[qs], 0, b * kHi);
                         tma_load_2d(sm.qbuf[qs] + kIdxQBytes / 2, &tmQ, &sm.qfull[qs], 64,
                                     b * kHi);
+                        ++nq;
+                        cur_b = b;
                     }
-                }
-                const int s = g % kIdxStages;
-                if (ok) ok = mbar_wait(&sm.empty[s], ((g / kIdxStages) & 1) ^ 1, p.err);
-                if (ok) {
+                    const int s = g % kIdxStages;
+                    ok = mbar_wait(&sm.empty[s], ((g / kIdxStages) & 1) ^ 1, p.err);
+                    if (!ok) break;
                     mbar_arrive_expect_tx(&sm.full[s], kIdxTileBytes);
-                    // one 32 KB instruction when the pieces are contiguous (adjacent pages,
-                    // or pages of >= 128 tokens)
+                    // one 32 KB instruction when the pieces are contiguous (adjacent pages, or
+                    // pages of >= 128 tokens)
                     bool contiguous = true;
-#pragma unroll
-                    for (int sub = 1; sub < kItile / 16; ++sub)
-                        if (sub < per_tile && ys[sub] != ys[0] + sub * bp) contiguous = false;
+                    for (int sub = 1; sub < per_tile; ++sub)
+                        if (ys[sub] != ys[0] + sub * bp) contiguous = false;
                     if (contiguous && ys[0] + kItile <= p.num_pages * p.page_size) {
                         tma_load_3d(sm.stage[s], &tmK128, &sm.full[s], 0, ys[0], 0);
                     } else {
-#pragma unroll
-                        for (int sub = 0; sub < kItile / 16; ++sub) {
-                            if (sub >= per_tile) break;
+                        for (int sub = 0; sub < per_tile; ++sub)
                             for (int half = 0; half < 2; ++half)
                                 tma_load_2d(sm.stage[s] + half * (kIdxTileBytes / 2) +
                                                 sub * bp * 128,
                                             &tmK, &sm.full[s], half * 64, ys[sub]);
-                        }
                     }
+                    ++g;
                 }
             }
+            // the rows of this chunk stay until lane 0 has issued them
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (b != cur_b) {
-                ++nq;
-                cur_b = b;
-            }
-            ++g;
         }
         // copies still in flight complete before the CTA may exit
         if (lane == 0) {
@@ -197,8 +200,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             uint32_t g = 0, nq = 0, nt = 0;
             int qs = 0;
             bool ok = true;
-            for (int f = tr.begin; f < tr.end && ok; ++f) {
-                const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
+            IdxCursor tc(tr.begin, p.tiles_per_b);
+            for (int f = tr.begin; f < tr.end && ok; ++f, tc.next()) {
+                const int b = tc.b, j = tc.j;
                 if (b != cur_b) L = load_len(p.seq_lens, b, p.max_len, nullptr);
                 if (j * kItile >= L) continue;
                 if (b != cur_b) {
@@ -238,6 +242,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         const int etid = threadIdx.x - 64;  // 0..127
         int cur_b = -1, L = 0;
         uint32_t nt = 0, nb = 0;
+        float wr[kHi];  // the head weights of the current sequence
         auto flush_hist = [&](int b) {
             asm volatile("bar.sync 2, 128;" ::: "memory");
             for (int i = etid; i < kHistBins; i += 128) {
@@ -249,32 +254,39 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             }
             asm volatile("bar.sync 2, 128;" ::: "memory");
         };
-        for (int f = tr.begin; f < tr.end; ++f) {
-            const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
+        IdxCursor tc(tr.begin, p.tiles_per_b);
+        for (int f = tr.begin; f < tr.end; ++f, tc.next()) {
+            const int b = tc.b, j = tc.j;
             if (b != cur_b) L = load_len(p.seq_lens, b, p.max_len, nullptr);
             if (j * kItile >= L) continue;
             if (b != cur_b) {
                 if (cur_b >= 0) flush_hist(cur_b);
                 if (etid < kHi) sm.wv[nb & 1][etid] = p.w[static_cast<size_t>(b) * kHi + etid];
                 asm volatile("bar.sync 2, 128;" ::: "memory");
+#pragma unroll
+                for (int h = 0; h < kHi; ++h) wr[h] = sm.wv[nb & 1][h];
                 ++nb;
                 cur_b = b;
             }
-            const float* wv = sm.wv[(nb - 1) & 1];
             const int acc = nt & 1;
             if (!mbar_wait(&sm.tfull[acc], (nt >> 1) & 1, p.err)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * kHi;
-            float score = 0.f;
+            // both 32-column halves of the row in flight at once; four independent sums
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(taddr, r0);
+            tmem_ld_32x32b_x32(taddr + 32, r1);
+            tmem_ld_wait(r0);
+            tmem_ld_wait(r1);
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + half * 32, r);
-                tmem_ld_wait(r);
-#pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    score = fmaf(wv[half * 32 + c], fmaxf(__uint_as_float(r[c]), 0.f), score);
+            for (int c = 0; c < 32; c += 2) {
+                a0 = fmaf(wr[c], fmaxf(__uint_as_float(r0[c]), 0.f), a0);
+                a1 = fmaf(wr[c + 1], fmaxf(__uint_as_float(r0[c + 1]), 0.f), a1);
+                a2 = fmaf(wr[32 + c], fmaxf(__uint_as_float(r1[c]), 0.f), a2);
+                a3 = fmaf(wr[33 + c], fmaxf(__uint_as_float(r1[c + 1]), 0.f), a3);
             }
+            const float score = (a0 + a1) + (a2 + a3);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.tempty[acc]);
