@@ -391,7 +391,7 @@ void oracle_indexer_scores_fp8(const uint8_t *q8, const float *q_scale, const ui
  * columns, row-major), key k and query q (dk), value v (dv), write strength beta:
  *   fade:        S[i][j] *= a[j]   (KDA: one decay per key channel j; Gated DeltaNet: one
  *                                   value for the whole head, a_per_channel = 0)
- *   correction:  e[i] = v[i] - sum_j S[i][j] k[j]      (what the faded memory gets wrong)
+ *   correction:  e[i] = v[i] - sum_j S[i][j] k[j]      (recall error of the faded state for k)
  *   write:       S[i][j] += beta e[i] k[j]
  *   read:        o[i] = sum_j S[i][j] q[j]             (with the updated S)
  * S (float32 in) is widened to double; S_out and o are double. a holds n*dk values when
