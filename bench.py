@@ -39,33 +39,45 @@ HEADLINE = "llama3_8b_gqa_paged"
 
 
 # DRAM traffic (read + write bytes per launch) of a workload's dominant kernel from one ncu
-# capture (summaries in profiles/), reported only while the kernel's sources still hash to
-# the value recorded with the capture: a changed kernel reports null.
+# capture (summaries in profiles/), reported only while what the kernel is compiled from --
+# its source file, the device header and its argument struct -- still hashes to the value
+# recorded with the capture: a changed kernel reports null.
 NCU_TRAFFIC = {
     "llama3_8b_gqa_paged": {
         "bytes": 794.592512e6 + 4.951808e6,
-        "sources": ("gqa_decode.cu", "kvd_device.cuh", "kvd_host.h"),
-        "sha256": "c381c9546ccda1e219f5a315efb79f62bb821c0b1c14ce4d971093b39d307298",
+        "sources": ("gqa_decode.cu", "kvd_device.cuh"),
+        "structs": ("GqaParams",),
+        "sha256": "cee135d8631b6604e2b21a85d7ebd434842922e70455777e159374a437501733",
     },
     # the write-back of the last ~58 MB of the updated state is still in L2 when the kernel ends
     "kda_decode": {
         "bytes": 276.86272e6 + 210.739712e6,
-        "sources": ("delta_decode.cu", "kvd_device.cuh", "kvd_host.h"),
-        "sha256": "ac28b6af952af06de7b5ec95d9a6b2340ce246641fa3057b3f3391d3ec05040d",
+        "sources": ("delta_decode.cu", "kvd_device.cuh"),
+        "structs": ("DeltaParams",),
+        "sha256": "3458690fc00216eabdee212fe156da7140ffa09c8482645b492dced199e078c3",
     },
 }
 
 
 def ncu_traffic(workload):
     import hashlib
+    import re
     e = NCU_TRAFFIC.get(workload)
     if e is None:
         return None
+    csrc = os.path.join(ROOT, "kv_cache_decode_split_gb300", "csrc")
     h = hashlib.sha256()
     try:
         for f in e["sources"]:
-            with open(os.path.join(ROOT, "kv_cache_decode_split_gb300", "csrc", f), "rb") as fh:
+            with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(fh.read())
+        with open(os.path.join(csrc, "kvd_host.h")) as fh:
+            host = fh.read()
+        for name in e.get("structs", ()):
+            m = re.search(r"struct %s \{.*?\n\};" % name, host, re.S)
+            if m is None:
+                return None
+            h.update(m.group(0).encode())
     except OSError:
         return None
     return e["bytes"] if h.hexdigest() == e["sha256"] else None
