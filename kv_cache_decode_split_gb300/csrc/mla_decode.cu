@@ -674,6 +674,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.sempty);
+                const int T0 = lo + i * kTok;
+                // Dense, the sequence's last tile: the slots past its end (the rest of the last
+                // page, or another page of the sequence when pages are shorter than a tile) may
+                // hold anything, NaN and Inf included, and a zero probability times NaN is NaN.
+                // The score product has read the stage, so the group clears those rows of this
+                // CTA's four value boxes before the value product reads them (pfull below).
+                if (!kSparse && T0 + kTok > hi) {
+                    const int r0 = hi - T0;
+                    const int n16 = (kTok - r0) * 8;  // 16-byte chunks to clear per box
+                    uint8_t* st = sm.stage[j % kStages];
+                    for (int e = (warp & 3) * 32 + lane; e < 4 * n16; e += 128) {
+                        const int bx = e / n16, rem = e % n16;
+                        *reinterpret_cast<uint4*>(st + bx * kTileBox + (r0 + rem / 8) * 128 +
+                                                  (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();  // before the tensor core reads the stage
+                }
                 // 2. stage them for the exchange thread, each half once tile j - 1's copy of
                 //    that half has read y
 #pragma unroll
@@ -715,7 +732,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 // 4. tile max, then the running max handed over from tile j - 1 (within the
                 //    piece; the hand-over barrier is passed at every tile to keep its phases)
-                const int T0 = lo + i * kTok;
                 float mt = neg_inf();
 #pragma unroll
                 for (int c = 0; c < kTok; ++c) {

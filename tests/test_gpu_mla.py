@@ -142,3 +142,35 @@ def test_dsa_full_size_sparse_mla_sampled(kvd):
     ref, _ = oracle.mla(x.q, x.c_pool, x.block_table, x.seq_lens, x.scale, idx=idx, idx_count=cnt,
                         pairs=pr)
     assert_attn_close(out[pr[:, 0], pr[:, 1]], ref, what="sparse mla full size")
+
+
+def _poison_past_end(pool, bt, lens, P):
+    """A copy of a [num_pages, P, ...] pool whose slots past each sequence's last token
+    hold NaN, +Inf and -Inf in turn, and whose pages no sequence uses hold NaN: none of them
+    is visible, so the output must not change ("All the attentions", section 8)."""
+    pool = pool.clone()
+    used = set()
+    bad = [float("nan"), float("inf"), float("-inf")]
+    for b, L in enumerate(int(v) for v in lens):
+        n = -(-L // P)
+        used.update(int(v) for v in bt[b, :n])
+        last, r = int(bt[b, n - 1]), L - (n - 1) * P
+        for slot in range(r, P):
+            pool[last, slot] = bad[slot % 3]
+    for pg in range(pool.shape[0]):
+        if pg not in used:
+            pool[pg] = float("nan")
+    return pool
+
+
+@pytest.mark.parametrize("P", [64, 16])
+def test_mla_dense_non_finite_slots_past_end(kvd, P):
+    lens = [1, 63, 65, 127, 700, 3001]
+    x = W.make_mla(len(lens), 128, lens, page_size=P, shuffle=True, extra_pages=3,
+                   seed=650 + P)
+    x.c_pool = _poison_past_end(x.c_pool, x.block_table, lens, P)
+    out, lse = _dense(kvd, x)
+    ref, ref_lse = oracle.mla(x.q, x.c_pool, x.block_table, x.seq_lens, x.scale)
+    assert np.isfinite(ref).all()
+    assert_attn_close(out, ref, what=f"mla, non-finite slots past the end, P={P}")
+    assert np.max(np.abs(to_np(lse) - ref_lse)) < 2e-3 * max(1.0, np.abs(ref_lse).max())
