@@ -428,6 +428,35 @@ int kvd_delta_decode_step(float *S, const float *q, const float *k, const float 
                           const float *a, const float *beta, float *o, int n, int dk, int dv,
                           int a_per_channel, cudaStream_t stream);
 
+/*
+ * Process-wide options, for measurement and for tests of the library itself; normal use
+ * needs none of them (the pages have no counterpart). Each setting holds for calls made
+ * after it, from any thread, until it is set again.
+ *  KVD_OPT_PDL            1 (default): kernels are launched with programmatic dependent
+ *                         launch, so that a kernel's set-up overlaps the tail of the
+ *                         previous one on the stream; 0: plain launches.
+ *  KVD_OPT_GQA_CHUNK      0 (default): the GQA / SWA split plan picks the tokens per split;
+ *                         >= 64: that many tokens (rounded down to a multiple of 64) per
+ *                         split, raised if the plan would exceed its chunk limit.
+ *  KVD_OPT_MLA_MIN_TILES  >= 1 (default 1): the MLA plan gives each two-CTA cluster at least
+ *                         this many 64-token tiles.
+ *  KVD_OPT_WAIT_TIMEOUT_TEST  1: the next bf16 GQA / SWA call (and only that call) runs
+ *                         with a limit of about 1000 SM cycles on each bounded wait of its
+ *                         copy ring, and its consumer warps first wait on a barrier that
+ *                         nothing completes: the wait runs out, the call records
+ *                         KVD_ERR_TIMEOUT (read with kvd_check_device_error), waits for the
+ *                         copies it issued and returns; its outputs are undefined and its
+ *                         workspace stays ready for the next call.
+ * Returns KVD_OK, or KVD_ERR_INVALID_ARG for an unknown option or a value out of range.
+ */
+enum kvd_option {
+    KVD_OPT_PDL = 0,
+    KVD_OPT_GQA_CHUNK = 1,
+    KVD_OPT_MLA_MIN_TILES = 2,
+    KVD_OPT_WAIT_TIMEOUT_TEST = 3
+};
+int kvd_set_option(int option, long long value);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,7 @@ import math
 import torch
 
 from . import _lib
-from ._lib import KvdError, OP
+from ._lib import KvdError, OP, OPTION
 
 lib = _lib.load()
 
@@ -39,7 +39,7 @@ __all__ = [
     "quest_select_pages", "attn_decode_quest", "quest_page_bounds",
     "attn_decode_quest_from_bounds",
     "dsa_topk", "attn_decode_mla_sparse", "kvd_workspace_size", "kvd_check_device_error",
-    "Workspace", "KvdError",
+    "kvd_set_option", "Workspace", "KvdError",
 ]
 
 _DT = {torch.float32: 0, torch.bfloat16: 1}
@@ -80,6 +80,13 @@ def kvd_check_device_error(ws, stream=None):
     """Synchronise and return the device error recorded in a workspace (0 if none)."""
     buf = ws.buffer if isinstance(ws, Workspace) else ws
     return int(lib.kvd_check_device_error(_p(buf), _stream(stream)))
+
+
+def kvd_set_option(option, value):
+    """Process-wide library option (measurement and tests of the library; see kvdecode.h):
+    "pdl", "gqa_chunk", "mla_min_tiles" or "wait_timeout_test"."""
+    _check(lib.kvd_set_option(OPTION[option] if isinstance(option, str) else int(option),
+                              int(value)), "kvd_set_option")
 
 
 class Workspace:

@@ -33,6 +33,7 @@ EXPORTS = (
     "kvd_workspace_size",
     "kvd_check_device_error",
     "kvd_status_string",
+    "kvd_set_option",
 )
 
 STATUS = {
@@ -40,6 +41,7 @@ STATUS = {
     -4: "KVD_ERR_TIMEOUT", -5: "KVD_ERR_WORKSPACE_TOO_SMALL", -6: "KVD_ERR_DEVICE_OOB", -7: "KVD_ERR_DEVICE_STATE",
 }
 OP = {"gqa": 0, "swa": 1, "mla": 2, "dsa_topk": 3, "mla_sparse": 4}
+OPTION = {"pdl": 0, "gqa_chunk": 1, "mla_min_tiles": 2, "wait_timeout_test": 3}
 
 
 class KvdError(RuntimeError):
@@ -91,4 +93,6 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kvd_workspace_size.argtypes = [I] * 9
     lib.kvd_status_string.restype = ctypes.c_char_p
     lib.kvd_status_string.argtypes = [I]
+    lib.kvd_set_option.restype = I
+    lib.kvd_set_option.argtypes = [I, ctypes.c_longlong]
     return lib

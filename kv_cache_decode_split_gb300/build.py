@@ -28,23 +28,23 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libkvdecode.so")
 
 
-def flags(debug: bool = False):
-    f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
-                "-I", INCLUDE, "-I", CSRC, "-Xptxas", "-v" if os.environ.get("KVD_PTXAS_V") else "-O3"]
-    if debug:
-        f += ["-DKVD_DEBUG=1"]
-    return f
+def flags(ptxas_verbose: bool = False):
+    return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+                   "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC, "-Xptxas",
+                   "-v" if ptxas_verbose else "-O3"]
 
 
-def _compile(src: str, obj: str, debug: bool) -> tuple[str, str]:
-    cmd = [nvcc(), "-c", src, "-o", obj] + flags(debug)
+def _compile(src: str, obj: str, verbose: bool) -> tuple[str, str]:
+    cmd = [nvcc(), "-c", src, "-o", obj] + flags(verbose)
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
     return src, r.stderr
 
 
-def build(force: bool = False, debug: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile every CUDA source and link libkvdecode.so (skipped when it is up to date);
+    `verbose` prints ptxas register / shared-memory / spill figures per kernel."""
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     deps = srcs + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
         glob.glob(os.path.join(INCLUDE, "*.h"))
@@ -55,7 +55,7 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False) -> st
     os.makedirs(BUILD, exist_ok=True)
     objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        for src, log in ex.map(lambda so: _compile(so[0], so[1], debug), zip(srcs, objs)):
+        for src, log in ex.map(lambda so: _compile(so[0], so[1], verbose), zip(srcs, objs)):
             if verbose and log:
                 print(f"== {os.path.basename(src)}\n{log}", file=sys.stderr)
     tmp = LIB + f".tmp{os.getpid()}"

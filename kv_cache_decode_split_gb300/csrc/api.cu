@@ -5,7 +5,7 @@
 #include <cstdint>
 #include <cstring>
 #include <algorithm>
-#include <cstdlib>
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -24,15 +24,15 @@ inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
+// Process-wide options (kvd_set_option); the defaults are what the library is tuned for.
+std::atomic<int> g_opt_pdl{1};
+std::atomic<long long> g_opt_gqa_chunk{0};
+std::atomic<long long> g_opt_mla_min_tiles{1};
+std::atomic<int> g_opt_wait_test{0};
+
 }  // namespace
 
-bool pdl_enabled() {
-    static const bool on = [] {
-        const char* env = std::getenv("KVD_PDL");
-        return !(env && env[0] == '0');
-    }();
-    return on;
-}
+bool pdl_enabled() { return g_opt_pdl.load(std::memory_order_relaxed) != 0; }
 
 int num_sms() {
     static int n = 0;
@@ -145,10 +145,8 @@ int gqa_plan(int B, int Hq, int Hkv, int D, int page_size, int max_len, int wind
         chunk = std::max(256LL, (vis + per_group - 1) / per_group);
         chunk = (chunk + 63) / 64 * 64;
     }
-    if (const char* env = std::getenv("KVD_GQA_CHUNK")) {  // tuning override (tokens)
-        const long long c = std::atoll(env);
-        if (c >= 64) chunk = (c / 64) * 64;
-    }
+    if (const long long c = g_opt_gqa_chunk.load(std::memory_order_relaxed); c >= 64)
+        chunk = (c / 64) * 64;  // fixed chunk (KVD_OPT_GQA_CHUNK)
     auto chunks_for = [&](long long C) -> int {
         if (window <= 0) return cdiv(max_len, C);
         const int a = (n_sink > 0 ? cdiv(std::min(n_sink, max_len), C) : 0) +
@@ -195,11 +193,8 @@ MlaPlan mla_plan(int B, int max_items, bool sparse) {
     (void)sparse;
     MlaPlan pl;
     const long long max_tiles = (long long)B * ((max_items + 63) / 64);
-    long long min_tiles = 1;  // tiles a cluster takes at least
-    if (const char* env = std::getenv("KVD_MLA_MIN_TILES")) {  // tuning override
-        const long long t = std::atoll(env);
-        if (t >= 1) min_tiles = t;
-    }
+    // tiles a cluster takes at least (KVD_OPT_MLA_MIN_TILES)
+    const long long min_tiles = std::max(1LL, g_opt_mla_min_tiles.load(std::memory_order_relaxed));
     pl.n_clusters = static_cast<int>(std::max(
         1LL, std::min<long long>(num_sms() / 2, (max_tiles + min_tiles - 1) / min_tiles)));
     const size_t slots = (size_t)pl.n_clusters + B - 1;
@@ -273,14 +268,13 @@ using namespace kvd;
 
 namespace kvd {
 
-int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
-               const int32_t* seq_lens, void* out, float* lse_out, int B, int Hq, int Hkv, int D,
-               int page_size, int max_pages, int num_pages, float scale, int dtype, int window,
-               int n_sink, const float* sink_logit, void* ws, size_t ws_bytes,
-               cudaStream_t stream, int ring) {
-    if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out || !ws)
-        return KVD_ERR_INVALID_ARG;
-    if (ring < 0 || (ring > 0 && (window != 0 || n_sink != 0 || ring > max_pages * page_size)))
+int gqa_check(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+              const int32_t* seq_lens, const void* out, int B, int Hq, int Hkv, int D,
+              int page_size, int max_pages, int num_pages, float scale, int dtype, int window,
+              int n_sink, int ring) {
+    if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out) return KVD_ERR_INVALID_ARG;
+    if (ring < 0 || (ring > 0 && (window != 0 || n_sink != 0 ||
+                                  (long long)ring > (long long)max_pages * page_size)))
         return KVD_ERR_INVALID_ARG;
     if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_pages < 1 || num_pages < 1)
         return KVD_ERR_INVALID_ARG;
@@ -291,9 +285,20 @@ int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t
     if (Hq / Hkv > 128) return KVD_ERR_UNSUPPORTED;
     if ((long long)num_pages * Hkv * page_size >= (1LL << 31)) return KVD_ERR_UNSUPPORTED;
     if ((long long)max_pages * page_size >= (1LL << 30)) return KVD_ERR_UNSUPPORTED;
-    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
-        !aligned16(ws))
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
         return KVD_ERR_INVALID_ARG;
+    return KVD_OK;
+}
+
+int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+               const int32_t* seq_lens, void* out, float* lse_out, int B, int Hq, int Hkv, int D,
+               int page_size, int max_pages, int num_pages, float scale, int dtype, int window,
+               int n_sink, const float* sink_logit, void* ws, size_t ws_bytes,
+               cudaStream_t stream, int ring) {
+    const int st = gqa_check(q, k_pool, v_pool, block_table, seq_lens, out, B, Hq, Hkv, D,
+                             page_size, max_pages, num_pages, scale, dtype, window, n_sink, ring);
+    if (st != KVD_OK) return st;
+    if (!ws || !aligned16(ws)) return KVD_ERR_INVALID_ARG;
     const int max_len = max_pages * page_size;
     GqaPlan plan;
     if (gqa_plan(B, Hq, Hkv, D, page_size, max_len, window, n_sink, dtype, &plan) != KVD_OK)
@@ -335,6 +340,12 @@ int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t
     p.scale_log2 = scale * 1.4426950408889634f;
 
     if (dtype == KVD_F32) return gqa_launch(plan, p, nullptr, nullptr, stream);
+    // KVD_OPT_WAIT_TIMEOUT_TEST, taken by this call only: a short limit on every wait of the
+    // ring and consumers that first wait on a barrier nothing completes
+    if (g_opt_wait_test.exchange(0) != 0) {
+        p.wait_cycles = 1000;
+        p.stall_test = 1;
+    }
     CUtensorMap tk, tv;
     const uint64_t rows = (uint64_t)num_pages * Hkv * page_size;
     const uint32_t box_rows = (page_size < 64 ? page_size : 64) * plan.hpt;
@@ -842,6 +853,28 @@ int kvd_check_device_error(void* ws, cudaStream_t stream) {
         if (cudaMemset(ws, 0, sizeof flag) != cudaSuccess) return KVD_ERR_CUDA;
     }
     return flag;
+}
+
+int kvd_set_option(int option, long long value) {
+    switch (option) {
+        case KVD_OPT_PDL:
+            if (value != 0 && value != 1) return KVD_ERR_INVALID_ARG;
+            g_opt_pdl.store(static_cast<int>(value));
+            return KVD_OK;
+        case KVD_OPT_GQA_CHUNK:
+            if (value != 0 && (value < 64 || value > (1LL << 30))) return KVD_ERR_INVALID_ARG;
+            g_opt_gqa_chunk.store(value);
+            return KVD_OK;
+        case KVD_OPT_MLA_MIN_TILES:
+            if (value < 1 || value > (1LL << 30)) return KVD_ERR_INVALID_ARG;
+            g_opt_mla_min_tiles.store(value);
+            return KVD_OK;
+        case KVD_OPT_WAIT_TIMEOUT_TEST:
+            if (value != 0 && value != 1) return KVD_ERR_INVALID_ARG;
+            g_opt_wait_test.store(static_cast<int>(value));
+            return KVD_OK;
+        default: return KVD_ERR_INVALID_ARG;
+    }
 }
 
 const char* kvd_status_string(int status) {

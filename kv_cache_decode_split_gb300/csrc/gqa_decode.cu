@@ -269,7 +269,7 @@ struct GqaBf16Cfg {
     static constexpr int kCombBytes = static_cast<int>(sizeof(CombineSmem<HPT * NT * 8>));
     static constexpr int kOverlay =
         kRingBytes > kMergeBytes + kCombBytes ? kRingBytes : kMergeBytes + kCombBytes;
-    static constexpr int kSmem = 1024 + kOverlay + 2 * kStages * 8;
+    static constexpr int kSmem = 1024 + kOverlay + (2 * kStages + 1) * 8;
     static constexpr int kThreads = (kConsumers + 1) * 32;
 };
 
@@ -291,6 +291,7 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
     uint8_t* sV = smem + S * Cfg::kTileBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kOverlay);
     uint64_t* empty = full + S;
+    uint64_t* stall = empty + S;  // completed by nothing (give-up test only)
     // once the ring is drained: per-KV-head merge areas, then the combine scratch
     MS* ms = reinterpret_cast<MS*>(smem);
     CS& cs = *reinterpret_cast<CS*>(smem + Cfg::kMergeBytes);
@@ -317,9 +318,13 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumers);
         }
+        mbar_init(stall, 1);
         fence_mbar_init();
     }
     __syncthreads();
+    // Every wait of the ring is bounded; one that runs out records KVD_ERR_TIMEOUT and its
+    // warp leaves the loop. The call's limit is normally kWaitCycles.
+    const long long wait_limit = p.wait_cycles > 0 ? p.wait_cycles : kWaitCycles;
 
     if (warp == kConsumers) {
         // ------------------------------------------------------------------ producer
@@ -340,11 +345,12 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
                              p.err);
         };
         int cur = piece_page(lane), nxt = piece_page(32 + lane);
+        int issued = 0;  // tiles whose copies are in flight or landed
         for (int i = 0; i < n_tiles; ++i) {
             const int s = i % S;
             bool ok = true;
             if (lane == 0) {
-                ok = mbar_wait(&empty[s], ((i / S) & 1) ^ 1, p.err);
+                ok = mbar_wait(&empty[s], ((i / S) & 1) ^ 1, p.err, wait_limit);
                 if (ok) mbar_arrive_expect_tx(&full[s], 2 * Cfg::kTileBytes);
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -366,7 +372,18 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
                     tma_load_3d(sV + s * Cfg::kTileBytes + off, &tmV, &full[s], 0, y, 0);
                 }
             }
+            issued = i + 1;
         }
+        // The merge below overwrites the ring, and consumers that gave up on a wait leave
+        // tiles unread: every issued copy must have landed first. (After a normal loop these
+        // are the last tiles, which the consumers wait for as well.) The tile issued last in
+        // each stage completes that stage's latest phase; earlier ones completed before it
+        // was issued.
+        if (lane == 0)
+            for (int i = issued > S ? issued - S : 0; i < issued; ++i)
+                mbar_wait(&full[i % S], (i / S) & 1, p.err);
+        __syncwarp();
+        asm volatile("bar.sync 1, %0;" ::"r"((kConsumers + 1) * 32) : "memory");
     } else {
         // ------------------------------------------------------------------ consumers
         // tile layout [piece][block][head][slot][64]: 128-byte rows, 16-byte chunks XOR-ed
@@ -412,10 +429,13 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
             }
         const int r0 = warp * 16;
         const float sl2 = p.scale_log2;
+        // give-up test: this wait runs out, so the consumers read no tile (the producer's
+        // wait for a free stage then runs out as well)
+        const int n_read = (p.stall_test && !mbar_wait(stall, 0, p.err, wait_limit)) ? 0 : n_tiles;
 
-        for (int i = 0; i < n_tiles; ++i) {
+        for (int i = 0; i < n_read; ++i) {
             const int s = i % S;
-            if (!mbar_wait(&full[s], (i / S) & 1, p.err)) break;
+            if (!mbar_wait(&full[s], (i / S) & 1, p.err, wait_limit)) break;
             const int T = t0 + i * kTile;
             uint8_t* kt = sK + s * Cfg::kTileBytes;
             uint8_t* vt = sV + s * Cfg::kTileBytes;
@@ -522,8 +542,9 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
 #pragma unroll
                     for (int off = 4; off < 32; off <<= 1)
                         l_run[hh][nt][j] += __shfl_xor_sync(0xffffffffu, l_run[hh][nt][j], off);
-        // every consumer warp is done with the ring before the merge area overwrites it
-        asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
+        // every consumer warp is done with the ring, and every copy into it has landed,
+        // before the merge area overwrites it
+        asm volatile("bar.sync 1, %0;" ::"r"((kConsumers + 1) * 32) : "memory");
 #pragma unroll
         for (int hh = 0; hh < HPT; ++hh)
 #pragma unroll

@@ -50,23 +50,21 @@ extern "C" int attn_decode_gqa_paged_static_ws(const void* q, const void* k_pool
                                                float* lse_out, int B, int Hq, int Hkv, int D,
                                                int page_size, int max_pages, int num_pages,
                                                float scale, int dtype, cudaStream_t stream) {
-    // Arguments the plan depends on are checked here; gqa_run checks everything again.
-    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_pages < 1 || page_size < 1 ||
-        (D != 64 && D != 128) || (dtype != KVD_F32 && dtype != KVD_BF16))
-        return kvd::gqa_run(q, k_pool, v_pool, block_table, seq_lens, out, lse_out, B, Hq, Hkv,
-                            D, page_size, max_pages, num_pages, scale, dtype, 0, 0, nullptr,
-                            nullptr, 0, stream);
-    if ((long long)max_pages * page_size >= (1LL << 30)) return KVD_ERR_UNSUPPORTED;
+    // Every argument check runs before the shared array is touched: a rejected call leaves
+    // it (and any call still running on it) alone.
+    const int st = kvd::gqa_check(q, k_pool, v_pool, block_table, seq_lens, out, B, Hq, Hkv, D,
+                                  page_size, max_pages, num_pages, scale, dtype, 0, 0, 0);
+    if (st != KVD_OK) return st;
     kvd::GqaPlan plan;
     if (kvd::gqa_plan(B, Hq, Hkv, D, page_size, max_pages * page_size, 0, 0, dtype, &plan) !=
         KVD_OK)
         return KVD_ERR_UNSUPPORTED;
     if (plan.total > kStaticWsBytes) return KVD_ERR_WORKSPACE_TOO_SMALL;
     void* ws = nullptr;
-    const int st = static_ws_addr(&ws);
-    if (st != KVD_OK) return st;
+    const int sa = static_ws_addr(&ws);
+    if (sa != KVD_OK) return sa;
     // Every call shares the array and finds the previous call's contents in it: the error
-    // flag and the work-queue counters must start at zero.
+    // flag and the completion counters must start at zero.
     if (cudaMemsetAsync(ws, 0, plan.off_lse, stream) != cudaSuccess) return KVD_ERR_CUDA;
     return kvd::gqa_run(q, k_pool, v_pool, block_table, seq_lens, out, lse_out, B, Hq, Hkv, D,
                         page_size, max_pages, num_pages, scale, dtype, 0, 0, nullptr, ws,

@@ -62,13 +62,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed. Returns false (and
-// records KVD_ERR_TIMEOUT) if that does not happen within kWaitCycles.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+// records KVD_ERR_TIMEOUT) if that does not happen within `limit` cycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
+                                          long long limit = kWaitCycles) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const long long start = clock64();
     while (!mbar_try_wait(a, parity)) {
-        if (clock64() - start > kWaitCycles) {
+        if (clock64() - start > limit) {
             record_error(err, KVD_ERR_TIMEOUT);
             return false;
         }

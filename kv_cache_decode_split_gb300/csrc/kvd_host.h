@@ -36,6 +36,9 @@ struct GqaParams {
     int chunk, max_chunks;
     int dtype;
     float scale_log2;  // scale * log2(e)
+    long long wait_cycles;  // limit of each bounded wait of the bf16 kernel's ring
+    int stall_test;         // test of the give-up path: the consumers first wait on a
+                            // barrier that nothing completes, so their wait runs out
 };
 
 // Host-side split plan and workspace layout of one GQA / SWA call.
@@ -52,6 +55,12 @@ int gqa_plan(int B, int Hq, int Hkv, int D, int page_size, int max_len, int wind
              int dtype, GqaPlan* plan);
 int gqa_launch(const GqaPlan& plan, const GqaParams& p, const CUtensorMap* tk,
                const CUtensorMap* tv, cudaStream_t stream);
+
+// Host-side argument checks of one GQA / SWA decode (everything but the workspace).
+int gqa_check(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+              const int32_t* seq_lens, const void* out, int B, int Hq, int Hkv, int D,
+              int page_size, int max_pages, int num_pages, float scale, int dtype, int window,
+              int n_sink, int ring);
 
 // Validate, plan and launch one GQA / SWA decode (window <= 0: dense) using workspace ws.
 int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
@@ -218,7 +227,7 @@ int make_tmap_bf16_blocked(CUtensorMap* map, const void* base, uint64_t rows, ui
 
 int num_sms();
 
-// Programmatic dependent launch is on unless KVD_PDL=0 (read once).
+// Programmatic dependent launch is on unless kvd_set_option(KVD_OPT_PDL, 0).
 bool pdl_enabled();
 
 // Launch with programmatic stream serialization: the kernel may be scheduled while its

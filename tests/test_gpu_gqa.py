@@ -82,12 +82,15 @@ def test_page_sizes(kvd, P, D):
 
 @pytest.mark.parametrize("chunk", [64, 192])
 @pytest.mark.parametrize("D", [64, 128])
-def test_many_chunks(kvd, monkeypatch, chunk, D):
+def test_many_chunks(kvd, chunk, D):
     # short chunks: up to 126 chunk partials per head block in the final combine
-    monkeypatch.setenv("KVD_GQA_CHUNK", str(chunk))
     lens = [1, 100, 4000, 8000]
     x = W.make_gqa(len(lens), 16, 4, D, lens, page_size=64, shuffle=True, seed=400 + chunk + D)
-    _compare(kvd, x)
+    kvd.kvd_set_option("gqa_chunk", chunk)
+    try:
+        _compare(kvd, x)
+    finally:
+        kvd.kvd_set_option("gqa_chunk", 0)
 
 
 def test_fp32_paged_shuffled(kvd):
@@ -157,3 +160,51 @@ def test_out_of_range_page_is_recorded_not_faulted(kvd):
                               x.block_table.to(dev), x.seq_lens.to(dev), workspace=ws)
     assert kvd.kvd_check_device_error(ws) == -6
     assert kvd.kvd_check_device_error(ws) == 0   # cleared
+
+
+@pytest.mark.parametrize("D,P", [(128, 64), (64, 16), (64, 64)])
+def test_non_finite_slots_past_end(kvd, D, P):
+    # slots past each sequence's last token hold NaN, +Inf and -Inf in turn, unused pages
+    # NaN: none is visible, so the output must not change ("All the attentions", section 8)
+    lens = [1, 63, 65, 127, 700, 3001]
+    x = W.make_gqa(len(lens), 16, 4, D, lens, page_size=P, shuffle=True, extra_pages=3,
+                   seed=460 + D + P)
+    used = set()
+    bad = [float("nan"), float("inf"), float("-inf")]
+    for pool in (x.k_pool, x.v_pool):
+        for b, L in enumerate(lens):
+            n = -(-L // P)
+            used.update(int(v) for v in x.block_table[b, :n])
+            last, r = int(x.block_table[b, n - 1]), L - (n - 1) * P
+            for slot in range(r, P):
+                pool[last, :, slot] = bad[slot % 3]
+        for pg in range(pool.shape[0]):
+            if pg not in used:
+                pool[pg] = float("nan")
+    _compare(kvd, x)
+
+
+@pytest.mark.parametrize("D,lens", [(128, [100, 2000, 4000, 7000]), (64, [3, 64, 130])])
+def test_bounded_wait_gives_up_and_reports_timeout(kvd, D, lens):
+    # One call whose copy-ring waits are limited to ~1000 cycles and whose consumer warps
+    # first wait on a barrier nothing completes: the wait runs out, the call records
+    # KVD_ERR_TIMEOUT instead of hanging, waits for the copies it issued and returns. The
+    # next call on the same workspace is exact again (its counters were left at zero).
+    x = W.make_gqa(len(lens), 16, 4, D, lens, page_size=64, shuffle=True, seed=470 + D)
+    dev = "cuda"
+    ws = kvd.Workspace(dev)
+    args = (x.q.to(dev), x.k_pool.to(dev), x.v_pool.to(dev), x.block_table.to(dev),
+            x.seq_lens.to(dev))
+    kvd.kvd_set_option("wait_timeout_test", 1)
+    try:
+        kvd.attn_decode_gqa_paged(*args, scale=x.scale, workspace=ws)
+        assert kvd.kvd_check_device_error(ws) == -4
+    finally:
+        kvd.kvd_set_option("wait_timeout_test", 0)
+    for _ in range(2):
+        lse = torch.empty(x.B, x.Hq, dtype=torch.float32, device=dev)
+        out = kvd.attn_decode_gqa_paged(*args, scale=x.scale, lse_out=lse, workspace=ws)
+        assert kvd.kvd_check_device_error(ws) == 0
+        ref, ref_lse = oracle.gqa(x.q, x.k_pool, x.v_pool, x.block_table, x.seq_lens, x.scale)
+        assert_attn_close(out, ref, what="after a timed-out call")
+        assert np.max(np.abs(to_np(lse) - ref_lse)) < 2e-3
