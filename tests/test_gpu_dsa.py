@@ -13,6 +13,7 @@ import torch
 
 import oracle
 import workloads as W
+from tests.parity import assert_attn_close
 
 pytestmark = pytest.mark.gpu
 
@@ -201,3 +202,59 @@ def test_workspace_reused_across_shapes(kvd):
             assert int(cnt[b]) == min(k, L)
             assert np.array_equal(idx[b].cpu().numpy()[:len(ref)], ref), (B, L, k, b)
         assert kvd.kvd_check_device_error(ws) == 0
+
+
+def _chain(kvd, xi, xm, batches, n_pairs, seed):
+    """The DSA step as one pipeline ("Attention Optimizations", DSA / Computation Path:
+    indexer scores, top-k, then attention over the selected cache rows): the indexer's own
+    output (ascending positions, -1 padded, count) goes straight into the sparse MLA. The
+    oracle runs the same chain: its fp64 scores, its top-k on them rounded to float32, its
+    MLA over that selection. Where the GPU's selection differs only by near-ties (checked
+    first), the output is compared with the oracle's MLA over the GPU's selection."""
+    dev = "cuda"
+    bt, sl = xm.block_table.to(dev), xm.seq_lens.to(dev)
+    idx, cnt = kvd.dsa_indexer_topk(xi.q.to(dev), xi.k_pool.to(dev), xi.w.to(dev), bt, sl,
+                                    k=xi.k)
+    lse = torch.empty(xm.B, xm.H, dtype=torch.float32, device=dev)
+    out = kvd.attn_decode_mla_sparse(xm.q.to(dev), xm.c_pool.to(dev), bt, sl, idx, cnt,
+                                     scale=xm.scale, lse_out=lse)
+    torch.cuda.synchronize()
+    scores = oracle.indexer_scores(xi.q, xi.k_pool, xi.w, xi.block_table, xi.seq_lens,
+                                   batches=batches)
+    idx_h, cnt_h = idx.cpu().numpy(), cnt.cpu().numpy()
+    ref_idx = np.full((xm.B, xi.k), -1, np.int32)
+    ref_cnt = np.zeros(xm.B, np.int32)
+    use_idx, use_cnt = ref_idx.copy(), ref_cnt.copy()
+    for r, b in enumerate(batches):
+        L = int(xm.seq_lens[b])
+        _check_selection(idx[b], cnt[b], scores[r], L, xi.k)
+        sel = oracle.topk(scores[r, :L].astype(np.float32).astype(np.float64), xi.k)
+        ref_idx[b, :len(sel)], ref_cnt[b] = sel, len(sel)
+        same = np.array_equal(idx_h[b], ref_idx[b])
+        use_idx[b], use_cnt[b] = (ref_idx[b], ref_cnt[b]) if same else (idx_h[b], cnt_h[b])
+    rng = np.random.default_rng(seed)
+    pr = np.stack([rng.choice(batches, n_pairs), rng.integers(0, xm.H, n_pairs)], 1)
+    pr = pr.astype(np.int32)
+    ref, ref_lse = oracle.mla(xm.q, xm.c_pool, xm.block_table, xm.seq_lens, xm.scale,
+                              idx=use_idx, idx_count=use_cnt, pairs=pr)
+    assert_attn_close(out[pr[:, 0], pr[:, 1]], ref, what="indexer -> top-k -> sparse MLA")
+    got_lse = lse.cpu().double().numpy()[pr[:, 0], pr[:, 1]]
+    assert np.max(np.abs(got_lse - ref_lse)) < 2e-3 * max(1.0, np.abs(ref_lse).max())
+
+
+def test_dsa_chain_ragged(kvd):
+    # sequences shorter than k (every token kept, count < k, -1 padding), exactly k, and
+    # longer; sharp entries so that the selection decides the output
+    lens = [1, 100, 2047, 2048, 2049, 30000]
+    xm = W.make_mla(len(lens), 128, lens, page_size=64, shuffle=True, extra_pages=3, seed=910,
+                    factor=1.0)
+    xi = W.make_indexer(len(lens), lens, k=2048, page_size=64, seed=911,
+                        block_table=xm.block_table)
+    _chain(kvd, xi, xm, list(range(len(lens))), 96, 912)
+
+
+def test_dsa_chain_full_size(kvd):
+    # the DSA workload (B=4, L=131072, k=2048) in the launch configuration the bench times,
+    # sampled (sequence, head) outputs of two sequences
+    xi, xm = W.build("dsa_sparse_mla")
+    _chain(kvd, xi, xm, [0, 2], 48, 913)
