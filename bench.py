@@ -4,8 +4,12 @@ One step = one decode-attention call over one batch of synthetic, seeded inputs 
 KV cache is already resident in HBM. The headline workload is the Llama-3-8B-shaped GQA
 decode over a 64-token paged cache with a shuffled block table (B=32, Hq=32, Hkv=8,
 D=128, L ~ U[4096, 8192]); its KV bytes (~805 MB) exceed L2, so consecutive steps cannot
-be served from cache. The sliding-window, MLA and DSA workloads are measured too (one
-step each between L2 flushes, flush excluded) and reported under "workloads".
+be served from cache. The sliding-window, MLA, DSA, Quest and delta-rule workloads are
+measured too and reported under "workloads": steps back to back over ceil(2 L2 / bytes) + 1
+rotating copies of the cache (L2 size from the device; a CUDA graph of the steps, so no
+host launch overhead), and single steps between L2 flushes (flush excluded). Each one's
+configuration, byte and FLOP counts and roofline go on a "workload {...}" line before the
+result line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {kvdecode,reference}]
 
@@ -34,8 +38,12 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 NOMINAL_HBM_GBS = 8000.0
-L2_BYTES = 129e6                   # GB300 L2
 HEADLINE = "llama3_8b_gqa_paged"
+
+
+def l2_bytes(dev):
+    """L2 size of the device, as the CUDA runtime reports it."""
+    return int(torch.cuda.get_device_properties(dev).L2_cache_size)
 
 
 # DRAM traffic (read + write bytes per launch) of a workload's dominant kernel from one ncu
@@ -100,6 +108,7 @@ class GqaRunner:
     cache_append of the step's new token then attn_decode_swa_ring."""
     launches_per_step = 1          # split-KV kernel; its last CTA per group combines
     kernel = "gqa_decode_bf16_kernel"
+    cache_attrs = ("k", "v")       # the cache a step reads (copied for rotation)
 
     def __init__(self, name, dev):
         import kv_cache_decode_split_gb300 as kvd
@@ -227,6 +236,8 @@ class MlaRunner:
     """attn_decode_mla on the DeepSeek-V3-shaped workload (128 heads, 576-wide rows)."""
     launches_per_step = 2          # split kernel (2-CTA clusters) + combine kernel
     kernel = "mla_decode_kernel"
+    cache_attrs = ("c",)
+    tensor_path = True             # score and value products on tcgen05
 
     def __init__(self, name, dev, sharp=False):
         import kv_cache_decode_split_gb300 as kvd
@@ -294,6 +305,8 @@ class DsaRunner:
     """dsa_indexer_topk then attn_decode_mla_sparse (indexer, top-2048, sparse MLA)."""
     launches_per_step = 4          # indexer, selection, sparse MLA, combine
     kernel = "dsa_indexer_kernel"
+    cache_attrs = ("ki", "c")
+    tensor_path = True             # indexer and sparse MLA products on tcgen05
 
     def __init__(self, name, dev, sharp=False):
         import kv_cache_decode_split_gb300 as kvd
@@ -381,6 +394,7 @@ class DsaRunner:
 class DsaFp8Runner(DsaRunner):
     """dsa_indexer_topk_fp8 then attn_decode_mla_sparse (FP8 indexer, top-2048, sparse MLA)."""
     kernel = "dsa_indexer_fp8_kernel"
+    cache_attrs = ("ki", "ks", "c")
 
     def __init__(self, name, dev, sharp=False):
         import kv_cache_decode_split_gb300 as kvd
@@ -466,6 +480,7 @@ class DeltaRunner:
     """delta_decode_step: one gated delta-rule (KDA) token step over every head's state."""
     launches_per_step = 1
     kernel = "delta_step_kernel"
+    cache_attrs = ("S",)
     dtype = "f32"
     data = "synthetic: seeded float32 draws (state, unit-norm keys and queries), Kimi Linear shapes"
 
@@ -536,6 +551,7 @@ class QuestRunner(GqaRunner):
     as pages fill in a real decode)."""
     launches_per_step = 2          # bounds; choice + attention
     kernel = "quest_attn_kernel"
+    cache_attrs = ("k", "v", "kmin", "kmax")
 
     def __init__(self, name, dev):
         super().__init__(name, dev)
@@ -718,6 +734,52 @@ def time_flushed(fn, iters, stream, flush):
     return per
 
 
+def rotation_copies(nbytes, l2):
+    """Independent cache copies to rotate through so that no step finds its data in L2:
+    ceil(2 L2 / bytes) + 1 (two L2 sizes of other data between two reads of one copy)."""
+    return max(1, math.ceil(2 * l2 / max(1, nbytes)) + 1)
+
+
+def time_rotating(runner, copies, stream, steps_min=40, repeats=5):
+    """Per-step time (ms, median of `repeats`) of steps run back to back, step i reading
+    cache copy i mod `copies` (the runner's cache_attrs swapped in), captured once into a
+    CUDA graph and replayed, so that host-side launch overhead is not in the number (a
+    caller launching from C++ or from its own graph pays none either). Falls back to an
+    eager loop if the capture fails; returns (ms, how)."""
+    attrs = runner.cache_attrs
+    orig = {a: getattr(runner, a) for a in attrs}
+    sets = [orig] + [{a: t.clone() for a, t in orig.items()} for _ in range(copies - 1)]
+    n = max(steps_min, copies) // copies * copies
+
+    def run_all():
+        for i in range(n):
+            for a, t in sets[i % copies].items():
+                setattr(runner, a, t)
+            runner.step()
+
+    run_all()          # every copy once, eagerly (workspaces sized before capture)
+    torch.cuda.synchronize()
+    how = "cuda graph"
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run_all()
+        replay = g.replay
+        replay()
+        torch.cuda.synchronize()
+    except Exception:  # noqa: BLE001 -- capture unsupported: time the same loop eagerly
+        g, replay, how = None, run_all, "eager"
+        torch.cuda.synchronize()
+    per = []
+    for _ in range(repeats):
+        total, _ = time_steps(replay, 1, stream)
+        per.append(total / n)
+    for a, t in orig.items():
+        setattr(runner, a, t)
+    del sets, g
+    return statistics.median(per), how
+
+
 # ---------------------------------------------------------------------------------------
 def oracle_runner(name):
     """A runner holding only the CPU inputs of a workload, for timing the oracle."""
@@ -797,22 +859,31 @@ def main():
     peaks, peak_src = measured_peaks()
 
     r = make_runner(args.workload, dev)
+    # a workload whose data would stay in L2 between steps rotates through independent
+    # copies of its cache; larger ones run back to back on one copy
+    l2 = l2_bytes(dev)
+    copies = rotation_copies(r.bytes, l2) if r.bytes < 2 * l2 else 1
+    if copies > 1:
+        for a, t in {a: getattr(r, a) for a in r.cache_attrs}.items():
+            setattr(r, a + "_rot", [t] + [t.clone() for _ in range(copies - 1)])
+        i_step = [0]
+
+        def step_main():
+            i = i_step[0] % copies
+            for a in r.cache_attrs:
+                setattr(r, a, getattr(r, a + "_rot")[i])
+            i_step[0] += 1
+            r.step()
+    else:
+        step_main = r.step
     for _ in range(args.warmup):
-        r.step()
+        step_main()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    # a workload whose data fit in L2 is timed one step at a time between L2 flushes (flush
-    # excluded); larger ones back to back
-    small = r.bytes < L2_BYTES
-    flush_main = torch.zeros(128 << 20, dtype=torch.float32, device=dev) if small else None
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
-        if small:
-            per = time_flushed(r.step, args.steps, stream, lambda: flush_l2(flush_main))
-            total_ms = sum(per)
-        else:
-            total_ms, per = time_steps(r.step, args.steps, stream)
+        total_ms, per = time_steps(step_main, args.steps, stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -836,10 +907,9 @@ def main():
         "metric": "decode-attn KV GB/s", "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": getattr(r, "dtype", "bf16"),
-        "data": getattr(r, "data", "synthetic: seeded N(0,1) rounded to bf16, shapes of the "
-                                   "named workload"),
-        "config": dict(r.config(), l2=("flushed before each step (512 MB read), flush "
-                                       "excluded" if small else
+        "data": getattr(r, "data", "synthetic: seeded N(0,1) rounded to bf16, workload shapes"),
+        "config": dict(r.config(), l2=(f"{copies} cache copies rotated, steps back to back"
+                                       if copies > 1 else
                                        "KV bytes larger than L2; steps back to back"),
                        parallelism=f"replicas{world}" if world > 1 else "single"),
         "steps_per_s": 1000.0 / ms,
@@ -856,41 +926,57 @@ def main():
         "gpu_launches": r.launches_per_step * args.steps,
         "clocks": clocks,
     }
+    del r, step_main
+    torch.cuda.empty_cache()
 
-    # other workloads: one step between L2 flushes (flush excluded from the timing)
+    # The other workloads: each step's roofline against the measured peaks, from steps run
+    # back to back over rotating cache copies (us), and from single steps between L2
+    # flushes, flush excluded (us_flushed). Their configurations and byte / FLOP counts go
+    # on lines of their own before the result line, which stays short.
     extras = [] if args.extra == "none" else (
         [n for n in W.WORKLOADS if n not in (args.workload, "tiny_gqa_fp32")] if args.extra == "all"
         else [n for n in args.extra.split(",") if n])
     if extras and rank == 0:
-        flush_buf = torch.zeros(128 << 20, dtype=torch.float32, device=dev)   # 512 MB
+        flush_buf = torch.zeros(2 * l2 // 4 + (1 << 20), dtype=torch.float32, device=dev)
         res = {}
-        del r
         for name in extras:
             try:
                 rr = make_runner(name, dev)
-            except KeyError:
-                res[name] = {"status": "not built"}
-                continue
-            try:
                 for _ in range(3):
                     rr.step()
                 torch.cuda.synchronize()
                 per = time_flushed(rr.step, max(10, args.steps // 2), stream,
                                    lambda: flush_l2(flush_buf))
-            except Exception as e:  # an entry point not built yet reports, not crashes
-                res[name] = {"status": f"error: {e}"}
-                del rr
+                n_copies = rotation_copies(rr.bytes, l2)
+                rot_ms, how = time_rotating(rr, n_copies, stream)
+            except Exception as e:  # an entry point that fails reports, not crashes
+                res[name] = {"status": f"error: {e}"[:120]}
                 continue
-            med = statistics.median(per)
-            gbs = rr.bytes / (med * 1e-3) / 1e9
-            res[name] = {"us_per_step": med * 1e3, "kv_GBps": gbs, "steps_per_s": 1000.0 / med,
-                         "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
-                         "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
-                         "tflops": rr.flops / (med * 1e-3) / 1e12, "kernel": rr.kernel,
-                         "l2": "flushed before each step (512 MB read)", "config": rr.config()}
+            flushed_ms = statistics.median(per)
+            gbs = rr.bytes / (rot_ms * 1e-3) / 1e9
+            entry = {"us": round(rot_ms * 1e3, 2), "us_flushed": round(flushed_ms * 1e3, 2),
+                     "GBps": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
+            tfl = rr.flops / (rot_ms * 1e-3) / 1e12
+            if getattr(rr, "tensor_path", False):
+                entry["TFLOPs"] = round(tfl, 1)
+                entry["tensor_frac"] = round(tfl / peaks["bf16_tflops_sustained"], 4)
+            res[name] = entry
+            print("workload " + json.dumps({
+                "name": name, "config": rr.config(), "kernel": rr.kernel,
+                "launches_per_step": rr.launches_per_step, "algorithmic_bytes": rr.bytes,
+                "flops": rr.flops, "rotation": f"{n_copies} copies, {how}",
+                "flush": f"{flush_buf.numel() * 4 >> 20} MiB read between steps",
+                "roofline": {"bound": "hbm", "achieved_GBps": gbs, "peak_GBps": peaks["hbm_gbs"],
+                             "frac": gbs / peaks["hbm_gbs"], "achieved_TFLOPs": tfl,
+                             "peak_TFLOPs": peaks["bf16_tflops_sustained"],
+                             "traffic": ncu_traffic(name)},
+                "us_per_step": rot_ms * 1e3, "us_flushed": flushed_ms * 1e3}), flush=True)
             del rr
             torch.cuda.empty_cache()
         line["workloads"] = res
+        line["workloads_note"] = ("us: back to back over rotating cache copies; frac: algorithmic "
+                                  "bytes / us over measured HBM; tensor_frac: FLOPs / us over "
+                                  "measured sustained bf16")
 
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         rr = oracle_runner(args.workload)
