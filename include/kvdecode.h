@@ -447,13 +447,20 @@ int kvd_delta_decode_step(float *S, const float *q, const float *k, const float 
  *                         KVD_ERR_TIMEOUT (read with kvd_check_device_error), waits for the
  *                         copies it issued and returns; its outputs are undefined and its
  *                         workspace stays ready for the next call.
+ *  KVD_OPT_GQA_CLUSTER    1 (default): a bf16 GQA / SWA call with few (sequence, KV head)
+ *                         groups, whose groups need few chunks, runs each group's chunks as
+ *                         one thread-block cluster that combines them in distributed shared
+ *                         memory; 2: also with many groups, when each needs at most 8 chunks;
+ *                         0: the chunk partials always go through the workspace and the last
+ *                         CTA of each group combines them.
  * Returns KVD_OK, or KVD_ERR_INVALID_ARG for an unknown option or a value out of range.
  */
 enum kvd_option {
     KVD_OPT_PDL = 0,
     KVD_OPT_GQA_CHUNK = 1,
     KVD_OPT_MLA_MIN_TILES = 2,
-    KVD_OPT_WAIT_TIMEOUT_TEST = 3
+    KVD_OPT_WAIT_TIMEOUT_TEST = 3,
+    KVD_OPT_GQA_CLUSTER = 4
 };
 int kvd_set_option(int option, long long value);
 

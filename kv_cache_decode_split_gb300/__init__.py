@@ -84,7 +84,7 @@ def kvd_check_device_error(ws, stream=None):
 
 def kvd_set_option(option, value):
     """Process-wide library option (measurement and tests of the library; see kvdecode.h):
-    "pdl", "gqa_chunk", "mla_min_tiles" or "wait_timeout_test"."""
+    "pdl", "gqa_chunk", "mla_min_tiles", "wait_timeout_test" or "gqa_cluster"."""
     _check(lib.kvd_set_option(OPTION[option] if isinstance(option, str) else int(option),
                               int(value)), "kvd_set_option")
 

@@ -41,7 +41,8 @@ STATUS = {
     -4: "KVD_ERR_TIMEOUT", -5: "KVD_ERR_WORKSPACE_TOO_SMALL", -6: "KVD_ERR_DEVICE_OOB", -7: "KVD_ERR_DEVICE_STATE",
 }
 OP = {"gqa": 0, "swa": 1, "mla": 2, "dsa_topk": 3, "mla_sparse": 4}
-OPTION = {"pdl": 0, "gqa_chunk": 1, "mla_min_tiles": 2, "wait_timeout_test": 3}
+OPTION = {"pdl": 0, "gqa_chunk": 1, "mla_min_tiles": 2, "wait_timeout_test": 3,
+          "gqa_cluster": 4}
 
 
 class KvdError(RuntimeError):

@@ -29,6 +29,7 @@ std::atomic<int> g_opt_pdl{1};
 std::atomic<long long> g_opt_gqa_chunk{0};
 std::atomic<long long> g_opt_mla_min_tiles{1};
 std::atomic<int> g_opt_wait_test{0};
+std::atomic<int> g_opt_gqa_cluster{1};
 
 }  // namespace
 
@@ -145,8 +146,8 @@ int gqa_plan(int B, int Hq, int Hkv, int D, int page_size, int max_len, int wind
         chunk = std::max(256LL, (vis + per_group - 1) / per_group);
         chunk = (chunk + 63) / 64 * 64;
     }
-    if (const long long c = g_opt_gqa_chunk.load(std::memory_order_relaxed); c >= 64)
-        chunk = (c / 64) * 64;  // fixed chunk (KVD_OPT_GQA_CHUNK)
+    const long long forced = g_opt_gqa_chunk.load(std::memory_order_relaxed);
+    if (forced >= 64) chunk = (forced / 64) * 64;  // fixed chunk (KVD_OPT_GQA_CHUNK)
     auto chunks_for = [&](long long C) -> int {
         if (window <= 0) return cdiv(max_len, C);
         const int a = (n_sink > 0 ? cdiv(std::min(n_sink, max_len), C) : 0) +
@@ -155,6 +156,25 @@ int gqa_plan(int B, int Hq, int Hkv, int D, int page_size, int max_len, int wind
         return std::max(a, m);
     };
     while (chunks_for(chunk) > kGqaMaxChunks) chunk += 64;
+    // Cluster combine (bf16): the chunks of a group form one thread-block cluster of at most
+    // 8 CTAs and combine through distributed shared memory, with no global round trip after
+    // the last chunk (measured: the workspace combine is ~3.5 us of a sliding-window step).
+    // Taken when a group needs at most 8 chunks anyway, or when raising the chunk to get 8
+    // still leaves at least three quarters of a wave of CTAs.
+    // (KVD_OPT_GQA_CLUSTER = 2 also takes it for many groups when they need <= 8 chunks.)
+    plan->cluster = 0;
+    const int copt = g_opt_gqa_cluster.load(std::memory_order_relaxed);
+    if (dtype == KVD_BF16 && forced < 64 && copt > 0) {
+        const long long slots = 2LL * num_sms();
+        long long cc = chunk;
+        while (chunks_for(cc) > 8) cc += 64;
+        const bool few = 2 * groups <= slots;
+        if ((few && (chunks_for(chunk) <= 8 || 4 * groups * chunks_for(cc) >= 3 * slots)) ||
+            (copt == 2 && chunks_for(chunk) <= 8)) {
+            chunk = cc;
+            plan->cluster = std::max(1, chunks_for(cc));
+        }
+    }
     plan->chunk = static_cast<int>(chunk);
     plan->max_chunks = std::max(1, chunks_for(chunk));
     size_t off = kWsHeaderBytes;
@@ -872,6 +892,10 @@ int kvd_set_option(int option, long long value) {
         case KVD_OPT_WAIT_TIMEOUT_TEST:
             if (value != 0 && value != 1) return KVD_ERR_INVALID_ARG;
             g_opt_wait_test.store(static_cast<int>(value));
+            return KVD_OK;
+        case KVD_OPT_GQA_CLUSTER:
+            if (value < 0 || value > 2) return KVD_ERR_INVALID_ARG;
+            g_opt_gqa_cluster.store(static_cast<int>(value));
             return KVD_OK;
         default: return KVD_ERR_INVALID_ARG;
     }

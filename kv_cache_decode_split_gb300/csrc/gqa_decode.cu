@@ -258,6 +258,128 @@ __device__ void finish_group(const GqaParams& p, CombineSmem<ROWS>& cs, int b, i
 }
 
 // ---------------------------------------------------------------------------------------
+// Cluster combine: when the CTAs of one group (its chunks) form a thread-block cluster, the
+// chunk partials never leave the cluster. Each CTA merges its four warps into a partial in
+// its own shared memory; after a cluster barrier, CTA r combines rows r, r + CS, ... of the
+// group from every CTA's partial over distributed shared memory and writes them; a second
+// barrier keeps every partial in place until all have been read. No workspace counters,
+// no global round trips.
+// ---------------------------------------------------------------------------------------
+template <int D, int ROWS>
+struct ClusterPart {
+    float lse[ROWS];   // log2-sum-exp of the chunk; -inf when the chunk saw nothing
+    float o[ROWS][D];  // the chunk's output, normalised by its own sum
+};
+
+template <int D, int HP, int ROWS>
+__device__ void merge_to_part(MergeSmem<D, HP>* ms, ClusterPart<D, ROWS>& pt, int nkv, int G_cta) {
+    const int rows = nkv * G_cta;
+    for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+        MergeSmem<D, HP>& m = ms[r / G_cta];
+        const int h = r % G_cta;
+        float M = neg_inf();
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, m.m[w][h]);
+        if (M == neg_inf()) {  // an empty chunk (its outputs are zeros)
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) m.m[w][h] = 0.f;
+            pt.lse[r] = neg_inf();
+            continue;
+        }
+        float f[kConsumers], L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) {
+            f[w] = fast_exp2(m.m[w][h] - M);
+            L += m.l[w][h] * f[w];
+        }
+        const float inv = 1.f / L;
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) m.m[w][h] = f[w] * inv;
+        pt.lse[r] = M + log2f(L);
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < rows * (D / 4); idx += blockDim.x) {
+        const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
+        const MergeSmem<D, HP>& m = ms[r / G_cta];
+        const int h = r % G_cta;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) {
+            const float f = m.m[w][h];
+            const float4 v = *reinterpret_cast<const float4*>(&m.o[w][h][d]);
+            o.x += f * v.x;
+            o.y += f * v.y;
+            o.z += f * v.z;
+            o.w += f * v.w;
+        }
+        *reinterpret_cast<float4*>(&pt.o[r][d]) = o;
+    }
+}
+
+template <int D, int ROWS>
+__device__ void combine_cluster(const GqaParams& p, const ClusterPart<D, ROWS>& pt,
+                                CombineSmem<ROWS>& cs, int b, int kv0, int nkv, int hg, int G_cta,
+                                int CS, int rank) {
+    const int rows = nkv * G_cta;
+    const int mine = rank < rows ? (rows - rank + CS - 1) / CS : 0;  // rows rank + CS i
+    const uint32_t lse0 = smem_u32(&pt.lse[0]), o0 = smem_u32(&pt.o[0][0]);
+    uint32_t peer_lse[8], peer_o[8];
+    for (int c = 0; c < CS; ++c) {
+        peer_lse[c] = map_peer(lse0, c);
+        peer_o[c] = map_peer(o0, c);
+    }
+    for (int idx = threadIdx.x; idx < mine * CS; idx += blockDim.x) {
+        const int rl = idx / CS, c = idx % CS;
+        cs.wgt[rl][c] = ld_cluster_f32(peer_lse[c] + (rank + rl * CS) * 4);
+    }
+    __syncthreads();
+    for (int rl = threadIdx.x; rl < mine; rl += blockDim.x) {
+        const int r = rank + rl * CS;
+        const int hq = (kv0 + r / G_cta) * p.G + hg * kMaxHP + r % G_cta;
+        float M = p.sink_logit ? p.sink_logit[hq] * kLog2e : neg_inf();
+        const float sig = M;
+        for (int c = 0; c < CS; ++c) M = fmaxf(M, cs.wgt[rl][c]);
+        float den = p.sink_logit ? fast_exp2(sig - M) : 0.f;
+        for (int c = 0; c < CS; ++c) {
+            const float wv = fast_exp2(cs.wgt[rl][c] - M);
+            cs.wgt[rl][c] = wv;
+            den += wv;
+        }
+        cs.inv_denom[rl] = 1.f / den;
+        cs.lse_nat[rl] = (M + log2f(den)) * kLn2;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < mine * (D / 4); idx += blockDim.x) {
+        const int rl = idx / (D / 4), d = (idx % (D / 4)) * 4;
+        const int r = rank + rl * CS;
+        const uint32_t off = static_cast<uint32_t>((r * D + d) * 4);
+        float4 v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            if (c < CS) v[c] = ld_cluster_v4(peer_o[c] + off);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            if (c < CS) {
+                const float w = cs.wgt[rl][c];
+                acc.x += w * v[c].x;
+                acc.y += w * v[c].y;
+                acc.z += w * v[c].z;
+                acc.w += w * v[c].w;
+            }
+        }
+        const float inv = cs.inv_denom[rl];
+        const int hq = (kv0 + r / G_cta) * p.G + hg * kMaxHP + r % G_cta;
+        const size_t o = (static_cast<size_t>(b) * p.Hq + hq) * D + d;
+        __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&lo2), *reinterpret_cast<uint32_t*>(&hi2));
+        if (d == 0 && p.lse_out) p.lse_out[static_cast<size_t>(b) * p.Hq + hq] = cs.lse_nat[rl];
+    }
+}
+
+// ---------------------------------------------------------------------------------------
 // bf16 kernel: TMA ring + mma.sync, HPT KV heads per tile
 // ---------------------------------------------------------------------------------------
 template <int D, int NT, int HPT>
@@ -267,13 +389,17 @@ struct GqaBf16Cfg {
     static constexpr int kRingBytes = 2 * kStages * kTileBytes;
     static constexpr int kMergeBytes = HPT * static_cast<int>(sizeof(MergeSmem<D, NT * 8>));
     static constexpr int kCombBytes = static_cast<int>(sizeof(CombineSmem<HPT * NT * 8>));
-    static constexpr int kOverlay =
-        kRingBytes > kMergeBytes + kCombBytes ? kRingBytes : kMergeBytes + kCombBytes;
+    static constexpr int kPartBytes = static_cast<int>(sizeof(ClusterPart<D, HPT * NT * 8>));
+    static constexpr int kAfterRing = kMergeBytes + kCombBytes + kPartBytes;
+    static constexpr int kOverlay = kRingBytes > kAfterRing ? kRingBytes : kAfterRing;
     static constexpr int kSmem = 1024 + kOverlay + (2 * kStages + 1) * 8;
     static constexpr int kThreads = (kConsumers + 1) * 32;
 };
 
-template <int D, int NT, int HPT>
+// kClu: the grid's x blocks (the chunks of one group) form a cluster and combine through
+// distributed shared memory; otherwise the last CTA of each group combines through the
+// workspace.
+template <int D, int NT, int HPT, bool kClu>
 __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
     gqa_decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
@@ -281,6 +407,7 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
     using Cfg = GqaBf16Cfg<D, NT, HPT>;
     using MS = MergeSmem<D, NT * 8>;
     using CS = CombineSmem<HPT * NT * 8>;
+    using PT = ClusterPart<D, HPT * NT * 8>;
     constexpr int S = Cfg::kStages;
     constexpr int KT = D / 16;  // k-steps of QK, m-tiles of PV
     constexpr int NB = D / 64;  // 64-dim column blocks
@@ -295,6 +422,7 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
     // once the ring is drained: per-KV-head merge areas, then the combine scratch
     MS* ms = reinterpret_cast<MS*>(smem);
     CS& cs = *reinterpret_cast<CS*>(smem + Cfg::kMergeBytes);
+    PT& pt = *reinterpret_cast<PT*>(smem + Cfg::kMergeBytes + Cfg::kCombBytes);
 
     const int c = blockIdx.x;
     const int n_kvg = p.Hkv / HPT;
@@ -303,8 +431,11 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
     const int b = blockIdx.z;
     const int L = visible_len(p, b);
     const Ranges R = visible_ranges(L, p.window, p.n_sink);
-    int lo, hi;
-    if (!chunk_bounds(R, p.chunk, c, lo, hi)) return;
+    int lo = 0, hi = 0;
+    // an empty chunk exits, except in a cluster, where it joins the combine with nothing
+    const bool has = chunk_bounds(R, p.chunk, c, lo, hi);
+    if (!kClu && !has) return;
+    if (!has) lo = hi = 0;
     const int n_chunks = total_chunks(R, p.chunk);
     const int t0 = lo & ~(kTile - 1);
     const int n_tiles = (hi - t0 + kTile - 1) / kTile;
@@ -567,9 +698,17 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
             }
     }
     __syncthreads();
-    merge_chunks<D, NT * 8>(p, ms, b, kvg * HPT, HPT, hg, c, G_cta);
-    const int grp = (b * n_kvg + kvg) * p.NHG + hg;
-    finish_group<D, HPT * NT * 8>(p, cs, b, kvg * HPT, HPT, hg, grp, n_chunks, G_cta);
+    if constexpr (kClu) {
+        merge_to_part<D, NT * 8, HPT * NT * 8>(ms, pt, HPT, G_cta);
+        cluster_sync();  // every chunk's partial is in place
+        combine_cluster<D, HPT * NT * 8>(p, pt, cs, b, kvg * HPT, HPT, hg, G_cta, gridDim.x,
+                                         static_cast<int>(cluster_rank()));
+        cluster_sync();  // every partial has been read
+    } else {
+        merge_chunks<D, NT * 8>(p, ms, b, kvg * HPT, HPT, hg, c, G_cta);
+        const int grp = (b * n_kvg + kvg) * p.NHG + hg;
+        finish_group<D, HPT * NT * 8>(p, cs, b, kvg * HPT, HPT, hg, grp, n_chunks, G_cta);
+    }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -664,13 +803,42 @@ template <int D, int NT, int HPT>
 int launch_bf16(const GqaPlan& plan, const GqaParams& p, const CUtensorMap& tk,
                 const CUtensorMap& tv, cudaStream_t stream) {
     using Cfg = GqaBf16Cfg<D, NT, HPT>;
-    auto kern = gqa_decode_bf16_kernel<D, NT, HPT>;
-    static int configured = 0;
+    auto kern = gqa_decode_bf16_kernel<D, NT, HPT, false>;
+    auto kern_clu = gqa_decode_bf16_kernel<D, NT, HPT, true>;
+    // per cluster size: 0 not yet checked, 1 a cluster of that size fits on the GPU, -1 not
+    static int configured = 0, clu_ok[9] = {};
     if (!configured) {
-        if (set_smem(kern, Cfg::kSmem) != KVD_OK) return KVD_ERR_CUDA;
+        if (set_smem(kern, Cfg::kSmem) != KVD_OK || set_smem(kern_clu, Cfg::kSmem) != KVD_OK)
+            return KVD_ERR_CUDA;
         configured = 1;
     }
     const dim3 grid(plan.max_chunks, (p.Hkv / HPT) * p.NHG, p.B);
+    const int cs = plan.cluster;
+    if (cs >= 1 && cs <= 8 && cs == plan.max_chunks) {
+        if (clu_ok[cs] == 0) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = grid;
+            cfg.blockDim = dim3(Cfg::kThreads);
+            cfg.dynamicSmemBytes = Cfg::kSmem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            clu_ok[cs] = (cudaOccupancyMaxActiveClusters(&n, kern_clu, &cfg) == cudaSuccess && n >= 1)
+                             ? 1 : -1;
+            cudaGetLastError();
+        }
+        if (clu_ok[cs] == 1) {
+            if (launch_kernel_cluster(kern_clu, grid, dim3(Cfg::kThreads), Cfg::kSmem, cs, stream,
+                                      tk, tv, p) != cudaSuccess)
+                return KVD_ERR_CUDA;
+            return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
+        }
+    }
     if (launch_kernel(kern, grid, dim3(Cfg::kThreads), Cfg::kSmem, stream, tk, tv, p) !=
         cudaSuccess)
         return KVD_ERR_CUDA;

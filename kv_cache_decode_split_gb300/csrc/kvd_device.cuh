@@ -111,9 +111,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 
 // Wait until the grids this one depends on (programmatic launch) have completed and their
-// memory is visible; returns at once for a plain launch. First statement of every kernel.
+// memory is visible; returns at once for a plain launch. Then allow the next kernel on the
+// stream, if it was launched with programmatic serialization, to be scheduled: its blocks
+// take SM slots as this grid's blocks exit and do their set-up while this grid finishes,
+// and each waits for this grid's completion in its own griddep_wait before it touches
+// memory. Every kernel calls this before its first global memory access.
 __device__ __forceinline__ void griddep_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Hint: bring the global line holding `ptr` into L2 (no data returned).
@@ -412,6 +417,22 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
                  "f"(c), "f"(d)
                  : "memory");
+}
+
+// Loads from another CTA's shared memory (cluster address from map_peer).
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 // Asynchronous 16-byte store into another CTA's shared memory that counts its bytes on

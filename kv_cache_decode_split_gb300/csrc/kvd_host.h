@@ -48,6 +48,7 @@ struct GqaPlan {
     int hpt;         // KV heads per K/V tile (2: D = 64 pages of <= 64 tokens, G <= 8)
     int NHG;         // head blocks of <= 16 query heads per KV head
     int units;       // B * Hkv * NHG
+    int cluster;     // > 0: the chunks of a group form a cluster of this many CTAs (= chunks)
     size_t off_counters, off_lse, off_o, total;
 };
 
@@ -233,21 +234,39 @@ bool pdl_enabled();
 // Launch with programmatic stream serialization: the kernel may be scheduled while its
 // predecessor on the stream finishes (launch and set-up overlap that tail). Every kernel of
 // the library waits for the predecessor (griddepcontrol.wait) before it touches memory, so
-// the order of memory effects is that of a plain launch.
+// the order of memory effects is that of a plain launch. With cluster_x > 0 the blocks form
+// thread-block clusters of cluster_x blocks along x (grid.x a multiple of it).
 template <typename... P, typename... A>
-inline cudaError_t launch_kernel(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
-                                 cudaStream_t stream, A&&... args) {
+inline cudaError_t launch_kernel_cluster(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                                         int cluster_x, cudaStream_t stream, A&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pdl_enabled()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_x > 0) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+}
+
+template <typename... P, typename... A>
+inline cudaError_t launch_kernel(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, A&&... args) {
+    return launch_kernel_cluster(kernel, grid, block, smem, 0, stream, static_cast<A&&>(args)...);
 }
 
 }  // namespace kvd

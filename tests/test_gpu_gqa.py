@@ -208,3 +208,30 @@ def test_bounded_wait_gives_up_and_reports_timeout(kvd, D, lens):
         ref, ref_lse = oracle.gqa(x.q, x.k_pool, x.v_pool, x.block_table, x.seq_lens, x.scale)
         assert_attn_close(out, ref, what="after a timed-out call")
         assert np.max(np.abs(to_np(lse) - ref_lse)) < 2e-3
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("case", ["ragged128", "ragged64", "swa_sinks", "swa_learned", "short"])
+def test_combine_paths(kvd, mode, case):
+    # the chunk partials combined through the workspace by the last CTA of each group (0), or
+    # inside a thread-block cluster over distributed shared memory (1: when groups are few;
+    # 2: whenever a group needs at most 8 chunks); chunks past a short sequence's end take
+    # part in the cluster combine with nothing
+    spec = {
+        "ragged128": dict(B=8, hq=32, hkv=8, D=128, lens=[1, 63, 64, 65, 200, 1000, 1500, 4097]),
+        "ragged64": dict(B=6, hq=16, hkv=4, D=64, lens=[1, 2, 129, 640, 3000, 9000]),
+        "swa_sinks": dict(B=3, hq=64, hkv=8, D=64, lens=[50, 4100, 9000], window=4096, n_sink=4),
+        "swa_learned": dict(B=2, hq=32, hkv=8, D=128, lens=[5000, 700], window=1000,
+                            learned=True),
+        "short": dict(B=2, hq=8, hkv=2, D=128, lens=[1, 3]),
+    }[case]
+    x = W.make_gqa(spec["B"], spec["hq"], spec["hkv"], spec["D"], spec["lens"], page_size=64,
+                   shuffle=True, extra_pages=3, seed=480 + mode + len(case),
+                   window=spec.get("window", 0), n_sink=spec.get("n_sink", 0),
+                   learned_sink=spec.get("learned", False))
+    kvd.kvd_set_option("gqa_cluster", mode)
+    try:
+        _compare(kvd, x)
+        _compare(kvd, x)   # the same workspace again
+    finally:
+        kvd.kvd_set_option("gqa_cluster", 1)
