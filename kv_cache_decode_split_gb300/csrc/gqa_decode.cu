@@ -259,31 +259,36 @@ __device__ void finish_group(const GqaParams& p, CombineSmem<ROWS>& cs, int b, i
 
 // ---------------------------------------------------------------------------------------
 // Cluster combine: when the CTAs of one group (its chunks) form a thread-block cluster, the
-// chunk partials never leave the cluster. Each CTA merges its four warps into a partial in
-// its own shared memory; after a cluster barrier, CTA r combines rows r, r + CS, ... of the
-// group from every CTA's partial over distributed shared memory and writes them; a second
-// barrier keeps every partial in place until all have been read. No workspace counters,
-// no global round trips.
+// chunk partials never leave the cluster. Row r of the group is combined by CTA r mod CS:
+// every CTA merges its four warps and stores each row's partial straight into the shared
+// memory of that row's CTA (distributed shared memory); after one cluster barrier each
+// CTA combines its rows from its own shared memory and writes them. No workspace counters,
+// no global round trip, no remote load.
 // ---------------------------------------------------------------------------------------
 template <int D, int ROWS>
-struct ClusterPart {
-    float lse[ROWS];   // log2-sum-exp of the chunk; -inf when the chunk saw nothing
-    float o[ROWS][D];  // the chunk's output, normalised by its own sum
+struct ClusterRx {
+    // slot c * stride + i: chunk c's partial of this CTA's i-th row (stride = ceil(rows / CS))
+    float lse[ROWS + 8];     // log2-sum-exp; -inf when the chunk saw nothing
+    float o[ROWS + 8][D];    // the chunk's output, normalised by its own sum
 };
 
 template <int D, int HP, int ROWS>
-__device__ void merge_to_part(MergeSmem<D, HP>* ms, ClusterPart<D, ROWS>& pt, int nkv, int G_cta) {
+__device__ void merge_push(MergeSmem<D, HP>* ms, ClusterRx<D, ROWS>& rx, int nkv, int G_cta,
+                           int CS, int rank) {
     const int rows = nkv * G_cta;
+    const int stride = (rows + CS - 1) / CS;
+    const uint32_t lse0 = smem_u32(&rx.lse[0]), o0 = smem_u32(&rx.o[0][0]);
     for (int r = threadIdx.x; r < rows; r += blockDim.x) {
         MergeSmem<D, HP>& m = ms[r / G_cta];
         const int h = r % G_cta;
         float M = neg_inf();
 #pragma unroll
         for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, m.m[w][h]);
+        const int slot = rank * stride + r / CS;
         if (M == neg_inf()) {  // an empty chunk (its outputs are zeros)
 #pragma unroll
             for (int w = 0; w < kConsumers; ++w) m.m[w][h] = 0.f;
-            pt.lse[r] = neg_inf();
+            st_cluster_f32(map_peer(lse0 + slot * 4, r % CS), neg_inf());
             continue;
         }
         float f[kConsumers], L = 0.f;
@@ -295,7 +300,7 @@ __device__ void merge_to_part(MergeSmem<D, HP>* ms, ClusterPart<D, ROWS>& pt, in
         const float inv = 1.f / L;
 #pragma unroll
         for (int w = 0; w < kConsumers; ++w) m.m[w][h] = f[w] * inv;
-        pt.lse[r] = M + log2f(L);
+        st_cluster_f32(map_peer(lse0 + slot * 4, r % CS), M + log2f(L));
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < rows * (D / 4); idx += blockDim.x) {
@@ -312,87 +317,73 @@ __device__ void merge_to_part(MergeSmem<D, HP>* ms, ClusterPart<D, ROWS>& pt, in
             o.z += f * v.z;
             o.w += f * v.w;
         }
-        *reinterpret_cast<float4*>(&pt.o[r][d]) = o;
+        const int slot = rank * stride + r / CS;
+        st_cluster_v4(map_peer(o0 + static_cast<uint32_t>((slot * D + d) * 4), r % CS), o.x, o.y,
+                      o.z, o.w);
     }
 }
 
 template <int D, int ROWS>
-__device__ void combine_cluster(const GqaParams& p, const ClusterPart<D, ROWS>& pt,
-                                CombineSmem<ROWS>& cs, int b, int kv0, int nkv, int hg, int G_cta,
-                                int CS, int rank) {
+__device__ void combine_rx(const GqaParams& p, const ClusterRx<D, ROWS>& rx, CombineSmem<ROWS>& cs,
+                           int b, int kv0, int nkv, int hg, int G_cta, int CS, int rank) {
     const int rows = nkv * G_cta;
+    const int stride = (rows + CS - 1) / CS;
     const int mine = rank < rows ? (rows - rank + CS - 1) / CS : 0;  // rows rank + CS i
-    const uint32_t lse0 = smem_u32(&pt.lse[0]), o0 = smem_u32(&pt.o[0][0]);
-    uint32_t peer_lse[8], peer_o[8];
-    for (int c = 0; c < CS; ++c) {
-        peer_lse[c] = map_peer(lse0, c);
-        peer_o[c] = map_peer(o0, c);
-    }
-    for (int idx = threadIdx.x; idx < mine * CS; idx += blockDim.x) {
-        const int rl = idx / CS, c = idx % CS;
-        cs.wgt[rl][c] = ld_cluster_f32(peer_lse[c] + (rank + rl * CS) * 4);
-    }
-    __syncthreads();
-    for (int rl = threadIdx.x; rl < mine; rl += blockDim.x) {
-        const int r = rank + rl * CS;
+    for (int i = threadIdx.x; i < mine; i += blockDim.x) {
+        const int r = rank + i * CS;
         const int hq = (kv0 + r / G_cta) * p.G + hg * kMaxHP + r % G_cta;
         float M = p.sink_logit ? p.sink_logit[hq] * kLog2e : neg_inf();
         const float sig = M;
-        for (int c = 0; c < CS; ++c) M = fmaxf(M, cs.wgt[rl][c]);
+        for (int c = 0; c < CS; ++c) M = fmaxf(M, rx.lse[c * stride + i]);
         float den = p.sink_logit ? fast_exp2(sig - M) : 0.f;
         for (int c = 0; c < CS; ++c) {
-            const float wv = fast_exp2(cs.wgt[rl][c] - M);
-            cs.wgt[rl][c] = wv;
+            const float wv = fast_exp2(rx.lse[c * stride + i] - M);
+            cs.wgt[i][c] = wv;
             den += wv;
         }
-        cs.inv_denom[rl] = 1.f / den;
-        cs.lse_nat[rl] = (M + log2f(den)) * kLn2;
+        cs.inv_denom[i] = 1.f / den;
+        cs.lse_nat[i] = (M + log2f(den)) * kLn2;
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < mine * (D / 4); idx += blockDim.x) {
-        const int rl = idx / (D / 4), d = (idx % (D / 4)) * 4;
-        const int r = rank + rl * CS;
-        const uint32_t off = static_cast<uint32_t>((r * D + d) * 4);
-        float4 v[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-            if (c < CS) v[c] = ld_cluster_v4(peer_o[c] + off);
+        const int i = idx / (D / 4), d = (idx % (D / 4)) * 4;
+        const int r = rank + i * CS;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            if (c < CS) {
-                const float w = cs.wgt[rl][c];
-                acc.x += w * v[c].x;
-                acc.y += w * v[c].y;
-                acc.z += w * v[c].z;
-                acc.w += w * v[c].w;
-            }
+        for (int c = 0; c < CS; ++c) {
+            const float w = cs.wgt[i][c];
+            const float4 v = *reinterpret_cast<const float4*>(&rx.o[c * stride + i][d]);
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
         }
-        const float inv = cs.inv_denom[rl];
+        const float inv = cs.inv_denom[i];
         const int hq = (kv0 + r / G_cta) * p.G + hg * kMaxHP + r % G_cta;
         const size_t o = (static_cast<size_t>(b) * p.Hq + hq) * D + d;
         __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
         __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
         *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o) =
             make_uint2(*reinterpret_cast<uint32_t*>(&lo2), *reinterpret_cast<uint32_t*>(&hi2));
-        if (d == 0 && p.lse_out) p.lse_out[static_cast<size_t>(b) * p.Hq + hq] = cs.lse_nat[rl];
+        if (d == 0 && p.lse_out) p.lse_out[static_cast<size_t>(b) * p.Hq + hq] = cs.lse_nat[i];
     }
 }
 
 // ---------------------------------------------------------------------------------------
 // bf16 kernel: TMA ring + mma.sync, HPT KV heads per tile
 // ---------------------------------------------------------------------------------------
-template <int D, int NT, int HPT>
+template <int D, int NT, int HPT, bool kClu>
 struct GqaBf16Cfg {
     static constexpr int kStages = 3;
     static constexpr int kTileBytes = HPT * kTile * D * 2;  // one K (or V) tile
     static constexpr int kRingBytes = 2 * kStages * kTileBytes;
     static constexpr int kMergeBytes = HPT * static_cast<int>(sizeof(MergeSmem<D, NT * 8>));
     static constexpr int kCombBytes = static_cast<int>(sizeof(CombineSmem<HPT * NT * 8>));
-    static constexpr int kPartBytes = static_cast<int>(sizeof(ClusterPart<D, HPT * NT * 8>));
-    static constexpr int kAfterRing = kMergeBytes + kCombBytes + kPartBytes;
+    static constexpr int kAfterRing = kMergeBytes + kCombBytes;
     static constexpr int kOverlay = kRingBytes > kAfterRing ? kRingBytes : kAfterRing;
-    static constexpr int kSmem = 1024 + kOverlay + (2 * kStages + 1) * 8;
+    // cluster combine: the partials other CTAs push, outside the ring (they may arrive while
+    // this CTA still streams)
+    static constexpr int kRxBytes = kClu ? static_cast<int>(sizeof(ClusterRx<D, HPT * NT * 8>)) : 0;
+    static constexpr int kSmem = 1024 + kOverlay + kRxBytes + (2 * kStages + 1) * 8;
     static constexpr int kThreads = (kConsumers + 1) * 32;
 };
 
@@ -400,14 +391,14 @@ struct GqaBf16Cfg {
 // distributed shared memory; otherwise the last CTA of each group combines through the
 // workspace.
 template <int D, int NT, int HPT, bool kClu>
-__global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
+__global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
     gqa_decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
     griddep_wait();
-    using Cfg = GqaBf16Cfg<D, NT, HPT>;
+    using Cfg = GqaBf16Cfg<D, NT, HPT, kClu>;
     using MS = MergeSmem<D, NT * 8>;
     using CS = CombineSmem<HPT * NT * 8>;
-    using PT = ClusterPart<D, HPT * NT * 8>;
+    using RX = ClusterRx<D, HPT * NT * 8>;
     constexpr int S = Cfg::kStages;
     constexpr int KT = D / 16;  // k-steps of QK, m-tiles of PV
     constexpr int NB = D / 64;  // 64-dim column blocks
@@ -416,13 +407,13 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sK = smem;
     uint8_t* sV = smem + S * Cfg::kTileBytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kOverlay);
+    RX& rx = *reinterpret_cast<RX*>(smem + Cfg::kOverlay);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kOverlay + Cfg::kRxBytes);
     uint64_t* empty = full + S;
     uint64_t* stall = empty + S;  // completed by nothing (give-up test only)
     // once the ring is drained: per-KV-head merge areas, then the combine scratch
     MS* ms = reinterpret_cast<MS*>(smem);
     CS& cs = *reinterpret_cast<CS*>(smem + Cfg::kMergeBytes);
-    PT& pt = *reinterpret_cast<PT*>(smem + Cfg::kMergeBytes + Cfg::kCombBytes);
 
     const int c = blockIdx.x;
     const int n_kvg = p.Hkv / HPT;
@@ -453,6 +444,9 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
         fence_mbar_init();
     }
     __syncthreads();
+    // cluster combine: no CTA stores into another's shared memory before every CTA of the
+    // cluster has started (this arrival; the matching wait comes before the first store)
+    if constexpr (kClu) cluster_arrive_relaxed();
     // Every wait of the ring is bounded; one that runs out records KVD_ERR_TIMEOUT and its
     // warp leaves the loop. The call's limit is normally kWaitCycles.
     const long long wait_limit = p.wait_cycles > 0 ? p.wait_cycles : kWaitCycles;
@@ -699,11 +693,11 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT>::kThreads, 2)
     }
     __syncthreads();
     if constexpr (kClu) {
-        merge_to_part<D, NT * 8, HPT * NT * 8>(ms, pt, HPT, G_cta);
-        cluster_sync();  // every chunk's partial is in place
-        combine_cluster<D, HPT * NT * 8>(p, pt, cs, b, kvg * HPT, HPT, hg, G_cta, gridDim.x,
-                                         static_cast<int>(cluster_rank()));
-        cluster_sync();  // every partial has been read
+        const int rank = static_cast<int>(cluster_rank());
+        cluster_wait();  // every CTA of the cluster has started
+        merge_push<D, NT * 8, HPT * NT * 8>(ms, rx, HPT, G_cta, gridDim.x, rank);
+        cluster_sync();  // every chunk's partial is in its combining CTA
+        combine_rx<D, HPT * NT * 8>(p, rx, cs, b, kvg * HPT, HPT, hg, G_cta, gridDim.x, rank);
     } else {
         merge_chunks<D, NT * 8>(p, ms, b, kvg * HPT, HPT, hg, c, G_cta);
         const int grp = (b * n_kvg + kvg) * p.NHG + hg;
@@ -802,13 +796,14 @@ int set_smem(K kernel, int bytes) {
 template <int D, int NT, int HPT>
 int launch_bf16(const GqaPlan& plan, const GqaParams& p, const CUtensorMap& tk,
                 const CUtensorMap& tv, cudaStream_t stream) {
-    using Cfg = GqaBf16Cfg<D, NT, HPT>;
+    using Cfg = GqaBf16Cfg<D, NT, HPT, false>;
+    using CfgC = GqaBf16Cfg<D, NT, HPT, true>;
     auto kern = gqa_decode_bf16_kernel<D, NT, HPT, false>;
     auto kern_clu = gqa_decode_bf16_kernel<D, NT, HPT, true>;
     // per cluster size: 0 not yet checked, 1 a cluster of that size fits on the GPU, -1 not
     static int configured = 0, clu_ok[9] = {};
     if (!configured) {
-        if (set_smem(kern, Cfg::kSmem) != KVD_OK || set_smem(kern_clu, Cfg::kSmem) != KVD_OK)
+        if (set_smem(kern, Cfg::kSmem) != KVD_OK || set_smem(kern_clu, CfgC::kSmem) != KVD_OK)
             return KVD_ERR_CUDA;
         configured = 1;
     }
@@ -818,8 +813,8 @@ int launch_bf16(const GqaPlan& plan, const GqaParams& p, const CUtensorMap& tk,
         if (clu_ok[cs] == 0) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = grid;
-            cfg.blockDim = dim3(Cfg::kThreads);
-            cfg.dynamicSmemBytes = Cfg::kSmem;
+            cfg.blockDim = dim3(CfgC::kThreads);
+            cfg.dynamicSmemBytes = CfgC::kSmem;
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
             attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
@@ -833,8 +828,8 @@ int launch_bf16(const GqaPlan& plan, const GqaParams& p, const CUtensorMap& tk,
             cudaGetLastError();
         }
         if (clu_ok[cs] == 1) {
-            if (launch_kernel_cluster(kern_clu, grid, dim3(Cfg::kThreads), Cfg::kSmem, cs, stream,
-                                      tk, tv, p) != cudaSuccess)
+            if (launch_kernel_cluster(kern_clu, grid, dim3(CfgC::kThreads), CfgC::kSmem, cs,
+                                      stream, tk, tv, p) != cudaSuccess)
                 return KVD_ERR_CUDA;
             return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
         }
