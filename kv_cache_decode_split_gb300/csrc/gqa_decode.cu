@@ -39,6 +39,7 @@ namespace {
 constexpr int kTile = 64;        // tokens per K/V tile
 constexpr int kConsumers = 4;    // consumer warps, 16 tokens of each tile each
 constexpr int kMaxHP = 16;       // query heads per KV head handled by one CTA
+constexpr int kRowCache = 512;   // block-table entries the producer loads at once (one row)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -383,7 +384,8 @@ struct GqaBf16Cfg {
     // cluster combine: the partials other CTAs push, outside the ring (they may arrive while
     // this CTA still streams)
     static constexpr int kRxBytes = kClu ? static_cast<int>(sizeof(ClusterRx<D, HPT * NT * 8>)) : 0;
-    static constexpr int kSmem = 1024 + kOverlay + kRxBytes + (2 * kStages + 1) * 8;
+    static constexpr int kSmem =
+        1024 + kOverlay + kRxBytes + (2 * kStages + 1) * 8 + kRowCache * 4;
     static constexpr int kThreads = (kConsumers + 1) * 32;
 };
 
@@ -411,6 +413,7 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kOverlay + Cfg::kRxBytes);
     uint64_t* empty = full + S;
     uint64_t* stall = empty + S;  // completed by nothing (give-up test only)
+    int* bt_row = reinterpret_cast<int*>(stall + 1);  // the sequence's block-table row
     // once the ring is drained: per-KV-head merge areas, then the combine scratch
     MS* ms = reinterpret_cast<MS*>(smem);
     CS& cs = *reinterpret_cast<CS*>(smem + Cfg::kMergeBytes);
@@ -420,6 +423,19 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
     const int kvg = blockIdx.y % n_kvg;
     const int hg = blockIdx.y / n_kvg;
     const int b = blockIdx.z;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // The producer loads the sequence's whole block-table row (up to kRowCache entries) while
+    // the sequence length is on its way, instead of the entries the length points to after
+    // it: one memory round trip less before the first copy. Entries are checked when used.
+    constexpr int kRowRegs = kRowCache / 32;
+    const bool row_cached = p.max_pages <= kRowCache;
+    int row[kRowRegs];
+    if (warp == kConsumers && row_cached) {
+        const int32_t* btr = p.block_table + static_cast<size_t>(b) * p.max_pages;
+#pragma unroll
+        for (int j = 0; j < kRowRegs; ++j)
+            row[j] = lane + 32 * j < p.max_pages ? btr[lane + 32 * j] : 0;
+    }
     const int L = visible_len(p, b);
     const Ranges R = visible_ranges(L, p.window, p.n_sink);
     int lo = 0, hi = 0;
@@ -434,7 +450,6 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
     const int bp = min(p.page_size, kTile);  // tokens per page piece (power of two)
     const int lbp = 31 - __clz(bp);
 
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
@@ -462,12 +477,25 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
         }
         const int per_tile = kTile / bp;
         const int n_pieces = n_tiles * per_tile;
+        if (row_cached) {
+#pragma unroll
+            for (int j = 0; j < kRowRegs; ++j)
+                if (lane + 32 * j < p.max_pages) bt_row[lane + 32 * j] = row[j];
+            __syncwarp();
+        }
         auto piece_page = [&](int pc) -> int {
             if (pc >= n_pieces) return 0;
             const int t = t0 + pc * bp;
             const int tc = t < L ? t : L - 1;  // pieces past the end: any valid page
-            return load_page(p.block_table, p.max_pages, p.num_pages, b, tc / p.page_size,
-                             p.err);
+            if (!row_cached)
+                return load_page(p.block_table, p.max_pages, p.num_pages, b, tc / p.page_size,
+                                 p.err);
+            int pg = bt_row[tc / p.page_size];
+            if (pg < 0 || pg >= p.num_pages) {
+                record_error(p.err, KVD_ERR_DEVICE_OOB);
+                pg = 0;
+            }
+            return pg;
         };
         int cur = piece_page(lane), nxt = piece_page(32 + lane);
         int issued = 0;  // tiles whose copies are in flight or landed
