@@ -111,14 +111,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 
 // Wait until the grids this one depends on (programmatic launch) have completed and their
-// memory is visible; returns at once for a plain launch. Then allow the next kernel on the
-// stream, if it was launched with programmatic serialization, to be scheduled: its blocks
-// take SM slots as this grid's blocks exit and do their set-up while this grid finishes,
-// and each waits for this grid's completion in its own griddep_wait before it touches
-// memory. Every kernel calls this before its first global memory access.
+// memory is visible; returns at once for a plain launch. Every kernel calls this before its
+// first global memory access. (No kernel triggers its dependents early: letting the next
+// kernel's blocks take SM slots while this grid runs measured slower, by 7 us on the DSA
+// step's four kernels and 0.3 us on a sliding-window step, and faster on none.)
 __device__ __forceinline__ void griddep_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Hint: bring the global line holding `ptr` into L2 (no data returned).
