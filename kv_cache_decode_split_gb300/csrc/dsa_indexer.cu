@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         uint32_t g = 0, nq = 0;
         int cur_b = -1;
         bool ok = true;
+        const uint64_t pol = l2_evict_first_policy();  // keys are read once
         for (int c0 = tr.begin; c0 < tr.end && ok; c0 += chunk) {
             const int c1 = min(tr.end, c0 + chunk);
             // the warp resolves the chunk's piece rows (first physical row of each piece, or
@@ -172,13 +173,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                     for (int sub = 1; sub < per_tile; ++sub)
                         if (ys[sub] != ys[0] + sub * bp) contiguous = false;
                     if (contiguous && ys[0] + kItile <= p.num_pages * p.page_size) {
-                        tma_load_3d(sm.stage[s], &tmK128, &sm.full[s], 0, ys[0], 0);
+                        tma_load_3d(sm.stage[s], &tmK128, &sm.full[s], 0, ys[0], 0, pol);
                     } else {
                         for (int sub = 0; sub < per_tile; ++sub)
                             for (int half = 0; half < 2; ++half)
                                 tma_load_2d(sm.stage[s] + half * (kIdxTileBytes / 2) +
                                                 sub * bp * 128,
-                                            &tmK, &sm.full[s], half * 64, ys[sub]);
+                                            &tmK, &sm.full[s], half * 64, ys[sub], pol);
                     }
                     ++g;
                 }

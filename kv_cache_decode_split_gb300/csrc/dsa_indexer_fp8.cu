@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         uint32_t g = 0, nq = 0;
         int cur_b = -1;
         bool ok = true;
+        const uint64_t pol = l2_evict_first_policy();  // codes and scales are read once
         for (int c0 = tr.begin; c0 < tr.end && ok; c0 += chunk) {
             const int c1 = min(tr.end, c0 + chunk);
             // the warp resolves the chunk's piece rows (first physical row of each piece, or
@@ -176,14 +177,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     for (int sub = 1; sub < per_tile; ++sub)
                         if (ys[sub] != ys[0] + sub * bp) contiguous = false;
                     if (contiguous && ys[0] + kFTile <= p.num_pages * p.page_size) {
-                        tma_load_2d(sm.stage[s], &tmK128, &sm.full[s], 0, ys[0]);
-                        bulk_load(sm.ks[ss], p.k_scale + ys[0], kFTile * 4, &sm.sfull[ss]);
+                        tma_load_2d(sm.stage[s], &tmK128, &sm.full[s], 0, ys[0], pol);
+                        bulk_load(sm.ks[ss], p.k_scale + ys[0], kFTile * 4, &sm.sfull[ss], pol);
                     } else {
                         for (int sub = 0; sub < per_tile; ++sub) {
                             tma_load_2d(sm.stage[s] + sub * bp * kFDi, &tmK, &sm.full[s], 0,
-                                        ys[sub]);
+                                        ys[sub], pol);
                             bulk_load(sm.ks[ss] + sub * bp, p.k_scale + ys[sub], bp * 4,
-                                      &sm.sfull[ss]);
+                                      &sm.sfull[ss], pol);
                         }
                     }
                     ++g;

@@ -498,6 +498,7 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
             return pg;
         };
         int cur = piece_page(lane), nxt = piece_page(32 + lane);
+        const uint64_t pol = l2_evict_first_policy();  // K and V are read once
         int issued = 0;  // tiles whose copies are in flight or landed
         for (int i = 0; i < n_tiles; ++i) {
             const int s = i % S;
@@ -521,8 +522,8 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
                     const int y =
                         (pg * p.Hkv + kvg * HPT) * p.page_size + (t & (p.page_size - 1));
                     const uint32_t off = static_cast<uint32_t>(sub * NB * HPT) << (lbp + 7);
-                    tma_load_3d(sK + s * Cfg::kTileBytes + off, &tmK, &full[s], 0, y, 0);
-                    tma_load_3d(sV + s * Cfg::kTileBytes + off, &tmV, &full[s], 0, y, 0);
+                    tma_load_3d(sK + s * Cfg::kTileBytes + off, &tmK, &full[s], 0, y, 0, pol);
+                    tma_load_3d(sV + s * Cfg::kTileBytes + off, &tmV, &full[s], 0, y, 0, pol);
                 }
             }
             issued = i + 1;

@@ -93,7 +93,7 @@ struct MlaSmem {
     uint64_t yfree[2][kGroups];  // [half][tile group]: the copy of y[half] has read it
     uint64_t hand[kGroups];  // group published its running max
     uint64_t ofree;          // O of the current piece has been read (eight softmax warps)
-    uint64_t qfull;          // dense: the first piece's queries have landed in stages 2-3
+    uint64_t qfull;          // the first piece's queries have landed in stages 2-3
     uint32_t tmem_base;
     // the cluster's schedule, built once: tile range and its pieces (n_pieces < 0: more
     // pieces than the table holds, walked from the sequence lengths instead)
@@ -319,10 +319,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (warp == kWarpQK) tmem_dealloc(tmem, 512);
         return;
     }
-    // Dense, with the piece table: the first piece's query slice comes by TMA into ring
-    // stages 2-3 (16 KB per 64-dim box), issued ahead of the first tiles, which take stages
-    // 0-1; the producer reuses stages 2-3 once the queries are in tensor memory.
-    const bool tma_q = !kSparse && sm.n_pieces > 0;
+    // With the piece table: the first piece's query slice comes by TMA into ring stages 2-3
+    // (16 KB per 64-dim box), issued ahead of the first tiles, which take stages 0-1; the
+    // producer reuses stages 2-3 once the queries are in tensor memory.
+    const bool tma_q = sm.n_pieces > 0;
     constexpr int kQBox = kH * 128;
     // the partner's partial scores of the first tile of each group (later tiles: armed by
     // the group once the slot's previous phase has completed). A copy that lands before
@@ -345,6 +345,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         int g = 0;  // tile index within this CTA's range
         bool ok = true;
+        const uint64_t pol = l2_evict_first_policy();  // latent rows are read once
         // Dense: no tile is of use before the first piece's queries are in tensor memory, so
         // their loads go out first instead of queueing behind every SM's first tiles (page
         // ids of the first tiles are resolved meanwhile).
@@ -389,11 +390,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             const int y = pg * p.page_size + (t % p.page_size);
                             if (bp == kTok) {
                                 // all of this CTA's 64-dim blocks in one instruction
-                                tma_load_3d(sm.stage[s], &tmC, &sm.full[s], 0, y, dim0 / 64);
+                                tma_load_3d(sm.stage[s], &tmC, &sm.full[s], 0, y, dim0 / 64,
+                                            pol);
                             } else {
                                 for (int bx = 0; bx < nbox; ++bx)
                                     tma_load_2d(sm.stage[s] + bx * kTileBox + sub * bp * 128,
-                                                &tmC2, &sm.full[s], dim0 + 64 * bx, y);
+                                                &tmC2, &sm.full[s], dim0 + 64 * bx, y, pol);
                             }
                         }
                     }
@@ -440,8 +442,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 for (int i = 0; i < nt && ok; ++i, ++g) {
                     const int s = g % kStages;
-                    // (no wait for the queries here: the gather's latency dominates)
-                    if (lane == 0) ok = mbar_wait(&sm.empty[s], ((g / kStages) & 1) ^ 1, p.err);
+                    if (tma_q && g == 2) wait_queries();  // stages 2-3 held the queries
+                    if (lane == 0 && ok)
+                        ok = mbar_wait(&sm.empty[s], ((g / kStages) & 1) ^ 1, p.err);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
                     const int t_nn0 = tok_of(i + 2, 0), t_nn1 = tok_of(i + 2, 1);
@@ -455,7 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             const int bx = c >> 3, cc = c & 7;
                             const uint32_t dst =
                                 base + bx * kTileBox + r * 128 + ((cc ^ (r & 7)) << 4);
-                            cp_async_16(dst, src ? src + c * 8 : cpool, src ? 16u : 0u);
+                            cp_async_16(dst, src ? src + c * 8 : cpool, src ? 16u : 0u, pol);
                         }
                     }
                     cp_async_commit();
