@@ -438,8 +438,8 @@ int kvd_delta_decode_step(float *S, const float *q, const float *k, const float 
  *  KVD_OPT_GQA_CHUNK      0 (default): the GQA / SWA split plan picks the tokens per split;
  *                         >= 64: that many tokens (rounded down to a multiple of 64) per
  *                         split, raised if the plan would exceed its chunk limit.
- *  KVD_OPT_MLA_MIN_TILES  >= 1 (default 1): the MLA plan gives each two-CTA cluster at least
- *                         this many 64-token tiles.
+ *  KVD_OPT_MLA_MIN_TILES  0 (default): the MLA plan gives each two-CTA cluster at least one
+ *                         64-token tile (dense) or two (sparse); >= 1: at least that many.
  *  KVD_OPT_WAIT_TIMEOUT_TEST  1: the next bf16 GQA / SWA call (and only that call) runs
  *                         with a limit of about 1000 SM cycles on each bounded wait of its
  *                         copy ring, and its consumer warps first wait on a barrier that

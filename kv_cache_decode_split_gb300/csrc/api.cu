@@ -27,7 +27,7 @@ std::once_flag g_encode_once;
 // Process-wide options (kvd_set_option); the defaults are what the library is tuned for.
 std::atomic<int> g_opt_pdl{1};
 std::atomic<long long> g_opt_gqa_chunk{0};
-std::atomic<long long> g_opt_mla_min_tiles{1};
+std::atomic<long long> g_opt_mla_min_tiles{0};
 std::atomic<int> g_opt_wait_test{0};
 std::atomic<int> g_opt_gqa_cluster{1};
 
@@ -210,11 +210,14 @@ TopkLayout topk_layout(int B, int max_len, int k, bool with_scores) {
 // MLA split plan: dense units are (sequence, token chunk), about three per SM pair;
 // sparse units are (sequence, chunk of the index list), about one per SM pair.
 MlaPlan mla_plan(int B, int max_items, bool sparse) {
-    (void)sparse;
     MlaPlan pl;
     const long long max_tiles = (long long)B * ((max_items + 63) / 64);
-    // tiles a cluster takes at least (KVD_OPT_MLA_MIN_TILES)
-    const long long min_tiles = std::max(1LL, g_opt_mla_min_tiles.load(std::memory_order_relaxed));
+    // Tiles a cluster takes at least (KVD_OPT_MLA_MIN_TILES overrides): 2 for the sparse
+    // decode, whose few tiles would otherwise spread one per cluster and each cluster writes a
+    // whole 128 x 512 partial (measured on the DSA workload: 61.6 -> 60.6 us a step; 3 was
+    // slower), 1 for the dense decode.
+    const long long opt = g_opt_mla_min_tiles.load(std::memory_order_relaxed);
+    const long long min_tiles = opt >= 1 ? opt : (sparse ? 2 : 1);
     pl.n_clusters = static_cast<int>(std::max(
         1LL, std::min<long long>(num_sms() / 2, (max_tiles + min_tiles - 1) / min_tiles)));
     const size_t slots = (size_t)pl.n_clusters + B - 1;
@@ -886,7 +889,7 @@ int kvd_set_option(int option, long long value) {
             g_opt_gqa_chunk.store(value);
             return KVD_OK;
         case KVD_OPT_MLA_MIN_TILES:
-            if (value < 1 || value > (1LL << 30)) return KVD_ERR_INVALID_ARG;
+            if (value < 0 || value > (1LL << 30)) return KVD_ERR_INVALID_ARG;
             g_opt_mla_min_tiles.store(value);
             return KVD_OK;
         case KVD_OPT_WAIT_TIMEOUT_TEST:

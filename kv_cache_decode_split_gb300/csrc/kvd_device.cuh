@@ -520,6 +520,11 @@ __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Wait until the issuing thread's bulk copies have completed (their writes performed).
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Remote arrive without release ordering: for "slot consumed" signals whose reads have
 // already returned (their values are in registers), so nothing needs to be made visible.
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar) {

@@ -94,6 +94,7 @@ struct MlaSmem {
     uint64_t hand[kGroups];  // group published its running max
     uint64_t ofree;          // O of the current piece has been read (eight softmax warps)
     uint64_t qfull;          // the first piece's queries have landed in stages 2-3
+    uint64_t qkend, pvend;   // every product the score / value issuer started has completed
     uint32_t tmem_base;
     // the cluster's schedule, built once: tile range and its pieces (n_pieces < 0: more
     // pieces than the table holds, walked from the sequence lengths instead)
@@ -301,6 +302,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(&sm.ofinal, 1);
         mbar_init(&sm.ofree, kSoftWarps);
         mbar_init(&sm.qfull, 1);
+        mbar_init(&sm.qkend, 1);
+        mbar_init(&sm.pvend, 1);
         fence_mbar_init();
     }
     if (warp == kWarpQK) tmem_alloc(&sm.tmem_base, 512);
@@ -480,7 +483,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 mbar_arrive(&sm.full[(g - 1) % kStages]);
             }
-        } else if (lane == 0 && ok) {
+        } else if (lane == 0) {
+            // every issued copy lands before the CTA goes on (also after a wait gave up: the
+            // ring's shared memory must not be written once the CTA has exited)
             const int first = g > kStages ? g - kStages : 0;
             for (int i = first; i < g; ++i)
                 mbar_wait(&sm.full[i % kStages], (i / kStages) & 1, p.err);
@@ -509,6 +514,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tc_commit(&sm.sfull[g % kGroups]);
                 }
             });
+            // every product issued here completes before TMEM can be released (also after a
+            // wait gave up)
+            tc_commit(&sm.qkend);
+            mbar_wait(&sm.qkend, 0, p.err);
         }
     } else if (warp == kWarpPV) {
         // ------------------------------------------------------------------ value products
@@ -530,6 +539,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tc_commit(&sm.ofinal);  // every product of the piece (and before) completed
             });
+            tc_commit(&sm.pvend);
+            mbar_wait(&sm.pvend, 0, p.err);
         }
     } else if (warp == kWarpX) {
         // ------------------------------------------------------------------ score exchange
@@ -561,6 +572,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             bulk_wait_read_all();
             if (ok) mbar_arrive(&sm.yfree[1][(n_tiles - 1) % kGroups]);
+            // the copies have landed in the partner before the pair's final barrier lets it exit
+            bulk_wait_all();
         }
     } else {
         // ------------------------------------------------------------------ softmax
