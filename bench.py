@@ -46,23 +46,64 @@ def l2_bytes(dev):
     return int(torch.cuda.get_device_properties(dev).L2_cache_size)
 
 
-# DRAM traffic (read + write bytes per launch) of a workload's dominant kernel from one ncu
-# capture (summaries in profiles/), reported only while what the kernel is compiled from --
-# its source file, the device header and its argument struct -- still hashes to the value
-# recorded with the capture: a changed kernel reports null.
+# DRAM traffic (read + write bytes per launch) of each workload's dominant kernel from one ncu
+# capture (summaries in profiles/, one per workload and kernel), reported only while what the
+# kernel is compiled from -- its source file, the device header and its argument struct --
+# still hashes to the value recorded with the capture: a changed kernel reports null.
 NCU_TRAFFIC = {
-    "llama3_8b_gqa_paged": {
-        "bytes": 794.592512e6 + 4.951808e6,
-        "sources": ("gqa_decode.cu", "kvd_device.cuh"),
-        "structs": ("GqaParams",),
-        "sha256": "cee135d8631b6604e2b21a85d7ebd434842922e70455777e159374a437501733",
+    "llama3_8b_gqa_paged": {  # gqa_decode_bf16_kernel<128, 1, 1, 0>
+        "bytes": 794.194688e6 + 4.014336e6,
+        "sources": ('gqa_decode.cu', 'kvd_device.cuh'),
+        "structs": ('GqaParams',),
+        "sha256": "d3f4e5b8c44da12d42b9a3b09d811f3d191b448386bbbee30c6075bccca24015",
     },
-    # the write-back of the last ~58 MB of the updated state is still in L2 when the kernel ends
-    "kda_decode": {
-        "bytes": 276.86272e6 + 210.739712e6,
-        "sources": ("delta_decode.cu", "kvd_device.cuh"),
-        "structs": ("DeltaParams",),
-        "sha256": "3458690fc00216eabdee212fe156da7140ffa09c8482645b492dced199e078c3",
+    "swa_sink_tokens": {  # gqa_decode_bf16_kernel<64, 1, 2, 1>
+        "bytes": 68.293120e6 + 0.768000e6,
+        "sources": ('gqa_decode.cu', 'kvd_device.cuh'),
+        "structs": ('GqaParams',),
+        "sha256": "d3f4e5b8c44da12d42b9a3b09d811f3d191b448386bbbee30c6075bccca24015",
+    },
+    "swa_learned_sink": {  # gqa_decode_bf16_kernel<64, 1, 2, 1>
+        "bytes": 67.245056e6 + 0.760320e6,
+        "sources": ('gqa_decode.cu', 'kvd_device.cuh'),
+        "structs": ('GqaParams',),
+        "sha256": "d3f4e5b8c44da12d42b9a3b09d811f3d191b448386bbbee30c6075bccca24015",
+    },
+    "swa_ring_sink_tokens": {  # gqa_decode_bf16_kernel<64, 1, 2, 1>
+        "bytes": 68.277248e6 + 0.676096e6,
+        "sources": ('gqa_decode.cu', 'kvd_device.cuh'),
+        "structs": ('GqaParams',),
+        "sha256": "d3f4e5b8c44da12d42b9a3b09d811f3d191b448386bbbee30c6075bccca24015",
+    },
+    "mla_dsv3": {  # mla_decode_kernel<0>
+        "bytes": 304.508928e6 + 4.190464e6,
+        "sources": ('mla_decode.cu', 'kvd_device.cuh'),
+        "structs": ('MlaParams',),
+        "sha256": "26749f2aaf8e7ebe94821c459aa1c13902c3371608c3d275dec9d024e866c762",
+    },
+    "dsa_sparse_mla": {  # dsa_indexer_kernel
+        "bytes": 134.376192e6 + 3.294208e6,
+        "sources": ('dsa_indexer.cu', 'kvd_device.cuh'),
+        "structs": ('IdxParams',),
+        "sha256": "436281c68af07dd1e4d59fd4941d906345474c15c8e2a984118836e07d9867de",
+    },
+    "dsa_fp8_sparse_mla": {  # dsa_indexer_fp8_kernel
+        "bytes": 69.331456e6 + 0.465920e6,
+        "sources": ('dsa_indexer_fp8.cu', 'kvd_device.cuh'),
+        "structs": ('IdxParams',),
+        "sha256": "6efa27a304d2e44aa8116f1dc37da2add191ddb2fc8681cd09215a84f7d95f57",
+    },
+    "quest_llama3": {  # quest_attn_kernel<4, 1, 1>
+        "bytes": 114.779392e6 + 3.625216e6,
+        "sources": ('quest.cu', 'kvd_device.cuh'),
+        "structs": ('QuestParams',),
+        "sha256": "33a891ee74a3d48c3552bc2b2957bd24a8f9f13571998d69b24c97003088857b",
+    },
+    "kda_decode": {  # delta_step_kernel<4>
+        "bytes": 276.856320e6 + 211.294976e6,
+        "sources": ('delta_decode.cu', 'kvd_device.cuh'),
+        "structs": ('DeltaParams',),
+        "sha256": "d4174dd2930227e6e9f717d5737a5f7ed5c44eb1d53acf85abef7cf44b9cf56c",
     },
 }
 
@@ -956,6 +997,8 @@ def main():
             gbs = rr.bytes / (rot_ms * 1e-3) / 1e9
             entry = {"us": round(rot_ms * 1e3, 2), "us_flushed": round(flushed_ms * 1e3, 2),
                      "GBps": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
+            t = ncu_traffic(name)
+            entry["dram_MB"] = round(t / 1e6, 1) if t is not None else None
             tfl = rr.flops / (rot_ms * 1e-3) / 1e12
             if getattr(rr, "tensor_path", False):
                 entry["TFLOPs"] = round(tfl, 1)
