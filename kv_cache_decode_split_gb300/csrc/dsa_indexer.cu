@@ -33,7 +33,8 @@ constexpr int kHi = 64;                 // indexer heads (MMA N)
 constexpr int kDi = 128;                // indexer head dim (MMA K)
 constexpr int kIdxTileBytes = kItile * kDi * 2;   // 32 KB: two 64-dim boxes of 16 KB
 constexpr int kIdxQBytes = kHi * kDi * 2;         // 16 KB: two 64-dim boxes of 8 KB
-constexpr int kIdxStages = 5;
+constexpr int kIdxStages = 2;
+constexpr int kIdxCtasPerSm = 2;        // two independent pipelines per SM
 constexpr int kIdxThreads = 6 * 32;     // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kHistBins = 2048;         // top 11 key bits
 constexpr int kIdxRowCap = 512;         // page pieces resolved ahead (a chunk)
@@ -72,7 +73,7 @@ __device__ __forceinline__ TileRange my_tiles(int total) {
     return TileRange{static_cast<int>(i * total / G), static_cast<int>((i + 1) * total / G)};
 }
 
-__global__ void __launch_bounds__(kIdxThreads, 1)
+__global__ void __launch_bounds__(kIdxThreads, kIdxCtasPerSm)
     dsa_indexer_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmK128,
                        const __grid_constant__ CUtensorMap tmQ, const IdxParams p) {
@@ -771,7 +772,7 @@ int dsa_indexer_launch(const IdxParams& p, const CUtensorMap& tk, const CUtensor
         configured = 1;
     }
     const int total = p.B * p.tiles_per_b;
-    const int grid = total < num_sms() ? total : num_sms();
+    const int grid = std::min(total, kIdxCtasPerSm * num_sms());
     if (launch_kernel(dsa_indexer_kernel, dim3(grid), dim3(kIdxThreads), kIdxSmem, stream, tk,
                       tk128, tq, p) != cudaSuccess)
         return KVD_ERR_CUDA;

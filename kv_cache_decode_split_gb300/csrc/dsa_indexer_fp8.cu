@@ -31,8 +31,9 @@ constexpr int kFHi = 64;                          // indexer heads (MMA N)
 constexpr int kFDi = 128;                         // head dim = bytes per key row (MMA K)
 constexpr int kFTileBytes = kFTile * kFDi;        // 16 KB
 constexpr int kFQBytes = kFHi * kFDi;             // 8 KB
-constexpr int kFStages = 8;
-constexpr int kFScaleSlots = 8;
+constexpr int kFStages = 4;
+constexpr int kFScaleSlots = 4;
+constexpr int kFCtasPerSm = 2;                    // two independent pipelines per SM
 constexpr int kFThreads = 6 * 32;                 // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kFHistBins = 2048;                  // top 11 key bits
 constexpr int kFRowCap = 512;                     // page pieces resolved ahead (a chunk)
@@ -71,7 +72,7 @@ struct TileCursor {
     }
 };
 
-__global__ void __launch_bounds__(kFThreads, 1)
+__global__ void __launch_bounds__(kFThreads, kFCtasPerSm)
     dsa_indexer_fp8_kernel(const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmK128,
                            const __grid_constant__ CUtensorMap tmQ, const IdxParams p) {
@@ -363,7 +364,7 @@ int dsa_indexer_fp8_launch(const IdxParams& p, const CUtensorMap& tk, const CUte
         configured = 1;
     }
     const int total = p.B * p.tiles_per_b;
-    const int grid = total < num_sms() ? total : num_sms();
+    const int grid = std::min(total, kFCtasPerSm * num_sms());
     if (launch_kernel(dsa_indexer_fp8_kernel, dim3(grid), dim3(kFThreads), kFSmem, stream, tk,
                       tk128, tq, p) != cudaSuccess)
         return KVD_ERR_CUDA;
