@@ -193,6 +193,8 @@ TopkLayout topk_layout(int B, int max_len, int k, bool with_scores) {
     size_t off = kWsHeaderBytes;
     l.off_hist = off;
     off = round256(off + sizeof(uint32_t) * (size_t)B * 2048);
+    l.off_hist2 = off;
+    off = round256(off + sizeof(uint32_t) * (size_t)B * 256);
     l.off_counts = off;
     off = round256(off + sizeof(int) * (size_t)B * 4);
     l.off_sel = off;
@@ -690,6 +692,7 @@ static int indexer_topk(bool fp8, const void* q_idx, const float* q_scale, const
     tp.score_stride = max_len;
     tp.lens = seq_lens;
     tp.hist = ip.hist;
+    tp.hist2 = reinterpret_cast<uint32_t*>(wb + lay.off_hist2);
     tp.counts = reinterpret_cast<int*>(wb + lay.off_counts);
     tp.sel = reinterpret_cast<int*>(wb + lay.off_sel);
     tp.cand = reinterpret_cast<uint64_t*>(wb + lay.off_cand);
@@ -818,6 +821,7 @@ int dsa_topk(const float* scores, const int32_t* lens, int32_t* topk_idx, int32_
     tp.score_stride = score_stride;
     tp.lens = lens;
     tp.hist = reinterpret_cast<uint32_t*>(wb + lay.off_hist);
+    tp.hist2 = reinterpret_cast<uint32_t*>(wb + lay.off_hist2);
     tp.counts = reinterpret_cast<int*>(wb + lay.off_counts);
     tp.sel = reinterpret_cast<int*>(wb + lay.off_sel);
     tp.cand = reinterpret_cast<uint64_t*>(wb + lay.off_cand);

@@ -413,6 +413,7 @@ __device__ __forceinline__ void load_hist(uint32_t* h, const uint32_t* src) {
 }
 
 constexpr int kSelThreads = 512;
+static_assert(kSelThreads >= 256, "a thread per second-level bin");
 constexpr int kSelPerThread = 16;
 constexpr int kRankMax = 256;  // a threshold bucket this small is finished by ranking its keys
 constexpr int kRadixBits = 8;  // digit of the passes after the histogram's top 11 bits
@@ -460,6 +461,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const TopkPara
     __shared__ int s_nlist, s_nchosen;
     __shared__ int s_base[2];
     __shared__ int s_last;
+    __shared__ uint32_t h2[256];  // this block's candidates by their next 8 key bits
     extern __shared__ uint64_t sel_dyn[];
     const int b = blockIdx.y;
     const int tid = threadIdx.x;
@@ -472,6 +474,8 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const TopkPara
         if (blockIdx.x == 0) {
             for (int i = tid; i < p.k; i += kSelThreads) idx_out[i] = i < L ? i : -1;
             for (int i = tid; i < kHistBins; i += kSelThreads) hist[i] = 0;
+            for (int i = tid; i < 256; i += kSelThreads)
+                p.hist2[static_cast<size_t>(b) * 256 + i] = 0u;
             if (tid == 0) p.topk_count[b] = L;
         }
         return;
@@ -492,6 +496,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const TopkPara
     };
     load_span(blockIdx.x * kSpan);
     load_hist<kSelThreads>(h, hist);
+    for (int i = tid; i < 256; i += kSelThreads) h2[i] = 0u;
     __syncthreads();
     int b1, above, in_b1, total;
     find_bucket<kSelThreads>(h, kHistBins, p.k, b1, above, in_b1, tmp, &total);
@@ -518,8 +523,13 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const TopkPara
         const int incl = block_incl_scan<kSelThreads>(packed, tmp);
         const int excl = incl - packed;
         if (tid == kSelThreads - 1) {
-            s_base[0] = (incl & 0xFFFF) ? atomicAdd(cnt, incl & 0xFFFF) : 0;
-            s_base[1] = (incl >> 16) ? atomicAdd(cnt + 1, incl >> 16) : 0;
+            // both lists' slots in one 64-bit atomic (selected count low, candidates high)
+            const unsigned long long inc =
+                (static_cast<unsigned long long>(incl >> 16) << 32) | static_cast<unsigned>(incl & 0xFFFF);
+            const unsigned long long old =
+                atomicAdd(reinterpret_cast<unsigned long long*>(cnt), inc);
+            s_base[0] = static_cast<int>(static_cast<uint32_t>(old));
+            s_base[1] = static_cast<int>(static_cast<uint32_t>(old >> 32));
         }
         __syncthreads();
         int si = s_base[0] + (excl & 0xFFFF), ci = s_base[1] + (excl >> 16);
@@ -536,12 +546,18 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const TopkPara
                 else record_error(p.err, KVD_ERR_DEVICE_STATE);
                 ++si;
             } else if (c == 2u) {
+                atomicAdd(&h2[(float_key(v[k]) >> 13) & 255u], 1u);
                 if (ci >= 0 && ci < p.max_len) cand[ci] = composite_key(v[k], t);
                 else record_error(p.err, KVD_ERR_DEVICE_STATE);
                 ++ci;
             }
         }
     }
+    // the candidates' next-digit counts go to the sequence's second-level histogram, so that
+    // the finishing block starts its radix search one digit further
+    __syncthreads();
+    for (int i = tid; i < 256; i += kSelThreads)
+        if (h2[i]) atomicAdd(p.hist2 + static_cast<size_t>(b) * 256 + i, h2[i]);
     // the last block of the sequence finishes it
     __threadfence();
     __syncthreads();
@@ -576,6 +592,8 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const TopkPara
         tv[r] = i < above_c ? __ldcg(sel + i) : -1;
     }
     int nc = __ldcg(cnt + 1);
+    // the second-level histogram, in flight with the lists
+    const uint32_t h2v = tid < 256 ? __ldcg(p.hist2 + static_cast<size_t>(b) * 256 + tid) : 0u;
     if (nc < 0 || nc > L || above != above_c) {  // not a zeroed workspace
         if (tid == 0) record_error(p.err, KVD_ERR_DEVICE_STATE);
         nc = min(max(nc, 0), L);
@@ -605,6 +623,22 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const TopkPara
     uint64_t prefix = static_cast<uint64_t>(b1);
     int done_bits = 11;
     int in_b = in_b1;
+    // the first digit below the top 11 bits from the second-level histogram (when it counts
+    // exactly the candidates: else the radix passes start from the top 11 bits)
+    if (in_b != need && in_b > kRankMax) {
+        if (tid < 256) h[tid] = h2v;
+        __syncthreads();
+        int bb, ab, ib, tot2;
+        find_bucket<kSelThreads>(h, 256, need, bb, ab, ib, tmp, &tot2);
+        if (tot2 == nc && nc == in_b1) {
+            prefix = (prefix << 8) | static_cast<uint64_t>(bb);
+            need -= ab;
+            in_b = ib;
+            done_bits = 19;
+        } else if (tid == 0) {
+            record_error(p.err, KVD_ERR_DEVICE_STATE);
+        }
+    }
     while (done_bits < 64 && in_b != need && in_b > kRankMax) {
         const int wdt = min(kRadixBits, 64 - done_bits);
         const int shift = 64 - done_bits - wdt;
@@ -755,6 +789,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const TopkPara
     if (tid == 0) p.topk_count[b] = p.k;
     // leave the histogram and counters zeroed for the next call
     for (int i = tid; i < kHistBins; i += kSelThreads) hist[i] = 0;
+    for (int i = tid; i < 256; i += kSelThreads) p.hist2[static_cast<size_t>(b) * 256 + i] = 0u;
     if (tid < 3) cnt[tid] = 0;
 }
 

@@ -109,6 +109,7 @@ struct TopkParams {
     long long score_stride;
     const int32_t* lens;       // [B]
     uint32_t* hist;            // [B, 2048]
+    uint32_t* hist2;           // [B, 256] next 8 key bits of the threshold bucket's keys
     int* counts;               // [B, 4]: selected, candidates, blocks done, (pad)
     int* sel;                  // [B, k] selected positions
     uint64_t* cand;            // [B, max_len] candidates' (score key, reversed position) keys
@@ -121,7 +122,7 @@ struct TopkParams {
 
 // Workspace layout of the DSA selection (offsets from the workspace base).
 struct TopkLayout {
-    size_t off_hist, off_counts, off_sel, off_cand, off_bitmap, off_scores, total;
+    size_t off_hist, off_hist2, off_counts, off_sel, off_cand, off_bitmap, off_scores, total;
 };
 TopkLayout topk_layout(int B, int max_len, int k, bool with_scores);
 
