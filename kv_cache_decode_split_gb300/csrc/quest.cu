@@ -34,7 +34,11 @@ namespace {
 
 constexpr float kQLog2e = 1.4426950408889634f;
 constexpr int kAttnWarps = 4;
-constexpr int kRowsInFlight = 16;
+// Eight K and V rows in flight per warp, few enough registers for seven CTAs per SM: on the
+// Llama-3-shaped workload all 1024 (sequence, head) CTAs are then resident at once instead of
+// running in two waves (step 74 -> 62 us; with 16 rows and 128 registers, four per SM).
+constexpr int kRowsInFlight = 8;
+constexpr int kAttnCtasPerSm = 7;
 
 // VEC consecutive elements of a row as float (bf16 or float32 storage).
 template <int VEC, bool BF16>
@@ -132,11 +136,19 @@ __global__ void __launch_bounds__(256) quest_minmax_kernel(const QuestParams p) 
     load_vec<VEC, BF16>(p.k_pool, row0 * D + lane * VEC, lo);
 #pragma unroll
     for (int j = 0; j < VEC; ++j) hi[j] = lo[j];
-    for (int t = 1; t < p.page_size; ++t) {
-        float x[VEC];
-        load_vec<VEC, BF16>(p.k_pool, (row0 + t) * D + lane * VEC, x);
+    // rows kRows at a time, all their loads issued before any is used (page sizes are powers
+    // of two >= 16, so the batches divide the page)
+    constexpr int kRows = 8;
+    for (int t0 = 0; t0 < p.page_size; t0 += kRows) {
+        float x[kRows][VEC];
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) lo[j] = fminf(lo[j], x[j]), hi[j] = fmaxf(hi[j], x[j]);
+        for (int r = 0; r < kRows; ++r)
+            load_vec<VEC, BF16>(p.k_pool, (row0 + t0 + r) * D + lane * VEC, x[r]);
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                lo[j] = fminf(lo[j], x[r][j]), hi[j] = fmaxf(hi[j], x[r][j]);
     }
     const size_t o = (static_cast<size_t>(pg) * p.Hkv + g) * D + lane * VEC;
 #pragma unroll
@@ -234,6 +246,28 @@ constexpr int kChooseWarps = 4;
 
 // Sort key of a bound: larger bound first, then the lower page (a NaN bound ranks below
 // every number); 0 marks "no candidate".
+__device__ __forceinline__ uint64_t bound_key(float v, int m);
+
+// The sort keys of a head's full pages, key[m] for m < full, from its bound row (global):
+// each lane's loads are issued kBatch at a time before any is used, so that the row costs a
+// few memory round trips instead of one per page a lane holds.
+__device__ __forceinline__ void load_bound_keys(const float* src, int full, uint64_t* key) {
+    constexpr int kBatch = 8;
+    const int lane = threadIdx.x % 32;
+    for (int m0 = lane; m0 < full; m0 += 32 * kBatch) {
+        float v[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int m = m0 + 32 * i;
+            v[i] = m < full ? __ldcg(src + m) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int m = m0 + 32 * i;
+            if (m < full) key[m] = bound_key(v[i], m);
+        }
+    }
+}
 __device__ __forceinline__ uint64_t bound_key(float v, int m) {
     uint32_t o = 0u;
     if (v == v) {
@@ -298,8 +332,7 @@ __global__ void __launch_bounds__(kChooseWarps * 32) quest_choose_kernel(const Q
     const int L = load_len(p.seq_lens, b, p.max_len, p.err);
     const int full = L / p.page_size;
     uint64_t* u = ubs + static_cast<size_t>(warp) * p.max_pages;
-    const float* src = p.ub_out + static_cast<size_t>(bh) * p.max_pages;
-    for (int m = lane; m < full; m += 32) u[m] = bound_key(src[m], m);
+    load_bound_keys(p.ub_out + static_cast<size_t>(bh) * p.max_pages, full, u);
     __syncwarp();
     choose_pages(u, full, p.n_sel, p.sel + static_cast<size_t>(bh) * p.n_sel);
 }
@@ -308,7 +341,8 @@ __global__ void __launch_bounds__(kChooseWarps * 32) quest_choose_kernel(const Q
 // CHOOSE: warp 0 first picks the head's pages from its bounds (p.ub_out), writes them to
 // p.sel for the caller, and the CTA attends over them (no separate choice launch).
 template <int VEC, bool BF16, bool CHOOSE>
-__global__ void __launch_bounds__(kAttnWarps * 32) quest_attn_kernel(const QuestParams p) {
+__global__ void __launch_bounds__(kAttnWarps * 32, kAttnCtasPerSm)
+    quest_attn_kernel(const QuestParams p) {
     constexpr int D = VEC * 32;
     __shared__ float m_s[kAttnWarps], l_s[kAttnWarps];
     __shared__ float o_s[kAttnWarps][D];
@@ -325,8 +359,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) quest_attn_kernel(const Quest
     const int32_t* sel = p.sel + (static_cast<size_t>(b) * p.Hq + h) * p.n_sel;
     if constexpr (CHOOSE) {
         if (warp == 0) {
-            const float* src = p.ub_out + (static_cast<size_t>(b) * p.Hq + h) * p.max_pages;
-            for (int m = lane; m < full; m += 32) ubrow[m] = bound_key(src[m], m);
+            load_bound_keys(p.ub_out + (static_cast<size_t>(b) * p.Hq + h) * p.max_pages, full,
+                            ubrow);
             __syncwarp();
             choose_pages(ubrow, full, p.n_sel, sel_s);
             __syncwarp();
