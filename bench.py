@@ -82,22 +82,22 @@ NCU_TRAFFIC = {
         "sha256": "26749f2aaf8e7ebe94821c459aa1c13902c3371608c3d275dec9d024e866c762",
     },
     "dsa_sparse_mla": {  # dsa_indexer_kernel
-        "bytes": 134.376192e6 + 3.294208e6,
+        "bytes": 134.395392e6 + 3.844096e6,
         "sources": ('dsa_indexer.cu', 'kvd_device.cuh'),
         "structs": ('IdxParams',),
-        "sha256": "436281c68af07dd1e4d59fd4941d906345474c15c8e2a984118836e07d9867de",
+        "sha256": "2815ab8bc4e938c17d33e4e0704f2b3121df52ca1b3018d439571d23b841132f",
     },
     "dsa_fp8_sparse_mla": {  # dsa_indexer_fp8_kernel
-        "bytes": 69.331456e6 + 0.465920e6,
+        "bytes": 69.331712e6 + 0.527360e6,
         "sources": ('dsa_indexer_fp8.cu', 'kvd_device.cuh'),
         "structs": ('IdxParams',),
-        "sha256": "6efa27a304d2e44aa8116f1dc37da2add191ddb2fc8681cd09215a84f7d95f57",
+        "sha256": "5985ab34b1f1896fc5f546ba968792192122720e1ca48b879ac947f8635a4f2e",
     },
     "quest_llama3": {  # quest_attn_kernel<4, 1, 1>
-        "bytes": 114.779392e6 + 3.625216e6,
+        "bytes": 115.002624e6 + 3.696896e6,
         "sources": ('quest.cu', 'kvd_device.cuh'),
         "structs": ('QuestParams',),
-        "sha256": "33a891ee74a3d48c3552bc2b2957bd24a8f9f13571998d69b24c97003088857b",
+        "sha256": "92bad60166a1ade8efaed8858cb87859df791997b381ccd2f94f8f0117a0f673",
     },
     "kda_decode": {  # delta_step_kernel<4>
         "bytes": 276.856320e6 + 211.294976e6,
