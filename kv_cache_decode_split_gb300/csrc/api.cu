@@ -271,6 +271,8 @@ int mla_run(const void* q, const void* c_pool, const int32_t* block_table,
     p.n_clusters = pl.n_clusters;
     p.idx_stride = k;
     p.sparse = sparse ? 1 : 0;
+    p.tile = 64;
+    p.gap = 6;
     p.scale_log2 = scale * 1.4426950408889634f;
     // 3-D maps (rank 0: 4 blocks of 64 dims, rank 1: 5) for 64-token tiles within a page,
     // and a 2-D map for pages shorter than a tile

@@ -42,7 +42,7 @@ constexpr int kIdxRowCap = 512;         // page pieces resolved ahead (a chunk)
 struct IdxSmem {
     uint8_t stage[kIdxStages][kIdxTileBytes];   // 1024-aligned (offset 0)
     uint8_t qbuf[2][kIdxQBytes];
-    uint32_t hist[kHistBins];
+    alignas(16) uint32_t hist[kHistBins];  // read as uint4 by the flush
     float wv[2][kHi];
     uint64_t full[kIdxStages], empty[kIdxStages];
     uint64_t qfull[2], qempty[2], tfull[2], tempty[2], done;
@@ -134,16 +134,9 @@ __global__ void __launch_bounds__(kIdxThreads, kIdxCtasPerSm)
             for (int q = lane; q < (c1 - c0) * per_tile; q += 32) {
                 const int f = c0 + q / per_tile, sub = q % per_tile;
                 const int b = f / p.tiles_per_b, j = f % p.tiles_per_b;
-                const int L = load_len(p.seq_lens, b, p.max_len, p.err);
-                int row = -1;
-                if (j * kItile < L) {
-                    const int t = j * kItile + sub * bp;
-                    const int tc = t < L ? t : L - 1;  // rows past the end: a valid page
-                    const int pg = load_page(p.block_table, p.max_pages, p.num_pages, b,
-                                             tc / p.page_size, p.err);
-                    row = pg * p.page_size + (t % p.page_size);
-                }
-                sm.prow[q] = row;
+                sm.prow[q] = piece_row(p.seq_lens, p.block_table, p.max_len, p.max_pages,
+                                       p.num_pages, p.page_size, b, j * kItile,
+                                       j * kItile + sub * bp, p.err);
             }
             __syncwarp();
             // lane 0 alone issues the chunk's copies: no warp-wide step per tile
@@ -245,16 +238,27 @@ __global__ void __launch_bounds__(kIdxThreads, kIdxCtasPerSm)
         int cur_b = -1, L = 0;
         uint32_t nt = 0, nb = 0;
         float wr[kHi];  // the head weights of the current sequence
-        auto flush_hist = [&](int b) {
+        // The sequence's counts into the global histogram (16-byte reads, all in flight at
+        // once), the shared one left zeroed for the next sequence (`last`: no next one, no
+        // barrier after).
+        auto flush_hist = [&](int b, bool last) {
             asm volatile("bar.sync 2, 128;" ::: "memory");
-            for (int i = etid; i < kHistBins; i += 128) {
-                const uint32_t c = sm.hist[i];
-                if (c) {
-                    atomicAdd(p.hist + static_cast<size_t>(b) * kHistBins + i, c);
-                    sm.hist[i] = 0;
-                }
+            uint32_t* gh = p.hist + static_cast<size_t>(b) * kHistBins;
+            uint4 v[kHistBins / 4 / 128];
+#pragma unroll
+            for (int k = 0; k < kHistBins / 4 / 128; ++k)
+                v[k] = reinterpret_cast<const uint4*>(sm.hist)[etid + 128 * k];
+#pragma unroll
+            for (int k = 0; k < kHistBins / 4 / 128; ++k) {
+                const int i = 4 * (etid + 128 * k);
+                if (v[k].x) atomicAdd(gh + i, v[k].x);
+                if (v[k].y) atomicAdd(gh + i + 1, v[k].y);
+                if (v[k].z) atomicAdd(gh + i + 2, v[k].z);
+                if (v[k].w) atomicAdd(gh + i + 3, v[k].w);
+                if (!last && (v[k].x | v[k].y | v[k].z | v[k].w))
+                    reinterpret_cast<uint4*>(sm.hist)[etid + 128 * k] = make_uint4(0u, 0u, 0u, 0u);
             }
-            asm volatile("bar.sync 2, 128;" ::: "memory");
+            if (!last) asm volatile("bar.sync 2, 128;" ::: "memory");
         };
         IdxCursor tc(tr.begin, p.tiles_per_b);
         for (int f = tr.begin; f < tr.end; ++f, tc.next()) {
@@ -262,7 +266,7 @@ __global__ void __launch_bounds__(kIdxThreads, kIdxCtasPerSm)
             if (b != cur_b) L = load_len(p.seq_lens, b, p.max_len, nullptr);
             if (j * kItile >= L) continue;
             if (b != cur_b) {
-                if (cur_b >= 0) flush_hist(cur_b);
+                if (cur_b >= 0) flush_hist(cur_b, false);
                 if (etid < kHi) sm.wv[nb & 1][etid] = p.w[static_cast<size_t>(b) * kHi + etid];
                 asm volatile("bar.sync 2, 128;" ::: "memory");
 #pragma unroll
@@ -299,7 +303,7 @@ __global__ void __launch_bounds__(kIdxThreads, kIdxCtasPerSm)
             }
             ++nt;
         }
-        if (cur_b >= 0) flush_hist(cur_b);
+        if (cur_b >= 0) flush_hist(cur_b, true);
     }
     tc_fence_before();
     __syncthreads();

@@ -273,6 +273,29 @@ __device__ __forceinline__ int load_len(const int32_t* seq_lens, int b, int max_
     return L;
 }
 
+// Physical row of token t of sequence b, the first token of a piece of the tile starting at
+// token tile_t0, with the sequence's length and its block-table entry at t's page loaded at
+// once (one memory round trip instead of two). -1: the tile lies past the sequence's end. The
+// entry is checked only when t holds a token; a piece past the end inside the last tile takes
+// a valid page without a check (its rows are never used).
+__device__ __forceinline__ int piece_row(const int32_t* seq_lens, const int32_t* block_table,
+                                         int max_len, int max_pages, int num_pages,
+                                         int page_size, int b, int tile_t0, int t, int* err) {
+    const int n = min(t / page_size, max_pages - 1);
+    int L = seq_lens[b];
+    int pg = block_table[static_cast<size_t>(b) * max_pages + n];
+    if (L < 1 || L > max_len) {
+        record_error(err, KVD_ERR_DEVICE_OOB);
+        L = min(max(L, 1), max_len);
+    }
+    if (tile_t0 >= L) return -1;
+    if (pg < 0 || pg >= num_pages) {
+        if (t < L) record_error(err, KVD_ERR_DEVICE_OOB);
+        pg = 0;
+    }
+    return pg * page_size + (t % page_size);
+}
+
 // Physical page of logical page n of sequence b, clamped to a valid page.
 __device__ __forceinline__ int load_page(const int32_t* block_table, int max_pages,
                                          int num_pages, int b, int n, int* err) {

@@ -198,6 +198,8 @@ struct MlaParams {
     int* err;
     int B, page_size, max_pages, num_pages, max_len;
     int n_clusters, idx_stride, sparse;
+    int tile;                  // tokens per tile of the kernel that wrote the partials
+    int gap;                   // virtual tiles before each later sequence (piece_gap)
     float scale_log2;
 };
 

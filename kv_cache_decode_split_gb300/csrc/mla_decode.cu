@@ -29,16 +29,14 @@
 
 #include <algorithm>
 
-#include "kvd_device.cuh"
-#include "kvd_host.h"
+#include "mla_common.cuh"
 
 namespace kvd {
 
 namespace {
 
-constexpr int kH = 128;               // heads (MMA M)
-constexpr int kDqk = 576;
-constexpr int kDv = 512;
+using namespace mla;
+
 constexpr int kTok = 64;              // tokens per tile
 constexpr int kNBox = 5;              // 64-dim boxes held per CTA (rank 0 uses 4)
 constexpr int kStages = 4;
@@ -52,26 +50,6 @@ constexpr int kSoftWarps = 4 * kGroups;
 constexpr int kThreads = (kSoftWarps + 4) * 32;
 constexpr int kWarpLoad = kSoftWarps, kWarpQK = kSoftWarps + 1, kWarpPV = kSoftWarps + 2,
               kWarpX = kSoftWarps + 3;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr float kLn2 = 0.6931471805599453f;
-
-// Part of a cluster's tile range inside one sequence: tokens [lo, hi) of sequence b, which
-// holds `items` tokens (or selected tokens).
-struct Piece {
-    int b, items, lo, hi;
-};
-constexpr int kMaxPieces = 32;
-
-// A range that moves on to the next sequence pays for an output write and a query load,
-// worth about kPieceGap tiles of streaming. Ranges are cut in a virtual tile list with
-// kPieceGap empty positions before every sequence but the first, so that such a range holds
-// fewer tiles; only when ranges span at least 2 kPieceGap positions, so that every range
-// still holds tiles.
-constexpr int kPieceGap = 6;
-__device__ __forceinline__ long long piece_gap(long long T, int B, int n_clusters) {
-    const long long V = T + static_cast<long long>(kPieceGap) * (B - 1);
-    return V >= 2LL * kPieceGap * n_clusters ? kPieceGap : 0;
-}
 
 struct MlaSmem {
     uint8_t stage[kStages][kStageBytes];   // offset 0, 1024-aligned
@@ -96,12 +74,7 @@ struct MlaSmem {
     uint64_t qfull;          // the first piece's queries have landed in stages 2-3
     uint64_t qkend, pvend;   // every product the score / value issuer started has completed
     uint32_t tmem_base;
-    // the cluster's schedule, built once: tile range and its pieces (n_pieces < 0: more
-    // pieces than the table holds, walked from the sequence lengths instead)
-    long long t0, t1, gap;   // virtual tile range and the gap before each later sequence
-    int n_tiles;             // tiles of the range
-    int n_pieces;
-    Piece piece[kMaxPieces];
+    Sched sched;             // the cluster's tile range and pieces, built once
 };
 
 // Tensor-memory columns (all 512): this CTA's query slice (bf16 pairs, up to 320 dims), one
@@ -111,33 +84,6 @@ constexpr uint32_t kColQ = 0, kColS = 160, kColP = 224, kColO = 256;
 // the kernel declares no static shared memory (checked at run time).
 constexpr int kMlaSmem = static_cast<int>(sizeof(MlaSmem));
 static_assert(kMlaSmem <= 227 * 1024, "MLA shared memory");
-
-__device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
-
-// Transpose an 8 x 8 array of 16-byte chunks held by each group of eight lanes: lane i of the
-// group holds chunk j of row i in ch[j] on entry and chunk i of row j on exit (three
-// butterfly stages of shuffles). All lanes of the warp take part.
-__device__ __forceinline__ void transpose8_chunks(float4 (&ch)[8], int lane) {
-#pragma unroll
-    for (int m = 4; m >= 1; m >>= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (j & m) continue;
-            const int hi = j | m;
-            float4 send = upper ? ch[j] : ch[hi];
-            float4 recv;
-            recv.x = __shfl_xor_sync(0xffffffffu, send.x, m);
-            recv.y = __shfl_xor_sync(0xffffffffu, send.y, m);
-            recv.z = __shfl_xor_sync(0xffffffffu, send.z, m);
-            recv.w = __shfl_xor_sync(0xffffffffu, send.w, m);
-            if (upper)
-                ch[j] = recv;
-            else
-                ch[hi] = recv;
-        }
-    }
-}
 
 // Score product of one tile: S (TMEM) = q_r (TMEM, NK 16-dim k-steps) x this CTA's
 // 64-dim boxes of the tile (shared memory, K-major). Fully unrolled with the descriptors
@@ -163,95 +109,6 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t tile_addr, bool
         tc_mma_bf16_ts(tmem + kColO, tmem + kColP + ks * 8,
                        bd + static_cast<uint64_t>((ks * 16 * 128) >> 4), idesc,
                        (accumulate || ks > 0) ? 1u : 0u);
-}
-
-// Work of one sequence: its item count (tokens, or selected tokens) and 64-token tiles.
-template <bool kSparse>
-__device__ __forceinline__ int seq_items(const MlaParams& p, int b, int* err) {
-    if (kSparse) return min(max(p.idx_count[b], 0), p.idx_stride);
-    return load_len(p.seq_lens, b, p.max_len, err);
-}
-
-// Cluster c's range [t0, t1) of the list of all sequences' tiles and the pieces it meets,
-// into shared memory. One warp: the lanes load 32 sequences' lengths at a time and a warp
-// scan turns their tile counts into tile offsets, so that the walk costs one memory round
-// trip per 32 sequences.
-template <bool kSparse>
-__device__ void build_schedule(const MlaParams& p, int c, int n_clusters, MlaSmem& sm,
-                               int lane, int* err) {
-    long long T = 0;
-    for (int base = 0; base < p.B; base += 32) {
-        const int bb = base + lane;
-        int n = bb < p.B ? (seq_items<kSparse>(p, bb, err) + kTok - 1) / kTok : 0;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
-        T += n;
-    }
-    const long long X = piece_gap(T, p.B, n_clusters);
-    const long long V = T + X * (p.B - 1);
-    const long long t0 = V * c / n_clusters, t1 = V * (c + 1) / n_clusters;
-    long long run = 0;  // tiles of the sequences before this batch
-    int np = 0, n_real = 0;
-    for (int base = 0; base < p.B && run + X * base < t1; base += 32) {
-        const int bb = base + lane;
-        const int items = bb < p.B ? seq_items<kSparse>(p, bb, nullptr) : 0;
-        const int n = (items + kTok - 1) / kTok;
-        int incl = n;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += v;
-        }
-        const long long sb = run + incl - n + X * bb;  // the lane's sequence's first position
-        const long long lo_t = max(t0, sb) - sb, hi_t = min(t1, sb + n) - sb;
-        const bool has = bb < p.B && hi_t > lo_t;
-        const unsigned m = __ballot_sync(0xffffffffu, has);
-        const int slot = np + __popc(m & ((1u << lane) - 1u));
-        if (has && slot < kMaxPieces)
-            sm.piece[slot] = Piece{bb, items, static_cast<int>(lo_t) * kTok,
-                                   min(static_cast<int>(hi_t) * kTok, items)};
-        int nr = has ? static_cast<int>(hi_t - lo_t) : 0;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) nr += __shfl_xor_sync(0xffffffffu, nr, off);
-        n_real += nr;
-        np += __popc(m);
-        run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) {
-        sm.t0 = t0;
-        sm.t1 = t1;
-        sm.gap = X;
-        sm.n_tiles = n_real;
-        sm.n_pieces = np <= kMaxPieces ? np : -1;
-    }
-}
-
-// Calls f(b, items, lo, hi, k) for the k-th piece of the range: tokens [lo, hi) of
-// sequence b (multiples of 64 except at the end of the sequence).
-template <bool kSparse, typename F>
-__device__ __forceinline__ void for_each_piece(const MlaParams& p, const MlaSmem& sm, F&& f) {
-    const int np = sm.n_pieces;
-    if (np >= 0) {
-        for (int k = 0; k < np; ++k) {
-            const Piece pc = sm.piece[k];
-            f(pc.b, pc.items, pc.lo, pc.hi, k);
-        }
-        return;
-    }
-    const long long t0 = sm.t0, t1 = sm.t1, X = sm.gap;
-    long long base = 0;  // virtual position of sequence b's first tile
-    int k = 0;
-    for (int b = 0; b < p.B && base < t1; ++b) {
-        const int items = seq_items<kSparse>(p, b, nullptr);
-        const int n = (items + kTok - 1) / kTok;
-        const long long lo_t = max(t0, base) - base, hi_t = min(t1, base + n) - base;
-        if (hi_t > lo_t) {
-            f(b, items, static_cast<int>(lo_t) * kTok,
-              min(static_cast<int>(hi_t) * kTok, items), k);
-            ++k;
-        }
-        base += n + X;
-    }
 }
 
 template <bool kSparse>
@@ -315,9 +172,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     griddep_wait();  // lengths, selected indices and the workspace are read from here on
     if (warp == 0)
-        build_schedule<kSparse>(p, cl, n_cl, sm, lane, rank == 0 ? p.err : nullptr);
+        build_schedule<kSparse, kTok>(p, cl, n_cl, sm.sched, lane, rank == 0 ? p.err : nullptr);
     __syncthreads();
-    const int n_tiles = sm.n_tiles;
+    const int n_tiles = sm.sched.n_tiles;
     if (n_tiles == 0) {  // both CTAs of the pair take this exit together, with no remote access
         if (warp == kWarpQK) tmem_dealloc(tmem, 512);
         return;
@@ -325,7 +182,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // With the piece table: the first piece's query slice comes by TMA into ring stages 2-3
     // (16 KB per 64-dim box), issued ahead of the first tiles, which take stages 0-1; the
     // producer reuses stages 2-3 once the queries are in tensor memory.
-    const bool tma_q = sm.n_pieces > 0;
+    const bool tma_q = sm.sched.n_pieces > 0;
     constexpr int kQBox = kH * 128;
     // the partner's partial scores of the first tile of each group (later tiles: armed by
     // the group once the slot's previous phase has completed). A copy that lands before
@@ -343,7 +200,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&sm.qfull, nbox * kQBox);
                 for (int bx = 0; bx < nbox; ++bx)
                     tma_load_2d(sm.stage[2] + bx * kQBox, &tmQ, &sm.qfull, dim0 + 64 * bx,
-                                sm.piece[0].b * kH);
+                                sm.sched.piece[0].b * kH);
             }
         }
         int g = 0;  // tile index within this CTA's range
@@ -356,7 +213,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0) ok = mbar_wait(&sm.qready, 0, p.err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
         };
-        for_each_piece<kSparse>(p, sm, [&](int b, int items, int lo, int hi, int) {
+        for_each_piece<kSparse, kTok>(p, sm.sched, [&](int b, int items, int lo, int hi, int) {
             if (!ok) return;
             const int nt = (hi - lo + kTok - 1) / kTok;
             if (!kSparse) {
@@ -498,7 +355,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int g = 0;
             bool ok = true;
-            for_each_piece<kSparse>(p, sm, [&](int, int, int lo, int hi, int k) {
+            for_each_piece<kSparse, kTok>(p, sm.sched, [&](int, int, int lo, int hi, int k) {
                 if (!ok || !(ok = mbar_wait(&sm.qready, k & 1, p.err))) return;
                 const int nt = (hi - lo + kTok - 1) / kTok;
                 for (int i = 0; i < nt; ++i, ++g) {
@@ -524,7 +381,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int g = 0;
             bool ok = true;
-            for_each_piece<kSparse>(p, sm, [&](int, int, int lo, int hi, int k) {
+            for_each_piece<kSparse, kTok>(p, sm.sched, [&](int, int, int lo, int hi, int k) {
                 if (!ok) return;
                 const int nt = (hi - lo + kTok - 1) / kTok;
                 for (int i = 0; i < nt; ++i, ++g) {
@@ -646,12 +503,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // With the piece table, the next piece's queries are loaded as soon as the current
         // piece's score products have all completed (before its output is written), so that
         // the next products overlap that write; otherwise each piece loads its own.
-        const int n_pieces = sm.n_pieces;
+        const int n_pieces = sm.sched.n_pieces;
         // Every piece ends in two named barriers of all eight warps, reached even after a
         // failed wait, so that no warp is left waiting there.
-        for_each_piece<kSparse>(p, sm, [&](int b, int, int lo, int hi, int k) {
+        for_each_piece<kSparse, kTok>(p, sm.sched, [&](int b, int, int lo, int hi, int k) {
             const int nt = (hi - lo + kTok - 1) / kTok;
-            const int next_b = (n_pieces >= 0 && k + 1 < n_pieces) ? sm.piece[k + 1].b : -1;
+            const int next_b = (n_pieces >= 0 && k + 1 < n_pieces) ? sm.sched.piece[k + 1].b : -1;
             if (ok && k == 0 && tma_q) {
                 load_q_staged();
             } else if (ok && (k == 0 || n_pieces < 0)) {
@@ -913,7 +770,7 @@ __global__ void __launch_bounds__(256, 4) mla_combine_kernel(const MlaParams p,
             if (bb < p.B)
                 items = p.sparse ? min(max(p.idx_count[bb], 0), p.idx_stride)
                                  : load_len(p.seq_lens, bb, p.max_len, nullptr);
-            const int n = (items + kTok - 1) / kTok;
+            const int n = (items + p.tile - 1) / p.tile;
             int incl = n;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -931,7 +788,7 @@ __global__ void __launch_bounds__(256, 4) mla_combine_kernel(const MlaParams p,
         if (lane == 0) {
             const long long C = p.n_clusters;
             // the decode kernel's virtual tile list (a gap before every later sequence)
-            const long long X = piece_gap(T, p.B, p.n_clusters);
+            const long long X = piece_gap(T, p.B, p.n_clusters, p.gap);
             const long long V = T + X * (p.B - 1), Vb = Sb + X * b;
             int n = 0;
             if (nb > 0 && (X > 0 || T >= C)) {
