@@ -418,7 +418,7 @@ __device__ __forceinline__ void load_hist(uint32_t* h, const uint32_t* src) {
 
 constexpr int kSelThreads = 512;
 static_assert(kSelThreads >= 256, "a thread per second-level bin");
-constexpr int kSelPerThread = 16;
+constexpr int kSelPerThread = 8;
 constexpr int kRankMax = 256;  // a threshold bucket this small is finished by ranking its keys
 constexpr int kRadixBits = 8;  // digit of the passes after the histogram's top 11 bits
 

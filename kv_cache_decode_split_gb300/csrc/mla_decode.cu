@@ -275,10 +275,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 auto tok_of = [&](int i, int rr) -> int {
                     return has_row(i, rr) ? idx[lo + i * kTok + lane + 32 * rr] : -1;
                 };
+                // the block-table entry of t's page, read without waiting for the length
+                // (checked once both have arrived)
                 auto page_of = [&](int t) -> int {
-                    return (t >= 0 && t < L) ? load_page(p.block_table, p.max_pages, p.num_pages,
-                                                         b, t / p.page_size, p.err)
-                                             : 0;
+                    if (t < 0) return 0;
+                    const int pg = p.block_table[static_cast<size_t>(b) * p.max_pages +
+                                                 min(t / p.page_size, p.max_pages - 1)];
+                    if (t >= L) return 0;
+                    if (pg < 0 || pg >= p.num_pages) {
+                        record_error(p.err, KVD_ERR_DEVICE_OOB);
+                        return 0;
+                    }
+                    return pg;
                 };
                 // the row's first element of this CTA's dims, or null for a zero row
                 auto src_of = [&](bool has, int t, int pg) -> const __nv_bfloat16* {
@@ -742,7 +750,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // Merge the pieces of each (sequence, head): o = sum_i 2^{lse_i - M} o_i / sum_i 2^{lse_i - M}.
 // Two heads per block; each thread owns four value dims and streams every piece. Sequence
 // b's pieces come from the clusters whose tile ranges meet b's tiles (slot = cluster + b).
-__global__ void __launch_bounds__(256, 4) mla_combine_kernel(const MlaParams p,
+// kBuf partials of each thread in flight at once: 16 for the sparse decode (its sequences
+// meet about 16 pieces each), 8 for the dense one (about 5, four blocks per SM).
+template <int kBuf>
+__global__ void __launch_bounds__(256, kBuf > 8 ? 2 : 4) mla_combine_kernel(const MlaParams p,
                                                              __nv_bfloat16* out,
                                                              float* lse_out) {
     griddep_wait();
@@ -819,7 +830,6 @@ __global__ void __launch_bounds__(256, 4) mla_combine_kernel(const MlaParams p,
         return __ldcg(reinterpret_cast<const float4*>(
             p.part_o + (static_cast<size_t>(s_slot[i]) * kH + h) * kDv + d));
     };
-    constexpr int kBuf = 8;
     float4 vb[kBuf];
 #pragma unroll
     for (int i = 0; i < kBuf; ++i)
@@ -875,9 +885,12 @@ int mla_launch(const MlaParams& p, const CUtensorMap& tc0, const CUtensorMap& tc
                  : launch_kernel(mla_decode_kernel<false>, dim3(grid), dim3(kThreads), kMlaSmem,
                                  stream, tc0, tc1, tc2, tq, p);
     if (e1 != cudaSuccess) return KVD_ERR_CUDA;
-    if (launch_kernel(mla_combine_kernel, dim3(p.B * (kH / 2)), dim3(256), 0, stream, p,
-                      static_cast<__nv_bfloat16*>(out), lse_out) != cudaSuccess)
-        return KVD_ERR_CUDA;
+    const cudaError_t e2 =
+        p.sparse ? launch_kernel(mla_combine_kernel<16>, dim3(p.B * (kH / 2)), dim3(256), 0,
+                                 stream, p, static_cast<__nv_bfloat16*>(out), lse_out)
+                 : launch_kernel(mla_combine_kernel<8>, dim3(p.B * (kH / 2)), dim3(256), 0,
+                                 stream, p, static_cast<__nv_bfloat16*>(out), lse_out);
+    if (e2 != cudaSuccess) return KVD_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }
 
