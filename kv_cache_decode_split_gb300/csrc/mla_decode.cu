@@ -263,9 +263,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             } else {
                 // gather the selected rows: each lane copies rows lane and lane + 32 of the
                 // tile (one row per lane and instruction issues faster than one row per
-                // instruction); a tile's arrival is signalled once the next tile's copies are
-                // issued. Row sources are resolved a tile ahead (token indices two tiles
-                // ahead), so that neither dependent load waits in front of the copies.
+                // instruction); each lane's copies arrive on the tile's barrier when they land,
+                // without the lane waiting. Row sources are resolved a tile ahead (token
+                // indices two tiles ahead), so that neither dependent load waits in front of
+                // the copies.
                 const int L = load_len(p.seq_lens, b, p.max_len, nullptr);
                 const __nv_bfloat16* cpool = reinterpret_cast<const __nv_bfloat16*>(p.c_pool);
                 const int32_t* idx = p.idx + static_cast<size_t>(b) * p.idx_stride;
@@ -329,12 +330,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             cp_async_16(dst, src ? src + c * 8 : cpool, src ? 16u : 0u, pol);
                         }
                     }
-                    cp_async_commit();
-                    if (g >= 1) {
-                        cp_async_wait<1>();
-                        fence_proxy_async_smem();
-                        mbar_arrive(&sm.full[(g - 1) % kStages]);
-                    }
+                    // the tile's arrival: each lane's share once its copies have landed (the
+                    // product issuers order these generic-proxy writes before their reads)
+                    cp_async_arrive_noinc(&sm.full[s]);
                     src_cur[0] = src_of(has_row(i + 1, 0), t_nxt[0], pg_n0);
                     src_cur[1] = src_of(has_row(i + 1, 1), t_nxt[1], pg_n1);
                     t_nxt[0] = t_nn0;
@@ -343,11 +341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
         });
         if (kSparse) {
-            cp_async_wait<0>();
-            if (ok) {
-                fence_proxy_async_smem();
-                mbar_arrive(&sm.full[(g - 1) % kStages]);
-            }
+            cp_async_wait<0>();  // every issued copy lands before the CTA goes on
         } else if (lane == 0) {
             // every issued copy lands before the CTA goes on (also after a wait gave up: the
             // ring's shared memory must not be written once the CTA has exited)
@@ -371,6 +365,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     ok = mbar_wait(&sm.full[s], (g / kStages) & 1, p.err) &&
                          mbar_wait(&sm.sempty, (g & 1) ^ 1, p.err);
                     if (!ok) return;
+                    // gathered rows were written by cp.async (generic proxy): ordered before
+                    // the tensor core's reads here
+                    if (kSparse) fence_proxy_async_smem();
                     tc_fence_after();
                     if (nbox == 4)
                         issue_qk<16>(tmem, smem_u32(sm.stage[s]));
@@ -397,6 +394,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // a piece's first product overwrites O: the previous piece's O is read
                     if (i == 0 && k > 0 && !(ok = mbar_wait(&sm.ofree, (k - 1) & 1, p.err))) return;
                     if (!(ok = mbar_wait(&sm.pfull, g & 1, p.err))) return;
+                    if (kSparse) fence_proxy_async_smem();
                     tc_fence_after();
                     issue_pv(tmem, smem_u32(sm.stage[s]), i > 0);
                     tc_commit(&sm.pvdone[g % kGroups]);
