@@ -10,9 +10,9 @@
 //  * quest_minmax_kernel: one warp per (page, KV head): the page's keys once, min and max in
 //    the cache's own dtype (exact). Run once per page, when it fills.
 //  * quest_bounds_kernel: one CTA per (sequence, KV head, 128 pages), a warp per 32 pages
-//    (their page ids in one load, eight pages' summaries in flight): a lane holds its D/32
-//    dims of kmin/kmax and of the group's queries, and warp sums give every query head of
-//    the group its bound, written to the caller's bound array.
+//    (their page ids in one load, all their summaries copied into shared memory at once): a
+//    lane holds its D/32 dims of kmin/kmax and of the group's queries, and warp sums give
+//    every query head of the group its bound, written to the caller's bound array.
 //  * quest_choose_kernel: one warp per (sequence, query head) picks the n_sel best bounds
 //    (value, then lower index): each lane sorts its own pages once, then every round takes
 //    the best of the lanes' heads by two warp max-reductions; written in ascending order.
@@ -166,63 +166,118 @@ __global__ void __launch_bounds__(256) quest_minmax_kernel(const QuestParams p) 
 
 // ---------------------------------------------------------------------------- bounds
 // One CTA of kBoundWarps warps per (sequence, KV head, 32 * kBoundWarps pages); a warp takes
-// 32 pages: their page ids in one load, then kPagesInFlight pages' summaries at once, and
-// for each page the bounds of the KG (>= G) query heads of the group by warp sums.
+// 32 pages. The sequence's length and the warp's 32 page ids are read together, then all the
+// warp's pages' summaries (the kmin and kmax rows) are copied into its shared-memory slot at
+// once (cp.async, no registers held): one memory round trip for the summaries instead of one
+// per batch of pages. The bounds are computed from shared memory: a lane holds D/32 dims of
+// each page and of the group's queries, and 32 / KG pages' (page, head) partial sums at a
+// time are reduced across the warp by a transposing butterfly (31 shuffles for all 32 sums,
+// lane i ending with sum i) instead of five shuffle levels per sum.
 constexpr int kBoundWarps = 4;
+
+template <int VEC, bool BF16>
+constexpr int bound_row_bytes() {  // one summary row (kmin or kmax) of a (page, KV head)
+    return VEC * 32 * (BF16 ? 2 : 4);
+}
+template <int VEC, bool BF16>
+constexpr int bound_smem_bytes() {
+    return kBoundWarps * 32 * 2 * bound_row_bytes<VEC, BF16>();
+}
 
 template <int VEC, bool BF16, int KG>
 __global__ void __launch_bounds__(kBoundWarps * 32) quest_bounds_kernel(const QuestParams p) {
     constexpr int D = VEC * 32;
+    constexpr int kRow = bound_row_bytes<VEC, BF16>();
+    constexpr int kPieces = 2 * kRow / 16;  // 16-byte pieces of a page's two rows
+    extern __shared__ __align__(16) uint8_t bsm[];
     griddep_wait();
     const int b = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
     const int G = p.Hq / p.Hkv;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int L = load_len(p.seq_lens, b, p.max_len, p.err);
-    const int full = L / p.page_size;
     const int m0 = (blockIdx.y * kBoundWarps + warp) * 32;
+    const int my = m0 + lane;
+    // the length and this lane's block-table entry in flight together
+    int L = p.seq_lens[b];
+    const int pg_raw = my < p.max_pages ? p.block_table[static_cast<size_t>(b) * p.max_pages + my]
+                                        : 0;
+    if (L < 1 || L > p.max_len) {
+        record_error(p.err, KVD_ERR_DEVICE_OOB);
+        L = min(max(L, 1), p.max_len);
+    }
+    const int full = L / p.page_size;
     float* ub = p.ub_out + (static_cast<size_t>(b) * p.Hq + g * G) * p.max_pages;
     // pages that are not full have no bound
     for (int j = 0; j < G; ++j)
-        if (m0 + lane >= full && m0 + lane < p.max_pages)
-            ub[static_cast<size_t>(j) * p.max_pages + m0 + lane] = __int_as_float(0x7fc00000);
+        if (my >= full && my < p.max_pages)
+            ub[static_cast<size_t>(j) * p.max_pages + my] = __int_as_float(0x7fc00000);
     if (m0 >= full) return;
+    int pg_lane = 0;
+    if (my < full) {
+        pg_lane = pg_raw;
+        if (pg_lane < 0 || pg_lane >= p.num_pages) {
+            record_error(p.err, KVD_ERR_DEVICE_OOB);
+            pg_lane = 0;
+        }
+    }
+    const int n_here = min(32, full - m0);
+    // page k of the warp: its kmin row at ws + 2 k kRow, its kmax row after it
+    uint8_t* ws = bsm + warp * 32 * 2 * kRow;
+    for (int k = 0; k < n_here; ++k) {
+        const int pg = __shfl_sync(0xffffffffu, pg_lane, k);
+        const size_t row = (static_cast<size_t>(pg) * p.Hkv + g) * kRow;
+        for (int pc = lane; pc < kPieces; pc += 32) {
+            const bool upper = pc >= kRow / 16;
+            const uint8_t* src = static_cast<const uint8_t*>(upper ? p.kmax : p.kmin) + row +
+                                 (upper ? pc - kRow / 16 : pc) * 16;
+            cp_async_16(smem_u32(ws + k * 2 * kRow + pc * 16), src, 16u);
+        }
+    }
+    cp_async_commit();
+    // the group's queries while the summaries are on their way
     float q[KG][VEC];
 #pragma unroll
     for (int j = 0; j < KG; ++j)
         if (j < G)
             load_vec<VEC, BF16>(p.q, (static_cast<size_t>(b) * p.Hq + g * G + j) * D + lane * VEC,
                                 q[j]);
-    const int my = m0 + lane;
-    const int pg_lane =
-        my < full ? load_page(p.block_table, p.max_pages, p.num_pages, b, my, p.err) : 0;
-    const int n_here = min(32, full - m0);
-    // 32 / KG pages at a time: their 32 (page, head) partial sums are reduced across the
-    // warp together by a transposing butterfly (31 shuffles for all 32 sums; lane i ends
-    // with sum i), instead of five shuffle levels per sum
+    // bf16 summaries: max(q kmin, q kmax) = q+ kmax + q- kmin (q+ = max(q, 0), q- = min(q, 0),
+    // kmin <= kmax), two fused multiply-adds a term. A bf16 x bf16 product is exact in fp32
+    // and one of the two is zero, so every partial sum is rounded exactly as in the max form
+    // (for finite summaries). float32 summaries keep the max form.
+    float qp[KG][VEC], qn[KG][VEC];
+#pragma unroll
+    for (int j = 0; j < KG; ++j)
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            qp[j][i] = fmaxf(q[j][i], 0.f);
+            qn[j][i] = fminf(q[j][i], 0.f);
+        }
+    cp_async_wait<0>();
+    __syncwarp();
     constexpr int NP = 32 / KG;
     for (int c = 0; c < n_here; c += NP) {
-        Raw<VEC, BF16> lo[NP], hi[NP];
-#pragma unroll
-        for (int k = 0; k < NP; ++k) {
-            const int pg = __shfl_sync(0xffffffffu, pg_lane, (c + k) & 31);
-            if (c + k < n_here) {
-                const size_t o = (static_cast<size_t>(pg) * p.Hkv + g) * D + lane * VEC;
-                lo[k].load(p.kmin, o);
-                hi[k].load(p.kmax, o);
-            }
-        }
         float v[32];  // v[k * KG + j]: page c + k, head j
 #pragma unroll
-        for (int k = 0; k < NP; ++k)
+        for (int k = 0; k < NP; ++k) {
+            Raw<VEC, BF16> lo, hi;
+            if (c + k < n_here) {
+                lo.load(ws + (c + k) * 2 * kRow, lane * VEC);
+                hi.load(ws + (c + k) * 2 * kRow + kRow, lane * VEC);
+            }
 #pragma unroll
             for (int j = 0; j < KG; ++j) {
                 float a = 0.f;
                 if (c + k < n_here)
 #pragma unroll
-                    for (int i = 0; i < VEC; ++i)
-                        a += fmaxf(q[j][i] * lo[k].at(i), q[j][i] * hi[k].at(i));
+                    for (int i = 0; i < VEC; ++i) {
+                        if constexpr (BF16)
+                            a = fmaf(qp[j][i], hi.at(i), fmaf(qn[j][i], lo.at(i), a));
+                        else
+                            a += fmaxf(q[j][i] * lo.at(i), q[j][i] * hi.at(i));
+                    }
                 v[k * KG + j] = a;
             }
+        }
 #pragma unroll
         for (int sft = 16; sft >= 1; sft >>= 1) {
             const bool upper = (lane & sft) != 0;
@@ -325,7 +380,7 @@ __device__ __forceinline__ void choose_pages(uint64_t* key, int full, int n_sel,
 __global__ void __launch_bounds__(kChooseWarps * 32) quest_choose_kernel(const QuestParams p) {
     extern __shared__ uint64_t ubs[];  // [kChooseWarps][max_pages] sort keys
     griddep_wait();
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int warp = threadIdx.x / 32;
     const int bh = blockIdx.x * kChooseWarps + warp;
     if (bh >= p.B * p.Hq) return;
     const int b = bh / p.Hq;
@@ -504,15 +559,29 @@ size_t quest_select_smem(int Hq, int Hkv, int max_pages) {
     return sizeof(uint64_t) * static_cast<size_t>(kChooseWarps) * max_pages;
 }
 
+template <int VEC, bool BF16, int KG>
+static cudaError_t bounds_launch_kg(const QuestParams& p, dim3 grid, cudaStream_t stream) {
+    constexpr int kSmem = bound_smem_bytes<VEC, BF16>();
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(quest_bounds_kernel<VEC, BF16, KG>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   kSmem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    return launch_kernel(quest_bounds_kernel<VEC, BF16, KG>, grid, dim3(kBoundWarps * 32), kSmem,
+                         stream, p);
+}
+
 template <int VEC, bool BF16>
 static cudaError_t bounds_launch(const QuestParams& p, dim3 grid, cudaStream_t stream) {
     const int G = p.Hq / p.Hkv;
-    const dim3 block(kBoundWarps * 32);
-    if (G <= 1) return launch_kernel(quest_bounds_kernel<VEC, BF16, 1>, grid, block, 0, stream, p);
-    if (G <= 2) return launch_kernel(quest_bounds_kernel<VEC, BF16, 2>, grid, block, 0, stream, p);
-    if (G <= 4) return launch_kernel(quest_bounds_kernel<VEC, BF16, 4>, grid, block, 0, stream, p);
-    if (G <= 8) return launch_kernel(quest_bounds_kernel<VEC, BF16, 8>, grid, block, 0, stream, p);
-    return launch_kernel(quest_bounds_kernel<VEC, BF16, 16>, grid, block, 0, stream, p);
+    if (G <= 1) return bounds_launch_kg<VEC, BF16, 1>(p, grid, stream);
+    if (G <= 2) return bounds_launch_kg<VEC, BF16, 2>(p, grid, stream);
+    if (G <= 4) return bounds_launch_kg<VEC, BF16, 4>(p, grid, stream);
+    if (G <= 8) return bounds_launch_kg<VEC, BF16, 8>(p, grid, stream);
+    return bounds_launch_kg<VEC, BF16, 16>(p, grid, stream);
 }
 
 int quest_bounds_launch(const QuestParams& p, cudaStream_t stream) {
