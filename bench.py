@@ -52,58 +52,58 @@ def l2_bytes(dev):
 # still hashes to the value recorded with the capture: a changed kernel reports null.
 NCU_TRAFFIC = {
     "llama3_8b_gqa_paged": {  # gqa_decode_bf16_kernel<128, 1, 1, 0>
-        "bytes": 794.194688e6 + 4.014336e6,
+        "bytes": 794.202880e6 + 4.013312e6,
         "sources": ('gqa_decode.cu', 'kvd_device.cuh'),
         "structs": ('GqaParams',),
-        "sha256": "d3f4e5b8c44da12d42b9a3b09d811f3d191b448386bbbee30c6075bccca24015",
+        "sha256": "49ac76b60bfa4876c6d331712741cb6d3b1d9b38e5c30611856a42b442d0682f",
     },
     "swa_sink_tokens": {  # gqa_decode_bf16_kernel<64, 1, 2, 1>
-        "bytes": 68.293120e6 + 0.768000e6,
+        "bytes": 68.293376e6 + 0.753152e6,
         "sources": ('gqa_decode.cu', 'kvd_device.cuh'),
         "structs": ('GqaParams',),
-        "sha256": "d3f4e5b8c44da12d42b9a3b09d811f3d191b448386bbbee30c6075bccca24015",
+        "sha256": "49ac76b60bfa4876c6d331712741cb6d3b1d9b38e5c30611856a42b442d0682f",
     },
     "swa_learned_sink": {  # gqa_decode_bf16_kernel<64, 1, 2, 1>
-        "bytes": 67.245056e6 + 0.760320e6,
+        "bytes": 67.244288e6 + 0.715008e6,
         "sources": ('gqa_decode.cu', 'kvd_device.cuh'),
         "structs": ('GqaParams',),
-        "sha256": "d3f4e5b8c44da12d42b9a3b09d811f3d191b448386bbbee30c6075bccca24015",
+        "sha256": "49ac76b60bfa4876c6d331712741cb6d3b1d9b38e5c30611856a42b442d0682f",
     },
     "swa_ring_sink_tokens": {  # gqa_decode_bf16_kernel<64, 1, 2, 1>
-        "bytes": 68.277248e6 + 0.676096e6,
+        "bytes": 68.276736e6 + 0.685312e6,
         "sources": ('gqa_decode.cu', 'kvd_device.cuh'),
         "structs": ('GqaParams',),
-        "sha256": "d3f4e5b8c44da12d42b9a3b09d811f3d191b448386bbbee30c6075bccca24015",
+        "sha256": "49ac76b60bfa4876c6d331712741cb6d3b1d9b38e5c30611856a42b442d0682f",
     },
     "mla_dsv3": {  # mla_decode_kernel<0>
-        "bytes": 304.508928e6 + 4.190464e6,
-        "sources": ('mla_decode.cu', 'kvd_device.cuh'),
+        "bytes": 304.507392e6 + 4.335360e6,
+        "sources": ('mla_decode.cu', 'mla_common.cuh', 'kvd_device.cuh'),
         "structs": ('MlaParams',),
-        "sha256": "26749f2aaf8e7ebe94821c459aa1c13902c3371608c3d275dec9d024e866c762",
+        "sha256": "d12bc57790b9e330179925ba9015a850cbfcad63e53a63110d264751ac33c05e",
     },
     "dsa_sparse_mla": {  # dsa_indexer_kernel
-        "bytes": 134.395392e6 + 3.844096e6,
+        "bytes": 134.377216e6 + 3.348992e6,
         "sources": ('dsa_indexer.cu', 'kvd_device.cuh'),
         "structs": ('IdxParams',),
-        "sha256": "2815ab8bc4e938c17d33e4e0704f2b3121df52ca1b3018d439571d23b841132f",
+        "sha256": "c7e6d104625ea3a605c70f8e1a103e5d9eb247401d7f6865facefc13e5f61177",
     },
     "dsa_fp8_sparse_mla": {  # dsa_indexer_fp8_kernel
-        "bytes": 69.331712e6 + 0.527360e6,
+        "bytes": 69.332480e6 + 0.649728e6,
         "sources": ('dsa_indexer_fp8.cu', 'kvd_device.cuh'),
         "structs": ('IdxParams',),
-        "sha256": "5985ab34b1f1896fc5f546ba968792192122720e1ca48b879ac947f8635a4f2e",
+        "sha256": "0a55f484ed0efb079b2451142ee561ee3a5964cf54d2c6cdaea73d54580fc1c9",
     },
     "quest_llama3": {  # quest_attn_kernel<4, 1, 1>
-        "bytes": 115.002624e6 + 3.696896e6,
+        "bytes": 115.007232e6 + 3.532544e6,
         "sources": ('quest.cu', 'kvd_device.cuh'),
         "structs": ('QuestParams',),
-        "sha256": "92bad60166a1ade8efaed8858cb87859df791997b381ccd2f94f8f0117a0f673",
+        "sha256": "6c403345102d1b15eaa76dc2ded113d3183617cb6d3a178aa20e474cf9ec37dd",
     },
     "kda_decode": {  # delta_step_kernel<4>
-        "bytes": 276.856320e6 + 211.294976e6,
+        "bytes": 276.865280e6 + 210.527488e6,
         "sources": ('delta_decode.cu', 'kvd_device.cuh'),
         "structs": ('DeltaParams',),
-        "sha256": "d4174dd2930227e6e9f717d5737a5f7ed5c44eb1d53acf85abef7cf44b9cf56c",
+        "sha256": "2cf6fbe2cec874d93563e27b72dd3fc3b8e4570552f784b73e86f25932109165",
     },
 }
 
