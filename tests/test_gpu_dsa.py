@@ -43,12 +43,16 @@ def _check_selection(idx, cnt, ref_scores, L, k):
 
 
 def _run_indexer(kvd, x, k):
+    # table slots past a sequence's last page hold -1; the indexer reads some of them ahead of
+    # the length and must neither use nor report them
     dev = "cuda"
+    ws = kvd.Workspace(dev)
     scores = torch.full((x.B, x.max_pages * x.page_size), float("nan"), device=dev)
     idx, cnt = kvd.dsa_indexer_topk(x.q.to(dev), x.k_pool.to(dev), x.w.to(dev),
                                     x.block_table.to(dev), x.seq_lens.to(dev), k=k,
-                                    scores_out=scores)
+                                    scores_out=scores, workspace=ws)
     torch.cuda.synchronize()
+    assert kvd.kvd_check_device_error(ws) == 0
     return idx, cnt, scores
 
 
@@ -213,12 +217,14 @@ def _chain(kvd, xi, xm, batches, n_pairs, seed):
     first), the output is compared with the oracle's MLA over the GPU's selection."""
     dev = "cuda"
     bt, sl = xm.block_table.to(dev), xm.seq_lens.to(dev)
+    ws_i, ws_m = kvd.Workspace(dev), kvd.Workspace(dev)
     idx, cnt = kvd.dsa_indexer_topk(xi.q.to(dev), xi.k_pool.to(dev), xi.w.to(dev), bt, sl,
-                                    k=xi.k)
+                                    k=xi.k, workspace=ws_i)
     lse = torch.empty(xm.B, xm.H, dtype=torch.float32, device=dev)
     out = kvd.attn_decode_mla_sparse(xm.q.to(dev), xm.c_pool.to(dev), bt, sl, idx, cnt,
-                                     scale=xm.scale, lse_out=lse)
+                                     scale=xm.scale, lse_out=lse, workspace=ws_m)
     torch.cuda.synchronize()
+    assert kvd.kvd_check_device_error(ws_i) == 0 and kvd.kvd_check_device_error(ws_m) == 0
     scores = oracle.indexer_scores(xi.q, xi.k_pool, xi.w, xi.block_table, xi.seq_lens,
                                    batches=batches)
     idx_h, cnt_h = idx.cpu().numpy(), cnt.cpu().numpy()

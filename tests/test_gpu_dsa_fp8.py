@@ -26,13 +26,17 @@ def kvd():
 
 
 def _run(kvd, x, k, workspace=None):
+    # table slots past a sequence's last page hold -1; the indexer reads some of them ahead of
+    # the length and must neither use nor report them
     dev = "cuda"
+    ws = kvd.Workspace(dev) if workspace is None else workspace
     scores = torch.full((x.B, x.max_pages * x.page_size), float("nan"), device=dev)
     idx, cnt = kvd.dsa_indexer_topk_fp8(x.q8.to(dev), x.q_scale.to(dev), x.k8_pool.to(dev),
                                         x.k_scale.to(dev), x.w.to(dev), x.block_table.to(dev),
                                         x.seq_lens.to(dev), k=k, scores_out=scores,
-                                        workspace=workspace)
+                                        workspace=ws)
     torch.cuda.synchronize()
+    assert kvd.kvd_check_device_error(ws) == 0
     return idx, cnt, scores
 
 

@@ -25,22 +25,30 @@ def kvd():
     return m
 
 
+# Block-table slots past a sequence's last page hold -1 in every workload: the kernels read
+# some of them ahead of the length (one memory round trip less) and must neither use nor
+# report them, so every call here also checks the device error flag.
 def _dense(kvd, x):
     dev = "cuda"
+    ws = kvd.Workspace(dev)
     lse = torch.empty(x.B, x.H, dtype=torch.float32, device=dev)
     out = kvd.attn_decode_mla(x.q.to(dev), x.c_pool.to(dev), x.block_table.to(dev),
-                              x.seq_lens.to(dev), scale=x.scale, lse_out=lse)
+                              x.seq_lens.to(dev), scale=x.scale, lse_out=lse, workspace=ws)
     torch.cuda.synchronize()
+    assert kvd.kvd_check_device_error(ws) == 0
     return out, lse
 
 
 def _sparse(kvd, x, idx, cnt):
     dev = "cuda"
+    ws = kvd.Workspace(dev)
     lse = torch.empty(x.B, x.H, dtype=torch.float32, device=dev)
     out = kvd.attn_decode_mla_sparse(x.q.to(dev), x.c_pool.to(dev), x.block_table.to(dev),
                                      x.seq_lens.to(dev), torch.as_tensor(idx).to(dev),
-                                     torch.as_tensor(cnt).to(dev), scale=x.scale, lse_out=lse)
+                                     torch.as_tensor(cnt).to(dev), scale=x.scale, lse_out=lse,
+                                     workspace=ws)
     torch.cuda.synchronize()
+    assert kvd.kvd_check_device_error(ws) == 0
     return out, lse
 
 
