@@ -146,7 +146,7 @@ def measured_peaks():
 # ---------------------------------------------------------------------------------------
 class GqaRunner:
     """attn_decode_gqa_paged / attn_decode_swa_sink on a named workload; on rolling caches,
-    cache_append of the step's new token then attn_decode_swa_ring."""
+    attn_decode_swa_ring_append (the step's new token appended, then attention: one call)."""
     launches_per_step = 1          # split-KV kernel; its last CTA per group combines
     kernel = "gqa_decode_bf16_kernel"
     cache_attrs = ("k", "v")       # the cache a step reads (copied for rotation)
@@ -173,8 +173,7 @@ class GqaRunner:
             self.h_knew = W.normal((x.B, x.Hkv, x.D), 1000 * wid + 20, 1.0, x.q.dtype)
             self.h_vnew = W.normal((x.B, x.Hkv, x.D), 1000 * wid + 21, 1.0, x.q.dtype)
             self.knew, self.vnew = self.h_knew.to(dev), self.h_vnew.to(dev)
-            self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-            self.launches_per_step = 2
+            self.launches_per_step = 1  # the attention launch writes the new rows itself
         self._config, self.bytes, self.flops = self.describe(name, x)
 
     @staticmethod
@@ -197,7 +196,7 @@ class GqaRunner:
                "seq_len_mean": float(x.seq_lens.float().mean()), "kv_bytes": nbytes}
         if x.ring:
             cfg["cache"] = f"rolling, {x.n_sink + x.window} slots per sequence"
-            cfg["step"] = "cache_append of the new token, then attention"
+            cfg["step"] = "the new token appended, then attention (attn_decode_swa_ring_append)"
         return cfg, nbytes, flops
 
     def step(self, q=None, out=None):
@@ -205,11 +204,10 @@ class GqaRunner:
         q = self.q if q is None else q
         out = self.out if out is None else out
         if self.ring:
-            self.kvd.cache_append(self.knew, self.vnew, self.k, self.v, self.bt, self.sl,
-                                  window=x.window, n_sink=x.n_sink, err=self.err)
-            return self.kvd.attn_decode_swa_ring(q, self.k, self.v, self.bt, self.sl, x.window,
-                                                 x.n_sink, self.sink, scale=x.scale, out=out,
-                                                 workspace=self.ws)
+            return self.kvd.attn_decode_swa_ring_append(q, self.knew, self.vnew, self.k, self.v,
+                                                        self.bt, self.sl, x.window, x.n_sink,
+                                                        self.sink, scale=x.scale, out=out,
+                                                        workspace=self.ws)
         if self.swa:
             return self.kvd.attn_decode_swa_sink(q, self.k, self.v, self.bt, self.sl, x.window,
                                                  x.n_sink, self.sink, scale=x.scale, out=out,

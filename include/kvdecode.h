@@ -31,11 +31,12 @@
  *    the indexer on e4m3 codes with row scales and the quantizer that fills its
  *    cache. "Long context, KV eviction and sparse attention", exact selection
  *    with a fast scorer (the indexer runs in FP8).
- *  - kvd_cache_append, attn_decode_swa_ring: the new token's K/V (or latent
- *    row) written into a paged or rolling cache, and sliding-window attention
- *    read from the rolling cache. "Attention Optimizations", DSA / Computation
- *    Path (update_cache before attention) and Sliding-window (a rolling buffer
- *    of W entries); "All the attentions", section 4.
+ *  - kvd_cache_append, attn_decode_swa_ring, attn_decode_swa_ring_append: the
+ *    new token's K/V (or latent row) written into a paged or rolling cache, and
+ *    sliding-window attention read from the rolling cache (the last one does
+ *    both in one call). "Attention Optimizations", DSA / Computation Path
+ *    (update_cache before attention) and Sliding-window (a rolling buffer of W
+ *    entries); "All the attentions", section 4.
  *  - quest_page_minmax, quest_select_pages, attn_decode_quest (and the split
  *    quest_page_bounds + attn_decode_quest_from_bounds): query-aware page
  *    selection. "Long context, KV eviction and sparse attention", Sparse attention
@@ -193,6 +194,29 @@ int attn_decode_swa_ring(const void *q, const void *k_ring, const void *v_ring,
                          int max_pages, int num_pages, float scale, int dtype, int window,
                          int n_sink_tokens, const float *sink_logit, void *ws, size_t ws_bytes,
                          cudaStream_t stream);
+
+/*
+ * One decode step on a rolling cache: exactly kvd_cache_append of the newest token's rows
+ * (k_new, v_new [B, Hkv, D], device, 16-byte aligned, the cache's dtype) into k_ring / v_ring
+ * with this window and n_sink_tokens, followed by attn_decode_swa_ring on the updated ring
+ * ("Attention Optimizations", DSA / Computation Path: the new token's cache row is written
+ * before attention runs; "All the attentions", section 4: the newest entry of the rolling
+ * buffer replaces the oldest). k_ring and v_ring are updated in place. For bf16 rings the
+ * attention launch writes the rows itself (each chunk of the ring that holds the newest
+ * slot writes them before reading it: one launch instead of two); float32 rings take the
+ * append's launch, then the attention's. A length below 1 or an out-of-range page id of the
+ * newest slot records KVD_ERR_DEVICE_OOB in the workspace's error flag (read it with
+ * kvd_check_device_error) and that sequence's rows are not written. Other arguments,
+ * workspace and host-side errors as attn_decode_swa_ring; every check runs before anything
+ * is written.
+ */
+int attn_decode_swa_ring_append(const void *q, const void *k_new, const void *v_new,
+                                void *k_ring, void *v_ring, const int32_t *block_table,
+                                const int32_t *seq_lens, void *out, float *lse_out, int B,
+                                int Hq, int Hkv, int D, int page_size, int max_pages,
+                                int num_pages, float scale, int dtype, int window,
+                                int n_sink_tokens, const float *sink_logit, void *ws,
+                                size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Cache append ("Attention Optimizations", DSA / Computation Path: the new token's cache

@@ -18,6 +18,7 @@ Operations:
   delta_decode_step       one gated delta-rule (Gated DeltaNet / KDA) decode step
   cache_append            the new token's K/V (or latent row) into a paged or rolling cache
   attn_decode_swa_ring    sliding window + sinks over a rolling cache
+  attn_decode_swa_ring_append   cache_append of the newest token, then attn_decode_swa_ring
   quest_page_minmax, quest_select_pages, attn_decode_quest   Quest page selection
 """
 from __future__ import annotations
@@ -35,7 +36,8 @@ lib = _lib.load()
 __all__ = [
     "attn_decode_gqa_paged", "attn_decode_swa_sink", "attn_decode_mla", "dsa_indexer_topk",
     "dsa_indexer_topk_fp8", "quantize_e4m3_rows", "dsa_indexer_cache_append_fp8",
-    "delta_decode_step", "attn_decode_swa_ring", "cache_append", "quest_page_minmax",
+    "delta_decode_step", "attn_decode_swa_ring", "attn_decode_swa_ring_append", "cache_append",
+    "quest_page_minmax",
     "quest_select_pages", "attn_decode_quest", "quest_page_bounds",
     "attn_decode_quest_from_bounds",
     "dsa_topk", "attn_decode_mla_sparse", "kvd_workspace_size", "kvd_check_device_error",
@@ -207,6 +209,32 @@ def attn_decode_swa_ring(q, k_ring, v_ring, block_table, seq_lens, window, n_sin
                                   scale, _DT[q.dtype], int(window), int(n_sink_tokens),
                                   _p(sink_logit), _p(ws), ws.numel(), _stream(stream))
     _check(st, "attn_decode_swa_ring")
+    return out
+
+
+def attn_decode_swa_ring_append(q, k_new, v_new, k_ring, v_ring, block_table, seq_lens, window,
+                                n_sink_tokens=0, sink_logit=None, scale=None, out=None,
+                                lse_out=None, workspace=None, stream=None):
+    """One decode step on a rolling cache: cache_append of each sequence's newest token
+    (k_new, v_new [B, Hkv, D]) into k_ring / v_ring (updated in place), then
+    attn_decode_swa_ring over the updated ring, in one call (one launch for bf16 rings). A
+    bad length or page id of the newest slot is recorded in the workspace's error flag."""
+    B, Hq, Hkv, D, P, max_pages, num_pages = _gqa_args(q, k_ring, v_ring, block_table, seq_lens)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n, q.dtype, 3)
+        if tuple(t.shape) != (B, Hkv, D):
+            raise ValueError(f"{n} must be [B, Hkv, D]")
+    if sink_logit is not None:
+        _need(sink_logit, "sink_logit", torch.float32, 1)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    nbytes = kvd_workspace_size("gqa", B, Hq, Hkv, D, max_pages * P)
+    ws = _ws(workspace, nbytes, q.device, "gqa", layout=("gqa", B, Hq, Hkv, D, max_pages * P))
+    st = lib.attn_decode_swa_ring_append(
+        _p(q), _p(k_new), _p(v_new), _p(k_ring), _p(v_ring), _p(block_table), _p(seq_lens),
+        _p(out), _p(lse_out), B, Hq, Hkv, D, P, max_pages, num_pages, scale, _DT[q.dtype],
+        int(window), int(n_sink_tokens), _p(sink_logit), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "attn_decode_swa_ring_append")
     return out
 
 

@@ -22,6 +22,7 @@ EXPORTS = (
     "dsa_indexer_cache_append_fp8",
     "kvd_delta_decode_step",
     "attn_decode_swa_ring",
+    "attn_decode_swa_ring_append",
     "kvd_cache_append",
     "quest_page_minmax",
     "quest_select_pages",
@@ -69,6 +70,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dsa_indexer_cache_append_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P]
     lib.kvd_delta_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P]
     lib.attn_decode_swa_ring.argtypes = gqa + [I, I, P, P, Z, P]
+    lib.attn_decode_swa_ring_append.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I,
+                                                F, I, I, I, P, P, Z, P]
     lib.kvd_cache_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P]
     lib.quest_page_minmax.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P]
     lib.quest_select_pages.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P]
@@ -83,7 +86,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     for name in ("attn_decode_gqa_paged", "attn_decode_gqa_paged_static_ws", "attn_decode_swa_sink", "attn_decode_mla",
                  "dsa_indexer_topk", "dsa_indexer_topk_fp8", "kvd_quantize_e4m3_rows",
                  "dsa_indexer_cache_append_fp8", "kvd_delta_decode_step",
-                 "attn_decode_swa_ring", "kvd_cache_append", "quest_page_minmax",
+                 "attn_decode_swa_ring", "attn_decode_swa_ring_append", "kvd_cache_append",
+                 "quest_page_minmax",
                  "quest_select_pages", "attn_decode_quest", "quest_page_bounds",
                  "attn_decode_quest_from_bounds", "dsa_topk",
                  "attn_decode_mla_sparse",

@@ -321,7 +321,8 @@ int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t
                const int32_t* seq_lens, void* out, float* lse_out, int B, int Hq, int Hkv, int D,
                int page_size, int max_pages, int num_pages, float scale, int dtype, int window,
                int n_sink, const float* sink_logit, void* ws, size_t ws_bytes,
-               cudaStream_t stream, int ring) {
+               cudaStream_t stream, int ring, int ring_sink, const void* k_new,
+               const void* v_new) {
     const int st = gqa_check(q, k_pool, v_pool, block_table, seq_lens, out, B, Hq, Hkv, D,
                              page_size, max_pages, num_pages, scale, dtype, window, n_sink, ring);
     if (st != KVD_OK) return st;
@@ -361,6 +362,9 @@ int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t
     p.window = window;
     p.n_sink = n_sink;
     p.ring = ring;
+    p.ring_sink = ring_sink;
+    p.k_new = k_new;
+    p.v_new = v_new;
     p.chunk = plan.chunk;
     p.max_chunks = plan.max_chunks;
     p.dtype = dtype;
@@ -421,6 +425,56 @@ int attn_decode_swa_ring(const void* q, const void* k_ring, const void* v_ring,
     return gqa_run(q, k_ring, v_ring, block_table, seq_lens, out, lse_out, B, Hq, Hkv, D,
                    page_size, max_pages, num_pages, scale, dtype, 0, 0, sink_logit, ws, ws_bytes,
                    stream, static_cast<int>(cap));
+}
+
+int attn_decode_swa_ring_append(const void* q, const void* k_new, const void* v_new,
+                                void* k_ring, void* v_ring, const int32_t* block_table,
+                                const int32_t* seq_lens, void* out, float* lse_out, int B,
+                                int Hq, int Hkv, int D, int page_size, int max_pages,
+                                int num_pages, float scale, int dtype, int window,
+                                int n_sink_tokens, const float* sink_logit, void* ws,
+                                size_t ws_bytes, cudaStream_t stream) {
+    if (!k_new || !v_new || !k_ring || !v_ring) return KVD_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return KVD_ERR_INVALID_ARG;
+    if (window < 1 || n_sink_tokens < 0) return KVD_ERR_INVALID_ARG;
+    const long long cap = (long long)n_sink_tokens + window;
+    if (cap > (long long)max_pages * page_size) return KVD_ERR_INVALID_ARG;
+    // every argument check (the attention's) before anything is written
+    const int st = gqa_check(q, k_ring, v_ring, block_table, seq_lens, out, B, Hq, Hkv, D,
+                             page_size, max_pages, num_pages, scale, dtype, 0, 0,
+                             static_cast<int>(cap));
+    if (st != KVD_OK) return st;
+    if (!ws || !aligned16(ws)) return KVD_ERR_INVALID_ARG;
+    if (dtype == KVD_F32) {
+        // float32 rings: the append's own launch, then the attention (the bf16 kernel
+        // writes the rows itself)
+        AppendParams ap;
+        std::memset(&ap, 0, sizeof ap);
+        ap.src[0] = k_new;
+        ap.pool[0] = k_ring;
+        ap.src[1] = v_new;
+        ap.pool[1] = v_ring;
+        ap.n_pools = 2;
+        ap.block_table = block_table;
+        ap.seq_lens = seq_lens;
+        ap.err = static_cast<int*>(ws);
+        ap.B = B;
+        ap.H = Hkv;
+        ap.row_bytes = D * 4;
+        ap.page_size = page_size;
+        ap.max_pages = max_pages;
+        ap.num_pages = num_pages;
+        ap.window = window;
+        ap.n_sink = n_sink_tokens;
+        const int ea = append_launch(ap, stream);
+        if (ea != KVD_OK) return ea;
+        return gqa_run(q, k_ring, v_ring, block_table, seq_lens, out, lse_out, B, Hq, Hkv, D,
+                       page_size, max_pages, num_pages, scale, dtype, 0, 0, sink_logit, ws,
+                       ws_bytes, stream, static_cast<int>(cap), n_sink_tokens);
+    }
+    return gqa_run(q, k_ring, v_ring, block_table, seq_lens, out, lse_out, B, Hq, Hkv, D,
+                   page_size, max_pages, num_pages, scale, dtype, 0, 0, sink_logit, ws, ws_bytes,
+                   stream, static_cast<int>(cap), n_sink_tokens, k_new, v_new);
 }
 
 int kvd_cache_append(const void* k_new, const void* v_new, void* k_pool, void* v_pool,

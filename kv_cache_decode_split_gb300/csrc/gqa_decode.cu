@@ -497,6 +497,47 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
             }
             return pg;
         };
+        // Ring with the newest token's rows in the call (append + attention in one launch):
+        // the CTA whose chunk holds the token's ring slot writes its KV heads' K and V rows
+        // there before any copy of its own (every query-head block of the group writes the
+        // same bytes), ordered before the copies' reads by the proxy fence; no other chunk
+        // reads that slot, and the previous kernel has finished with it (dependency wait).
+        if (p.k_new != nullptr && has) {
+            const int Lt = p.seq_lens[b];  // its validity is recorded by visible_len
+            if (Lt >= 1) {
+                const long long t = Lt - 1;
+                const int win = p.ring - p.ring_sink;
+                const int slot = t < p.ring_sink
+                                     ? static_cast<int>(t)
+                                     : p.ring_sink + static_cast<int>((t - p.ring_sink) % win);
+                if (slot >= lo && slot < hi) {
+                    const int pg = row_cached ? bt_row[slot / p.page_size]
+                                              : p.block_table[static_cast<size_t>(b) * p.max_pages +
+                                                              slot / p.page_size];
+                    if (pg < 0 || pg >= p.num_pages) {
+                        if (lane == 0) record_error(p.err, KVD_ERR_DEVICE_OOB);
+                    } else {
+                        constexpr int kPieces = D * 2 / 16;  // 16-byte pieces of a bf16 row
+                        for (int e = lane; e < HPT * 2 * kPieces; e += 32) {
+                            const int hh = e / (2 * kPieces), isv = (e / kPieces) & 1;
+                            const int pc = e % kPieces;
+                            const int kvh = kvg * HPT + hh;
+                            const size_t src = (static_cast<size_t>(b) * p.Hkv + kvh) * D * 2 + pc * 16;
+                            const size_t dst =
+                                ((static_cast<size_t>(pg) * p.Hkv + kvh) * p.page_size +
+                                 slot % p.page_size) * D * 2 + pc * 16;
+                            const uint4 v = *reinterpret_cast<const uint4*>(
+                                static_cast<const uint8_t*>(isv ? p.v_new : p.k_new) + src);
+                            *reinterpret_cast<uint4*>(
+                                const_cast<uint8_t*>(static_cast<const uint8_t*>(
+                                    isv ? p.v_pool : p.k_pool)) + dst) = v;
+                        }
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                    }
+                }
+            }
+            __syncwarp();
+        }
         int cur = piece_page(lane), nxt = piece_page(32 + lane);
         const uint64_t pol = l2_evict_first_policy();  // K and V are read once
         int issued = 0;  // tiles whose copies are in flight or landed

@@ -33,6 +33,11 @@ struct GqaParams {
     int page_size, max_pages, num_pages, max_len;
     int window, n_sink;  // window <= 0: dense
     int ring;            // > 0: a rolling cache of this many slots; visible = min(L, ring)
+    int ring_sink;       // the ring's pinned sink slots (ring - ring_sink = the window)
+    // ring mode, bf16: the newest token's K and V rows [B, Hkv, D], written into their ring
+    // slot by the attention kernel before it reads the ring (null: the rows are in place)
+    const void* k_new;
+    const void* v_new;
     int chunk, max_chunks;
     int dtype;
     float scale_log2;  // scale * log2(e)
@@ -68,7 +73,8 @@ int gqa_run(const void* q, const void* k_pool, const void* v_pool, const int32_t
             const int32_t* seq_lens, void* out, float* lse_out, int B, int Hq, int Hkv, int D,
             int page_size, int max_pages, int num_pages, float scale, int dtype, int window,
             int n_sink, const float* sink_logit, void* ws, size_t ws_bytes, cudaStream_t stream,
-            int ring = 0);
+            int ring = 0, int ring_sink = 0, const void* k_new = nullptr,
+            const void* v_new = nullptr);
 
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix with a {64, box_rows} box and
 // 128-byte swizzle (cols a multiple of 64). Returns KVD_OK or KVD_ERR_CUDA.

@@ -135,9 +135,84 @@ def test_ring_full_size_sampled(kvd):
     assert_attn_close(out[pi[:, 0], pi[:, 1]], ref, what="ring full size")
 
 
-def test_decode_loop_ring_equals_window_over_history(kvd):
-    # every step: the GPU appends the token's K/V into the ring, then attends from the ring;
-    # the outputs follow the plain window oracle over the whole history
+def _two_calls_and_one(kvd, r, k_new, v_new, chunk=0):
+    """The append then the ring attention (two calls), and the same step as one call, each on
+    its own copy of the ring: outputs, lse and the updated rings."""
+    sink = r.sink_logit.to(DEV) if r.sink_logit is not None else None
+    bt, sl, q = r.block_table.to(DEV), r.seq_lens.to(DEV), r.q.to(DEV)
+    kvd.kvd_set_option("gqa_chunk", chunk)
+    try:
+        k2, v2 = r.k_pool.clone().to(DEV), r.v_pool.clone().to(DEV)
+        err = kvd.cache_append(k_new, v_new, k2, v2, bt, sl, window=r.window, n_sink=r.n_sink)
+        ws2 = kvd.Workspace(DEV)
+        lse2 = torch.empty(r.B, r.Hq, device=DEV)
+        out2 = kvd.attn_decode_swa_ring(q, k2, v2, bt, sl, r.window, r.n_sink, sink,
+                                        scale=r.scale, lse_out=lse2, workspace=ws2)
+        k1, v1 = r.k_pool.clone().to(DEV), r.v_pool.clone().to(DEV)
+        ws1 = kvd.Workspace(DEV)
+        lse1 = torch.empty(r.B, r.Hq, device=DEV)
+        out1 = kvd.attn_decode_swa_ring_append(q, k_new, v_new, k1, v1, bt, sl, r.window,
+                                               r.n_sink, sink, scale=r.scale, lse_out=lse1,
+                                               workspace=ws1)
+        torch.cuda.synchronize()
+    finally:
+        kvd.kvd_set_option("gqa_chunk", 0)
+    assert int(err.item()) == 0 and kvd.kvd_check_device_error(ws2) == 0
+    assert kvd.kvd_check_device_error(ws1) == 0
+    return (out1, lse1, k1, v1), (out2, lse2, k2, v2)
+
+
+@pytest.mark.parametrize("dtype,D,P,window,n_sink,chunk", [
+    (torch.bfloat16, 64, 64, 256, 4, 0),     # two KV heads per tile
+    (torch.bfloat16, 64, 16, 300, 4, 64),    # many chunks: one of them holds the newest slot
+    (torch.bfloat16, 128, 16, 100, 0, 0),    # one KV head per tile, no sinks
+    (torch.float32, 64, 16, 64, 2, 0)])      # float32: the append's launch, then attention
+def test_ring_append_one_call_equals_two_calls(kvd, dtype, D, P, window, n_sink, chunk):
+    # "Attention Optimizations", DSA / Computation Path (the new token's row written before
+    # attention); "All the attentions", section 4 (the newest entry replaces the oldest):
+    # one call is the append followed by the ring attention, bit for bit
+    cap = window + n_sink
+    lens = [1, 2, n_sink + 1, cap - 1, cap, cap + 1, 7 * cap + 5]
+    r = W.make_ring(len(lens), 16, 4, D, lens, window, n_sink=n_sink, page_size=P,
+                    extra_pages=2, seed=8900 + D + P + window, learned_sink=True, dtype=dtype)
+    k_new = W.normal((r.B, r.Hkv, D), 8950 + D, 1.0, dtype).to(DEV)
+    v_new = W.normal((r.B, r.Hkv, D), 8951 + D, 1.0, dtype).to(DEV)
+    (o1, l1, k1, v1), (o2, l2, k2, v2) = _two_calls_and_one(kvd, r, k_new, v_new, chunk)
+    assert torch.equal(k1, k2) and torch.equal(v1, v2)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # and the output is the ring oracle's over the updated ring
+    ref, _ = oracle.gqa(r.q, k1.cpu(), v1.cpu(), r.block_table, r.seq_lens, r.scale, window,
+                        n_sink, r.sink_logit, ring=True)
+    tol = dict(max_abs=1e-4, mean_abs=1e-4, rel_l2=1e-4) if dtype == torch.float32 else {}
+    assert_attn_close(o1, ref, what="ring append + attention, one call", **tol)
+
+
+def test_ring_append_one_call_bad_page_is_flagged(kvd):
+    # the newest slot's page id out of range: recorded in the workspace's error flag, and the
+    # pool is left as it was there
+    r = W.make_ring(2, 8, 2, 64, [10, 40], 32, n_sink=2, page_size=16, seed=8990)
+    bt = r.block_table.clone()
+    slot = 2 + (40 - 1 - 2) % 32  # sequence 1's newest token
+    bt[1, slot // 16] = r.num_pages + 7
+    k_new = W.normal((2, 2, 64), 8991, 1.0, torch.bfloat16).to(DEV)
+    v_new = W.normal((2, 2, 64), 8992, 1.0, torch.bfloat16).to(DEV)
+    kp, vp = r.k_pool.clone().to(DEV), r.v_pool.clone().to(DEV)
+    ws = kvd.Workspace(DEV)
+    kvd.attn_decode_swa_ring_append(r.q.to(DEV), k_new, v_new, kp, vp, bt.to(DEV),
+                                    r.seq_lens.to(DEV), 32, 2, None, workspace=ws)
+    assert kvd.kvd_check_device_error(ws) == -6
+    # sequence 0's row is in place; nothing else of the pool changed but that one row
+    pg0 = int(r.block_table[0, 9 // 16])
+    assert torch.equal(kp[pg0, :, 9 % 16].cpu(), k_new[0].cpu())
+    changed = (kp.cpu() != r.k_pool).any(dim=(1, 2, 3)).nonzero().flatten().tolist()
+    assert changed in ([pg0], [])
+
+
+@pytest.mark.parametrize("one_call", [False, True])
+def test_decode_loop_ring_equals_window_over_history(kvd, one_call):
+    # every step: the GPU appends the token's K/V into the ring, then attends from the ring
+    # (two calls, or the one-call step); the outputs follow the plain window oracle over the
+    # whole history
     B, Hq, Hkv, D, P, window, n_sink, T = 2, 8, 2, 64, 16, 48, 4, 180
     full = W.make_gqa(B, Hq, Hkv, D, [T] * B, page_size=P, shuffle=True, seed=8700,
                       window=window, n_sink=n_sink, learned_sink=True)
@@ -153,9 +228,14 @@ def test_decode_loop_ring_equals_window_over_history(kvd):
         k_new = torch.stack([full.k_pool[pg, :, s] for pg, s in rows]).to(DEV)
         v_new = torch.stack([full.v_pool[pg, :, s] for pg, s in rows]).to(DEV)
         lens = torch.full((B,), t, dtype=torch.int32, device=DEV)
-        kvd.cache_append(k_new, v_new, kr, vr, bt_r, lens, window=window, n_sink=n_sink, err=err)
-        out = kvd.attn_decode_swa_ring(q, kr, vr, bt_r, lens, window, n_sink, sink,
-                                       scale=full.scale, workspace=ws)
+        if one_call:
+            out = kvd.attn_decode_swa_ring_append(q, k_new, v_new, kr, vr, bt_r, lens, window,
+                                                  n_sink, sink, scale=full.scale, workspace=ws)
+        else:
+            kvd.cache_append(k_new, v_new, kr, vr, bt_r, lens, window=window, n_sink=n_sink,
+                             err=err)
+            out = kvd.attn_decode_swa_ring(q, kr, vr, bt_r, lens, window, n_sink, sink,
+                                           scale=full.scale, workspace=ws)
         if t in checks:
             torch.cuda.synchronize()
             ref, _ = oracle.gqa(full.q, full.k_pool, full.v_pool, full.block_table,
