@@ -273,84 +273,112 @@ struct ClusterRx {
     float o[ROWS + 8][D];    // the chunk's output, normalised by its own sum
 };
 
+// Both steps are a handful of dependent operations per row; they run once per CTA at the end
+// of the call, so they are spread over lanes and reduced by shuffles rather than looped by
+// one thread per row (a per-row loop over the warps or the chunks costs a shared-memory round
+// trip per step: ~0.5-0.7 us each, measured).
 template <int D, int HP, int ROWS>
 __device__ void merge_push(MergeSmem<D, HP>* ms, ClusterRx<D, ROWS>& rx, int nkv, int G_cta,
                            int CS, int rank) {
+    static_assert(kConsumers == 4, "four lanes per row below");
     const int rows = nkv * G_cta;
     const int stride = (rows + CS - 1) / CS;
     const uint32_t lse0 = smem_u32(&rx.lse[0]), o0 = smem_u32(&rx.o[0][0]);
-    for (int r = threadIdx.x; r < rows; r += blockDim.x) {
-        MergeSmem<D, HP>& m = ms[r / G_cta];
-        const int h = r % G_cta;
-        float M = neg_inf();
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, m.m[w][h]);
-        const int slot = rank * stride + r / CS;
-        if (M == neg_inf()) {  // an empty chunk (its outputs are zeros)
-#pragma unroll
-            for (int w = 0; w < kConsumers; ++w) m.m[w][h] = 0.f;
-            st_cluster_f32(map_peer(lse0 + slot * 4, r % CS), neg_inf());
-            continue;
-        }
-        float f[kConsumers], L = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) {
-            f[w] = fast_exp2(m.m[w][h] - M);
-            L += m.l[w][h] * f[w];
-        }
-        const float inv = 1.f / L;
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) m.m[w][h] = f[w] * inv;
-        st_cluster_f32(map_peer(lse0 + slot * 4, r % CS), M + log2f(L));
+    // lane w of each group of four: warp w's partial of the row; the row's max and sum by
+    // two shuffle steps; the weights f_w / L replace the warps' maxima in place
+    for (int base = 0; base < rows * kConsumers; base += blockDim.x) {
+        const int e = base + static_cast<int>(threadIdx.x);
+        const int r = e / kConsumers, w = e % kConsumers;
+        const bool act = r < rows;
+        MergeSmem<D, HP>& m = ms[act ? r / G_cta : 0];
+        const int h = act ? r % G_cta : 0;
+        const float mw = act ? m.m[w][h] : neg_inf();
+        float M = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+        const float f = M == neg_inf() ? 0.f : fast_exp2(mw - M);
+        float L = act ? m.l[w][h] * f : 0.f;
+        L += __shfl_xor_sync(0xffffffffu, L, 1);
+        L += __shfl_xor_sync(0xffffffffu, L, 2);
+        if (!act) continue;
+        // an empty chunk (all four maxima -inf) contributes zeros
+        m.m[w][h] = M == neg_inf() ? 0.f : f * (1.f / L);
+        if (w == 0)
+            st_cluster_f32(map_peer(lse0 + (rank * stride + r / CS) * 4, r % CS),
+                           M == neg_inf() ? neg_inf() : M + log2f(L));
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < rows * (D / 4); idx += blockDim.x) {
-        const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
-        const MergeSmem<D, HP>& m = ms[r / G_cta];
-        const int h = r % G_cta;
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    // the merged rows, two 16-byte pieces per thread per pass with both pieces' loads ahead
+    // of both remote stores
+    const int n_items = rows * (D / 4);
+    for (int base = threadIdx.x; base < n_items; base += 2 * blockDim.x) {
+        float4 o[2];
+        uint32_t dst[2];
 #pragma unroll
-        for (int w = 0; w < kConsumers; ++w) {
-            const float f = m.m[w][h];
-            const float4 v = *reinterpret_cast<const float4*>(&m.o[w][h][d]);
-            o.x += f * v.x;
-            o.y += f * v.y;
-            o.z += f * v.z;
-            o.w += f * v.w;
+        for (int k = 0; k < 2; ++k) {
+            const int idx = base + k * static_cast<int>(blockDim.x);
+            o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            dst[k] = 0u;
+            if (idx >= n_items) continue;
+            const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
+            const MergeSmem<D, HP>& m = ms[r / G_cta];
+            const int h = r % G_cta;
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) {
+                const float f = m.m[w][h];
+                const float4 v = *reinterpret_cast<const float4*>(&m.o[w][h][d]);
+                o[k].x += f * v.x;
+                o[k].y += f * v.y;
+                o[k].z += f * v.z;
+                o[k].w += f * v.w;
+            }
+            const int slot = rank * stride + r / CS;
+            dst[k] = map_peer(o0 + static_cast<uint32_t>((slot * D + d) * 4), r % CS);
         }
-        const int slot = rank * stride + r / CS;
-        st_cluster_v4(map_peer(o0 + static_cast<uint32_t>((slot * D + d) * 4), r % CS), o.x, o.y,
-                      o.z, o.w);
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            if (base + k * static_cast<int>(blockDim.x) < n_items)
+                st_cluster_v4(dst[k], o[k].x, o[k].y, o[k].z, o[k].w);
     }
 }
 
 template <int D, int ROWS>
 __device__ void combine_rx(const GqaParams& p, const ClusterRx<D, ROWS>& rx, CombineSmem<ROWS>& cs,
                            int b, int kv0, int nkv, int hg, int G_cta, int CS, int rank) {
+    constexpr int kMaxCS = 8;  // portable cluster size: lane c of a group of eight is chunk c
     const int rows = nkv * G_cta;
     const int stride = (rows + CS - 1) / CS;
     const int mine = rank < rows ? (rows - rank + CS - 1) / CS : 0;  // rows rank + CS i
-    for (int i = threadIdx.x; i < mine; i += blockDim.x) {
+    for (int base = 0; base < mine * kMaxCS; base += blockDim.x) {
+        const int e = base + static_cast<int>(threadIdx.x);
+        const int i = e / kMaxCS, c = e % kMaxCS;
+        const bool act = i < mine;
         const int r = rank + i * CS;
         const int hq = (kv0 + r / G_cta) * p.G + hg * kMaxHP + r % G_cta;
-        float M = p.sink_logit ? p.sink_logit[hq] * kLog2e : neg_inf();
-        const float sig = M;
-        for (int c = 0; c < CS; ++c) M = fmaxf(M, rx.lse[c * stride + i]);
-        float den = p.sink_logit ? fast_exp2(sig - M) : 0.f;
-        for (int c = 0; c < CS; ++c) {
-            const float wv = fast_exp2(rx.lse[c * stride + i] - M);
-            cs.wgt[i][c] = wv;
-            den += wv;
+        const float lc = act && c < CS ? rx.lse[c * stride + i] : neg_inf();
+        // the learned sink enters the max and the sum once (lane 0 of the row)
+        const float sig = act && c == 0 && p.sink_logit ? p.sink_logit[hq] * kLog2e : neg_inf();
+        float M = fmaxf(lc, sig);
+#pragma unroll
+        for (int off = 1; off < kMaxCS; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float wv = lc == neg_inf() ? 0.f : fast_exp2(lc - M);
+        float den = wv + (sig == neg_inf() ? 0.f : fast_exp2(sig - M));
+#pragma unroll
+        for (int off = 1; off < kMaxCS; off <<= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+        if (!act) continue;
+        if (c < CS) cs.wgt[i][c] = wv;
+        if (c == 0) {
+            cs.inv_denom[i] = 1.f / den;
+            cs.lse_nat[i] = (M + log2f(den)) * kLn2;
         }
-        cs.inv_denom[i] = 1.f / den;
-        cs.lse_nat[i] = (M + log2f(den)) * kLn2;
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < mine * (D / 4); idx += blockDim.x) {
         const int i = idx / (D / 4), d = (idx % (D / 4)) * 4;
         const int r = rank + i * CS;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < CS; ++c) {
+#pragma unroll
+        for (int c = 0; c < kMaxCS; ++c) {
+            if (c >= CS) break;
             const float w = cs.wgt[i][c];
             const float4 v = *reinterpret_cast<const float4*>(&rx.o[c * stride + i][d]);
             acc.x += w * v.x;
@@ -396,7 +424,6 @@ template <int D, int NT, int HPT, bool kClu>
 __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
     gqa_decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
-    griddep_wait();
     using Cfg = GqaBf16Cfg<D, NT, HPT, kClu>;
     using MS = MergeSmem<D, NT * 8>;
     using CS = CombineSmem<HPT * NT * 8>;
@@ -424,6 +451,40 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
     const int hg = blockIdx.y / n_kvg;
     const int b = blockIdx.z;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int bp = min(p.page_size, kTile);  // tokens per page piece (power of two)
+    const int lbp = 31 - __clz(bp);
+
+    // Before the dependency wait, while the previous grid drains: the producer warp reads the
+    // length and the block-table entries of the chunk's first S tiles with L2-only loads and
+    // has TMA prefetch those tiles into L2. The values may still be changing (the previous
+    // grid's writes are not yet visible): they only choose what to prefetch, and a prefetch
+    // cannot leave stale data (L2 is the point of coherence). Everything used is read again
+    // after the wait.
+    if (warp == kConsumers) {
+        if (lane == 0) {
+            prefetch_tensormap(&tmK);
+            prefetch_tensormap(&tmV);
+        }
+        int Lp = __ldcg(p.seq_lens + b);
+        Lp = min(Lp, p.ring > 0 ? p.ring : p.max_len);
+        int plo = 0, phi = 0;
+        if (Lp >= 1 &&
+            chunk_bounds(visible_ranges(Lp, p.window, p.n_sink), p.chunk, c, plo, phi)) {
+            const int pt0 = plo & ~(kTile - 1);
+            const int n_pre = min(S, (phi - pt0 + kTile - 1) / kTile) * (kTile / bp);
+            for (int pc = lane; pc < n_pre; pc += 32) {
+                const int t = pt0 + pc * bp;
+                if (t >= Lp) continue;
+                const int pg =
+                    __ldcg(p.block_table + static_cast<size_t>(b) * p.max_pages + t / p.page_size);
+                if (pg < 0 || pg >= p.num_pages) continue;
+                const int y = (pg * p.Hkv + kvg * HPT) * p.page_size + (t & (p.page_size - 1));
+                tma_prefetch_3d(&tmK, 0, y, 0);
+                tma_prefetch_3d(&tmV, 0, y, 0);
+            }
+        }
+    }
+    griddep_wait();
     // The producer loads the sequence's whole block-table row (up to kRowCache entries) while
     // the sequence length is on its way, instead of the entries the length points to after
     // it: one memory round trip less before the first copy. Entries are checked when used.
@@ -447,8 +508,6 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
     const int t0 = lo & ~(kTile - 1);
     const int n_tiles = (hi - t0 + kTile - 1) / kTile;
     const int G_cta = min(kMaxHP, p.G - hg * kMaxHP);
-    const int bp = min(p.page_size, kTile);  // tokens per page piece (power of two)
-    const int lbp = 31 - __clz(bp);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -471,10 +530,6 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
         // The warp resolves the page ids of the CTA's page pieces 32 at a time (lane k: piece
         // 32 m + k), the next batch in flight while the current one is used, so that filling
         // the ring costs one lookup round trip rather than one per tile; lane 0 issues.
-        if (lane == 0) {
-            prefetch_tensormap(&tmK);
-            prefetch_tensormap(&tmV);
-        }
         const int per_tile = kTile / bp;
         const int n_pieces = n_tiles * per_tile;
         if (row_cached) {
@@ -569,6 +624,9 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
             }
             issued = i + 1;
         }
+        // Every copy of this CTA is issued: the next grid on the stream may be scheduled
+        // (its prefetches then overlap this grid's last tiles, merge and combine).
+        griddep_launch_dependents();
         // The merge below overwrites the ring, and consumers that gave up on a wait leave
         // tiles unread: every issued copy must have landed first. (After a normal loop these
         // are the last tiles, which the consumers wait for as well.) The tile issued last in
@@ -727,6 +785,7 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
+        griddep_launch_dependents();  // (as the producer: every thread of the CTA has it)
         // row sums: reduce over the 8 lanes that share a head column
 #pragma unroll
         for (int hh = 0; hh < HPT; ++hh)

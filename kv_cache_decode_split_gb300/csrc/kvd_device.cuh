@@ -159,6 +159,23 @@ __device__ __forceinline__ void griddep_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Lets the grid launched next on the stream (programmatic dependent launch) be scheduled
+// once every CTA of this grid has executed this or exited. That grid still waits for this
+// one's completion and memory flush (griddep_wait) before it reads anything written here.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Hint: bring the box at (x, y, z) of a 3-D tensor map into L2 (no data returned, no
+// barrier). L2 is the GPU's point of coherence, so a prefetch issued before the data's last
+// write leaves nothing stale behind.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // Hint: bring the global line holding `ptr` into L2 (no data returned).
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
