@@ -458,8 +458,10 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
     // length and the block-table entries of the chunk's first S tiles with L2-only loads and
     // has TMA prefetch those tiles into L2. The values may still be changing (the previous
     // grid's writes are not yet visible): they only choose what to prefetch, and a prefetch
-    // cannot leave stale data (L2 is the point of coherence). Everything used is read again
-    // after the wait.
+    // cannot leave stale data (L2 is the point of coherence). The lane of piece k keeps the
+    // page it read (spg) and the length (sLp): when both are read again unchanged after the
+    // wait, the first copies are issued from them at once (nothing is copied before the wait).
+    int sLp = -1, spg = -1, s_idx = 0, s_n = 0;
     if (warp == kConsumers) {
         if (lane == 0) {
             prefetch_tensormap(&tmK);
@@ -471,18 +473,29 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
         if (Lp >= 1 &&
             chunk_bounds(visible_ranges(Lp, p.window, p.n_sink), p.chunk, c, plo, phi)) {
             const int pt0 = plo & ~(kTile - 1);
-            const int n_pre = min(S, (phi - pt0 + kTile - 1) / kTile) * (kTile / bp);
-            for (int pc = lane; pc < n_pre; pc += 32) {
-                const int t = pt0 + pc * bp;
-                if (t >= Lp) continue;
-                const int pg =
-                    __ldcg(p.block_table + static_cast<size_t>(b) * p.max_pages + t / p.page_size);
-                if (pg < 0 || pg >= p.num_pages) continue;
-                const int y = (pg * p.Hkv + kvg * HPT) * p.page_size + (t & (p.page_size - 1));
-                tma_prefetch_3d(&tmK, 0, y, 0);
-                tma_prefetch_3d(&tmV, 0, y, 0);
+            sLp = Lp;
+            s_n = min(S, (phi - pt0 + kTile - 1) / kTile) * (kTile / bp);  // <= 32 pieces
+            if (lane < s_n) {
+                const int t = pt0 + lane * bp;
+                s_idx = min(t, Lp - 1) / p.page_size;  // as the copy loop picks it
+                spg = __ldcg(p.block_table + static_cast<size_t>(b) * p.max_pages + s_idx);
+                if (spg < 0 || spg >= p.num_pages) spg = -1;
+                if (spg >= 0 && t < Lp) {
+                    const int y =
+                        (spg * p.Hkv + kvg * HPT) * p.page_size + (t & (p.page_size - 1));
+                    tma_prefetch_3d(&tmK, 0, y, 0);
+                    tma_prefetch_3d(&tmV, 0, y, 0);
+                }
             }
         }
+    }
+    if (threadIdx.x == 0) {  // shared memory only: published by the barrier after the wait
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumers);
+        }
+        mbar_init(stall, 1);
+        fence_mbar_init();
     }
     griddep_wait();
     // The producer loads the sequence's whole block-table row (up to kRowCache entries) while
@@ -491,11 +504,15 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
     constexpr int kRowRegs = kRowCache / 32;
     const bool row_cached = p.max_pages <= kRowCache;
     int row[kRowRegs];
-    if (warp == kConsumers && row_cached) {
+    int vpg = -1;  // the entry behind spg, read again
+    if (warp == kConsumers) {
         const int32_t* btr = p.block_table + static_cast<size_t>(b) * p.max_pages;
+        if (lane < s_n) vpg = btr[s_idx];
+        if (row_cached) {
 #pragma unroll
-        for (int j = 0; j < kRowRegs; ++j)
-            row[j] = lane + 32 * j < p.max_pages ? btr[lane + 32 * j] : 0;
+            for (int j = 0; j < kRowRegs; ++j)
+                row[j] = lane + 32 * j < p.max_pages ? btr[lane + 32 * j] : 0;
+        }
     }
     const int L = visible_len(p, b);
     const Ranges R = visible_ranges(L, p.window, p.n_sink);
@@ -508,15 +525,6 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
     const int t0 = lo & ~(kTile - 1);
     const int n_tiles = (hi - t0 + kTile - 1) / kTile;
     const int G_cta = min(kMaxHP, p.G - hg * kMaxHP);
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumers);
-        }
-        mbar_init(stall, 1);
-        fence_mbar_init();
-    }
     __syncthreads();
     // cluster combine: no CTA stores into another's shared memory before every CTA of the
     // cluster has started (this arrival; the matching wait comes before the first store)
@@ -532,6 +540,42 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
         // the ring costs one lookup round trip rather than one per tile; lane 0 issues.
         const int per_tile = kTile / bp;
         const int n_pieces = n_tiles * per_tile;
+        const uint64_t pol = l2_evict_first_policy();  // K and V are read once
+        // The newest token's ring slot, when this call appends it (below).
+        int slot = -1;
+        if (p.k_new != nullptr && has) {
+            const int Lt = p.seq_lens[b];  // its validity is recorded by visible_len
+            if (Lt >= 1) {
+                const long long t = Lt - 1;
+                const int win = p.ring - p.ring_sink;
+                slot = t < p.ring_sink ? static_cast<int>(t)
+                                       : p.ring_sink + static_cast<int>((t - p.ring_sink) % win);
+                if (slot < lo || slot >= hi) slot = -1;
+            }
+        }
+        // First copies from the values read before the wait, when the length and every entry
+        // they used are unchanged now (a chunk that appends the newest token's rows first
+        // writes them, so it takes the ordinary path).
+        int n_fast = 0;
+        if (slot < 0 && has && sLp == L && s_n == min(S, n_tiles) * per_tile &&
+            __all_sync(0xffffffffu, lane >= s_n || (spg >= 0 && vpg == spg))) {
+            n_fast = min(S, n_tiles);
+            for (int i = 0; i < n_fast; ++i) {
+                if (lane == 0) mbar_arrive_expect_tx(&full[i], 2 * Cfg::kTileBytes);
+                for (int sub = 0; sub < per_tile; ++sub) {
+                    const int pc = i * per_tile + sub;
+                    const int pg = __shfl_sync(0xffffffffu, spg, pc);
+                    if (lane == 0) {
+                        const int t = t0 + pc * bp;
+                        const int y =
+                            (pg * p.Hkv + kvg * HPT) * p.page_size + (t & (p.page_size - 1));
+                        const uint32_t off = static_cast<uint32_t>(sub * NB * HPT) << (lbp + 7);
+                        tma_load_3d(sK + i * Cfg::kTileBytes + off, &tmK, &full[i], 0, y, 0, pol);
+                        tma_load_3d(sV + i * Cfg::kTileBytes + off, &tmV, &full[i], 0, y, 0, pol);
+                    }
+                }
+            }
+        }
         if (row_cached) {
 #pragma unroll
             for (int j = 0; j < kRowRegs; ++j)
@@ -557,46 +601,35 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
         // there before any copy of its own (every query-head block of the group writes the
         // same bytes), ordered before the copies' reads by the proxy fence; no other chunk
         // reads that slot, and the previous kernel has finished with it (dependency wait).
-        if (p.k_new != nullptr && has) {
-            const int Lt = p.seq_lens[b];  // its validity is recorded by visible_len
-            if (Lt >= 1) {
-                const long long t = Lt - 1;
-                const int win = p.ring - p.ring_sink;
-                const int slot = t < p.ring_sink
-                                     ? static_cast<int>(t)
-                                     : p.ring_sink + static_cast<int>((t - p.ring_sink) % win);
-                if (slot >= lo && slot < hi) {
-                    const int pg = row_cached ? bt_row[slot / p.page_size]
-                                              : p.block_table[static_cast<size_t>(b) * p.max_pages +
-                                                              slot / p.page_size];
-                    if (pg < 0 || pg >= p.num_pages) {
-                        if (lane == 0) record_error(p.err, KVD_ERR_DEVICE_OOB);
-                    } else {
-                        constexpr int kPieces = D * 2 / 16;  // 16-byte pieces of a bf16 row
-                        for (int e = lane; e < HPT * 2 * kPieces; e += 32) {
-                            const int hh = e / (2 * kPieces), isv = (e / kPieces) & 1;
-                            const int pc = e % kPieces;
-                            const int kvh = kvg * HPT + hh;
-                            const size_t src = (static_cast<size_t>(b) * p.Hkv + kvh) * D * 2 + pc * 16;
-                            const size_t dst =
-                                ((static_cast<size_t>(pg) * p.Hkv + kvh) * p.page_size +
-                                 slot % p.page_size) * D * 2 + pc * 16;
-                            const uint4 v = *reinterpret_cast<const uint4*>(
-                                static_cast<const uint8_t*>(isv ? p.v_new : p.k_new) + src);
-                            *reinterpret_cast<uint4*>(
-                                const_cast<uint8_t*>(static_cast<const uint8_t*>(
-                                    isv ? p.v_pool : p.k_pool)) + dst) = v;
-                        }
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
-                    }
+        if (slot >= 0) {
+            const int pg = row_cached ? bt_row[slot / p.page_size]
+                                      : p.block_table[static_cast<size_t>(b) * p.max_pages +
+                                                      slot / p.page_size];
+            if (pg < 0 || pg >= p.num_pages) {
+                if (lane == 0) record_error(p.err, KVD_ERR_DEVICE_OOB);
+            } else {
+                constexpr int kPieces = D * 2 / 16;  // 16-byte pieces of a bf16 row
+                for (int e = lane; e < HPT * 2 * kPieces; e += 32) {
+                    const int hh = e / (2 * kPieces), isv = (e / kPieces) & 1;
+                    const int pc = e % kPieces;
+                    const int kvh = kvg * HPT + hh;
+                    const size_t src = (static_cast<size_t>(b) * p.Hkv + kvh) * D * 2 + pc * 16;
+                    const size_t dst =
+                        ((static_cast<size_t>(pg) * p.Hkv + kvh) * p.page_size +
+                         slot % p.page_size) * D * 2 + pc * 16;
+                    const uint4 v = *reinterpret_cast<const uint4*>(
+                        static_cast<const uint8_t*>(isv ? p.v_new : p.k_new) + src);
+                    *reinterpret_cast<uint4*>(
+                        const_cast<uint8_t*>(static_cast<const uint8_t*>(
+                            isv ? p.v_pool : p.k_pool)) + dst) = v;
                 }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
             }
             __syncwarp();
         }
         int cur = piece_page(lane), nxt = piece_page(32 + lane);
-        const uint64_t pol = l2_evict_first_policy();  // K and V are read once
-        int issued = 0;  // tiles whose copies are in flight or landed
-        for (int i = 0; i < n_tiles; ++i) {
+        int issued = n_fast;  // tiles whose copies are in flight or landed
+        for (int i = n_fast; i < n_tiles; ++i) {  // (pieces of fast tiles are < 32)
             const int s = i % S;
             bool ok = true;
             if (lane == 0) {
