@@ -273,127 +273,98 @@ struct ClusterRx {
     float o[ROWS + 8][D];    // the chunk's output, normalised by its own sum
 };
 
-// Both steps are a handful of dependent operations per row; they run once per CTA at the end
-// of the call, so they are spread over lanes and reduced by shuffles rather than looped by
-// one thread per row (a per-row loop over the warps or the chunks costs a shared-memory round
-// trip per step: ~0.5-0.7 us each, measured).
+// Both steps run once per CTA at the end of the call, while the SM's other CTA may still be
+// streaming: every dependent step there costs ~0.4-0.6 us (measured), so each thread takes
+// whole output pieces and derives the row's weights itself (a few redundant exponentials)
+// instead of weights first, a barrier, then the outputs.
 template <int D, int HP, int ROWS>
-__device__ void merge_push(MergeSmem<D, HP>* ms, ClusterRx<D, ROWS>& rx, int nkv, int G_cta,
-                           int CS, int rank) {
-    static_assert(kConsumers == 4, "four lanes per row below");
+__device__ void merge_push(const MergeSmem<D, HP>* ms, ClusterRx<D, ROWS>& rx, int nkv,
+                           int G_cta, int CS, int rank) {
     const int rows = nkv * G_cta;
     const int stride = (rows + CS - 1) / CS;
     const uint32_t lse0 = smem_u32(&rx.lse[0]), o0 = smem_u32(&rx.o[0][0]);
-    // lane w of each group of four: warp w's partial of the row; the row's max and sum by
-    // two shuffle steps; the weights f_w / L replace the warps' maxima in place
-    for (int base = 0; base < rows * kConsumers; base += blockDim.x) {
-        const int e = base + static_cast<int>(threadIdx.x);
-        const int r = e / kConsumers, w = e % kConsumers;
-        const bool act = r < rows;
-        MergeSmem<D, HP>& m = ms[act ? r / G_cta : 0];
-        const int h = act ? r % G_cta : 0;
-        const float mw = act ? m.m[w][h] : neg_inf();
-        float M = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
-        const float f = M == neg_inf() ? 0.f : fast_exp2(mw - M);
-        float L = act ? m.l[w][h] * f : 0.f;
-        L += __shfl_xor_sync(0xffffffffu, L, 1);
-        L += __shfl_xor_sync(0xffffffffu, L, 2);
-        if (!act) continue;
-        // an empty chunk (all four maxima -inf) contributes zeros
-        m.m[w][h] = M == neg_inf() ? 0.f : f * (1.f / L);
-        if (w == 0)
-            st_cluster_f32(map_peer(lse0 + (rank * stride + r / CS) * 4, r % CS),
-                           M == neg_inf() ? neg_inf() : M + log2f(L));
-    }
-    __syncthreads();
-    // the merged rows, two 16-byte pieces per thread per pass with both pieces' loads ahead
-    // of both remote stores
     const int n_items = rows * (D / 4);
-    for (int base = threadIdx.x; base < n_items; base += 2 * blockDim.x) {
-        float4 o[2];
-        uint32_t dst[2];
+    for (int idx = threadIdx.x; idx < n_items; idx += blockDim.x) {
+        const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
+        const MergeSmem<D, HP>& m = ms[r / G_cta];
+        const int h = r % G_cta;
+        float mw[kConsumers], lw[kConsumers];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int idx = base + k * static_cast<int>(blockDim.x);
-            o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            dst[k] = 0u;
-            if (idx >= n_items) continue;
-            const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
-            const MergeSmem<D, HP>& m = ms[r / G_cta];
-            const int h = r % G_cta;
+        for (int w = 0; w < kConsumers; ++w) mw[w] = m.m[w][h], lw[w] = m.l[w][h];
+        float M = neg_inf();
 #pragma unroll
-            for (int w = 0; w < kConsumers; ++w) {
-                const float f = m.m[w][h];
-                const float4 v = *reinterpret_cast<const float4*>(&m.o[w][h][d]);
-                o[k].x += f * v.x;
-                o[k].y += f * v.y;
-                o[k].z += f * v.z;
-                o[k].w += f * v.w;
-            }
-            const int slot = rank * stride + r / CS;
-            dst[k] = map_peer(o0 + static_cast<uint32_t>((slot * D + d) * 4), r % CS);
+        for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, mw[w]);
+        const int slot = rank * stride + r / CS;
+        const uint32_t peer = static_cast<uint32_t>(r % CS);
+        if (M == neg_inf()) {  // an empty chunk (its outputs are zeros)
+            if (d == 0) st_cluster_f32(map_peer(lse0 + slot * 4, peer), neg_inf());
+            st_cluster_v4(map_peer(o0 + static_cast<uint32_t>((slot * D + d) * 4), peer), 0.f,
+                          0.f, 0.f, 0.f);
+            continue;
         }
+        float f[kConsumers], L = 0.f;
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
-            if (base + k * static_cast<int>(blockDim.x) < n_items)
-                st_cluster_v4(dst[k], o[k].x, o[k].y, o[k].z, o[k].w);
+        for (int w = 0; w < kConsumers; ++w) {
+            f[w] = fast_exp2(mw[w] - M);
+            L += lw[w] * f[w];
+        }
+        const float inv = 1.f / L;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) {
+            const float g = f[w] * inv;
+            const float4 v = *reinterpret_cast<const float4*>(&m.o[w][h][d]);
+            o.x += g * v.x;
+            o.y += g * v.y;
+            o.z += g * v.z;
+            o.w += g * v.w;
+        }
+        if (d == 0) st_cluster_f32(map_peer(lse0 + slot * 4, peer), M + log2f(L));
+        st_cluster_v4(map_peer(o0 + static_cast<uint32_t>((slot * D + d) * 4), peer), o.x, o.y,
+                      o.z, o.w);
     }
 }
 
 template <int D, int ROWS>
-__device__ void combine_rx(const GqaParams& p, const ClusterRx<D, ROWS>& rx, CombineSmem<ROWS>& cs,
-                           int b, int kv0, int nkv, int hg, int G_cta, int CS, int rank) {
-    constexpr int kMaxCS = 8;  // portable cluster size: lane c of a group of eight is chunk c
+__device__ void combine_rx(const GqaParams& p, const ClusterRx<D, ROWS>& rx, int b, int kv0,
+                           int nkv, int hg, int G_cta, int CS, int rank) {
+    constexpr int kMaxCS = 8;  // portable cluster size
     const int rows = nkv * G_cta;
     const int stride = (rows + CS - 1) / CS;
     const int mine = rank < rows ? (rows - rank + CS - 1) / CS : 0;  // rows rank + CS i
-    for (int base = 0; base < mine * kMaxCS; base += blockDim.x) {
-        const int e = base + static_cast<int>(threadIdx.x);
-        const int i = e / kMaxCS, c = e % kMaxCS;
-        const bool act = i < mine;
-        const int r = rank + i * CS;
-        const int hq = (kv0 + r / G_cta) * p.G + hg * kMaxHP + r % G_cta;
-        const float lc = act && c < CS ? rx.lse[c * stride + i] : neg_inf();
-        // the learned sink enters the max and the sum once (lane 0 of the row)
-        const float sig = act && c == 0 && p.sink_logit ? p.sink_logit[hq] * kLog2e : neg_inf();
-        float M = fmaxf(lc, sig);
-#pragma unroll
-        for (int off = 1; off < kMaxCS; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        const float wv = lc == neg_inf() ? 0.f : fast_exp2(lc - M);
-        float den = wv + (sig == neg_inf() ? 0.f : fast_exp2(sig - M));
-#pragma unroll
-        for (int off = 1; off < kMaxCS; off <<= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-        if (!act) continue;
-        if (c < CS) cs.wgt[i][c] = wv;
-        if (c == 0) {
-            cs.inv_denom[i] = 1.f / den;
-            cs.lse_nat[i] = (M + log2f(den)) * kLn2;
-        }
-    }
-    __syncthreads();
     for (int idx = threadIdx.x; idx < mine * (D / 4); idx += blockDim.x) {
         const int i = idx / (D / 4), d = (idx % (D / 4)) * 4;
         const int r = rank + i * CS;
+        const int hq = (kv0 + r / G_cta) * p.G + hg * kMaxHP + r % G_cta;
+        float lc[kMaxCS];
+        float M = p.sink_logit ? p.sink_logit[hq] * kLog2e : neg_inf();
+        const float sig = M;
+#pragma unroll
+        for (int c = 0; c < kMaxCS; ++c) {
+            lc[c] = c < CS ? rx.lse[c * stride + i] : neg_inf();
+            M = fmaxf(M, lc[c]);
+        }
+        float den = p.sink_logit ? fast_exp2(sig - M) : 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < kMaxCS; ++c) {
             if (c >= CS) break;
-            const float w = cs.wgt[i][c];
+            const float w = fast_exp2(lc[c] - M);
+            den += w;
             const float4 v = *reinterpret_cast<const float4*>(&rx.o[c * stride + i][d]);
             acc.x += w * v.x;
             acc.y += w * v.y;
             acc.z += w * v.z;
             acc.w += w * v.w;
         }
-        const float inv = cs.inv_denom[i];
-        const int hq = (kv0 + r / G_cta) * p.G + hg * kMaxHP + r % G_cta;
+        const float inv = 1.f / den;
         const size_t o = (static_cast<size_t>(b) * p.Hq + hq) * D + d;
         __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
         __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
         *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o) =
             make_uint2(*reinterpret_cast<uint32_t*>(&lo2), *reinterpret_cast<uint32_t*>(&hi2));
-        if (d == 0 && p.lse_out) p.lse_out[static_cast<size_t>(b) * p.Hq + hq] = cs.lse_nat[i];
+        if (d == 0 && p.lse_out)
+            p.lse_out[static_cast<size_t>(b) * p.Hq + hq] = (M + log2f(den)) * kLn2;
     }
 }
 
@@ -859,7 +830,7 @@ __global__ void __launch_bounds__(GqaBf16Cfg<D, NT, HPT, kClu>::kThreads, 2)
         cluster_wait();  // every CTA of the cluster has started
         merge_push<D, NT * 8, HPT * NT * 8>(ms, rx, HPT, G_cta, gridDim.x, rank);
         cluster_sync();  // every chunk's partial is in its combining CTA
-        combine_rx<D, HPT * NT * 8>(p, rx, cs, b, kvg * HPT, HPT, hg, G_cta, gridDim.x, rank);
+        combine_rx<D, HPT * NT * 8>(p, rx, b, kvg * HPT, HPT, hg, G_cta, gridDim.x, rank);
     } else {
         merge_chunks<D, NT * 8>(p, ms, b, kvg * HPT, HPT, hg, c, G_cta);
         const int grp = (b * n_kvg + kvg) * p.NHG + hg;
