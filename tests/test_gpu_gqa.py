@@ -235,3 +235,45 @@ def test_combine_paths(kvd, mode, case):
         _compare(kvd, x)   # the same workspace again
     finally:
         kvd.kvd_set_option("gqa_cluster", 1)
+
+
+@pytest.mark.parametrize("D,window,n_sink", [(64, 1024, 4), (128, 0, 0)])
+def test_lengths_and_table_rewritten_by_the_previous_kernel(kvd, D, window, n_sink):
+    """The bf16 kernel reads the lengths and block-table entries before its dependency wait
+    (L2 prefetch hints, and its first copies once the same values are read again after the
+    wait). Here the kernel just before it on the stream rewrites both, alternating two sets
+    of values over one pool: every call must follow the values that kernel wrote."""
+    dev = "cuda"
+    B, Hq, Hkv = 4, 16, 4
+    lens_new = [3000, 2500, 1900, 3100]
+    x = W.make_gqa(B, Hq, Hkv, D, lens_new, page_size=64, shuffle=True, extra_pages=3,
+                   seed=900 + D, window=window, n_sink=n_sink)
+    # the other set: each sequence takes the next one's block-table row, shorter lengths
+    bt_old = torch.roll(x.block_table, 1, dims=0)
+    lens_old = torch.tensor([1500, 2900, 700, 1800], dtype=torch.int32)  # within the rows
+    refs = {}
+    for name, bt, sl in (("new", x.block_table, x.seq_lens), ("old", bt_old, lens_old)):
+        refs[name] = oracle.gqa(x.q, x.k_pool, x.v_pool, bt, sl, x.scale, x.window, x.n_sink,
+                                None)
+    q, kp, vp = x.q.to(dev), x.k_pool.to(dev), x.v_pool.to(dev)
+    src = {"new": (x.block_table.to(dev), x.seq_lens.to(dev)),
+           "old": (bt_old.to(dev), lens_old.to(dev))}
+    bt_d = torch.empty_like(src["new"][0])
+    sl_d = torch.empty_like(src["new"][1])
+    ws = kvd.Workspace(dev)
+    outs = []
+    for it in range(12):
+        name = "new" if it % 2 == 0 else "old"
+        # elementwise kernels (not copies) write the inputs just before the attention launch
+        torch.add(src[name][0], 0, out=bt_d)
+        torch.add(src[name][1], 0, out=sl_d)
+        if window > 0:
+            out = kvd.attn_decode_swa_sink(q, kp, vp, bt_d, sl_d, window, n_sink, None,
+                                           scale=x.scale, workspace=ws)
+        else:
+            out = kvd.attn_decode_gqa_paged(q, kp, vp, bt_d, sl_d, scale=x.scale, workspace=ws)
+        outs.append((name, out))
+    torch.cuda.synchronize()
+    assert kvd.kvd_check_device_error(ws) == 0
+    for name, out in outs:
+        assert_attn_close(out, refs[name][0], what=f"{name} values")
