@@ -22,9 +22,15 @@
 //   S^T[16 tok x 8 heads] = K[16 x D] q^T        (mma.sync m16n8k16, tokens as M)
 //   O^T[D x 8 heads]     += V^T[D x 16 tok] P^T  (P^T via movmatrix, V^T via ldmatrix.trans)
 // The warps are merged in shared memory into one (o, log2-sum-exp) partial per chunk and
-// KV head; the CTA that finishes last (a completion counter per group) combines all chunk
-// partials with log-sum-exp weights, adds the learned sink once and writes the output.
-// One launch per call.
+// KV head. When groups are few, the chunks of a group form a thread-block cluster and push
+// their partials into the combining CTAs' shared memory; otherwise the CTA that finishes
+// last (a completion counter per group) combines them through the workspace. Either way
+// the partials are weighted by log-sum-exp, the learned sink enters once, and one launch
+// serves the call (on a rolling cache it can also write the newest token's rows first).
+// Start and end of a call overlap its neighbours on the stream: before the dependency wait
+// the producer has the first tiles prefetched into L2 (and issues their copies right after
+// it when the values it read are unchanged), and once a CTA's copies are all issued it lets
+// the next grid be scheduled.
 //
 // The float32 variant (tiny shapes, exact fp32 arithmetic) walks the block table with
 // plain loads on CUDA cores and shares the merge and combine code.
