@@ -55,25 +55,25 @@ NCU_TRAFFIC = {
         "bytes": 794.209280e6 + 3.381504e6,
         "sources": ('gqa_decode.cu', 'kvd_device.cuh'),
         "structs": ('GqaParams',),
-        "sha256": "2fdc853ad65b71fe7123b039eac9b3e9daa7872e53a4e8c0e18d9ff04717aac0",
+        "sha256": "c0c24a8b630924cc7e5bd8d48f2a7081a33e87842b6a55136d613008fbfb3764",
     },
     "swa_sink_tokens": {  # gqa_decode_bf16_kernel<64, 1, 2, 1>
         "bytes": 68.300032e6 + 0.942592e6,
         "sources": ('gqa_decode.cu', 'kvd_device.cuh'),
         "structs": ('GqaParams',),
-        "sha256": "2fdc853ad65b71fe7123b039eac9b3e9daa7872e53a4e8c0e18d9ff04717aac0",
+        "sha256": "c0c24a8b630924cc7e5bd8d48f2a7081a33e87842b6a55136d613008fbfb3764",
     },
     "swa_learned_sink": {  # gqa_decode_bf16_kernel<64, 1, 2, 1>
         "bytes": 67.251456e6 + 0.820736e6,
         "sources": ('gqa_decode.cu', 'kvd_device.cuh'),
         "structs": ('GqaParams',),
-        "sha256": "2fdc853ad65b71fe7123b039eac9b3e9daa7872e53a4e8c0e18d9ff04717aac0",
+        "sha256": "c0c24a8b630924cc7e5bd8d48f2a7081a33e87842b6a55136d613008fbfb3764",
     },
     "swa_ring_sink_tokens": {  # gqa_decode_bf16_kernel<64, 1, 2, 1>
         "bytes": 68.299520e6 + 0.531200e6,
         "sources": ('gqa_decode.cu', 'kvd_device.cuh'),
         "structs": ('GqaParams',),
-        "sha256": "2fdc853ad65b71fe7123b039eac9b3e9daa7872e53a4e8c0e18d9ff04717aac0",
+        "sha256": "c0c24a8b630924cc7e5bd8d48f2a7081a33e87842b6a55136d613008fbfb3764",
     },
     "mla_dsv3": {  # mla_decode_kernel<0>
         "bytes": 304.526848e6 + 4.448512e6,
