@@ -145,6 +145,16 @@ def test_quest_bf16(kvd, D, P, n_sel):
     _check(kvd, x, n_sel)
 
 
+@pytest.mark.parametrize("n_sel", [16, 64])
+def test_quest_choice_both_paths(kvd, n_sel):
+    # heads with at most 512 full pages choose with their keys in registers, longer ones with
+    # the keys in shared memory: lengths on both sides of 512 pages of 16 tokens
+    lens = [16 * 512, 16 * 512 + 15, 16 * 513, 9000, 300]
+    x = W.make_gqa(len(lens), 8, 2, 64, lens, page_size=16, shuffle=True, extra_pages=3,
+                   seed=9200 + n_sel)
+    _check(kvd, x, n_sel)
+
+
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (16, 2), (32, 2), (12, 4)])
 def test_quest_group_sizes(kvd, hq, hkv):
     # every bound-kernel width (group sizes 1, 2, 8, 16 and a padded 3)
