@@ -94,10 +94,10 @@ NCU_TRAFFIC = {
         "sha256": "de9e49f6b6f46d0374108ed8d03f9b6e9b8b10c5f89b6f69a9da8ef6f42d955b",
     },
     "quest_llama3": {  # quest_attn_kernel<4, 1, 1>
-        "bytes": 115.015168e6 + 3.543552e6,
+        "bytes": 115.033600e6 + 3.841792e6,
         "sources": ('quest.cu', 'kvd_device.cuh'),
         "structs": ('QuestParams',),
-        "sha256": "cc0203882456d54b92a93ee7e961f2f8003b2bfec1a8549f8b6b8c92226a4284",
+        "sha256": "7716a52f75ab4165dd9b75304e0038b3badd1680dc098ec5e7c25e5fd9be914f",
     },
     "kda_decode": {  # delta_step_kernel<4>
         "bytes": 276.864768e6 + 210.739456e6,
