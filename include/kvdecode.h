@@ -458,7 +458,16 @@ int kvd_delta_decode_step(float *S, const float *q, const float *k, const float 
  * after it, from any thread, until it is set again.
  *  KVD_OPT_PDL            1 (default): kernels are launched with programmatic dependent
  *                         launch, so that a kernel's set-up overlaps the tail of the
- *                         previous one on the stream; 0: plain launches.
+ *                         previous one on the stream; 0: plain launches. Before its
+ *                         dependency wait a kernel touches no global memory, except that the
+ *                         bf16 GQA / SWA kernel reads lengths and block-table entries
+ *                         (L2-only) to prefetch its first tiles into L2, and issues its first
+ *                         copies from them only if the same values are read after the wait.
+ *                         That kernel also lets the next kernel on the stream be scheduled
+ *                         once its copies are issued; a kernel launched after it with
+ *                         programmatic dependent launch must wait for it (griddepcontrol.wait
+ *                         / cudaGridDependencySynchronize) before reading its outputs, as
+ *                         that launch mode requires in any case.
  *  KVD_OPT_GQA_CHUNK      0 (default): the GQA / SWA split plan picks the tokens per split;
  *                         >= 64: that many tokens (rounded down to a multiple of 64) per
  *                         split, raised if the plan would exceed its chunk limit.
