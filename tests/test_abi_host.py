@@ -126,6 +126,22 @@ def test_append_ring_and_quest_argument_checks(lib):
     assert ring(n_sink=-1) == -1
     assert ring(window=64, n_sink=4, max_pages=4) == -1   # 68 slots > 4 pages of 16
 
+    def ring_append(k_new=A, v_new=A, window=64, n_sink=4, max_pages=8, D=64, dtype=1,
+                    ws_bytes=1 << 30):
+        return lib.attn_decode_swa_ring_append(
+            vp(A), vp(k_new) if k_new else None, vp(v_new) if v_new else None, vp(A), vp(A),
+            vp(A), vp(A), vp(A), None, 2, 8, 2, D, 16, max_pages, 16, 0.125, dtype, window,
+            n_sink, None, vp(A), ws_bytes, None)
+    assert ring_append(k_new=0) == -1
+    assert ring_append(v_new=0) == -1
+    assert ring_append(window=0) == -1
+    assert ring_append(n_sink=-1) == -1
+    assert ring_append(window=64, n_sink=4, max_pages=4) == -1   # 68 slots > 4 pages of 16
+    assert ring_append(k_new=A + 8) == -1           # not 16-byte aligned
+    assert ring_append(D=96) == -2
+    assert ring_append(dtype=7) == -2
+    assert ring_append(ws_bytes=16) == -5           # checked before anything is written
+
     def select(n_sel=16, Hq=8, Hkv=2, ub=A, D=128):
         return lib.quest_select_pages(vp(A), vp(A), vp(A), vp(A), vp(A), vp(A),
                                       vp(ub) if ub else None, 2, Hq, Hkv, D, 16, 64, 128, n_sel,
